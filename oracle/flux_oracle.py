@@ -1,0 +1,308 @@
+"""Plain, slow, obviously correct CPU oracle (numpy, float64).
+
+TEST INFRASTRUCTURE ONLY -- see the package docstring.  Nothing in the CUDA
+path imports this module; it shares no code, table or constant with it.
+
+What it computes and where that is defined
+------------------------------------------
+* The dense tensor-parallel MLP of the FLUX paper (FLUX paper review,
+  section "三、技术架构 / MLP 前向传播"):
+      Output1 = GEMM(AllGather(X), W1)                       -> :func:`ag_gemm`
+      Output2 = ReduceScatter(GEMM(Output1, W2))             -> :func:`gemm_rs`
+  The shard directions follow the Megatron-style reading: X is split by rows
+  (tokens) and W1 [K x N] by columns; Output1 is split by columns and W2 by
+  rows, so rank r's partial product A_r . B_r covers its K/R slice and owner
+  rank o receives rows [o M/R, (o+1) M/R) of the sum over ranks.
+* The COMET MoE variant (Comet article, section "COMET 的技术原理": the
+  shared tensor is decomposed along the token dimension, tokens are gathered
+  to experts, and the expert outputs are combined back by token):
+      routing (stable counting sort of the top-k slots by expert) -> :func:`moe_route`
+      layer0 = gather-by-expert(AllGather(X)) . W1_{e,r}         -> :func:`moe_layer0`
+      layer1 = ReduceScatter_by_token(sum_k g_k . (H_r . W2_{e,r})) -> :func:`moe_layer1`
+
+Precision: the pages fix none, so every floating-point result here is the
+exact float64 value of the stored 16-bit inputs combined in float64 (a
+library matmul serves as the dot-product step).  Ranks are summed in
+ascending rank order and top-k contributions in ascending k, as the plain
+reading of "sum over ranks" states.  Routing is integer and exact.
+
+Storage formats of the inputs: "f16" arrays are np.float16; "bf16" arrays are
+np.uint16 bfloat16 bit patterns, which :func:`widen` decodes itself.
+
+Every function here is pinned by ``tests/test_oracle.py`` to facts other
+than its own formula (brute force on tiny inputs, identities, closed forms,
+library special cases).
+"""
+from __future__ import annotations
+
+import numpy as np
+
+__all__ = [
+    "widen", "round_to", "gemm", "ag_gemm", "gemm_rs", "moe_route",
+    "moe_layer0", "moe_layer1", "ag_gemm_at", "gemm_rs_at", "moe_layer0_rows",
+    "moe_layer1_rows",
+]
+
+
+# --------------------------------------------------------------------------
+# number formats
+# --------------------------------------------------------------------------
+def widen(a, dtype: str) -> np.ndarray:
+    """Exact float64 value of a stored 16-bit array.
+
+    bf16 is the upper half of an IEEE binary32, so its value is the float32
+    whose high 16 bits are the stored pattern and whose low 16 bits are zero.
+    """
+    if dtype == "f16":
+        return np.asarray(a, dtype=np.float16).astype(np.float64)
+    if dtype == "bf16":
+        bits = np.asarray(a, dtype=np.uint16).astype(np.uint32) << np.uint32(16)
+        return bits.view(np.float32).astype(np.float64)
+    if dtype in ("f32", "f64"):
+        return np.asarray(a, dtype=np.float64)
+    raise ValueError(f"unknown dtype {dtype!r}")
+
+
+def round_to(x: np.ndarray, dtype: str) -> np.ndarray:
+    """Round float64 values to the 16-bit storage format, nearest-even.
+
+    Returns the rounded values as float64.  fp16 uses numpy's correctly
+    rounded double->half conversion.  bf16 keeps 8 significant bits: the
+    significand from frexp (in [0.5, 1)) is scaled by 2^8 and rounded
+    half-to-even by rint.  (Normal range only; the workloads never reach the
+    bf16 subnormal range.)
+    """
+    x = np.asarray(x, dtype=np.float64)
+    if dtype == "f16":
+        return x.astype(np.float16).astype(np.float64)
+    if dtype == "bf16":
+        m, e = np.frexp(x)
+        return np.ldexp(np.rint(m * 256.0) / 256.0, e)
+    raise ValueError(dtype)
+
+
+# --------------------------------------------------------------------------
+# dense GEMM and the two fused collectives
+# --------------------------------------------------------------------------
+def gemm(A: np.ndarray, B: np.ndarray) -> np.ndarray:
+    """C[i, j] = sum_k A[i, k] B[k, j] in float64 (the non-split GEMM)."""
+    A = np.asarray(A, dtype=np.float64)
+    B = np.asarray(B, dtype=np.float64)
+    if A.ndim != 2 or B.ndim != 2 or A.shape[1] != B.shape[0]:
+        raise ValueError(f"bad GEMM shapes {A.shape} x {B.shape}")
+    return A @ B
+
+
+def ag_gemm(x_shards, w_shards, dtype: str):
+    """Output1_r = GEMM(AllGather(X), W1_r) for every rank r.
+
+    AllGather concatenates the row shards X_0 .. X_{R-1} in rank order
+    (FLUX paper review, "MLP 前向传播", first GEMM).  Returns R float64 arrays
+    of shape [M, N/R].
+    """
+    R = len(x_shards)
+    if len(w_shards) != R or R == 0:
+        raise ValueError("need R x shards and R w shards")
+    xfull = np.concatenate([widen(x, dtype) for x in x_shards], axis=0)
+    return [gemm(xfull, widen(w, dtype)) for w in w_shards]
+
+
+def gemm_rs(a_shards, b_shards, dtype: str):
+    """Output2_o = rows [o M/R, (o+1) M/R) of sum_r GEMM(A_r, B_r).
+
+    Rank r's partial is A_r . B_r over its K/R slice; the partials are summed
+    in ascending rank order, then scattered so that owner o keeps its row chunk
+    (FLUX paper review, "MLP 前向传播", second GEMM).  Returns R float64 arrays
+    of shape [M/R, N].
+    """
+    R = len(a_shards)
+    if len(b_shards) != R or R == 0:
+        raise ValueError("need R a shards and R b shards")
+    M = np.asarray(a_shards[0]).shape[0]
+    if M % R:
+        raise ValueError("M must divide by R")
+    total = None
+    for r in range(R):
+        p = gemm(widen(a_shards[r], dtype), widen(b_shards[r], dtype))
+        total = p if total is None else total + p
+    h = M // R
+    return [total[o * h:(o + 1) * h].copy() for o in range(R)]
+
+
+def ag_gemm_at(x_shards, w_shards, dtype: str, r: int, rows, cols) -> np.ndarray:
+    """Output1_r[rows[i], cols[i]] for sampled index pairs (float64)."""
+    rows = np.asarray(rows, dtype=np.int64)
+    cols = np.asarray(cols, dtype=np.int64)
+    m_local = np.asarray(x_shards[0]).shape[0]
+    out = np.empty(rows.shape[0], dtype=np.float64)
+    w = widen(w_shards[r], dtype)
+    for i, (row, col) in enumerate(zip(rows, cols)):
+        s, lr = divmod(int(row), m_local)
+        xrow = widen(np.asarray(x_shards[s])[lr], dtype)
+        out[i] = float(np.dot(xrow, w[:, col]))
+    return out
+
+
+def gemm_rs_at(a_shards, b_shards, dtype: str, o: int, rows, cols) -> np.ndarray:
+    """Output2_o[rows[i], cols[i]] (rows local to owner o) for sampled pairs."""
+    R = len(a_shards)
+    M = np.asarray(a_shards[0]).shape[0]
+    h = M // R
+    rows = np.asarray(rows, dtype=np.int64)
+    cols = np.asarray(cols, dtype=np.int64)
+    out = np.zeros(rows.shape[0], dtype=np.float64)
+    for i, (row, col) in enumerate(zip(rows, cols)):
+        g = o * h + int(row)
+        acc = 0.0
+        for r in range(R):
+            a = widen(np.asarray(a_shards[r])[g], dtype)
+            b = widen(np.asarray(b_shards[r])[:, col], dtype)
+            acc = acc + float(np.dot(a, b))
+        out[i] = acc
+    return out
+
+
+# --------------------------------------------------------------------------
+# MoE
+# --------------------------------------------------------------------------
+def moe_route(topk_ids: np.ndarray, E: int):
+    """Stable counting sort of the top-k slots by expert.
+
+    Slot s = t * topk + k holds expert id[t, k].  Returns int32 arrays
+      counts[e]       number of slots routed to expert e
+      offsets[e]      exclusive prefix sum of counts (offsets[E] = T * topk)
+      slot_to_row[s]  offsets[id[s]] + (number of earlier slots with the same id)
+      row_to_slot[r]  the inverse permutation
+    i.e. rows are grouped by expert in ascending expert order and, within one
+    expert, keep ascending slot order (tokens gathered to experts, Comet
+    article, "共享张量依赖解析").
+    """
+    ids = np.asarray(topk_ids).reshape(-1)
+    n = ids.shape[0]
+    counts = [0] * E
+    for s in range(n):
+        e = int(ids[s])
+        if e < 0 or e >= E:
+            raise ValueError(f"expert id {e} out of range [0, {E})")
+        counts[e] += 1
+    offsets = [0] * (E + 1)
+    for e in range(E):
+        offsets[e + 1] = offsets[e] + counts[e]
+    seen = [0] * E
+    slot_to_row = [0] * n
+    row_to_slot = [0] * n
+    for s in range(n):
+        e = int(ids[s])
+        row = offsets[e] + seen[e]
+        seen[e] += 1
+        slot_to_row[s] = row
+        row_to_slot[row] = s
+    i32 = lambda v: np.asarray(v, dtype=np.int32)  # noqa: E731
+    return i32(counts), i32(offsets), i32(slot_to_row), i32(row_to_slot)
+
+
+def moe_layer0(x_shards, w1_shards, topk_ids, E: int, dtype: str):
+    """layer0: H_r[row] = AllGather(X)[token(row)] . W1_r[expert(row)].
+
+    Rows are in the grouped (expert-sorted) order of :func:`moe_route`; for row
+    ``row`` the slot is s = row_to_slot[row], the token t = s // topk and the
+    expert id[t, s % topk].  Returns (list of R float64 [T*topk, F/R],
+    routing tuple).
+    """
+    ids = np.asarray(topk_ids)
+    T, topk = ids.shape
+    routing_ = moe_route(ids, E)
+    counts, offsets, slot_to_row, row_to_slot = routing_
+    xfull = np.concatenate([widen(x, dtype) for x in x_shards], axis=0)
+    if xfull.shape[0] != T:
+        raise ValueError("token count mismatch")
+    outs = []
+    for w1 in w1_shards:
+        w = widen(w1, dtype)  # [E, H, F/R]
+        h = np.zeros((T * topk, w.shape[2]), dtype=np.float64)
+        for e in range(E):
+            lo, hi = int(offsets[e]), int(offsets[e + 1])
+            if hi == lo:
+                continue
+            tokens = row_to_slot[lo:hi].astype(np.int64) // topk
+            h[lo:hi] = gemm(xfull[tokens], w[e])
+        outs.append(h)
+    return outs, routing_
+
+
+def moe_layer1(h_shards, w2_shards, topk_ids, topk_weights, E: int, dtype: str,
+               routing_=None, h_dtype: str | None = None):
+    """layer1: Y[t] = sum_r sum_k g[t,k] (H_r[row(t,k)] . W2_r[id[t,k]]), scattered by token.
+
+    Rank order ascending, then k ascending.  Owner o receives token rows
+    [o T/R, (o+1) T/R).  ``h_dtype`` is the storage format of the H shards
+    ("f64" when chaining exact layer0 values; defaults to ``dtype``).
+    Returns R float64 arrays [T/R, H].
+    """
+    ids = np.asarray(topk_ids)
+    g = np.asarray(topk_weights, dtype=np.float32).astype(np.float64)
+    T, topk = ids.shape
+    R = len(h_shards)
+    if T % R:
+        raise ValueError("T must divide by R")
+    if routing_ is None:
+        routing_ = moe_route(ids, E)
+    _, offsets, slot_to_row, row_to_slot = routing_
+    hd = dtype if h_dtype is None else h_dtype
+    Y = None
+    s2r = np.asarray(slot_to_row, dtype=np.int64).reshape(T, topk)
+    for r in range(R):
+        hr = widen(h_shards[r], hd)
+        w = widen(w2_shards[r], dtype)  # [E, F/R, H]
+        P = np.zeros((T * topk, w.shape[2]), dtype=np.float64)
+        for e in range(E):
+            lo, hi = int(offsets[e]), int(offsets[e + 1])
+            if hi > lo:
+                P[lo:hi] = gemm(hr[lo:hi], w[e])
+        if Y is None:
+            Y = np.zeros((T, w.shape[2]), dtype=np.float64)
+        for k in range(topk):
+            # contribution of slot (t, k) of rank r, for every token t at once
+            Y = Y + g[:, k:k + 1] * P[s2r[:, k]]
+    h = T // R
+    return [Y[o * h:(o + 1) * h].copy() for o in range(R)]
+
+
+def moe_layer0_rows(x_shards, w1_shards, topk_ids, E: int, dtype: str, r: int, rows):
+    """H_r[rows] (full F/R width) for sampled grouped-order rows (float64)."""
+    ids = np.asarray(topk_ids)
+    T, topk = ids.shape
+    _, _, _, row_to_slot = moe_route(ids, E)
+    t_local = np.asarray(x_shards[0]).shape[0]
+    w = widen(w1_shards[r], dtype)
+    out = []
+    for row in np.asarray(rows, dtype=np.int64):
+        s = int(row_to_slot[row])
+        t, k = divmod(s, topk)
+        e = int(ids[t, k])
+        src, lt = divmod(t, t_local)
+        out.append(widen(np.asarray(x_shards[src])[lt], dtype) @ w[e])
+    return np.asarray(out)
+
+
+def moe_layer1_rows(h_shards, w2_shards, topk_ids, topk_weights, E: int, dtype: str,
+                    o: int, rows):
+    """Output_o[rows] (full H width) for sampled owner-local token rows (float64)."""
+    ids = np.asarray(topk_ids)
+    g = np.asarray(topk_weights, dtype=np.float32).astype(np.float64)
+    T, topk = ids.shape
+    R = len(h_shards)
+    _, _, slot_to_row, _ = moe_route(ids, E)
+    h = T // R
+    out = []
+    for lr in np.asarray(rows, dtype=np.int64):
+        t = o * h + int(lr)
+        acc = None
+        for r in range(R):
+            for k in range(topk):
+                e = int(ids[t, k])
+                hrow = widen(np.asarray(h_shards[r])[slot_to_row[t * topk + k]], dtype)
+                v = g[t, k] * (hrow @ widen(np.asarray(w2_shards[r])[e], dtype))
+                acc = v if acc is None else acc + v
+        out.append(acc)
+    return np.asarray(out)
