@@ -1,0 +1,237 @@
+/*
+ * flux_gb300.h -- C ABI of the GB300 (sm_103a) fused GEMM + tensor-parallel
+ * collective library.
+ *
+ * What it computes.  The dense tensor-parallel MLP of FLUX ("FLUX: Fast
+ * Software-based Communication Overlap On GPUs Through Kernel Fusion", paper
+ * review, section 三 "技术架构", subsection "MLP 前向传播"):
+ *     Output1 = GEMM(AllGather(X), W1)          flux_ag_gemm
+ *     Output2 = ReduceScatter(GEMM(Output1, W2)) flux_gemm_rs
+ * and the MoE variant of COMET (COMET article, section "COMET 的技术原理":
+ * the shared tensor is cut along the token dimension, tokens are gathered to
+ * experts, expert outputs are combined back per token):
+ *     routing (histogram + prefix sum + stable permutation)  flux_moe_route
+ *     AllGather + gather-by-expert + grouped GEMM            flux_moe_ag_grouped_gemm
+ *     grouped GEMM + top-k weighted combine + ReduceScatter  flux_moe_grouped_gemm_rs
+ * plus the plain non-split GEMM that the effective-communication-time metric
+ * ECT = OverallTime - GEMM_non-split is measured against (paper review,
+ * section 三, "核心公式"): flux_gemm.  The operator list is the one the Flux
+ * quick start exercises (Flux tool page, section "快速开始": gemm_only,
+ * ag_gemm, gemm_rs, moe_ag_scatter, moe_gather_rs).
+ *
+ * Tensor-parallel ranks are VIRTUAL: the R ranks of one call are R sets of
+ * buffers in the memory of the one GPU the call runs on.  The "communication"
+ * is tile movement between those buffers inside one fused kernel, gated by
+ * per-shard ready flags; nothing is sent between GPUs.
+ *
+ * Conventions shared by every entry point
+ *   - Every buffer argument is caller-owned.  Pointers documented "device" are
+ *     device (or managed) memory of the current CUDA device; arrays of R
+ *     pointers ("x_shards" etc.) are HOST arrays holding R device pointers.
+ *     The library allocates no device memory and keeps no pointer after the
+ *     call returns (it does keep a per-process cache of kernel attributes).
+ *   - Matrices are row-major; the leading dimension equals the row length.
+ *   - dtype selects fp16 (IEEE binary16) or bf16 for every 16-bit operand
+ *     and output; accumulation is always fp32 in tensor memory, rounding of
+ *     16-bit outputs is to nearest even.
+ *   - Calls are asynchronous on `stream` (a cudaStream_t passed as void*,
+ *     NULL = the legacy default stream).
+ *   - Argument errors return at once with nothing launched.  A CUDA launch
+ *     failure returns FLUX_ERR_CUDA (flux_last_cuda_error() gives the code).
+ *     Errors found on the device (a bounded wait that ran out) are recorded
+ *     in the workspace header and returned by flux_get_status().
+ *   - 16-byte alignment is required for every base pointer, and every row
+ *     pitch must be a multiple of 16 bytes (so inner dimensions are multiples
+ *     of 8 elements).  Violations return FLUX_ERR_UNSUPPORTED; there is no
+ *     fallback path.
+ *   - Workspaces must be 256-byte aligned, at least flux_*workspace_size()
+ *     bytes, and zero-filled once before first use (flux_workspace_init).
+ *     Every successful call leaves its workspace zero again.  Calls that share
+ *     one workspace must be ordered on the GPU (same stream or events); calls
+ *     that overlap on the GPU need separate workspaces.
+ */
+#ifndef FLUX_GB300_H
+#define FLUX_GB300_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define FLUX_MAX_RANKS 16
+#define FLUX_MAX_EXPERTS 1024
+
+typedef enum {
+  FLUX_OK = 0,
+  FLUX_ERR_INVALID_ARG = 1, /* null pointer, negative or inconsistent size, R out of range */
+  FLUX_ERR_UNSUPPORTED = 2, /* alignment / pitch / divisibility rule not met */
+  FLUX_ERR_WORKSPACE = 3,   /* workspace null, misaligned or smaller than required */
+  FLUX_ERR_CUDA = 4,        /* a CUDA runtime or driver call failed */
+  FLUX_ERR_TIMEOUT = 5,     /* device: a ready flag or pipeline wait exceeded timeout_ns */
+  FLUX_ERR_NO_DEVICE = 6    /* current device is not an sm_100-family (tcgen05) GPU */
+} flux_status_t;
+
+typedef enum { FLUX_F16 = 0, FLUX_BF16 = 1 } flux_dtype_t;
+
+typedef enum {
+  FLUX_OP_GEMM = 0,
+  FLUX_OP_AG_GEMM = 1,
+  FLUX_OP_GEMM_RS = 2,
+  FLUX_OP_MOE_AG = 3,
+  FLUX_OP_MOE_RS = 4
+} flux_op_t;
+
+/* Optional per-call settings; pass NULL for the defaults. */
+typedef struct {
+  uint32_t epoch;       /* AG ops: shard s is ready when ready_flags[s] >= epoch (default 1) */
+  uint32_t reserved0;
+  uint64_t timeout_ns;  /* bound on every device-side wait (0 = 2 s) */
+  int32_t num_ctas;     /* persistent grid size (0 = one CTA per SM) */
+  int32_t group_n;      /* tile raster: n-tiles per band (0 = 8) */
+  int32_t tiles_per_group; /* GEMM-RS: output tiles per rank-group (0 = grid size) */
+  int32_t reserved1;
+} flux_opts_t;
+
+/* What flux_get_status found in a workspace header. */
+typedef struct {
+  uint32_t status; /* flux_status_t of the first device-side error, 0 if none */
+  uint32_t where;  /* which wait gave up: 1 ready flag, 2 smem slot free, 3 smem slot full,
+                      4 accumulator free, 5 accumulator full, 6 drain */
+  uint32_t arg0;   /* flag wait: shard index; pipeline waits: CTA index */
+  uint32_t arg1;   /* flag wait: last flag value seen; pipeline waits: stage / buffer */
+} flux_device_report_t;
+
+/* ---------------------------------------------------------------- housekeeping */
+
+/* Version of this ABI (major * 10000 + minor * 100 + patch). */
+int flux_version(void);
+
+/* Human-readable name of a status code (static string, never NULL). */
+const char* flux_status_string(flux_status_t s);
+
+/* The cudaError_t of the most recent FLUX_ERR_CUDA on the calling thread. */
+int flux_last_cuda_error(void);
+
+/* Bytes of workspace a dense op needs (FLUX_OP_GEMM / AG_GEMM / GEMM_RS).
+ * M, N, K as in the op's own signature.  GEMM and AG-GEMM need only the
+ * 256-byte status header; GEMM-RS adds per-tile arrival counters and the fp32
+ * accumulation buffer of the owners' row chunks (M x N floats).  Returns 0 for
+ * an unknown op or invalid sizes. */
+size_t flux_workspace_size(flux_op_t op, int R, int M, int N, int K);
+
+/* Bytes of workspace a MoE op needs (FLUX_OP_MOE_AG / FLUX_OP_MOE_RS). */
+size_t flux_moe_workspace_size(flux_op_t op, int R, int T, int H, int F, int E, int topk);
+
+/* Zero `bytes` of a workspace on `stream` (cudaMemsetAsync). */
+flux_status_t flux_workspace_init(void* workspace, size_t bytes, void* stream);
+
+/* Synchronise `stream`, then read the device status of `workspace`.
+ * Returns FLUX_OK or the first device-side error recorded by a call that used
+ * this workspace.  If `report` is non-NULL it receives the details.  After an
+ * error the whole workspace (`bytes`) is zeroed again, so it can be reused. */
+flux_status_t flux_get_status(void* workspace, size_t bytes, void* stream,
+                              flux_device_report_t* report);
+
+/* ---------------------------------------------------------------- dense ops */
+
+/* Plain non-split GEMM: C[M x N] = A[M x K] . B[K x N].
+ * The GEMM_non-split baseline of ECT (paper review, section 三, "核心公式").
+ * A, B, C device; K = 0 writes zeros. */
+flux_status_t flux_gemm(int M, int N, int K, flux_dtype_t dtype, const void* A, const void* B,
+                        void* C, void* workspace, size_t workspace_bytes, const flux_opts_t* opts,
+                        void* stream);
+
+/* Output1_r = GEMM(AllGather(X), W1_r) for r in [0, R)
+ * (paper review, section 三, "MLP 前向传播", first GEMM; AllGather overlap,
+ * section 三 "AllGather 重叠").
+ *   x_shards[s]  device, [M/R x K]: the rows [s M/R, (s+1) M/R) of X owned by rank s
+ *   w_shards[r]  device, [K x N/R]: rank r's column block of W1
+ *   out[r]       device, [M x N/R]: rank r's Output1
+ *   ready_flags  device uint32[R] or NULL: the kernel pulls a tile of X_s only
+ *                after reading ready_flags[s] >= opts->epoch (acquire, gpu
+ *                scope); NULL means every shard is ready.  A flag that never
+ *                becomes ready ends the call with FLUX_ERR_TIMEOUT (reported by
+ *                flux_get_status) after opts->timeout_ns.
+ * Requires 1 <= R <= FLUX_MAX_RANKS, M and N divisible by R, (M/R) % 8 == 0,
+ * K % 8 == 0, (N/R) % 8 == 0. */
+flux_status_t flux_ag_gemm(int R, int M, int N, int K, flux_dtype_t dtype,
+                           const void* const* x_shards, const void* const* w_shards,
+                           void* const* out, const uint32_t* ready_flags, void* workspace,
+                           size_t workspace_bytes, const flux_opts_t* opts, void* stream);
+
+/* Output2_o = rows [o M/R, (o+1) M/R) of sum_r A_r . B_r, for o in [0, R)
+ * (paper review, section 三, "MLP 前向传播", second GEMM; ReduceScatter overlap,
+ * section 三 "ReduceScatter 重叠").
+ *   a_shards[r]  device, [M x K/R]: rank r's column block of Output1
+ *   b_shards[r]  device, [K/R x N]: rank r's row block of W2
+ *   out[o]       device, [M/R x N]: owner rank o's row chunk of the reduced product
+ * Every rank's partial tile is accumulated in fp32 into the owner's chunk of
+ * the workspace; the last partial to arrive converts the tile to 16 bits and
+ * stores it in out[owner].  Requires M and K divisible by R, (K/R) % 8 == 0,
+ * N % 8 == 0. */
+flux_status_t flux_gemm_rs(int R, int M, int N, int K, flux_dtype_t dtype,
+                           const void* const* a_shards, const void* const* b_shards,
+                           void* const* out, void* workspace, size_t workspace_bytes,
+                           const flux_opts_t* opts, void* stream);
+
+/* ---------------------------------------------------------------- MoE ops */
+
+/* Routing of T tokens with topk experts each (COMET article, section
+ * "COMET 的技术原理", token-dimension decomposition).  Slot s = t*topk + k.
+ *   topk_ids     device int32[T*topk], values in [0, E)
+ *   counts       device int32[E]      slots per expert
+ *   offsets      device int32[E+1]    exclusive prefix sum, offsets[E] = T*topk
+ *   slot_to_row  device int32[T*topk] offsets[id[s]] + #{s' < s : id[s'] = id[s]}
+ *   row_to_slot  device int32[T*topk] the inverse permutation (rows grouped by expert)
+ * Bit-exact and deterministic.  An id outside [0, E) is counted nowhere and
+ * makes the call record FLUX_ERR_INVALID_ARG in `workspace` (which must then
+ * hold at least 256 bytes; may be NULL to skip the check). */
+flux_status_t flux_moe_route(int T, int E, int topk, const int32_t* topk_ids, int32_t* counts,
+                             int32_t* offsets, int32_t* slot_to_row, int32_t* row_to_slot,
+                             void* workspace, size_t workspace_bytes, void* stream);
+
+/* MoE layer0: H_r[row] = AllGather(X)[token(row)] . W1_r[expert(row)] for r in [0, R),
+ * rows in the grouped (expert-sorted) order of flux_moe_route, which this call
+ * runs first and whose outputs it writes to counts/offsets/slot_to_row/row_to_slot.
+ *   x_shards[s]   device, [T/R x H]: token rows owned by rank s
+ *   w1_shards[r]  device, [E x H x F/R]: rank r's column block of every expert's W1
+ *   topk_ids      device int32[T x topk]
+ *   h_out[r]      device, [T*topk x F/R]
+ *   ready_flags   as in flux_ag_gemm (per token shard), or NULL
+ * Requires T and F divisible by R, H % 8 == 0, (F/R) % 8 == 0, 1 <= E <= FLUX_MAX_EXPERTS. */
+flux_status_t flux_moe_ag_grouped_gemm(int R, int T, int H, int F, int E, int topk,
+                                       flux_dtype_t dtype, const void* const* x_shards,
+                                       const void* const* w1_shards, const int32_t* topk_ids,
+                                       void* const* h_out, int32_t* counts, int32_t* offsets,
+                                       int32_t* slot_to_row, int32_t* row_to_slot,
+                                       const uint32_t* ready_flags, void* workspace,
+                                       size_t workspace_bytes, const flux_opts_t* opts,
+                                       void* stream);
+
+/* MoE layer1: Out_o[t] = sum_r sum_k topk_weights[t,k] . (H_r[slot_to_row[t*topk+k]] .
+ * W2_r[topk_ids[t,k]]) for the tokens t in [o T/R, (o+1) T/R) owned by rank o.
+ *   h_shards[r]   device, [T*topk x F/R]: layer0 output of rank r, grouped order
+ *   w2_shards[r]  device, [E x F/R x H]: rank r's row block of every expert's W2
+ *   topk_ids      device int32[T x topk]; topk_weights device float32[T x topk]
+ *   offsets, slot_to_row, row_to_slot: the routing that ordered h_shards
+ *                 (from flux_moe_route or layer0), or all three NULL to have
+ *                 this call recompute them in its workspace
+ *   out[o]        device, [T/R x H]
+ * Contributions are accumulated in fp32 in the workspace; the last of the
+ * R*topk contributions to a token row converts it to 16 bits.
+ * Requires T and F divisible by R, (F/R) % 8 == 0, H % 8 == 0. */
+flux_status_t flux_moe_grouped_gemm_rs(int R, int T, int H, int F, int E, int topk,
+                                       flux_dtype_t dtype, const void* const* h_shards,
+                                       const void* const* w2_shards, const int32_t* topk_ids,
+                                       const float* topk_weights, const int32_t* offsets,
+                                       const int32_t* slot_to_row, const int32_t* row_to_slot,
+                                       void* const* out, void* workspace, size_t workspace_bytes,
+                                       const flux_opts_t* opts, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FLUX_GB300_H */

@@ -1,0 +1,236 @@
+"""ctypes binding of libflux_gb300.so: argument marshalling only.
+
+Every function here has the name and the argument order of its C entry point
+in ``include/flux_gb300.h``.  Pointer arguments accept torch tensors (their
+``data_ptr()`` is passed), plain integers, or None for NULL; arrays of R
+pointers accept a list of tensors.  ``stream`` defaults to torch's current
+CUDA stream.  A non-OK status raises :class:`FluxError`.  No step of the
+computation happens in Python, and there is no fallback: importing this module
+raises if the compiled library is missing.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(HERE, "libflux_gb300.so")
+
+if not os.path.exists(LIB_PATH):
+    raise ImportError(
+        f"{LIB_PATH} is missing: build it with `python -m reducescatter_tcgen05_tmem_gb300.build` "
+        "(the library has no CPU or Python fallback)")
+
+_lib = ctypes.CDLL(LIB_PATH)
+
+# ---------------------------------------------------------------- constants
+FLUX_OK = 0
+FLUX_ERR_INVALID_ARG = 1
+FLUX_ERR_UNSUPPORTED = 2
+FLUX_ERR_WORKSPACE = 3
+FLUX_ERR_CUDA = 4
+FLUX_ERR_TIMEOUT = 5
+FLUX_ERR_NO_DEVICE = 6
+
+FLUX_F16 = 0
+FLUX_BF16 = 1
+
+FLUX_OP_GEMM = 0
+FLUX_OP_AG_GEMM = 1
+FLUX_OP_GEMM_RS = 2
+FLUX_OP_MOE_AG = 3
+FLUX_OP_MOE_RS = 4
+
+FLUX_MAX_RANKS = 16
+FLUX_MAX_EXPERTS = 1024
+
+WAIT_SITES = {1: "ready flag", 2: "smem slot free", 3: "smem slot full",
+              4: "accumulator free", 5: "accumulator full", 6: "drain"}
+
+
+class flux_opts_t(ctypes.Structure):
+    _fields_ = [("epoch", ctypes.c_uint32), ("reserved0", ctypes.c_uint32),
+                ("timeout_ns", ctypes.c_uint64), ("num_ctas", ctypes.c_int32),
+                ("group_n", ctypes.c_int32), ("tiles_per_group", ctypes.c_int32),
+                ("reserved1", ctypes.c_int32)]
+
+
+class flux_device_report_t(ctypes.Structure):
+    _fields_ = [("status", ctypes.c_uint32), ("where", ctypes.c_uint32),
+                ("arg0", ctypes.c_uint32), ("arg1", ctypes.c_uint32)]
+
+
+class FluxError(RuntimeError):
+    def __init__(self, status: int, what: str):
+        self.status = status
+        name = _lib.flux_status_string(status).decode()
+        extra = ""
+        if status == FLUX_ERR_CUDA:
+            extra = f" (cudaError {_lib.flux_last_cuda_error()})"
+        super().__init__(f"{what}: {name}{extra}")
+
+
+_vp = ctypes.c_void_p
+_i = ctypes.c_int
+_sz = ctypes.c_size_t
+_vpp = ctypes.POINTER(ctypes.c_void_p)
+_opt = ctypes.POINTER(flux_opts_t)
+
+_SIGS = {
+    "flux_version": ([], ctypes.c_int),
+    "flux_status_string": ([_i], ctypes.c_char_p),
+    "flux_last_cuda_error": ([], ctypes.c_int),
+    "flux_workspace_size": ([_i, _i, _i, _i, _i], _sz),
+    "flux_moe_workspace_size": ([_i, _i, _i, _i, _i, _i, _i], _sz),
+    "flux_workspace_init": ([_vp, _sz, _vp], _i),
+    "flux_get_status": ([_vp, _sz, _vp, ctypes.POINTER(flux_device_report_t)], _i),
+    "flux_gemm": ([_i, _i, _i, _i, _vp, _vp, _vp, _vp, _sz, _opt, _vp], _i),
+    "flux_ag_gemm": ([_i, _i, _i, _i, _i, _vpp, _vpp, _vpp, _vp, _vp, _sz, _opt, _vp], _i),
+    "flux_gemm_rs": ([_i, _i, _i, _i, _i, _vpp, _vpp, _vpp, _vp, _sz, _opt, _vp], _i),
+    "flux_moe_route": ([_i, _i, _i, _vp, _vp, _vp, _vp, _vp, _vp, _sz, _vp], _i),
+    "flux_moe_ag_grouped_gemm": ([_i, _i, _i, _i, _i, _i, _i, _vpp, _vpp, _vp, _vpp, _vp, _vp,
+                                  _vp, _vp, _vp, _vp, _sz, _opt, _vp], _i),
+    "flux_moe_grouped_gemm_rs": ([_i, _i, _i, _i, _i, _i, _i, _vpp, _vpp, _vp, _vp, _vp, _vp,
+                                  _vp, _vpp, _vp, _sz, _opt, _vp], _i),
+}
+for _name, (_args, _res) in _SIGS.items():
+    _fn = getattr(_lib, _name)
+    _fn.argtypes = _args
+    _fn.restype = _res
+
+EXPORTED = tuple(_SIGS)
+
+
+# ---------------------------------------------------------------- marshalling
+def _ptr(x):
+    if x is None:
+        return None
+    if isinstance(x, int):
+        return x
+    return x.data_ptr()
+
+
+def _ptrs(xs):
+    arr = (ctypes.c_void_p * len(xs))()
+    for i, x in enumerate(xs):
+        arr[i] = _ptr(x)
+    return arr
+
+
+def _nbytes(t):
+    return t.numel() * t.element_size()
+
+
+def _stream(stream):
+    if stream is None:
+        import torch
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream
+
+
+def _opts(opts):
+    if opts is None:
+        return None
+    if isinstance(opts, dict):
+        o = flux_opts_t()
+        for k, v in opts.items():
+            setattr(o, k, v)
+        opts = o
+    return ctypes.byref(opts)
+
+
+def _check(st, what):
+    if st != FLUX_OK:
+        raise FluxError(st, what)
+
+
+def dtype_code(t) -> int:
+    """FLUX_F16 / FLUX_BF16 for a torch dtype or tensor."""
+    import torch
+    dt = t.dtype if hasattr(t, "dtype") else t
+    if dt == torch.float16:
+        return FLUX_F16
+    if dt == torch.bfloat16:
+        return FLUX_BF16
+    raise ValueError(f"unsupported dtype {dt}")
+
+
+# ---------------------------------------------------------------- API (same names as the C ABI)
+def flux_version() -> int:
+    return _lib.flux_version()
+
+
+def flux_status_string(status: int) -> str:
+    return _lib.flux_status_string(status).decode()
+
+
+def flux_workspace_size(op: int, R: int, M: int, N: int, K: int) -> int:
+    return int(_lib.flux_workspace_size(op, R, M, N, K))
+
+
+def flux_moe_workspace_size(op: int, R: int, T: int, H: int, F: int, E: int, topk: int) -> int:
+    return int(_lib.flux_moe_workspace_size(op, R, T, H, F, E, topk))
+
+
+def flux_workspace_init(workspace, stream=None) -> None:
+    _check(_lib.flux_workspace_init(_ptr(workspace), _nbytes(workspace), _stream(stream)),
+           "flux_workspace_init")
+
+
+def flux_get_status(workspace, stream=None):
+    """(status, report) after synchronising the stream; never raises for device errors."""
+    rep = flux_device_report_t()
+    st = _lib.flux_get_status(_ptr(workspace), _nbytes(workspace), _stream(stream), ctypes.byref(rep))
+    if st in (FLUX_ERR_CUDA, FLUX_ERR_WORKSPACE):
+        raise FluxError(st, "flux_get_status")
+    return st, {"status": rep.status, "where": WAIT_SITES.get(rep.where, rep.where),
+                "arg0": rep.arg0, "arg1": rep.arg1}
+
+
+def flux_gemm(M, N, K, dtype, A, B, C, workspace, opts=None, stream=None) -> None:
+    _check(_lib.flux_gemm(M, N, K, dtype, _ptr(A), _ptr(B), _ptr(C), _ptr(workspace),
+                          _nbytes(workspace), _opts(opts), _stream(stream)), "flux_gemm")
+
+
+def flux_ag_gemm(R, M, N, K, dtype, x_shards, w_shards, out, ready_flags, workspace,
+                 opts=None, stream=None) -> None:
+    _check(_lib.flux_ag_gemm(R, M, N, K, dtype, _ptrs(x_shards), _ptrs(w_shards), _ptrs(out),
+                             _ptr(ready_flags), _ptr(workspace), _nbytes(workspace), _opts(opts),
+                             _stream(stream)), "flux_ag_gemm")
+
+
+def flux_gemm_rs(R, M, N, K, dtype, a_shards, b_shards, out, workspace, opts=None,
+                 stream=None) -> None:
+    _check(_lib.flux_gemm_rs(R, M, N, K, dtype, _ptrs(a_shards), _ptrs(b_shards), _ptrs(out),
+                             _ptr(workspace), _nbytes(workspace), _opts(opts), _stream(stream)),
+           "flux_gemm_rs")
+
+
+def flux_moe_route(T, E, topk, topk_ids, counts, offsets, slot_to_row, row_to_slot,
+                   workspace=None, stream=None) -> None:
+    _check(_lib.flux_moe_route(T, E, topk, _ptr(topk_ids), _ptr(counts), _ptr(offsets),
+                               _ptr(slot_to_row), _ptr(row_to_slot), _ptr(workspace),
+                               0 if workspace is None else _nbytes(workspace), _stream(stream)),
+           "flux_moe_route")
+
+
+def flux_moe_ag_grouped_gemm(R, T, H, F, E, topk, dtype, x_shards, w1_shards, topk_ids, h_out,
+                             counts, offsets, slot_to_row, row_to_slot, ready_flags, workspace,
+                             opts=None, stream=None) -> None:
+    _check(_lib.flux_moe_ag_grouped_gemm(
+        R, T, H, F, E, topk, dtype, _ptrs(x_shards), _ptrs(w1_shards), _ptr(topk_ids),
+        _ptrs(h_out), _ptr(counts), _ptr(offsets), _ptr(slot_to_row), _ptr(row_to_slot),
+        _ptr(ready_flags), _ptr(workspace), _nbytes(workspace), _opts(opts), _stream(stream)),
+        "flux_moe_ag_grouped_gemm")
+
+
+def flux_moe_grouped_gemm_rs(R, T, H, F, E, topk, dtype, h_shards, w2_shards, topk_ids,
+                             topk_weights, offsets, slot_to_row, row_to_slot, out, workspace,
+                             opts=None, stream=None) -> None:
+    _check(_lib.flux_moe_grouped_gemm_rs(
+        R, T, H, F, E, topk, dtype, _ptrs(h_shards), _ptrs(w2_shards), _ptr(topk_ids),
+        _ptr(topk_weights), _ptr(offsets), _ptr(slot_to_row), _ptr(row_to_slot), _ptrs(out),
+        _ptr(workspace), _nbytes(workspace), _opts(opts), _stream(stream)),
+        "flux_moe_grouped_gemm_rs")

@@ -1,0 +1,82 @@
+"""Build libflux_gb300.so (the C-ABI library) in place with nvcc for sm_103a.
+
+Each translation unit under ``csrc/`` is compiled in parallel, then linked
+into a shared library beside this file.  The CUDA runtime is linked
+dynamically so the library shares one runtime instance with PyTorch.
+
+Usage:  python -m reducescatter_tcgen05_tmem_gb300.build  [--verbose]
+"""
+from __future__ import annotations
+
+import os
+import shutil
+import subprocess
+import sys
+from concurrent.futures import ThreadPoolExecutor
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+CSRC = os.path.join(HERE, "csrc")
+BUILD = os.path.join(HERE, "_build")
+LIB_NAME = "libflux_gb300.so"
+LIB_PATH = os.path.join(HERE, LIB_NAME)
+
+SOURCES = ["flux_core.cu", "flux_dense.cu", "flux_moe.cu"]
+ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
+CFLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-Xcompiler", "-O2",
+          "-diag-suppress", "550", "-Xptxas", "-v"]
+
+
+def _nvcc() -> str:
+    cand = [os.environ.get("NVCC"), shutil.which("nvcc"), "/usr/local/cuda/bin/nvcc"]
+    for c in cand:
+        if c and os.path.exists(c):
+            return c
+    raise RuntimeError("nvcc not found")
+
+
+def _cuda_lib_dir(nvcc: str) -> str:
+    root = os.path.dirname(os.path.dirname(os.path.realpath(nvcc)))
+    for sub in ("lib64", "lib", "targets/sbsa-linux/lib", "targets/x86_64-linux/lib"):
+        d = os.path.join(root, sub)
+        if os.path.exists(os.path.join(d, "libcudart.so")):
+            return d
+    return os.path.join(root, "lib64")
+
+
+def _run(cmd, verbose):
+    r = subprocess.run(cmd, capture_output=True, text=True)
+    if verbose or r.returncode != 0:
+        sys.stderr.write(" ".join(cmd) + "\n" + r.stdout + r.stderr)
+    if r.returncode != 0:
+        raise RuntimeError(f"command failed ({r.returncode}): {' '.join(cmd[:3])} ...")
+    return r.stdout + r.stderr
+
+
+def build(verbose: bool = False, force: bool = False) -> str:
+    """Compile and link; returns the path of the shared library."""
+    nvcc = _nvcc()
+    os.makedirs(BUILD, exist_ok=True)
+    deps = [os.path.join(CSRC, f) for f in os.listdir(CSRC)]
+    deps.append(os.path.join(os.path.dirname(HERE), "include", "flux_gb300.h"))
+    newest = max(os.path.getmtime(d) for d in deps)
+    if (not force and os.path.exists(LIB_PATH) and os.path.getmtime(LIB_PATH) >= newest
+            and os.path.getmtime(LIB_PATH) >= os.path.getmtime(__file__)):
+        return LIB_PATH
+
+    def compile_one(src):
+        obj = os.path.join(BUILD, src.replace(".cu", ".o"))
+        _run([nvcc, *ARCH, *CFLAGS, "-c", os.path.join(CSRC, src), "-o", obj], verbose)
+        return obj
+
+    with ThreadPoolExecutor(len(SOURCES)) as ex:
+        objs = list(ex.map(compile_one, SOURCES))
+    libdir = _cuda_lib_dir(nvcc)
+    tmp = LIB_PATH + ".tmp"
+    _run([nvcc, *ARCH, "-shared", "-cudart", "shared", "-o", tmp, *objs,
+          f"-L{libdir}", "-Xlinker", f"-rpath={libdir}"], verbose)
+    os.replace(tmp, LIB_PATH)
+    return LIB_PATH
+
+
+if __name__ == "__main__":
+    print(build(verbose="--verbose" in sys.argv, force="--force" in sys.argv))

@@ -1,0 +1,51 @@
+// Host-side helpers shared by the C-ABI entry points: device checks, tensor
+// map encoding, argument validation and the per-call launch bookkeeping.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include "../../include/flux_gb300.h"
+
+namespace flux {
+
+constexpr size_t WS_HEADER = 256;  // status header at the start of every workspace
+constexpr size_t WS_ALIGN = 256;
+
+struct DeviceInfo {
+  int device;
+  int sm_count;
+  int cc_major, cc_minor;
+  size_t max_smem_optin;
+};
+
+// Current device's properties (cached); FLUX_ERR_NO_DEVICE if it has no tcgen05.
+flux_status_t current_device(DeviceInfo* info);
+
+// Remember a failing cudaError_t for flux_last_cuda_error() and return FLUX_ERR_CUDA.
+flux_status_t cuda_fail(cudaError_t e);
+
+// Fresh per-call id (never 0) written into the abort word if the call aborts.
+uint32_t next_seq();
+
+// 2-D row-major tensor [outer x inner] of 16-bit elements with 128-byte swizzle.
+flux_status_t encode_2d(CUtensorMap* map, flux_dtype_t dt, const void* base, uint64_t inner,
+                        uint64_t outer, uint64_t row_pitch_bytes, uint32_t box_inner,
+                        uint32_t box_outer);
+
+// 3-D row-major tensor [d2 x d1 x d0] of 16-bit elements with 128-byte swizzle.
+flux_status_t encode_3d(CUtensorMap* map, flux_dtype_t dt, const void* base, uint64_t d0,
+                        uint64_t d1, uint64_t d2, uint32_t box0, uint32_t box1);
+
+inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+inline size_t round_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+
+// Validate a workspace pointer and size.
+flux_status_t check_workspace(const void* ws, size_t have, size_t need);
+
+// Default timeout when opts is NULL or timeout_ns == 0.
+constexpr uint64_t DEFAULT_TIMEOUT_NS = 2000000000ull;
+
+}  // namespace flux

@@ -1,0 +1,728 @@
+// Persistent, warp-specialised tcgen05 GEMM with fused tensor-parallel
+// collectives over R virtual ranks (all ranks' buffers live on this GPU).
+//
+//   producer warp(s)  TMA (or cp.async row gather) of A/B k-slices into a
+//                     STAGES-deep shared-memory ring; for AllGather, the A tile
+//                     is pulled from the rank that owns its rows only after that
+//                     rank's ready flag is seen (acquire)
+//   MMA warp          one thread issues tcgen05.mma (128 x 256 x 16, fp32 in
+//                     TMEM) per k-substep; accumulators are double-buffered in
+//                     the 512 TMEM columns so the epilogue of one tile overlaps
+//                     the main loop of the next
+//   epilogue warps    tcgen05.ld TMEM -> registers, then one of:
+//                       STORE        convert to 16 bits, store (AllGather-GEMM, plain GEMM)
+//                       REDUCE       fp32 add into the owner rank's row chunk of the
+//                                    workspace; the last partial converts and stores
+//                                    (GEMM + ReduceScatter)
+//                       MOE_GATHER   STORE with A rows gathered by expert (MoE layer0)
+//                       MOE_SCATTER  gate-weighted fp32 add into the owning token row;
+//                                    the last of R*topk contributions converts (MoE layer1)
+//
+// Every wait is bounded: after timeout_ns (or an iteration cap) the thread
+// records FLUX_ERR_TIMEOUT in the workspace header, raises the per-call abort
+// word, and the CTA drains its in-flight copies and MMAs, frees TMEM and exits.
+#pragma once
+
+#include "flux_ptx.cuh"
+
+namespace flux {
+
+constexpr int BM = 128;  // tile rows (MMA M)
+constexpr int BN = 256;  // tile columns (MMA N)
+constexpr int BK = 64;   // k-slice per pipeline stage (one 128-byte swizzle row of 16-bit data)
+constexpr int UK = 16;   // K of one tcgen05.mma kind::f16
+constexpr int STAGES = 4;
+constexpr int A_STAGE = BM * BK * 2;  // 16 KB
+constexpr int B_STAGE = BN * BK * 2;  // 32 KB
+constexpr int B_BOX_N = 64;           // 64 columns = 128 bytes, one swizzle span
+constexpr int TMEM_COLS = 2 * BN;     // two fp32 accumulators
+constexpr int MAXR = 16;
+constexpr int EPI_WARPS = 4;
+constexpr int GATHER_LAG = 2;         // cp.async groups in flight before a stage is published
+
+constexpr int SMEM_BYTES = STAGES * (A_STAGE + B_STAGE) + 1024 /*align*/ + 256 /*barriers*/;
+
+enum Mode { MODE_STORE = 0, MODE_REDUCE = 1, MODE_MOE_GATHER = 2, MODE_MOE_SCATTER = 3 };
+
+// device status header at the start of every workspace (256 bytes)
+enum HdrField { H_STATUS = 0, H_WHERE = 1, H_ARG0 = 2, H_ARG1 = 3, H_ABORT = 4 };
+enum WaitSite { W_FLAG = 1, W_EMPTY = 2, W_FULL = 3, W_TEMPTY = 4, W_TFULL = 5, W_DRAIN = 6 };
+constexpr uint32_t ST_TIMEOUT = 5;
+constexpr uint32_t ST_INVALID = 1;
+
+struct KParams {
+  CUtensorMap tmA[MAXR];   // per-rank A operand maps (K-major, 128B swizzle)
+  CUtensorMap tmB[MAXR];   // per-rank B operand maps (N-major, 128B swizzle)
+  void* out[MAXR];         // per-rank outputs
+  const void* xsrc[MAXR];  // MOE_GATHER: per-shard token rows
+  int R;
+  int M;                   // rows of the A row space (AG: gathered rows; MoE: T*topk)
+  int N;                   // output columns of one rank
+  int K;                   // reduction length of one rank
+  int Mt, Nt, KT;          // tiles along M, N and k-slices along K
+  int ldo;                 // output row pitch (elements)
+  int rows_per_rank;       // AG: rows per X shard; RS: rows per owner chunk; MoE: tokens per rank
+  int a_box_m;             // rows per A TMA box (AG)
+  int group_n;             // raster band width in n-tiles
+  int tiles_per_group;     // REDUCE: output tiles per rank-group
+  int stream_k;            // REDUCE: 1 = contiguous k-step ranges per CTA
+  int num_units;           // dense modes: number of work units
+  long long total_ksteps;  // REDUCE stream-K: num_units * KT
+  const uint32_t* flags;   // AG ready flags (nullptr = all ready)
+  uint32_t epoch;
+  uint32_t seq;            // per-call id, written to the abort word on error
+  uint64_t timeout_ns;
+  uint32_t* hdr;           // workspace header
+  uint32_t* counters;      // REDUCE / MOE_SCATTER arrival counters
+  float* acc;              // REDUCE / MOE_SCATTER fp32 accumulation rows
+  // MoE routing (device arrays)
+  const int32_t* offsets;      // [E+1]
+  const int32_t* row_to_slot;  // [T*topk]
+  const int32_t* tile_off;     // [E+1] first m-tile of each expert
+  const float* topk_w;         // [T*topk]
+  int E, topk, T, H;
+};
+
+struct Ctl {
+  uint32_t* hdr;
+  uint32_t seq;
+  uint64_t flag_timeout;
+  uint64_t pipe_timeout;
+};
+
+__device__ __forceinline__ bool aborted(const Ctl& c) {
+  return ld_volatile_u32(c.hdr + H_ABORT) == c.seq;
+}
+
+static __device__ __noinline__ void raise_error(const Ctl& c, uint32_t code, uint32_t where,
+                                         uint32_t a0, uint32_t a1) {
+  if (atomicCAS(c.hdr + H_STATUS, 0u, code) == 0u) {
+    c.hdr[H_WHERE] = where;
+    c.hdr[H_ARG0] = a0;
+    c.hdr[H_ARG1] = a1;
+  }
+  __threadfence();
+  atomicExch(c.hdr + H_ABORT, c.seq);
+}
+
+// Bounded mbarrier wait.  0 = phase completed, 1 = timed out (recorded),
+// 2 = another thread aborted this call.  `check_abort` = false is used by the
+// final drains, which must outlive an abort.
+static __device__ __noinline__ int wait_bar_slow(uint32_t bar, uint32_t parity, const Ctl& c,
+                                          uint32_t where, uint32_t arg1, bool check_abort) {
+  const uint64_t t0 = globaltimer();
+  for (uint32_t it = 1;; ++it) {
+    if (mbar_try_wait(bar, parity)) return 0;
+    if ((it & 15u) == 0u) {
+      if (check_abort && aborted(c)) return 2;
+      if (globaltimer() - t0 > c.pipe_timeout || it > (1u << 30)) {
+        raise_error(c, ST_TIMEOUT, where, blockIdx.x, arg1);
+        return 1;
+      }
+    }
+  }
+}
+
+__device__ __forceinline__ int wait_bar(uint32_t bar, uint32_t parity, const Ctl& c,
+                                        uint32_t where, uint32_t arg1, bool check_abort = true) {
+  if (mbar_try_wait(bar, parity)) return 0;
+  return wait_bar_slow(bar, parity, c, where, arg1, check_abort);
+}
+
+// Bounded wait for ready_flags[s] >= epoch (acquire at gpu scope).  True when ready.
+static __device__ __noinline__ bool wait_flag(const uint32_t* flags, int s, uint32_t epoch, const Ctl& c) {
+  uint32_t v = ld_acquire_u32(flags + s);
+  if (v >= epoch) return true;
+  const uint64_t t0 = globaltimer();
+  for (uint32_t it = 1;; ++it) {
+    __nanosleep(128);
+    v = ld_acquire_u32(flags + s);
+    if (v >= epoch) return true;
+    if ((it & 7u) == 0u) {
+      if (aborted(c)) return false;
+      if (globaltimer() - t0 > c.flag_timeout || it > (1u << 28)) {
+        raise_error(c, ST_TIMEOUT, W_FLAG, static_cast<uint32_t>(s), v);
+        return false;
+      }
+    }
+  }
+}
+
+// ---------------------------------------------------------------- tile schedule
+// Band raster: bands of `group_n` n-tiles; inside a band the m-tile index runs
+// fastest, so the CTAs of one wave share a few B column tiles and sweep A.
+__device__ __forceinline__ void raster(int t, int Mt, int Nt, int group_n, int& mt, int& nt) {
+  const int band = Mt * group_n;
+  const int g = t / band;
+  const int local = t - g * band;
+  mt = local % Mt;
+  nt = g * group_n + local / Mt;
+}
+
+struct Work {
+  int r;       // rank whose operands feed the tile
+  int mt, nt;  // tile coordinates (mt: m-tile in the A row space)
+  int m0;      // first A row of the tile
+  int row_end; // rows >= row_end are not part of the tile's problem
+  int e;       // expert (MoE)
+  int k0, k1;  // k-slice range of this item
+  int tile;    // linear output-tile id (REDUCE counters)
+};
+
+// AllGather / plain GEMM: unit -> (rank, m-tile, n-tile).  Ranks are the
+// outer loop; inside a rank the m order is rotated so that rank r starts with
+// the rows it owns (the local shard is the first to be ready) and then walks
+// the other ranks' shards in ring order.
+__device__ __forceinline__ Work decode_store(const KParams& p, int u) {
+  Work w;
+  const int per_rank = p.Mt * p.Nt;
+  w.r = u / per_rank;
+  int mt, nt;
+  raster(u - w.r * per_rank, p.Mt, p.Nt, p.group_n, mt, nt);
+  const int mt_per_shard = p.rows_per_rank / BM;
+  if (mt_per_shard > 0 && p.rows_per_rank % BM == 0) mt = (mt + w.r * mt_per_shard) % p.Mt;
+  w.mt = mt;
+  w.nt = nt;
+  w.m0 = mt * BM;
+  w.row_end = p.M;
+  w.e = 0;
+  w.k0 = 0;
+  w.k1 = p.KT;
+  w.tile = 0;
+  return w;
+}
+
+// GEMM + ReduceScatter: unit -> (tile group, rank, tile).  The R partials of
+// one output tile are `tiles_per_group` units apart, so with a strided
+// persistent schedule they land in consecutive waves while the owner's fp32
+// tile is still in L2.
+__device__ __forceinline__ Work decode_reduce(const KParams& p, int u) {
+  Work w;
+  const int tiles = p.Mt * p.Nt;
+  const int TG = p.tiles_per_group;
+  const int full_groups = tiles / TG;
+  int t;
+  if (u < full_groups * TG * p.R) {
+    const int g = u / (TG * p.R);
+    const int rem = u - g * TG * p.R;
+    w.r = rem / TG;
+    t = g * TG + (rem - w.r * TG);
+  } else {
+    const int tl = tiles - full_groups * TG;
+    const int rem = u - full_groups * TG * p.R;
+    w.r = rem / tl;
+    t = full_groups * TG + (rem - w.r * tl);
+  }
+  raster(t, p.Mt, p.Nt, p.group_n, w.mt, w.nt);
+  w.tile = w.mt * p.Nt + w.nt;
+  w.m0 = w.mt * BM;
+  w.row_end = p.M;
+  w.e = 0;
+  w.k0 = 0;
+  w.k1 = p.KT;
+  return w;
+}
+
+// MoE: unit -> (rank, grouped m-tile, n-tile); the expert of an m-tile comes
+// from the device tile-offset table written by the routing kernel.
+__device__ __forceinline__ Work decode_moe(const KParams& p, int u, int total_mt) {
+  Work w;
+  const int per_rank = total_mt * p.Nt;
+  w.r = u / per_rank;
+  int t = u - w.r * per_rank;
+  int gmt, nt;
+  // m-tile fastest inside bands of group_n n-tiles
+  raster(t, total_mt, p.Nt, p.group_n, gmt, nt);
+  int lo = 0, hi = p.E;  // largest e with tile_off[e] <= gmt
+  while (hi - lo > 1) {
+    const int mid = (lo + hi) >> 1;
+    if (__ldg(p.tile_off + mid) <= gmt) lo = mid; else hi = mid;
+  }
+  w.e = lo;
+  const int e_off = __ldg(p.offsets + lo);
+  w.m0 = e_off + (gmt - __ldg(p.tile_off + lo)) * BM;
+  w.row_end = __ldg(p.offsets + lo + 1);
+  w.mt = gmt;
+  w.nt = nt;
+  w.k0 = 0;
+  w.k1 = p.KT;
+  w.tile = 0;
+  return w;
+}
+
+// Iterates the items of this CTA identically in every role.
+template <int MODE>
+struct ItemIter {
+  const KParams& p;
+  int total_mt;      // MoE: device-computed number of m-tiles
+  int num_units;
+  long long pos, end;  // stream-K k-step range
+  int u;
+
+  __device__ ItemIter(const KParams& p_, int total_mt_) : p(p_), total_mt(total_mt_) {
+    if (MODE == MODE_MOE_GATHER || MODE == MODE_MOE_SCATTER) {
+      num_units = total_mt * p.Nt * p.R;
+    } else {
+      num_units = p.num_units;
+    }
+    u = blockIdx.x;
+    if (MODE == MODE_REDUCE && p.stream_k) {
+      const long long L = p.total_ksteps;
+      pos = L * blockIdx.x / gridDim.x;
+      end = L * (blockIdx.x + 1) / gridDim.x;
+    }
+  }
+
+  __device__ bool next(Work& w) {
+    if (MODE == MODE_REDUCE && p.stream_k) {
+      if (pos >= end) return false;
+      const int unit = static_cast<int>(pos / p.KT);
+      const int k0 = static_cast<int>(pos - static_cast<long long>(unit) * p.KT);
+      long long k1 = k0 + (end - pos);
+      if (k1 > p.KT) k1 = p.KT;
+      w = decode_reduce(p, unit);
+      w.k0 = k0;
+      w.k1 = static_cast<int>(k1);
+      pos += k1 - k0;
+      return true;
+    }
+    if (u >= num_units) return false;
+    if (MODE == MODE_STORE) w = decode_store(p, u);
+    else if (MODE == MODE_REDUCE) w = decode_reduce(p, u);
+    else w = decode_moe(p, u, total_mt);
+    u += gridDim.x;
+    return true;
+  }
+};
+
+// ---------------------------------------------------------------- roles
+struct Smem {
+  uint8_t* a;       // STAGES x A_STAGE
+  uint8_t* b;       // STAGES x B_STAGE
+  uint64_t* full;   // [STAGES]
+  uint64_t* empty;  // [STAGES]
+  uint64_t* tfull;  // [2]
+  uint64_t* tempty; // [2]
+  uint64_t* drain;  // [1]
+  uint32_t* tmem_slot;
+};
+
+// TMA producer (one thread).
+template <int MODE>
+__device__ void producer_tma(const KParams& p, const Smem& s, const Ctl& c, int total_mt) {
+  ItemIter<MODE> iter(p, total_mt);
+  Work w;
+  uint32_t stage = 0, phase = 0;
+  uint32_t issued = 0;
+  uint32_t ready = (p.flags == nullptr) ? 0xFFFFFFFFu : 0u;
+  bool ok = true;
+  while (ok && iter.next(w)) {
+    int nbox_a = 0;
+    if (MODE == MODE_STORE) {
+      // shards covering the valid rows of this tile must be published first
+      const int last_row = min(w.m0 + BM, w.row_end) - 1;
+      const int s0 = w.m0 / p.rows_per_rank, s1 = last_row / p.rows_per_rank;
+      for (int sh = s0; sh <= s1 && ok; ++sh) {
+        if (!((ready >> sh) & 1u)) {
+          if (!wait_flag(p.flags, sh, p.epoch, c)) ok = false;
+          else ready |= 1u << sh;
+        }
+      }
+      if (!ok) break;
+      if (p.flags != nullptr) fence_proxy_async_global();
+      nbox_a = (min(w.m0 + BM, w.row_end) - w.m0 + p.a_box_m - 1) / p.a_box_m;
+    }
+    const int nbox_b = min(BN / B_BOX_N, (p.N - w.nt * BN + B_BOX_N - 1) / B_BOX_N);
+    const uint32_t bytes_a = (MODE == MODE_STORE) ? nbox_a * p.a_box_m * BK * 2 : A_STAGE;
+    const uint32_t bytes = bytes_a + nbox_b * B_BOX_N * BK * 2;
+    for (int k = w.k0; k < w.k1; ++k) {
+      if (wait_bar(smem_u32(&s.empty[stage]), phase ^ 1u, c, W_EMPTY, stage) != 0) { ok = false; break; }
+      const uint32_t fb = smem_u32(&s.full[stage]);
+      mbar_arrive_expect_tx(fb, bytes);
+      const uint32_t sa = smem_u32(s.a + stage * A_STAGE);
+      const uint32_t sb = smem_u32(s.b + stage * B_STAGE);
+      const int kc = k * BK;
+      if (MODE == MODE_STORE) {
+        for (int bx = 0; bx < nbox_a; ++bx) {
+          const int row = w.m0 + bx * p.a_box_m;
+          const int sh = row / p.rows_per_rank;
+          tma_load_2d(sa + bx * p.a_box_m * BK * 2, &p.tmA[sh], fb, kc, row - sh * p.rows_per_rank);
+        }
+      } else {
+        tma_load_2d(sa, &p.tmA[w.r], fb, kc, w.m0);
+      }
+      for (int j = 0; j < nbox_b; ++j) {
+        const int n = w.nt * BN + j * B_BOX_N;
+        if (MODE == MODE_MOE_SCATTER)
+          tma_load_3d(sb + j * B_BOX_N * BK * 2, &p.tmB[w.r], fb, n, kc, w.e);
+        else
+          tma_load_2d(sb + j * B_BOX_N * BK * 2, &p.tmB[w.r], fb, n, kc);
+      }
+      ++issued;
+      if (++stage == STAGES) { stage = 0; phase ^= 1u; }
+    }
+  }
+  // drain: every issued copy must land before the CTA may exit
+  for (uint32_t st = 0; st < STAGES; ++st) {
+    const uint32_t fills = issued / STAGES + (st < issued % STAGES ? 1u : 0u);
+    if (fills > 0) wait_bar(smem_u32(&s.full[st]), (fills - 1u) & 1u, c, W_DRAIN, st, false);
+  }
+}
+
+// cp.async row-gather producer for MoE layer0 (all producer threads).  Thread i
+// copies row i of the A tile (128 bytes per k-slice) from the token row of the
+// rank that owns it, into the 128B-swizzled layout the MMA descriptor expects;
+// thread 0 also issues the B tile by TMA.
+template <int NPROD>
+__device__ void producer_gather(const KParams& p, const Smem& s, const Ctl& c, int total_mt) {
+  ItemIter<MODE_MOE_GATHER> iter(p, total_mt);
+  const int tid = threadIdx.x;  // producer warps are warps 0 .. NPROD/32-1
+  Work w;
+  uint32_t stage = 0, phase = 0, issued = 0;
+  int pending = 0;  // stages whose cp.async group is committed but not yet published
+  uint32_t ready = (p.flags == nullptr) ? 0xFFFFFFFFu : 0u;
+  bool ok = true;
+  const char* any_src = static_cast<const char*>(p.xsrc[0]);
+  while (ok && iter.next(w)) {
+    // my row of this tile
+    const int row = w.m0 + tid;
+    const char* src = nullptr;
+    if (tid < BM && row < w.row_end) {
+      const int slot = __ldg(p.row_to_slot + row);
+      const int tok = slot / p.topk;
+      const int sh = tok / p.rows_per_rank;
+      if (!((ready >> sh) & 1u)) {
+        if (!wait_flag(p.flags, sh, p.epoch, c)) ok = false;
+        else ready |= 1u << sh;
+      }
+      src = static_cast<const char*>(p.xsrc[sh]) +
+            static_cast<size_t>(tok - sh * p.rows_per_rank) * p.H * 2;
+    }
+    if (!ok) break;
+    const int nbox_b = min(BN / B_BOX_N, (p.N - w.nt * BN + B_BOX_N - 1) / B_BOX_N);
+    const uint32_t bytes_b = nbox_b * B_BOX_N * BK * 2;
+    for (int k = w.k0; k < w.k1; ++k) {
+      int wr = wait_bar(smem_u32(&s.empty[stage]), phase ^ 1u, c, W_EMPTY, stage);
+      if (wr != 0) { ok = false; break; }
+      const uint32_t fb = smem_u32(&s.full[stage]);
+      const uint32_t sa = smem_u32(s.a + stage * A_STAGE);
+      const uint32_t sb = smem_u32(s.b + stage * B_STAGE);
+      const int kc = k * BK;
+      if (tid == 0) {
+        mbar_arrive_expect_tx(fb, bytes_b);
+        for (int j = 0; j < nbox_b; ++j)
+          tma_load_3d(sb + j * B_BOX_N * BK * 2, &p.tmB[w.r], fb, w.nt * BN + j * B_BOX_N, kc, w.e);
+      }
+      if (tid < BM) {
+        const uint32_t drow = sa + tid * 128;
+#pragma unroll
+        for (int ch = 0; ch < 8; ++ch) {
+          const uint32_t dst = drow + ((ch ^ (tid & 7)) << 4);
+          const int col = kc + ch * 8;
+          if (src != nullptr && col < p.H) cp_async_16(dst, src + static_cast<size_t>(col) * 2);
+          else cp_async_zero_16(dst, any_src);
+        }
+      }
+      cp_async_commit();
+      ++issued;
+      ++pending;
+      if (pending > GATHER_LAG) {
+        cp_async_wait<GATHER_LAG>();
+        fence_proxy_async_smem();
+        const uint32_t old_stage = (stage + STAGES - GATHER_LAG) % STAGES;
+        mbar_arrive(smem_u32(&s.full[old_stage]));
+        --pending;
+      }
+      if (++stage == STAGES) { stage = 0; phase ^= 1u; }
+    }
+  }
+  // publish what is still pending (also on abort, so the copies are complete)
+  cp_async_wait<0>();
+  fence_proxy_async_smem();
+  for (; pending > 0; --pending) {
+    const uint32_t old_stage = (stage + STAGES - pending) % STAGES;
+    mbar_arrive(smem_u32(&s.full[old_stage]));
+  }
+  if (tid == 0) {
+    for (uint32_t st = 0; st < STAGES; ++st) {
+      const uint32_t fills = issued / STAGES + (st < issued % STAGES ? 1u : 0u);
+      if (fills > 0) wait_bar(smem_u32(&s.full[st]), (fills - 1u) & 1u, c, W_DRAIN, st, false);
+    }
+  }
+}
+
+// MMA issuer (one thread).
+template <int MODE, int DT>
+__device__ void mma_issuer(const KParams& p, const Smem& s, const Ctl& c, uint32_t tmem_base,
+                           int total_mt) {
+  constexpr uint32_t IDESC = idesc_f16(DT, BM, BN, 0, 1);
+  ItemIter<MODE> iter(p, total_mt);
+  Work w;
+  uint32_t stage = 0, phase = 0;
+  int it = 0;
+  bool any = false;
+  bool ok = true;
+  while (ok && iter.next(w)) {
+    const uint32_t b = it & 1;
+    const uint32_t use = static_cast<uint32_t>(it >> 1);
+    if (wait_bar(smem_u32(&s.tempty[b]), (use & 1u) ^ 1u, c, W_TEMPTY, b) != 0) break;
+    tc_fence_after();
+    const uint32_t d = tmem_base + b * BN;
+    for (int k = w.k0; k < w.k1; ++k) {
+      if (wait_bar(smem_u32(&s.full[stage]), phase, c, W_FULL, stage) != 0) { ok = false; break; }
+      tc_fence_after();
+      const uint32_t sa = smem_u32(s.a + stage * A_STAGE);
+      const uint32_t sb = smem_u32(s.b + stage * B_STAGE);
+#pragma unroll
+      for (int kk = 0; kk < BK / UK; ++kk) {
+        // A: K-major rows of 128 B, 8-row groups 1024 B apart; a 16-wide k step is +32 B.
+        const uint64_t ad = sdesc_sw128(sa + kk * UK * 2, 16, 1024);
+        // B: N-major; 64-column (128 B) panels BK*128 B apart, 8-k-row groups 1024 B
+        // apart; a 16-deep k step is 16 rows = +2048 B.
+        const uint64_t bd = sdesc_sw128(sb + kk * UK * 128, BK * 128, 1024);
+        umma_f16(d, ad, bd, IDESC, (k > w.k0 || kk > 0) ? 1u : 0u);
+      }
+      umma_commit(smem_u32(&s.empty[stage]));
+      any = true;
+      if (++stage == STAGES) { stage = 0; phase ^= 1u; }
+    }
+    if (!ok) break;
+    umma_commit(smem_u32(&s.tfull[b]));
+    ++it;
+  }
+  if (any) {
+    umma_commit(smem_u32(s.drain));
+    wait_bar(smem_u32(s.drain), 0, c, W_DRAIN, 0, false);
+  }
+}
+
+// epilogue helpers -----------------------------------------------------------
+template <int DT>
+__device__ __forceinline__ void store_row_chunk(void* out, long long row_off_elems, int col0,
+                                                int ncols_valid, const uint32_t (&v)[32]) {
+  // 32 fp32 -> 32 x 16-bit, four 16-byte stores (columns col0 .. col0+31)
+  uint16_t* o = static_cast<uint16_t*>(out) + row_off_elems + col0;
+#pragma unroll
+  for (int g = 0; g < 4; ++g) {
+    if (g * 8 < ncols_valid) {
+      uint4 q;
+      q.x = pack2<DT>(__uint_as_float(v[g * 8 + 0]), __uint_as_float(v[g * 8 + 1]));
+      q.y = pack2<DT>(__uint_as_float(v[g * 8 + 2]), __uint_as_float(v[g * 8 + 3]));
+      q.z = pack2<DT>(__uint_as_float(v[g * 8 + 4]), __uint_as_float(v[g * 8 + 5]));
+      q.w = pack2<DT>(__uint_as_float(v[g * 8 + 6]), __uint_as_float(v[g * 8 + 7]));
+      *reinterpret_cast<uint4*>(o + g * 8) = q;
+    }
+  }
+}
+
+__device__ __forceinline__ void red_row_chunk(float* dst, int ncols_valid, const uint32_t (&v)[32],
+                                              float scale) {
+#pragma unroll
+  for (int g = 0; g < 8; ++g) {
+    if (g * 4 < ncols_valid) {
+      float4 q = make_float4(__uint_as_float(v[g * 4 + 0]) * scale, __uint_as_float(v[g * 4 + 1]) * scale,
+                             __uint_as_float(v[g * 4 + 2]) * scale, __uint_as_float(v[g * 4 + 3]) * scale);
+      atomicAdd(reinterpret_cast<float4*>(dst + g * 4), q);
+    }
+  }
+}
+
+// Convert 8 consecutive fp32 accumulators (L2) to 16 bits, store them, and
+// zero the accumulators for the next call.
+template <int DT>
+__device__ __forceinline__ void convert8(float* src, uint16_t* dst) {
+  const float4 a = ld_cg_f4(src);
+  const float4 b = ld_cg_f4(src + 4);
+  uint4 q;
+  q.x = pack2<DT>(a.x, a.y);
+  q.y = pack2<DT>(a.z, a.w);
+  q.z = pack2<DT>(b.x, b.y);
+  q.w = pack2<DT>(b.z, b.w);
+  *reinterpret_cast<uint4*>(dst) = q;
+  const float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
+  st_cg_f4(src, z);
+  st_cg_f4(src + 4, z);
+}
+
+template <int MODE, int DT>
+__device__ void epilogue(const KParams& p, const Smem& s, const Ctl& c, uint32_t tmem_base,
+                         int total_mt, int warp) {
+  const int lane = threadIdx.x & 31;
+  const int q = warp & 3;  // TMEM lane quarter this warp may access
+  ItemIter<MODE> iter(p, total_mt);
+  Work w;
+  int it = 0;
+  while (iter.next(w)) {
+    const uint32_t b = it & 1;
+    const uint32_t use = static_cast<uint32_t>(it >> 1);
+    // one lane waits so that the whole warp takes the same exit decision
+    // before the warp-collective tcgen05.ld below
+    int wr = 0;
+    if (lane == 0) wr = wait_bar(smem_u32(&s.tfull[b]), use & 1u, c, W_TFULL, b);
+    wr = __shfl_sync(0xFFFFFFFFu, wr, 0);
+    if (wr != 0) break;
+    tc_fence_after();
+    const int row = w.m0 + q * 32 + lane;  // row of the A row space held by this thread
+    const bool row_ok = row < w.row_end;
+    const uint32_t taddr = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + b * BN;
+    const int n0 = w.nt * BN;
+    const int ncols = min(BN, p.N - n0);
+    // per-row routing data
+    float gate = 1.0f;
+    int tok = 0;
+    if (MODE == MODE_MOE_SCATTER && row_ok) {
+      const int slot = __ldg(p.row_to_slot + row);
+      tok = slot / p.topk;
+      gate = __ldg(p.topk_w + slot);
+    }
+    for (int ch = 0; ch < BN / 32; ++ch) {
+      if (ch * 32 >= ncols) break;  // warp-uniform
+      uint32_t v[32];
+      tmem_ld_32x32b_x32(taddr + ch * 32, v);
+      const int nv = ncols - ch * 32;
+      if (!row_ok) continue;
+      if (MODE == MODE_STORE || MODE == MODE_MOE_GATHER) {
+        store_row_chunk<DT>(p.out[w.r], static_cast<long long>(row) * p.ldo, n0 + ch * 32, nv, v);
+      } else if (MODE == MODE_REDUCE) {
+        red_row_chunk(p.acc + static_cast<long long>(row) * p.N + n0 + ch * 32, nv, v, 1.0f);
+      } else {
+        red_row_chunk(p.acc + static_cast<long long>(tok) * p.N + n0 + ch * 32, nv, v, gate);
+      }
+    }
+    // hand the accumulator back to the MMA warp
+    tc_fence_before();
+    __syncwarp();
+    if (lane == 0) mbar_arrive(smem_u32(&s.tempty[b]));
+    ++it;
+
+    if (MODE == MODE_REDUCE) {
+      // arrival counter of this tile's 32-row quarter counts k-slices
+      __threadfence();
+      __syncwarp();
+      const uint32_t nk = static_cast<uint32_t>(w.k1 - w.k0);
+      const uint32_t target = static_cast<uint32_t>(p.R) * static_cast<uint32_t>(p.KT);
+      uint32_t* cnt = p.counters + (static_cast<size_t>(w.tile) * 4 + q);
+      uint32_t old = 0;
+      if (lane == 0) old = atomicAdd(cnt, nk);
+      old = __shfl_sync(0xFFFFFFFFu, old, 0);
+      if (old + nk == target) {
+        __threadfence();
+        const int col = n0 + lane * 8;
+        for (int i = 0; i < 32; ++i) {
+          const int grow = w.m0 + q * 32 + i;
+          if (grow >= w.row_end) break;
+          const int o = grow / p.rows_per_rank;
+          const int lr = grow - o * p.rows_per_rank;
+          if (col < p.N)
+            convert8<DT>(p.acc + static_cast<long long>(grow) * p.N + col,
+                         static_cast<uint16_t*>(p.out[o]) + static_cast<long long>(lr) * p.ldo + col);
+        }
+        if (lane == 0) atomicExch(cnt, 0u);
+      }
+    } else if (MODE == MODE_MOE_SCATTER) {
+      __threadfence();
+      uint32_t* cnt = p.counters + (static_cast<size_t>(tok) * p.Nt + w.nt);
+      bool last = false;
+      if (row_ok) {
+        const uint32_t old = atomicAdd(cnt, 1u);
+        last = (old + 1u == static_cast<uint32_t>(p.R * p.topk));
+      }
+      uint32_t lmask = __ballot_sync(0xFFFFFFFFu, last);
+      if (lmask) __threadfence();
+      while (lmask) {
+        const int src = __ffs(lmask) - 1;
+        lmask &= lmask - 1;
+        const int t = __shfl_sync(0xFFFFFFFFu, tok, src);
+        const int o = t / p.rows_per_rank;
+        const int lt = t - o * p.rows_per_rank;
+        const int col = n0 + lane * 8;
+        if (col < p.N)
+          convert8<DT>(p.acc + static_cast<long long>(t) * p.N + col,
+                       static_cast<uint16_t*>(p.out[o]) + static_cast<long long>(lt) * p.ldo + col);
+        if (lane == src) atomicExch(p.counters + (static_cast<size_t>(t) * p.Nt + w.nt), 0u);
+      }
+    }
+  }
+}
+
+// ---------------------------------------------------------------- kernel
+template <int MODE, int DT>
+struct KernelShape {
+  static constexpr int PRODUCER_WARPS = (MODE == MODE_MOE_GATHER) ? 4 : 1;
+  static constexpr int MMA_WARP = PRODUCER_WARPS;
+  static constexpr int EPI_WARP0 = PRODUCER_WARPS + 1;
+  static constexpr int THREADS = 32 * (PRODUCER_WARPS + 1 + EPI_WARPS);
+  static constexpr int FULL_COUNT = (MODE == MODE_MOE_GATHER) ? (BM + 1) : 1;
+};
+
+template <int MODE, int DT>
+__global__ void __launch_bounds__(KernelShape<MODE, DT>::THREADS, 1)
+fused_gemm_kernel(const __grid_constant__ KParams p) {
+  using KS = KernelShape<MODE, DT>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~static_cast<uintptr_t>(1023));
+  Smem s;
+  s.a = base;
+  s.b = base + STAGES * A_STAGE;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(base + STAGES * (A_STAGE + B_STAGE));
+  s.full = bars;
+  s.empty = bars + STAGES;
+  s.tfull = bars + 2 * STAGES;
+  s.tempty = bars + 2 * STAGES + 2;
+  s.drain = bars + 2 * STAGES + 4;
+  s.tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * STAGES + 5);
+
+  const int warp = threadIdx.x >> 5;
+  Ctl c;
+  c.hdr = p.hdr;
+  c.seq = p.seq;
+  c.flag_timeout = p.timeout_ns;
+  c.pipe_timeout = 2 * p.timeout_ns + 10000000ull;
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < STAGES; ++i) {
+      mbar_init(smem_u32(&s.full[i]), KS::FULL_COUNT);
+      mbar_init(smem_u32(&s.empty[i]), 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(smem_u32(&s.tfull[i]), 1);
+      mbar_init(smem_u32(&s.tempty[i]), EPI_WARPS);
+    }
+    mbar_init(smem_u32(s.drain), 1);
+    fence_mbar_init();
+  }
+  if (warp == KS::MMA_WARP) {
+    tmem_alloc(smem_u32(s.tmem_slot), TMEM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *s.tmem_slot;
+
+  int total_mt = 0;
+  if (MODE == MODE_MOE_GATHER || MODE == MODE_MOE_SCATTER) total_mt = __ldg(p.tile_off + p.E);
+
+  if (warp < KS::PRODUCER_WARPS) {
+    if (MODE == MODE_MOE_GATHER) {
+      producer_gather<KS::PRODUCER_WARPS * 32>(p, s, c, total_mt);
+    } else if ((threadIdx.x & 31) == 0) {
+      producer_tma<MODE>(p, s, c, total_mt);
+    }
+  } else if (warp == KS::MMA_WARP) {
+    if ((threadIdx.x & 31) == 0) mma_issuer<MODE, DT>(p, s, c, tmem_base, total_mt);
+    __syncwarp();
+  } else {
+    epilogue<MODE, DT>(p, s, c, tmem_base, total_mt, warp);
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == KS::MMA_WARP) {
+    tc_fence_after();
+    tmem_dealloc(tmem_base, TMEM_COLS);
+  }
+}
+
+}  // namespace flux

@@ -1,0 +1,389 @@
+// MoE entry points: routing (histogram, prefix sum, stable permutation),
+// AllGather + gather-by-expert + grouped GEMM (layer0), and grouped GEMM +
+// gate-weighted combine + ReduceScatter by token (layer1).
+#include <mutex>
+
+#include "flux_host.h"
+#include "flux_kernels.cuh"
+
+namespace flux {
+
+constexpr int ROUTE_THREADS = 1024;
+constexpr int ROUTE_CHUNK = 8192;  // expert ids staged in shared memory per pass
+
+// Exclusive block-wide prefix sum of one int per thread (blockDim.x == 1024).
+__device__ int block_exclusive_scan(int v, int* warp_sums, int* total) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  int x = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int y = __shfl_up_sync(0xFFFFFFFFu, x, o);
+    if (lane >= o) x += y;
+  }
+  if (lane == 31) warp_sums[warp] = x;
+  __syncthreads();
+  if (warp == 0) {
+    int w = warp_sums[lane];
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(0xFFFFFFFFu, w, o);
+      if (lane >= o) w += y;
+    }
+    warp_sums[lane] = w;  // inclusive over warps
+  }
+  __syncthreads();
+  const int before = (warp > 0 ? warp_sums[warp - 1] : 0) + x - v;
+  if (total) *total = warp_sums[31];
+  __syncthreads();
+  return before;
+}
+
+// One CTA: counts[e], offsets[e] (exclusive prefix sum), the stable
+// permutation slot_to_row / row_to_slot (rows grouped by expert, ascending slot
+// order inside an expert) and, if tile_off != nullptr, the first BM-row tile of
+// each expert in the grouped GEMM.  Ids outside [0, E) are not routed; their
+// slot_to_row entry is -1 and FLUX_ERR_INVALID_ARG is recorded in hdr.
+__global__ void __launch_bounds__(ROUTE_THREADS, 1)
+moe_route_kernel(const int32_t* __restrict__ ids, int n, int E, int32_t* counts,
+                 int32_t* offsets, int32_t* slot_to_row, int32_t* row_to_slot, int32_t* tile_off,
+                 uint32_t* hdr) {
+  __shared__ int hist[FLUX_MAX_EXPERTS];
+  __shared__ int base[FLUX_MAX_EXPERTS];
+  __shared__ int warp_sums[32];
+  __shared__ int totals[2];
+  __shared__ int stage[ROUTE_CHUNK];
+  const int tid = threadIdx.x;
+  for (int e = tid; e < E; e += ROUTE_THREADS) hist[e] = 0;
+  __syncthreads();
+  int bad = 0;
+  for (int s = tid; s < n; s += ROUTE_THREADS) {
+    const int e = ids[s];
+    if (e >= 0 && e < E) atomicAdd(&hist[e], 1);
+    else bad = 1;
+  }
+  bad = __syncthreads_or(bad);
+  // E <= 1024 = blockDim: one expert per thread
+  const int cnt = tid < E ? hist[tid] : 0;
+  const int off = block_exclusive_scan(cnt, warp_sums, &totals[0]);
+  const int ntile = (cnt + BM - 1) / BM;
+  const int toff = block_exclusive_scan(ntile, warp_sums, &totals[1]);
+  if (tid < E) {
+    counts[tid] = cnt;
+    offsets[tid] = off;
+    base[tid] = off;
+    if (tile_off) tile_off[tid] = toff;
+  }
+  if (tid == 0) {
+    offsets[E] = totals[0];
+    if (tile_off) tile_off[E] = totals[1];
+  }
+  __syncthreads();
+  // stable permutation: the first warp walks the slots in order, 32 at a time
+  const int lane = tid & 31;
+  for (int c0 = 0; c0 < n; c0 += ROUTE_CHUNK) {
+    const int cn = min(ROUTE_CHUNK, n - c0);
+    for (int i = tid; i < cn; i += ROUTE_THREADS) stage[i] = ids[c0 + i];
+    __syncthreads();
+    if (tid < 32) {
+      for (int i0 = 0; i0 < cn; i0 += 32) {
+        const int i = i0 + lane;
+        const int e = i < cn ? stage[i] : -1;
+        const bool valid = i < cn && e >= 0 && e < E;
+        // invalid lanes get distinct keys so they never group with a real expert
+        const int key = valid ? e : -1 - lane;
+        const unsigned mask = __match_any_sync(0xFFFFFFFFu, key);
+        const int rank = __popc(mask & ((1u << lane) - 1u));
+        if (valid) {
+          const int row = base[e] + rank;
+          slot_to_row[c0 + i] = row;
+          row_to_slot[row] = c0 + i;
+        } else if (i < cn) {
+          slot_to_row[c0 + i] = -1;
+        }
+        __syncwarp();
+        if (valid && lane == __ffs(mask) - 1) base[e] += __popc(mask);
+        __syncwarp();
+      }
+    }
+    __syncthreads();
+  }
+  if (bad && hdr != nullptr && tid == 0) atomicCAS(hdr + H_STATUS, 0u, ST_INVALID);
+}
+
+// tile_off[e] = sum_{e' < e} ceil(count_e' / BM) from a given offsets array.
+__global__ void tile_offsets_kernel(const int32_t* offsets, int E, int32_t* tile_off) {
+  if (threadIdx.x != 0 || blockIdx.x != 0) return;
+  int acc = 0;
+  for (int e = 0; e < E; ++e) {
+    tile_off[e] = acc;
+    const int c = offsets[e + 1] - offsets[e];
+    acc += (c > 0 ? (c + BM - 1) / BM : 0);
+  }
+  tile_off[E] = acc;
+}
+
+namespace {
+
+template <int MODE, int DT>
+flux_status_t launch(const KParams& p, int grid, cudaStream_t stream) {
+  using KS = KernelShape<MODE, DT>;
+  static std::once_flag once;
+  static cudaError_t attr_err = cudaSuccess;
+  std::call_once(once, [] {
+    attr_err = cudaFuncSetAttribute(fused_gemm_kernel<MODE, DT>,
+                                    cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+  });
+  if (attr_err != cudaSuccess) return cuda_fail(attr_err);
+  fused_gemm_kernel<MODE, DT><<<grid, KS::THREADS, SMEM_BYTES, stream>>>(p);
+  cudaError_t e = cudaGetLastError();
+  return e == cudaSuccess ? FLUX_OK : cuda_fail(e);
+}
+
+template <int MODE>
+flux_status_t launch_dt(flux_dtype_t dt, const KParams& p, int grid, cudaStream_t s) {
+  return dt == FLUX_BF16 ? launch<MODE, 1>(p, grid, s) : launch<MODE, 0>(p, grid, s);
+}
+
+bool moe_shape_ok(int R, int T, int H, int F, int E, int topk) {
+  return R >= 1 && R <= FLUX_MAX_RANKS && T >= 0 && H >= 0 && F >= 0 && E >= 1 &&
+         E <= FLUX_MAX_EXPERTS && topk >= 1 && topk <= E && T % R == 0 && F % R == 0 &&
+         static_cast<long long>(T) * topk < (1ll << 31);
+}
+
+size_t a256(size_t v) { return round_up(v, WS_ALIGN); }
+
+// workspace layout (offsets from the start)
+struct MoeWs {
+  size_t tile_off, counts, offsets, s2r, r2s, counters, acc, total;
+};
+
+MoeWs moe_layout(flux_op_t op, int R, int T, int H, int F, int E, int topk) {
+  (void)R;
+  (void)F;
+  MoeWs w{};
+  const size_t n = static_cast<size_t>(T) * topk;
+  size_t o = WS_HEADER;
+  w.tile_off = o;
+  o += a256((E + 1) * sizeof(int32_t));
+  if (op == FLUX_OP_MOE_RS) {
+    // routing recomputed here when the caller passes none
+    w.counts = o;
+    o += a256(E * sizeof(int32_t));
+    w.offsets = o;
+    o += a256((E + 1) * sizeof(int32_t));
+    w.s2r = o;
+    o += a256(n * sizeof(int32_t));
+    w.r2s = o;
+    o += a256(n * sizeof(int32_t));
+    const size_t Nt = (static_cast<size_t>(H) + BN - 1) / BN;
+    w.counters = o;
+    o += a256(static_cast<size_t>(T) * Nt * sizeof(uint32_t));
+    w.acc = o;
+    o += a256(static_cast<size_t>(T) * H * sizeof(float));
+  }
+  w.total = o;
+  return w;
+}
+
+flux_status_t launch_route(const int32_t* ids, int n, int E, int32_t* counts, int32_t* offsets,
+                           int32_t* s2r, int32_t* r2s, int32_t* tile_off, uint32_t* hdr,
+                           cudaStream_t s) {
+  moe_route_kernel<<<1, ROUTE_THREADS, 0, s>>>(ids, n, E, counts, offsets, s2r, r2s, tile_off, hdr);
+  cudaError_t e = cudaGetLastError();
+  return e == cudaSuccess ? FLUX_OK : cuda_fail(e);
+}
+
+}  // namespace
+}  // namespace flux
+
+using namespace flux;
+
+extern "C" size_t flux_moe_workspace_size(flux_op_t op, int R, int T, int H, int F, int E,
+                                          int topk) {
+  if (!moe_shape_ok(R, T, H, F, E, topk)) return 0;
+  if (op != FLUX_OP_MOE_AG && op != FLUX_OP_MOE_RS) return 0;
+  return moe_layout(op, R, T, H, F, E, topk).total;
+}
+
+extern "C" flux_status_t flux_moe_route(int T, int E, int topk, const int32_t* topk_ids,
+                                        int32_t* counts, int32_t* offsets, int32_t* slot_to_row,
+                                        int32_t* row_to_slot, void* workspace,
+                                        size_t workspace_bytes, void* stream) {
+  if (T < 0 || E < 1 || E > FLUX_MAX_EXPERTS || topk < 1 ||
+      static_cast<long long>(T) * topk >= (1ll << 31))
+    return FLUX_ERR_INVALID_ARG;
+  if (counts == nullptr || offsets == nullptr) return FLUX_ERR_INVALID_ARG;
+  const int n = T * topk;
+  if (n > 0 && (topk_ids == nullptr || slot_to_row == nullptr || row_to_slot == nullptr))
+    return FLUX_ERR_INVALID_ARG;
+  if (workspace != nullptr) {
+    flux_status_t st = check_workspace(workspace, workspace_bytes, WS_HEADER);
+    if (st != FLUX_OK) return st;
+  }
+  DeviceInfo dev;
+  flux_status_t st = current_device(&dev);
+  if (st != FLUX_OK) return st;
+  return launch_route(topk_ids, n, E, counts, offsets, slot_to_row, row_to_slot, nullptr,
+                      static_cast<uint32_t*>(workspace), static_cast<cudaStream_t>(stream));
+}
+
+extern "C" flux_status_t flux_moe_ag_grouped_gemm(
+    int R, int T, int H, int F, int E, int topk, flux_dtype_t dtype, const void* const* x_shards,
+    const void* const* w1_shards, const int32_t* topk_ids, void* const* h_out, int32_t* counts,
+    int32_t* offsets, int32_t* slot_to_row, int32_t* row_to_slot, const uint32_t* ready_flags,
+    void* workspace, size_t workspace_bytes, const flux_opts_t* opts, void* stream) {
+  if (!moe_shape_ok(R, T, H, F, E, topk) || (dtype != FLUX_F16 && dtype != FLUX_BF16))
+    return FLUX_ERR_INVALID_ARG;
+  if (x_shards == nullptr || w1_shards == nullptr || h_out == nullptr || counts == nullptr ||
+      offsets == nullptr || slot_to_row == nullptr || row_to_slot == nullptr ||
+      (T > 0 && topk_ids == nullptr))
+    return FLUX_ERR_INVALID_ARG;
+  const MoeWs L = moe_layout(FLUX_OP_MOE_AG, R, T, H, F, E, topk);
+  flux_status_t st = check_workspace(workspace, workspace_bytes, L.total);
+  if (st != FLUX_OK) return st;
+  const int Fr = F / R, rows = T / R, n = T * topk;
+  for (int r = 0; r < R; ++r) {
+    if (x_shards[r] == nullptr || w1_shards[r] == nullptr || h_out[r] == nullptr)
+      return FLUX_ERR_INVALID_ARG;
+    if (!aligned16(x_shards[r]) || !aligned16(w1_shards[r]) || !aligned16(h_out[r]))
+      return FLUX_ERR_UNSUPPORTED;
+  }
+  if (H % 8 || Fr % 8) return FLUX_ERR_UNSUPPORTED;
+  DeviceInfo dev;
+  if ((st = current_device(&dev)) != FLUX_OK) return st;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  int32_t* tile_off = reinterpret_cast<int32_t*>(ws + L.tile_off);
+  if ((st = launch_route(topk_ids, n, E, counts, offsets, slot_to_row, row_to_slot, tile_off,
+                         static_cast<uint32_t*>(workspace), s)) != FLUX_OK)
+    return st;
+  if (n == 0 || Fr == 0) return FLUX_OK;
+  if (H == 0) {
+    for (int r = 0; r < R; ++r) {
+      cudaError_t e = cudaMemsetAsync(h_out[r], 0, static_cast<size_t>(n) * Fr * 2, s);
+      if (e != cudaSuccess) return cuda_fail(e);
+    }
+    return FLUX_OK;
+  }
+  KParams p{};
+  for (int r = 0; r < R; ++r) {
+    if ((st = encode_3d(&p.tmB[r], dtype, w1_shards[r], Fr, H, E, B_BOX_N, BK)) != FLUX_OK) return st;
+    p.out[r] = h_out[r];
+    p.xsrc[r] = x_shards[r];
+  }
+  p.R = R;
+  p.M = n;
+  p.N = Fr;
+  p.K = H;
+  p.Nt = (Fr + BN - 1) / BN;
+  p.KT = (H + BK - 1) / BK;
+  p.ldo = Fr;
+  p.rows_per_rank = rows;
+  p.flags = ready_flags;
+  p.offsets = offsets;
+  p.row_to_slot = row_to_slot;
+  p.tile_off = tile_off;
+  p.E = E;
+  p.topk = topk;
+  p.T = T;
+  p.H = H;
+  p.timeout_ns = (opts && opts->timeout_ns) ? opts->timeout_ns : DEFAULT_TIMEOUT_NS;
+  p.epoch = (opts && opts->epoch) ? opts->epoch : 1u;
+  p.group_n = (opts && opts->group_n > 0) ? opts->group_n : 8;
+  p.seq = next_seq();
+  p.hdr = static_cast<uint32_t*>(workspace);
+  const long long max_units =
+      (static_cast<long long>((n + BM - 1) / BM) + E) * p.Nt * static_cast<long long>(R);
+  int grid = (opts && opts->num_ctas > 0) ? opts->num_ctas : dev.sm_count;
+  if (max_units < grid) grid = static_cast<int>(max_units);
+  return launch_dt<MODE_MOE_GATHER>(dtype, p, grid < 1 ? 1 : grid, s);
+}
+
+extern "C" flux_status_t flux_moe_grouped_gemm_rs(
+    int R, int T, int H, int F, int E, int topk, flux_dtype_t dtype, const void* const* h_shards,
+    const void* const* w2_shards, const int32_t* topk_ids, const float* topk_weights,
+    const int32_t* offsets, const int32_t* slot_to_row, const int32_t* row_to_slot,
+    void* const* out, void* workspace, size_t workspace_bytes, const flux_opts_t* opts,
+    void* stream) {
+  if (!moe_shape_ok(R, T, H, F, E, topk) || (dtype != FLUX_F16 && dtype != FLUX_BF16))
+    return FLUX_ERR_INVALID_ARG;
+  const bool given = offsets != nullptr;
+  if (given != (slot_to_row != nullptr) || given != (row_to_slot != nullptr))
+    return FLUX_ERR_INVALID_ARG;
+  if (h_shards == nullptr || w2_shards == nullptr || out == nullptr ||
+      (T > 0 && (topk_ids == nullptr || topk_weights == nullptr)))
+    return FLUX_ERR_INVALID_ARG;
+  const MoeWs L = moe_layout(FLUX_OP_MOE_RS, R, T, H, F, E, topk);
+  flux_status_t st = check_workspace(workspace, workspace_bytes, L.total);
+  if (st != FLUX_OK) return st;
+  const int Fr = F / R, rows = T / R, n = T * topk;
+  for (int r = 0; r < R; ++r) {
+    if (h_shards[r] == nullptr || w2_shards[r] == nullptr || out[r] == nullptr)
+      return FLUX_ERR_INVALID_ARG;
+    if (!aligned16(h_shards[r]) || !aligned16(w2_shards[r]) || !aligned16(out[r]))
+      return FLUX_ERR_UNSUPPORTED;
+  }
+  if (H % 8 || Fr % 8) return FLUX_ERR_UNSUPPORTED;
+  DeviceInfo dev;
+  if ((st = current_device(&dev)) != FLUX_OK) return st;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (T == 0 || H == 0) return FLUX_OK;
+  if (Fr == 0) {
+    for (int r = 0; r < R; ++r) {
+      cudaError_t e = cudaMemsetAsync(out[r], 0, static_cast<size_t>(rows) * H * 2, s);
+      if (e != cudaSuccess) return cuda_fail(e);
+    }
+    return FLUX_OK;
+  }
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  int32_t* tile_off = reinterpret_cast<int32_t*>(ws + L.tile_off);
+  if (!given) {
+    offsets = reinterpret_cast<int32_t*>(ws + L.offsets);
+    row_to_slot = reinterpret_cast<int32_t*>(ws + L.r2s);
+    if ((st = launch_route(topk_ids, n, E, reinterpret_cast<int32_t*>(ws + L.counts),
+                           const_cast<int32_t*>(offsets), reinterpret_cast<int32_t*>(ws + L.s2r),
+                           const_cast<int32_t*>(row_to_slot), tile_off,
+                           static_cast<uint32_t*>(workspace), s)) != FLUX_OK)
+      return st;
+  } else {
+    tile_offsets_kernel<<<1, 32, 0, s>>>(offsets, E, tile_off);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return cuda_fail(e);
+  }
+  KParams p{};
+  for (int r = 0; r < R; ++r) {
+    if ((st = encode_2d(&p.tmA[r], dtype, h_shards[r], Fr, n, static_cast<uint64_t>(Fr) * 2, BK,
+                        BM)) != FLUX_OK)
+      return st;
+    if ((st = encode_3d(&p.tmB[r], dtype, w2_shards[r], H, Fr, E, B_BOX_N, BK)) != FLUX_OK) return st;
+    p.out[r] = out[r];
+  }
+  p.R = R;
+  p.M = n;
+  p.N = H;
+  p.K = Fr;
+  p.Nt = (H + BN - 1) / BN;
+  p.KT = (Fr + BK - 1) / BK;
+  p.ldo = H;
+  p.rows_per_rank = rows;
+  p.offsets = offsets;
+  p.row_to_slot = row_to_slot;
+  p.tile_off = tile_off;
+  p.topk_w = topk_weights;
+  p.E = E;
+  p.topk = topk;
+  p.T = T;
+  p.H = H;
+  p.counters = reinterpret_cast<uint32_t*>(ws + L.counters);
+  p.acc = reinterpret_cast<float*>(ws + L.acc);
+  p.timeout_ns = (opts && opts->timeout_ns) ? opts->timeout_ns : DEFAULT_TIMEOUT_NS;
+  p.epoch = (opts && opts->epoch) ? opts->epoch : 1u;
+  p.group_n = (opts && opts->group_n > 0) ? opts->group_n : 8;
+  p.seq = next_seq();
+  p.hdr = static_cast<uint32_t*>(workspace);
+  const long long max_units =
+      (static_cast<long long>((n + BM - 1) / BM) + E) * p.Nt * static_cast<long long>(R);
+  int grid = (opts && opts->num_ctas > 0) ? opts->num_ctas : dev.sm_count;
+  if (max_units < grid) grid = static_cast<int>(max_units);
+  return launch_dt<MODE_MOE_SCATTER>(dtype, p, grid < 1 ? 1 : grid, s);
+}

@@ -8,3 +8,9 @@ if ROOT not in sys.path:
 
 def pytest_configure(config):
     config.addinivalue_line("markers", "gpu: needs a CUDA GPU (sm_103a) and the built library")
+
+
+def ensure_built():
+    """Build the C-ABI library in place if needed (nvcc is required)."""
+    import __graft_entry__
+    __graft_entry__._build_module().build()

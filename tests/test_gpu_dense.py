@@ -1,0 +1,213 @@
+"""GPU parity of the dense ops (plain GEMM, AllGather+GEMM, GEMM+ReduceScatter)
+against the float64 CPU oracle, through the C ABI."""
+import numpy as np
+import pytest
+
+import oracle
+from tests.parity import check_close
+from workloads import configs, gen
+from workloads.torch_io import from_device, to_device, torch_dtype
+
+pytestmark = pytest.mark.gpu
+
+torch = pytest.importorskip("torch")
+if not torch.cuda.is_available():  # pragma: no cover - CPU-only machines skip the module
+    pytest.skip("needs a CUDA GPU", allow_module_level=True)
+
+import reducescatter_tcgen05_tmem_gb300 as fx  # noqa: E402
+
+DT = {"f16": fx.FLUX_F16, "bf16": fx.FLUX_BF16}
+
+
+def _ws(nbytes):
+    ws = torch.zeros(max(nbytes, 256) // 4 + 64, dtype=torch.int32, device="cuda")
+    # 256-byte aligned view
+    off = (-ws.data_ptr()) % 256 // 4
+    return ws[off:off + max(nbytes, 256) // 4]
+
+
+def _out(rows, cols, dtype):
+    return torch.full((rows, cols), float("nan"), dtype=torch_dtype(dtype), device="cuda")
+
+
+def _ok(ws):
+    st, rep = fx.flux_get_status(ws)
+    assert st == fx.FLUX_OK, rep
+
+
+# ---------------------------------------------------------------- plain GEMM
+@pytest.mark.parametrize("dtype", ["f16", "bf16"])
+@pytest.mark.parametrize("M,N,K", [(128, 256, 64), (300, 264, 200), (1, 8, 8), (257, 520, 1032),
+                                   (512, 768, 4096)])
+def test_gemm_matches_oracle(dtype, M, N, K):
+    A = gen.normal16((7, 1), (M, K), 1.0, dtype)
+    B = gen.normal16((7, 2), (K, N), 0.05, dtype)
+    C = _out(M, N, dtype)
+    ws = _ws(fx.flux_workspace_size(fx.FLUX_OP_GEMM, 1, M, N, K))
+    fx.flux_gemm(M, N, K, DT[dtype], to_device(A, dtype), to_device(B, dtype), C, ws)
+    _ok(ws)
+    ref = oracle.gemm(oracle.widen(A, dtype), oracle.widen(B, dtype))
+    check_close(oracle.widen(from_device(C), dtype), ref, f"gemm {M}x{N}x{K} {dtype}")
+
+
+@pytest.mark.parametrize("dtype", ["f16", "bf16"])
+def test_gemm_integer_inputs_are_bit_exact(dtype):
+    # |partial sums| <= 2*2*64 = 256: exact in fp32 and in both 16-bit formats
+    M, N, K = 200, 320, 64
+    A = gen.integers16((8, 1), (M, K), -2, 2, dtype)
+    B = gen.integers16((8, 2), (K, N), -2, 2, dtype)
+    C = _out(M, N, dtype)
+    ws = _ws(256)
+    fx.flux_gemm(M, N, K, DT[dtype], to_device(A, dtype), to_device(B, dtype), C, ws)
+    _ok(ws)
+    ref = oracle.gemm(oracle.widen(A, dtype), oracle.widen(B, dtype))
+    assert np.array_equal(oracle.widen(from_device(C), dtype), ref)
+
+
+def test_gemm_k_zero_writes_zeros():
+    C = _out(64, 64, "f16")
+    a = torch.zeros(64, 8, dtype=torch.float16, device="cuda")
+    fx.flux_gemm(64, 64, 0, fx.FLUX_F16, a, a, C, _ws(256))
+    torch.cuda.synchronize()
+    assert torch.count_nonzero(C).item() == 0
+
+
+# ---------------------------------------------------------------- AllGather + GEMM
+def _ag_case(c, ready=None, opts=None):
+    xs, ws_ = configs.ag_inputs(c)
+    d = c.dtype
+    X = [to_device(x, d) for x in xs]
+    W = [to_device(w, d) for w in ws_]
+    out = [_out(c.M, c.N // c.R, d) for _ in range(c.R)]
+    ws = _ws(fx.flux_workspace_size(fx.FLUX_OP_AG_GEMM, c.R, c.M, c.N, c.K))
+    fx.flux_ag_gemm(c.R, c.M, c.N, c.K, DT[d], X, W, out, ready, ws, opts=opts)
+    return xs, ws_, out, ws
+
+
+@pytest.mark.parametrize("R,M,N,K,dtype", [
+    (1, 256, 512, 256, "f16"),
+    (2, 256, 1024, 512, "f16"),
+    (4, 512, 1024, 320, "bf16"),
+    (8, 320, 576, 200, "f16"),     # 40 rows per shard (8-row boxes), ragged N and K tails
+    (8, 1024, 2048, 128, "bf16"),  # shard = 128 rows: rank-rotated m order
+])
+def test_ag_gemm_matches_oracle(R, M, N, K, dtype):
+    c = configs.small(configs.CONFIGS["ag_mlp0"], R=R, M=M, N=N, K=K, dtype=dtype, seed=20 + R)
+    xs, w_s, out, ws = _ag_case(c)
+    _ok(ws)
+    ref = oracle.ag_gemm(xs, w_s, dtype)
+    for r in range(R):
+        check_close(oracle.widen(from_device(out[r]), dtype), ref[r], f"ag rank {r}")
+
+
+def test_ag_gemm_flags_published_with_epoch():
+    c = configs.small(configs.CONFIGS["ag_mlp0"], R=4, M=512, N=1024, K=256, seed=31)
+    flags = torch.full((4,), 7, dtype=torch.int32, device="cuda")
+    xs, w_s, out, ws = _ag_case(c, ready=flags, opts={"epoch": 7})
+    _ok(ws)
+    ref = oracle.ag_gemm(xs, w_s, c.dtype)
+    for r in range(4):
+        check_close(oracle.widen(from_device(out[r]), c.dtype), ref[r], f"ag flags rank {r}")
+
+
+def test_ag_gemm_withheld_flag_times_out_and_gpu_stays_usable():
+    # shard 2 never publishes: the pull of its rows must give up after the timeout
+    c = configs.small(configs.CONFIGS["ag_mlp0"], R=4, M=512, N=512, K=128, seed=32)
+    flags = torch.tensor([1, 1, 0, 1], dtype=torch.int32, device="cuda")
+    _, _, _, ws = _ag_case(c, ready=flags, opts={"timeout_ns": 20_000_000})
+    st, rep = fx.flux_get_status(ws)
+    assert st == fx.FLUX_ERR_TIMEOUT
+    assert rep["where"] == "ready flag" and rep["arg0"] == 2 and rep["arg1"] == 0
+    # the same workspace (reset by flux_get_status) and GPU work normally afterwards
+    flags.fill_(1)
+    xs, w_s, out, ws = _ag_case(c, ready=flags)
+    _ok(ws)
+    ref = oracle.ag_gemm(xs, w_s, c.dtype)
+    check_close(oracle.widen(from_device(out[2]), c.dtype), ref[2], "after timeout")
+
+
+# ---------------------------------------------------------------- GEMM + ReduceScatter
+def _rs_case(c, opts=None, ws=None, calls=1):
+    As, Bs = configs.rs_inputs(c)
+    d = c.dtype
+    A = [to_device(a, d) for a in As]
+    B = [to_device(b, d) for b in Bs]
+    out = [_out(c.M // c.R, c.N, d) for _ in range(c.R)]
+    if ws is None:
+        ws = _ws(fx.flux_workspace_size(fx.FLUX_OP_GEMM_RS, c.R, c.M, c.N, c.K))
+    for _ in range(calls):
+        fx.flux_gemm_rs(c.R, c.M, c.N, c.K, DT[d], A, B, out, ws, opts=opts)
+    return As, Bs, out, ws
+
+
+def test_rs_config_r2_small_matches_oracle():
+    c = configs.CONFIGS["rs_r2_small"]
+    As, Bs, out, ws = _rs_case(c)
+    _ok(ws)
+    ref = oracle.gemm_rs(As, Bs, c.dtype)
+    for o in range(c.R):
+        check_close(oracle.widen(from_device(out[o]), c.dtype), ref[o], f"rs owner {o}")
+
+
+@pytest.mark.parametrize("R,M,N,K,dtype,num_ctas", [
+    (2, 256, 512, 1024, "f16", 0),
+    (4, 512, 1024, 1024, "bf16", 8),    # many units per CTA: strided whole-tile schedule
+    (8, 192, 264, 576, "f16", 0),       # ragged M/N tails, 24-row owner chunks
+    (8, 128, 2048, 4096, "bf16", 0),    # decode-like: split along K over the grid
+    (8, 128, 2048, 4096, "bf16", 5),    # odd grid: k ranges straddle tiles
+    (1, 300, 136, 200, "f16", 0),
+])
+def test_gemm_rs_matches_oracle(R, M, N, K, dtype, num_ctas):
+    c = configs.small(configs.CONFIGS["rs_mlp1"], R=R, M=M, N=N, K=K, dtype=dtype, seed=40 + R)
+    opts = {"num_ctas": num_ctas} if num_ctas else None
+    As, Bs, out, ws = _rs_case(c, opts=opts)
+    _ok(ws)
+    ref = oracle.gemm_rs(As, Bs, dtype)
+    for o in range(R):
+        check_close(oracle.widen(from_device(out[o]), dtype), ref[o], f"rs owner {o}")
+
+
+def test_gemm_rs_integer_inputs_bit_exact_and_workspace_returns_to_zero():
+    c = configs.small(configs.CONFIGS["rs_mlp1"], R=4, M=256, N=512, K=128, dist="int", seed=45)
+    As, Bs, out, ws = _rs_case(c, calls=3)  # repeated calls reuse the zeroed accumulators
+    _ok(ws)
+    ref = oracle.gemm_rs(As, Bs, c.dtype)
+    for o in range(c.R):
+        assert np.array_equal(oracle.widen(from_device(out[o]), c.dtype), ref[o])
+    assert torch.count_nonzero(ws).item() == 0
+
+
+def test_gemm_rs_owner_chunk_layout_is_exact():
+    # one-hot rows: each owner's chunk must hold exactly its rows (bit-exact layout)
+    R, M, N, K = 4, 256, 256, 256
+    Kr = K // R
+    As = [np.zeros((M, Kr), np.float16) for _ in range(R)]
+    Bs = [np.zeros((Kr, N), np.float16) for _ in range(R)]
+    for r in range(R):
+        for i in range(M):
+            As[r][i, i % Kr] = 1.0
+        for k in range(Kr):
+            Bs[r][k, (k * 3 + r) % N] = float(r + 1)
+    A = [to_device(a, "f16") for a in As]
+    B = [to_device(b, "f16") for b in Bs]
+    out = [_out(M // R, N, "f16") for _ in range(R)]
+    ws = _ws(fx.flux_workspace_size(fx.FLUX_OP_GEMM_RS, R, M, N, K))
+    fx.flux_gemm_rs(R, M, N, K, fx.FLUX_F16, A, B, out, ws)
+    _ok(ws)
+    ref = oracle.gemm_rs(As, Bs, "f16")
+    for o in range(R):
+        assert np.array_equal(from_device(out[o]).astype(np.float64), ref[o])
+
+
+# ---------------------------------------------------------------- argument checks (GPU present)
+def test_argument_errors_launch_nothing():
+    a = torch.zeros(64, 64, dtype=torch.float16, device="cuda")
+    ws = _ws(256)
+    with pytest.raises(fx.FluxError, match="INVALID_ARG"):
+        fx.flux_ag_gemm(3, 64, 64, 64, fx.FLUX_F16, [a] * 3, [a] * 3, [a] * 3, None, ws)
+    with pytest.raises(fx.FluxError, match="UNSUPPORTED"):
+        fx.flux_gemm(64, 64, 60, fx.FLUX_F16, a, a, a, ws)
+    with pytest.raises(fx.FluxError, match="WORKSPACE"):
+        fx.flux_gemm_rs(2, 64, 64, 64, fx.FLUX_F16, [a] * 2, [a] * 2, [a] * 2, ws)
+    with pytest.raises(fx.FluxError, match="UNSUPPORTED"):
+        fx.flux_gemm(64, 64, 64, fx.FLUX_F16, a.data_ptr() + 2, a, a, ws)

@@ -1,0 +1,158 @@
+"""GPU parity of the MoE path (routing, layer0 AllGather + grouped GEMM,
+layer1 grouped GEMM + top-k combine + ReduceScatter) against the CPU oracle,
+through the C ABI."""
+import numpy as np
+import pytest
+
+import oracle
+from tests.parity import check_close
+from workloads import configs, gen
+from workloads.torch_io import from_device, to_device, torch_dtype
+
+pytestmark = pytest.mark.gpu
+
+torch = pytest.importorskip("torch")
+if not torch.cuda.is_available():  # pragma: no cover
+    pytest.skip("needs a CUDA GPU", allow_module_level=True)
+
+import reducescatter_tcgen05_tmem_gb300 as fx  # noqa: E402
+
+DT = {"f16": fx.FLUX_F16, "bf16": fx.FLUX_BF16}
+
+
+def _ws(nbytes):
+    n = max(nbytes, 256) // 4
+    ws = torch.zeros(n + 64, dtype=torch.int32, device="cuda")
+    off = (-ws.data_ptr()) % 256 // 4
+    return ws[off:off + n]
+
+
+def _i32(n):
+    return torch.full((max(n, 1),), -7, dtype=torch.int32, device="cuda")
+
+
+def _route_gpu(ids, E, ws=None):
+    T, topk = ids.shape
+    n = T * topk
+    d_ids = torch.from_numpy(np.ascontiguousarray(ids)).cuda()
+    counts, offsets, s2r, r2s = _i32(E), _i32(E + 1), _i32(n), _i32(n)
+    fx.flux_moe_route(T, E, topk, d_ids, counts, offsets, s2r, r2s, ws)
+    torch.cuda.synchronize()
+    return (counts[:E].cpu().numpy(), offsets[:E + 1].cpu().numpy(), s2r[:n].cpu().numpy(),
+            r2s[:n].cpu().numpy())
+
+
+# ---------------------------------------------------------------- routing
+@pytest.mark.parametrize("T,E,topk,empty", [(4096, 8, 2, ()), (33, 5, 3, ()), (1000, 64, 2, (3, 9)),
+                                            (257, 1, 1, ()), (8192, 256, 4, ()), (0, 4, 2, ())])
+def test_routing_bit_exact(T, E, topk, empty):
+    ids, _ = gen.routing((77, T, E), T, E, topk, force_empty=empty) if T else \
+        (np.zeros((0, topk), np.int32), None)
+    got = _route_gpu(ids, E)
+    want = oracle.moe_route(ids, E)
+    for g, w, name in zip(got, want, ("counts", "offsets", "slot_to_row", "row_to_slot")):
+        assert np.array_equal(g, w), name
+
+
+def test_routing_records_invalid_expert_id():
+    ids = np.array([[0, 1], [5, 2], [1, 0]], dtype=np.int32)  # 5 is outside [0, 4)
+    ws = _ws(256)
+    counts, offsets, s2r, r2s = _route_gpu(ids, 4, ws)
+    st, _ = fx.flux_get_status(ws)
+    assert st == fx.FLUX_ERR_INVALID_ARG
+    assert counts.tolist() == [2, 2, 1, 0] and offsets[-1] == 5 and s2r[2] == -1
+
+
+# ---------------------------------------------------------------- layer0
+def _layer0(c, d=None, flags=None, opts=None):
+    if d is None:
+        d = configs.moe_inputs(c)
+    dt = c.dtype
+    n = c.T * c.topk
+    Fr = c.F // c.R
+    X = [to_device(x, dt) for x in d["x_shards"]]
+    W1 = [to_device(w, dt) for w in d["w1_shards"]]
+    ids = torch.from_numpy(d["topk_ids"]).cuda()
+    H = [torch.full((n, Fr), float("nan"), dtype=torch_dtype(dt), device="cuda") for _ in range(c.R)]
+    counts, offsets, s2r, r2s = _i32(c.E), _i32(c.E + 1), _i32(n), _i32(n)
+    ws = _ws(fx.flux_moe_workspace_size(fx.FLUX_OP_MOE_AG, c.R, c.T, c.H, c.F, c.E, c.topk))
+    fx.flux_moe_ag_grouped_gemm(c.R, c.T, c.H, c.F, c.E, c.topk, DT[dt], X, W1, ids, H, counts,
+                                offsets, s2r, r2s, flags, ws, opts=opts)
+    st, rep = fx.flux_get_status(ws)
+    assert st == fx.FLUX_OK, rep
+    routing = (counts[:c.E], offsets[:c.E + 1], s2r[:n], r2s[:n])
+    return d, H, routing
+
+
+@pytest.mark.parametrize("R,T,H,F,E,topk,dtype,empty", [
+    (2, 256, 256, 640, 4, 2, "bf16", ()),      # F/R = 320: ragged n tail
+    (4, 512, 192, 1024, 8, 2, "f16", (5,)),    # H = 192: ragged k tail; an empty expert
+    (8, 1024, 512, 2048, 8, 2, "bf16", ()),    # the MoE workload's structure, reduced
+    (1, 64, 64, 256, 3, 1, "f16", ()),
+])
+def test_layer0_matches_oracle(R, T, H, F, E, topk, dtype, empty):
+    c = configs.small(configs.CONFIGS["moe"], R=R, T=T, H=H, F=F, E=E, topk=topk, dtype=dtype,
+                      seed=60 + R, force_empty=empty)
+    d, Hd, routing = _layer0(c)
+    ref, want_routing = oracle.moe_layer0(d["x_shards"], d["w1_shards"], d["topk_ids"], E, dtype)
+    for g, w in zip(routing, want_routing):
+        assert np.array_equal(g.cpu().numpy(), w)
+    for r in range(R):
+        check_close(oracle.widen(from_device(Hd[r]), dtype), ref[r], f"layer0 rank {r}")
+
+
+# ---------------------------------------------------------------- layer1
+def _layer1(c, d, h_dev=None, routing=None):
+    dt = c.dtype
+    n = c.T * c.topk
+    Hs = h_dev if h_dev is not None else [to_device(h, dt) for h in d["h_shards"]]
+    W2 = [to_device(w, dt) for w in d["w2_shards"]]
+    ids = torch.from_numpy(d["topk_ids"]).cuda()
+    gw = torch.from_numpy(d["topk_weights"]).cuda()
+    out = [torch.full((c.T // c.R, c.H), float("nan"), dtype=torch_dtype(dt), device="cuda")
+           for _ in range(c.R)]
+    ws = _ws(fx.flux_moe_workspace_size(fx.FLUX_OP_MOE_RS, c.R, c.T, c.H, c.F, c.E, c.topk))
+    off = s2r = r2s = None
+    if routing is not None:
+        _, off, s2r, r2s = routing
+    fx.flux_moe_grouped_gemm_rs(c.R, c.T, c.H, c.F, c.E, c.topk, DT[dt], Hs, W2, ids, gw, off, s2r,
+                                r2s, out, ws)
+    st, rep = fx.flux_get_status(ws)
+    assert st == fx.FLUX_OK, rep
+    return out, ws
+
+
+@pytest.mark.parametrize("R,T,H,F,E,topk,dtype,given", [
+    (2, 256, 320, 512, 4, 2, "bf16", False),   # H = 320: ragged n tail
+    (4, 512, 256, 768, 8, 2, "f16", True),     # F/R = 192: ragged k tail
+    (8, 1024, 512, 2048, 8, 2, "bf16", True),
+    (1, 96, 256, 128, 2, 2, "f16", False),
+])
+def test_layer1_matches_oracle(R, T, H, F, E, topk, dtype, given):
+    c = configs.small(configs.CONFIGS["moe"], R=R, T=T, H=H, F=F, E=E, topk=topk, dtype=dtype,
+                      seed=80 + R)
+    d = configs.moe_inputs(c)
+    routing = None
+    if given:
+        ids = d["topk_ids"]
+        routing = tuple(torch.from_numpy(a).cuda() for a in oracle.moe_route(ids, E))
+    out, ws = _layer1(c, d, routing=routing)
+    ref = oracle.moe_layer1(d["h_shards"], d["w2_shards"], d["topk_ids"], d["topk_weights"], E, dtype)
+    for o in range(R):
+        check_close(oracle.widen(from_device(out[o]), dtype), ref[o], f"layer1 owner {o}")
+    # the arrival counters and fp32 accumulators (the tail of the workspace) are left at zero
+    nt = (H + 255) // 256
+    tail = (-(-T * nt * 4 // 256) * 256 + -(-T * H * 4 // 256) * 256) // 4
+    assert torch.count_nonzero(ws[-tail:]).item() == 0
+
+
+def test_layer0_then_layer1_chained():
+    c = configs.small(configs.CONFIGS["moe"], R=4, T=512, H=256, F=1024, E=8, topk=2, seed=91)
+    d, Hd, routing = _layer0(c)
+    out, _ = _layer1(c, d, h_dev=Hd, routing=routing)
+    h_ref, _ = oracle.moe_layer0(d["x_shards"], d["w1_shards"], d["topk_ids"], c.E, c.dtype)
+    h_rounded = [oracle.round_to(h, c.dtype) for h in h_ref]  # layer0 stores 16-bit H
+    ref = oracle.moe_layer1(h_rounded, d["w2_shards"], d["topk_ids"], d["topk_weights"], c.E,
+                            c.dtype, h_dtype="f64")
+    for o in range(c.R):
+        check_close(oracle.widen(from_device(out[o]), c.dtype), ref[o], f"chain owner {o}")
