@@ -1,0 +1,526 @@
+"""Throughput of the fused GEMM + tensor-parallel collective hot path on GB300.
+
+One step = one pass of the whole hot path over one batch of synthetic input,
+every rank virtual (R = 8 buffer sets on this GPU):
+
+  dense TP-MLP   AllGather+GEMM  X[4096 x 12288] . W1[12288 x 49152]  (fp16)
+                 -> GEMM+ReduceScatter Output1[4096 x 49152] . W2[49152 x 12288]
+  decode         GEMM+ReduceScatter act[128 x 28672] . W2[28672 x 8192]  (bf16)
+  MoE layer      routing (T=4096, E=8, top-2, Zipf(1.2) bias) -> layer0 AllGather +
+                 gather-by-expert grouped GEMM [.. x 4096] . [4096 x 14336] -> layer1
+                 grouped GEMM [.. x 14336] . [14336 x 4096] + top-k combine +
+                 ReduceScatter (bf16)
+
+Prints ONE JSON line (rank 0).  ``--impl reference`` times the CPU oracle on
+this host's cores instead, on a bounded row sample of the same workload.
+Under torchrun (N > 1) every rank runs its own replica of the step on its own
+GPU (the path has no exchange between GPUs); the time is the max over ranks.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+from workloads import configs  # noqa: E402
+
+METRIC = "fused AG-GEMM/GEMM-RS TFLOP/s vs fp16 peak; overhead vs plain GEMM (us)"
+UNIT = "TFLOP/s"
+WORKLOAD = ("hot-path step, R=8 virtual ranks: dense TP-MLP AG-GEMM 4096x12288x49152 -> "
+            "GEMM-RS 4096x49152x12288 (fp16); decode GEMM-RS 128x28672x8192 (bf16); "
+            "MoE layer T=4096 H=4096 F=14336 E=8 top-2 routing+layer0+layer1 (bf16)")
+DTYPE = "f16/bf16 operands, fp32 accumulate"
+KERNEL_SOURCES = ["flux_kernels.cuh", "flux_ptx.cuh", "flux_dense.cu", "flux_moe.cu"]
+
+
+def kernel_hash() -> str:
+    h = hashlib.sha256()
+    for f in KERNEL_SOURCES:
+        with open(os.path.join(ROOT, "reducescatter_tcgen05_tmem_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            p = json.load(f)
+        return {"hbm": p["hbm_gbs"], "tc": p["bf16_tflops"], "tc_sus": p["bf16_tflops_sustained"],
+                "src": "measured"}
+    except Exception:
+        return {"hbm": 6800.0, "tc": 1900.0, "tc_sus": 1700.0, "src": "fallback"}
+
+
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+# ---------------------------------------------------------------- clocks
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.idx = gpu_index
+        self.proc = None
+        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_rank{gpu_index}.csv")
+
+    def start(self):
+        try:
+            os.makedirs(os.path.dirname(self.path), exist_ok=True)
+            self.fh = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.idx), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=self.fh, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.fh.close()
+        sm, smax, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        with open(self.path) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) < 9:
+                    continue
+                try:
+                    sm.append(float(parts[1]))
+                    smax = float(parts[2])
+                except ValueError:
+                    continue
+                for n, v in zip(names, parts[5:9]):
+                    if v.lower() == "active":
+                        reasons.add(n)
+        under = [s for s in sm if smax and s > 0.5 * smax] or sm
+        return {"sm_mhz": statistics.median(under) if under else None, "sm_max_mhz": smax,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ---------------------------------------------------------------- our arm
+class Step:
+    """Device buffers and the launch sequence of one hot-path step."""
+
+    def __init__(self, torch, fx, dev, small=False):
+        from workloads.torch_io import to_device, torch_dtype
+        self.torch, self.fx, self.dev = torch, fx, dev
+        C = configs.CONFIGS
+        ag, rs, dec, moe = C["ag_mlp0"], C["rs_mlp1"], C["rs_decode"], C["moe"]
+        if small:  # same structure, reduced sizes (profiling captures)
+            ag = configs.small(ag, M=1024, N=8192, K=4096)
+            rs = configs.small(rs, M=1024, N=4096, K=8192)
+            dec = configs.small(dec, N=4096, K=14336)
+            moe = configs.small(moe, T=1024, H=2048, F=4096)
+        self.ag, self.rs, self.dec, self.moe = ag, rs, dec, moe
+        t0 = time.time()
+        xs, w1 = configs.ag_inputs(ag)
+        # the GEMM-RS input of the chained step is the AG-GEMM output; W2 comes from the rs workload
+        _, w2 = configs.rs_inputs(configs.small(rs, M=rs.R * 8))
+        da, dw = configs.rs_inputs(dec)
+        md = configs.moe_inputs(moe, with_h=False)
+        self.gen_s = time.time() - t0
+        T = lambda a, d: to_device(a, d, dev)  # noqa: E731
+        self.X = [T(x, "f16") for x in xs]
+        self.W1 = [T(w, "f16") for w in w1]
+        self.W2 = [T(w, "f16") for w in w2]
+        self.out1 = [torch.empty(ag.M, ag.N // ag.R, dtype=torch.float16, device=dev) for _ in range(ag.R)]
+        self.out2 = [torch.empty(rs.M // rs.R, rs.N, dtype=torch.float16, device=dev) for _ in range(rs.R)]
+        self.dA = [T(a, "bf16") for a in da]
+        self.dW = [T(w, "bf16") for w in dw]
+        self.dout = [torch.empty(dec.M // dec.R, dec.N, dtype=torch.bfloat16, device=dev) for _ in range(dec.R)]
+        n = moe.T * moe.topk
+        self.mX = [T(x, "bf16") for x in md["x_shards"]]
+        self.mW1 = [T(w, "bf16") for w in md["w1_shards"]]
+        self.mW2 = [T(w, "bf16") for w in md["w2_shards"]]
+        self.ids = torch.from_numpy(md["topk_ids"]).to(dev)
+        self.gw = torch.from_numpy(md["topk_weights"]).to(dev)
+        self.mH = [torch.empty(n, moe.F // moe.R, dtype=torch.bfloat16, device=dev) for _ in range(moe.R)]
+        self.mY = [torch.empty(moe.T // moe.R, moe.H, dtype=torch.bfloat16, device=dev) for _ in range(moe.R)]
+        self.counts = torch.empty(moe.E, dtype=torch.int32, device=dev)
+        self.offsets = torch.empty(moe.E + 1, dtype=torch.int32, device=dev)
+        self.s2r = torch.empty(n, dtype=torch.int32, device=dev)
+        self.r2s = torch.empty(n, dtype=torch.int32, device=dev)
+
+        def ws(nbytes):
+            return torch.zeros(max(nbytes, 256) // 4, dtype=torch.int32, device=dev)
+        self.ws_ag = ws(fx.flux_workspace_size(fx.FLUX_OP_AG_GEMM, ag.R, ag.M, ag.N, ag.K))
+        self.ws_rs = ws(fx.flux_workspace_size(fx.FLUX_OP_GEMM_RS, rs.R, rs.M, rs.N, rs.K))
+        self.ws_dec = ws(fx.flux_workspace_size(fx.FLUX_OP_GEMM_RS, dec.R, dec.M, dec.N, dec.K))
+        self.ws_m0 = ws(fx.flux_moe_workspace_size(fx.FLUX_OP_MOE_AG, moe.R, moe.T, moe.H, moe.F, moe.E, moe.topk))
+        self.ws_m1 = ws(fx.flux_moe_workspace_size(fx.FLUX_OP_MOE_RS, moe.R, moe.T, moe.H, moe.F, moe.E, moe.topk))
+        self.flags = torch.ones(ag.R, dtype=torch.int32, device=dev)
+        self.mflags = torch.ones(moe.R, dtype=torch.int32, device=dev)
+        self.flops = {
+            "ag_gemm": ag.flops, "gemm_rs": rs.flops, "decode_rs": dec.flops,
+            "moe_layer0": moe.flops_per_layer, "moe_layer1": moe.flops_per_layer,
+        }
+        self.launches_per_step = 7  # ag, rs, decode rs, route + layer0, tile table + layer1
+        self.ops = ["ag_gemm", "gemm_rs", "decode_rs", "moe_layer0", "moe_layer1"]
+
+    def run_op(self, name):
+        fx, ag, rs, dec, moe = self.fx, self.ag, self.rs, self.dec, self.moe
+        if name == "ag_gemm":
+            fx.flux_ag_gemm(ag.R, ag.M, ag.N, ag.K, fx.FLUX_F16, self.X, self.W1, self.out1, self.flags,
+                            self.ws_ag)
+        elif name == "gemm_rs":
+            fx.flux_gemm_rs(rs.R, rs.M, rs.N, rs.K, fx.FLUX_F16, self.out1, self.W2, self.out2, self.ws_rs)
+        elif name == "decode_rs":
+            fx.flux_gemm_rs(dec.R, dec.M, dec.N, dec.K, fx.FLUX_BF16, self.dA, self.dW, self.dout, self.ws_dec)
+        elif name == "moe_layer0":
+            fx.flux_moe_ag_grouped_gemm(moe.R, moe.T, moe.H, moe.F, moe.E, moe.topk, fx.FLUX_BF16, self.mX,
+                                        self.mW1, self.ids, self.mH, self.counts, self.offsets, self.s2r,
+                                        self.r2s, self.mflags, self.ws_m0)
+        elif name == "moe_layer1":
+            fx.flux_moe_grouped_gemm_rs(moe.R, moe.T, moe.H, moe.F, moe.E, moe.topk, fx.FLUX_BF16, self.mH,
+                                        self.mW2, self.ids, self.gw, self.offsets, self.s2r, self.r2s,
+                                        self.mY, self.ws_m1)
+
+    def step(self, events=None):
+        for name in self.ops:
+            if events is not None:
+                events[name][0].record()
+            self.run_op(name)
+            if events is not None:
+                events[name][1].record()
+
+    def check_status(self):
+        for w in (self.ws_ag, self.ws_rs, self.ws_dec, self.ws_m0, self.ws_m1):
+            st, rep = self.fx.flux_get_status(w)
+            if st != self.fx.FLUX_OK:
+                raise RuntimeError(f"device status {st}: {rep}")
+
+    def total_flops(self):
+        return sum(self.flops[o] for o in self.ops)
+
+
+def time_plain(torch, fx, dev, M, N, K, dtype, iters=5):
+    """min(cuBLAS, own tcgen05 plain GEMM) time in ms for C[M x N] = A[M x K] B[K x N]."""
+    td = torch.float16 if dtype == "f16" else torch.bfloat16
+    A = torch.randn(M, K, device=dev, dtype=td)
+    B = torch.randn(K, N, device=dev, dtype=td) * 0.02
+    C = torch.empty(M, N, device=dev, dtype=td)
+    ws = torch.zeros(64, dtype=torch.int32, device=dev)
+    code = fx.FLUX_F16 if dtype == "f16" else fx.FLUX_BF16
+    res = {}
+    for name, fn in (("cublas", lambda: torch.matmul(A, B, out=C)),
+                     ("own", lambda: fx.flux_gemm(M, N, K, code, A, B, C, ws))):
+        for _ in range(2):
+            fn()
+        torch.cuda.synchronize()
+        ts = []
+        for _ in range(iters):
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            fn()
+            e1.record()
+            torch.cuda.synchronize()
+            ts.append(e0.elapsed_time(e1))
+        res[name] = min(ts)
+    del A, B, C
+    torch.cuda.empty_cache()
+    return res
+
+
+def run_ours(args):
+    import torch
+    ws_, rank, local = dist_env()
+    if ws_ > 1:
+        import torch.distributed as td
+        td.init_process_group("gloo")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    import __graft_entry__
+    __graft_entry__.build()
+    import reducescatter_tcgen05_tmem_gb300 as fx
+
+    st = Step(torch, fx, dev, small=args.small)
+    if args.ops:
+        st.ops = args.ops.split(",")
+    for _ in range(args.warmup):
+        st.step()
+    torch.cuda.synchronize()
+    st.check_status()
+
+    # ------------------------------------------------------------ device-timed region
+    events = {o: (torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+              for o in st.ops}
+    per_op = {o: 0.0 for o in st.ops}
+    clocks = ClockSampler(local)
+    clocks.start()
+    time.sleep(0.3)
+    if ws_ > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    t_start = torch.cuda.Event(enable_timing=True)
+    t_end = torch.cuda.Event(enable_timing=True)
+    t_start.record()
+    per_step_events = []
+    for _ in range(args.steps):
+        ev = {o: (torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+              for o in st.ops}
+        st.step(ev)
+        per_step_events.append(ev)
+    t_end.record()
+    torch.cuda.synchronize()
+    if ws_ > 1:
+        torch.distributed.barrier()
+    clk = clocks.stop()
+    ms_total = t_start.elapsed_time(t_end)
+    for ev in per_step_events:
+        for o in st.ops:
+            per_op[o] += ev[o][0].elapsed_time(ev[o][1])
+    st.check_status()
+    if ws_ > 1:
+        t = torch.tensor([ms_total], dtype=torch.float64)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        ms_total = float(t.item())
+    ms_step = ms_total / args.steps
+    flops = st.total_flops()
+    value = flops * ws_ / (ms_step * 1e-3) / 1e12
+
+    # ------------------------------------------------------------ end to end through the public API
+    e2e = e2e_measure(torch, st, args, dev)
+
+    # ------------------------------------------------------------ overhead vs plain unsplit GEMMs
+    overhead = {}
+    if not args.no_overhead:
+        shapes = {
+            "ag_gemm": (st.ag.M, st.ag.N, st.ag.K, "f16"),
+            "gemm_rs": (st.rs.M, st.rs.N, st.rs.K, "f16"),
+            "decode_rs": (st.dec.M, st.dec.N, st.dec.K, "bf16"),
+            "moe_layer0": (st.moe.T * st.moe.topk, st.moe.F, st.moe.H, "bf16"),
+            "moe_layer1": (st.moe.T * st.moe.topk, st.moe.H, st.moe.F, "bf16"),
+        }
+        for o in st.ops:
+            M, N, K, d = shapes[o]
+            tp = time_plain(torch, fx, dev, M, N, K, d)
+            fused = per_op[o] / args.steps
+            best = min(tp.values())
+            overhead[o] = {"fused_us": round(fused * 1e3, 1), "plain_cublas_us": round(tp["cublas"] * 1e3, 1),
+                           "plain_own_us": round(tp["own"] * 1e3, 1),
+                           "overhead_us": round((fused - best) * 1e3, 1),
+                           "plain_shape": f"{M}x{N}x{K} {d}"}
+
+    pk = peaks()
+    breakdown = {o: {"ms": round(per_op[o] / args.steps, 4),
+                     "tflops": round(st.flops[o] / (per_op[o] / args.steps * 1e-3) / 1e12, 1)}
+                 for o in st.ops}
+    dom = max(st.ops, key=lambda o: per_op[o])
+    dom_ms = per_op[dom] / args.steps
+    dom_tf = st.flops[dom] / (dom_ms * 1e-3) / 1e12
+    traffic = load_traffic(dom)
+    roofline = {"kernel": dom, "bound": "tensor", "achieved": round(dom_tf, 1),
+                "peak": pk["tc_sus"], "unit": "TFLOP/s", "frac": round(dom_tf / pk["tc_sus"], 4),
+                "peak_kind": f"bf16 dense, sustained ({pk['src']}); fp16 has the same nominal rate",
+                "traffic": traffic,
+                "algorithmic_flops_per_launch": st.flops[dom]}
+    line = {
+        "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": ws_, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(ms_step, 4), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": DTYPE,
+        "data": "synthetic (seeded normal / Zipf-routed inputs, random-init weights)",
+        "config": {"workload": WORKLOAD + (" [reduced sizes]" if args.small else ""),
+                   "parallelism": f"R=8 virtual TP ranks per GPU; replicas x{ws_}",
+                   "l2": "inputs larger than L2 (weights 0.47-1.2 GB per op stream from HBM every step)",
+                   "step_tflop": round(flops / 1e12, 3)},
+        "roofline": roofline,
+        "breakdown": breakdown,
+        "overhead_vs_plain_gemm": overhead,
+        "e2e": e2e,
+        "gpu_launches": st.launches_per_step * args.steps,
+        "clocks": clk,
+    }
+    if rank == 0 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(args)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if ws_ > 1:
+        torch.distributed.destroy_process_group()
+
+
+def load_traffic(kernel):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken on
+    the current kernel sources (else None)."""
+    p = os.path.join(ROOT, "profiles", "ncu_traffic.json")
+    try:
+        with open(p) as f:
+            d = json.load(f)
+    except Exception:
+        return None
+    ent = d.get(kernel)
+    if not ent or ent.get("kernel_hash") != kernel_hash():
+        return None
+    return ent.get("dram_bytes_per_launch")
+
+
+def e2e_measure(torch, st, args, dev):
+    """Same metric through the public API with host buffers: pinned H2D of the
+    step's activations and routing, the step, and D2H of its results."""
+    host_in = []
+    dev_in = st.X + st.dA + st.mX + [st.ids, st.gw]
+    for t in dev_in:
+        host_in.append(torch.empty(t.shape, dtype=t.dtype, pin_memory=True).copy_(t))
+    dev_out = st.out2 + st.dout + st.mY
+    host_out = [torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in dev_out]
+    h2d = sum(t.numel() * t.element_size() for t in host_in)
+    d2h = sum(t.numel() * t.element_size() for t in host_out)
+    n = max(3, args.steps // 2)
+    torch.cuda.synchronize()
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    t0.record()
+    for _ in range(n):
+        for h, d in zip(host_in, dev_in):
+            d.copy_(h, non_blocking=True)
+        st.step()
+        for d, h in zip(dev_out, host_out):
+            h.copy_(d, non_blocking=True)
+    t1.record()
+    torch.cuda.synchronize()
+    ms = t0.elapsed_time(t1) / n
+    return {"value": round(st.total_flops() / (ms * 1e-3) / 1e12, 2), "unit": UNIT,
+            "ms_per_step": round(ms, 4), "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+            "resident": "weights stay resident in HBM; activations, routing and results cross the link"}
+
+
+# ---------------------------------------------------------------- CPU oracle (baseline / reference arm)
+_SAMPLE_CACHE = {}
+
+
+def _sample_configs(rows, cols, tokens, fcols):
+    """Row/column samples of each op of the step: same K, same rank structure,
+    fewer output rows and columns (all drawn by the same seeded generator)."""
+    C = configs.CONFIGS
+    ag, rs, dec, moe = C["ag_mlp0"], C["rs_mlp1"], C["rs_decode"], C["moe"]
+    return (configs.small(ag, M=ag.R * max(rows // ag.R, 1), N=ag.R * cols),
+            configs.small(rs, M=rs.R * max(rows // rs.R, 1), N=cols),
+            configs.small(dec, N=cols),
+            configs.small(moe, T=moe.R * max(tokens // moe.R, 1), F=moe.R * fcols))
+
+
+def _sample_inputs(key):
+    if key not in _SAMPLE_CACHE:
+        ag, rs, dec, m = _sample_configs(*key)
+        _SAMPLE_CACHE.clear()
+        _SAMPLE_CACHE[key] = (configs.ag_inputs(ag), configs.rs_inputs(rs), configs.rs_inputs(dec),
+                              configs.moe_inputs(m, with_h=False))
+    return _SAMPLE_CACHE[key]
+
+
+def oracle_sample(rows, cols, tokens, fcols):
+    """One bounded CPU-oracle sample of the step (AG-GEMM, GEMM-RS, decode
+    GEMM-RS, MoE routing + layer0 + layer1) on a row/column sample of every op.
+    Returns (flops, seconds of oracle time; input generation excluded)."""
+    import oracle
+    ag, rs, dec, m = _sample_configs(rows, cols, tokens, fcols)
+    (xs, w1), (As, Bs), (da, dw), md = _sample_inputs((rows, cols, tokens, fcols))
+    t = time.time()
+    oracle.ag_gemm(xs, w1, ag.dtype)
+    oracle.gemm_rs(As, Bs, rs.dtype)
+    oracle.gemm_rs(da, dw, dec.dtype)
+    h, routing = oracle.moe_layer0(md["x_shards"], md["w1_shards"], md["topk_ids"], m.E, m.dtype)
+    oracle.moe_layer1(h, md["w2_shards"], md["topk_ids"], md["topk_weights"], m.E, m.dtype,
+                      routing_=routing, h_dtype="f64")
+    secs = time.time() - t
+    flops = ag.flops + rs.flops + dec.flops + 2 * m.flops_per_layer
+    return flops, secs
+
+
+def _cores():
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count()
+
+
+def _sample_desc(rows, cols, tokens, fcols):
+    return (f"float64 numpy oracle on a sample of every op: {rows} token rows x {cols} output "
+            f"columns per rank (AG-GEMM, GEMM-RS), 128 x {cols} (decode), {tokens} MoE tokens with "
+            f"F/R = {fcols}; full reduction lengths")
+
+
+def cpu_baseline(args):
+    key = (args.cpu_rows, args.cpu_cols, args.cpu_tokens, args.cpu_fcols)
+    flops, secs = oracle_sample(*key)
+    return {"value": round(flops / secs / 1e12, 5), "unit": UNIT, "cores": _cores(), "kind": "oracle",
+            "sample": _sample_desc(*key) + f" ({flops / 1e9:.1f} GFLOP in {secs:.1f} s)"}
+
+
+def run_reference(args):
+    ws_, rank, _ = dist_env()
+    if rank != 0:
+        return
+    key = (args.ref_rows, args.ref_cols, args.ref_tokens, args.ref_fcols)
+    for _ in range(args.warmup):
+        oracle_sample(*key)
+    tot_f, tot_s = 0.0, 0.0
+    t0 = time.time()
+    for _ in range(args.steps):
+        f, s = oracle_sample(*key)
+        tot_f += f
+        tot_s += s
+    wall = time.time() - t0
+    value = tot_f / tot_s / 1e12
+    line = {
+        "impl": "reference", "metric": METRIC, "value": round(value, 5), "unit": UNIT, "n_gpus": ws_,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(wall / args.steps * 1e3, 1),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64 (oracle)",
+        "data": "synthetic (seeded)",
+        "config": {"workload": WORKLOAD, "sample": _sample_desc(*key)},
+        "cpu_baseline": {"value": round(value, 5), "unit": UNIT, "cores": _cores(), "kind": "oracle",
+                         "sample": "each step: " + _sample_desc(*key)},
+        "e2e": {"value": round(value, 5), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--small", action="store_true", help="reduced sizes (profiling captures)")
+    ap.add_argument("--ops", default="", help="comma list of ops to run (default: the whole step)")
+    ap.add_argument("--no-overhead", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-rows", type=int, default=128)
+    ap.add_argument("--cpu-cols", type=int, default=4096)
+    ap.add_argument("--cpu-tokens", type=int, default=512)
+    ap.add_argument("--cpu-fcols", type=int, default=512)
+    ap.add_argument("--ref-rows", type=int, default=32)
+    ap.add_argument("--ref-cols", type=int, default=512)
+    ap.add_argument("--ref-tokens", type=int, default=128)
+    ap.add_argument("--ref-fcols", type=int, default=128)
+    args = ap.parse_args()
+    if args.warmup < 3 and args.impl == "ours":
+        args.warmup = 3
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()
