@@ -176,6 +176,27 @@ flux_status_t flux_gemm_rs(int R, int M, int N, int K, flux_dtype_t dtype,
                            void* const* out, void* workspace, size_t workspace_bytes,
                            const flux_opts_t* opts, void* stream);
 
+/* GEMM + ReduceScatter that allocates nothing and takes no workspace.
+ * No counterpart in the FLUX or COMET pages: it exists for callers that cannot
+ * allocate device memory or hand over a workspace (plugin hosts and inference
+ * runtimes whose device-memory budget is fixed before serving starts, wrappers
+ * without an allocator).  Same arguments, results and requirements as
+ * flux_gemm_rs, minus the workspace.  Scratch comes from a 256-byte aligned
+ * __device__ array of FLUX_NOALLOC_SCRATCH_BYTES inside the library, held by
+ * every GPU that loads the library until the process exits.
+ *   - Returns FLUX_ERR_WORKSPACE, launching nothing, when
+ *     flux_workspace_size(FLUX_OP_GEMM_RS, R, M, N, K) exceeds that size.
+ *   - The first call on a device looks up the array's device address (with
+ *     that device current); make it before any stream capture begins.
+ *   - All calls on a device share the array and it keeps the last call's
+ *     contents; each call zeroes the part it uses on `stream` first.  Calls
+ *     that overlap on the GPU race on it: order them (one stream or events).
+ *   - Device-side status (flux_get_status) is not available for these calls. */
+#define FLUX_NOALLOC_SCRATCH_BYTES (16u * 1024u * 1024u)
+flux_status_t flux_gemm_rs_noalloc(int R, int M, int N, int K, flux_dtype_t dtype,
+                                   const void* const* a_shards, const void* const* b_shards,
+                                   void* const* out, const flux_opts_t* opts, void* stream);
+
 /* ---------------------------------------------------------------- MoE ops */
 
 /* Routing of T tokens with topk experts each (COMET article, section

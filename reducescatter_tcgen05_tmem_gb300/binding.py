@@ -43,6 +43,7 @@ FLUX_OP_MOE_RS = 4
 
 FLUX_MAX_RANKS = 16
 FLUX_MAX_EXPERTS = 1024
+FLUX_NOALLOC_SCRATCH_BYTES = 16 * 1024 * 1024
 
 WAIT_SITES = {1: "ready flag", 2: "smem slot free", 3: "smem slot full",
               4: "accumulator free", 5: "accumulator full", 6: "drain"}
@@ -87,6 +88,7 @@ _SIGS = {
     "flux_gemm": ([_i, _i, _i, _i, _vp, _vp, _vp, _vp, _sz, _opt, _vp], _i),
     "flux_ag_gemm": ([_i, _i, _i, _i, _i, _vpp, _vpp, _vpp, _vp, _vp, _sz, _opt, _vp], _i),
     "flux_gemm_rs": ([_i, _i, _i, _i, _i, _vpp, _vpp, _vpp, _vp, _sz, _opt, _vp], _i),
+    "flux_gemm_rs_noalloc": ([_i, _i, _i, _i, _i, _vpp, _vpp, _vpp, _opt, _vp], _i),
     "flux_moe_route": ([_i, _i, _i, _vp, _vp, _vp, _vp, _vp, _vp, _sz, _vp], _i),
     "flux_moe_ag_grouped_gemm": ([_i, _i, _i, _i, _i, _i, _i, _vpp, _vpp, _vp, _vpp, _vp, _vp,
                                   _vp, _vp, _vp, _vp, _sz, _opt, _vp], _i),
@@ -206,6 +208,15 @@ def flux_gemm_rs(R, M, N, K, dtype, a_shards, b_shards, out, workspace, opts=Non
     _check(_lib.flux_gemm_rs(R, M, N, K, dtype, _ptrs(a_shards), _ptrs(b_shards), _ptrs(out),
                              _ptr(workspace), _nbytes(workspace), _opts(opts), _stream(stream)),
            "flux_gemm_rs")
+
+
+def flux_gemm_rs_noalloc(R, M, N, K, dtype, a_shards, b_shards, out, opts=None,
+                         stream=None) -> None:
+    """flux_gemm_rs without a workspace: scratch lives in a fixed device array of
+    the library (FLUX_NOALLOC_SCRATCH_BYTES), for callers that cannot allocate."""
+    _check(_lib.flux_gemm_rs_noalloc(R, M, N, K, dtype, _ptrs(a_shards), _ptrs(b_shards),
+                                     _ptrs(out), _opts(opts), _stream(stream)),
+           "flux_gemm_rs_noalloc")
 
 
 def flux_moe_route(T, E, topk, topk_ids, counts, offsets, slot_to_row, row_to_slot,
