@@ -40,7 +40,13 @@ constexpr int MAXR = 16;
 constexpr int EPI_WARPS = 4;
 constexpr int GATHER_LAG = 2;         // cp.async groups in flight before a stage is published
 
-constexpr int SMEM_BYTES = STAGES * (A_STAGE + B_STAGE) + 1024 /*align*/ + 256 /*barriers*/;
+// epilogue staging for the fp32 reduce modes: per epilogue warp 32 rows of 32
+// floats, each row padded to 144 bytes (16-byte aligned rows for the bulk
+// reduce; the pad spreads the rows of one 16-byte store over all banks)
+constexpr int STG_PITCH = 144;
+constexpr int STG_WARP = 32 * STG_PITCH;
+constexpr int SMEM_BYTES = STAGES * (A_STAGE + B_STAGE) + 1024 /*align*/ + 256 /*barriers*/ +
+                           EPI_WARPS * STG_WARP;
 
 enum Mode { MODE_STORE = 0, MODE_REDUCE = 1, MODE_MOE_GATHER = 2, MODE_MOE_SCATTER = 3 };
 
@@ -305,6 +311,7 @@ struct Smem {
   uint64_t* tempty; // [2]
   uint64_t* drain;  // [1]
   uint32_t* tmem_slot;
+  uint8_t* stg;     // EPI_WARPS x STG_WARP epilogue staging
 };
 
 // TMA producer (one thread).
@@ -515,16 +522,24 @@ __device__ __forceinline__ void store_row_chunk(void* out, long long row_off_ele
   }
 }
 
-__device__ __forceinline__ void red_row_chunk(float* dst, int ncols_valid, const uint32_t (&v)[32],
-                                              float scale) {
+// Stage this thread's 32 fp32 values (times `scale`) as one 128-byte row of
+// the warp's staging buffer and hand the row to a bulk reduce-add into
+// global[dst .. dst + 4 * ncols_valid).  The previous bulk reduce of this
+// thread must have finished reading the row first.
+__device__ __forceinline__ void stage_and_reduce(float* dst, uint32_t srow, int ncols_valid,
+                                                 const uint32_t (&v)[32], float scale) {
+  bulk_wait_read_all();
 #pragma unroll
   for (int g = 0; g < 8; ++g) {
-    if (g * 4 < ncols_valid) {
-      float4 q = make_float4(__uint_as_float(v[g * 4 + 0]) * scale, __uint_as_float(v[g * 4 + 1]) * scale,
-                             __uint_as_float(v[g * 4 + 2]) * scale, __uint_as_float(v[g * 4 + 3]) * scale);
-      atomicAdd(reinterpret_cast<float4*>(dst + g * 4), q);
-    }
+    const float a = __uint_as_float(v[g * 4 + 0]) * scale, b = __uint_as_float(v[g * 4 + 1]) * scale;
+    const float c = __uint_as_float(v[g * 4 + 2]) * scale, d = __uint_as_float(v[g * 4 + 3]) * scale;
+    asm volatile("st.shared.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(srow + g * 16), "f"(a), "f"(b),
+                 "f"(c), "f"(d) : "memory");
   }
+  fence_proxy_async_smem();
+  const int n = ncols_valid < 32 ? ncols_valid : 32;
+  bulk_reduce_add_f32(dst, srow, static_cast<uint32_t>(n) * 4u);
+  bulk_commit();
 }
 
 // Convert 8 consecutive fp32 accumulators (L2) to 16 bits, store them, and
@@ -575,6 +590,7 @@ __device__ void epilogue(const KParams& p, const Smem& s, const Ctl& c, uint32_t
       tok = slot / p.topk;
       gate = __ldg(p.topk_w + slot);
     }
+    const uint32_t srow = smem_u32(s.stg + q * STG_WARP + lane * STG_PITCH);
     for (int ch = 0; ch < BN / 32; ++ch) {
       if (ch * 32 >= ncols) break;  // warp-uniform
       uint32_t v[32];
@@ -584,9 +600,9 @@ __device__ void epilogue(const KParams& p, const Smem& s, const Ctl& c, uint32_t
       if (MODE == MODE_STORE || MODE == MODE_MOE_GATHER) {
         store_row_chunk<DT>(p.out[w.r], static_cast<long long>(row) * p.ldo, n0 + ch * 32, nv, v);
       } else if (MODE == MODE_REDUCE) {
-        red_row_chunk(p.acc + static_cast<long long>(row) * p.N + n0 + ch * 32, nv, v, 1.0f);
+        stage_and_reduce(p.acc + static_cast<long long>(row) * p.N + n0 + ch * 32, srow, nv, v, 1.0f);
       } else {
-        red_row_chunk(p.acc + static_cast<long long>(tok) * p.N + n0 + ch * 32, nv, v, gate);
+        stage_and_reduce(p.acc + static_cast<long long>(tok) * p.N + n0 + ch * 32, srow, nv, v, gate);
       }
     }
     // hand the accumulator back to the MMA warp
@@ -595,6 +611,11 @@ __device__ void epilogue(const KParams& p, const Smem& s, const Ctl& c, uint32_t
     if (lane == 0) mbar_arrive(smem_u32(&s.tempty[b]));
     ++it;
 
+    if (MODE == MODE_REDUCE || MODE == MODE_MOE_SCATTER) {
+      // this thread's reduce-adds are performed and visible before any arrival count
+      bulk_wait_all();
+      fence_proxy_async_global();
+    }
     if (MODE == MODE_REDUCE) {
       // arrival counter of this tile's 32-row quarter counts k-slices
       __threadfence();
@@ -672,6 +693,7 @@ fused_gemm_kernel(const __grid_constant__ KParams p) {
   s.tempty = bars + 2 * STAGES + 2;
   s.drain = bars + 2 * STAGES + 4;
   s.tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * STAGES + 5);
+  s.stg = base + STAGES * (A_STAGE + B_STAGE) + 256;
 
   const int warp = threadIdx.x >> 5;
   Ctl c;
