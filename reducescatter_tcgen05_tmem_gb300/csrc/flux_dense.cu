@@ -3,28 +3,21 @@
 
 #include "flux_host.h"
 #include "flux_kernels.cuh"
+#include "flux_launch.cuh"
 
 namespace flux {
 namespace {
 
-template <int MODE, int DT>
-flux_status_t launch(const KParams& p, int grid, cudaStream_t stream) {
-  using KS = KernelShape<MODE, DT>;
-  static std::once_flag once;
-  static cudaError_t attr_err = cudaSuccess;
-  std::call_once(once, [] {
-    attr_err = cudaFuncSetAttribute(fused_gemm_kernel<MODE, DT>,
-                                    cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
-  });
-  if (attr_err != cudaSuccess) return cuda_fail(attr_err);
-  fused_gemm_kernel<MODE, DT><<<grid, KS::THREADS, SMEM_BYTES, stream>>>(p);
-  cudaError_t e = cudaGetLastError();
-  return e == cudaSuccess ? FLUX_OK : cuda_fail(e);
+template <int MODE, int PAIR>
+flux_status_t launch_dt(flux_dtype_t dt, const KParams& p, int grid, cudaStream_t s) {
+  return dt == FLUX_BF16 ? Launcher<MODE, 1, PAIR>::launch(p, grid, s)
+                         : Launcher<MODE, 0, PAIR>::launch(p, grid, s);
 }
 
-template <int MODE>
-flux_status_t launch_dt(flux_dtype_t dt, const KParams& p, int grid, cudaStream_t s) {
-  return dt == FLUX_BF16 ? launch<MODE, 1>(p, grid, s) : launch<MODE, 0>(p, grid, s);
+template <int MODE, int PAIR>
+int grid_dt(flux_dtype_t dt, const DeviceInfo& dev, const flux_opts_t* opts, long long units) {
+  return dt == FLUX_BF16 ? grid_for<MODE, 1, PAIR>(dev, opts, units)
+                         : grid_for<MODE, 0, PAIR>(dev, opts, units);
 }
 
 bool valid_dtype(flux_dtype_t dt) { return dt == FLUX_F16 || dt == FLUX_BF16; }
@@ -35,12 +28,6 @@ void fill_common(KParams& p, const flux_opts_t* opts, void* ws) {
   p.group_n = (opts && opts->group_n > 0) ? opts->group_n : 8;
   p.seq = next_seq();
   p.hdr = static_cast<uint32_t*>(ws);
-}
-
-int grid_size(const DeviceInfo& d, const flux_opts_t* opts, long long work) {
-  int g = (opts && opts->num_ctas > 0) ? opts->num_ctas : d.sm_count;
-  if (work < g) g = static_cast<int>(work);
-  return g < 1 ? 1 : g;
 }
 
 flux_status_t zero_outputs(void* const* out, int n, size_t bytes, cudaStream_t s) {
@@ -116,11 +103,12 @@ extern "C" flux_status_t flux_ag_gemm(int R, int M, int N, int K, flux_dtype_t d
       return st;
     p.out[r] = out[r];
   }
+  constexpr int PAIR = 2;  // 256 x 256 tiles on CTA pairs
   p.R = R;
   p.M = M;
   p.N = Nr;
   p.K = K;
-  p.Mt = (M + BM - 1) / BM;
+  p.Mt = (M + Geo<PAIR>::TILE_M - 1) / Geo<PAIR>::TILE_M;
   p.Nt = (Nr + BN - 1) / BN;
   p.KT = (K + BK - 1) / BK;
   p.ldo = Nr;
@@ -129,7 +117,9 @@ extern "C" flux_status_t flux_ag_gemm(int R, int M, int N, int K, flux_dtype_t d
   p.num_units = R * p.Mt * p.Nt;
   p.flags = ready_flags;
   fill_common(p, opts, workspace);
-  return launch_dt<MODE_STORE>(dtype, p, grid_size(dev, opts, p.num_units), s);
+  const int grid = grid_dt<MODE_STORE, PAIR>(dtype, dev, opts, p.num_units);
+  if (grid == 0) return FLUX_ERR_CUDA;
+  return launch_dt<MODE_STORE, PAIR>(dtype, p, grid, s);
 }
 
 extern "C" flux_status_t flux_gemm(int M, int N, int K, flux_dtype_t dtype, const void* A,
@@ -180,35 +170,44 @@ extern "C" flux_status_t flux_gemm_rs(int R, int M, int N, int K, flux_dtype_t d
   p.M = M;
   p.N = N;
   p.K = Kr;
-  p.Mt = (M + BM - 1) / BM;
   p.Nt = (N + BN - 1) / BN;
   p.KT = (Kr + BK - 1) / BK;
   p.ldo = N;
   p.rows_per_rank = rows;
   p.a_box_m = BM;
-  const int tiles = p.Mt * p.Nt;
-  p.num_units = tiles * R;
-  p.total_ksteps = static_cast<long long>(p.num_units) * p.KT;
   uint8_t* ws = static_cast<uint8_t*>(workspace);
   p.counters = reinterpret_cast<uint32_t*>(ws + WS_HEADER);
   p.acc = reinterpret_cast<float*>(ws + WS_HEADER + rs_counter_bytes(M, N));
   fill_common(p, opts, workspace);
 
-  // Few tiles per SM (decode shapes): give every CTA an equal contiguous range
-  // of k-slices (tiles split along K add into the same fp32 owner tile).
-  // Otherwise: whole tiles, strided over a persistent grid.
-  int grid;
+  // Few tiles per SM (decode shapes): single-CTA 128-row tiles and an equal
+  // contiguous range of k-slices per CTA (tiles split along K add into the same
+  // fp32 owner tile).  Otherwise: whole 256 x 256 tiles on CTA pairs, strided
+  // over a persistent grid.
   const int sm = (opts && opts->num_ctas > 0) ? opts->num_ctas : dev.sm_count;
-  if (p.num_units < 4 * sm) {
+  const long long units128 = static_cast<long long>((M + BM - 1) / BM) * p.Nt * R;
+  if (units128 < 4 * sm) {
+    p.Mt = (M + BM - 1) / BM;
+    p.num_units = p.Mt * p.Nt * R;
+    p.total_ksteps = static_cast<long long>(p.num_units) * p.KT;
     p.stream_k = 1;
-    long long per = p.total_ksteps / sm;
-    grid = per >= 4 ? sm : static_cast<int>((p.total_ksteps + 3) / 4);
+    const int cap = grid_dt<MODE_REDUCE, 1>(dtype, dev, opts, p.total_ksteps);
+    if (cap == 0) return FLUX_ERR_CUDA;
+    long long per = p.total_ksteps / cap;
+    int grid = per >= 4 ? cap : static_cast<int>((p.total_ksteps + 3) / 4);
     if (grid < 1) grid = 1;
-  } else {
-    p.stream_k = 0;
-    grid = grid_size(dev, opts, p.num_units);
+    p.tiles_per_group = p.Mt * p.Nt;
+    return launch_dt<MODE_REDUCE, 1>(dtype, p, grid, s);
   }
-  int tg = (opts && opts->tiles_per_group > 0) ? opts->tiles_per_group : grid;
+  constexpr int PAIR = 2;
+  p.Mt = (M + Geo<PAIR>::TILE_M - 1) / Geo<PAIR>::TILE_M;
+  const int tiles = p.Mt * p.Nt;
+  p.num_units = tiles * R;
+  p.total_ksteps = static_cast<long long>(p.num_units) * p.KT;
+  p.stream_k = 0;
+  const int grid = grid_dt<MODE_REDUCE, PAIR>(dtype, dev, opts, p.num_units);
+  if (grid == 0) return FLUX_ERR_CUDA;
+  const int tg = (opts && opts->tiles_per_group > 0) ? opts->tiles_per_group : grid / PAIR;
   p.tiles_per_group = tg < tiles ? tg : tiles;
-  return launch_dt<MODE_REDUCE>(dtype, p, grid, s);
+  return launch_dt<MODE_REDUCE, PAIR>(dtype, p, grid, s);
 }

@@ -2,13 +2,13 @@
 // collectives over R virtual ranks (all ranks' buffers live on this GPU).
 //
 //   producer warp(s)  TMA (or cp.async row gather) of A/B k-slices into a
-//                     STAGES-deep shared-memory ring; for AllGather, the A tile
-//                     is pulled from the rank that owns its rows only after that
-//                     rank's ready flag is seen (acquire)
-//   MMA warp          one thread issues tcgen05.mma (128 x 256 x 16, fp32 in
-//                     TMEM) per k-substep; accumulators are double-buffered in
-//                     the 512 TMEM columns so the epilogue of one tile overlaps
-//                     the main loop of the next
+//                     shared-memory ring; for AllGather, the A tile is pulled
+//                     from the rank that owns its rows only after that rank's
+//                     ready flag is seen (acquire)
+//   MMA warp          one thread issues tcgen05.mma (fp32 accumulators in
+//                     TMEM); accumulators are double-buffered in the 512 TMEM
+//                     columns so the epilogue of one tile overlaps the main
+//                     loop of the next
 //   epilogue warps    tcgen05.ld TMEM -> registers, then one of:
 //                       STORE        convert to 16 bits, store (AllGather-GEMM, plain GEMM)
 //                       REDUCE       fp32 add into the owner rank's row chunk of the
@@ -17,6 +17,18 @@
 //                       MOE_GATHER   STORE with A rows gathered by expert (MoE layer0)
 //                       MOE_SCATTER  gate-weighted fp32 add into the owning token row;
 //                                    the last of R*topk contributions converts (MoE layer1)
+//
+// PAIR = 1: one CTA computes a 128 x 256 tile with tcgen05.mma.cta_group::1
+//           (4-stage ring of 48 KB: A 128x64 + B 64x256).
+// PAIR = 2: a cluster of two CTAs computes a 256 x 256 tile with
+//           tcgen05.mma.cta_group::2 issued by the even CTA.  Each CTA holds
+//           its own 128 rows of A and its own 128 columns of B (6-stage ring
+//           of 32 KB), so every SM streams two thirds of the operand bytes of
+//           the PAIR = 1 tile per unit of tensor work.  Both CTAs' TMA loads
+//           complete on the even CTA's "full" barrier, whose producer expects
+//           the bytes of both.  Commits are multicast to both CTAs' "empty"
+//           and "accumulator full" barriers; both CTAs' epilogue warps arrive
+//           on the even CTA's "accumulator empty" barrier.
 //
 // Every wait is bounded: after timeout_ns (or an iteration cap) the thread
 // records FLUX_ERR_TIMEOUT in the workspace header, raises the per-call abort
@@ -27,13 +39,11 @@
 
 namespace flux {
 
-constexpr int BM = 128;  // tile rows (MMA M)
+constexpr int BM = 128;  // rows of A per CTA (TMEM lanes)
 constexpr int BN = 256;  // tile columns (MMA N)
 constexpr int BK = 64;   // k-slice per pipeline stage (one 128-byte swizzle row of 16-bit data)
 constexpr int UK = 16;   // K of one tcgen05.mma kind::f16
-constexpr int STAGES = 4;
 constexpr int A_STAGE = BM * BK * 2;  // 16 KB
-constexpr int B_STAGE = BN * BK * 2;  // 32 KB
 constexpr int B_BOX_N = 64;           // 64 columns = 128 bytes, one swizzle span
 constexpr int TMEM_COLS = 2 * BN;     // two fp32 accumulators
 constexpr int MAXR = 16;
@@ -45,8 +55,18 @@ constexpr int GATHER_LAG = 2;         // cp.async groups in flight before a stag
 // reduce; the pad spreads the rows of one 16-byte store over all banks)
 constexpr int STG_PITCH = 144;
 constexpr int STG_WARP = 32 * STG_PITCH;
-constexpr int SMEM_BYTES = STAGES * (A_STAGE + B_STAGE) + 1024 /*align*/ + 256 /*barriers*/ +
-                           EPI_WARPS * STG_WARP;
+
+template <int PAIR>
+struct Geo {
+  static constexpr int STAGES = PAIR == 2 ? 6 : 4;
+  static constexpr int B_COLS = BN / PAIR;             // B columns held by one CTA
+  static constexpr int B_BOXES = B_COLS / B_BOX_N;
+  static constexpr int B_STAGE = B_COLS * BK * 2;      // 16 KB or 32 KB
+  static constexpr int TILE_M = BM * PAIR;             // rows of one scheduled tile
+  static constexpr int SMEM = STAGES * (A_STAGE + B_STAGE) + 1024 /*align*/ + 512 /*barriers*/ +
+                              EPI_WARPS * STG_WARP;
+};
+constexpr int SMEM_BYTES = Geo<1>::SMEM > Geo<2>::SMEM ? Geo<1>::SMEM : Geo<2>::SMEM;
 
 enum Mode { MODE_STORE = 0, MODE_REDUCE = 1, MODE_MOE_GATHER = 2, MODE_MOE_SCATTER = 3 };
 
@@ -65,7 +85,7 @@ struct KParams {
   int M;                   // rows of the A row space (AG: gathered rows; MoE: T*topk)
   int N;                   // output columns of one rank
   int K;                   // reduction length of one rank
-  int Mt, Nt, KT;          // tiles along M, N and k-slices along K
+  int Mt, Nt, KT;          // scheduled tiles along M (TILE_M rows), N, and k-slices
   int ldo;                 // output row pitch (elements)
   int rows_per_rank;       // AG: rows per X shard; RS: rows per owner chunk; MoE: tokens per rank
   int a_box_m;             // rows per A TMA box (AG)
@@ -101,7 +121,7 @@ __device__ __forceinline__ bool aborted(const Ctl& c) {
 }
 
 static __device__ __noinline__ void raise_error(const Ctl& c, uint32_t code, uint32_t where,
-                                         uint32_t a0, uint32_t a1) {
+                                                uint32_t a0, uint32_t a1) {
   if (atomicCAS(c.hdr + H_STATUS, 0u, code) == 0u) {
     c.hdr[H_WHERE] = where;
     c.hdr[H_ARG0] = a0;
@@ -111,15 +131,22 @@ static __device__ __noinline__ void raise_error(const Ctl& c, uint32_t code, uin
   atomicExch(c.hdr + H_ABORT, c.seq);
 }
 
+// Waits that have not finished within this many SM cycles start the (slow)
+// checks of the global timer and the abort word; a healthy pipeline never gets
+// there, so the hot path costs one probe per iteration.
+constexpr long long LAZY_CHECK_CYCLES = 1ll << 20;
+
 // Bounded mbarrier wait.  0 = phase completed, 1 = timed out (recorded),
 // 2 = another thread aborted this call.  `check_abort` = false is used by the
 // final drains, which must outlive an abort.
 static __device__ __noinline__ int wait_bar_slow(uint32_t bar, uint32_t parity, const Ctl& c,
-                                          uint32_t where, uint32_t arg1, bool check_abort) {
-  const uint64_t t0 = globaltimer();
+                                                 uint32_t where, uint32_t arg1, bool check_abort) {
+  const long long c0 = clock64();
+  uint64_t t0 = 0;
   for (uint32_t it = 1;; ++it) {
     if (mbar_try_wait(bar, parity)) return 0;
-    if ((it & 15u) == 0u) {
+    if ((it & 63u) == 0u && (clock64() - c0 > LAZY_CHECK_CYCLES || it > (1u << 24))) {
+      if (t0 == 0) t0 = globaltimer();
       if (check_abort && aborted(c)) return 2;
       if (globaltimer() - t0 > c.pipe_timeout || it > (1u << 30)) {
         raise_error(c, ST_TIMEOUT, where, blockIdx.x, arg1);
@@ -135,8 +162,47 @@ __device__ __forceinline__ int wait_bar(uint32_t bar, uint32_t parity, const Ctl
   return wait_bar_slow(bar, parity, c, where, arg1, check_abort);
 }
 
+// Drain form of wait_bar_remote: ignores the abort word (the copies being
+// waited for must land even when the call aborted).
+static __device__ __noinline__ int wait_bar_remote_drain(uint32_t bar, uint32_t parity,
+                                                         const Ctl& c, uint32_t where, uint32_t arg1) {
+  const long long c0 = clock64();
+  uint64_t t0 = 0;
+  for (uint32_t it = 1;; ++it) {
+    if (mbar_test_wait(bar, parity)) return 0;
+    if ((it & 255u) == 0u && (clock64() - c0 > LAZY_CHECK_CYCLES || it > (1u << 24))) {
+      if (t0 == 0) t0 = globaltimer();
+      if (globaltimer() - t0 > c.pipe_timeout || it > (1u << 30)) {
+        raise_error(c, ST_TIMEOUT, where, blockIdx.x, arg1);
+        return 1;
+      }
+    }
+  }
+}
+
+// The same bound for a barrier completed by another CTA of the cluster: polled
+// with the non-blocking test_wait.
+static __device__ __noinline__ int wait_bar_remote(uint32_t bar, uint32_t parity, const Ctl& c,
+                                                   uint32_t where, uint32_t arg1) {
+  if (mbar_test_wait(bar, parity)) return 0;
+  const long long c0 = clock64();
+  uint64_t t0 = 0;
+  for (uint32_t it = 1;; ++it) {
+    if (mbar_test_wait(bar, parity)) return 0;
+    if ((it & 255u) == 0u && (clock64() - c0 > LAZY_CHECK_CYCLES || it > (1u << 24))) {
+      if (t0 == 0) t0 = globaltimer();
+      if (aborted(c)) return 2;
+      if (globaltimer() - t0 > c.pipe_timeout || it > (1u << 30)) {
+        raise_error(c, ST_TIMEOUT, where, blockIdx.x, arg1);
+        return 1;
+      }
+    }
+  }
+}
+
 // Bounded wait for ready_flags[s] >= epoch (acquire at gpu scope).  True when ready.
-static __device__ __noinline__ bool wait_flag(const uint32_t* flags, int s, uint32_t epoch, const Ctl& c) {
+static __device__ __noinline__ bool wait_flag(const uint32_t* flags, int s, uint32_t epoch,
+                                              const Ctl& c) {
   uint32_t v = ld_acquire_u32(flags + s);
   if (v >= epoch) return true;
   const uint64_t t0 = globaltimer();
@@ -167,29 +233,31 @@ __device__ __forceinline__ void raster(int t, int Mt, int Nt, int group_n, int& 
 
 struct Work {
   int r;       // rank whose operands feed the tile
-  int mt, nt;  // tile coordinates (mt: m-tile in the A row space)
-  int m0;      // first A row of the tile
+  int mt, nt;  // scheduled tile coordinates (mt counts TILE_M-row tiles)
+  int m0;      // first A row of THIS CTA's part of the tile
   int row_end; // rows >= row_end are not part of the tile's problem
   int e;       // expert (MoE)
   int k0, k1;  // k-slice range of this item
-  int tile;    // linear output-tile id (REDUCE counters)
+  int tile;    // linear 128-row output-tile id of this CTA's part (REDUCE counters)
 };
 
 // AllGather / plain GEMM: unit -> (rank, m-tile, n-tile).  Ranks are the
 // outer loop; inside a rank the m order is rotated so that rank r starts with
 // the rows it owns (the local shard is the first to be ready) and then walks
 // the other ranks' shards in ring order.
-__device__ __forceinline__ Work decode_store(const KParams& p, int u) {
+template <int PAIR>
+__device__ __forceinline__ Work decode_store(const KParams& p, int u, int cta) {
+  constexpr int TM = Geo<PAIR>::TILE_M;
   Work w;
   const int per_rank = p.Mt * p.Nt;
   w.r = u / per_rank;
   int mt, nt;
   raster(u - w.r * per_rank, p.Mt, p.Nt, p.group_n, mt, nt);
-  const int mt_per_shard = p.rows_per_rank / BM;
-  if (mt_per_shard > 0 && p.rows_per_rank % BM == 0) mt = (mt + w.r * mt_per_shard) % p.Mt;
+  const int mt_per_shard = p.rows_per_rank / TM;
+  if (mt_per_shard > 0 && p.rows_per_rank % TM == 0) mt = (mt + w.r * mt_per_shard) % p.Mt;
   w.mt = mt;
   w.nt = nt;
-  w.m0 = mt * BM;
+  w.m0 = mt * TM + cta * BM;
   w.row_end = p.M;
   w.e = 0;
   w.k0 = 0;
@@ -202,7 +270,9 @@ __device__ __forceinline__ Work decode_store(const KParams& p, int u) {
 // one output tile are `tiles_per_group` units apart, so with a strided
 // persistent schedule they land in consecutive waves while the owner's fp32
 // tile is still in L2.
-__device__ __forceinline__ Work decode_reduce(const KParams& p, int u) {
+template <int PAIR>
+__device__ __forceinline__ Work decode_reduce(const KParams& p, int u, int cta) {
+  constexpr int TM = Geo<PAIR>::TILE_M;
   Work w;
   const int tiles = p.Mt * p.Nt;
   const int TG = p.tiles_per_group;
@@ -220,8 +290,8 @@ __device__ __forceinline__ Work decode_reduce(const KParams& p, int u) {
     t = full_groups * TG + (rem - w.r * tl);
   }
   raster(t, p.Mt, p.Nt, p.group_n, w.mt, w.nt);
-  w.tile = w.mt * p.Nt + w.nt;
-  w.m0 = w.mt * BM;
+  w.tile = (w.mt * PAIR + cta) * p.Nt + w.nt;
+  w.m0 = w.mt * TM + cta * BM;
   w.row_end = p.M;
   w.e = 0;
   w.k0 = 0;
@@ -256,26 +326,28 @@ __device__ __forceinline__ Work decode_moe(const KParams& p, int u, int total_mt
   return w;
 }
 
-// Iterates the items of this CTA identically in every role.
-template <int MODE>
+// Iterates the items of this CTA identically in every role.  With PAIR = 2
+// both CTAs of a cluster walk the same units (cluster index = blockIdx / 2).
+template <int MODE, int PAIR>
 struct ItemIter {
   const KParams& p;
   int total_mt;      // MoE: device-computed number of m-tiles
   int num_units;
   long long pos, end;  // stream-K k-step range
-  int u;
+  int u, stride, cta;
 
-  __device__ ItemIter(const KParams& p_, int total_mt_) : p(p_), total_mt(total_mt_) {
+  __device__ ItemIter(const KParams& p_, int total_mt_, int cta_) : p(p_), total_mt(total_mt_), cta(cta_) {
     if (MODE == MODE_MOE_GATHER || MODE == MODE_MOE_SCATTER) {
       num_units = total_mt * p.Nt * p.R;
     } else {
       num_units = p.num_units;
     }
-    u = blockIdx.x;
+    u = blockIdx.x / PAIR;
+    stride = gridDim.x / PAIR;
     if (MODE == MODE_REDUCE && p.stream_k) {
       const long long L = p.total_ksteps;
-      pos = L * blockIdx.x / gridDim.x;
-      end = L * (blockIdx.x + 1) / gridDim.x;
+      pos = L * u / stride;
+      end = L * (u + 1) / stride;
     }
   }
 
@@ -286,17 +358,17 @@ struct ItemIter {
       const int k0 = static_cast<int>(pos - static_cast<long long>(unit) * p.KT);
       long long k1 = k0 + (end - pos);
       if (k1 > p.KT) k1 = p.KT;
-      w = decode_reduce(p, unit);
+      w = decode_reduce<PAIR>(p, unit, cta);
       w.k0 = k0;
       w.k1 = static_cast<int>(k1);
       pos += k1 - k0;
       return true;
     }
     if (u >= num_units) return false;
-    if (MODE == MODE_STORE) w = decode_store(p, u);
-    else if (MODE == MODE_REDUCE) w = decode_reduce(p, u);
+    if (MODE == MODE_STORE) w = decode_store<PAIR>(p, u, cta);
+    else if (MODE == MODE_REDUCE) w = decode_reduce<PAIR>(p, u, cta);
     else w = decode_moe(p, u, total_mt);
-    u += gridDim.x;
+    u += stride;
     return true;
   }
 };
@@ -305,8 +377,8 @@ struct ItemIter {
 struct Smem {
   uint8_t* a;       // STAGES x A_STAGE
   uint8_t* b;       // STAGES x B_STAGE
-  uint64_t* full;   // [STAGES]
-  uint64_t* empty;  // [STAGES]
+  uint64_t* full;   // [STAGES] this CTA's operands landed
+  uint64_t* empty;  // [STAGES] the MMAs reading the stage completed
   uint64_t* tfull;  // [2]
   uint64_t* tempty; // [2]
   uint64_t* drain;  // [1]
@@ -314,65 +386,108 @@ struct Smem {
   uint8_t* stg;     // EPI_WARPS x STG_WARP epilogue staging
 };
 
-// TMA producer (one thread).
+// Bytes the odd CTA of a pair loads for one stage of work item `w` (the even
+// CTA's view of the item): its 128 rows of A and its 128 columns of B.
 template <int MODE>
-__device__ void producer_tma(const KParams& p, const Smem& s, const Ctl& c, int total_mt) {
-  ItemIter<MODE> iter(p, total_mt);
+__device__ __forceinline__ uint32_t pair_peer_bytes(const KParams& p, const Work& w) {
+  const int m0 = w.m0 + BM;
+  int nbox_a = m0 < w.row_end ? 1 : 0;
+  uint32_t a = nbox_a * A_STAGE;
+  if (MODE == MODE_STORE && nbox_a)
+    a = ((min(m0 + BM, w.row_end) - m0 + p.a_box_m - 1) / p.a_box_m) * p.a_box_m * BK * 2;
+  const int n_cta = w.nt * BN + Geo<2>::B_COLS;
+  const int nbox_b = max(0, min(Geo<2>::B_BOXES, (p.N - n_cta + B_BOX_N - 1) / B_BOX_N));
+  return a + nbox_b * B_BOX_N * BK * 2;
+}
+
+// TMA producer (one thread).
+template <int MODE, int PAIR>
+__device__ void producer_tma(const KParams& p, const Smem& s, const Ctl& c, int total_mt, int cta) {
+  using G = Geo<PAIR>;
+  ItemIter<MODE, PAIR> iter(p, total_mt, cta);
   Work w;
   uint32_t stage = 0, phase = 0;
   uint32_t issued = 0;
   uint32_t ready = (p.flags == nullptr) ? 0xFFFFFFFFu : 0u;
   bool ok = true;
   while (ok && iter.next(w)) {
-    int nbox_a = 0;
+    int nbox_a = w.m0 < w.row_end ? 1 : 0;  // a CTA part wholly past the last row loads no A
     if (MODE == MODE_STORE) {
-      // shards covering the valid rows of this tile must be published first
-      const int last_row = min(w.m0 + BM, w.row_end) - 1;
-      const int s0 = w.m0 / p.rows_per_rank, s1 = last_row / p.rows_per_rank;
-      for (int sh = s0; sh <= s1 && ok; ++sh) {
-        if (!((ready >> sh) & 1u)) {
-          if (!wait_flag(p.flags, sh, p.epoch, c)) ok = false;
-          else ready |= 1u << sh;
+      // shards covering the valid rows of this CTA's part must be published first
+      nbox_a = 0;
+      if (w.m0 < w.row_end) {
+        const int last_row = min(w.m0 + BM, w.row_end) - 1;
+        const int s0 = w.m0 / p.rows_per_rank, s1 = last_row / p.rows_per_rank;
+        for (int sh = s0; sh <= s1 && ok; ++sh) {
+          if (!((ready >> sh) & 1u)) {
+            if (!wait_flag(p.flags, sh, p.epoch, c)) ok = false;
+            else ready |= 1u << sh;
+          }
         }
+        if (!ok) break;
+        if (p.flags != nullptr) fence_proxy_async_global();
+        nbox_a = (min(w.m0 + BM, w.row_end) - w.m0 + p.a_box_m - 1) / p.a_box_m;
       }
-      if (!ok) break;
-      if (p.flags != nullptr) fence_proxy_async_global();
-      nbox_a = (min(w.m0 + BM, w.row_end) - w.m0 + p.a_box_m - 1) / p.a_box_m;
     }
-    const int nbox_b = min(BN / B_BOX_N, (p.N - w.nt * BN + B_BOX_N - 1) / B_BOX_N);
-    const uint32_t bytes_a = (MODE == MODE_STORE) ? nbox_a * p.a_box_m * BK * 2 : A_STAGE;
-    const uint32_t bytes = bytes_a + nbox_b * B_BOX_N * BK * 2;
+    const int n_cta = w.nt * BN + cta * G::B_COLS;  // first B column this CTA loads
+    const int nbox_b = max(0, min(G::B_BOXES, (p.N - n_cta + B_BOX_N - 1) / B_BOX_N));
+    uint32_t bytes = ((MODE == MODE_STORE) ? nbox_a * p.a_box_m * BK * 2 : nbox_a * A_STAGE) +
+                     nbox_b * B_BOX_N * BK * 2;
+    if (PAIR == 2 && cta == 0) {
+      // the even CTA's barrier also counts the odd CTA's bytes of the same stage
+      bytes += pair_peer_bytes<MODE>(p, w);
+    }
     for (int k = w.k0; k < w.k1; ++k) {
-      if (wait_bar(smem_u32(&s.empty[stage]), phase ^ 1u, c, W_EMPTY, stage) != 0) { ok = false; break; }
+      if ((PAIR == 2 && cta != 0
+               ? wait_bar_remote(smem_u32(&s.empty[stage]), phase ^ 1u, c, W_EMPTY, stage)
+               : wait_bar(smem_u32(&s.empty[stage]), phase ^ 1u, c, W_EMPTY, stage)) != 0) {
+        ok = false;
+        break;
+      }
       const uint32_t fb = smem_u32(&s.full[stage]);
-      mbar_arrive_expect_tx(fb, bytes);
+      if (PAIR == 1 || cta == 0) mbar_arrive_expect_tx(fb, bytes);
+      const uint32_t fbc = PAIR == 2 ? mapa_shared(fb, 0) : fb;  // barrier in the even CTA
       const uint32_t sa = smem_u32(s.a + stage * A_STAGE);
-      const uint32_t sb = smem_u32(s.b + stage * B_STAGE);
+      const uint32_t sb = smem_u32(s.b + stage * G::B_STAGE);
       const int kc = k * BK;
       if (MODE == MODE_STORE) {
         for (int bx = 0; bx < nbox_a; ++bx) {
           const int row = w.m0 + bx * p.a_box_m;
           const int sh = row / p.rows_per_rank;
-          tma_load_2d(sa + bx * p.a_box_m * BK * 2, &p.tmA[sh], fb, kc, row - sh * p.rows_per_rank);
+          if (PAIR == 2)
+            tma_load_2d_pair(sa + bx * p.a_box_m * BK * 2, &p.tmA[sh], fbc, kc, row - sh * p.rows_per_rank);
+          else
+            tma_load_2d(sa + bx * p.a_box_m * BK * 2, &p.tmA[sh], fb, kc, row - sh * p.rows_per_rank);
         }
-      } else {
-        tma_load_2d(sa, &p.tmA[w.r], fb, kc, w.m0);
+      } else if (nbox_a) {
+        if (PAIR == 2) tma_load_2d_pair(sa, &p.tmA[w.r], fbc, kc, w.m0);
+        else tma_load_2d(sa, &p.tmA[w.r], fb, kc, w.m0);
       }
       for (int j = 0; j < nbox_b; ++j) {
-        const int n = w.nt * BN + j * B_BOX_N;
+        const int n = n_cta + j * B_BOX_N;
         if (MODE == MODE_MOE_SCATTER)
           tma_load_3d(sb + j * B_BOX_N * BK * 2, &p.tmB[w.r], fb, n, kc, w.e);
+        else if (PAIR == 2)
+          tma_load_2d_pair(sb + j * B_BOX_N * BK * 2, &p.tmB[w.r], fbc, n, kc);
         else
           tma_load_2d(sb + j * B_BOX_N * BK * 2, &p.tmB[w.r], fb, n, kc);
       }
       ++issued;
-      if (++stage == STAGES) { stage = 0; phase ^= 1u; }
+      if (++stage == G::STAGES) { stage = 0; phase ^= 1u; }
     }
   }
-  // drain: every issued copy must land before the CTA may exit
-  for (uint32_t st = 0; st < STAGES; ++st) {
-    const uint32_t fills = issued / STAGES + (st < issued % STAGES ? 1u : 0u);
-    if (fills > 0) wait_bar(smem_u32(&s.full[st]), (fills - 1u) & 1u, c, W_DRAIN, st, false);
+  // drain: every issued copy must land before the CTA may exit.  The odd CTA of
+  // a pair cannot see its copies complete (they count on the even CTA's
+  // barrier); it waits until the MMAs that read its last fill of each stage
+  // completed, which implies the fill landed (bounded, like every wait).
+  for (uint32_t st = 0; st < G::STAGES; ++st) {
+    const uint32_t fills = issued / G::STAGES + (st < issued % G::STAGES ? 1u : 0u);
+    if (fills == 0) continue;
+    if (PAIR == 2 && cta != 0) {
+      wait_bar_remote_drain(smem_u32(&s.empty[st]), (fills - 1u) & 1u, c, W_DRAIN, st);
+    } else {
+      wait_bar(smem_u32(&s.full[st]), (fills - 1u) & 1u, c, W_DRAIN, st, false);
+    }
   }
 }
 
@@ -382,7 +497,8 @@ __device__ void producer_tma(const KParams& p, const Smem& s, const Ctl& c, int 
 // thread 0 also issues the B tile by TMA.
 template <int NPROD>
 __device__ void producer_gather(const KParams& p, const Smem& s, const Ctl& c, int total_mt) {
-  ItemIter<MODE_MOE_GATHER> iter(p, total_mt);
+  using G = Geo<1>;
+  ItemIter<MODE_MOE_GATHER, 1> iter(p, total_mt, 0);
   const int tid = threadIdx.x;  // producer warps are warps 0 .. NPROD/32-1
   Work w;
   uint32_t stage = 0, phase = 0, issued = 0;
@@ -406,14 +522,14 @@ __device__ void producer_gather(const KParams& p, const Smem& s, const Ctl& c, i
             static_cast<size_t>(tok - sh * p.rows_per_rank) * p.H * 2;
     }
     if (!ok) break;
-    const int nbox_b = min(BN / B_BOX_N, (p.N - w.nt * BN + B_BOX_N - 1) / B_BOX_N);
+    const int nbox_b = min(G::B_BOXES, (p.N - w.nt * BN + B_BOX_N - 1) / B_BOX_N);
     const uint32_t bytes_b = nbox_b * B_BOX_N * BK * 2;
     for (int k = w.k0; k < w.k1; ++k) {
       int wr = wait_bar(smem_u32(&s.empty[stage]), phase ^ 1u, c, W_EMPTY, stage);
       if (wr != 0) { ok = false; break; }
       const uint32_t fb = smem_u32(&s.full[stage]);
       const uint32_t sa = smem_u32(s.a + stage * A_STAGE);
-      const uint32_t sb = smem_u32(s.b + stage * B_STAGE);
+      const uint32_t sb = smem_u32(s.b + stage * G::B_STAGE);
       const int kc = k * BK;
       if (tid == 0) {
         mbar_arrive_expect_tx(fb, bytes_b);
@@ -436,34 +552,35 @@ __device__ void producer_gather(const KParams& p, const Smem& s, const Ctl& c, i
       if (pending > GATHER_LAG) {
         cp_async_wait<GATHER_LAG>();
         fence_proxy_async_smem();
-        const uint32_t old_stage = (stage + STAGES - GATHER_LAG) % STAGES;
+        const uint32_t old_stage = (stage + G::STAGES - GATHER_LAG) % G::STAGES;
         mbar_arrive(smem_u32(&s.full[old_stage]));
         --pending;
       }
-      if (++stage == STAGES) { stage = 0; phase ^= 1u; }
+      if (++stage == G::STAGES) { stage = 0; phase ^= 1u; }
     }
   }
   // publish what is still pending (also on abort, so the copies are complete)
   cp_async_wait<0>();
   fence_proxy_async_smem();
   for (; pending > 0; --pending) {
-    const uint32_t old_stage = (stage + STAGES - pending) % STAGES;
+    const uint32_t old_stage = (stage + G::STAGES - pending) % G::STAGES;
     mbar_arrive(smem_u32(&s.full[old_stage]));
   }
   if (tid == 0) {
-    for (uint32_t st = 0; st < STAGES; ++st) {
-      const uint32_t fills = issued / STAGES + (st < issued % STAGES ? 1u : 0u);
+    for (uint32_t st = 0; st < G::STAGES; ++st) {
+      const uint32_t fills = issued / G::STAGES + (st < issued % G::STAGES ? 1u : 0u);
       if (fills > 0) wait_bar(smem_u32(&s.full[st]), (fills - 1u) & 1u, c, W_DRAIN, st, false);
     }
   }
 }
 
-// MMA issuer (one thread).
-template <int MODE, int DT>
+// MMA issuer (one thread; with PAIR = 2 only in the even CTA).
+template <int MODE, int DT, int PAIR>
 __device__ void mma_issuer(const KParams& p, const Smem& s, const Ctl& c, uint32_t tmem_base,
                            int total_mt) {
-  constexpr uint32_t IDESC = idesc_f16(DT, BM, BN, 0, 1);
-  ItemIter<MODE> iter(p, total_mt);
+  using G = Geo<PAIR>;
+  constexpr uint32_t IDESC = idesc_f16(DT, BM * PAIR, BN, 0, 1);
+  ItemIter<MODE, PAIR> iter(p, total_mt, 0);
   Work w;
   uint32_t stage = 0, phase = 0;
   int it = 0;
@@ -472,14 +589,16 @@ __device__ void mma_issuer(const KParams& p, const Smem& s, const Ctl& c, uint32
   while (ok && iter.next(w)) {
     const uint32_t b = it & 1;
     const uint32_t use = static_cast<uint32_t>(it >> 1);
-    if (wait_bar(smem_u32(&s.tempty[b]), (use & 1u) ^ 1u, c, W_TEMPTY, b) != 0) break;
+    if ((PAIR == 2 ? wait_bar_remote(smem_u32(&s.tempty[b]), (use & 1u) ^ 1u, c, W_TEMPTY, b)
+                   : wait_bar(smem_u32(&s.tempty[b]), (use & 1u) ^ 1u, c, W_TEMPTY, b)) != 0)
+      break;
     tc_fence_after();
     const uint32_t d = tmem_base + b * BN;
     for (int k = w.k0; k < w.k1; ++k) {
       if (wait_bar(smem_u32(&s.full[stage]), phase, c, W_FULL, stage) != 0) { ok = false; break; }
       tc_fence_after();
       const uint32_t sa = smem_u32(s.a + stage * A_STAGE);
-      const uint32_t sb = smem_u32(s.b + stage * B_STAGE);
+      const uint32_t sb = smem_u32(s.b + stage * G::B_STAGE);
 #pragma unroll
       for (int kk = 0; kk < BK / UK; ++kk) {
         // A: K-major rows of 128 B, 8-row groups 1024 B apart; a 16-wide k step is +32 B.
@@ -487,18 +606,22 @@ __device__ void mma_issuer(const KParams& p, const Smem& s, const Ctl& c, uint32
         // B: N-major; 64-column (128 B) panels BK*128 B apart, 8-k-row groups 1024 B
         // apart; a 16-deep k step is 16 rows = +2048 B.
         const uint64_t bd = sdesc_sw128(sb + kk * UK * 128, BK * 128, 1024);
-        umma_f16(d, ad, bd, IDESC, (k > w.k0 || kk > 0) ? 1u : 0u);
+        if (PAIR == 2) umma2_f16(d, ad, bd, IDESC, (k > w.k0 || kk > 0) ? 1u : 0u);
+        else umma_f16(d, ad, bd, IDESC, (k > w.k0 || kk > 0) ? 1u : 0u);
       }
-      umma_commit(smem_u32(&s.empty[stage]));
+      if (PAIR == 2) umma2_commit_mc(smem_u32(&s.empty[stage]), 0x3);
+      else umma_commit(smem_u32(&s.empty[stage]));
       any = true;
-      if (++stage == STAGES) { stage = 0; phase ^= 1u; }
+      if (++stage == G::STAGES) { stage = 0; phase ^= 1u; }
     }
     if (!ok) break;
-    umma_commit(smem_u32(&s.tfull[b]));
+    if (PAIR == 2) umma2_commit_mc(smem_u32(&s.tfull[b]), 0x3);
+    else umma_commit(smem_u32(&s.tfull[b]));
     ++it;
   }
   if (any) {
-    umma_commit(smem_u32(s.drain));
+    if (PAIR == 2) umma2_commit(smem_u32(s.drain));
+    else umma_commit(smem_u32(s.drain));
     wait_bar(smem_u32(s.drain), 0, c, W_DRAIN, 0, false);
   }
 }
@@ -559,21 +682,27 @@ __device__ __forceinline__ void convert8(float* src, uint16_t* dst) {
   st_cg_f4(src + 4, z);
 }
 
-template <int MODE, int DT>
+template <int MODE, int DT, int PAIR>
 __device__ void epilogue(const KParams& p, const Smem& s, const Ctl& c, uint32_t tmem_base,
-                         int total_mt, int warp) {
+                         int total_mt, int warp, int cta) {
   const int lane = threadIdx.x & 31;
   const int q = warp & 3;  // TMEM lane quarter this warp may access
-  ItemIter<MODE> iter(p, total_mt);
+  ItemIter<MODE, PAIR> iter(p, total_mt, cta);
   Work w;
   int it = 0;
+  // the accumulator-empty barrier lives in the even CTA of a pair
+  const uint32_t tempty0 = (PAIR == 2 && cta != 0) ? mapa_shared(smem_u32(&s.tempty[0]), 0)
+                                                   : smem_u32(&s.tempty[0]);
+  const uint32_t srow = smem_u32(s.stg + q * STG_WARP + lane * STG_PITCH);
   while (iter.next(w)) {
     const uint32_t b = it & 1;
     const uint32_t use = static_cast<uint32_t>(it >> 1);
     // one lane waits so that the whole warp takes the same exit decision
     // before the warp-collective tcgen05.ld below
     int wr = 0;
-    if (lane == 0) wr = wait_bar(smem_u32(&s.tfull[b]), use & 1u, c, W_TFULL, b);
+    if (lane == 0)
+      wr = (PAIR == 2 && cta != 0) ? wait_bar_remote(smem_u32(&s.tfull[b]), use & 1u, c, W_TFULL, b)
+                                   : wait_bar(smem_u32(&s.tfull[b]), use & 1u, c, W_TFULL, b);
     wr = __shfl_sync(0xFFFFFFFFu, wr, 0);
     if (wr != 0) break;
     tc_fence_after();
@@ -590,7 +719,6 @@ __device__ void epilogue(const KParams& p, const Smem& s, const Ctl& c, uint32_t
       tok = slot / p.topk;
       gate = __ldg(p.topk_w + slot);
     }
-    const uint32_t srow = smem_u32(s.stg + q * STG_WARP + lane * STG_PITCH);
     for (int ch = 0; ch < BN / 32; ++ch) {
       if (ch * 32 >= ncols) break;  // warp-uniform
       uint32_t v[32];
@@ -608,7 +736,10 @@ __device__ void epilogue(const KParams& p, const Smem& s, const Ctl& c, uint32_t
     // hand the accumulator back to the MMA warp
     tc_fence_before();
     __syncwarp();
-    if (lane == 0) mbar_arrive(smem_u32(&s.tempty[b]));
+    if (lane == 0) {
+      if (PAIR == 2 && cta != 0) mbar_arrive_remote(tempty0 + b * 8);
+      else mbar_arrive(smem_u32(&s.tempty[b]));
+    }
     ++it;
 
     if (MODE == MODE_REDUCE || MODE == MODE_MOE_SCATTER) {
@@ -617,7 +748,9 @@ __device__ void epilogue(const KParams& p, const Smem& s, const Ctl& c, uint32_t
       fence_proxy_async_global();
     }
     if (MODE == MODE_REDUCE) {
-      // arrival counter of this tile's 32-row quarter counts k-slices
+      // arrival counter of this tile's 32-row quarter counts k-slices; quarters
+      // wholly past the last row have nothing to count
+      if (w.m0 + q * 32 >= w.row_end) continue;
       __threadfence();
       __syncwarp();
       const uint32_t nk = static_cast<uint32_t>(w.k1 - w.k0);
@@ -667,7 +800,7 @@ __device__ void epilogue(const KParams& p, const Smem& s, const Ctl& c, uint32_t
 }
 
 // ---------------------------------------------------------------- kernel
-template <int MODE, int DT>
+template <int MODE, int DT, int PAIR>
 struct KernelShape {
   static constexpr int PRODUCER_WARPS = (MODE == MODE_MOE_GATHER) ? 4 : 1;
   static constexpr int MMA_WARP = PRODUCER_WARPS;
@@ -676,26 +809,29 @@ struct KernelShape {
   static constexpr int FULL_COUNT = (MODE == MODE_MOE_GATHER) ? (BM + 1) : 1;
 };
 
-template <int MODE, int DT>
-__global__ void __launch_bounds__(KernelShape<MODE, DT>::THREADS, 1)
+template <int MODE, int DT, int PAIR>
+__global__ void __launch_bounds__(KernelShape<MODE, DT, PAIR>::THREADS, 1)
 fused_gemm_kernel(const __grid_constant__ KParams p) {
-  using KS = KernelShape<MODE, DT>;
+  using KS = KernelShape<MODE, DT, PAIR>;
+  using G = Geo<PAIR>;
+  static_assert(PAIR == 1 || (MODE == MODE_STORE || MODE == MODE_REDUCE), "pairs: dense modes");
   extern __shared__ uint8_t smem_raw[];
   uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
   Smem s;
   s.a = base;
-  s.b = base + STAGES * A_STAGE;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(base + STAGES * (A_STAGE + B_STAGE));
+  s.b = base + G::STAGES * A_STAGE;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(base + G::STAGES * (A_STAGE + G::B_STAGE));
   s.full = bars;
-  s.empty = bars + STAGES;
-  s.tfull = bars + 2 * STAGES;
-  s.tempty = bars + 2 * STAGES + 2;
-  s.drain = bars + 2 * STAGES + 4;
-  s.tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * STAGES + 5);
-  s.stg = base + STAGES * (A_STAGE + B_STAGE) + 256;
+  s.empty = bars + G::STAGES;
+  s.tfull = bars + 2 * G::STAGES;
+  s.tempty = bars + 2 * G::STAGES + 2;
+  s.drain = bars + 2 * G::STAGES + 4;
+  s.tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * G::STAGES + 5);
+  s.stg = base + G::STAGES * (A_STAGE + G::B_STAGE) + 512;
 
   const int warp = threadIdx.x >> 5;
+  const int cta = PAIR == 2 ? static_cast<int>(cluster_ctarank()) : 0;
   Ctl c;
   c.hdr = p.hdr;
   c.seq = p.seq;
@@ -703,47 +839,62 @@ fused_gemm_kernel(const __grid_constant__ KParams p) {
   c.pipe_timeout = 2 * p.timeout_ns + 10000000ull;
 
   if (threadIdx.x == 0) {
-    for (int i = 0; i < STAGES; ++i) {
+    for (int i = 0; i < G::STAGES; ++i) {
       mbar_init(smem_u32(&s.full[i]), KS::FULL_COUNT);
       mbar_init(smem_u32(&s.empty[i]), 1);
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(smem_u32(&s.tfull[i]), 1);
-      mbar_init(smem_u32(&s.tempty[i]), EPI_WARPS);
+      mbar_init(smem_u32(&s.tempty[i]), EPI_WARPS * PAIR);
     }
     mbar_init(smem_u32(s.drain), 1);
     fence_mbar_init();
   }
   if (warp == KS::MMA_WARP) {
-    tmem_alloc(smem_u32(s.tmem_slot), TMEM_COLS);
-    tmem_relinquish();
+    if (PAIR == 2) {
+      tmem_alloc2(smem_u32(s.tmem_slot), TMEM_COLS);
+      tmem_relinquish2();
+    } else {
+      tmem_alloc(smem_u32(s.tmem_slot), TMEM_COLS);
+      tmem_relinquish();
+    }
   }
   tc_fence_before();
   __syncthreads();
+  if (PAIR == 2) cluster_sync();  // peer barriers initialised and TMEM allocated in both CTAs
   tc_fence_after();
   const uint32_t tmem_base = *s.tmem_slot;
 
   int total_mt = 0;
   if (MODE == MODE_MOE_GATHER || MODE == MODE_MOE_SCATTER) total_mt = __ldg(p.tile_off + p.E);
 
+  const int lane = threadIdx.x & 31;
+  if (warp == 0 && lane < p.R) {
+    // bring this call's tensor maps into the TMA descriptor cache
+    tma_prefetch_desc(&p.tmB[lane]);
+    if (MODE != MODE_MOE_GATHER) tma_prefetch_desc(&p.tmA[lane]);
+  }
   if (warp < KS::PRODUCER_WARPS) {
     if (MODE == MODE_MOE_GATHER) {
       producer_gather<KS::PRODUCER_WARPS * 32>(p, s, c, total_mt);
-    } else if ((threadIdx.x & 31) == 0) {
-      producer_tma<MODE>(p, s, c, total_mt);
+    } else if (lane == 0) {
+      producer_tma<MODE, PAIR>(p, s, c, total_mt, cta);
     }
   } else if (warp == KS::MMA_WARP) {
-    if ((threadIdx.x & 31) == 0) mma_issuer<MODE, DT>(p, s, c, tmem_base, total_mt);
+    // the even CTA of a pair issues the MMAs for both
+    if (lane == 0 && cta == 0) mma_issuer<MODE, DT, PAIR>(p, s, c, tmem_base, total_mt);
     __syncwarp();
   } else {
-    epilogue<MODE, DT>(p, s, c, tmem_base, total_mt, warp);
+    epilogue<MODE, DT, PAIR>(p, s, c, tmem_base, total_mt, warp, cta);
   }
 
   tc_fence_before();
   __syncthreads();
+  if (PAIR == 2) cluster_sync();  // no CTA frees TMEM or leaves while its peer still works
   if (warp == KS::MMA_WARP) {
     tc_fence_after();
-    tmem_dealloc(tmem_base, TMEM_COLS);
+    if (PAIR == 2) tmem_dealloc2(tmem_base, TMEM_COLS);
+    else tmem_dealloc(tmem_base, TMEM_COLS);
   }
 }
 

@@ -1,0 +1,102 @@
+// Host-side launch of one instantiation of the fused kernel: sets the shared
+// memory attribute once, sizes CTA-pair grids to the clusters that fit at
+// once, and launches on the caller's stream.
+#pragma once
+
+#include <cstdio>
+#include <cstdlib>
+#include <mutex>
+
+#include "flux_host.h"
+#include "flux_kernels.cuh"
+
+namespace flux {
+
+// FLUX_DEBUG=1 in the environment prints each launch's configuration to stderr.
+inline bool debug_enabled() {
+  static const bool on = [] {
+    const char* v = std::getenv("FLUX_DEBUG");
+    return v != nullptr && v[0] != '\0' && v[0] != '0';
+  }();
+  return on;
+}
+
+template <int MODE, int DT, int PAIR>
+struct Launcher {
+  // Largest grid (CTAs) that is resident at once; 0 on error.
+  static int max_ctas(const DeviceInfo& dev) {
+    static std::once_flag once;
+    static cudaError_t err = cudaSuccess;
+    static int ctas = 0;
+    std::call_once(once, [&dev] {
+      err = cudaFuncSetAttribute(fused_gemm_kernel<MODE, DT, PAIR>,
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+      if (err != cudaSuccess) return;
+      if (PAIR == 1) {
+        ctas = dev.sm_count;
+        return;
+      }
+      cudaLaunchConfig_t cfg = {};
+      cfg.gridDim = dim3(2 * (dev.sm_count / 2), 1, 1);
+      cfg.blockDim = dim3(KernelShape<MODE, DT, PAIR>::THREADS, 1, 1);
+      cfg.dynamicSmemBytes = SMEM_BYTES;
+      cudaLaunchAttribute attr[1];
+      attr[0].id = cudaLaunchAttributeClusterDimension;
+      attr[0].val.clusterDim.x = PAIR;
+      attr[0].val.clusterDim.y = 1;
+      attr[0].val.clusterDim.z = 1;
+      cfg.attrs = attr;
+      cfg.numAttrs = 1;
+      int clusters = 0;
+      err = cudaOccupancyMaxActiveClusters(&clusters, fused_gemm_kernel<MODE, DT, PAIR>, &cfg);
+      ctas = clusters * PAIR;
+      if (debug_enabled())
+        std::fprintf(stderr, "[flux] mode %d dtype %d pair %d: %d clusters resident at once\n",
+                     MODE, DT, PAIR, clusters);
+    });
+    if (err != cudaSuccess) {
+      cuda_fail(err);
+      return 0;
+    }
+    return ctas;
+  }
+
+  static flux_status_t launch(const KParams& p, int grid, cudaStream_t stream) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid, 1, 1);
+    cfg.blockDim = dim3(KernelShape<MODE, DT, PAIR>::THREADS, 1, 1);
+    cfg.dynamicSmemBytes = SMEM_BYTES;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = PAIR;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = PAIR > 1 ? 1 : 0;
+    if (debug_enabled())
+      std::fprintf(stderr,
+                   "[flux] mode %d dtype %d pair %d: grid %d x %d threads, %d B smem, units %d, "
+                   "tiles %d x %d, k-slices %d, stream-k %d\n",
+                   MODE, DT, PAIR, grid, KernelShape<MODE, DT, PAIR>::THREADS, SMEM_BYTES,
+                   p.num_units, p.Mt, p.Nt, p.KT, p.stream_k);
+    cudaError_t e = cudaLaunchKernelEx(&cfg, fused_gemm_kernel<MODE, DT, PAIR>, p);
+    return e == cudaSuccess ? FLUX_OK : cuda_fail(e);
+  }
+};
+
+// Grid for `units` work units of PAIR CTAs each, capped at the resident CTAs
+// (or opts->num_ctas); a multiple of PAIR, at least PAIR.
+template <int MODE, int DT, int PAIR>
+int grid_for(const DeviceInfo& dev, const flux_opts_t* opts, long long units) {
+  int cap = Launcher<MODE, DT, PAIR>::max_ctas(dev);
+  if (cap <= 0) return 0;
+  if (opts && opts->num_ctas > 0 && opts->num_ctas < cap) cap = opts->num_ctas;
+  long long g = units * PAIR;
+  if (g > cap) g = cap;
+  g -= g % PAIR;
+  if (g < PAIR) g = PAIR;
+  return static_cast<int>(g);
+}
+
+}  // namespace flux

@@ -5,6 +5,7 @@
 
 #include "flux_host.h"
 #include "flux_kernels.cuh"
+#include "flux_launch.cuh"
 
 namespace flux {
 
@@ -124,24 +125,16 @@ __global__ void tile_offsets_kernel(const int32_t* offsets, int E, int32_t* tile
 
 namespace {
 
-template <int MODE, int DT>
-flux_status_t launch(const KParams& p, int grid, cudaStream_t stream) {
-  using KS = KernelShape<MODE, DT>;
-  static std::once_flag once;
-  static cudaError_t attr_err = cudaSuccess;
-  std::call_once(once, [] {
-    attr_err = cudaFuncSetAttribute(fused_gemm_kernel<MODE, DT>,
-                                    cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
-  });
-  if (attr_err != cudaSuccess) return cuda_fail(attr_err);
-  fused_gemm_kernel<MODE, DT><<<grid, KS::THREADS, SMEM_BYTES, stream>>>(p);
-  cudaError_t e = cudaGetLastError();
-  return e == cudaSuccess ? FLUX_OK : cuda_fail(e);
+template <int MODE>
+flux_status_t launch_dt(flux_dtype_t dt, const KParams& p, int grid, cudaStream_t s) {
+  return dt == FLUX_BF16 ? Launcher<MODE, 1, 1>::launch(p, grid, s)
+                         : Launcher<MODE, 0, 1>::launch(p, grid, s);
 }
 
 template <int MODE>
-flux_status_t launch_dt(flux_dtype_t dt, const KParams& p, int grid, cudaStream_t s) {
-  return dt == FLUX_BF16 ? launch<MODE, 1>(p, grid, s) : launch<MODE, 0>(p, grid, s);
+int grid_dt(flux_dtype_t dt, const DeviceInfo& dev, const flux_opts_t* opts, long long units) {
+  return dt == FLUX_BF16 ? grid_for<MODE, 1, 1>(dev, opts, units)
+                         : grid_for<MODE, 0, 1>(dev, opts, units);
 }
 
 bool moe_shape_ok(int R, int T, int H, int F, int E, int topk) {
@@ -294,9 +287,9 @@ extern "C" flux_status_t flux_moe_ag_grouped_gemm(
   p.hdr = static_cast<uint32_t*>(workspace);
   const long long max_units =
       (static_cast<long long>((n + BM - 1) / BM) + E) * p.Nt * static_cast<long long>(R);
-  int grid = (opts && opts->num_ctas > 0) ? opts->num_ctas : dev.sm_count;
-  if (max_units < grid) grid = static_cast<int>(max_units);
-  return launch_dt<MODE_MOE_GATHER>(dtype, p, grid < 1 ? 1 : grid, s);
+  const int grid = grid_dt<MODE_MOE_GATHER>(dtype, dev, opts, max_units);
+  if (grid == 0) return FLUX_ERR_CUDA;
+  return launch_dt<MODE_MOE_GATHER>(dtype, p, grid, s);
 }
 
 extern "C" flux_status_t flux_moe_grouped_gemm_rs(
@@ -383,7 +376,7 @@ extern "C" flux_status_t flux_moe_grouped_gemm_rs(
   p.hdr = static_cast<uint32_t*>(workspace);
   const long long max_units =
       (static_cast<long long>((n + BM - 1) / BM) + E) * p.Nt * static_cast<long long>(R);
-  int grid = (opts && opts->num_ctas > 0) ? opts->num_ctas : dev.sm_count;
-  if (max_units < grid) grid = static_cast<int>(max_units);
-  return launch_dt<MODE_MOE_SCATTER>(dtype, p, grid < 1 ? 1 : grid, s);
+  const int grid = grid_dt<MODE_MOE_SCATTER>(dtype, dev, opts, max_units);
+  if (grid == 0) return FLUX_ERR_CUDA;
+  return launch_dt<MODE_MOE_SCATTER>(dtype, p, grid, s);
 }
