@@ -127,11 +127,11 @@ class Step:
         self.torch, self.fx, self.dev = torch, fx, dev
         C = configs.CONFIGS
         ag, rs, dec, moe = C["ag_mlp0"], C["rs_mlp1"], C["rs_decode"], C["moe"]
-        if small:  # same structure, reduced sizes (profiling captures)
-            ag = configs.small(ag, M=1024, N=8192, K=4096)
-            rs = configs.small(rs, M=1024, N=4096, K=8192)
-            dec = configs.small(dec, N=4096, K=14336)
-            moe = configs.small(moe, T=1024, H=2048, F=4096)
+        if small:  # same structure, reduced sizes with >= 5 waves per op (profiling captures)
+            ag = configs.small(ag, N=8 * 768, K=8192)
+            rs = configs.small(rs, N=3072, K=8 * 2048)
+            dec = configs.small(dec, K=8 * 1792)
+            moe = configs.small(moe, T=2048, F=8 * 896)
         self.ag, self.rs, self.dec, self.moe = ag, rs, dec, moe
         t0 = time.time()
         xs, w1 = configs.ag_inputs(ag)
@@ -505,10 +505,10 @@ def main():
     ap.add_argument("--ops", default="", help="comma list of ops to run (default: the whole step)")
     ap.add_argument("--no-overhead", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--cpu-rows", type=int, default=128)
-    ap.add_argument("--cpu-cols", type=int, default=4096)
-    ap.add_argument("--cpu-tokens", type=int, default=512)
-    ap.add_argument("--cpu-fcols", type=int, default=512)
+    ap.add_argument("--cpu-rows", type=int, default=512)
+    ap.add_argument("--cpu-cols", type=int, default=8192)
+    ap.add_argument("--cpu-tokens", type=int, default=2048)
+    ap.add_argument("--cpu-fcols", type=int, default=1024)
     ap.add_argument("--ref-rows", type=int, default=32)
     ap.add_argument("--ref-cols", type=int, default=512)
     ap.add_argument("--ref-tokens", type=int, default=128)
