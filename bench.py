@@ -61,6 +61,19 @@ def peaks():
         return {"hbm": 6800.0, "tc": 1900.0, "tc_sus": 1700.0, "src": "fallback"}
 
 
+def max_over_ranks(value: float) -> float:
+    """Largest `value` over the ranks of the default process group (or `value`
+    itself without one).  The only collective of the benchmark: the timing of
+    independent per-GPU replicas is reduced on the host."""
+    import torch
+    import torch.distributed as td
+    if not (td.is_available() and td.is_initialized()) or td.get_world_size() == 1:
+        return value
+    t = torch.tensor([value], dtype=torch.float64)
+    td.all_reduce(t, op=td.ReduceOp.MAX)
+    return float(t.item())
+
+
 def dist_env():
     ws = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -291,10 +304,7 @@ def run_ours(args):
         for o in st.ops:
             per_op[o] += ev[o][0].elapsed_time(ev[o][1])
     st.check_status()
-    if ws_ > 1:
-        t = torch.tensor([ms_total], dtype=torch.float64)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        ms_total = float(t.item())
+    ms_total = max_over_ranks(ms_total)
     ms_step = ms_total / args.steps
     flops = st.total_flops()
     value = flops * ws_ / (ms_step * 1e-3) / 1e12
