@@ -103,13 +103,13 @@ extern "C" flux_status_t flux_ag_gemm(int R, int M, int N, int K, flux_dtype_t d
       return st;
     p.out[r] = out[r];
   }
-  constexpr int PAIR = 2;  // 256 x 256 tiles on CTA pairs
+  constexpr int PAIR = 2;  // 256 x 512 tiles on CTA pairs
   p.R = R;
   p.M = M;
   p.N = Nr;
   p.K = K;
   p.Mt = (M + Geo<PAIR>::TILE_M - 1) / Geo<PAIR>::TILE_M;
-  p.Nt = (Nr + BN - 1) / BN;
+  p.Nt = (Nr + Geo<PAIR>::TILE_N - 1) / Geo<PAIR>::TILE_N;
   p.KT = (K + BK - 1) / BK;
   p.ldo = Nr;
   p.rows_per_rank = rows;
@@ -170,7 +170,6 @@ extern "C" flux_status_t flux_gemm_rs(int R, int M, int N, int K, flux_dtype_t d
   p.M = M;
   p.N = N;
   p.K = Kr;
-  p.Nt = (N + BN - 1) / BN;
   p.KT = (Kr + BK - 1) / BK;
   p.ldo = N;
   p.rows_per_rank = rows;
@@ -180,13 +179,14 @@ extern "C" flux_status_t flux_gemm_rs(int R, int M, int N, int K, flux_dtype_t d
   p.acc = reinterpret_cast<float*>(ws + WS_HEADER + rs_counter_bytes(M, N));
   fill_common(p, opts, workspace);
 
-  // Few tiles per SM (decode shapes): single-CTA 128-row tiles and an equal
+  // Few tiles per SM (decode shapes): single-CTA 128 x 256 tiles and an equal
   // contiguous range of k-slices per CTA (tiles split along K add into the same
-  // fp32 owner tile).  Otherwise: whole 256 x 256 tiles on CTA pairs, strided
+  // fp32 owner tile).  Otherwise: whole 256 x 512 tiles on CTA pairs, strided
   // over a persistent grid.
   const int sm = (opts && opts->num_ctas > 0) ? opts->num_ctas : dev.sm_count;
-  const long long units128 = static_cast<long long>((M + BM - 1) / BM) * p.Nt * R;
+  const long long units128 = static_cast<long long>((M + BM - 1) / BM) * ((N + BN - 1) / BN) * R;
   if (units128 < 4 * sm) {
+    p.Nt = (N + BN - 1) / BN;
     p.Mt = (M + BM - 1) / BM;
     p.num_units = p.Mt * p.Nt * R;
     p.total_ksteps = static_cast<long long>(p.num_units) * p.KT;
@@ -200,6 +200,7 @@ extern "C" flux_status_t flux_gemm_rs(int R, int M, int N, int K, flux_dtype_t d
     return launch_dt<MODE_REDUCE, 1>(dtype, p, grid, s);
   }
   constexpr int PAIR = 2;
+  p.Nt = (N + Geo<PAIR>::TILE_N - 1) / Geo<PAIR>::TILE_N;
   p.Mt = (M + Geo<PAIR>::TILE_M - 1) / Geo<PAIR>::TILE_M;
   const int tiles = p.Mt * p.Nt;
   p.num_units = tiles * R;

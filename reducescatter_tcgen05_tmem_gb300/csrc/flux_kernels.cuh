@@ -19,16 +19,21 @@
 //                                    the last of R*topk contributions converts (MoE layer1)
 //
 // PAIR = 1: one CTA computes a 128 x 256 tile with tcgen05.mma.cta_group::1
-//           (4-stage ring of 48 KB: A 128x64 + B 64x256).
-// PAIR = 2: a cluster of two CTAs computes a 256 x 256 tile with
-//           tcgen05.mma.cta_group::2 issued by the even CTA.  Each CTA holds
-//           its own 128 rows of A and its own 128 columns of B (6-stage ring
-//           of 32 KB), so every SM streams two thirds of the operand bytes of
-//           the PAIR = 1 tile per unit of tensor work.  Both CTAs' TMA loads
-//           complete on the even CTA's "full" barrier, whose producer expects
-//           the bytes of both.  Commits are multicast to both CTAs' "empty"
-//           and "accumulator full" barriers; both CTAs' epilogue warps arrive
-//           on the even CTA's "accumulator empty" barrier.
+//           (4-stage ring of 48 KB: A 128x64 + B 64x256); two 256-column
+//           accumulators, so the epilogue of one tile overlaps the next.
+// PAIR = 2: a cluster of two CTAs computes a 256 x 512 tile with two
+//           tcgen05.mma.cta_group::2 (M 256, N 256) per 16-deep k step, issued
+//           by the even CTA.  Each CTA holds its own 128 rows of A and, of each
+//           256-column half of the tile, its own 128 columns of B (4-stage ring
+//           of 48 KB).  Per unit of tensor work an SM then requests half the
+//           operand bytes of the PAIR = 1 tile: the load path (TMA requests in
+//           flight per SM), not the tensor pipe, is what bounds these kernels.
+//           The 128 x 512 fp32 accumulator of a CTA fills all 512 TMEM
+//           columns, so the MMAs of the next tile wait for the epilogue.
+//           Both CTAs' TMA loads complete on the even CTA's "full" barrier,
+//           whose producer expects the bytes of both.  Commits are multicast
+//           to both CTAs' "empty" and "accumulator full" barriers; both CTAs'
+//           epilogue warps arrive on the even CTA's "accumulator empty" barrier.
 //
 // Every wait is bounded: after timeout_ns (or an iteration cap) the thread
 // records FLUX_ERR_TIMEOUT in the workspace header, raises the per-call abort
@@ -45,7 +50,7 @@ constexpr int BK = 64;   // k-slice per pipeline stage (one 128-byte swizzle row
 constexpr int UK = 16;   // K of one tcgen05.mma kind::f16
 constexpr int A_STAGE = BM * BK * 2;  // 16 KB
 constexpr int B_BOX_N = 64;           // 64 columns = 128 bytes, one swizzle span
-constexpr int TMEM_COLS = 2 * BN;     // two fp32 accumulators
+constexpr int TMEM_COLS = 2 * BN;     // all 512 TMEM columns: fp32 accumulators
 constexpr int MAXR = 16;
 constexpr int EPI_WARPS = 4;
 constexpr int GATHER_LAG = 2;         // cp.async groups in flight before a stage is published
@@ -58,15 +63,42 @@ constexpr int STG_WARP = 32 * STG_PITCH;
 
 template <int PAIR>
 struct Geo {
-  static constexpr int STAGES = PAIR == 2 ? 6 : 4;
-  static constexpr int B_COLS = BN / PAIR;             // B columns held by one CTA
-  static constexpr int B_BOXES = B_COLS / B_BOX_N;
-  static constexpr int B_STAGE = B_COLS * BK * 2;      // 16 KB or 32 KB
+  static constexpr int STAGES = 4;
   static constexpr int TILE_M = BM * PAIR;             // rows of one scheduled tile
+  static constexpr int TILE_N = BN * PAIR;             // columns of one scheduled tile
+  static constexpr int N_MMA = PAIR;                   // N = 256 MMAs per 16-deep k step
+  static constexpr int B_BOXES = 4;                    // 64-column B boxes per CTA and stage
+  static constexpr int B_STAGE = B_BOXES * B_BOX_N * BK * 2;  // 32 KB
+  static constexpr int ACC_BUFS = 2 / PAIR;            // accumulators in the 512 TMEM columns
+  static constexpr int ACC_COLS = TILE_N;              // TMEM columns of one accumulator
   static constexpr int SMEM = STAGES * (A_STAGE + B_STAGE) + 1024 /*align*/ + 512 /*barriers*/ +
                               EPI_WARPS * STG_WARP;
 };
 constexpr int SMEM_BYTES = Geo<1>::SMEM > Geo<2>::SMEM ? Geo<1>::SMEM : Geo<2>::SMEM;
+static_assert(Geo<1>::ACC_BUFS * Geo<1>::ACC_COLS == TMEM_COLS, "TMEM budget");
+static_assert(Geo<2>::ACC_BUFS * Geo<2>::ACC_COLS == TMEM_COLS, "TMEM budget");
+
+// First output column of B box j (0..3) of CTA `cta` in a tile starting at
+// column n0.  A single CTA holds columns n0 .. n0+255 in order; a pair splits
+// each 256-column half h of its tile, CTA c holding n0 + 256h + 128c + [0, 128),
+// so that the two halves of one N = 256 MMA sit at the same shared-memory
+// offset in both CTAs.
+template <int PAIR>
+__device__ __forceinline__ int b_box_col(int n0, int cta, int j) {
+  return PAIR == 2 ? n0 + (j >> 1) * BN + cta * (BN / 2) + (j & 1) * B_BOX_N : n0 + j * B_BOX_N;
+}
+
+// Boxes (bit j) that start inside the N columns; the others are not loaded
+// (their shared-memory slots keep stale data that only feeds columns >= N,
+// which are never stored).
+template <int PAIR>
+__device__ __forceinline__ uint32_t b_box_mask(int N, int n0, int cta) {
+  uint32_t m = 0;
+#pragma unroll
+  for (int j = 0; j < 4; ++j)
+    if (b_box_col<PAIR>(n0, cta, j) < N) m |= 1u << j;
+  return m;
+}
 
 enum Mode { MODE_STORE = 0, MODE_REDUCE = 1, MODE_MOE_GATHER = 2, MODE_MOE_SCATTER = 3 };
 
@@ -387,7 +419,7 @@ struct Smem {
 };
 
 // Bytes the odd CTA of a pair loads for one stage of work item `w` (the even
-// CTA's view of the item): its 128 rows of A and its 128 columns of B.
+// CTA's view of the item): its 128 rows of A and its 256 columns of B.
 template <int MODE>
 __device__ __forceinline__ uint32_t pair_peer_bytes(const KParams& p, const Work& w) {
   const int m0 = w.m0 + BM;
@@ -395,9 +427,8 @@ __device__ __forceinline__ uint32_t pair_peer_bytes(const KParams& p, const Work
   uint32_t a = nbox_a * A_STAGE;
   if (MODE == MODE_STORE && nbox_a)
     a = ((min(m0 + BM, w.row_end) - m0 + p.a_box_m - 1) / p.a_box_m) * p.a_box_m * BK * 2;
-  const int n_cta = w.nt * BN + Geo<2>::B_COLS;
-  const int nbox_b = max(0, min(Geo<2>::B_BOXES, (p.N - n_cta + B_BOX_N - 1) / B_BOX_N));
-  return a + nbox_b * B_BOX_N * BK * 2;
+  const uint32_t mask = b_box_mask<2>(p.N, w.nt * Geo<2>::TILE_N, 1);
+  return a + __popc(mask) * B_BOX_N * BK * 2;
 }
 
 // TMA producer (one thread).
@@ -429,10 +460,10 @@ __device__ void producer_tma(const KParams& p, const Smem& s, const Ctl& c, int 
         nbox_a = (min(w.m0 + BM, w.row_end) - w.m0 + p.a_box_m - 1) / p.a_box_m;
       }
     }
-    const int n_cta = w.nt * BN + cta * G::B_COLS;  // first B column this CTA loads
-    const int nbox_b = max(0, min(G::B_BOXES, (p.N - n_cta + B_BOX_N - 1) / B_BOX_N));
+    const int n0 = w.nt * G::TILE_N;
+    const uint32_t bmask = b_box_mask<PAIR>(p.N, n0, cta);
     uint32_t bytes = ((MODE == MODE_STORE) ? nbox_a * p.a_box_m * BK * 2 : nbox_a * A_STAGE) +
-                     nbox_b * B_BOX_N * BK * 2;
+                     __popc(bmask) * B_BOX_N * BK * 2;
     if (PAIR == 2 && cta == 0) {
       // the even CTA's barrier also counts the odd CTA's bytes of the same stage
       bytes += pair_peer_bytes<MODE>(p, w);
@@ -463,8 +494,9 @@ __device__ void producer_tma(const KParams& p, const Smem& s, const Ctl& c, int 
         if (PAIR == 2) tma_load_2d_pair(sa, &p.tmA[w.r], fbc, kc, w.m0);
         else tma_load_2d(sa, &p.tmA[w.r], fb, kc, w.m0);
       }
-      for (int j = 0; j < nbox_b; ++j) {
-        const int n = n_cta + j * B_BOX_N;
+      for (int j = 0; j < G::B_BOXES; ++j) {
+        if (!((bmask >> j) & 1u)) continue;
+        const int n = b_box_col<PAIR>(n0, cta, j);
         if (MODE == MODE_MOE_SCATTER)
           tma_load_3d(sb + j * B_BOX_N * BK * 2, &p.tmB[w.r], fb, n, kc, w.e);
         else if (PAIR == 2)
@@ -587,13 +619,13 @@ __device__ void mma_issuer(const KParams& p, const Smem& s, const Ctl& c, uint32
   bool any = false;
   bool ok = true;
   while (ok && iter.next(w)) {
-    const uint32_t b = it & 1;
-    const uint32_t use = static_cast<uint32_t>(it >> 1);
+    const uint32_t b = it % G::ACC_BUFS;
+    const uint32_t use = static_cast<uint32_t>(it / G::ACC_BUFS);
     if ((PAIR == 2 ? wait_bar_remote(smem_u32(&s.tempty[b]), (use & 1u) ^ 1u, c, W_TEMPTY, b)
                    : wait_bar(smem_u32(&s.tempty[b]), (use & 1u) ^ 1u, c, W_TEMPTY, b)) != 0)
       break;
     tc_fence_after();
-    const uint32_t d = tmem_base + b * BN;
+    const uint32_t d = tmem_base + b * G::ACC_COLS;
     for (int k = w.k0; k < w.k1; ++k) {
       if (wait_bar(smem_u32(&s.full[stage]), phase, c, W_FULL, stage) != 0) { ok = false; break; }
       tc_fence_after();
@@ -603,11 +635,17 @@ __device__ void mma_issuer(const KParams& p, const Smem& s, const Ctl& c, uint32
       for (int kk = 0; kk < BK / UK; ++kk) {
         // A: K-major rows of 128 B, 8-row groups 1024 B apart; a 16-wide k step is +32 B.
         const uint64_t ad = sdesc_sw128(sa + kk * UK * 2, 16, 1024);
-        // B: N-major; 64-column (128 B) panels BK*128 B apart, 8-k-row groups 1024 B
-        // apart; a 16-deep k step is 16 rows = +2048 B.
-        const uint64_t bd = sdesc_sw128(sb + kk * UK * 128, BK * 128, 1024);
-        if (PAIR == 2) umma2_f16(d, ad, bd, IDESC, (k > w.k0 || kk > 0) ? 1u : 0u);
-        else umma_f16(d, ad, bd, IDESC, (k > w.k0 || kk > 0) ? 1u : 0u);
+        const uint32_t acc = (k > w.k0 || kk > 0) ? 1u : 0u;
+#pragma unroll
+        for (int h = 0; h < G::N_MMA; ++h) {
+          // B: N-major; 64-column (128 B) panels BK*128 B apart, 8-k-row groups
+          // 1024 B apart; a 16-deep k step is 16 rows = +2048 B.  MMA h of a
+          // pair reads panels 2h, 2h+1 and writes TMEM columns 256h ..
+          const uint64_t bd =
+              sdesc_sw128(sb + h * (BN / PAIR) * BK * 2 + kk * UK * 128, BK * 128, 1024);
+          if (PAIR == 2) umma2_f16(d + h * BN, ad, bd, IDESC, acc);
+          else umma_f16(d + h * BN, ad, bd, IDESC, acc);
+        }
       }
       if (PAIR == 2) umma2_commit_mc(smem_u32(&s.empty[stage]), 0x3);
       else umma_commit(smem_u32(&s.empty[stage]));
@@ -694,9 +732,10 @@ __device__ void epilogue(const KParams& p, const Smem& s, const Ctl& c, uint32_t
   const uint32_t tempty0 = (PAIR == 2 && cta != 0) ? mapa_shared(smem_u32(&s.tempty[0]), 0)
                                                    : smem_u32(&s.tempty[0]);
   const uint32_t srow = smem_u32(s.stg + q * STG_WARP + lane * STG_PITCH);
+  using G = Geo<PAIR>;
   while (iter.next(w)) {
-    const uint32_t b = it & 1;
-    const uint32_t use = static_cast<uint32_t>(it >> 1);
+    const uint32_t b = it % G::ACC_BUFS;
+    const uint32_t use = static_cast<uint32_t>(it / G::ACC_BUFS);
     // one lane waits so that the whole warp takes the same exit decision
     // before the warp-collective tcgen05.ld below
     int wr = 0;
@@ -708,9 +747,9 @@ __device__ void epilogue(const KParams& p, const Smem& s, const Ctl& c, uint32_t
     tc_fence_after();
     const int row = w.m0 + q * 32 + lane;  // row of the A row space held by this thread
     const bool row_ok = row < w.row_end;
-    const uint32_t taddr = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + b * BN;
-    const int n0 = w.nt * BN;
-    const int ncols = min(BN, p.N - n0);
+    const uint32_t taddr = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + b * G::ACC_COLS;
+    const int n0 = w.nt * G::TILE_N;
+    const int ncols = min(G::TILE_N, p.N - n0);
     // per-row routing data
     float gate = 1.0f;
     int tok = 0;
@@ -719,7 +758,7 @@ __device__ void epilogue(const KParams& p, const Smem& s, const Ctl& c, uint32_t
       tok = slot / p.topk;
       gate = __ldg(p.topk_w + slot);
     }
-    for (int ch = 0; ch < BN / 32; ++ch) {
+    for (int ch = 0; ch < G::TILE_N / 32; ++ch) {
       if (ch * 32 >= ncols) break;  // warp-uniform
       uint32_t v[32];
       tmem_ld_32x32b_x32(taddr + ch * 32, v);
@@ -761,15 +800,18 @@ __device__ void epilogue(const KParams& p, const Smem& s, const Ctl& c, uint32_t
       old = __shfl_sync(0xFFFFFFFFu, old, 0);
       if (old + nk == target) {
         __threadfence();
-        const int col = n0 + lane * 8;
         for (int i = 0; i < 32; ++i) {
           const int grow = w.m0 + q * 32 + i;
           if (grow >= w.row_end) break;
           const int o = grow / p.rows_per_rank;
           const int lr = grow - o * p.rows_per_rank;
-          if (col < p.N)
-            convert8<DT>(p.acc + static_cast<long long>(grow) * p.N + col,
-                         static_cast<uint16_t*>(p.out[o]) + static_cast<long long>(lr) * p.ldo + col);
+#pragma unroll
+          for (int c0 = 0; c0 < G::TILE_N; c0 += 256) {
+            const int col = n0 + c0 + lane * 8;
+            if (col < p.N)
+              convert8<DT>(p.acc + static_cast<long long>(grow) * p.N + col,
+                           static_cast<uint16_t*>(p.out[o]) + static_cast<long long>(lr) * p.ldo + col);
+          }
         }
         if (lane == 0) atomicExch(cnt, 0u);
       }
