@@ -8,17 +8,22 @@
 namespace flux {
 namespace {
 
-template <int MODE, int PAIR>
+template <int MODE, int CL>
 flux_status_t launch_dt(flux_dtype_t dt, const KParams& p, int grid, cudaStream_t s) {
-  return dt == FLUX_BF16 ? Launcher<MODE, 1, PAIR>::launch(p, grid, s)
-                         : Launcher<MODE, 0, PAIR>::launch(p, grid, s);
+  return dt == FLUX_BF16 ? Launcher<MODE, 1, CL>::launch(p, grid, s)
+                         : Launcher<MODE, 0, CL>::launch(p, grid, s);
 }
 
-template <int MODE, int PAIR>
+template <int MODE, int CL>
 int grid_dt(flux_dtype_t dt, const DeviceInfo& dev, const flux_opts_t* opts, long long units) {
-  return dt == FLUX_BF16 ? grid_for<MODE, 1, PAIR>(dev, opts, units)
-                         : grid_for<MODE, 0, PAIR>(dev, opts, units);
+  return dt == FLUX_BF16 ? grid_for<MODE, 1, CL>(dev, opts, units)
+                         : grid_for<MODE, 0, CL>(dev, opts, units);
 }
+
+// Dense whole-tile kernels run on clusters of two CTA pairs stacked along M
+// (512 x 512 per cluster, B multicast between the pairs).
+constexpr int DENSE_CL = 4;
+using DenseGeo = Geo<Unit<DENSE_CL>::PAIR>;
 
 bool valid_dtype(flux_dtype_t dt) { return dt == FLUX_F16 || dt == FLUX_BF16; }
 
@@ -103,13 +108,12 @@ extern "C" flux_status_t flux_ag_gemm(int R, int M, int N, int K, flux_dtype_t d
       return st;
     p.out[r] = out[r];
   }
-  constexpr int PAIR = 2;  // 256 x 512 tiles on CTA pairs
   p.R = R;
   p.M = M;
   p.N = Nr;
   p.K = K;
-  p.Mt = (M + Geo<PAIR>::TILE_M - 1) / Geo<PAIR>::TILE_M;
-  p.Nt = (Nr + Geo<PAIR>::TILE_N - 1) / Geo<PAIR>::TILE_N;
+  p.Mt = (M + Unit<DENSE_CL>::ROWS - 1) / Unit<DENSE_CL>::ROWS;
+  p.Nt = (Nr + DenseGeo::TILE_N - 1) / DenseGeo::TILE_N;
   p.KT = (K + BK - 1) / BK;
   p.ldo = Nr;
   p.rows_per_rank = rows;
@@ -117,9 +121,9 @@ extern "C" flux_status_t flux_ag_gemm(int R, int M, int N, int K, flux_dtype_t d
   p.num_units = R * p.Mt * p.Nt;
   p.flags = ready_flags;
   fill_common(p, opts, workspace);
-  const int grid = grid_dt<MODE_STORE, PAIR>(dtype, dev, opts, p.num_units);
+  const int grid = grid_dt<MODE_STORE, DENSE_CL>(dtype, dev, opts, p.num_units);
   if (grid == 0) return FLUX_ERR_CUDA;
-  return launch_dt<MODE_STORE, PAIR>(dtype, p, grid, s);
+  return launch_dt<MODE_STORE, DENSE_CL>(dtype, p, grid, s);
 }
 
 extern "C" flux_status_t flux_gemm(int M, int N, int K, flux_dtype_t dtype, const void* A,
@@ -181,8 +185,8 @@ extern "C" flux_status_t flux_gemm_rs(int R, int M, int N, int K, flux_dtype_t d
 
   // Few tiles per SM (decode shapes): single-CTA 128 x 256 tiles and an equal
   // contiguous range of k-slices per CTA (tiles split along K add into the same
-  // fp32 owner tile).  Otherwise: whole 256 x 512 tiles on CTA pairs, strided
-  // over a persistent grid.
+  // fp32 owner tile).  Otherwise: whole 512 x 512 units on clusters of two CTA
+  // pairs, strided over a persistent grid.
   const int sm = (opts && opts->num_ctas > 0) ? opts->num_ctas : dev.sm_count;
   const long long units128 = static_cast<long long>((M + BM - 1) / BM) * ((N + BN - 1) / BN) * R;
   if (units128 < 4 * sm) {
@@ -199,16 +203,15 @@ extern "C" flux_status_t flux_gemm_rs(int R, int M, int N, int K, flux_dtype_t d
     p.tiles_per_group = p.Mt * p.Nt;
     return launch_dt<MODE_REDUCE, 1>(dtype, p, grid, s);
   }
-  constexpr int PAIR = 2;
-  p.Nt = (N + Geo<PAIR>::TILE_N - 1) / Geo<PAIR>::TILE_N;
-  p.Mt = (M + Geo<PAIR>::TILE_M - 1) / Geo<PAIR>::TILE_M;
+  p.Nt = (N + DenseGeo::TILE_N - 1) / DenseGeo::TILE_N;
+  p.Mt = (M + Unit<DENSE_CL>::ROWS - 1) / Unit<DENSE_CL>::ROWS;
   const int tiles = p.Mt * p.Nt;
   p.num_units = tiles * R;
   p.total_ksteps = static_cast<long long>(p.num_units) * p.KT;
   p.stream_k = 0;
-  const int grid = grid_dt<MODE_REDUCE, PAIR>(dtype, dev, opts, p.num_units);
+  const int grid = grid_dt<MODE_REDUCE, DENSE_CL>(dtype, dev, opts, p.num_units);
   if (grid == 0) return FLUX_ERR_CUDA;
-  const int tg = (opts && opts->tiles_per_group > 0) ? opts->tiles_per_group : grid / PAIR;
+  const int tg = (opts && opts->tiles_per_group > 0) ? opts->tiles_per_group : grid / DENSE_CL;
   p.tiles_per_group = tg < tiles ? tg : tiles;
-  return launch_dt<MODE_REDUCE, PAIR>(dtype, p, grid, s);
+  return launch_dt<MODE_REDUCE, DENSE_CL>(dtype, p, grid, s);
 }

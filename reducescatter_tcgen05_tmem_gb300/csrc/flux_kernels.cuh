@@ -34,6 +34,16 @@
 //           whose producer expects the bytes of both.  Commits are multicast
 //           to both CTAs' "empty" and "accumulator full" barriers; both CTAs'
 //           epilogue warps arrive on the even CTA's "accumulator empty" barrier.
+// CL = 4:   a cluster of two such pairs stacked along M (a 512 x 512 unit).
+//           CTAs r and r^2 need the same B columns, so each issues half of
+//           them (the 256-column half h = r / 2) as a TMA multicast to both;
+//           every CTA's bytes still complete on its own pair's even-CTA
+//           barrier.  A stage may be refilled only when both pairs' MMAs have
+//           read it: each "empty" barrier counts one commit per pair.
+//
+// The template parameter CL is the number of CTAs of a cluster (1, 2 or 4);
+// PAIR = min(CL, 2) is the tcgen05 CTA group and MC = CL / PAIR the pairs that
+// share B.
 //
 // Every wait is bounded: after timeout_ns (or an iteration cap) the thread
 // records FLUX_ERR_TIMEOUT in the workspace header, raises the per-call abort
@@ -273,13 +283,22 @@ struct Work {
   int tile;    // linear 128-row output-tile id of this CTA's part (REDUCE counters)
 };
 
+// Rows of A covered by one work unit: 128 per CTA of the cluster.
+template <int CL>
+struct Unit {
+  static constexpr int PAIR = CL >= 2 ? 2 : 1;
+  static constexpr int MC = CL / PAIR;
+  static constexpr int ROWS = BM * CL;
+};
+
 // AllGather / plain GEMM: unit -> (rank, m-tile, n-tile).  Ranks are the
 // outer loop; inside a rank the m order is rotated so that rank r starts with
 // the rows it owns (the local shard is the first to be ready) and then walks
-// the other ranks' shards in ring order.
-template <int PAIR>
+// the other ranks' shards in ring order.  `cta` is the CTA's rank in its
+// cluster; it holds rows m0 .. m0+127 of the unit.
+template <int CL>
 __device__ __forceinline__ Work decode_store(const KParams& p, int u, int cta) {
-  constexpr int TM = Geo<PAIR>::TILE_M;
+  constexpr int TM = Unit<CL>::ROWS;
   Work w;
   const int per_rank = p.Mt * p.Nt;
   w.r = u / per_rank;
@@ -302,9 +321,9 @@ __device__ __forceinline__ Work decode_store(const KParams& p, int u, int cta) {
 // one output tile are `tiles_per_group` units apart, so with a strided
 // persistent schedule they land in consecutive waves while the owner's fp32
 // tile is still in L2.
-template <int PAIR>
+template <int CL>
 __device__ __forceinline__ Work decode_reduce(const KParams& p, int u, int cta) {
-  constexpr int TM = Geo<PAIR>::TILE_M;
+  constexpr int TM = Unit<CL>::ROWS;
   Work w;
   const int tiles = p.Mt * p.Nt;
   const int TG = p.tiles_per_group;
@@ -322,7 +341,7 @@ __device__ __forceinline__ Work decode_reduce(const KParams& p, int u, int cta) 
     t = full_groups * TG + (rem - w.r * tl);
   }
   raster(t, p.Mt, p.Nt, p.group_n, w.mt, w.nt);
-  w.tile = (w.mt * PAIR + cta) * p.Nt + w.nt;
+  w.tile = (w.mt * CL + cta) * p.Nt + w.nt;
   w.m0 = w.mt * TM + cta * BM;
   w.row_end = p.M;
   w.e = 0;
@@ -358,9 +377,9 @@ __device__ __forceinline__ Work decode_moe(const KParams& p, int u, int total_mt
   return w;
 }
 
-// Iterates the items of this CTA identically in every role.  With PAIR = 2
-// both CTAs of a cluster walk the same units (cluster index = blockIdx / 2).
-template <int MODE, int PAIR>
+// Iterates the items of this CTA identically in every role.  All CTAs of a
+// cluster walk the same units (cluster index = blockIdx / CL).
+template <int MODE, int CL>
 struct ItemIter {
   const KParams& p;
   int total_mt;      // MoE: device-computed number of m-tiles
@@ -374,8 +393,8 @@ struct ItemIter {
     } else {
       num_units = p.num_units;
     }
-    u = blockIdx.x / PAIR;
-    stride = gridDim.x / PAIR;
+    u = blockIdx.x / CL;
+    stride = gridDim.x / CL;
     if (MODE == MODE_REDUCE && p.stream_k) {
       const long long L = p.total_ksteps;
       pos = L * u / stride;
@@ -390,15 +409,15 @@ struct ItemIter {
       const int k0 = static_cast<int>(pos - static_cast<long long>(unit) * p.KT);
       long long k1 = k0 + (end - pos);
       if (k1 > p.KT) k1 = p.KT;
-      w = decode_reduce<PAIR>(p, unit, cta);
+      w = decode_reduce<CL>(p, unit, cta);
       w.k0 = k0;
       w.k1 = static_cast<int>(k1);
       pos += k1 - k0;
       return true;
     }
     if (u >= num_units) return false;
-    if (MODE == MODE_STORE) w = decode_store<PAIR>(p, u, cta);
-    else if (MODE == MODE_REDUCE) w = decode_reduce<PAIR>(p, u, cta);
+    if (MODE == MODE_STORE) w = decode_store<CL>(p, u, cta);
+    else if (MODE == MODE_REDUCE) w = decode_reduce<CL>(p, u, cta);
     else w = decode_moe(p, u, total_mt);
     u += stride;
     return true;
@@ -431,11 +450,16 @@ __device__ __forceinline__ uint32_t pair_peer_bytes(const KParams& p, const Work
   return a + __popc(mask) * B_BOX_N * BK * 2;
 }
 
-// TMA producer (one thread).
-template <int MODE, int PAIR>
-__device__ void producer_tma(const KParams& p, const Smem& s, const Ctl& c, int total_mt, int cta) {
+// TMA producer (one thread).  `rank` is the CTA's rank in its cluster.
+template <int MODE, int CL>
+__device__ void producer_tma(const KParams& p, const Smem& s, const Ctl& c, int total_mt, int rank) {
+  constexpr int PAIR = Unit<CL>::PAIR;
+  constexpr int MC = Unit<CL>::MC;
   using G = Geo<PAIR>;
-  ItemIter<MODE, PAIR> iter(p, total_mt, cta);
+  const int cta = rank & (PAIR - 1);  // position in the pair
+  const int half = rank / PAIR;       // MC = 2: the B half this CTA multicasts
+  const uint16_t mc_mask = static_cast<uint16_t>((1u << rank) | (1u << (rank ^ 2)));
+  ItemIter<MODE, CL> iter(p, total_mt, rank);
   Work w;
   uint32_t stage = 0, phase = 0;
   uint32_t issued = 0;
@@ -469,7 +493,8 @@ __device__ void producer_tma(const KParams& p, const Smem& s, const Ctl& c, int 
       bytes += pair_peer_bytes<MODE>(p, w);
     }
     for (int k = w.k0; k < w.k1; ++k) {
-      if ((PAIR == 2 && cta != 0
+      // the empty barrier is completed by a remote commit whenever another CTA's MMAs read the stage
+      if (((PAIR == 2 && cta != 0) || MC == 2
                ? wait_bar_remote(smem_u32(&s.empty[stage]), phase ^ 1u, c, W_EMPTY, stage)
                : wait_bar(smem_u32(&s.empty[stage]), phase ^ 1u, c, W_EMPTY, stage)) != 0) {
         ok = false;
@@ -477,7 +502,8 @@ __device__ void producer_tma(const KParams& p, const Smem& s, const Ctl& c, int 
       }
       const uint32_t fb = smem_u32(&s.full[stage]);
       if (PAIR == 1 || cta == 0) mbar_arrive_expect_tx(fb, bytes);
-      const uint32_t fbc = PAIR == 2 ? mapa_shared(fb, 0) : fb;  // barrier in the even CTA
+      // barrier in the even CTA of this CTA's pair
+      const uint32_t fbc = PAIR == 2 ? mapa_shared(fb, static_cast<uint32_t>(rank & ~1)) : fb;
       const uint32_t sa = smem_u32(s.a + stage * A_STAGE);
       const uint32_t sb = smem_u32(s.b + stage * G::B_STAGE);
       const int kc = k * BK;
@@ -499,7 +525,10 @@ __device__ void producer_tma(const KParams& p, const Smem& s, const Ctl& c, int 
         const int n = b_box_col<PAIR>(n0, cta, j);
         if (MODE == MODE_MOE_SCATTER)
           tma_load_3d(sb + j * B_BOX_N * BK * 2, &p.tmB[w.r], fb, n, kc, w.e);
-        else if (PAIR == 2)
+        else if (MC == 2) {
+          if ((j >> 1) == half)
+            tma_load_2d_pair_mc(sb + j * B_BOX_N * BK * 2, &p.tmB[w.r], fbc, n, kc, mc_mask);
+        } else if (PAIR == 2)
           tma_load_2d_pair(sb + j * B_BOX_N * BK * 2, &p.tmB[w.r], fbc, n, kc);
         else
           tma_load_2d(sb + j * B_BOX_N * BK * 2, &p.tmB[w.r], fb, n, kc);
@@ -516,6 +545,8 @@ __device__ void producer_tma(const KParams& p, const Smem& s, const Ctl& c, int 
     const uint32_t fills = issued / G::STAGES + (st < issued % G::STAGES ? 1u : 0u);
     if (fills == 0) continue;
     if (PAIR == 2 && cta != 0) {
+      // (with MC = 2 the empty barrier also waits for the other pair, whose
+      // multicast copies land here too)
       wait_bar_remote_drain(smem_u32(&s.empty[st]), (fills - 1u) & 1u, c, W_DRAIN, st);
     } else {
       wait_bar(smem_u32(&s.full[st]), (fills - 1u) & 1u, c, W_DRAIN, st, false);
@@ -606,13 +637,18 @@ __device__ void producer_gather(const KParams& p, const Smem& s, const Ctl& c, i
   }
 }
 
-// MMA issuer (one thread; with PAIR = 2 only in the even CTA).
-template <int MODE, int DT, int PAIR>
+// MMA issuer (one thread; with pairs only in the even CTA of each pair).
+template <int MODE, int DT, int CL>
 __device__ void mma_issuer(const KParams& p, const Smem& s, const Ctl& c, uint32_t tmem_base,
-                           int total_mt) {
+                           int total_mt, int rank) {
+  constexpr int PAIR = Unit<CL>::PAIR;
   using G = Geo<PAIR>;
   constexpr uint32_t IDESC = idesc_f16(DT, BM * PAIR, BN, 0, 1);
-  ItemIter<MODE, PAIR> iter(p, total_mt, 0);
+  // stage release reaches every CTA whose shared memory the stage's copies
+  // fill; the accumulator-full signal only this pair
+  constexpr uint16_t EMPTY_MASK = static_cast<uint16_t>((1u << CL) - 1u);
+  const uint16_t pair_mask = static_cast<uint16_t>(0x3u << (rank & ~1));
+  ItemIter<MODE, CL> iter(p, total_mt, rank);
   Work w;
   uint32_t stage = 0, phase = 0;
   int it = 0;
@@ -647,13 +683,13 @@ __device__ void mma_issuer(const KParams& p, const Smem& s, const Ctl& c, uint32
           else umma_f16(d + h * BN, ad, bd, IDESC, acc);
         }
       }
-      if (PAIR == 2) umma2_commit_mc(smem_u32(&s.empty[stage]), 0x3);
+      if (PAIR == 2) umma2_commit_mc(smem_u32(&s.empty[stage]), EMPTY_MASK);
       else umma_commit(smem_u32(&s.empty[stage]));
       any = true;
       if (++stage == G::STAGES) { stage = 0; phase ^= 1u; }
     }
     if (!ok) break;
-    if (PAIR == 2) umma2_commit_mc(smem_u32(&s.tfull[b]), 0x3);
+    if (PAIR == 2) umma2_commit_mc(smem_u32(&s.tfull[b]), pair_mask);
     else umma_commit(smem_u32(&s.tfull[b]));
     ++it;
   }
@@ -720,17 +756,20 @@ __device__ __forceinline__ void convert8(float* src, uint16_t* dst) {
   st_cg_f4(src + 4, z);
 }
 
-template <int MODE, int DT, int PAIR>
+template <int MODE, int DT, int CL>
 __device__ void epilogue(const KParams& p, const Smem& s, const Ctl& c, uint32_t tmem_base,
-                         int total_mt, int warp, int cta) {
+                         int total_mt, int warp, int rank) {
+  constexpr int PAIR = Unit<CL>::PAIR;
+  const int cta = rank & (PAIR - 1);
   const int lane = threadIdx.x & 31;
   const int q = warp & 3;  // TMEM lane quarter this warp may access
-  ItemIter<MODE, PAIR> iter(p, total_mt, cta);
+  ItemIter<MODE, CL> iter(p, total_mt, rank);
   Work w;
   int it = 0;
   // the accumulator-empty barrier lives in the even CTA of a pair
-  const uint32_t tempty0 = (PAIR == 2 && cta != 0) ? mapa_shared(smem_u32(&s.tempty[0]), 0)
-                                                   : smem_u32(&s.tempty[0]);
+  const uint32_t tempty0 = (PAIR == 2 && cta != 0)
+                               ? mapa_shared(smem_u32(&s.tempty[0]), static_cast<uint32_t>(rank & ~1))
+                               : smem_u32(&s.tempty[0]);
   const uint32_t srow = smem_u32(s.stg + q * STG_WARP + lane * STG_PITCH);
   using G = Geo<PAIR>;
   while (iter.next(w)) {
@@ -842,7 +881,7 @@ __device__ void epilogue(const KParams& p, const Smem& s, const Ctl& c, uint32_t
 }
 
 // ---------------------------------------------------------------- kernel
-template <int MODE, int DT, int PAIR>
+template <int MODE, int DT, int CL>
 struct KernelShape {
   static constexpr int PRODUCER_WARPS = (MODE == MODE_MOE_GATHER) ? 4 : 1;
   static constexpr int MMA_WARP = PRODUCER_WARPS;
@@ -851,12 +890,15 @@ struct KernelShape {
   static constexpr int FULL_COUNT = (MODE == MODE_MOE_GATHER) ? (BM + 1) : 1;
 };
 
-template <int MODE, int DT, int PAIR>
-__global__ void __launch_bounds__(KernelShape<MODE, DT, PAIR>::THREADS, 1)
+template <int MODE, int DT, int CL>
+__global__ void __launch_bounds__(KernelShape<MODE, DT, CL>::THREADS, 1)
 fused_gemm_kernel(const __grid_constant__ KParams p) {
-  using KS = KernelShape<MODE, DT, PAIR>;
+  using KS = KernelShape<MODE, DT, CL>;
+  constexpr int PAIR = Unit<CL>::PAIR;
+  constexpr int MC = Unit<CL>::MC;
   using G = Geo<PAIR>;
-  static_assert(PAIR == 1 || (MODE == MODE_STORE || MODE == MODE_REDUCE), "pairs: dense modes");
+  static_assert(CL == 1 || CL == 2 || CL == 4, "cluster of 1, 2 or 4 CTAs");
+  static_assert(CL == 1 || (MODE == MODE_STORE || MODE == MODE_REDUCE), "clusters: dense modes");
   extern __shared__ uint8_t smem_raw[];
   uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
@@ -873,7 +915,8 @@ fused_gemm_kernel(const __grid_constant__ KParams p) {
   s.stg = base + G::STAGES * (A_STAGE + G::B_STAGE) + 512;
 
   const int warp = threadIdx.x >> 5;
-  const int cta = PAIR == 2 ? static_cast<int>(cluster_ctarank()) : 0;
+  const int rank = CL > 1 ? static_cast<int>(cluster_ctarank()) : 0;
+  const int cta = rank & (PAIR - 1);
   Ctl c;
   c.hdr = p.hdr;
   c.seq = p.seq;
@@ -883,7 +926,7 @@ fused_gemm_kernel(const __grid_constant__ KParams p) {
   if (threadIdx.x == 0) {
     for (int i = 0; i < G::STAGES; ++i) {
       mbar_init(smem_u32(&s.full[i]), KS::FULL_COUNT);
-      mbar_init(smem_u32(&s.empty[i]), 1);
+      mbar_init(smem_u32(&s.empty[i]), MC);  // one commit per pair that reads the stage
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(smem_u32(&s.tfull[i]), 1);
@@ -903,7 +946,7 @@ fused_gemm_kernel(const __grid_constant__ KParams p) {
   }
   tc_fence_before();
   __syncthreads();
-  if (PAIR == 2) cluster_sync();  // peer barriers initialised and TMEM allocated in both CTAs
+  if (CL > 1) cluster_sync();  // peer barriers initialised and TMEM allocated in every CTA
   tc_fence_after();
   const uint32_t tmem_base = *s.tmem_slot;
 
@@ -920,19 +963,19 @@ fused_gemm_kernel(const __grid_constant__ KParams p) {
     if (MODE == MODE_MOE_GATHER) {
       producer_gather<KS::PRODUCER_WARPS * 32>(p, s, c, total_mt);
     } else if (lane == 0) {
-      producer_tma<MODE, PAIR>(p, s, c, total_mt, cta);
+      producer_tma<MODE, CL>(p, s, c, total_mt, rank);
     }
   } else if (warp == KS::MMA_WARP) {
     // the even CTA of a pair issues the MMAs for both
-    if (lane == 0 && cta == 0) mma_issuer<MODE, DT, PAIR>(p, s, c, tmem_base, total_mt);
+    if (lane == 0 && cta == 0) mma_issuer<MODE, DT, CL>(p, s, c, tmem_base, total_mt, rank);
     __syncwarp();
   } else {
-    epilogue<MODE, DT, PAIR>(p, s, c, tmem_base, total_mt, warp, cta);
+    epilogue<MODE, DT, CL>(p, s, c, tmem_base, total_mt, warp, rank);
   }
 
   tc_fence_before();
   __syncthreads();
-  if (PAIR == 2) cluster_sync();  // no CTA frees TMEM or leaves while its peer still works
+  if (CL > 1) cluster_sync();  // no CTA frees TMEM or leaves while another still works
   if (warp == KS::MMA_WARP) {
     tc_fence_after();
     if (PAIR == 2) tmem_dealloc2(tmem_base, TMEM_COLS);

@@ -21,7 +21,7 @@ inline bool debug_enabled() {
   return on;
 }
 
-template <int MODE, int DT, int PAIR>
+template <int MODE, int DT, int CL>
 struct Launcher {
   // Largest grid (CTAs) that is resident at once; 0 on error.
   static int max_ctas(const DeviceInfo& dev) {
@@ -29,30 +29,30 @@ struct Launcher {
     static cudaError_t err = cudaSuccess;
     static int ctas = 0;
     std::call_once(once, [&dev] {
-      err = cudaFuncSetAttribute(fused_gemm_kernel<MODE, DT, PAIR>,
+      err = cudaFuncSetAttribute(fused_gemm_kernel<MODE, DT, CL>,
                                  cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
       if (err != cudaSuccess) return;
-      if (PAIR == 1) {
+      if (CL == 1) {
         ctas = dev.sm_count;
         return;
       }
       cudaLaunchConfig_t cfg = {};
-      cfg.gridDim = dim3(2 * (dev.sm_count / 2), 1, 1);
-      cfg.blockDim = dim3(KernelShape<MODE, DT, PAIR>::THREADS, 1, 1);
+      cfg.gridDim = dim3(CL * (dev.sm_count / CL), 1, 1);
+      cfg.blockDim = dim3(KernelShape<MODE, DT, CL>::THREADS, 1, 1);
       cfg.dynamicSmemBytes = SMEM_BYTES;
       cudaLaunchAttribute attr[1];
       attr[0].id = cudaLaunchAttributeClusterDimension;
-      attr[0].val.clusterDim.x = PAIR;
+      attr[0].val.clusterDim.x = CL;
       attr[0].val.clusterDim.y = 1;
       attr[0].val.clusterDim.z = 1;
       cfg.attrs = attr;
       cfg.numAttrs = 1;
       int clusters = 0;
-      err = cudaOccupancyMaxActiveClusters(&clusters, fused_gemm_kernel<MODE, DT, PAIR>, &cfg);
-      ctas = clusters * PAIR;
+      err = cudaOccupancyMaxActiveClusters(&clusters, fused_gemm_kernel<MODE, DT, CL>, &cfg);
+      ctas = clusters * CL;
       if (debug_enabled())
-        std::fprintf(stderr, "[flux] mode %d dtype %d pair %d: %d clusters resident at once\n",
-                     MODE, DT, PAIR, clusters);
+        std::fprintf(stderr, "[flux] mode %d dtype %d cluster %d: %d clusters resident at once\n",
+                     MODE, DT, CL, clusters);
     });
     if (err != cudaSuccess) {
       cuda_fail(err);
@@ -64,38 +64,38 @@ struct Launcher {
   static flux_status_t launch(const KParams& p, int grid, cudaStream_t stream) {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(grid, 1, 1);
-    cfg.blockDim = dim3(KernelShape<MODE, DT, PAIR>::THREADS, 1, 1);
+    cfg.blockDim = dim3(KernelShape<MODE, DT, CL>::THREADS, 1, 1);
     cfg.dynamicSmemBytes = SMEM_BYTES;
     cfg.stream = stream;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = PAIR;
+    attr[0].val.clusterDim.x = CL;
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
     cfg.attrs = attr;
-    cfg.numAttrs = PAIR > 1 ? 1 : 0;
+    cfg.numAttrs = CL > 1 ? 1 : 0;
     if (debug_enabled())
       std::fprintf(stderr,
-                   "[flux] mode %d dtype %d pair %d: grid %d x %d threads, %d B smem, units %d, "
+                   "[flux] mode %d dtype %d cluster %d: grid %d x %d threads, %d B smem, units %d, "
                    "tiles %d x %d, k-slices %d, stream-k %d\n",
-                   MODE, DT, PAIR, grid, KernelShape<MODE, DT, PAIR>::THREADS, SMEM_BYTES,
+                   MODE, DT, CL, grid, KernelShape<MODE, DT, CL>::THREADS, SMEM_BYTES,
                    p.num_units, p.Mt, p.Nt, p.KT, p.stream_k);
-    cudaError_t e = cudaLaunchKernelEx(&cfg, fused_gemm_kernel<MODE, DT, PAIR>, p);
+    cudaError_t e = cudaLaunchKernelEx(&cfg, fused_gemm_kernel<MODE, DT, CL>, p);
     return e == cudaSuccess ? FLUX_OK : cuda_fail(e);
   }
 };
 
-// Grid for `units` work units of PAIR CTAs each, capped at the resident CTAs
-// (or opts->num_ctas); a multiple of PAIR, at least PAIR.
-template <int MODE, int DT, int PAIR>
+// Grid for `units` work units of CL CTAs each, capped at the resident CTAs
+// (or opts->num_ctas); a multiple of CL, at least CL.
+template <int MODE, int DT, int CL>
 int grid_for(const DeviceInfo& dev, const flux_opts_t* opts, long long units) {
-  int cap = Launcher<MODE, DT, PAIR>::max_ctas(dev);
+  int cap = Launcher<MODE, DT, CL>::max_ctas(dev);
   if (cap <= 0) return 0;
   if (opts && opts->num_ctas > 0 && opts->num_ctas < cap) cap = opts->num_ctas;
-  long long g = units * PAIR;
+  long long g = units * CL;
   if (g > cap) g = cap;
-  g -= g % PAIR;
-  if (g < PAIR) g = PAIR;
+  g -= g % CL;
+  if (g < CL) g = CL;
   return static_cast<int>(g);
 }
 
