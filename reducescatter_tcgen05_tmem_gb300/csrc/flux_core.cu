@@ -93,6 +93,22 @@ flux_status_t encode_2d(CUtensorMap* map, flux_dtype_t dt, const void* base, uin
   return FLUX_OK;
 }
 
+flux_status_t encode_2d_f32(CUtensorMap* map, const void* base, uint64_t inner, uint64_t outer,
+                            uint64_t row_pitch_bytes, uint32_t box_inner, uint32_t box_outer) {
+  PFN_cuTensorMapEncodeTiled_v12000 fn;
+  flux_status_t st = encoder(&fn);
+  if (st != FLUX_OK) return st;
+  cuuint64_t dims[2] = {inner, outer};
+  cuuint64_t strides[1] = {row_pitch_bytes};
+  cuuint32_t box[2] = {box_inner, box_outer};
+  cuuint32_t es[2] = {1, 1};
+  CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<void*>(base), dims, strides, box,
+                  es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return cuda_fail(cudaErrorInvalidValue);
+  return FLUX_OK;
+}
+
 flux_status_t encode_3d(CUtensorMap* map, flux_dtype_t dt, const void* base, uint64_t d0,
                         uint64_t d1, uint64_t d2, uint32_t box0, uint32_t box1) {
   PFN_cuTensorMapEncodeTiled_v12000 fn;

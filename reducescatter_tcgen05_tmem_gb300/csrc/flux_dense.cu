@@ -181,6 +181,8 @@ extern "C" flux_status_t flux_gemm_rs(int R, int M, int N, int K, flux_dtype_t d
   uint8_t* ws = static_cast<uint8_t*>(workspace);
   p.counters = reinterpret_cast<uint32_t*>(ws + WS_HEADER);
   p.acc = reinterpret_cast<float*>(ws + WS_HEADER + rs_counter_bytes(M, N));
+  if ((st = encode_2d_f32(&p.tmAcc, p.acc, N, M, static_cast<uint64_t>(N) * 4, 32, 32)) != FLUX_OK)
+    return st;
   fill_common(p, opts, workspace);
 
   // Few tiles per SM (decode shapes): single-CTA 128 x 256 tiles and an equal

@@ -35,6 +35,11 @@ flux_status_t encode_2d(CUtensorMap* map, flux_dtype_t dt, const void* base, uin
                         uint64_t outer, uint64_t row_pitch_bytes, uint32_t box_inner,
                         uint32_t box_outer);
 
+// 2-D row-major fp32 tensor with 128-byte swizzle (the accumulation rows of the
+// reduce epilogue).
+flux_status_t encode_2d_f32(CUtensorMap* map, const void* base, uint64_t inner, uint64_t outer,
+                            uint64_t row_pitch_bytes, uint32_t box_inner, uint32_t box_outer);
+
 // 3-D row-major tensor [d2 x d1 x d0] of 16-bit elements with 128-byte swizzle.
 flux_status_t encode_3d(CUtensorMap* map, flux_dtype_t dt, const void* base, uint64_t d0,
                         uint64_t d1, uint64_t d2, uint32_t box0, uint32_t box1);

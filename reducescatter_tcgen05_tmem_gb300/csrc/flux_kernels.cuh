@@ -65,11 +65,17 @@ constexpr int MAXR = 16;
 constexpr int EPI_WARPS = 4;
 constexpr int GATHER_LAG = 2;         // cp.async groups in flight before a stage is published
 
-// epilogue staging for the fp32 reduce modes: per epilogue warp 32 rows of 32
-// floats, each row padded to 144 bytes (16-byte aligned rows for the bulk
-// reduce; the pad spreads the rows of one 16-byte store over all banks)
+// Epilogue staging for the fp32 reduce modes, 8 KB per epilogue warp.
+//   REDUCE: two 4 KB buffers, each a 32-row x 32-float box in the 128-byte
+//           swizzled layout of the accumulator tensor map (one tensor bulk
+//           reduce per buffer; the swizzle keeps the row-per-thread stores
+//           free of bank conflicts).
+//   MOE_SCATTER: 32 rows of 32 floats, each row padded to 144 bytes (one bulk
+//           reduce per row into that row's token).
+constexpr int STG_BOX = 32 * 32 * 4;
 constexpr int STG_PITCH = 144;
-constexpr int STG_WARP = 32 * STG_PITCH;
+constexpr int STG_WARP = 2 * STG_BOX;
+static_assert(32 * STG_PITCH <= STG_WARP, "row staging fits");
 
 template <int PAIR>
 struct Geo {
@@ -81,8 +87,8 @@ struct Geo {
   static constexpr int B_STAGE = B_BOXES * B_BOX_N * BK * 2;  // 32 KB
   static constexpr int ACC_BUFS = 2 / PAIR;            // accumulators in the 512 TMEM columns
   static constexpr int ACC_COLS = TILE_N;              // TMEM columns of one accumulator
-  static constexpr int SMEM = STAGES * (A_STAGE + B_STAGE) + 1024 /*align*/ + 512 /*barriers*/ +
-                              EPI_WARPS * STG_WARP;
+  static constexpr int SMEM = STAGES * (A_STAGE + B_STAGE) + EPI_WARPS * STG_WARP + 1024 /*align*/ +
+                              512 /*barriers*/;
 };
 constexpr int SMEM_BYTES = Geo<1>::SMEM > Geo<2>::SMEM ? Geo<1>::SMEM : Geo<2>::SMEM;
 static_assert(Geo<1>::ACC_BUFS * Geo<1>::ACC_COLS == TMEM_COLS, "TMEM budget");
@@ -121,6 +127,7 @@ constexpr uint32_t ST_INVALID = 1;
 struct KParams {
   CUtensorMap tmA[MAXR];   // per-rank A operand maps (K-major, 128B swizzle)
   CUtensorMap tmB[MAXR];   // per-rank B operand maps (N-major, 128B swizzle)
+  CUtensorMap tmAcc;       // REDUCE: fp32 accumulation rows [M x N], 32 x 32 boxes
   void* out[MAXR];         // per-rank outputs
   const void* xsrc[MAXR];  // MOE_GATHER: per-shard token rows
   int R;
@@ -434,7 +441,7 @@ struct Smem {
   uint64_t* tempty; // [2]
   uint64_t* drain;  // [1]
   uint32_t* tmem_slot;
-  uint8_t* stg;     // EPI_WARPS x STG_WARP epilogue staging
+  uint8_t* stg;     // EPI_WARPS x STG_WARP epilogue staging (1024-byte aligned)
 };
 
 // Bytes the odd CTA of a pair loads for one stage of work item `w` (the even
@@ -770,7 +777,8 @@ __device__ void epilogue(const KParams& p, const Smem& s, const Ctl& c, uint32_t
   const uint32_t tempty0 = (PAIR == 2 && cta != 0)
                                ? mapa_shared(smem_u32(&s.tempty[0]), static_cast<uint32_t>(rank & ~1))
                                : smem_u32(&s.tempty[0]);
-  const uint32_t srow = smem_u32(s.stg + q * STG_WARP + lane * STG_PITCH);
+  const uint32_t sstg = smem_u32(s.stg + q * STG_WARP);
+  const uint32_t srow = sstg + lane * STG_PITCH;
   using G = Geo<PAIR>;
   while (iter.next(w)) {
     const uint32_t b = it % G::ACC_BUFS;
@@ -797,16 +805,37 @@ __device__ void epilogue(const KParams& p, const Smem& s, const Ctl& c, uint32_t
       tok = slot / p.topk;
       gate = __ldg(p.topk_w + slot);
     }
+    const int row0 = w.m0 + q * 32;  // first row of this warp's 32-row box
     for (int ch = 0; ch < G::TILE_N / 32; ++ch) {
       if (ch * 32 >= ncols) break;  // warp-uniform
       uint32_t v[32];
       tmem_ld_32x32b_x32(taddr + ch * 32, v);
+      if (MODE == MODE_REDUCE) {
+        // the warp's 32 x 32 fp32 box goes out as one tensor bulk reduce-add;
+        // buffer ch & 1 is free once at most one newer group still reads
+        if (row0 >= w.row_end) continue;  // warp-uniform: nothing of the box is inside
+        const uint32_t buf = sstg + (ch & 1) * STG_BOX;
+        if (ch >= 2) {
+          if (lane == 0) bulk_wait_read<1>();
+          __syncwarp();
+        }
+#pragma unroll
+        for (int g = 0; g < 8; ++g)
+          asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};"
+                       ::"r"(buf + lane * 128 + ((g ^ (lane & 7)) << 4)), "r"(v[g * 4 + 0]),
+                         "r"(v[g * 4 + 1]), "r"(v[g * 4 + 2]), "r"(v[g * 4 + 3]) : "memory");
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+          tma_reduce_add_2d(&p.tmAcc, buf, n0 + ch * 32, row0);
+          bulk_commit();
+        }
+        continue;
+      }
       const int nv = ncols - ch * 32;
       if (!row_ok) continue;
       if (MODE == MODE_STORE || MODE == MODE_MOE_GATHER) {
         store_row_chunk<DT>(p.out[w.r], static_cast<long long>(row) * p.ldo, n0 + ch * 32, nv, v);
-      } else if (MODE == MODE_REDUCE) {
-        stage_and_reduce(p.acc + static_cast<long long>(row) * p.N + n0 + ch * 32, srow, nv, v, 1.0f);
       } else {
         stage_and_reduce(p.acc + static_cast<long long>(tok) * p.N + n0 + ch * 32, srow, nv, v, gate);
       }
@@ -905,14 +934,14 @@ fused_gemm_kernel(const __grid_constant__ KParams p) {
   Smem s;
   s.a = base;
   s.b = base + G::STAGES * A_STAGE;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(base + G::STAGES * (A_STAGE + G::B_STAGE));
+  s.stg = base + G::STAGES * (A_STAGE + G::B_STAGE);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(s.stg + EPI_WARPS * STG_WARP);
   s.full = bars;
   s.empty = bars + G::STAGES;
   s.tfull = bars + 2 * G::STAGES;
   s.tempty = bars + 2 * G::STAGES + 2;
   s.drain = bars + 2 * G::STAGES + 4;
   s.tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * G::STAGES + 5);
-  s.stg = base + G::STAGES * (A_STAGE + G::B_STAGE) + 512;
 
   const int warp = threadIdx.x >> 5;
   const int rank = CL > 1 ? static_cast<int>(cluster_ctarank()) : 0;
