@@ -561,10 +561,12 @@ __device__ void producer_tma(const KParams& p, const Smem& s, const Ctl& c, int 
   }
 }
 
-// cp.async row-gather producer for MoE layer0 (all producer threads).  Thread i
-// copies row i of the A tile (128 bytes per k-slice) from the token row of the
-// rank that owns it, into the 128B-swizzled layout the MMA descriptor expects;
-// thread 0 also issues the B tile by TMA.
+// cp.async row-gather producer for MoE layer0 (all producer threads).  Eight
+// consecutive threads copy one 128-byte row of a k-slice (16 bytes each), so a
+// warp instruction moves four whole rows; thread t serves rows 16i + t/8
+// (i = 0..7) of the A tile, each from the token row of the rank that owns it,
+// into the 128B-swizzled layout the MMA descriptor expects.  Thread 0 also
+// issues the B tile by TMA.
 template <int NPROD>
 __device__ void producer_gather(const KParams& p, const Smem& s, const Ctl& c, int total_mt) {
   using G = Geo<1>;
@@ -576,20 +578,29 @@ __device__ void producer_gather(const KParams& p, const Smem& s, const Ctl& c, i
   uint32_t ready = (p.flags == nullptr) ? 0xFFFFFFFFu : 0u;
   bool ok = true;
   const char* any_src = static_cast<const char*>(p.xsrc[0]);
+  static_assert(NPROD == BM, "one producer thread per 16-byte chunk of 16 rows");
+  constexpr int ROWS_PER_PASS = NPROD / 8;
+  constexpr int PASSES = BM / ROWS_PER_PASS;
+  const int sub = tid >> 3;   // row within a pass
+  const int chunk = tid & 7;  // 16-byte chunk of the 128-byte row
   while (ok && iter.next(w)) {
-    // my row of this tile
-    const int row = w.m0 + tid;
-    const char* src = nullptr;
-    if (tid < BM && row < w.row_end) {
-      const int slot = __ldg(p.row_to_slot + row);
-      const int tok = slot / p.topk;
-      const int sh = tok / p.rows_per_rank;
-      if (!((ready >> sh) & 1u)) {
-        if (!wait_flag(p.flags, sh, p.epoch, c)) ok = false;
-        else ready |= 1u << sh;
+    // my rows of this tile (nullptr: past the expert's last row)
+    const char* src[PASSES];
+#pragma unroll
+    for (int i = 0; i < PASSES; ++i) {
+      const int row = w.m0 + i * ROWS_PER_PASS + sub;
+      src[i] = nullptr;
+      if (row < w.row_end) {
+        const int slot = __ldg(p.row_to_slot + row);
+        const int tok = slot / p.topk;
+        const int sh = tok / p.rows_per_rank;
+        if (!((ready >> sh) & 1u)) {
+          if (!wait_flag(p.flags, sh, p.epoch, c)) ok = false;
+          else ready |= 1u << sh;
+        }
+        src[i] = static_cast<const char*>(p.xsrc[sh]) +
+                 static_cast<size_t>(tok - sh * p.rows_per_rank) * p.H * 2 + chunk * 16;
       }
-      src = static_cast<const char*>(p.xsrc[sh]) +
-            static_cast<size_t>(tok - sh * p.rows_per_rank) * p.H * 2;
     }
     if (!ok) break;
     const int nbox_b = min(G::B_BOXES, (p.N - w.nt * BN + B_BOX_N - 1) / B_BOX_N);
@@ -606,13 +617,13 @@ __device__ void producer_gather(const KParams& p, const Smem& s, const Ctl& c, i
         for (int j = 0; j < nbox_b; ++j)
           tma_load_3d(sb + j * B_BOX_N * BK * 2, &p.tmB[w.r], fb, w.nt * BN + j * B_BOX_N, kc, w.e);
       }
-      if (tid < BM) {
-        const uint32_t drow = sa + tid * 128;
+      {
+        const bool col_ok = kc + chunk * 8 < p.H;
 #pragma unroll
-        for (int ch = 0; ch < 8; ++ch) {
-          const uint32_t dst = drow + ((ch ^ (tid & 7)) << 4);
-          const int col = kc + ch * 8;
-          if (src != nullptr && col < p.H) cp_async_16(dst, src + static_cast<size_t>(col) * 2);
+        for (int i = 0; i < PASSES; ++i) {
+          const int r = i * ROWS_PER_PASS + sub;
+          const uint32_t dst = sa + r * 128 + ((chunk ^ (r & 7)) << 4);
+          if (src[i] != nullptr && col_ok) cp_async_16(dst, src[i] + static_cast<size_t>(kc) * 2);
           else cp_async_zero_16(dst, any_src);
         }
       }
@@ -989,7 +1000,7 @@ fused_gemm_kernel(const __grid_constant__ KParams p) {
     if (MODE != MODE_MOE_GATHER) tma_prefetch_desc(&p.tmA[lane]);
   }
   if (warp < KS::PRODUCER_WARPS) {
-    if (MODE == MODE_MOE_GATHER) {
+    if constexpr (MODE == MODE_MOE_GATHER) {
       producer_gather<KS::PRODUCER_WARPS * 32>(p, s, c, total_mt);
     } else if (lane == 0) {
       producer_tma<MODE, CL>(p, s, c, total_mt, rank);
