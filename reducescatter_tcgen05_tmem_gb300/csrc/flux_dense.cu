@@ -23,7 +23,8 @@ int grid_dt(flux_dtype_t dt, const DeviceInfo& dev, const flux_opts_t* opts, lon
 // Dense whole-tile kernels run on clusters of two CTA pairs stacked along M
 // (512 x 512 per cluster, B multicast between the pairs).
 constexpr int DENSE_CL = 4;
-using DenseGeo = Geo<Unit<DENSE_CL>::PAIR>;
+using DenseUnit = Unit<MODE_STORE, DENSE_CL>;
+using DenseGeo = Geo<DenseUnit::PAIR>;
 
 bool valid_dtype(flux_dtype_t dt) { return dt == FLUX_F16 || dt == FLUX_BF16; }
 
@@ -112,7 +113,7 @@ extern "C" flux_status_t flux_ag_gemm(int R, int M, int N, int K, flux_dtype_t d
   p.M = M;
   p.N = Nr;
   p.K = K;
-  p.Mt = (M + Unit<DENSE_CL>::ROWS - 1) / Unit<DENSE_CL>::ROWS;
+  p.Mt = (M + DenseUnit::ROWS - 1) / DenseUnit::ROWS;
   p.Nt = (Nr + DenseGeo::TILE_N - 1) / DenseGeo::TILE_N;
   p.KT = (K + BK - 1) / BK;
   p.ldo = Nr;
@@ -206,7 +207,7 @@ extern "C" flux_status_t flux_gemm_rs(int R, int M, int N, int K, flux_dtype_t d
     return launch_dt<MODE_REDUCE, 1>(dtype, p, grid, s);
   }
   p.Nt = (N + DenseGeo::TILE_N - 1) / DenseGeo::TILE_N;
-  p.Mt = (M + Unit<DENSE_CL>::ROWS - 1) / Unit<DENSE_CL>::ROWS;
+  p.Mt = (M + DenseUnit::ROWS - 1) / DenseUnit::ROWS;
   const int tiles = p.Mt * p.Nt;
   p.num_units = tiles * R;
   p.total_ksteps = static_cast<long long>(p.num_units) * p.KT;

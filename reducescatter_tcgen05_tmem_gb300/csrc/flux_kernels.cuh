@@ -41,9 +41,14 @@
 //           barrier.  A stage may be refilled only when both pairs' MMAs have
 //           read it: each "empty" barrier counts one commit per pair.
 //
-// The template parameter CL is the number of CTAs of a cluster (1, 2 or 4);
-// PAIR = min(CL, 2) is the tcgen05 CTA group and MC = CL / PAIR the pairs that
-// share B.
+// MoE, CL = 2: two single-CTA 128 x 256 tiles stacked along M inside one
+//           expert (a 256-row unit) share the B tile: each CTA loads half of
+//           the B boxes as a TMA multicast to both, and each CTA's MMA commit
+//           releases the stage in both.
+//
+// The template parameter CL is the number of CTAs of a cluster (1, 2 or 4).
+// For the dense modes PAIR = min(CL, 2) is the tcgen05 CTA group; the MoE
+// modes always use single-CTA MMAs.  MC = CL / PAIR tiles share each B box.
 //
 // Every wait is bounded: after timeout_ns (or an iteration cap) the thread
 // records FLUX_ERR_TIMEOUT in the workspace header, raises the per-call abort
@@ -291,9 +296,10 @@ struct Work {
 };
 
 // Rows of A covered by one work unit: 128 per CTA of the cluster.
-template <int CL>
+template <int MODE, int CL>
 struct Unit {
-  static constexpr int PAIR = CL >= 2 ? 2 : 1;
+  static constexpr bool DENSE = MODE == MODE_STORE || MODE == MODE_REDUCE;
+  static constexpr int PAIR = (CL >= 2 && DENSE) ? 2 : 1;
   static constexpr int MC = CL / PAIR;
   static constexpr int ROWS = BM * CL;
 };
@@ -305,7 +311,7 @@ struct Unit {
 // cluster; it holds rows m0 .. m0+127 of the unit.
 template <int CL>
 __device__ __forceinline__ Work decode_store(const KParams& p, int u, int cta) {
-  constexpr int TM = Unit<CL>::ROWS;
+  constexpr int TM = Unit<MODE_STORE, CL>::ROWS;
   Work w;
   const int per_rank = p.Mt * p.Nt;
   w.r = u / per_rank;
@@ -330,7 +336,7 @@ __device__ __forceinline__ Work decode_store(const KParams& p, int u, int cta) {
 // tile is still in L2.
 template <int CL>
 __device__ __forceinline__ Work decode_reduce(const KParams& p, int u, int cta) {
-  constexpr int TM = Unit<CL>::ROWS;
+  constexpr int TM = Unit<MODE_REDUCE, CL>::ROWS;
   Work w;
   const int tiles = p.Mt * p.Nt;
   const int TG = p.tiles_per_group;
@@ -357,9 +363,11 @@ __device__ __forceinline__ Work decode_reduce(const KParams& p, int u, int cta) 
   return w;
 }
 
-// MoE: unit -> (rank, grouped m-tile, n-tile); the expert of an m-tile comes
-// from the device tile-offset table written by the routing kernel.
-__device__ __forceinline__ Work decode_moe(const KParams& p, int u, int total_mt) {
+// MoE: unit -> (rank, grouped m-unit, n-tile); the expert of an m-unit comes
+// from the device table of each expert's first unit (units of BM * CL rows)
+// written by the routing kernel.  `cta` picks the 128-row part of the unit.
+template <int CL>
+__device__ __forceinline__ Work decode_moe(const KParams& p, int u, int total_mt, int cta) {
   Work w;
   const int per_rank = total_mt * p.Nt;
   w.r = u / per_rank;
@@ -374,7 +382,7 @@ __device__ __forceinline__ Work decode_moe(const KParams& p, int u, int total_mt
   }
   w.e = lo;
   const int e_off = __ldg(p.offsets + lo);
-  w.m0 = e_off + (gmt - __ldg(p.tile_off + lo)) * BM;
+  w.m0 = e_off + (gmt - __ldg(p.tile_off + lo)) * (BM * CL) + cta * BM;
   w.row_end = __ldg(p.offsets + lo + 1);
   w.mt = gmt;
   w.nt = nt;
@@ -425,7 +433,7 @@ struct ItemIter {
     if (u >= num_units) return false;
     if (MODE == MODE_STORE) w = decode_store<CL>(p, u, cta);
     else if (MODE == MODE_REDUCE) w = decode_reduce<CL>(p, u, cta);
-    else w = decode_moe(p, u, total_mt);
+    else w = decode_moe<CL>(p, u, total_mt, cta);
     u += stride;
     return true;
   }
@@ -460,12 +468,13 @@ __device__ __forceinline__ uint32_t pair_peer_bytes(const KParams& p, const Work
 // TMA producer (one thread).  `rank` is the CTA's rank in its cluster.
 template <int MODE, int CL>
 __device__ void producer_tma(const KParams& p, const Smem& s, const Ctl& c, int total_mt, int rank) {
-  constexpr int PAIR = Unit<CL>::PAIR;
-  constexpr int MC = Unit<CL>::MC;
+  constexpr int PAIR = Unit<MODE, CL>::PAIR;
+  constexpr int MC = Unit<MODE, CL>::MC;
   using G = Geo<PAIR>;
   const int cta = rank & (PAIR - 1);  // position in the pair
   const int half = rank / PAIR;       // MC = 2: the B half this CTA multicasts
-  const uint16_t mc_mask = static_cast<uint16_t>((1u << rank) | (1u << (rank ^ 2)));
+  // MC = 2: this CTA and the one holding the same B columns in the other tile
+  const uint16_t mc_mask = static_cast<uint16_t>((1u << rank) | (1u << (rank ^ PAIR)));
   ItemIter<MODE, CL> iter(p, total_mt, rank);
   Work w;
   uint32_t stage = 0, phase = 0;
@@ -501,7 +510,7 @@ __device__ void producer_tma(const KParams& p, const Smem& s, const Ctl& c, int 
     }
     for (int k = w.k0; k < w.k1; ++k) {
       // the empty barrier is completed by a remote commit whenever another CTA's MMAs read the stage
-      if (((PAIR == 2 && cta != 0) || MC == 2
+      if (((PAIR == 2 && cta != 0) || (MC == 2 && PAIR == 2)
                ? wait_bar_remote(smem_u32(&s.empty[stage]), phase ^ 1u, c, W_EMPTY, stage)
                : wait_bar(smem_u32(&s.empty[stage]), phase ^ 1u, c, W_EMPTY, stage)) != 0) {
         ok = false;
@@ -529,16 +538,18 @@ __device__ void producer_tma(const KParams& p, const Smem& s, const Ctl& c, int 
       }
       for (int j = 0; j < G::B_BOXES; ++j) {
         if (!((bmask >> j) & 1u)) continue;
+        if (MC == 2 && (j >> 1) != half) continue;  // the partner multicasts this box
         const int n = b_box_col<PAIR>(n0, cta, j);
-        if (MODE == MODE_MOE_SCATTER)
-          tma_load_3d(sb + j * B_BOX_N * BK * 2, &p.tmB[w.r], fb, n, kc, w.e);
-        else if (MC == 2) {
-          if ((j >> 1) == half)
-            tma_load_2d_pair_mc(sb + j * B_BOX_N * BK * 2, &p.tmB[w.r], fbc, n, kc, mc_mask);
-        } else if (PAIR == 2)
-          tma_load_2d_pair(sb + j * B_BOX_N * BK * 2, &p.tmB[w.r], fbc, n, kc);
-        else
-          tma_load_2d(sb + j * B_BOX_N * BK * 2, &p.tmB[w.r], fb, n, kc);
+        const uint32_t dst = sb + j * B_BOX_N * BK * 2;
+        if (MODE == MODE_MOE_SCATTER) {
+          if (MC == 2) tma_load_3d_mc(dst, &p.tmB[w.r], fb, n, kc, w.e, mc_mask);
+          else tma_load_3d(dst, &p.tmB[w.r], fb, n, kc, w.e);
+        } else if (PAIR == 2) {
+          if (MC == 2) tma_load_2d_pair_mc(dst, &p.tmB[w.r], fbc, n, kc, mc_mask);
+          else tma_load_2d_pair(dst, &p.tmB[w.r], fbc, n, kc);
+        } else {
+          tma_load_2d(dst, &p.tmB[w.r], fb, n, kc);
+        }
       }
       ++issued;
       if (++stage == G::STAGES) { stage = 0; phase ^= 1u; }
@@ -567,10 +578,13 @@ __device__ void producer_tma(const KParams& p, const Smem& s, const Ctl& c, int 
 // (i = 0..7) of the A tile, each from the token row of the rank that owns it,
 // into the 128B-swizzled layout the MMA descriptor expects.  Thread 0 also
 // issues the B tile by TMA.
-template <int NPROD>
-__device__ void producer_gather(const KParams& p, const Smem& s, const Ctl& c, int total_mt) {
+template <int NPROD, int CL>
+__device__ void producer_gather(const KParams& p, const Smem& s, const Ctl& c, int total_mt,
+                                int rank) {
   using G = Geo<1>;
-  ItemIter<MODE_MOE_GATHER, 1> iter(p, total_mt, 0);
+  constexpr int MC = Unit<MODE_MOE_GATHER, CL>::MC;
+  const uint16_t mc_mask = static_cast<uint16_t>((1u << rank) | (1u << (rank ^ 1)));
+  ItemIter<MODE_MOE_GATHER, CL> iter(p, total_mt, rank);
   const int tid = threadIdx.x;  // producer warps are warps 0 .. NPROD/32-1
   Work w;
   uint32_t stage = 0, phase = 0, issued = 0;
@@ -606,16 +620,25 @@ __device__ void producer_gather(const KParams& p, const Smem& s, const Ctl& c, i
     const int nbox_b = min(G::B_BOXES, (p.N - w.nt * BN + B_BOX_N - 1) / B_BOX_N);
     const uint32_t bytes_b = nbox_b * B_BOX_N * BK * 2;
     for (int k = w.k0; k < w.k1; ++k) {
-      int wr = wait_bar(smem_u32(&s.empty[stage]), phase ^ 1u, c, W_EMPTY, stage);
+      // (with MC = 2 the partner's MMA commit also completes this barrier; a
+      // blocking try_wait still sees that, and 128 polling threads cost more)
+      const int wr = wait_bar(smem_u32(&s.empty[stage]), phase ^ 1u, c, W_EMPTY, stage);
       if (wr != 0) { ok = false; break; }
       const uint32_t fb = smem_u32(&s.full[stage]);
       const uint32_t sa = smem_u32(s.a + stage * A_STAGE);
       const uint32_t sb = smem_u32(s.b + stage * G::B_STAGE);
       const int kc = k * BK;
       if (tid == 0) {
-        mbar_arrive_expect_tx(fb, bytes_b);
-        for (int j = 0; j < nbox_b; ++j)
-          tma_load_3d(sb + j * B_BOX_N * BK * 2, &p.tmB[w.r], fb, w.nt * BN + j * B_BOX_N, kc, w.e);
+        mbar_arrive_expect_tx(fb, bytes_b);  // all boxes land here, half of them from the partner
+        for (int j = 0; j < nbox_b; ++j) {
+          const uint32_t dst = sb + j * B_BOX_N * BK * 2;
+          const int n = w.nt * BN + j * B_BOX_N;
+          if (MC == 2) {
+            if ((j >> 1) == rank) tma_load_3d_mc(dst, &p.tmB[w.r], fb, n, kc, w.e, mc_mask);
+          } else {
+            tma_load_3d(dst, &p.tmB[w.r], fb, n, kc, w.e);
+          }
+        }
       }
       {
         const bool col_ok = kc + chunk * 8 < p.H;
@@ -659,7 +682,8 @@ __device__ void producer_gather(const KParams& p, const Smem& s, const Ctl& c, i
 template <int MODE, int DT, int CL>
 __device__ void mma_issuer(const KParams& p, const Smem& s, const Ctl& c, uint32_t tmem_base,
                            int total_mt, int rank) {
-  constexpr int PAIR = Unit<CL>::PAIR;
+  constexpr int PAIR = Unit<MODE, CL>::PAIR;
+  constexpr int MC = Unit<MODE, CL>::MC;
   using G = Geo<PAIR>;
   constexpr uint32_t IDESC = idesc_f16(DT, BM * PAIR, BN, 0, 1);
   // stage release reaches every CTA whose shared memory the stage's copies
@@ -702,6 +726,7 @@ __device__ void mma_issuer(const KParams& p, const Smem& s, const Ctl& c, uint32
         }
       }
       if (PAIR == 2) umma2_commit_mc(smem_u32(&s.empty[stage]), EMPTY_MASK);
+      else if (MC == 2) umma_commit_mc(smem_u32(&s.empty[stage]), EMPTY_MASK);
       else umma_commit(smem_u32(&s.empty[stage]));
       any = true;
       if (++stage == G::STAGES) { stage = 0; phase ^= 1u; }
@@ -777,7 +802,7 @@ __device__ __forceinline__ void convert8(float* src, uint16_t* dst) {
 template <int MODE, int DT, int CL>
 __device__ void epilogue(const KParams& p, const Smem& s, const Ctl& c, uint32_t tmem_base,
                          int total_mt, int warp, int rank) {
-  constexpr int PAIR = Unit<CL>::PAIR;
+  constexpr int PAIR = Unit<MODE, CL>::PAIR;
   const int cta = rank & (PAIR - 1);
   const int lane = threadIdx.x & 31;
   const int q = warp & 3;  // TMEM lane quarter this warp may access
@@ -934,11 +959,11 @@ template <int MODE, int DT, int CL>
 __global__ void __launch_bounds__(KernelShape<MODE, DT, CL>::THREADS, 1)
 fused_gemm_kernel(const __grid_constant__ KParams p) {
   using KS = KernelShape<MODE, DT, CL>;
-  constexpr int PAIR = Unit<CL>::PAIR;
-  constexpr int MC = Unit<CL>::MC;
+  constexpr int PAIR = Unit<MODE, CL>::PAIR;
+  constexpr int MC = Unit<MODE, CL>::MC;
   using G = Geo<PAIR>;
   static_assert(CL == 1 || CL == 2 || CL == 4, "cluster of 1, 2 or 4 CTAs");
-  static_assert(CL == 1 || (MODE == MODE_STORE || MODE == MODE_REDUCE), "clusters: dense modes");
+  static_assert(MC <= 2, "at most two tiles share a B box");
   extern __shared__ uint8_t smem_raw[];
   uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
@@ -1001,7 +1026,7 @@ fused_gemm_kernel(const __grid_constant__ KParams p) {
   }
   if (warp < KS::PRODUCER_WARPS) {
     if constexpr (MODE == MODE_MOE_GATHER) {
-      producer_gather<KS::PRODUCER_WARPS * 32>(p, s, c, total_mt);
+      producer_gather<KS::PRODUCER_WARPS * 32, CL>(p, s, c, total_mt, rank);
     } else if (lane == 0) {
       producer_tma<MODE, CL>(p, s, c, total_mt, rank);
     }

@@ -10,6 +10,13 @@
 namespace flux {
 
 constexpr int ROUTE_THREADS = 1024;
+// CTAs per cluster of the grouped GEMMs.  With 2, the two CTAs' 128-row tiles
+// are stacked in one expert and share B by multicast, and the tile-offset
+// table counts 256-row units; measured slower than single CTAs (the MoE
+// kernels are bound by the row gather and the scatter epilogue, not by TMA
+// requests), so single CTAs it is.
+constexpr int MOE_CL = 1;
+constexpr int MOE_UNIT_ROWS = BM * MOE_CL;
 constexpr int ROUTE_CHUNK = 8192;  // expert ids staged in shared memory per pass
 
 // Exclusive block-wide prefix sum of one int per thread (blockDim.x == 1024).
@@ -41,8 +48,8 @@ __device__ int block_exclusive_scan(int v, int* warp_sums, int* total) {
 
 // One CTA: counts[e], offsets[e] (exclusive prefix sum), the stable
 // permutation slot_to_row / row_to_slot (rows grouped by expert, ascending slot
-// order inside an expert) and, if tile_off != nullptr, the first BM-row tile of
-// each expert in the grouped GEMM.  Ids outside [0, E) are not routed; their
+// order inside an expert) and, if tile_off != nullptr, the first MOE_UNIT_ROWS-row
+// unit of each expert in the grouped GEMM.  Ids outside [0, E) are not routed; their
 // slot_to_row entry is -1 and FLUX_ERR_INVALID_ARG is recorded in hdr.
 __global__ void __launch_bounds__(ROUTE_THREADS, 1)
 moe_route_kernel(const int32_t* __restrict__ ids, int n, int E, int32_t* counts,
@@ -66,7 +73,7 @@ moe_route_kernel(const int32_t* __restrict__ ids, int n, int E, int32_t* counts,
   // E <= 1024 = blockDim: one expert per thread
   const int cnt = tid < E ? hist[tid] : 0;
   const int off = block_exclusive_scan(cnt, warp_sums, &totals[0]);
-  const int ntile = (cnt + BM - 1) / BM;
+  const int ntile = (cnt + MOE_UNIT_ROWS - 1) / MOE_UNIT_ROWS;
   const int toff = block_exclusive_scan(ntile, warp_sums, &totals[1]);
   if (tid < E) {
     counts[tid] = cnt;
@@ -111,14 +118,14 @@ moe_route_kernel(const int32_t* __restrict__ ids, int n, int E, int32_t* counts,
   if (bad && hdr != nullptr && tid == 0) atomicCAS(hdr + H_STATUS, 0u, ST_INVALID);
 }
 
-// tile_off[e] = sum_{e' < e} ceil(count_e' / BM) from a given offsets array.
+// tile_off[e] = sum_{e' < e} ceil(count_e' / MOE_UNIT_ROWS) from a given offsets array.
 __global__ void tile_offsets_kernel(const int32_t* offsets, int E, int32_t* tile_off) {
   if (threadIdx.x != 0 || blockIdx.x != 0) return;
   int acc = 0;
   for (int e = 0; e < E; ++e) {
     tile_off[e] = acc;
     const int c = offsets[e + 1] - offsets[e];
-    acc += (c > 0 ? (c + BM - 1) / BM : 0);
+    acc += (c > 0 ? (c + MOE_UNIT_ROWS - 1) / MOE_UNIT_ROWS : 0);
   }
   tile_off[E] = acc;
 }
@@ -127,14 +134,14 @@ namespace {
 
 template <int MODE>
 flux_status_t launch_dt(flux_dtype_t dt, const KParams& p, int grid, cudaStream_t s) {
-  return dt == FLUX_BF16 ? Launcher<MODE, 1, 1>::launch(p, grid, s)
-                         : Launcher<MODE, 0, 1>::launch(p, grid, s);
+  return dt == FLUX_BF16 ? Launcher<MODE, 1, MOE_CL>::launch(p, grid, s)
+                         : Launcher<MODE, 0, MOE_CL>::launch(p, grid, s);
 }
 
 template <int MODE>
 int grid_dt(flux_dtype_t dt, const DeviceInfo& dev, const flux_opts_t* opts, long long units) {
-  return dt == FLUX_BF16 ? grid_for<MODE, 1, 1>(dev, opts, units)
-                         : grid_for<MODE, 0, 1>(dev, opts, units);
+  return dt == FLUX_BF16 ? grid_for<MODE, 1, MOE_CL>(dev, opts, units)
+                         : grid_for<MODE, 0, MOE_CL>(dev, opts, units);
 }
 
 bool moe_shape_ok(int R, int T, int H, int F, int E, int topk) {
@@ -286,7 +293,8 @@ extern "C" flux_status_t flux_moe_ag_grouped_gemm(
   p.seq = next_seq();
   p.hdr = static_cast<uint32_t*>(workspace);
   const long long max_units =
-      (static_cast<long long>((n + BM - 1) / BM) + E) * p.Nt * static_cast<long long>(R);
+      (static_cast<long long>((n + MOE_UNIT_ROWS - 1) / MOE_UNIT_ROWS) + E) * p.Nt *
+      static_cast<long long>(R);
   const int grid = grid_dt<MODE_MOE_GATHER>(dtype, dev, opts, max_units);
   if (grid == 0) return FLUX_ERR_CUDA;
   return launch_dt<MODE_MOE_GATHER>(dtype, p, grid, s);
@@ -375,7 +383,8 @@ extern "C" flux_status_t flux_moe_grouped_gemm_rs(
   p.seq = next_seq();
   p.hdr = static_cast<uint32_t*>(workspace);
   const long long max_units =
-      (static_cast<long long>((n + BM - 1) / BM) + E) * p.Nt * static_cast<long long>(R);
+      (static_cast<long long>((n + MOE_UNIT_ROWS - 1) / MOE_UNIT_ROWS) + E) * p.Nt *
+      static_cast<long long>(R);
   const int grid = grid_dt<MODE_MOE_SCATTER>(dtype, dev, opts, max_units);
   if (grid == 0) return FLUX_ERR_CUDA;
   return launch_dt<MODE_MOE_SCATTER>(dtype, p, grid, s);
