@@ -24,7 +24,7 @@ int grid_dt(flux_dtype_t dt, const DeviceInfo& dev, const flux_opts_t* opts, lon
 // (512 x 512 per cluster, B multicast between the pairs).
 constexpr int DENSE_CL = 4;
 using DenseUnit = Unit<MODE_STORE, DENSE_CL>;
-using DenseGeo = Geo<DenseUnit::PAIR>;
+using DenseGeo = DenseUnit::G;
 
 bool valid_dtype(flux_dtype_t dt) { return dt == FLUX_F16 || dt == FLUX_BF16; }
 

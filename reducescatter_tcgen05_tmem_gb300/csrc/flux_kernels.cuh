@@ -75,29 +75,35 @@ constexpr int GATHER_LAG = 2;         // cp.async groups in flight before a stag
 //           swizzled layout of the accumulator tensor map (one tensor bulk
 //           reduce per buffer; the swizzle keeps the row-per-thread stores
 //           free of bank conflicts).
-//   MOE_SCATTER: 32 rows of 32 floats, each row padded to 144 bytes (one bulk
-//           reduce per row into that row's token).
+//   MOE_SCATTER: 32 rows of 32 floats, each row padded to 144 bytes (written
+//           by the row's thread, read back row-contiguously for the
+//           vector atomic adds into the rows' tokens).
 constexpr int STG_BOX = 32 * 32 * 4;
 constexpr int STG_PITCH = 144;
 constexpr int STG_WARP = 2 * STG_BOX;
 static_assert(32 * STG_PITCH <= STG_WARP, "row staging fits");
 
-template <int PAIR>
+// Tile geometry: PAIR CTAs form one tcgen05 CTA group (M = 128 PAIR), and NM
+// MMAs of N = 256 cover the tile's columns at every 16-deep k step.
+//   <1,1> 128 x 256, B 256 columns per CTA, 4 stages of 48 KB, 2 accumulators
+//   <2,1> 256 x 256, B 128 columns per CTA, 6 stages of 32 KB, 2 accumulators
+//   <2,2> 256 x 512, B 256 columns per CTA, 4 stages of 48 KB, 1 accumulator
+template <int PAIR, int NM>
 struct Geo {
-  static constexpr int STAGES = 4;
-  static constexpr int TILE_M = BM * PAIR;             // rows of one scheduled tile
-  static constexpr int TILE_N = BN * PAIR;             // columns of one scheduled tile
-  static constexpr int N_MMA = PAIR;                   // N = 256 MMAs per 16-deep k step
-  static constexpr int B_BOXES = 4;                    // 64-column B boxes per CTA and stage
-  static constexpr int B_STAGE = B_BOXES * B_BOX_N * BK * 2;  // 32 KB
-  static constexpr int ACC_BUFS = 2 / PAIR;            // accumulators in the 512 TMEM columns
+  static constexpr int TILE_M = BM * PAIR;             // rows of one tile
+  static constexpr int TILE_N = BN * NM;               // columns of one tile
+  static constexpr int N_MMA = NM;                     // N = 256 MMAs per 16-deep k step
+  static constexpr int B_BOXES = TILE_N / PAIR / B_BOX_N;  // 64-column B boxes per CTA and stage
+  static constexpr int B_STAGE = B_BOXES * B_BOX_N * BK * 2;
+  static constexpr int STAGES = (192 * 1024) / (A_STAGE + B_STAGE);
+  static constexpr int ACC_BUFS = 2 / NM;              // accumulators in the 512 TMEM columns
   static constexpr int ACC_COLS = TILE_N;              // TMEM columns of one accumulator
   static constexpr int SMEM = STAGES * (A_STAGE + B_STAGE) + EPI_WARPS * STG_WARP + 1024 /*align*/ +
                               512 /*barriers*/;
+  static_assert(ACC_BUFS * ACC_COLS == TMEM_COLS, "TMEM budget");
 };
-constexpr int SMEM_BYTES = Geo<1>::SMEM > Geo<2>::SMEM ? Geo<1>::SMEM : Geo<2>::SMEM;
-static_assert(Geo<1>::ACC_BUFS * Geo<1>::ACC_COLS == TMEM_COLS, "TMEM budget");
-static_assert(Geo<2>::ACC_BUFS * Geo<2>::ACC_COLS == TMEM_COLS, "TMEM budget");
+constexpr int cmax(int a, int b) { return a > b ? a : b; }
+constexpr int SMEM_BYTES = cmax(Geo<1, 1>::SMEM, cmax(Geo<2, 1>::SMEM, Geo<2, 2>::SMEM));
 
 // First output column of B box j (0..3) of CTA `cta` in a tile starting at
 // column n0.  A single CTA holds columns n0 .. n0+255 in order; a pair splits
@@ -112,11 +118,11 @@ __device__ __forceinline__ int b_box_col(int n0, int cta, int j) {
 // Boxes (bit j) that start inside the N columns; the others are not loaded
 // (their shared-memory slots keep stale data that only feeds columns >= N,
 // which are never stored).
-template <int PAIR>
+template <int PAIR, int NBOX>
 __device__ __forceinline__ uint32_t b_box_mask(int N, int n0, int cta) {
   uint32_t m = 0;
 #pragma unroll
-  for (int j = 0; j < 4; ++j)
+  for (int j = 0; j < NBOX; ++j)
     if (b_box_col<PAIR>(n0, cta, j) < N) m |= 1u << j;
   return m;
 }
@@ -295,13 +301,20 @@ struct Work {
   int tile;    // linear 128-row output-tile id of this CTA's part (REDUCE counters)
 };
 
-// Rows of A covered by one work unit: 128 per CTA of the cluster.
+// Shape of the work of one cluster of CL CTAs (128 rows of A per CTA).
+//   dense modes, CL 2 / 4: CTA pairs with 256 x 512 tiles (MC pairs share B)
+//   MOE_SCATTER, CL 2: one CTA pair, 256 x 256 tiles
+//   MOE_GATHER, CL 2: two single-CTA tiles sharing B (the gathered A rows
+//                     cannot complete on the other CTA's barrier)
 template <int MODE, int CL>
 struct Unit {
   static constexpr bool DENSE = MODE == MODE_STORE || MODE == MODE_REDUCE;
-  static constexpr int PAIR = (CL >= 2 && DENSE) ? 2 : 1;
+  static constexpr int PAIR = (CL >= 2 && MODE != MODE_MOE_GATHER) ? 2 : 1;
+  static constexpr int NM = (DENSE && PAIR == 2) ? 2 : 1;
   static constexpr int MC = CL / PAIR;
   static constexpr int ROWS = BM * CL;
+  using G = Geo<PAIR, NM>;
+  static_assert(!(MODE == MODE_MOE_SCATTER && MC == 2), "MoE layer1: no B sharing between pairs");
 };
 
 // AllGather / plain GEMM: unit -> (rank, m-tile, n-tile).  Ranks are the
@@ -453,15 +466,15 @@ struct Smem {
 };
 
 // Bytes the odd CTA of a pair loads for one stage of work item `w` (the even
-// CTA's view of the item): its 128 rows of A and its 256 columns of B.
-template <int MODE>
+// CTA's view of the item): its 128 rows of A and its columns of B.
+template <int MODE, class G>
 __device__ __forceinline__ uint32_t pair_peer_bytes(const KParams& p, const Work& w) {
   const int m0 = w.m0 + BM;
   int nbox_a = m0 < w.row_end ? 1 : 0;
   uint32_t a = nbox_a * A_STAGE;
   if (MODE == MODE_STORE && nbox_a)
     a = ((min(m0 + BM, w.row_end) - m0 + p.a_box_m - 1) / p.a_box_m) * p.a_box_m * BK * 2;
-  const uint32_t mask = b_box_mask<2>(p.N, w.nt * Geo<2>::TILE_N, 1);
+  const uint32_t mask = b_box_mask<2, G::B_BOXES>(p.N, w.nt * G::TILE_N, 1);
   return a + __popc(mask) * B_BOX_N * BK * 2;
 }
 
@@ -470,7 +483,7 @@ template <int MODE, int CL>
 __device__ void producer_tma(const KParams& p, const Smem& s, const Ctl& c, int total_mt, int rank) {
   constexpr int PAIR = Unit<MODE, CL>::PAIR;
   constexpr int MC = Unit<MODE, CL>::MC;
-  using G = Geo<PAIR>;
+  using G = typename Unit<MODE, CL>::G;
   const int cta = rank & (PAIR - 1);  // position in the pair
   const int half = rank / PAIR;       // MC = 2: the B half this CTA multicasts
   // MC = 2: this CTA and the one holding the same B columns in the other tile
@@ -501,12 +514,12 @@ __device__ void producer_tma(const KParams& p, const Smem& s, const Ctl& c, int 
       }
     }
     const int n0 = w.nt * G::TILE_N;
-    const uint32_t bmask = b_box_mask<PAIR>(p.N, n0, cta);
+    const uint32_t bmask = b_box_mask<PAIR, G::B_BOXES>(p.N, n0, cta);
     uint32_t bytes = ((MODE == MODE_STORE) ? nbox_a * p.a_box_m * BK * 2 : nbox_a * A_STAGE) +
                      __popc(bmask) * B_BOX_N * BK * 2;
     if (PAIR == 2 && cta == 0) {
       // the even CTA's barrier also counts the odd CTA's bytes of the same stage
-      bytes += pair_peer_bytes<MODE>(p, w);
+      bytes += pair_peer_bytes<MODE, G>(p, w);
     }
     for (int k = w.k0; k < w.k1; ++k) {
       // the empty barrier is completed by a remote commit whenever another CTA's MMAs read the stage
@@ -542,7 +555,7 @@ __device__ void producer_tma(const KParams& p, const Smem& s, const Ctl& c, int 
         const int n = b_box_col<PAIR>(n0, cta, j);
         const uint32_t dst = sb + j * B_BOX_N * BK * 2;
         if (MODE == MODE_MOE_SCATTER) {
-          if (MC == 2) tma_load_3d_mc(dst, &p.tmB[w.r], fb, n, kc, w.e, mc_mask);
+          if (PAIR == 2) tma_load_3d_pair(dst, &p.tmB[w.r], fbc, n, kc, w.e);
           else tma_load_3d(dst, &p.tmB[w.r], fb, n, kc, w.e);
         } else if (PAIR == 2) {
           if (MC == 2) tma_load_2d_pair_mc(dst, &p.tmB[w.r], fbc, n, kc, mc_mask);
@@ -581,7 +594,7 @@ __device__ void producer_tma(const KParams& p, const Smem& s, const Ctl& c, int 
 template <int NPROD, int CL>
 __device__ void producer_gather(const KParams& p, const Smem& s, const Ctl& c, int total_mt,
                                 int rank) {
-  using G = Geo<1>;
+  using G = typename Unit<MODE_MOE_GATHER, CL>::G;
   constexpr int MC = Unit<MODE_MOE_GATHER, CL>::MC;
   const uint16_t mc_mask = static_cast<uint16_t>((1u << rank) | (1u << (rank ^ 1)));
   ItemIter<MODE_MOE_GATHER, CL> iter(p, total_mt, rank);
@@ -684,7 +697,7 @@ __device__ void mma_issuer(const KParams& p, const Smem& s, const Ctl& c, uint32
                            int total_mt, int rank) {
   constexpr int PAIR = Unit<MODE, CL>::PAIR;
   constexpr int MC = Unit<MODE, CL>::MC;
-  using G = Geo<PAIR>;
+  using G = typename Unit<MODE, CL>::G;
   constexpr uint32_t IDESC = idesc_f16(DT, BM * PAIR, BN, 0, 1);
   // stage release reaches every CTA whose shared memory the stage's copies
   // fill; the accumulator-full signal only this pair
@@ -762,24 +775,41 @@ __device__ __forceinline__ void store_row_chunk(void* out, long long row_off_ele
   }
 }
 
-// Stage this thread's 32 fp32 values (times `scale`) as one 128-byte row of
-// the warp's staging buffer and hand the row to a bulk reduce-add into
-// global[dst .. dst + 4 * ncols_valid).  The previous bulk reduce of this
-// thread must have finished reading the row first.
-__device__ __forceinline__ void stage_and_reduce(float* dst, uint32_t srow, int ncols_valid,
-                                                 const uint32_t (&v)[32], float scale) {
-  bulk_wait_read_all();
+// Gate-weighted scatter-add of one 32-column chunk of a warp's 32 rows: every
+// thread stages its row (times its gate) in the warp's staging rows, then the
+// rows are read back so that eight lanes cover one 128-byte row and each
+// warp instruction adds four whole rows into their tokens' fp32 rows with
+// red.global.add.v4.f32 (the load/store path, clear of the TMA queue that
+// feeds the main loop).  Rows with row_ok == false add nothing.
+__device__ __forceinline__ void scatter_add_chunk(float* acc, int ld_acc, int col0, int ncols_valid,
+                                                  uint32_t sstg, int lane, int tok, bool row_ok,
+                                                  float gate, const uint32_t (&v)[32]) {
+  const uint32_t srow = sstg + lane * STG_PITCH;
+  __syncwarp();  // the previous chunk's read-back is done
 #pragma unroll
   for (int g = 0; g < 8; ++g) {
-    const float a = __uint_as_float(v[g * 4 + 0]) * scale, b = __uint_as_float(v[g * 4 + 1]) * scale;
-    const float c = __uint_as_float(v[g * 4 + 2]) * scale, d = __uint_as_float(v[g * 4 + 3]) * scale;
+    const float a = __uint_as_float(v[g * 4 + 0]) * gate, b = __uint_as_float(v[g * 4 + 1]) * gate;
+    const float c = __uint_as_float(v[g * 4 + 2]) * gate, d = __uint_as_float(v[g * 4 + 3]) * gate;
     asm volatile("st.shared.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(srow + g * 16), "f"(a), "f"(b),
                  "f"(c), "f"(d) : "memory");
   }
-  fence_proxy_async_smem();
-  const int n = ncols_valid < 32 ? ncols_valid : 32;
-  bulk_reduce_add_f32(dst, srow, static_cast<uint32_t>(n) * 4u);
-  bulk_commit();
+  __syncwarp();
+  const int cc = (lane & 7) * 4;  // float column inside the chunk
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const int rr = i * 4 + (lane >> 3);  // row of the warp's 32
+    const int t = __shfl_sync(0xFFFFFFFFu, tok, rr);
+    const int ok = __shfl_sync(0xFFFFFFFFu, row_ok ? 1 : 0, rr);
+    float x0, x1, x2, x3;
+    asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];"
+                 : "=f"(x0), "=f"(x1), "=f"(x2), "=f"(x3) : "r"(sstg + rr * STG_PITCH + cc * 4)
+                 : "memory");
+    if (ok && cc < ncols_valid) {
+      float* dst = acc + static_cast<long long>(t) * ld_acc + col0 + cc;
+      asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(dst), "f"(x0), "f"(x1),
+                   "f"(x2), "f"(x3) : "memory");
+    }
+  }
 }
 
 // Convert 8 consecutive fp32 accumulators (L2) to 16 bits, store them, and
@@ -814,8 +844,7 @@ __device__ void epilogue(const KParams& p, const Smem& s, const Ctl& c, uint32_t
                                ? mapa_shared(smem_u32(&s.tempty[0]), static_cast<uint32_t>(rank & ~1))
                                : smem_u32(&s.tempty[0]);
   const uint32_t sstg = smem_u32(s.stg + q * STG_WARP);
-  const uint32_t srow = sstg + lane * STG_PITCH;
-  using G = Geo<PAIR>;
+  using G = typename Unit<MODE, CL>::G;
   while (iter.next(w)) {
     const uint32_t b = it % G::ACC_BUFS;
     const uint32_t use = static_cast<uint32_t>(it / G::ACC_BUFS);
@@ -869,12 +898,12 @@ __device__ void epilogue(const KParams& p, const Smem& s, const Ctl& c, uint32_t
         continue;
       }
       const int nv = ncols - ch * 32;
-      if (!row_ok) continue;
-      if (MODE == MODE_STORE || MODE == MODE_MOE_GATHER) {
-        store_row_chunk<DT>(p.out[w.r], static_cast<long long>(row) * p.ldo, n0 + ch * 32, nv, v);
-      } else {
-        stage_and_reduce(p.acc + static_cast<long long>(tok) * p.N + n0 + ch * 32, srow, nv, v, gate);
+      if (MODE == MODE_MOE_SCATTER) {  // whole warp: shuffles inside
+        scatter_add_chunk(p.acc, p.N, n0 + ch * 32, nv, sstg, lane, tok, row_ok, gate, v);
+        continue;
       }
+      if (!row_ok) continue;
+      store_row_chunk<DT>(p.out[w.r], static_cast<long long>(row) * p.ldo, n0 + ch * 32, nv, v);
     }
     // hand the accumulator back to the MMA warp
     tc_fence_before();
@@ -885,7 +914,7 @@ __device__ void epilogue(const KParams& p, const Smem& s, const Ctl& c, uint32_t
     }
     ++it;
 
-    if (MODE == MODE_REDUCE || MODE == MODE_MOE_SCATTER) {
+    if (MODE == MODE_REDUCE) {
       // this thread's reduce-adds are performed and visible before any arrival count
       bulk_wait_all();
       fence_proxy_async_global();
@@ -920,7 +949,10 @@ __device__ void epilogue(const KParams& p, const Smem& s, const Ctl& c, uint32_t
         if (lane == 0) atomicExch(cnt, 0u);
       }
     } else if (MODE == MODE_MOE_SCATTER) {
+      // a row's adds were issued by eight lanes of the warp: every lane fences
+      // its own, and the warp barrier orders them all before the row's count
       __threadfence();
+      __syncwarp();
       uint32_t* cnt = p.counters + (static_cast<size_t>(tok) * p.Nt + w.nt);
       bool last = false;
       if (row_ok) {
@@ -961,7 +993,7 @@ fused_gemm_kernel(const __grid_constant__ KParams p) {
   using KS = KernelShape<MODE, DT, CL>;
   constexpr int PAIR = Unit<MODE, CL>::PAIR;
   constexpr int MC = Unit<MODE, CL>::MC;
-  using G = Geo<PAIR>;
+  using G = typename Unit<MODE, CL>::G;
   static_assert(CL == 1 || CL == 2 || CL == 4, "cluster of 1, 2 or 4 CTAs");
   static_assert(MC <= 2, "at most two tiles share a B box");
   extern __shared__ uint8_t smem_raw[];

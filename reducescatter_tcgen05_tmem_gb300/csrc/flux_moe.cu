@@ -10,13 +10,15 @@
 namespace flux {
 
 constexpr int ROUTE_THREADS = 1024;
-// CTAs per cluster of the grouped GEMMs.  With 2, the two CTAs' 128-row tiles
-// are stacked in one expert and share B by multicast, and the tile-offset
-// table counts 256-row units; measured slower than single CTAs (the MoE
-// kernels are bound by the row gather and the scatter epilogue, not by TMA
-// requests), so single CTAs it is.
-constexpr int MOE_CL = 1;
-constexpr int MOE_UNIT_ROWS = BM * MOE_CL;
+// CTAs per cluster of the grouped GEMMs; the tile-offset table of each
+// counts units of BM * CL rows inside an expert.
+//   layer0 (row gather): single CTAs.  (Two CTAs sharing B by multicast were
+//     measured slower: the A gather bounds it, and multicast does not lower
+//     the bytes each SM receives.)
+//   layer1: CTA pairs with 256 x 256 tiles, which halves the B bytes each SM
+//     receives per unit of tensor work.
+constexpr int MOE0_CL = 1;
+constexpr int MOE1_CL = 2;
 constexpr int ROUTE_CHUNK = 8192;  // expert ids staged in shared memory per pass
 
 // Exclusive block-wide prefix sum of one int per thread (blockDim.x == 1024).
@@ -48,13 +50,13 @@ __device__ int block_exclusive_scan(int v, int* warp_sums, int* total) {
 
 // One CTA: counts[e], offsets[e] (exclusive prefix sum), the stable
 // permutation slot_to_row / row_to_slot (rows grouped by expert, ascending slot
-// order inside an expert) and, if tile_off != nullptr, the first MOE_UNIT_ROWS-row
-// unit of each expert in the grouped GEMM.  Ids outside [0, E) are not routed; their
+// order inside an expert) and, if tile_off != nullptr, the first unit of
+// `unit_rows` rows of each expert in the grouped GEMM.  Ids outside [0, E) are not routed; their
 // slot_to_row entry is -1 and FLUX_ERR_INVALID_ARG is recorded in hdr.
 __global__ void __launch_bounds__(ROUTE_THREADS, 1)
 moe_route_kernel(const int32_t* __restrict__ ids, int n, int E, int32_t* counts,
                  int32_t* offsets, int32_t* slot_to_row, int32_t* row_to_slot, int32_t* tile_off,
-                 uint32_t* hdr) {
+                 int unit_rows, uint32_t* hdr) {
   __shared__ int hist[FLUX_MAX_EXPERTS];
   __shared__ int base[FLUX_MAX_EXPERTS];
   __shared__ int warp_sums[32];
@@ -73,7 +75,7 @@ moe_route_kernel(const int32_t* __restrict__ ids, int n, int E, int32_t* counts,
   // E <= 1024 = blockDim: one expert per thread
   const int cnt = tid < E ? hist[tid] : 0;
   const int off = block_exclusive_scan(cnt, warp_sums, &totals[0]);
-  const int ntile = (cnt + MOE_UNIT_ROWS - 1) / MOE_UNIT_ROWS;
+  const int ntile = (cnt + unit_rows - 1) / unit_rows;
   const int toff = block_exclusive_scan(ntile, warp_sums, &totals[1]);
   if (tid < E) {
     counts[tid] = cnt;
@@ -118,30 +120,30 @@ moe_route_kernel(const int32_t* __restrict__ ids, int n, int E, int32_t* counts,
   if (bad && hdr != nullptr && tid == 0) atomicCAS(hdr + H_STATUS, 0u, ST_INVALID);
 }
 
-// tile_off[e] = sum_{e' < e} ceil(count_e' / MOE_UNIT_ROWS) from a given offsets array.
-__global__ void tile_offsets_kernel(const int32_t* offsets, int E, int32_t* tile_off) {
+// tile_off[e] = sum_{e' < e} ceil(count_e' / unit_rows) from a given offsets array.
+__global__ void tile_offsets_kernel(const int32_t* offsets, int E, int unit_rows, int32_t* tile_off) {
   if (threadIdx.x != 0 || blockIdx.x != 0) return;
   int acc = 0;
   for (int e = 0; e < E; ++e) {
     tile_off[e] = acc;
     const int c = offsets[e + 1] - offsets[e];
-    acc += (c > 0 ? (c + MOE_UNIT_ROWS - 1) / MOE_UNIT_ROWS : 0);
+    acc += (c > 0 ? (c + unit_rows - 1) / unit_rows : 0);
   }
   tile_off[E] = acc;
 }
 
 namespace {
 
-template <int MODE>
+template <int MODE, int CL>
 flux_status_t launch_dt(flux_dtype_t dt, const KParams& p, int grid, cudaStream_t s) {
-  return dt == FLUX_BF16 ? Launcher<MODE, 1, MOE_CL>::launch(p, grid, s)
-                         : Launcher<MODE, 0, MOE_CL>::launch(p, grid, s);
+  return dt == FLUX_BF16 ? Launcher<MODE, 1, CL>::launch(p, grid, s)
+                         : Launcher<MODE, 0, CL>::launch(p, grid, s);
 }
 
-template <int MODE>
+template <int MODE, int CL>
 int grid_dt(flux_dtype_t dt, const DeviceInfo& dev, const flux_opts_t* opts, long long units) {
-  return dt == FLUX_BF16 ? grid_for<MODE, 1, MOE_CL>(dev, opts, units)
-                         : grid_for<MODE, 0, MOE_CL>(dev, opts, units);
+  return dt == FLUX_BF16 ? grid_for<MODE, 1, CL>(dev, opts, units)
+                         : grid_for<MODE, 0, CL>(dev, opts, units);
 }
 
 bool moe_shape_ok(int R, int T, int H, int F, int E, int topk) {
@@ -186,9 +188,10 @@ MoeWs moe_layout(flux_op_t op, int R, int T, int H, int F, int E, int topk) {
 }
 
 flux_status_t launch_route(const int32_t* ids, int n, int E, int32_t* counts, int32_t* offsets,
-                           int32_t* s2r, int32_t* r2s, int32_t* tile_off, uint32_t* hdr,
-                           cudaStream_t s) {
-  moe_route_kernel<<<1, ROUTE_THREADS, 0, s>>>(ids, n, E, counts, offsets, s2r, r2s, tile_off, hdr);
+                           int32_t* s2r, int32_t* r2s, int32_t* tile_off, int unit_rows,
+                           uint32_t* hdr, cudaStream_t s) {
+  moe_route_kernel<<<1, ROUTE_THREADS, 0, s>>>(ids, n, E, counts, offsets, s2r, r2s, tile_off,
+                                               unit_rows, hdr);
   cudaError_t e = cudaGetLastError();
   return e == cudaSuccess ? FLUX_OK : cuda_fail(e);
 }
@@ -223,7 +226,7 @@ extern "C" flux_status_t flux_moe_route(int T, int E, int topk, const int32_t* t
   DeviceInfo dev;
   flux_status_t st = current_device(&dev);
   if (st != FLUX_OK) return st;
-  return launch_route(topk_ids, n, E, counts, offsets, slot_to_row, row_to_slot, nullptr,
+  return launch_route(topk_ids, n, E, counts, offsets, slot_to_row, row_to_slot, nullptr, BM,
                       static_cast<uint32_t*>(workspace), static_cast<cudaStream_t>(stream));
 }
 
@@ -255,7 +258,7 @@ extern "C" flux_status_t flux_moe_ag_grouped_gemm(
   uint8_t* ws = static_cast<uint8_t*>(workspace);
   int32_t* tile_off = reinterpret_cast<int32_t*>(ws + L.tile_off);
   if ((st = launch_route(topk_ids, n, E, counts, offsets, slot_to_row, row_to_slot, tile_off,
-                         static_cast<uint32_t*>(workspace), s)) != FLUX_OK)
+                         BM * MOE0_CL, static_cast<uint32_t*>(workspace), s)) != FLUX_OK)
     return st;
   if (n == 0 || Fr == 0) return FLUX_OK;
   if (H == 0) {
@@ -293,11 +296,11 @@ extern "C" flux_status_t flux_moe_ag_grouped_gemm(
   p.seq = next_seq();
   p.hdr = static_cast<uint32_t*>(workspace);
   const long long max_units =
-      (static_cast<long long>((n + MOE_UNIT_ROWS - 1) / MOE_UNIT_ROWS) + E) * p.Nt *
+      (static_cast<long long>((n + BM * MOE0_CL - 1) / (BM * MOE0_CL)) + E) * p.Nt *
       static_cast<long long>(R);
-  const int grid = grid_dt<MODE_MOE_GATHER>(dtype, dev, opts, max_units);
+  const int grid = grid_dt<MODE_MOE_GATHER, MOE0_CL>(dtype, dev, opts, max_units);
   if (grid == 0) return FLUX_ERR_CUDA;
-  return launch_dt<MODE_MOE_GATHER>(dtype, p, grid, s);
+  return launch_dt<MODE_MOE_GATHER, MOE0_CL>(dtype, p, grid, s);
 }
 
 extern "C" flux_status_t flux_moe_grouped_gemm_rs(
@@ -343,11 +346,11 @@ extern "C" flux_status_t flux_moe_grouped_gemm_rs(
     row_to_slot = reinterpret_cast<int32_t*>(ws + L.r2s);
     if ((st = launch_route(topk_ids, n, E, reinterpret_cast<int32_t*>(ws + L.counts),
                            const_cast<int32_t*>(offsets), reinterpret_cast<int32_t*>(ws + L.s2r),
-                           const_cast<int32_t*>(row_to_slot), tile_off,
+                           const_cast<int32_t*>(row_to_slot), tile_off, BM * MOE1_CL,
                            static_cast<uint32_t*>(workspace), s)) != FLUX_OK)
       return st;
   } else {
-    tile_offsets_kernel<<<1, 32, 0, s>>>(offsets, E, tile_off);
+    tile_offsets_kernel<<<1, 32, 0, s>>>(offsets, E, BM * MOE1_CL, tile_off);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return cuda_fail(e);
   }
@@ -383,9 +386,9 @@ extern "C" flux_status_t flux_moe_grouped_gemm_rs(
   p.seq = next_seq();
   p.hdr = static_cast<uint32_t*>(workspace);
   const long long max_units =
-      (static_cast<long long>((n + MOE_UNIT_ROWS - 1) / MOE_UNIT_ROWS) + E) * p.Nt *
+      (static_cast<long long>((n + BM * MOE1_CL - 1) / (BM * MOE1_CL)) + E) * p.Nt *
       static_cast<long long>(R);
-  const int grid = grid_dt<MODE_MOE_SCATTER>(dtype, dev, opts, max_units);
+  const int grid = grid_dt<MODE_MOE_SCATTER, MOE1_CL>(dtype, dev, opts, max_units);
   if (grid == 0) return FLUX_ERR_CUDA;
-  return launch_dt<MODE_MOE_SCATTER>(dtype, p, grid, s);
+  return launch_dt<MODE_MOE_SCATTER, MOE1_CL>(dtype, p, grid, s);
 }
