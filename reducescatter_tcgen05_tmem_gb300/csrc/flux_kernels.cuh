@@ -757,20 +757,41 @@ __device__ void mma_issuer(const KParams& p, const Smem& s, const Ctl& c, uint32
 }
 
 // epilogue helpers -----------------------------------------------------------
+// Store one 64-column chunk of a warp's 32 rows as 16-bit values: every
+// thread stages its row (128 bytes) in the warp's staging rows, then the rows
+// are read back so that eight lanes cover one row and each warp instruction
+// writes four whole 128-byte rows.  Rows >= rows_valid and columns >=
+// ncols_valid (a multiple of 8) are not written.
 template <int DT>
-__device__ __forceinline__ void store_row_chunk(void* out, long long row_off_elems, int col0,
-                                                int ncols_valid, const uint32_t (&v)[32]) {
-  // 32 fp32 -> 32 x 16-bit, four 16-byte stores (columns col0 .. col0+31)
-  uint16_t* o = static_cast<uint16_t*>(out) + row_off_elems + col0;
+__device__ __forceinline__ void store_rows_chunk64(void* out, int ldo, long long row0, int rows_valid,
+                                                   int col0, int ncols_valid, uint32_t sstg, int lane,
+                                                   const uint32_t (&v)[32], const uint32_t (&u)[32]) {
+  const uint32_t srow = sstg + lane * STG_PITCH;
+  __syncwarp();  // the previous chunk's read-back is done
 #pragma unroll
-  for (int g = 0; g < 4; ++g) {
-    if (g * 8 < ncols_valid) {
-      uint4 q;
-      q.x = pack2<DT>(__uint_as_float(v[g * 8 + 0]), __uint_as_float(v[g * 8 + 1]));
-      q.y = pack2<DT>(__uint_as_float(v[g * 8 + 2]), __uint_as_float(v[g * 8 + 3]));
-      q.z = pack2<DT>(__uint_as_float(v[g * 8 + 4]), __uint_as_float(v[g * 8 + 5]));
-      q.w = pack2<DT>(__uint_as_float(v[g * 8 + 6]), __uint_as_float(v[g * 8 + 7]));
-      *reinterpret_cast<uint4*>(o + g * 8) = q;
+  for (int g = 0; g < 8; ++g) {
+    const uint32_t(&x)[32] = g < 4 ? v : u;
+    const int b = (g & 3) * 8;
+    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};"
+                 ::"r"(srow + g * 16),
+                   "r"(pack2<DT>(__uint_as_float(x[b + 0]), __uint_as_float(x[b + 1]))),
+                   "r"(pack2<DT>(__uint_as_float(x[b + 2]), __uint_as_float(x[b + 3]))),
+                   "r"(pack2<DT>(__uint_as_float(x[b + 4]), __uint_as_float(x[b + 5]))),
+                   "r"(pack2<DT>(__uint_as_float(x[b + 6]), __uint_as_float(x[b + 7])))
+                 : "memory");
+  }
+  __syncwarp();
+  const int cc = (lane & 7) * 8;  // 16-bit column inside the chunk
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const int rr = i * 4 + (lane >> 3);
+    uint32_t a, b, c, d;
+    asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(a), "=r"(b), "=r"(c), "=r"(d) : "r"(sstg + rr * STG_PITCH + (lane & 7) * 16)
+                 : "memory");
+    if (rr < rows_valid && cc < ncols_valid) {
+      uint16_t* dst = static_cast<uint16_t*>(out) + (row0 + rr) * ldo + col0 + cc;
+      *reinterpret_cast<uint4*>(dst) = make_uint4(a, b, c, d);
     }
   }
 }
@@ -857,7 +878,8 @@ __device__ void epilogue(const KParams& p, const Smem& s, const Ctl& c, uint32_t
     wr = __shfl_sync(0xFFFFFFFFu, wr, 0);
     if (wr != 0) break;
     tc_fence_after();
-    const int row = w.m0 + q * 32 + lane;  // row of the A row space held by this thread
+    const int row0 = w.m0 + q * 32;       // first of this warp's 32 rows
+    const int row = row0 + lane;           // row of the A row space held by this thread
     const bool row_ok = row < w.row_end;
     const uint32_t taddr = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + b * G::ACC_COLS;
     const int n0 = w.nt * G::TILE_N;
@@ -870,40 +892,26 @@ __device__ void epilogue(const KParams& p, const Smem& s, const Ctl& c, uint32_t
       tok = slot / p.topk;
       gate = __ldg(p.topk_w + slot);
     }
-    const int row0 = w.m0 + q * 32;  // first row of this warp's 32-row box
-    for (int ch = 0; ch < G::TILE_N / 32; ++ch) {
-      if (ch * 32 >= ncols) break;  // warp-uniform
-      uint32_t v[32];
-      tmem_ld_32x32b_x32(taddr + ch * 32, v);
-      if (MODE == MODE_REDUCE) {
-        // the warp's 32 x 32 fp32 box goes out as one tensor bulk reduce-add;
-        // buffer ch & 1 is free once at most one newer group still reads
-        if (row0 >= w.row_end) continue;  // warp-uniform: nothing of the box is inside
-        const uint32_t buf = sstg + (ch & 1) * STG_BOX;
-        if (ch >= 2) {
-          if (lane == 0) bulk_wait_read<1>();
-          __syncwarp();
-        }
-#pragma unroll
-        for (int g = 0; g < 8; ++g)
-          asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};"
-                       ::"r"(buf + lane * 128 + ((g ^ (lane & 7)) << 4)), "r"(v[g * 4 + 0]),
-                         "r"(v[g * 4 + 1]), "r"(v[g * 4 + 2]), "r"(v[g * 4 + 3]) : "memory");
-        fence_proxy_async_smem();
-        __syncwarp();
-        if (lane == 0) {
-          tma_reduce_add_2d(&p.tmAcc, buf, n0 + ch * 32, row0);
-          bulk_commit();
-        }
-        continue;
+    if (MODE == MODE_STORE || MODE == MODE_MOE_GATHER) {
+      // 64 columns at a time: two TMEM loads, one row-contiguous store pass
+      for (int ch = 0; ch < G::TILE_N / 64; ++ch) {
+        if (ch * 64 >= ncols) break;  // warp-uniform
+        uint32_t v[32], u[32];
+        tmem_ld_32x32b_x32(taddr + ch * 64, v);
+        tmem_ld_32x32b_x32(taddr + ch * 64 + 32, u);
+        store_rows_chunk64<DT>(p.out[w.r], p.ldo, row0, w.row_end - row0, n0 + ch * 64,
+                               ncols - ch * 64, sstg, lane, v, u);
       }
-      const int nv = ncols - ch * 32;
-      if (MODE == MODE_MOE_SCATTER) {  // whole warp: shuffles inside
-        scatter_add_chunk(p.acc, p.N, n0 + ch * 32, nv, sstg, lane, tok, row_ok, gate, v);
-        continue;
+    } else {
+      // fp32 adds: into this tile's own rows (REDUCE) or the rows' tokens,
+      // gate-weighted (MOE_SCATTER)
+      const int key = MODE == MODE_REDUCE ? row : tok;
+      for (int ch = 0; ch < G::TILE_N / 32; ++ch) {
+        if (ch * 32 >= ncols) break;  // warp-uniform
+        uint32_t v[32];
+        tmem_ld_32x32b_x32(taddr + ch * 32, v);
+        scatter_add_chunk(p.acc, p.N, n0 + ch * 32, ncols - ch * 32, sstg, lane, key, row_ok, gate, v);
       }
-      if (!row_ok) continue;
-      store_row_chunk<DT>(p.out[w.r], static_cast<long long>(row) * p.ldo, n0 + ch * 32, nv, v);
     }
     // hand the accumulator back to the MMA warp
     tc_fence_before();
@@ -915,14 +923,11 @@ __device__ void epilogue(const KParams& p, const Smem& s, const Ctl& c, uint32_t
     ++it;
 
     if (MODE == MODE_REDUCE) {
-      // this thread's reduce-adds are performed and visible before any arrival count
-      bulk_wait_all();
-      fence_proxy_async_global();
-    }
-    if (MODE == MODE_REDUCE) {
       // arrival counter of this tile's 32-row quarter counts k-slices; quarters
       // wholly past the last row have nothing to count
-      if (w.m0 + q * 32 >= w.row_end) continue;
+      if (row0 >= w.row_end) continue;
+      // the rows' adds were issued by eight lanes each: every lane fences its
+      // own, and the warp barrier orders them all before the count
       __threadfence();
       __syncwarp();
       const uint32_t nk = static_cast<uint32_t>(w.k1 - w.k0);
