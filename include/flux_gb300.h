@@ -89,7 +89,7 @@ typedef struct {
   uint32_t reserved0;
   uint64_t timeout_ns;  /* bound on every device-side wait (0 = 2 s) */
   int32_t num_ctas;     /* persistent grid size (0 = one CTA per SM) */
-  int32_t group_n;      /* tile raster: n-tiles per band (0 = 8) */
+  int32_t group_n;      /* tile raster: n-tiles per band (0 = 4 for AllGather + GEMM, else 8) */
   int32_t tiles_per_group; /* GEMM-RS: output tiles per rank-group (0 = grid size) */
   int32_t reserved1;
 } flux_opts_t;

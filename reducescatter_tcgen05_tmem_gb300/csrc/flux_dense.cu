@@ -122,6 +122,8 @@ extern "C" flux_status_t flux_ag_gemm(int R, int M, int N, int K, flux_dtype_t d
   p.num_units = R * p.Mt * p.Nt;
   p.flags = ready_flags;
   fill_common(p, opts, workspace);
+  // bands of 4 n-tiles (2048 columns) measured best for the 512 x 512 units
+  if (!(opts && opts->group_n > 0)) p.group_n = 4;
   const int grid = grid_dt<MODE_STORE, DENSE_CL>(dtype, dev, opts, p.num_units);
   if (grid == 0) return FLUX_ERR_CUDA;
   return launch_dt<MODE_STORE, DENSE_CL>(dtype, p, grid, s);

@@ -19,7 +19,9 @@ constexpr int ROUTE_THREADS = 1024;
 //     receives per unit of tensor work.
 constexpr int MOE0_CL = 1;
 constexpr int MOE1_CL = 2;
-constexpr int ROUTE_CHUNK = 8192;  // expert ids staged in shared memory per pass
+constexpr int ROUTE_CHUNK = 4096;  // expert ids staged in shared memory per pass
+constexpr int ROUTE_WARPS = ROUTE_THREADS / 32;
+constexpr int ROUTE_PAR_E = 64;    // up to this many experts all warps share the permutation
 
 // Exclusive block-wide prefix sum of one int per thread (blockDim.x == 1024).
 __device__ int block_exclusive_scan(int v, int* warp_sums, int* total) {
@@ -62,6 +64,7 @@ moe_route_kernel(const int32_t* __restrict__ ids, int n, int E, int32_t* counts,
   __shared__ int warp_sums[32];
   __shared__ int totals[2];
   __shared__ int stage[ROUTE_CHUNK];
+  __shared__ int warp_base[ROUTE_WARPS][ROUTE_PAR_E];
   const int tid = threadIdx.x;
   for (int e = tid; e < E; e += ROUTE_THREADS) hist[e] = 0;
   __syncthreads();
@@ -88,13 +91,59 @@ moe_route_kernel(const int32_t* __restrict__ ids, int n, int E, int32_t* counts,
     if (tile_off) tile_off[E] = totals[1];
   }
   __syncthreads();
-  // stable permutation: the first warp walks the slots in order, 32 at a time
-  const int lane = tid & 31;
+  // stable permutation: row(slot) = offsets[e] + number of earlier slots of
+  // expert e.  Slots are taken 32 at a time; __match_any_sync ranks the lanes
+  // of one expert inside a group.
+  const int lane = tid & 31, warp = tid >> 5;
   for (int c0 = 0; c0 < n; c0 += ROUTE_CHUNK) {
     const int cn = min(ROUTE_CHUNK, n - c0);
     for (int i = tid; i < cn; i += ROUTE_THREADS) stage[i] = ids[c0 + i];
     __syncthreads();
-    if (tid < 32) {
+    if (E <= ROUTE_PAR_E) {
+      // every warp takes a contiguous run of the chunk: count per expert,
+      // scan the counts over the warps (in slot order), then place
+      const int per = ((cn + ROUTE_WARPS * 32 - 1) / (ROUTE_WARPS * 32)) * 32;
+      const int lo = warp * per, hi = min(cn, lo + per);
+      for (int e = lane; e < E; e += 32) warp_base[warp][e] = 0;
+      __syncwarp();
+      for (int i0 = lo; i0 < hi; i0 += 32) {
+        const int i = i0 + lane;
+        const int e = i < hi ? stage[i] : -1;
+        const bool valid = i < hi && e >= 0 && e < E;
+        const unsigned mask = __match_any_sync(0xFFFFFFFFu, valid ? e : -1 - lane);
+        if (valid && lane == __ffs(mask) - 1) warp_base[warp][e] += __popc(mask);
+        __syncwarp();
+      }
+      __syncthreads();
+      if (tid < E) {
+        int run = base[tid];
+        for (int w = 0; w < ROUTE_WARPS; ++w) {
+          const int c = warp_base[w][tid];
+          warp_base[w][tid] = run;
+          run += c;
+        }
+        base[tid] = run;
+      }
+      __syncthreads();
+      for (int i0 = lo; i0 < hi; i0 += 32) {
+        const int i = i0 + lane;
+        const int e = i < hi ? stage[i] : -1;
+        const bool valid = i < hi && e >= 0 && e < E;
+        const unsigned mask = __match_any_sync(0xFFFFFFFFu, valid ? e : -1 - lane);
+        const int rank = __popc(mask & ((1u << lane) - 1u));
+        if (valid) {
+          const int row = warp_base[warp][e] + rank;
+          slot_to_row[c0 + i] = row;
+          row_to_slot[row] = c0 + i;
+        } else if (i < hi) {
+          slot_to_row[c0 + i] = -1;
+        }
+        __syncwarp();
+        if (valid && lane == __ffs(mask) - 1) warp_base[warp][e] += __popc(mask);
+        __syncwarp();
+      }
+    } else if (tid < 32) {
+      // many experts: the first warp walks the chunk in order
       for (int i0 = 0; i0 < cn; i0 += 32) {
         const int i = i0 + lane;
         const int e = i < cn ? stage[i] : -1;
