@@ -91,14 +91,17 @@ typedef struct {
   int32_t num_ctas;     /* persistent grid size (0 = one CTA per SM) */
   int32_t group_n;      /* tile raster: n-tiles per band (0 = 4 for AllGather + GEMM, else 8) */
   int32_t tiles_per_group; /* GEMM-RS: output tiles per rank-group (0 = grid size) */
-  int32_t reserved1;
+  int32_t deterministic_rs; /* GEMM-RS: nonzero = add the ranks' fp32 partials in ascending
+                               rank order (bit-reproducible; slower: the adds of one tile
+                               are serialised over the ranks) */
 } flux_opts_t;
 
 /* What flux_get_status found in a workspace header. */
 typedef struct {
   uint32_t status; /* flux_status_t of the first device-side error, 0 if none */
   uint32_t where;  /* which wait gave up: 1 ready flag, 2 smem slot free, 3 smem slot full,
-                      4 accumulator free, 5 accumulator full, 6 drain */
+                      4 accumulator free, 5 accumulator full, 6 drain,
+                      7 deterministic GEMM-RS turn */
   uint32_t arg0;   /* flag wait: shard index; pipeline waits: CTA index */
   uint32_t arg1;   /* flag wait: last flag value seen; pipeline waits: stage / buffer */
 } flux_device_report_t;

@@ -194,7 +194,10 @@ extern "C" flux_status_t flux_gemm_rs(int R, int M, int N, int K, flux_dtype_t d
   // pairs, strided over a persistent grid.
   const int sm = (opts && opts->num_ctas > 0) ? opts->num_ctas : dev.sm_count;
   const long long units128 = static_cast<long long>((M + BM - 1) / BM) * ((N + BN - 1) / BN) * R;
-  if (units128 < 4 * sm) {
+  // deterministic_rs: whole tiles (no k split), each rank's partial of a tile
+  // on consecutive units (tile-major), added in ascending rank order
+  p.deterministic = (opts && opts->deterministic_rs) ? 1 : 0;
+  if (units128 < 4 * sm && !p.deterministic) {
     p.Nt = (N + BN - 1) / BN;
     p.Mt = (M + BM - 1) / BM;
     p.num_units = p.Mt * p.Nt * R;
@@ -216,7 +219,8 @@ extern "C" flux_status_t flux_gemm_rs(int R, int M, int N, int K, flux_dtype_t d
   p.stream_k = 0;
   const int grid = grid_dt<MODE_REDUCE, DENSE_CL>(dtype, dev, opts, p.num_units);
   if (grid == 0) return FLUX_ERR_CUDA;
-  const int tg = (opts && opts->tiles_per_group > 0) ? opts->tiles_per_group : grid / DENSE_CL;
+  const int tg = p.deterministic ? 1
+                : (opts && opts->tiles_per_group > 0) ? opts->tiles_per_group : grid / DENSE_CL;
   p.tiles_per_group = tg < tiles ? tg : tiles;
   return launch_dt<MODE_REDUCE, DENSE_CL>(dtype, p, grid, s);
 }

@@ -131,7 +131,7 @@ enum Mode { MODE_STORE = 0, MODE_REDUCE = 1, MODE_MOE_GATHER = 2, MODE_MOE_SCATT
 
 // device status header at the start of every workspace (256 bytes)
 enum HdrField { H_STATUS = 0, H_WHERE = 1, H_ARG0 = 2, H_ARG1 = 3, H_ABORT = 4 };
-enum WaitSite { W_FLAG = 1, W_EMPTY = 2, W_FULL = 3, W_TEMPTY = 4, W_TFULL = 5, W_DRAIN = 6 };
+enum WaitSite { W_FLAG = 1, W_EMPTY = 2, W_FULL = 3, W_TEMPTY = 4, W_TFULL = 5, W_DRAIN = 6, W_TURN = 7 };
 constexpr uint32_t ST_TIMEOUT = 5;
 constexpr uint32_t ST_INVALID = 1;
 
@@ -152,6 +152,7 @@ struct KParams {
   int group_n;             // raster band width in n-tiles
   int tiles_per_group;     // REDUCE: output tiles per rank-group
   int stream_k;            // REDUCE: 1 = contiguous k-step ranges per CTA
+  int deterministic;       // REDUCE: ranks add their partials in ascending order
   int num_units;           // dense modes: number of work units
   long long total_ksteps;  // REDUCE stream-K: num_units * KT
   const uint32_t* flags;   // AG ready flags (nullptr = all ready)
@@ -274,6 +275,27 @@ static __device__ __noinline__ bool wait_flag(const uint32_t* flags, int s, uint
       if (aborted(c)) return false;
       if (globaltimer() - t0 > c.flag_timeout || it > (1u << 28)) {
         raise_error(c, ST_TIMEOUT, W_FLAG, static_cast<uint32_t>(s), v);
+        return false;
+      }
+    }
+  }
+}
+
+// Bounded wait until *cnt >= target (acquire at gpu scope): the deterministic
+// GEMM-RS turn of one rank on one 32-row quarter.  True when it is this
+// rank's turn.
+static __device__ __noinline__ bool wait_turn(const uint32_t* cnt, uint32_t target, const Ctl& c) {
+  uint32_t v = ld_acquire_u32(cnt);
+  if (v >= target) return true;
+  const uint64_t t0 = globaltimer();
+  for (uint32_t it = 1;; ++it) {
+    __nanosleep(64);
+    v = ld_acquire_u32(cnt);
+    if (v >= target) return true;
+    if ((it & 7u) == 0u) {
+      if (aborted(c)) return false;
+      if (globaltimer() - t0 > c.pipe_timeout || it > (1u << 28)) {
+        raise_error(c, ST_TIMEOUT, W_TURN, target, v);
         return false;
       }
     }
@@ -906,6 +928,17 @@ __device__ void epilogue(const KParams& p, const Smem& s, const Ctl& c, uint32_t
       // fp32 adds: into this tile's own rows (REDUCE) or the rows' tokens,
       // gate-weighted (MOE_SCATTER)
       const int key = MODE == MODE_REDUCE ? row : tok;
+      if (MODE == MODE_REDUCE && p.deterministic && row0 < w.row_end) {
+        // ranks add in ascending order: wait until every lower rank's k-slices
+        // of this quarter are in (its adds were fenced before it counted them)
+        int ok_turn = 1;
+        if (lane == 0)
+          ok_turn = wait_turn(p.counters + (static_cast<size_t>(w.tile) * 4 + q),
+                              static_cast<uint32_t>(w.r) * static_cast<uint32_t>(p.KT), c) ? 1 : 0;
+        ok_turn = __shfl_sync(0xFFFFFFFFu, ok_turn, 0);
+        __syncwarp();  // the lanes' adds are ordered after lane 0's acquire
+        if (!ok_turn) break;  // TMEM stays held: the MMA side times out too
+      }
       for (int ch = 0; ch < G::TILE_N / 32; ++ch) {
         if (ch * 32 >= ncols) break;  // warp-uniform
         uint32_t v[32];

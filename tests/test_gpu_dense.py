@@ -177,6 +177,38 @@ def test_gemm_rs_integer_inputs_bit_exact_and_workspace_returns_to_zero():
     assert torch.count_nonzero(ws).item() == 0
 
 
+@pytest.mark.parametrize("R,M,N,K,dtype,num_ctas", [
+    (4, 512, 1024, 1024, "bf16", 0),   # whole 512 x 512 cluster units
+    (8, 128, 2048, 4096, "bf16", 0),   # decode-like shape: no k split in this mode
+    (8, 192, 264, 576, "f16", 8),      # ragged tails on two clusters: a tile's ranks alternate
+])
+def test_gemm_rs_deterministic_repeats_bit_for_bit(R, M, N, K, dtype, num_ctas):
+    # ranks add in ascending order: a second call on the re-zeroed workspace gives the same bits
+    c = configs.small(configs.CONFIGS["rs_mlp1"], R=R, M=M, N=N, K=K, dtype=dtype, seed=60 + R)
+    opts = {"deterministic_rs": 1, "num_ctas": num_ctas}
+    As, Bs, out, ws = _rs_case(c, opts=opts)
+    _ok(ws)
+    first = [o.clone() for o in out]
+    fx.flux_gemm_rs(R, M, N, K, DT[dtype], [to_device(a, dtype) for a in As],
+                    [to_device(b, dtype) for b in Bs], out, ws, opts=opts)
+    _ok(ws)
+    for o in range(R):
+        assert torch.equal(first[o].view(torch.int16), out[o].view(torch.int16)), f"owner {o}"
+    ref = oracle.gemm_rs(As, Bs, dtype)
+    for o in range(R):
+        check_close(oracle.widen(from_device(out[o]), dtype), ref[o], f"deterministic rs owner {o}")
+    assert torch.count_nonzero(ws).item() == 0
+
+
+def test_gemm_rs_deterministic_integer_inputs_bit_exact():
+    c = configs.small(configs.CONFIGS["rs_mlp1"], R=4, M=256, N=512, K=128, dist="int", seed=46)
+    As, Bs, out, ws = _rs_case(c, opts={"deterministic_rs": 1})
+    _ok(ws)
+    ref = oracle.gemm_rs(As, Bs, c.dtype)
+    for o in range(c.R):
+        assert np.array_equal(oracle.widen(from_device(out[o]), c.dtype), ref[o])
+
+
 def test_gemm_rs_owner_chunk_layout_is_exact():
     # one-hot rows: each owner's chunk must hold exactly its rows (bit-exact layout)
     R, M, N, K = 4, 256, 256, 256
