@@ -41,14 +41,13 @@
 //           barrier.  A stage may be refilled only when both pairs' MMAs have
 //           read it: each "empty" barrier counts one commit per pair.
 //
-// MoE, CL = 2: two single-CTA 128 x 256 tiles stacked along M inside one
-//           expert (a 256-row unit) share the B tile: each CTA loads half of
-//           the B boxes as a TMA multicast to both, and each CTA's MMA commit
-//           releases the stage in both.
+// MoE layer1, CL = 2: a CTA pair computes a 256 x 256 tile inside one expert.
+// MoE layer0 gathers its A rows with cp.async, whose completion can only be
+// signalled in the issuing CTA, so it runs on single CTAs.
 //
-// The template parameter CL is the number of CTAs of a cluster (1, 2 or 4).
-// For the dense modes PAIR = min(CL, 2) is the tcgen05 CTA group; the MoE
-// modes always use single-CTA MMAs.  MC = CL / PAIR tiles share each B box.
+// The template parameter CL is the number of CTAs of a cluster (1, 2 or 4);
+// PAIR = min(CL, 2) is the tcgen05 CTA group and MC = CL / PAIR the pairs that
+// share B (dense modes only).
 //
 // Every wait is bounded: after timeout_ns (or an iteration cap) the thread
 // records FLUX_ERR_TIMEOUT in the workspace header, raises the per-call abort
@@ -326,17 +325,17 @@ struct Work {
 // Shape of the work of one cluster of CL CTAs (128 rows of A per CTA).
 //   dense modes, CL 2 / 4: CTA pairs with 256 x 512 tiles (MC pairs share B)
 //   MOE_SCATTER, CL 2: one CTA pair, 256 x 256 tiles
-//   MOE_GATHER, CL 2: two single-CTA tiles sharing B (the gathered A rows
-//                     cannot complete on the other CTA's barrier)
+//   MOE_GATHER: single CTAs only (cp.async row gather)
 template <int MODE, int CL>
 struct Unit {
   static constexpr bool DENSE = MODE == MODE_STORE || MODE == MODE_REDUCE;
-  static constexpr int PAIR = (CL >= 2 && MODE != MODE_MOE_GATHER) ? 2 : 1;
+  static constexpr int PAIR = CL >= 2 ? 2 : 1;
   static constexpr int NM = (DENSE && PAIR == 2) ? 2 : 1;
   static constexpr int MC = CL / PAIR;
   static constexpr int ROWS = BM * CL;
   using G = Geo<PAIR, NM>;
-  static_assert(!(MODE == MODE_MOE_SCATTER && MC == 2), "MoE layer1: no B sharing between pairs");
+  static_assert(DENSE || MC == 1, "MoE tiles: no B sharing between pairs");
+  static_assert(MODE != MODE_MOE_GATHER || CL == 1, "MoE layer0: single CTAs");
 };
 
 // AllGather / plain GEMM: unit -> (rank, m-tile, n-tile).  Ranks are the
@@ -613,13 +612,10 @@ __device__ void producer_tma(const KParams& p, const Smem& s, const Ctl& c, int 
 // (i = 0..7) of the A tile, each from the token row of the rank that owns it,
 // into the 128B-swizzled layout the MMA descriptor expects.  Thread 0 also
 // issues the B tile by TMA.
-template <int NPROD, int CL>
-__device__ void producer_gather(const KParams& p, const Smem& s, const Ctl& c, int total_mt,
-                                int rank) {
-  using G = typename Unit<MODE_MOE_GATHER, CL>::G;
-  constexpr int MC = Unit<MODE_MOE_GATHER, CL>::MC;
-  const uint16_t mc_mask = static_cast<uint16_t>((1u << rank) | (1u << (rank ^ 1)));
-  ItemIter<MODE_MOE_GATHER, CL> iter(p, total_mt, rank);
+template <int NPROD>
+__device__ void producer_gather(const KParams& p, const Smem& s, const Ctl& c, int total_mt) {
+  using G = typename Unit<MODE_MOE_GATHER, 1>::G;
+  ItemIter<MODE_MOE_GATHER, 1> iter(p, total_mt, 0);
   const int tid = threadIdx.x;  // producer warps are warps 0 .. NPROD/32-1
   Work w;
   uint32_t stage = 0, phase = 0, issued = 0;
@@ -655,8 +651,6 @@ __device__ void producer_gather(const KParams& p, const Smem& s, const Ctl& c, i
     const int nbox_b = min(G::B_BOXES, (p.N - w.nt * BN + B_BOX_N - 1) / B_BOX_N);
     const uint32_t bytes_b = nbox_b * B_BOX_N * BK * 2;
     for (int k = w.k0; k < w.k1; ++k) {
-      // (with MC = 2 the partner's MMA commit also completes this barrier; a
-      // blocking try_wait still sees that, and 128 polling threads cost more)
       const int wr = wait_bar(smem_u32(&s.empty[stage]), phase ^ 1u, c, W_EMPTY, stage);
       if (wr != 0) { ok = false; break; }
       const uint32_t fb = smem_u32(&s.full[stage]);
@@ -664,16 +658,9 @@ __device__ void producer_gather(const KParams& p, const Smem& s, const Ctl& c, i
       const uint32_t sb = smem_u32(s.b + stage * G::B_STAGE);
       const int kc = k * BK;
       if (tid == 0) {
-        mbar_arrive_expect_tx(fb, bytes_b);  // all boxes land here, half of them from the partner
-        for (int j = 0; j < nbox_b; ++j) {
-          const uint32_t dst = sb + j * B_BOX_N * BK * 2;
-          const int n = w.nt * BN + j * B_BOX_N;
-          if (MC == 2) {
-            if ((j >> 1) == rank) tma_load_3d_mc(dst, &p.tmB[w.r], fb, n, kc, w.e, mc_mask);
-          } else {
-            tma_load_3d(dst, &p.tmB[w.r], fb, n, kc, w.e);
-          }
-        }
+        mbar_arrive_expect_tx(fb, bytes_b);
+        for (int j = 0; j < nbox_b; ++j)
+          tma_load_3d(sb + j * B_BOX_N * BK * 2, &p.tmB[w.r], fb, w.nt * BN + j * B_BOX_N, kc, w.e);
       }
       {
         const bool col_ok = kc + chunk * 8 < p.H;
@@ -761,7 +748,6 @@ __device__ void mma_issuer(const KParams& p, const Smem& s, const Ctl& c, uint32
         }
       }
       if (PAIR == 2) umma2_commit_mc(smem_u32(&s.empty[stage]), EMPTY_MASK);
-      else if (MC == 2) umma_commit_mc(smem_u32(&s.empty[stage]), EMPTY_MASK);
       else umma_commit(smem_u32(&s.empty[stage]));
       any = true;
       if (++stage == G::STAGES) { stage = 0; phase ^= 1u; }
@@ -1018,11 +1004,13 @@ __device__ void epilogue(const KParams& p, const Smem& s, const Ctl& c, uint32_t
 // ---------------------------------------------------------------- kernel
 template <int MODE, int DT, int CL>
 struct KernelShape {
-  static constexpr int PRODUCER_WARPS = (MODE == MODE_MOE_GATHER) ? 4 : 1;
+  // the cp.async row gather (single-CTA MoE layer0) takes four producer warps
+  static constexpr bool CPASYNC_GATHER = MODE == MODE_MOE_GATHER && CL == 1;
+  static constexpr int PRODUCER_WARPS = CPASYNC_GATHER ? 4 : 1;
   static constexpr int MMA_WARP = PRODUCER_WARPS;
   static constexpr int EPI_WARP0 = PRODUCER_WARPS + 1;
   static constexpr int THREADS = 32 * (PRODUCER_WARPS + 1 + EPI_WARPS);
-  static constexpr int FULL_COUNT = (MODE == MODE_MOE_GATHER) ? (BM + 1) : 1;
+  static constexpr int FULL_COUNT = CPASYNC_GATHER ? (BM + 1) : 1;
 };
 
 template <int MODE, int DT, int CL>
@@ -1092,11 +1080,11 @@ fused_gemm_kernel(const __grid_constant__ KParams p) {
   if (warp == 0 && lane < p.R) {
     // bring this call's tensor maps into the TMA descriptor cache
     tma_prefetch_desc(&p.tmB[lane]);
-    if (MODE != MODE_MOE_GATHER) tma_prefetch_desc(&p.tmA[lane]);
+    if (!KS::CPASYNC_GATHER) tma_prefetch_desc(&p.tmA[lane]);
   }
   if (warp < KS::PRODUCER_WARPS) {
-    if constexpr (MODE == MODE_MOE_GATHER) {
-      producer_gather<KS::PRODUCER_WARPS * 32, CL>(p, s, c, total_mt, rank);
+    if constexpr (KS::CPASYNC_GATHER) {
+      producer_gather<KS::PRODUCER_WARPS * 32>(p, s, c, total_mt);
     } else if (lane == 0) {
       producer_tma<MODE, CL>(p, s, c, total_mt, rank);
     }

@@ -12,11 +12,12 @@ namespace flux {
 constexpr int ROUTE_THREADS = 1024;
 // CTAs per cluster of the grouped GEMMs; the tile-offset table of each
 // counts units of BM * CL rows inside an expert.
-//   layer0 (row gather): single CTAs.  (Two CTAs sharing B by multicast were
-//     measured slower: the A gather bounds it, and multicast does not lower
-//     the bytes each SM receives.)
-//   layer1: CTA pairs with 256 x 256 tiles, which halves the B bytes each SM
-//     receives per unit of tensor work.
+//   layer0: single CTAs, A rows gathered with cp.async (eight threads per
+//     128-byte row).  Measured alternatives: two CTAs sharing B by multicast
+//     (slower; multicast does not lower the bytes an SM receives) and CTA
+//     pairs gathering rows with TMA tile::gather4 (2.7x slower: 32 gather
+//     operations per stage cost the TMA unit far more than one 128-row box).
+//   layer1: CTA pairs with 256 x 256 tiles (half the B bytes per SM).
 constexpr int MOE0_CL = 1;
 constexpr int MOE1_CL = 2;
 constexpr int ROUTE_CHUNK = 4096;  // expert ids staged in shared memory per pass
