@@ -80,7 +80,9 @@ typedef enum {
   FLUX_OP_AG_GEMM = 1,
   FLUX_OP_GEMM_RS = 2,
   FLUX_OP_MOE_AG = 3,
-  FLUX_OP_MOE_RS = 4
+  FLUX_OP_MOE_RS = 4,
+  FLUX_OP_MLP = 5,       /* flux_mlp_ag_rs */
+  FLUX_OP_MOE_LAYERS = 6 /* flux_moe_layers */
 } flux_op_t;
 
 /* Optional per-call settings; pass NULL for the defaults. */
@@ -117,14 +119,15 @@ const char* flux_status_string(flux_status_t s);
 /* The cudaError_t of the most recent FLUX_ERR_CUDA on the calling thread. */
 int flux_last_cuda_error(void);
 
-/* Bytes of workspace a dense op needs (FLUX_OP_GEMM / AG_GEMM / GEMM_RS).
- * M, N, K as in the op's own signature.  GEMM and AG-GEMM need only the
- * 256-byte status header; GEMM-RS adds per-tile arrival counters and the fp32
- * accumulation buffer of the owners' row chunks (M x N floats).  Returns 0 for
- * an unknown op or invalid sizes. */
+/* Bytes of workspace a dense op needs (FLUX_OP_GEMM / AG_GEMM / GEMM_RS / MLP).
+ * M, N, K as in the op's own signature (FLUX_OP_MLP: M, H, F).  GEMM and
+ * AG-GEMM need only the 256-byte status header; GEMM-RS adds per-tile arrival
+ * counters and the fp32 accumulation buffer of the owners' row chunks (M x N
+ * floats); the MLP needs what its GEMM-RS needs.  Returns 0 for an unknown op
+ * or invalid sizes. */
 size_t flux_workspace_size(flux_op_t op, int R, int M, int N, int K);
 
-/* Bytes of workspace a MoE op needs (FLUX_OP_MOE_AG / FLUX_OP_MOE_RS). */
+/* Bytes of workspace a MoE op needs (FLUX_OP_MOE_AG / MOE_RS / MOE_LAYERS). */
 size_t flux_moe_workspace_size(flux_op_t op, int R, int T, int H, int F, int E, int topk);
 
 /* Zero `bytes` of a workspace on `stream` (cudaMemsetAsync). */
@@ -178,6 +181,23 @@ flux_status_t flux_gemm_rs(int R, int M, int N, int K, flux_dtype_t dtype,
                            const void* const* a_shards, const void* const* b_shards,
                            void* const* out, void* workspace, size_t workspace_bytes,
                            const flux_opts_t* opts, void* stream);
+
+/* The dense tensor-parallel MLP in one call: both GEMMs of the paper review's
+ * "MLP 前向传播" (section 三), with no activation between them (the pages
+ * give none):
+ *   h[r]   = GEMM(AllGather(X), W1_r)            as flux_ag_gemm(R, M, F, H)
+ *   out[o] = rows of sum_r GEMM(h[r], W2_r)      as flux_gemm_rs(R, M, H, F)
+ *   x_shards[s]  device, [M/R x H];  w1_shards[r] device, [H x F/R]
+ *   h[r]         device, [M x F/R]: Output1, written and then read by the call
+ *   w2_shards[r] device, [F/R x H];  out[o] device, [M/R x H]
+ *   ready_flags  as in flux_ag_gemm
+ * Workspace: flux_workspace_size(FLUX_OP_MLP, R, M, H, F).  opts apply to both
+ * GEMMs.  Requirements: those of the two calls. */
+flux_status_t flux_mlp_ag_rs(int R, int M, int H, int F, flux_dtype_t dtype,
+                             const void* const* x_shards, const void* const* w1_shards,
+                             void* const* h, const void* const* w2_shards, void* const* out,
+                             const uint32_t* ready_flags, void* workspace, size_t workspace_bytes,
+                             const flux_opts_t* opts, void* stream);
 
 /* GEMM + ReduceScatter that allocates nothing and takes no workspace.
  * No counterpart in the FLUX or COMET pages: it exists for callers that cannot
@@ -253,6 +273,21 @@ flux_status_t flux_moe_grouped_gemm_rs(int R, int T, int H, int F, int E, int to
                                        const int32_t* slot_to_row, const int32_t* row_to_slot,
                                        void* const* out, void* workspace, size_t workspace_bytes,
                                        const flux_opts_t* opts, void* stream);
+
+/* The MoE layer in one call: routing, layer0 and layer1 (COMET article,
+ * "COMET 的技术原理"; the pages give no activation between the layers, so
+ * there is none):
+ *   h[r]   = flux_moe_ag_grouped_gemm output (grouped rows, [T*topk x F/R])
+ *   out[o] = flux_moe_grouped_gemm_rs of h with the same routing ([T/R x H])
+ * The routing (counts, offsets, slot_to_row, row_to_slot) is kept in the
+ * workspace: flux_moe_workspace_size(FLUX_OP_MOE_LAYERS, ...).  Other arguments
+ * and requirements as in the two calls. */
+flux_status_t flux_moe_layers(int R, int T, int H, int F, int E, int topk, flux_dtype_t dtype,
+                              const void* const* x_shards, const void* const* w1_shards,
+                              const void* const* w2_shards, const int32_t* topk_ids,
+                              const float* topk_weights, void* const* h, void* const* out,
+                              const uint32_t* ready_flags, void* workspace,
+                              size_t workspace_bytes, const flux_opts_t* opts, void* stream);
 
 #ifdef __cplusplus
 }

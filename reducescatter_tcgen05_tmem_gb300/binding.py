@@ -40,6 +40,8 @@ FLUX_OP_AG_GEMM = 1
 FLUX_OP_GEMM_RS = 2
 FLUX_OP_MOE_AG = 3
 FLUX_OP_MOE_RS = 4
+FLUX_OP_MLP = 5
+FLUX_OP_MOE_LAYERS = 6
 
 FLUX_MAX_RANKS = 16
 FLUX_MAX_EXPERTS = 1024
@@ -94,6 +96,9 @@ _SIGS = {
                                   _vp, _vp, _vp, _vp, _sz, _opt, _vp], _i),
     "flux_moe_grouped_gemm_rs": ([_i, _i, _i, _i, _i, _i, _i, _vpp, _vpp, _vp, _vp, _vp, _vp,
                                   _vp, _vpp, _vp, _sz, _opt, _vp], _i),
+    "flux_mlp_ag_rs": ([_i, _i, _i, _i, _i, _vpp, _vpp, _vpp, _vpp, _vpp, _vp, _vp, _sz, _opt, _vp], _i),
+    "flux_moe_layers": ([_i, _i, _i, _i, _i, _i, _i, _vpp, _vpp, _vpp, _vp, _vp, _vpp, _vpp, _vp,
+                         _vp, _sz, _opt, _vp], _i),
 }
 for _name, (_args, _res) in _SIGS.items():
     _fn = getattr(_lib, _name)
@@ -245,3 +250,20 @@ def flux_moe_grouped_gemm_rs(R, T, H, F, E, topk, dtype, h_shards, w2_shards, to
         _ptr(topk_weights), _ptr(offsets), _ptr(slot_to_row), _ptr(row_to_slot), _ptrs(out),
         _ptr(workspace), _nbytes(workspace), _opts(opts), _stream(stream)),
         "flux_moe_grouped_gemm_rs")
+
+
+def flux_mlp_ag_rs(R, M, H, F, dtype, x_shards, w1_shards, h, w2_shards, out, ready_flags,
+                   workspace, opts=None, stream=None) -> None:
+    """The dense MLP in one call: h = AG-GEMM(X, W1), out = GEMM-RS(h, W2)."""
+    _check(_lib.flux_mlp_ag_rs(R, M, H, F, dtype, _ptrs(x_shards), _ptrs(w1_shards), _ptrs(h),
+                               _ptrs(w2_shards), _ptrs(out), _ptr(ready_flags), _ptr(workspace),
+                               _nbytes(workspace), _opts(opts), _stream(stream)), "flux_mlp_ag_rs")
+
+
+def flux_moe_layers(R, T, H, F, E, topk, dtype, x_shards, w1_shards, w2_shards, topk_ids,
+                    topk_weights, h, out, ready_flags, workspace, opts=None, stream=None) -> None:
+    """The MoE layer in one call: routing, layer0 into h, layer1 into out."""
+    _check(_lib.flux_moe_layers(R, T, H, F, E, topk, dtype, _ptrs(x_shards), _ptrs(w1_shards),
+                                _ptrs(w2_shards), _ptr(topk_ids), _ptr(topk_weights), _ptrs(h),
+                                _ptrs(out), _ptr(ready_flags), _ptr(workspace), _nbytes(workspace),
+                                _opts(opts), _stream(stream)), "flux_moe_layers")

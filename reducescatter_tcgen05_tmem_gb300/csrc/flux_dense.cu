@@ -61,6 +61,7 @@ extern "C" size_t flux_workspace_size(flux_op_t op, int R, int M, int N, int K) 
     case FLUX_OP_AG_GEMM:
       return WS_HEADER;
     case FLUX_OP_GEMM_RS:
+    case FLUX_OP_MLP:  // (R, M, H, F): what its GEMM-RS (R, M, N = H, K = F) needs
       return WS_HEADER + rs_counter_bytes(M, N) + static_cast<size_t>(M) * N * sizeof(float);
     default:
       return 0;
@@ -223,4 +224,23 @@ extern "C" flux_status_t flux_gemm_rs(int R, int M, int N, int K, flux_dtype_t d
                 : (opts && opts->tiles_per_group > 0) ? opts->tiles_per_group : grid / DENSE_CL;
   p.tiles_per_group = tg < tiles ? tg : tiles;
   return launch_dt<MODE_REDUCE, DENSE_CL>(dtype, p, grid, s);
+}
+
+extern "C" flux_status_t flux_mlp_ag_rs(int R, int M, int H, int F, flux_dtype_t dtype,
+                                        const void* const* x_shards, const void* const* w1_shards,
+                                        void* const* h, const void* const* w2_shards,
+                                        void* const* out, const uint32_t* ready_flags,
+                                        void* workspace, size_t workspace_bytes,
+                                        const flux_opts_t* opts, void* stream) {
+  if (h == nullptr) return FLUX_ERR_INVALID_ARG;
+  // validate both calls before launching either
+  const size_t need = flux_workspace_size(FLUX_OP_MLP, R, M, H, F);
+  if (need == 0 || M % R || F % R || !valid_dtype(dtype)) return FLUX_ERR_INVALID_ARG;
+  flux_status_t st = check_workspace(workspace, workspace_bytes, need);
+  if (st != FLUX_OK) return st;
+  if ((st = flux_ag_gemm(R, M, F, H, dtype, x_shards, w1_shards, h, ready_flags, workspace,
+                         workspace_bytes, opts, stream)) != FLUX_OK)
+    return st;
+  return flux_gemm_rs(R, M, H, F, dtype, reinterpret_cast<const void* const*>(h), w2_shards, out,
+                      workspace, workspace_bytes, opts, stream);
 }

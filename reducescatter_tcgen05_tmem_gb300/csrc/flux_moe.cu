@@ -254,8 +254,10 @@ using namespace flux;
 extern "C" size_t flux_moe_workspace_size(flux_op_t op, int R, int T, int H, int F, int E,
                                           int topk) {
   if (!moe_shape_ok(R, T, H, F, E, topk)) return 0;
-  if (op != FLUX_OP_MOE_AG && op != FLUX_OP_MOE_RS) return 0;
-  return moe_layout(op, R, T, H, F, E, topk).total;
+  if (op != FLUX_OP_MOE_AG && op != FLUX_OP_MOE_RS && op != FLUX_OP_MOE_LAYERS) return 0;
+  // the one-call layer runs layer0 inside layer1's workspace, whose routing
+  // slots receive layer0's routing
+  return moe_layout(op == FLUX_OP_MOE_LAYERS ? FLUX_OP_MOE_RS : op, R, T, H, F, E, topk).total;
 }
 
 extern "C" flux_status_t flux_moe_route(int T, int E, int topk, const int32_t* topk_ids,
@@ -441,4 +443,31 @@ extern "C" flux_status_t flux_moe_grouped_gemm_rs(
   const int grid = grid_dt<MODE_MOE_SCATTER, MOE1_CL>(dtype, dev, opts, max_units);
   if (grid == 0) return FLUX_ERR_CUDA;
   return launch_dt<MODE_MOE_SCATTER, MOE1_CL>(dtype, p, grid, s);
+}
+
+extern "C" flux_status_t flux_moe_layers(int R, int T, int H, int F, int E, int topk,
+                                         flux_dtype_t dtype, const void* const* x_shards,
+                                         const void* const* w1_shards,
+                                         const void* const* w2_shards, const int32_t* topk_ids,
+                                         const float* topk_weights, void* const* h,
+                                         void* const* out, const uint32_t* ready_flags,
+                                         void* workspace, size_t workspace_bytes,
+                                         const flux_opts_t* opts, void* stream) {
+  if (!moe_shape_ok(R, T, H, F, E, topk) || h == nullptr) return FLUX_ERR_INVALID_ARG;
+  const MoeWs L = moe_layout(FLUX_OP_MOE_RS, R, T, H, F, E, topk);
+  flux_status_t st = check_workspace(workspace, workspace_bytes, L.total);
+  if (st != FLUX_OK) return st;
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  int32_t* counts = reinterpret_cast<int32_t*>(ws + L.counts);
+  int32_t* offsets = reinterpret_cast<int32_t*>(ws + L.offsets);
+  int32_t* s2r = reinterpret_cast<int32_t*>(ws + L.s2r);
+  int32_t* r2s = reinterpret_cast<int32_t*>(ws + L.r2s);
+  // layer0 uses the head of the same workspace (status header + its tile table)
+  if ((st = flux_moe_ag_grouped_gemm(R, T, H, F, E, topk, dtype, x_shards, w1_shards, topk_ids, h,
+                                     counts, offsets, s2r, r2s, ready_flags, workspace,
+                                     workspace_bytes, opts, stream)) != FLUX_OK)
+    return st;
+  return flux_moe_grouped_gemm_rs(R, T, H, F, E, topk, dtype, reinterpret_cast<const void* const*>(h),
+                                  w2_shards, topk_ids, topk_weights, offsets, s2r, r2s, out,
+                                  workspace, workspace_bytes, opts, stream);
 }
