@@ -212,8 +212,9 @@ extern "C" flux_status_t flux_gemm_rs(int R, int M, int N, int K, flux_dtype_t d
     p.tiles_per_group = p.Mt * p.Nt;
     return launch_dt<MODE_REDUCE, 1>(dtype, p, grid, s);
   }
-  p.Nt = (N + DenseGeo::TILE_N - 1) / DenseGeo::TILE_N;
-  p.Mt = (M + DenseUnit::ROWS - 1) / DenseUnit::ROWS;
+  using RsUnit = Unit<MODE_REDUCE, DENSE_CL>;
+  p.Nt = (N + RsUnit::G::TILE_N - 1) / RsUnit::G::TILE_N;
+  p.Mt = (M + RsUnit::ROWS - 1) / RsUnit::ROWS;
   const int tiles = p.Mt * p.Nt;
   p.num_units = tiles * R;
   p.total_ksteps = static_cast<long long>(p.num_units) * p.KT;
