@@ -209,6 +209,18 @@ extern "C" flux_status_t flux_gemm_rs(int R, int M, int N, int K, flux_dtype_t d
     long long per = p.total_ksteps / cap;
     int grid = per >= 4 ? cap : static_cast<int>((p.total_ksteps + 3) / 4);
     if (grid < 1) grid = 1;
+    // Default grid: whole units per CTA when that still keeps three quarters
+    // of the CTAs busy.  No unit is then split along K, so fewer partial tiles
+    // end the call with fp32 adds (decode 128 x 8192 x 28672: 256 units on 128
+    // CTAs, 112 -> 102 us).
+    if (!(opts && opts->num_ctas > 0) && grid == cap) {
+      for (int g = cap; g >= (3 * cap + 3) / 4; --g) {
+        if (p.num_units % g == 0) {
+          grid = g;
+          break;
+        }
+      }
+    }
     p.tiles_per_group = p.Mt * p.Nt;
     return launch_dt<MODE_REDUCE, 1>(dtype, p, grid, s);
   }
