@@ -354,3 +354,78 @@ def test_moe_rows_helpers_match_full():
     assert np.allclose(oracle.moe_layer1_rows(d["h_shards"], d["w2_shards"], d["topk_ids"],
                                               d["topk_weights"], c.E, "f16", 1, lr),
                        y[1][lr], rtol=1e-13, atol=1e-14)
+
+
+# ---------------------------------------------------------------- expert-parallel MoE
+def _ep_weights(c, seed=11, dist="normal"):
+    """Full expert weights W1 [E, H, F], W2 [E, F, H] and their TP and EP shards."""
+    if dist == "int":
+        W1 = gen.integers16((seed, 1), (c.E, c.H, c.F), -2, 2, "f16")
+        W2 = gen.integers16((seed, 2), (c.E, c.F, c.H), -2, 2, "f16")
+    else:
+        W1 = gen.normal16((seed, 1), (c.E, c.H, c.F), 0.5, "f16")
+        W2 = gen.normal16((seed, 2), (c.E, c.F, c.H), 0.5, "f16")
+    fr, el = c.F // c.R, c.E // c.R
+    w1_tp = [np.ascontiguousarray(W1[:, :, r * fr:(r + 1) * fr]) for r in range(c.R)]
+    w2_tp = [np.ascontiguousarray(W2[:, r * fr:(r + 1) * fr, :]) for r in range(c.R)]
+    w1_ep = [np.ascontiguousarray(W1[r * el:(r + 1) * el]) for r in range(c.R)]
+    w2_ep = [np.ascontiguousarray(W2[r * el:(r + 1) * el]) for r in range(c.R)]
+    return W1, W2, w1_tp, w2_tp, w1_ep, w2_ep
+
+
+def test_moe_ep_layer0_equals_the_tp_column_blocks():
+    # the same experts sharded by columns (TP) or by expert (EP) give the same rows
+    c, d = _moe_small(R=2, T=8, H=6, F=8, E=4, topk=2)
+    _, _, w1_tp, _, w1_ep, _ = _ep_weights(c)
+    h_tp, r_tp = oracle.moe_layer0(d["x_shards"], w1_tp, d["topk_ids"], c.E, "f16")
+    h_ep, r_ep = oracle.moe_ep_layer0(d["x_shards"], w1_ep, d["topk_ids"], c.E, "f16")
+    assert np.array_equal(h_ep, np.concatenate(h_tp, axis=1))
+    for a, b in zip(r_tp, r_ep):
+        assert np.array_equal(a, b)
+
+
+def test_moe_ep_layer1_equals_tp_with_row_blocks():
+    c, d = _moe_small(R=2, T=8, H=6, F=8, E=4, topk=2)
+    _, _, _, w2_tp, _, w2_ep = _ep_weights(c)
+    h = gen.normal16((21, 1), (c.T * c.topk, c.F), 1.0, "f16")
+    fr = c.F // c.R
+    h_tp = [np.ascontiguousarray(h[:, r * fr:(r + 1) * fr]) for r in range(c.R)]
+    y_tp = oracle.moe_layer1(h_tp, w2_tp, d["topk_ids"], d["topk_weights"], c.E, "f16")
+    y_ep = oracle.moe_ep_layer1(h, w2_ep, d["topk_ids"], d["topk_weights"], c.E, "f16", c.R)
+    for o in range(c.R):
+        assert np.allclose(y_ep[o], y_tp[o], rtol=1e-12, atol=1e-12)
+
+
+def test_moe_ep_chain_brute_force_integers():
+    # per token, per slot, in exact rationals: y_t = sum_k g (x_t W1_e) W2_e
+    c, d = _moe_small(R=2, T=4, H=3, F=4, E=2, topk=2, dist="int")
+    W1, W2, _, _, w1_ep, w2_ep = _ep_weights(c, dist="int")
+    ids, g = d["topk_ids"], d["topk_weights"]
+    h, _ = oracle.moe_ep_layer0(d["x_shards"], w1_ep, ids, c.E, "f16")
+    y = oracle.moe_ep_layer1(h, w2_ep, ids, g, c.E, "f16", c.R, h_dtype="f64")
+    X = np.concatenate(d["x_shards"]).astype(np.int64)
+    W1i, W2i = W1.astype(np.int64), W2.astype(np.int64)
+    for t in range(c.T):
+        o, lt = divmod(t, c.T // c.R)
+        for j in range(c.H):
+            acc = Fraction(0)
+            for k in range(c.topk):
+                e = int(ids[t, k])
+                hrow = [sum(int(X[t, i]) * int(W1i[e, i, f]) for i in range(c.H)) for f in range(c.F)]
+                acc += Fraction(float(g[t, k])) * sum(hrow[f] * int(W2i[e, f, j]) for f in range(c.F))
+            assert abs(Fraction(y[o][lt, j]) - acc) <= Fraction(1, 2 ** 30)
+
+
+def test_moe_ep_rank_rows_are_the_owner_experts():
+    # rank r's rows are those of experts [r E/R, (r+1) E/R): they come from x . W1 of its own experts
+    c, d = _moe_small(R=2, T=8, H=6, F=4, E=4, topk=2)
+    W1, _, _, _, w1_ep, _ = _ep_weights(c)
+    h, (_, offsets, _, r2s) = oracle.moe_ep_layer0(d["x_shards"], w1_ep, d["topk_ids"], c.E, "f16")
+    X = np.concatenate([oracle.widen(x, "f16") for x in d["x_shards"]])
+    el = c.E // c.R
+    for r in range(c.R):
+        for row in range(int(offsets[r * el]), int(offsets[(r + 1) * el])):
+            s = int(r2s[row])
+            e = int(d["topk_ids"][s // c.topk, s % c.topk])
+            assert e // el == r
+            assert np.allclose(h[row], X[s // c.topk] @ oracle.widen(W1[e], "f16"), rtol=1e-14)
