@@ -268,66 +268,85 @@ def moe_layer1(h_shards, w2_shards, topk_ids, topk_weights, E: int, dtype: str,
     return [Y[o * h:(o + 1) * h].copy() for o in range(R)]
 
 
-def moe_ep_layer0(x_shards, w1_ep, topk_ids, E: int, dtype: str):
+def moe_ep_layer0(x_shards, w1_ep, topk_ids, E: int, dtype: str, tp: int = 1):
     """Expert-parallel layer0: H[row] = X[token(row)] . W1_e, e the row's expert.
 
     The expert-parallel layout of the MoE layer (COMET article, "COMET 的技术
-    原理", the EP side of its EP x TP ratio): expert e lives on rank
-    e // (E/R) with its full [H, F] weight, ``w1_ep[r][e - r E/R]``.  The
-    dispatch sends each routed token row to the rank of its expert; rows stay
-    in the grouped order of :func:`moe_route`, so rank r's rows are
-    [offsets[r E/R], offsets[(r+1) E/R]).  Returns (float64 [T*topk, F],
-    routing tuple).
+    原理", its EP x TP ratio).  The R = len(w1_ep) ranks form EP = R / tp
+    groups of tp ranks; group g holds experts [g E/EP, (g+1) E/EP), and rank
+    r = g tp + t of the group holds column block t (F/tp wide) of each:
+    ``w1_ep[r][e - g E/EP]`` is [H, F/tp].  tp = 1 is pure expert parallel
+    (whole experts per rank), tp = R the tensor-parallel layout of
+    :func:`moe_layer0`.  The dispatch sends each routed token row to the ranks
+    of its expert; rows keep the grouped order of :func:`moe_route`, so group
+    g's rows are [offsets[g E/EP], offsets[(g+1) E/EP]).  Returns (float64
+    [T*topk, F] with rank r's block at those rows and columns
+    [t F/tp, (t+1) F/tp), routing tuple).
     """
     ids = np.asarray(topk_ids)
     T, topk = ids.shape
     R = len(w1_ep)
-    if E % R:
-        raise ValueError("E must divide by R")
-    el = E // R
+    if tp < 1 or R % tp:
+        raise ValueError("tp must divide R")
+    ep = R // tp
+    if E % ep:
+        raise ValueError("E must divide by R / tp")
+    el = E // ep
     routing_ = moe_route(ids, E)
     _, offsets, _, row_to_slot = routing_
     xfull = np.concatenate([widen(x, dtype) for x in x_shards], axis=0)
     if xfull.shape[0] != T:
         raise ValueError("token count mismatch")
-    F = np.asarray(w1_ep[0]).shape[2]
-    h = np.zeros((T * topk, F), dtype=np.float64)
+    fb = np.asarray(w1_ep[0]).shape[2]  # F / tp
+    h = np.zeros((T * topk, fb * tp), dtype=np.float64)
     for e in range(E):
         lo, hi = int(offsets[e]), int(offsets[e + 1])
         if hi == lo:
             continue
-        w = widen(np.asarray(w1_ep[e // el])[e % el], dtype)  # [H, F] of expert e
         tokens = row_to_slot[lo:hi].astype(np.int64) // topk
-        h[lo:hi] = gemm(xfull[tokens], w)
+        g = e // el
+        for t in range(tp):
+            w = widen(np.asarray(w1_ep[g * tp + t])[e % el], dtype)  # [H, F/tp]
+            h[lo:hi, t * fb:(t + 1) * fb] = gemm(xfull[tokens], w)
     return h, routing_
 
 
 def moe_ep_layer1(h, w2_ep, topk_ids, topk_weights, E: int, dtype: str, R: int,
-                  routing_=None, h_dtype: str | None = None):
+                  routing_=None, h_dtype: str | None = None, tp: int = 1):
     """Expert-parallel layer1 and combine: Y[t] = sum_k g[t,k] (H[row(t,k)] . W2_{id[t,k]}).
 
-    Expert e's full [F, H] weight lives on rank e // (E/R) as
-    ``w2_ep[r][e - r E/R]``; each (token, k) contributes once (k ascending),
-    and the combine returns every token row to its owner: owner o receives
-    rows [o T/R, (o+1) T/R).  Returns R float64 arrays [T/R, H].
+    Layout as in :func:`moe_ep_layer0`: rank r = g tp + t holds row block t
+    (F/tp tall) of each expert of group g, ``w2_ep[r][e - g E/EP]`` [F/tp, H],
+    and multiplies it with the matching column block of H.  A (token, k)
+    slot sums its tp partials (t ascending), the slots are weighted and added
+    k ascending, and the combine returns every token row to its owner: owner
+    o receives rows [o T/R, (o+1) T/R).  Returns R float64 arrays [T/R, H].
     """
     ids = np.asarray(topk_ids)
     g = np.asarray(topk_weights, dtype=np.float32).astype(np.float64)
     T, topk = ids.shape
-    if T % R or E % R or len(w2_ep) != R:
-        raise ValueError("T and E must divide by R, one w2 block per rank")
-    el = E // R
+    if tp < 1 or R % tp or len(w2_ep) != R:
+        raise ValueError("tp must divide R, one w2 block per rank")
+    ep = R // tp
+    if T % R or E % ep:
+        raise ValueError("T must divide by R and E by R / tp")
+    el = E // ep
     if routing_ is None:
         routing_ = moe_route(ids, E)
     _, offsets, slot_to_row, _ = routing_
     hd = dtype if h_dtype is None else h_dtype
     hh = widen(h, hd)
+    fb = np.asarray(w2_ep[0]).shape[1]  # F / tp
     Hn = np.asarray(w2_ep[0]).shape[2]
     P = np.zeros((T * topk, Hn), dtype=np.float64)
     for e in range(E):
         lo, hi = int(offsets[e]), int(offsets[e + 1])
-        if hi > lo:
-            P[lo:hi] = gemm(hh[lo:hi], widen(np.asarray(w2_ep[e // el])[e % el], dtype))
+        if hi == lo:
+            continue
+        grp = e // el
+        for t in range(tp):
+            w = widen(np.asarray(w2_ep[grp * tp + t])[e % el], dtype)
+            P[lo:hi] = P[lo:hi] + gemm(hh[lo:hi, t * fb:(t + 1) * fb], w)
     s2r = np.asarray(slot_to_row, dtype=np.int64).reshape(T, topk)
     Y = np.zeros((T, Hn), dtype=np.float64)
     for k in range(topk):

@@ -373,6 +373,51 @@ def _ep_weights(c, seed=11, dist="normal"):
     return W1, W2, w1_tp, w2_tp, w1_ep, w2_ep
 
 
+def _eptp_shards(W1, W2, R, tp):
+    """Rank r = g tp + t: experts of EP group g, column (W1) / row (W2) block t."""
+    E, _, F = W1.shape
+    el, fb = E // (R // tp), F // tp
+    w1 = [np.ascontiguousarray(W1[(r // tp) * el:(r // tp + 1) * el, :, (r % tp) * fb:(r % tp + 1) * fb])
+          for r in range(R)]
+    w2 = [np.ascontiguousarray(W2[(r // tp) * el:(r // tp + 1) * el, (r % tp) * fb:(r % tp + 1) * fb, :])
+          for r in range(R)]
+    return w1, w2
+
+
+def test_moe_eptp_layer0_does_not_depend_on_the_split():
+    # every EP x TP split of the same experts computes the same rows, and tp = R
+    # is the tensor-parallel layer0 exactly
+    c, d = _moe_small(R=4, T=8, H=6, F=8, E=4, topk=2)
+    W1, W2, w1_tp, _, _, _ = _ep_weights(c)
+    h_tp, _ = oracle.moe_layer0(d["x_shards"], w1_tp, d["topk_ids"], c.E, "f16")
+    for tp in (1, 2, 4):
+        w1, _ = _eptp_shards(W1, W2, c.R, tp)
+        h, _ = oracle.moe_ep_layer0(d["x_shards"], w1, d["topk_ids"], c.E, "f16", tp=tp)
+        assert np.array_equal(h, np.concatenate(h_tp, axis=1)), tp
+
+
+@pytest.mark.parametrize("tp", [1, 2, 4])
+def test_moe_eptp_chain_brute_force_integers(tp):
+    # exact rationals per token and slot, for every EP x TP split of R = 4
+    c, d = _moe_small(R=4, T=8, H=3, F=8, E=4, topk=2, dist="int")
+    W1, W2, _, _, _, _ = _ep_weights(c, dist="int")
+    w1, w2 = _eptp_shards(W1, W2, c.R, tp)
+    ids, g = d["topk_ids"], d["topk_weights"]
+    h, _ = oracle.moe_ep_layer0(d["x_shards"], w1, ids, c.E, "f16", tp=tp)
+    y = oracle.moe_ep_layer1(h, w2, ids, g, c.E, "f16", c.R, h_dtype="f64", tp=tp)
+    X = np.concatenate(d["x_shards"]).astype(np.int64)
+    W1i, W2i = W1.astype(np.int64), W2.astype(np.int64)
+    for t in range(c.T):
+        o, lt = divmod(t, c.T // c.R)
+        for j in range(c.H):
+            acc = Fraction(0)
+            for k in range(c.topk):
+                e = int(ids[t, k])
+                hrow = [sum(int(X[t, i]) * int(W1i[e, i, f]) for i in range(c.H)) for f in range(c.F)]
+                acc += Fraction(float(g[t, k])) * sum(hrow[f] * int(W2i[e, f, j]) for f in range(c.F))
+            assert abs(Fraction(y[o][lt, j]) - acc) <= Fraction(1, 2 ** 30)
+
+
 def test_moe_ep_layer0_equals_the_tp_column_blocks():
     # the same experts sharded by columns (TP) or by expert (EP) give the same rows
     c, d = _moe_small(R=2, T=8, H=6, F=8, E=4, topk=2)

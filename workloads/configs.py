@@ -22,7 +22,7 @@ import numpy as np
 from .gen import integers16, normal16, routing, uniform16
 
 __all__ = ["DenseAG", "DenseRS", "MoE", "CONFIGS", "ag_inputs", "rs_inputs",
-           "moe_inputs", "small"]
+           "moe_inputs", "moe_ep_inputs", "small"]
 
 
 @dataclass(frozen=True)
@@ -162,6 +162,36 @@ def moe_inputs(c: MoE, with_h: bool = True):
     }
     if with_h:
         d["h_shards"] = [_draw((c.seed, 4, r), (c.T * c.topk, Fr), 1.0, c.dtype, c.dist)
+                         for r in range(c.R)]
+    return d
+
+
+def moe_ep_inputs(c: MoE, tp: int, with_h: bool = True):
+    """Inputs of the MoE layer under an EP x TP split: EP = R / tp expert groups of
+    tp ranks; rank r = g tp + t holds block t of group g's experts.
+
+    x_shards  R x [T/R, H]               as in :func:`moe_inputs`
+    w1_shards R x [E/EP, H, F/tp]        column block t of group g's experts' W1
+    w2_shards R x [E/EP, F/tp, H]        row block t of group g's experts' W2
+    topk_ids, topk_weights               as in :func:`moe_inputs`
+    h_shards  R x [T*topk, F/tp]         a standalone layer1 input, N(0, 1)
+    """
+    if c.T % c.R or c.R % tp or c.E % (c.R // tp) or c.F % tp:
+        raise ValueError("need T % R == 0, R % tp == 0, E % (R/tp) == 0, F % tp == 0")
+    el, fb = c.E // (c.R // tp), c.F // tp
+    ids, w = routing((c.seed, 9), c.T, c.E, c.topk, c.zipf_s, c.force_empty)
+    d = {
+        "x_shards": [_draw((c.seed, 1, r), (c.T // c.R, c.H), c.x_std, c.dtype, c.dist)
+                     for r in range(c.R)],
+        "w1_shards": [_draw((c.seed, 5, r), (el, c.H, fb), c.w_std, c.dtype, c.dist)
+                      for r in range(c.R)],
+        "w2_shards": [_draw((c.seed, 6, r), (el, fb, c.H), c.w_std, c.dtype, c.dist)
+                      for r in range(c.R)],
+        "topk_ids": ids,
+        "topk_weights": w,
+    }
+    if with_h:
+        d["h_shards"] = [_draw((c.seed, 7, r), (c.T * c.topk, fb), 1.0, c.dtype, c.dist)
                          for r in range(c.R)]
     return d
 
