@@ -13,6 +13,10 @@
  *     routing (histogram + prefix sum + stable permutation)  flux_moe_route
  *     AllGather + gather-by-expert + grouped GEMM            flux_moe_ag_grouped_gemm
  *     grouped GEMM + top-k weighted combine + ReduceScatter  flux_moe_grouped_gemm_rs
+ * and the same two layers under an expert-parallel x tensor-parallel split of
+ * the experts (COMET's EP x TP ratio, same section):
+ *     dispatch by expert + grouped GEMM                     flux_moe_ep_dispatch_gemm
+ *     grouped GEMM + top-k weighted combine to the owners    flux_moe_ep_gemm_combine
  * plus the plain non-split GEMM that the effective-communication-time metric
  * ECT = OverallTime - GEMM_non-split is measured against (paper review,
  * section 三, "核心公式"): flux_gemm.  The operator list is the one the Flux
@@ -81,8 +85,10 @@ typedef enum {
   FLUX_OP_GEMM_RS = 2,
   FLUX_OP_MOE_AG = 3,
   FLUX_OP_MOE_RS = 4,
-  FLUX_OP_MLP = 5,       /* flux_mlp_ag_rs */
-  FLUX_OP_MOE_LAYERS = 6 /* flux_moe_layers */
+  FLUX_OP_MLP = 5,        /* flux_mlp_ag_rs */
+  FLUX_OP_MOE_LAYERS = 6, /* flux_moe_layers */
+  FLUX_OP_MOE_EP_AG = 7,  /* flux_moe_ep_dispatch_gemm */
+  FLUX_OP_MOE_EP_RS = 8   /* flux_moe_ep_gemm_combine */
 } flux_op_t;
 
 /* Optional per-call settings; pass NULL for the defaults. */
@@ -127,7 +133,8 @@ int flux_last_cuda_error(void);
  * or invalid sizes. */
 size_t flux_workspace_size(flux_op_t op, int R, int M, int N, int K);
 
-/* Bytes of workspace a MoE op needs (FLUX_OP_MOE_AG / MOE_RS / MOE_LAYERS). */
+/* Bytes of workspace a MoE op needs (FLUX_OP_MOE_AG / MOE_RS / MOE_LAYERS / MOE_EP_AG /
+ * MOE_EP_RS); 0 for an unknown op or invalid sizes. */
 size_t flux_moe_workspace_size(flux_op_t op, int R, int T, int H, int F, int E, int topk);
 
 /* Zero `bytes` of a workspace on `stream` (cudaMemsetAsync). */
@@ -288,6 +295,58 @@ flux_status_t flux_moe_layers(int R, int T, int H, int F, int E, int topk, flux_
                               const float* topk_weights, void* const* h, void* const* out,
                               const uint32_t* ready_flags, void* workspace,
                               size_t workspace_bytes, const flux_opts_t* opts, void* stream);
+
+/* ---------------------------------------------------------------- MoE, EP x TP split
+ *
+ * The R ranks form EP = R / tp expert groups of tp ranks (COMET article,
+ * "COMET 的技术原理": the EP x TP ratio of the MoE layer).  Group g holds
+ * experts [g E/EP, (g+1) E/EP); rank r = g tp + t holds block t (F/tp wide)
+ * of each of them.  tp = R is the tensor-parallel layout of
+ * flux_moe_ag_grouped_gemm / flux_moe_grouped_gemm_rs (same results); tp = 1
+ * is pure expert parallel: every expert whole on one rank, and each routed
+ * token row dispatched to that rank alone.
+ * Workspace: flux_moe_workspace_size(FLUX_OP_MOE_EP_AG / FLUX_OP_MOE_EP_RS,
+ * ...), which does not depend on tp.  Requires R % tp == 0, E % (R/tp) == 0,
+ * F % tp == 0, T % R == 0, H % 8 == 0, (F/tp) % 8 == 0.  Invalid sizes or a
+ * NULL buffer return FLUX_ERR_INVALID_ARG; unaligned buffers
+ * FLUX_ERR_UNSUPPORTED. */
+
+/* EP layer0: h_out[r][row] = X[token(row)] . W1[r][expert(row) - g E/EP] for
+ * the grouped-order rows of group g's experts, rows [offsets[g E/EP],
+ * offsets[(g+1) E/EP]); the call runs flux_moe_route first and writes
+ * counts/offsets/slot_to_row/row_to_slot as that call does.
+ *   x_shards[s]   device, [T/R x H]: token rows owned by rank s
+ *   w1_shards[r]  device, [E/EP x H x F/tp]: column block t of group g's experts
+ *   h_out[r]      device, [T*topk x F/tp]: only group g's rows are written (with
+ *                 H == 0 the whole buffer is zeroed), so ranks of different
+ *                 groups with the same t may pass one buffer
+ *   ready_flags   as in flux_ag_gemm (per token shard), or NULL */
+flux_status_t flux_moe_ep_dispatch_gemm(int R, int tp, int T, int H, int F, int E, int topk,
+                                        flux_dtype_t dtype, const void* const* x_shards,
+                                        const void* const* w1_shards, const int32_t* topk_ids,
+                                        void* const* h_out, int32_t* counts, int32_t* offsets,
+                                        int32_t* slot_to_row, int32_t* row_to_slot,
+                                        const uint32_t* ready_flags, void* workspace,
+                                        size_t workspace_bytes, const flux_opts_t* opts,
+                                        void* stream);
+
+/* EP layer1 + combine: Out_o[t] = sum_k topk_weights[t,k] . sum over the tp ranks
+ * r of expert e = topk_ids[t,k]'s group of (h_shards[r][slot_to_row[t*topk+k]] .
+ * W2[r][e - g E/EP]), for the tokens t in [o T/R, (o+1) T/R) owned by rank o.
+ *   h_shards[r]   device, [T*topk x F/tp]: rows of group g's experts are read
+ *   w2_shards[r]  device, [E/EP x F/tp x H]: row block t of group g's experts
+ *   offsets, slot_to_row, row_to_slot: the routing that ordered h_shards, or all
+ *                 three NULL to have this call recompute them in its workspace
+ *   out[o]        device, [T/R x H]
+ * The tp*topk contributions to a token row are added in fp32 in the workspace;
+ * the last one converts the row to 16 bits. */
+flux_status_t flux_moe_ep_gemm_combine(int R, int tp, int T, int H, int F, int E, int topk,
+                                       flux_dtype_t dtype, const void* const* h_shards,
+                                       const void* const* w2_shards, const int32_t* topk_ids,
+                                       const float* topk_weights, const int32_t* offsets,
+                                       const int32_t* slot_to_row, const int32_t* row_to_slot,
+                                       void* const* out, void* workspace, size_t workspace_bytes,
+                                       const flux_opts_t* opts, void* stream);
 
 #ifdef __cplusplus
 }

@@ -42,6 +42,8 @@ FLUX_OP_MOE_AG = 3
 FLUX_OP_MOE_RS = 4
 FLUX_OP_MLP = 5
 FLUX_OP_MOE_LAYERS = 6
+FLUX_OP_MOE_EP_AG = 7
+FLUX_OP_MOE_EP_RS = 8
 
 FLUX_MAX_RANKS = 16
 FLUX_MAX_EXPERTS = 1024
@@ -99,6 +101,10 @@ _SIGS = {
     "flux_mlp_ag_rs": ([_i, _i, _i, _i, _i, _vpp, _vpp, _vpp, _vpp, _vpp, _vp, _vp, _sz, _opt, _vp], _i),
     "flux_moe_layers": ([_i, _i, _i, _i, _i, _i, _i, _vpp, _vpp, _vpp, _vp, _vp, _vpp, _vpp, _vp,
                          _vp, _sz, _opt, _vp], _i),
+    "flux_moe_ep_dispatch_gemm": ([_i, _i, _i, _i, _i, _i, _i, _i, _vpp, _vpp, _vp, _vpp, _vp,
+                                   _vp, _vp, _vp, _vp, _vp, _sz, _opt, _vp], _i),
+    "flux_moe_ep_gemm_combine": ([_i, _i, _i, _i, _i, _i, _i, _i, _vpp, _vpp, _vp, _vp, _vp,
+                                  _vp, _vp, _vpp, _vp, _sz, _opt, _vp], _i),
 }
 for _name, (_args, _res) in _SIGS.items():
     _fn = getattr(_lib, _name)
@@ -267,3 +273,25 @@ def flux_moe_layers(R, T, H, F, E, topk, dtype, x_shards, w1_shards, w2_shards, 
                                 _ptrs(w2_shards), _ptr(topk_ids), _ptr(topk_weights), _ptrs(h),
                                 _ptrs(out), _ptr(ready_flags), _ptr(workspace), _nbytes(workspace),
                                 _opts(opts), _stream(stream)), "flux_moe_layers")
+
+
+def flux_moe_ep_dispatch_gemm(R, tp, T, H, F, E, topk, dtype, x_shards, w1_shards, topk_ids,
+                              h_out, counts, offsets, slot_to_row, row_to_slot, ready_flags,
+                              workspace, opts=None, stream=None) -> None:
+    """MoE layer0 under an EP x TP split (tp ranks per expert group)."""
+    _check(_lib.flux_moe_ep_dispatch_gemm(
+        R, tp, T, H, F, E, topk, dtype, _ptrs(x_shards), _ptrs(w1_shards), _ptr(topk_ids),
+        _ptrs(h_out), _ptr(counts), _ptr(offsets), _ptr(slot_to_row), _ptr(row_to_slot),
+        _ptr(ready_flags), _ptr(workspace), _nbytes(workspace), _opts(opts), _stream(stream)),
+        "flux_moe_ep_dispatch_gemm")
+
+
+def flux_moe_ep_gemm_combine(R, tp, T, H, F, E, topk, dtype, h_shards, w2_shards, topk_ids,
+                             topk_weights, offsets, slot_to_row, row_to_slot, out, workspace,
+                             opts=None, stream=None) -> None:
+    """MoE layer1 + top-k combine under an EP x TP split."""
+    _check(_lib.flux_moe_ep_gemm_combine(
+        R, tp, T, H, F, E, topk, dtype, _ptrs(h_shards), _ptrs(w2_shards), _ptr(topk_ids),
+        _ptr(topk_weights), _ptr(offsets), _ptr(slot_to_row), _ptr(row_to_slot), _ptrs(out),
+        _ptr(workspace), _nbytes(workspace), _opts(opts), _stream(stream)),
+        "flux_moe_ep_gemm_combine")

@@ -167,6 +167,8 @@ struct KParams {
   const int32_t* tile_off;     // [E+1] first m-tile of each expert
   const float* topk_w;         // [T*topk]
   int E, topk, T, H;
+  int moe_tp;  // MoE: ranks per expert group (R: tensor parallel, 1: expert parallel)
+  int moe_el;  // MoE: experts per group; rank g moe_tp + t holds block t of group g's experts
 };
 
 struct Ctl {
@@ -400,12 +402,16 @@ __device__ __forceinline__ Work decode_reduce(const KParams& p, int u, int cta) 
 // MoE: unit -> (rank, grouped m-unit, n-tile); the expert of an m-unit comes
 // from the device table of each expert's first unit (units of BM * CL rows)
 // written by the routing kernel.  `cta` picks the 128-row part of the unit.
+// An m-unit of expert e runs on the moe_tp ranks of e's group g = e / moe_el
+// (ranks g moe_tp + [0, moe_tp)), each with its block of the expert's weight
+// (local expert e % moe_el).  Tensor parallel: one group of R ranks; expert
+// parallel: R groups of one rank.
 template <int CL>
 __device__ __forceinline__ Work decode_moe(const KParams& p, int u, int total_mt, int cta) {
   Work w;
   const int per_rank = total_mt * p.Nt;
-  w.r = u / per_rank;
-  int t = u - w.r * per_rank;
+  const int tr = u / per_rank;  // rank inside the expert's group
+  int t = u - tr * per_rank;
   int gmt, nt;
   // m-tile fastest inside bands of group_n n-tiles
   raster(t, total_mt, p.Nt, p.group_n, gmt, nt);
@@ -414,7 +420,9 @@ __device__ __forceinline__ Work decode_moe(const KParams& p, int u, int total_mt
     const int mid = (lo + hi) >> 1;
     if (__ldg(p.tile_off + mid) <= gmt) lo = mid; else hi = mid;
   }
-  w.e = lo;
+  const int grp = lo / p.moe_el;
+  w.r = grp * p.moe_tp + tr;
+  w.e = lo - grp * p.moe_el;  // index into rank r's experts
   const int e_off = __ldg(p.offsets + lo);
   w.m0 = e_off + (gmt - __ldg(p.tile_off + lo)) * (BM * CL) + cta * BM;
   w.row_end = __ldg(p.offsets + lo + 1);
@@ -438,7 +446,7 @@ struct ItemIter {
 
   __device__ ItemIter(const KParams& p_, int total_mt_, int cta_) : p(p_), total_mt(total_mt_), cta(cta_) {
     if (MODE == MODE_MOE_GATHER || MODE == MODE_MOE_SCATTER) {
-      num_units = total_mt * p.Nt * p.R;
+      num_units = total_mt * p.Nt * p.moe_tp;
     } else {
       num_units = p.num_units;
     }
@@ -981,7 +989,8 @@ __device__ void epilogue(const KParams& p, const Smem& s, const Ctl& c, uint32_t
       bool last = false;
       if (row_ok) {
         const uint32_t old = atomicAdd(cnt, 1u);
-        last = (old + 1u == static_cast<uint32_t>(p.R * p.topk));
+        // every (token, k) adds once per rank of its expert's group
+        last = (old + 1u == static_cast<uint32_t>(p.moe_tp * p.topk));
       }
       uint32_t lmask = __ballot_sync(0xFFFFFFFFu, last);
       if (lmask) __threadfence();

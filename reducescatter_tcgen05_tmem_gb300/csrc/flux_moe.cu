@@ -196,10 +196,23 @@ int grid_dt(flux_dtype_t dt, const DeviceInfo& dev, const flux_opts_t* opts, lon
                          : grid_for<MODE, 0, CL>(dev, opts, units);
 }
 
-bool moe_shape_ok(int R, int T, int H, int F, int E, int topk) {
+// Sizes every MoE layout accepts (the workspace does not depend on the split).
+bool moe_common_ok(int R, int T, int H, int F, int E, int topk) {
   return R >= 1 && R <= FLUX_MAX_RANKS && T >= 0 && H >= 0 && F >= 0 && E >= 1 &&
-         E <= FLUX_MAX_EXPERTS && topk >= 1 && topk <= E && T % R == 0 && F % R == 0 &&
+         E <= FLUX_MAX_EXPERTS && topk >= 1 && topk <= E && T % R == 0 &&
          static_cast<long long>(T) * topk < (1ll << 31);
+}
+
+// EP x TP split: R / tp expert groups of tp ranks; each group holds E / (R/tp)
+// experts, each rank of a group an F/tp block of them.  tp = R is the
+// tensor-parallel layout, tp = 1 pure expert parallel.
+bool moe_split_ok(int R, int tp, int T, int H, int F, int E, int topk) {
+  return moe_common_ok(R, T, H, F, E, topk) && tp >= 1 && tp <= R && R % tp == 0 &&
+         E % (R / tp) == 0 && F % tp == 0;
+}
+
+bool moe_shape_ok(int R, int T, int H, int F, int E, int topk) {
+  return moe_split_ok(R, R, T, H, F, E, topk);
 }
 
 size_t a256(size_t v) { return round_up(v, WS_ALIGN); }
@@ -253,6 +266,12 @@ using namespace flux;
 
 extern "C" size_t flux_moe_workspace_size(flux_op_t op, int R, int T, int H, int F, int E,
                                           int topk) {
+  if (op == FLUX_OP_MOE_EP_AG || op == FLUX_OP_MOE_EP_RS) {
+    // any EP x TP split of these sizes; the call itself checks the split
+    if (!moe_common_ok(R, T, H, F, E, topk)) return 0;
+    return moe_layout(op == FLUX_OP_MOE_EP_AG ? FLUX_OP_MOE_AG : FLUX_OP_MOE_RS, R, T, H, F, E,
+                      topk).total;
+  }
   if (!moe_shape_ok(R, T, H, F, E, topk)) return 0;
   if (op != FLUX_OP_MOE_AG && op != FLUX_OP_MOE_RS && op != FLUX_OP_MOE_LAYERS) return 0;
   // the one-call layer runs layer0 inside layer1's workspace, whose routing
@@ -282,12 +301,21 @@ extern "C" flux_status_t flux_moe_route(int T, int E, int topk, const int32_t* t
                       static_cast<uint32_t*>(workspace), static_cast<cudaStream_t>(stream));
 }
 
-extern "C" flux_status_t flux_moe_ag_grouped_gemm(
-    int R, int T, int H, int F, int E, int topk, flux_dtype_t dtype, const void* const* x_shards,
-    const void* const* w1_shards, const int32_t* topk_ids, void* const* h_out, int32_t* counts,
-    int32_t* offsets, int32_t* slot_to_row, int32_t* row_to_slot, const uint32_t* ready_flags,
-    void* workspace, size_t workspace_bytes, const flux_opts_t* opts, void* stream) {
-  if (!moe_shape_ok(R, T, H, F, E, topk) || (dtype != FLUX_F16 && dtype != FLUX_BF16))
+namespace flux {
+namespace {
+
+// Layer0 for an EP x TP split (tp ranks per expert group; tp = R is tensor
+// parallel).  Rank r = g tp + t: w1_shards[r] [E/EP x H x F/tp] holds column
+// block t of the experts of group g, and h_out[r] [T*topk x F/tp] receives the
+// rows of those experts (the other rows are left as they were, so ranks of
+// different groups may share one buffer).
+flux_status_t moe_layer0_impl(
+    int tp, int R, int T, int H, int F, int E, int topk, flux_dtype_t dtype,
+    const void* const* x_shards, const void* const* w1_shards, const int32_t* topk_ids,
+    void* const* h_out, int32_t* counts, int32_t* offsets, int32_t* slot_to_row,
+    int32_t* row_to_slot, const uint32_t* ready_flags, void* workspace, size_t workspace_bytes,
+    const flux_opts_t* opts, void* stream) {
+  if (!moe_split_ok(R, tp, T, H, F, E, topk) || (dtype != FLUX_F16 && dtype != FLUX_BF16))
     return FLUX_ERR_INVALID_ARG;
   if (x_shards == nullptr || w1_shards == nullptr || h_out == nullptr || counts == nullptr ||
       offsets == nullptr || slot_to_row == nullptr || row_to_slot == nullptr ||
@@ -296,7 +324,8 @@ extern "C" flux_status_t flux_moe_ag_grouped_gemm(
   const MoeWs L = moe_layout(FLUX_OP_MOE_AG, R, T, H, F, E, topk);
   flux_status_t st = check_workspace(workspace, workspace_bytes, L.total);
   if (st != FLUX_OK) return st;
-  const int Fr = F / R, rows = T / R, n = T * topk;
+  // output columns per rank and experts per rank's weight block
+  const int Fr = F / tp, EB = E / (R / tp), rows = T / R, n = T * topk;
   for (int r = 0; r < R; ++r) {
     if (x_shards[r] == nullptr || w1_shards[r] == nullptr || h_out[r] == nullptr)
       return FLUX_ERR_INVALID_ARG;
@@ -322,10 +351,12 @@ extern "C" flux_status_t flux_moe_ag_grouped_gemm(
   }
   KParams p{};
   for (int r = 0; r < R; ++r) {
-    if ((st = encode_3d(&p.tmB[r], dtype, w1_shards[r], Fr, H, E, B_BOX_N, BK)) != FLUX_OK) return st;
+    if ((st = encode_3d(&p.tmB[r], dtype, w1_shards[r], Fr, H, EB, B_BOX_N, BK)) != FLUX_OK) return st;
     p.out[r] = h_out[r];
     p.xsrc[r] = x_shards[r];
   }
+  p.moe_tp = tp;
+  p.moe_el = EB;
   p.R = R;
   p.M = n;
   p.N = Fr;
@@ -349,19 +380,23 @@ extern "C" flux_status_t flux_moe_ag_grouped_gemm(
   p.hdr = static_cast<uint32_t*>(workspace);
   const long long max_units =
       (static_cast<long long>((n + BM * MOE0_CL - 1) / (BM * MOE0_CL)) + E) * p.Nt *
-      static_cast<long long>(R);
+      static_cast<long long>(tp);
   const int grid = grid_dt<MODE_MOE_GATHER, MOE0_CL>(dtype, dev, opts, max_units);
   if (grid == 0) return FLUX_ERR_CUDA;
   return launch_dt<MODE_MOE_GATHER, MOE0_CL>(dtype, p, grid, s);
 }
 
-extern "C" flux_status_t flux_moe_grouped_gemm_rs(
-    int R, int T, int H, int F, int E, int topk, flux_dtype_t dtype, const void* const* h_shards,
-    const void* const* w2_shards, const int32_t* topk_ids, const float* topk_weights,
-    const int32_t* offsets, const int32_t* slot_to_row, const int32_t* row_to_slot,
-    void* const* out, void* workspace, size_t workspace_bytes, const flux_opts_t* opts,
-    void* stream) {
-  if (!moe_shape_ok(R, T, H, F, E, topk) || (dtype != FLUX_F16 && dtype != FLUX_BF16))
+// Layer1 for an EP x TP split.  Rank r = g tp + t: h_shards[r] [T*topk x F/tp]
+// (only the rows of group g's experts are read) and w2_shards[r]
+// [E/EP x F/tp x H] (row block t of group g's experts); every (token, k) slot
+// adds tp partials.
+flux_status_t moe_layer1_impl(
+    int tp, int R, int T, int H, int F, int E, int topk, flux_dtype_t dtype,
+    const void* const* h_shards, const void* const* w2_shards, const int32_t* topk_ids,
+    const float* topk_weights, const int32_t* offsets, const int32_t* slot_to_row,
+    const int32_t* row_to_slot, void* const* out, void* workspace, size_t workspace_bytes,
+    const flux_opts_t* opts, void* stream) {
+  if (!moe_split_ok(R, tp, T, H, F, E, topk) || (dtype != FLUX_F16 && dtype != FLUX_BF16))
     return FLUX_ERR_INVALID_ARG;
   const bool given = offsets != nullptr;
   if (given != (slot_to_row != nullptr) || given != (row_to_slot != nullptr))
@@ -372,7 +407,8 @@ extern "C" flux_status_t flux_moe_grouped_gemm_rs(
   const MoeWs L = moe_layout(FLUX_OP_MOE_RS, R, T, H, F, E, topk);
   flux_status_t st = check_workspace(workspace, workspace_bytes, L.total);
   if (st != FLUX_OK) return st;
-  const int Fr = F / R, rows = T / R, n = T * topk;
+  // reduction length per rank and experts per rank's weight block
+  const int Fr = F / tp, EB = E / (R / tp), rows = T / R, n = T * topk;
   for (int r = 0; r < R; ++r) {
     if (h_shards[r] == nullptr || w2_shards[r] == nullptr || out[r] == nullptr)
       return FLUX_ERR_INVALID_ARG;
@@ -411,9 +447,11 @@ extern "C" flux_status_t flux_moe_grouped_gemm_rs(
     if ((st = encode_2d(&p.tmA[r], dtype, h_shards[r], Fr, n, static_cast<uint64_t>(Fr) * 2, BK,
                         BM)) != FLUX_OK)
       return st;
-    if ((st = encode_3d(&p.tmB[r], dtype, w2_shards[r], H, Fr, E, B_BOX_N, BK)) != FLUX_OK) return st;
+    if ((st = encode_3d(&p.tmB[r], dtype, w2_shards[r], H, Fr, EB, B_BOX_N, BK)) != FLUX_OK) return st;
     p.out[r] = out[r];
   }
+  p.moe_tp = tp;
+  p.moe_el = EB;
   p.R = R;
   p.M = n;
   p.N = H;
@@ -439,10 +477,56 @@ extern "C" flux_status_t flux_moe_grouped_gemm_rs(
   p.hdr = static_cast<uint32_t*>(workspace);
   const long long max_units =
       (static_cast<long long>((n + BM * MOE1_CL - 1) / (BM * MOE1_CL)) + E) * p.Nt *
-      static_cast<long long>(R);
+      static_cast<long long>(tp);
   const int grid = grid_dt<MODE_MOE_SCATTER, MOE1_CL>(dtype, dev, opts, max_units);
   if (grid == 0) return FLUX_ERR_CUDA;
   return launch_dt<MODE_MOE_SCATTER, MOE1_CL>(dtype, p, grid, s);
+}
+
+}  // namespace
+}  // namespace flux
+
+extern "C" flux_status_t flux_moe_ag_grouped_gemm(
+    int R, int T, int H, int F, int E, int topk, flux_dtype_t dtype, const void* const* x_shards,
+    const void* const* w1_shards, const int32_t* topk_ids, void* const* h_out, int32_t* counts,
+    int32_t* offsets, int32_t* slot_to_row, int32_t* row_to_slot, const uint32_t* ready_flags,
+    void* workspace, size_t workspace_bytes, const flux_opts_t* opts, void* stream) {
+  return moe_layer0_impl(R, R, T, H, F, E, topk, dtype, x_shards, w1_shards, topk_ids, h_out,
+                         counts, offsets, slot_to_row, row_to_slot, ready_flags, workspace,
+                         workspace_bytes, opts, stream);
+}
+
+extern "C" flux_status_t flux_moe_grouped_gemm_rs(
+    int R, int T, int H, int F, int E, int topk, flux_dtype_t dtype, const void* const* h_shards,
+    const void* const* w2_shards, const int32_t* topk_ids, const float* topk_weights,
+    const int32_t* offsets, const int32_t* slot_to_row, const int32_t* row_to_slot,
+    void* const* out, void* workspace, size_t workspace_bytes, const flux_opts_t* opts,
+    void* stream) {
+  return moe_layer1_impl(R, R, T, H, F, E, topk, dtype, h_shards, w2_shards, topk_ids,
+                         topk_weights, offsets, slot_to_row, row_to_slot, out, workspace,
+                         workspace_bytes, opts, stream);
+}
+
+extern "C" flux_status_t flux_moe_ep_dispatch_gemm(
+    int R, int tp, int T, int H, int F, int E, int topk, flux_dtype_t dtype,
+    const void* const* x_shards, const void* const* w1_shards, const int32_t* topk_ids,
+    void* const* h_out, int32_t* counts, int32_t* offsets, int32_t* slot_to_row,
+    int32_t* row_to_slot, const uint32_t* ready_flags, void* workspace, size_t workspace_bytes,
+    const flux_opts_t* opts, void* stream) {
+  return moe_layer0_impl(tp, R, T, H, F, E, topk, dtype, x_shards, w1_shards, topk_ids, h_out,
+                         counts, offsets, slot_to_row, row_to_slot, ready_flags, workspace,
+                         workspace_bytes, opts, stream);
+}
+
+extern "C" flux_status_t flux_moe_ep_gemm_combine(
+    int R, int tp, int T, int H, int F, int E, int topk, flux_dtype_t dtype,
+    const void* const* h_shards, const void* const* w2_shards, const int32_t* topk_ids,
+    const float* topk_weights, const int32_t* offsets, const int32_t* slot_to_row,
+    const int32_t* row_to_slot, void* const* out, void* workspace, size_t workspace_bytes,
+    const flux_opts_t* opts, void* stream) {
+  return moe_layer1_impl(tp, R, T, H, F, E, topk, dtype, h_shards, w2_shards, topk_ids,
+                         topk_weights, offsets, slot_to_row, row_to_slot, out, workspace,
+                         workspace_bytes, opts, stream);
 }
 
 extern "C" flux_status_t flux_moe_layers(int R, int T, int H, int F, int E, int topk,

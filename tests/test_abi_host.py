@@ -56,6 +56,10 @@ def test_workspace_sizes(fx):
     assert s >= 256 + 4096 * 4096 * 4 + 4096 * 16 * 4
     assert fx.flux_moe_workspace_size(fx.FLUX_OP_MOE_AG, 8, 4096, 4096, 14336, 8, 2) > 256
     assert fx.flux_moe_workspace_size(fx.FLUX_OP_MOE_AG, 3, 4096, 4096, 14336, 8, 2) == 0
+    # the EP x TP split does not change the workspace, and F need not divide by R
+    assert fx.flux_moe_workspace_size(fx.FLUX_OP_MOE_EP_RS, 8, 4096, 4096, 14336, 8, 2) == s
+    assert fx.flux_moe_workspace_size(fx.FLUX_OP_MOE_EP_AG, 3, 4095, 4096, 14336, 6, 2) > 256
+    assert fx.flux_moe_workspace_size(fx.FLUX_OP_MOE_EP_AG, 3, 4096, 4096, 14336, 6, 2) == 0
 
 
 FAKE = 1 << 20  # never dereferenced: every case below fails validation first
@@ -120,6 +124,14 @@ def test_host_validation_without_gpu(fx):
                 FAKE, FAKE, FAKE, FAKE, None, big, stream=S) == fx.FLUX_ERR_INVALID_ARG  # topk > E
     assert _err(fx, fx.flux_moe_grouped_gemm_rs, 2, 64, 64, 64, 4, 2, fx.FLUX_F16, p, p, FAKE, FAKE,
                 FAKE, None, None, p, big, stream=S) == fx.FLUX_ERR_INVALID_ARG  # partial routing
+    for tp in (1, 3):  # E = 6 experts over 4 groups; tp = 3 does not divide R = 4
+        assert _err(fx, fx.flux_moe_ep_dispatch_gemm, 4, tp, 64, 64, 64, 6, 2, fx.FLUX_F16, p, p,
+                    FAKE, p, FAKE, FAKE, FAKE, FAKE, None, big, stream=S) == fx.FLUX_ERR_INVALID_ARG
+        assert _err(fx, fx.flux_moe_ep_gemm_combine, 4, tp, 64, 64, 64, 6, 2, fx.FLUX_F16, p, p,
+                    FAKE, FAKE, None, None, None, p, big, stream=S) == fx.FLUX_ERR_INVALID_ARG
+    assert _err(fx, fx.flux_moe_ep_dispatch_gemm, 4, 2, 64, 64, 60, 4, 2, fx.FLUX_F16, p, p,
+                FAKE, p, FAKE, FAKE, FAKE, FAKE, None, big, stream=S) == \
+        fx.FLUX_ERR_UNSUPPORTED  # F/tp = 30 columns: rows not 16-byte aligned
 
 
 def test_valid_call_without_gpu_reports_instead_of_crashing(fx):
