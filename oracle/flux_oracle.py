@@ -19,6 +19,9 @@ What it computes and where that is defined
       routing (stable counting sort of the top-k slots by expert) -> :func:`moe_route`
       layer0 = gather-by-expert(AllGather(X)) . W1_{e,r}         -> :func:`moe_layer0`
       layer1 = ReduceScatter_by_token(sum_k g_k . (H_r . W2_{e,r})) -> :func:`moe_layer1`
+  the same two layers under the EP x TP split of the experts (the EP/TP ratio
+  of that section) -> :func:`moe_ep_layer0`, :func:`moe_ep_layer1`, and the
+  top-k gate that produces the routing from router scores -> :func:`moe_topk_gate`.
 
 Precision: the pages fix none, so every floating-point result here is the
 exact float64 value of the stored 16-bit inputs combined in float64 (a
@@ -40,7 +43,7 @@ import numpy as np
 __all__ = [
     "widen", "round_to", "gemm", "ag_gemm", "gemm_rs", "moe_route",
     "moe_layer0", "moe_layer1", "ag_gemm_at", "gemm_rs_at", "moe_layer0_rows",
-    "moe_layer1_rows", "moe_ep_layer0", "moe_ep_layer1",
+    "moe_layer1_rows", "moe_ep_layer0", "moe_ep_layer1", "moe_topk_gate",
 ]
 
 
@@ -199,6 +202,42 @@ def moe_route(topk_ids: np.ndarray, E: int):
         row_to_slot[row] = s
     i32 = lambda v: np.asarray(v, dtype=np.int32)  # noqa: E731
     return i32(counts), i32(offsets), i32(slot_to_row), i32(row_to_slot)
+
+
+def moe_topk_gate(logits, topk: int):
+    """Top-k expert choice and gate weights of each token from its router scores.
+
+    The pages name the MoE layer (COMET article, "COMET 是什么") but not its
+    gate; reading: the plainest Mixture-of-Experts gate.  For token t with fp32
+    scores s[t, 0..E-1] (a NaN counts as -inf):
+      ids[t]  the topk experts with the largest scores, largest first, equal
+              scores in ascending expert order;
+      w[t, j] = exp(s_j - s_0) / sum_i exp(s_i - s_0) over the chosen scores
+              (s_0 the largest), i.e. softmax over all E renormalised over the
+              chosen k.  If s_0 is infinite the chosen scores equal to s_0
+              share the weight equally and the others get 0 (the limit).
+    Returns (int32 [T, topk], float64 [T, topk]).  Decisions are taken on the
+    fp32 values exactly; the weights are float64.
+    """
+    import math
+    L = np.asarray(logits, dtype=np.float32)
+    T, E = L.shape
+    if not 1 <= topk <= E:
+        raise ValueError("need 1 <= topk <= E")
+    ids = np.zeros((T, topk), dtype=np.int32)
+    w = np.zeros((T, topk), dtype=np.float64)
+    for t in range(T):
+        s = [float("-inf") if math.isnan(float(v)) else float(v) for v in L[t]]
+        chosen = sorted(range(E), key=lambda e: (-s[e], e))[:topk]
+        top = s[chosen[0]]
+        if math.isinf(top):
+            z = [1.0 if s[e] == top else 0.0 for e in chosen]
+        else:
+            z = [math.exp(s[e] - top) for e in chosen]
+        total = math.fsum(z)
+        ids[t] = chosen
+        w[t] = [v / total for v in z]
+    return ids, w
 
 
 def moe_layer0(x_shards, w1_shards, topk_ids, E: int, dtype: str):

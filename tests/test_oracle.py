@@ -474,3 +474,52 @@ def test_moe_ep_rank_rows_are_the_owner_experts():
             e = int(d["topk_ids"][s // c.topk, s % c.topk])
             assert e // el == r
             assert np.allclose(h[row], X[s // c.topk] @ oracle.widen(W1[e], "f16"), rtol=1e-14)
+
+
+# ---------------------------------------------------------------- top-k gate
+def test_gate_topk_equals_e_is_the_softmax():
+    # k = E: every expert chosen, weights = the library softmax of the scores
+    from scipy.special import softmax
+    g = np.random.default_rng(3)
+    L = g.standard_normal((6, 5)).astype(np.float32) * 3
+    ids, w = oracle.moe_topk_gate(L, 5)
+    for t in range(6):
+        want = softmax(L[t].astype(np.float64))
+        assert np.allclose(w[t], want[ids[t]], rtol=1e-13, atol=0)
+        assert np.all(np.diff(L[t][ids[t]]) <= 0)  # largest first
+
+
+def test_gate_topk_is_the_renormalised_softmax():
+    from scipy.special import softmax
+    g = np.random.default_rng(4)
+    L = g.standard_normal((20, 16)).astype(np.float32)
+    for k in (1, 2, 5):
+        ids, w = oracle.moe_topk_gate(L, k)
+        for t in range(20):
+            full = softmax(L[t].astype(np.float64))
+            assert set(ids[t].tolist()) == set(np.argsort(-full, kind="stable")[:k].tolist())
+            assert np.allclose(w[t], full[ids[t]] / full[ids[t]].sum(), rtol=1e-13)
+        if k == 1:
+            assert np.array_equal(ids[:, 0], np.argmax(L, axis=1)) and np.all(w == 1.0)
+
+
+def test_gate_ties_shift_and_infinities():
+    L = np.array([[1, 3, 3, 2],            # tie: lower id first, equal weights
+                  [0, 0, 0, 0],            # all equal: ids 0, 1
+                  [np.nan, -1, 5, np.inf],  # +inf wins everything
+                  [-np.inf] * 4,           # all -inf: lowest ids, uniform
+                  [np.nan, np.nan, 2, 2]],  # NaN counts as -inf
+                 dtype=np.float32)
+    ids, w = oracle.moe_topk_gate(L, 2)
+    assert ids.tolist() == [[1, 2], [0, 1], [3, 2], [0, 1], [2, 3]]
+    assert w.tolist() == [[0.5, 0.5], [0.5, 0.5], [1.0, 0.0], [0.5, 0.5], [0.5, 0.5]]
+    # a constant shift of a token's scores changes nothing (exactly representable shift)
+    g = np.random.default_rng(5)
+    B = np.round(g.standard_normal((8, 8)) * 64).astype(np.float32) / 64
+    i0, w0 = oracle.moe_topk_gate(B, 3)
+    i1, w1 = oracle.moe_topk_gate(B + np.float32(8), 3)
+    assert np.array_equal(i0, i1) and np.allclose(w0, w1, rtol=1e-14)
+    # two chosen scores a, b: w = (1 / (1 + e^(b-a)), e^(b-a) / (1 + e^(b-a)))
+    _, w2 = oracle.moe_topk_gate(np.array([[0.0, 1.0, -7.0]], dtype=np.float32), 2)
+    e = np.exp(-1.0)
+    assert np.allclose(w2[0], [1 / (1 + e), e / (1 + e)], rtol=1e-15)
