@@ -10,6 +10,7 @@
  * and the MoE variant of COMET (COMET article, section "COMET 的技术原理":
  * the shared tensor is cut along the token dimension, tokens are gathered to
  * experts, expert outputs are combined back per token):
+ *     top-k gate (router scores -> expert ids, softmax weights) flux_moe_topk_gate
  *     routing (histogram + prefix sum + stable permutation)  flux_moe_route
  *     AllGather + gather-by-expert + grouped GEMM            flux_moe_ag_grouped_gemm
  *     grouped GEMM + top-k weighted combine + ReduceScatter  flux_moe_grouped_gemm_rs
@@ -228,6 +229,24 @@ flux_status_t flux_gemm_rs_noalloc(int R, int M, int N, int K, flux_dtype_t dtyp
                                    void* const* out, const flux_opts_t* opts, void* stream);
 
 /* ---------------------------------------------------------------- MoE ops */
+
+/* Top-k gate of T tokens over E experts from fp32 router scores.  The pages
+ * name the Mixture-of-Experts layer (COMET article, "COMET 是什么") but not
+ * its gate; this is the plain one:
+ *   logits        device float32[T x E]
+ *   topk_ids      device int32[T x topk]: the topk largest scores of the token,
+ *                 largest first, equal scores in ascending expert order (a NaN
+ *                 score counts as -inf)
+ *   topk_weights  device float32[T x topk]: softmax over the chosen scores,
+ *                 exp(s_j - s_0) / sum_i exp(s_i - s_0) in fp32 with expf (the
+ *                 softmax over all E renormalised over the chosen k); if the
+ *                 largest chosen score s_0 is infinite, the chosen scores equal
+ *                 to it share the weight equally and the rest get 0
+ * The ids are exact (decided on the fp32 scores); deterministic.  Requires
+ * 1 <= topk <= E <= FLUX_MAX_EXPERTS; bad sizes or NULL buffers (T > 0) return
+ * FLUX_ERR_INVALID_ARG. */
+flux_status_t flux_moe_topk_gate(int T, int E, int topk, const float* logits, int32_t* topk_ids,
+                                 float* topk_weights, void* stream);
 
 /* Routing of T tokens with topk experts each (COMET article, section
  * "COMET 的技术原理", token-dimension decomposition).  Slot s = t*topk + k.

@@ -93,6 +93,7 @@ _SIGS = {
     "flux_ag_gemm": ([_i, _i, _i, _i, _i, _vpp, _vpp, _vpp, _vp, _vp, _sz, _opt, _vp], _i),
     "flux_gemm_rs": ([_i, _i, _i, _i, _i, _vpp, _vpp, _vpp, _vp, _sz, _opt, _vp], _i),
     "flux_gemm_rs_noalloc": ([_i, _i, _i, _i, _i, _vpp, _vpp, _vpp, _opt, _vp], _i),
+    "flux_moe_topk_gate": ([_i, _i, _i, _vp, _vp, _vp, _vp], _i),
     "flux_moe_route": ([_i, _i, _i, _vp, _vp, _vp, _vp, _vp, _vp, _sz, _vp], _i),
     "flux_moe_ag_grouped_gemm": ([_i, _i, _i, _i, _i, _i, _i, _vpp, _vpp, _vp, _vpp, _vp, _vp,
                                   _vp, _vp, _vp, _vp, _sz, _opt, _vp], _i),
@@ -228,6 +229,12 @@ def flux_gemm_rs_noalloc(R, M, N, K, dtype, a_shards, b_shards, out, opts=None,
     _check(_lib.flux_gemm_rs_noalloc(R, M, N, K, dtype, _ptrs(a_shards), _ptrs(b_shards),
                                      _ptrs(out), _opts(opts), _stream(stream)),
            "flux_gemm_rs_noalloc")
+
+
+def flux_moe_topk_gate(T, E, topk, logits, topk_ids, topk_weights, stream=None) -> None:
+    """Top-k expert ids and softmax gate weights from fp32 router scores."""
+    _check(_lib.flux_moe_topk_gate(T, E, topk, _ptr(logits), _ptr(topk_ids), _ptr(topk_weights),
+                                   _stream(stream)), "flux_moe_topk_gate")
 
 
 def flux_moe_route(T, E, topk, topk_ids, counts, offsets, slot_to_row, row_to_slot,

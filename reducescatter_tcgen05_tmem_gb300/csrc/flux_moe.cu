@@ -1,6 +1,10 @@
-// MoE entry points: routing (histogram, prefix sum, stable permutation),
-// AllGather + gather-by-expert + grouped GEMM (layer0), and grouped GEMM +
-// gate-weighted combine + ReduceScatter by token (layer1).
+// MoE entry points: the top-k gate, routing (histogram, prefix sum, stable
+// permutation), AllGather + gather-by-expert + grouped GEMM (layer0), and
+// grouped GEMM + gate-weighted combine + ReduceScatter by token (layer1), in
+// the tensor-parallel layout and under an EP x TP split of the experts.
+#include <math.h>
+
+#include <algorithm>
 #include <mutex>
 
 #include "flux_host.h"
@@ -170,6 +174,76 @@ moe_route_kernel(const int32_t* __restrict__ ids, int n, int E, int32_t* counts,
   if (bad && hdr != nullptr && tid == 0) atomicCAS(hdr + H_STATUS, 0u, ST_INVALID);
 }
 
+constexpr int GATE_WARPS = 8;  // tokens per CTA at a time (one warp each)
+
+// Top-k gate, one warp per token.  The token's scores are staged in shared
+// memory (a NaN becomes -inf); topk rounds of a warp-wide arg-max (largest
+// score, then lowest expert id) pick the experts, each chosen score marked NaN
+// so that later rounds skip it; the chosen scores are then turned into
+// softmax weights in fp32: exp(s_j - s_0) / sum over the chosen, s_0 the
+// largest, or, when s_0 is infinite, equal shares among the scores equal to
+// it.  The weights array holds the chosen scores between the two passes.
+__global__ void __launch_bounds__(GATE_WARPS * 32)
+moe_topk_gate_kernel(const float* __restrict__ logits, int T, int E, int topk,
+                     int32_t* __restrict__ ids, float* __restrict__ weights) {
+  extern __shared__ float gate_scores[];
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  float* sv = gate_scores + warp * E;
+  for (int t = blockIdx.x * GATE_WARPS + warp; t < T; t += gridDim.x * GATE_WARPS) {
+    const float* row = logits + static_cast<size_t>(t) * E;
+    for (int e = lane; e < E; e += 32) {
+      const float v = __ldg(row + e);
+      sv[e] = (v != v) ? -INFINITY : v;
+    }
+    __syncwarp();
+    int32_t* id_out = ids + static_cast<size_t>(t) * topk;
+    float* w_out = weights + static_cast<size_t>(t) * topk;
+    float top = 0.0f;
+    for (int j = 0; j < topk; ++j) {
+      float best = -INFINITY;
+      int bi = E;  // no candidate yet; any unchosen score, even -inf, beats it
+      for (int e = lane; e < E; e += 32) {
+        const float v = sv[e];
+        if (v != v) continue;  // chosen in an earlier round
+        if (v > best || (v == best && e < bi)) {
+          best = v;
+          bi = e;
+        }
+      }
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) {
+        const float ob = __shfl_xor_sync(0xFFFFFFFFu, best, o);
+        const int oi = __shfl_xor_sync(0xFFFFFFFFu, bi, o);
+        if (ob > best || (ob == best && oi < bi)) {
+          best = ob;
+          bi = oi;
+        }
+      }
+      // (best, bi) is the same in every lane: a total order has one maximum,
+      // and j < topk <= E leaves at least one unchosen score
+      if (j == 0) top = best;
+      if (lane == 0) {
+        id_out[j] = bi;
+        w_out[j] = best;
+      }
+      if (lane == (bi & 31)) sv[bi] = NAN;
+      __syncwarp();
+    }
+    const bool inf_top = isinf(top);
+    float zsum = 0.0f;
+    for (int j = lane; j < topk; j += 32) {
+      const float sj = w_out[j];
+      const float z = inf_top ? (sj == top ? 1.0f : 0.0f) : expf(sj - top);
+      w_out[j] = z;
+      zsum += z;
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) zsum += __shfl_xor_sync(0xFFFFFFFFu, zsum, o);
+    for (int j = lane; j < topk; j += 32) w_out[j] = w_out[j] / zsum;
+    __syncwarp();
+  }
+}
+
 // tile_off[e] = sum_{e' < e} ceil(count_e' / unit_rows) from a given offsets array.
 __global__ void tile_offsets_kernel(const int32_t* offsets, int E, int unit_rows, int32_t* tile_off) {
   if (threadIdx.x != 0 || blockIdx.x != 0) return;
@@ -277,6 +351,28 @@ extern "C" size_t flux_moe_workspace_size(flux_op_t op, int R, int T, int H, int
   // the one-call layer runs layer0 inside layer1's workspace, whose routing
   // slots receive layer0's routing
   return moe_layout(op == FLUX_OP_MOE_LAYERS ? FLUX_OP_MOE_RS : op, R, T, H, F, E, topk).total;
+}
+
+extern "C" flux_status_t flux_moe_topk_gate(int T, int E, int topk, const float* logits,
+                                            int32_t* topk_ids, float* topk_weights,
+                                            void* stream) {
+  if (T < 0 || E < 1 || E > FLUX_MAX_EXPERTS || topk < 1 || topk > E ||
+      static_cast<long long>(T) * E >= (1ll << 40) ||
+      static_cast<long long>(T) * topk >= (1ll << 31))
+    return FLUX_ERR_INVALID_ARG;
+  if (T > 0 && (logits == nullptr || topk_ids == nullptr || topk_weights == nullptr))
+    return FLUX_ERR_INVALID_ARG;
+  DeviceInfo dev;
+  flux_status_t st = current_device(&dev);
+  if (st != FLUX_OK) return st;
+  if (T == 0) return FLUX_OK;
+  const long long want = (static_cast<long long>(T) + GATE_WARPS - 1) / GATE_WARPS;
+  const int grid = static_cast<int>(std::min<long long>(want, 8ll * dev.sm_count));
+  const size_t smem = static_cast<size_t>(GATE_WARPS) * E * sizeof(float);  // <= 32 KB
+  moe_topk_gate_kernel<<<grid, GATE_WARPS * 32, smem, static_cast<cudaStream_t>(stream)>>>(
+      logits, T, E, topk, topk_ids, topk_weights);
+  cudaError_t e = cudaGetLastError();
+  return e == cudaSuccess ? FLUX_OK : cuda_fail(e);
 }
 
 extern "C" flux_status_t flux_moe_route(int T, int E, int topk, const int32_t* topk_ids,

@@ -66,7 +66,7 @@ def moe_small():
     y = oracle.moe_layer1(d["h_shards"], d["w2_shards"], d["topk_ids"], d["topk_weights"], c.E, c.dtype)
     return {"source": "Comet article, 'COMET 的技术原理' (token-dimension decomposition, gather to "
                       "experts, combine by token); MoE R=8 reduced to T=64 H=64 F=128 E=8 top-2, "
-                      "Zipf(1.2) router bias, bf16, seed 5",
+                      "Zipf(1.2) expert load, bf16, seed 5",
             "config": "moe reduced T=64 H=64 F=128",
             "topk_ids": d["topk_ids"].tolist(),
             "counts": counts.tolist(), "offsets": offsets.tolist(),
@@ -76,9 +76,20 @@ def moe_small():
             "layer1_row0_head": [float(v) for v in y[0][0, :8]]}
 
 
+def gate_small():
+    from workloads import gen
+    L = gen.router_logits(17, 16, 8)
+    ids, w = oracle.moe_topk_gate(L, 2)
+    return {"source": "Comet article, 'COMET 是什么' (Mixture-of-Experts layer; the gate is the "
+                      "plain top-k + softmax reading); router scores N(0,1) + Zipf(1.2) bias, "
+                      "T=16 E=8 top-2, seed 17",
+            "config": "gate T=16 E=8 topk=2",
+            "topk_ids": ids.tolist(), "topk_weights": [[float(v) for v in row] for row in w]}
+
+
 def main():
     for name, fn in [("rs_r2_small.json", rs_r2_small), ("ag_small.json", ag_small),
-                     ("moe_small.json", moe_small)]:
+                     ("moe_small.json", moe_small), ("gate_small.json", gate_small)]:
         obj = fn()
         body = ",\n".join(f"{json.dumps(k)}: {json.dumps(v, ensure_ascii=False)}" for k, v in obj.items())
         with open(os.path.join(HERE, name), "w") as f:

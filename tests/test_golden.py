@@ -47,3 +47,11 @@ def test_moe_small_fixture():
     y = oracle.moe_layer1(d["h_shards"], d["w2_shards"], d["topk_ids"], d["topk_weights"], c.E, c.dtype)
     assert np.allclose([np.linalg.norm(x) for x in y], fx["layer1_frobenius"], rtol=1e-12)
     assert np.allclose(y[0][0, :8], fx["layer1_row0_head"], rtol=1e-12)
+
+
+def test_gate_small_fixture():
+    from workloads import gen
+    fx = _load("gate_small.json")
+    ids, w = oracle.moe_topk_gate(gen.router_logits(17, 16, 8), 2)
+    assert ids.tolist() == fx["topk_ids"]
+    assert np.allclose(w, fx["topk_weights"], rtol=1e-14, atol=0)

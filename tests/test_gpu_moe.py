@@ -63,6 +63,58 @@ def test_routing_records_invalid_expert_id():
     assert counts.tolist() == [2, 2, 1, 0] and offsets[-1] == 5 and s2r[2] == -1
 
 
+# ---------------------------------------------------------------- top-k gate
+def _gate_gpu(L, topk):
+    T, E = L.shape
+    d_l = torch.from_numpy(np.ascontiguousarray(L, dtype=np.float32)).cuda()
+    ids = torch.full((max(T * topk, 1),), -7, dtype=torch.int32, device="cuda")
+    w = torch.full((max(T * topk, 1),), float("nan"), dtype=torch.float32, device="cuda")
+    fx.flux_moe_topk_gate(T, E, topk, d_l, ids, w)
+    torch.cuda.synchronize()
+    return (ids[:T * topk].cpu().numpy().reshape(T, topk),
+            w[:T * topk].cpu().numpy().astype(np.float64).reshape(T, topk))
+
+
+def _check_gate(L, topk):
+    ids, w = _gate_gpu(L, topk)
+    rid, rw = oracle.moe_topk_gate(L, topk)
+    assert np.array_equal(ids, rid)
+    # expf and an fp32 sum over the k chosen scores: a few ulp relative
+    assert np.allclose(w, rw, rtol=4e-6 + 2e-7 * topk, atol=1e-37)
+
+
+@pytest.mark.parametrize("T,E,topk", [(4096, 8, 2), (33, 5, 3), (1000, 64, 8), (257, 1, 1),
+                                      (8192, 256, 4), (64, 1024, 32), (50, 40, 40), (0, 4, 2)])
+def test_gate_matches_oracle(T, E, topk):
+    _check_gate(gen.router_logits((88, T, E), T, E), topk)
+
+
+def test_gate_ties_and_specials():
+    g = np.random.default_rng(9)
+    ties = g.integers(-3, 4, size=(300, 48)).astype(np.float32)  # many equal scores
+    _check_gate(ties, 6)
+    sp = gen.router_logits(89, 64, 16)
+    sp[0, :] = np.nan
+    sp[1, 3] = np.inf
+    sp[2, [1, 5]] = np.inf
+    sp[3, :] = -np.inf
+    sp[4, ::2] = np.nan
+    sp[5, :] = 1e30
+    sp[6, 7] = -1e30
+    _check_gate(sp, 3)
+
+
+def test_gate_feeds_the_routing():
+    # gate -> route on the device equals the oracle's gate -> route
+    L = gen.router_logits(90, 512, 8, force_empty=(6,))
+    ids, _ = _gate_gpu(L, 2)
+    got = _route_gpu(ids, 8)
+    want = oracle.moe_route(oracle.moe_topk_gate(L, 2)[0], 8)
+    for a, b in zip(got, want):
+        assert np.array_equal(a, b)
+    assert got[0][6] == 0
+
+
 # ---------------------------------------------------------------- layer0
 def _layer0(c, d=None, flags=None, opts=None):
     if d is None:

@@ -24,7 +24,7 @@ import numpy as np
 
 __all__ = [
     "CHUNK", "DTYPES", "f32_to_bf16_bits", "bf16_bits_to_f32", "to_f32",
-    "normal16", "uniform16", "integers16", "routing", "zipf_bias",
+    "normal16", "uniform16", "integers16", "routing", "router_logits", "zipf_bias",
     "split_rows", "split_cols",
 ]
 
@@ -141,8 +141,8 @@ def integers16(seed, shape, lo: int, hi: int, dtype: str) -> np.ndarray:
 def zipf_bias(E: int, s: float) -> np.ndarray:
     """Per-expert additive router bias ln(p_e) with p_e proportional to (e+1)^-s.
 
-    Expert 0 is the most loaded; the bias skews top-k selection toward a
-    Zipf(s)-like load over the experts.
+    Expert 0 is the most loaded; added to N(0, 1) router scores it skews a
+    top-k gate toward a Zipf(s)-like load over the experts.
     """
     p = (np.arange(1, E + 1, dtype=np.float64)) ** (-float(s))
     p /= p.sum()
@@ -151,32 +151,40 @@ def zipf_bias(E: int, s: float) -> np.ndarray:
 
 def routing(seed, T: int, E: int, topk: int, zipf_s: float = 1.2,
             force_empty: tuple = ()):
-    """Top-k router outputs for T tokens over E experts.
+    """Top-k routing of T tokens over E experts, drawn directly (no gate).
 
-    logits ~ N(0, 1) [T x E] plus the Zipf bias; the top-k scores are chosen
-    (ties to the lower expert id, slot k=0 holds the highest score) and the gate
-    weights are the softmax over the k chosen scores.  Experts listed in
-    ``force_empty`` are never chosen (used to exercise empty experts).
+    Each token's topk distinct experts are drawn without replacement with
+    probabilities proportional to (e+1)^-s, a Zipf(s) load with expert 0 the
+    most loaded; experts listed in ``force_empty`` are never drawn (used to
+    exercise empty experts).  The gate weights of a token are a flat Dirichlet
+    draw over its k slots, largest in slot 0.  Router scores for the gate
+    itself come from :func:`router_logits`.
 
     Returns ``(topk_ids int32 [T, topk], topk_weights float32 [T, topk])``.
     """
-    if topk > E - len(force_empty):
+    empty = set(int(e) for e in force_empty)
+    sel = np.array([e for e in range(E) if e not in empty], dtype=np.int64)
+    if topk > sel.size:
         raise ValueError("topk larger than the number of selectable experts")
     g = np.random.Generator(np.random.PCG64(_seed_seq(seed, 0)))
-    logits = g.standard_normal((T, E))
-    score = logits + zipf_bias(E, zipf_s)[None, :]
-    for e in force_empty:
-        score[:, e] = -np.inf
-    # lexsort: primary key -score (descending score), secondary key expert id.
+    p = (sel + 1.0) ** (-float(zipf_s))
+    p /= p.sum()
     ids = np.empty((T, topk), dtype=np.int32)
-    eidx = np.arange(E)
     for t in range(T):
-        order = np.lexsort((eidx, -score[t]))
-        ids[t] = order[:topk]
-    chosen = np.take_along_axis(score, ids.astype(np.int64), axis=1)
-    z = np.exp(chosen - chosen.max(axis=1, keepdims=True))
-    w = (z / z.sum(axis=1, keepdims=True)).astype(np.float32)
+        ids[t] = sel[g.choice(sel.size, size=topk, replace=False, p=p)]
+    w = g.dirichlet(np.ones(topk), size=T) if T else np.zeros((0, topk))
+    w = np.ascontiguousarray(np.sort(w, axis=1)[:, ::-1]).astype(np.float32)
     return ids, w
+
+
+def router_logits(seed, T: int, E: int, zipf_s: float = 1.2, force_empty: tuple = ()):
+    """Router scores float32 [T x E]: N(0, 1) plus the Zipf bias of :func:`zipf_bias`,
+    -inf for the experts in ``force_empty``."""
+    g = np.random.Generator(np.random.PCG64(_seed_seq(seed, 0)))
+    L = (g.standard_normal((T, E)) + zipf_bias(E, zipf_s)[None, :]).astype(np.float32)
+    for e in force_empty:
+        L[:, int(e)] = -np.inf
+    return L
 
 
 def split_rows(a: np.ndarray, R: int):
