@@ -38,7 +38,8 @@ METRIC = "fused AG-GEMM/GEMM-RS TFLOP/s vs fp16 peak; overhead vs plain GEMM (us
 UNIT = "TFLOP/s"
 WORKLOAD = ("hot-path step, R=8 virtual ranks: dense TP-MLP AG-GEMM 4096x12288x49152 -> "
             "GEMM-RS 4096x49152x12288 (fp16); decode GEMM-RS 128x28672x8192 (bf16); "
-            "MoE layer T=4096 H=4096 F=14336 E=8 top-2 routing+layer0+layer1 (bf16)")
+            "MoE layer T=4096 H=4096 F=14336 E=8: top-2 gate on router scores + routing + "
+            "layer0 + layer1 (bf16)")
 DTYPE = "f16/bf16 operands, fp32 accumulate"
 KERNEL_SOURCES = ["flux_kernels.cuh", "flux_ptx.cuh", "flux_dense.cu", "flux_moe.cu"]
 
@@ -135,7 +136,15 @@ class ClockSampler:
 class Step:
     """Device buffers and the launch sequence of one hot-path step."""
 
-    def __init__(self, torch, fx, dev, small=False):
+    # the hot-path step (the MoE layer starts from router scores: gate, then
+    # routing + layer0, then layer1); the expert-parallel MoE layers on the
+    # same workload are extra ops selected with --ops
+    STEP_OPS = ["ag_gemm", "gemm_rs", "decode_rs", "moe_gate", "moe_layer0", "moe_layer1"]
+    EXTRA_OPS = ["moe_ep_layer0", "moe_ep_layer1"]
+    LAUNCHES = {"ag_gemm": 1, "gemm_rs": 1, "decode_rs": 1, "moe_layer0": 2, "moe_layer1": 2,
+                "moe_gate": 1, "moe_ep_layer0": 2, "moe_ep_layer1": 2}
+
+    def __init__(self, torch, fx, dev, small=False, ops=None):
         from workloads.torch_io import to_device, torch_dtype
         self.torch, self.fx, self.dev = torch, fx, dev
         C = configs.CONFIGS
@@ -166,8 +175,10 @@ class Step:
         self.mX = [T(x, "bf16") for x in md["x_shards"]]
         self.mW1 = [T(w, "bf16") for w in md["w1_shards"]]
         self.mW2 = [T(w, "bf16") for w in md["w2_shards"]]
-        self.ids = torch.from_numpy(md["topk_ids"]).to(dev)
-        self.gw = torch.from_numpy(md["topk_weights"]).to(dev)
+        # router scores; the gate writes the routing the layers read
+        self.logits = torch.from_numpy(md["logits"]).to(dev)
+        self.ids = torch.empty(moe.T, moe.topk, dtype=torch.int32, device=dev)
+        self.gw = torch.empty(moe.T, moe.topk, dtype=torch.float32, device=dev)
         self.mH = [torch.empty(n, moe.F // moe.R, dtype=torch.bfloat16, device=dev) for _ in range(moe.R)]
         self.mY = [torch.empty(moe.T // moe.R, moe.H, dtype=torch.bfloat16, device=dev) for _ in range(moe.R)]
         self.counts = torch.empty(moe.E, dtype=torch.int32, device=dev)
@@ -187,9 +198,26 @@ class Step:
         self.flops = {
             "ag_gemm": ag.flops, "gemm_rs": rs.flops, "decode_rs": dec.flops,
             "moe_layer0": moe.flops_per_layer, "moe_layer1": moe.flops_per_layer,
+            "moe_ep_layer0": moe.flops_per_layer, "moe_ep_layer1": moe.flops_per_layer,
+            "moe_gate": 0.0,
         }
-        self.launches_per_step = 7  # ag, rs, decode rs, route + layer0, tile table + layer1
-        self.ops = ["ag_gemm", "gemm_rs", "decode_rs", "moe_layer0", "moe_layer1"]
+        self.ops = list(ops) if ops else list(self.STEP_OPS)
+        unknown = [o for o in self.ops if o not in self.STEP_OPS + self.EXTRA_OPS]
+        if unknown:
+            raise SystemExit(f"unknown ops {unknown}")
+        if "moe_ep_layer0" in self.ops or "moe_ep_layer1" in self.ops:
+            self.tp = 1
+            ed = configs.moe_ep_inputs(moe, self.tp, with_h=False)
+            self.eW1 = [T(w, "bf16") for w in ed["w1_shards"]]
+            self.eW2 = [T(w, "bf16") for w in ed["w2_shards"]]
+            hbuf = torch.empty(n, moe.F // self.tp, dtype=torch.bfloat16, device=dev)
+            self.eH = [hbuf] * moe.R  # one grouped buffer: each rank writes its expert's rows
+            self.ws_e0 = ws(fx.flux_moe_workspace_size(fx.FLUX_OP_MOE_EP_AG, moe.R, moe.T, moe.H,
+                                                       moe.F, moe.E, moe.topk))
+            self.ws_e1 = ws(fx.flux_moe_workspace_size(fx.FLUX_OP_MOE_EP_RS, moe.R, moe.T, moe.H,
+                                                       moe.F, moe.E, moe.topk))
+        self.run_op("moe_gate")  # the layers find a routing even when the gate is not timed
+        self.launches_per_step = sum(self.LAUNCHES[o] for o in self.ops)
 
     def run_op(self, name):
         fx, ag, rs, dec, moe = self.fx, self.ag, self.rs, self.dec, self.moe
@@ -208,6 +236,17 @@ class Step:
             fx.flux_moe_grouped_gemm_rs(moe.R, moe.T, moe.H, moe.F, moe.E, moe.topk, fx.FLUX_BF16, self.mH,
                                         self.mW2, self.ids, self.gw, self.offsets, self.s2r, self.r2s,
                                         self.mY, self.ws_m1)
+        elif name == "moe_gate":
+            fx.flux_moe_topk_gate(moe.T, moe.E, moe.topk, self.logits, self.ids, self.gw)
+        elif name == "moe_ep_layer0":
+            fx.flux_moe_ep_dispatch_gemm(moe.R, self.tp, moe.T, moe.H, moe.F, moe.E, moe.topk,
+                                         fx.FLUX_BF16, self.mX, self.eW1, self.ids, self.eH,
+                                         self.counts, self.offsets, self.s2r, self.r2s, self.mflags,
+                                         self.ws_e0)
+        elif name == "moe_ep_layer1":
+            fx.flux_moe_ep_gemm_combine(moe.R, self.tp, moe.T, moe.H, moe.F, moe.E, moe.topk,
+                                        fx.FLUX_BF16, self.eH, self.eW2, self.ids, self.gw,
+                                        self.offsets, self.s2r, self.r2s, self.mY, self.ws_e1)
 
     def step(self, events=None):
         for name in self.ops:
@@ -218,7 +257,8 @@ class Step:
                 events[name][1].record()
 
     def check_status(self):
-        for w in (self.ws_ag, self.ws_rs, self.ws_dec, self.ws_m0, self.ws_m1):
+        extra = [getattr(self, a) for a in ("ws_e0", "ws_e1") if hasattr(self, a)]
+        for w in [self.ws_ag, self.ws_rs, self.ws_dec, self.ws_m0, self.ws_m1] + extra:
             st, rep = self.fx.flux_get_status(w)
             if st != self.fx.FLUX_OK:
                 raise RuntimeError(f"device status {st}: {rep}")
@@ -267,9 +307,7 @@ def run_ours(args):
     __graft_entry__.build()
     import reducescatter_tcgen05_tmem_gb300 as fx
 
-    st = Step(torch, fx, dev, small=args.small)
-    if args.ops:
-        st.ops = args.ops.split(",")
+    st = Step(torch, fx, dev, small=args.small, ops=args.ops.split(",") if args.ops else None)
     for _ in range(args.warmup):
         st.step()
     torch.cuda.synchronize()
@@ -322,7 +360,10 @@ def run_ours(args):
             "moe_layer0": (st.moe.T * st.moe.topk, st.moe.F, st.moe.H, "bf16"),
             "moe_layer1": (st.moe.T * st.moe.topk, st.moe.H, st.moe.F, "bf16"),
         }
+        shapes["moe_ep_layer0"], shapes["moe_ep_layer1"] = shapes["moe_layer0"], shapes["moe_layer1"]
         for o in st.ops:
+            if o not in shapes:
+                continue
             M, N, K, d = shapes[o]
             tp = time_plain(torch, fx, dev, M, N, K, d)
             fused = per_op[o] / args.steps
@@ -336,6 +377,7 @@ def run_ours(args):
     breakdown = {o: {"ms": round(per_op[o] / args.steps, 4),
                      "tflops": round(st.flops[o] / (per_op[o] / args.steps * 1e-3) / 1e12, 1)}
                  for o in st.ops}
+    breakdown = {o: (v if st.flops[o] else {"ms": v["ms"]}) for o, v in breakdown.items()}
     dom = max(st.ops, key=lambda o: per_op[o])
     dom_ms = per_op[dom] / args.steps
     dom_tf = st.flops[dom] / (dom_ms * 1e-3) / 1e12
@@ -388,7 +430,7 @@ def e2e_measure(torch, st, args, dev):
     """Same metric through the public API with host buffers: pinned H2D of the
     step's activations and routing, the step, and D2H of its results."""
     host_in = []
-    dev_in = st.X + st.dA + st.mX + [st.ids, st.gw]
+    dev_in = st.X + st.dA + st.mX + [st.logits]
     for t in dev_in:
         host_in.append(torch.empty(t.shape, dtype=t.dtype, pin_memory=True).copy_(t))
     dev_out = st.out2 + st.dout + st.mY
@@ -440,7 +482,7 @@ def _sample_inputs(key):
 
 def oracle_sample(rows, cols, tokens, fcols):
     """One bounded CPU-oracle sample of the step (AG-GEMM, GEMM-RS, decode
-    GEMM-RS, MoE routing + layer0 + layer1) on a row/column sample of every op.
+    GEMM-RS, MoE gate + routing + layer0 + layer1) on a row/column sample of every op.
     Returns (flops, seconds of oracle time; input generation excluded)."""
     import oracle
     ag, rs, dec, m = _sample_configs(rows, cols, tokens, fcols)
@@ -449,9 +491,9 @@ def oracle_sample(rows, cols, tokens, fcols):
     oracle.ag_gemm(xs, w1, ag.dtype)
     oracle.gemm_rs(As, Bs, rs.dtype)
     oracle.gemm_rs(da, dw, dec.dtype)
-    h, routing = oracle.moe_layer0(md["x_shards"], md["w1_shards"], md["topk_ids"], m.E, m.dtype)
-    oracle.moe_layer1(h, md["w2_shards"], md["topk_ids"], md["topk_weights"], m.E, m.dtype,
-                      routing_=routing, h_dtype="f64")
+    ids, gates = oracle.moe_topk_gate(md["logits"], m.topk)
+    h, routing = oracle.moe_layer0(md["x_shards"], md["w1_shards"], ids, m.E, m.dtype)
+    oracle.moe_layer1(h, md["w2_shards"], ids, gates, m.E, m.dtype, routing_=routing, h_dtype="f64")
     secs = time.time() - t
     flops = ag.flops + rs.flops + dec.flops + 2 * m.flops_per_layer
     return flops, secs

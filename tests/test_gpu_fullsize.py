@@ -90,6 +90,8 @@ def test_decode_rs_full_size_full_compare():
 
 
 def test_moe_full_size_routing_exact_and_layers_sampled():
+    # the workload's routing: top-2 gate on the router scores, on the device
+    # (the path) and in the oracle; ids bit-exact, the layers then sampled
     c = configs.CONFIGS["moe"]
     d = configs.moe_inputs(c)
     n, Fr = c.T * c.topk, c.F // c.R
@@ -97,8 +99,13 @@ def test_moe_full_size_routing_exact_and_layers_sampled():
     W1 = [to_device(w, c.dtype) for w in d["w1_shards"]]
     W2 = [to_device(w, c.dtype) for w in d["w2_shards"]]
     Hin = [to_device(h, c.dtype) for h in d["h_shards"]]
-    ids = torch.from_numpy(d["topk_ids"]).cuda()
-    gw = torch.from_numpy(d["topk_weights"]).cuda()
+    ids = torch.empty(c.T, c.topk, dtype=torch.int32, device="cuda")
+    gw = torch.empty(c.T, c.topk, dtype=torch.float32, device="cuda")
+    fx.flux_moe_topk_gate(c.T, c.E, c.topk, torch.from_numpy(d["logits"]).cuda(), ids, gw)
+    ref_ids, ref_gw = oracle.moe_topk_gate(d["logits"], c.topk)
+    assert np.array_equal(ids.cpu().numpy(), ref_ids)
+    assert np.allclose(gw.cpu().numpy(), ref_gw, rtol=5e-6, atol=1e-37)
+    d["topk_ids"], d["topk_weights"] = ref_ids, ref_gw  # the oracle continues from its own gate
     H = [torch.empty(n, Fr, dtype=torch.bfloat16, device="cuda") for _ in range(c.R)]
     counts = torch.empty(c.E, dtype=torch.int32, device="cuda")
     offsets = torch.empty(c.E + 1, dtype=torch.int32, device="cuda")

@@ -19,7 +19,7 @@ from dataclasses import dataclass, replace
 
 import numpy as np
 
-from .gen import integers16, normal16, routing, uniform16
+from .gen import integers16, normal16, router_logits, routing, uniform16
 
 __all__ = ["DenseAG", "DenseRS", "MoE", "CONFIGS", "ag_inputs", "rs_inputs",
            "moe_inputs", "moe_ep_inputs", "small"]
@@ -143,7 +143,12 @@ def moe_inputs(c: MoE, with_h: bool = True):
     x_shards  R x [T/R, H]            token rows owned by each rank
     w1_shards R x [E, H, F/R]         every expert's W1 column block of rank r
     w2_shards R x [E, F/R, H]         every expert's W2 row block of rank r
+    logits    float32 [T, E]          router scores of the workload: N(0, 1) plus the
+                                      Zipf(s) bias; the top-k gate (a step of the path,
+                                      and of the oracle) turns them into the routing
     topk_ids  int32 [T, topk], topk_weights float32 [T, topk]
+                                      a directly drawn Zipf(s) routing (no gate), the
+                                      input of the layer-level tests
     h_shards  R x [T*topk, F/R]       a standalone layer1 input, N(0, 1)
     """
     if c.T % c.R or c.F % c.R:
@@ -159,6 +164,7 @@ def moe_inputs(c: MoE, with_h: bool = True):
                       for r in range(c.R)],
         "topk_ids": ids,
         "topk_weights": w,
+        "logits": router_logits((c.seed, 10), c.T, c.E, c.zipf_s, c.force_empty),
     }
     if with_h:
         d["h_shards"] = [_draw((c.seed, 4, r), (c.T * c.topk, Fr), 1.0, c.dtype, c.dist)
