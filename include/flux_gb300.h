@@ -103,6 +103,11 @@ typedef struct {
   int32_t deterministic_rs; /* GEMM-RS: nonzero = add the ranks' fp32 partials in ascending
                                rank order (bit-reproducible; slower: the adds of one tile
                                are serialised over the ranks) */
+  int32_t moe_pull_gather;  /* MoE layer0: nonzero = the GEMM's producer warps gather each
+                               A tile's token rows themselves (single CTAs, 128 x 256
+                               tiles); 0 (default) = every CTA first stages a share of
+                               the grouped rows in the workspace and CTA pairs compute
+                               256 x 256 tiles once their rows' ready counts are in */
 } flux_opts_t;
 
 /* What flux_get_status found in a workspace header. */
@@ -110,7 +115,7 @@ typedef struct {
   uint32_t status; /* flux_status_t of the first device-side error, 0 if none */
   uint32_t where;  /* which wait gave up: 1 ready flag, 2 smem slot free, 3 smem slot full,
                       4 accumulator free, 5 accumulator full, 6 drain,
-                      7 deterministic GEMM-RS turn */
+                      7 deterministic GEMM-RS turn, 8 staged MoE rows of an m-tile */
   uint32_t arg0;   /* flag wait: shard index; pipeline waits: CTA index */
   uint32_t arg1;   /* flag wait: last flag value seen; pipeline waits: stage / buffer */
 } flux_device_report_t;
@@ -270,6 +275,11 @@ flux_status_t flux_moe_route(int T, int E, int topk, const int32_t* topk_ids, in
  *   topk_ids      device int32[T x topk]
  *   h_out[r]      device, [T*topk x F/R]
  *   ready_flags   as in flux_ag_gemm (per token shard), or NULL
+ * By default the rows are gathered once, inside the same kernel, into a
+ * grouped copy [T*topk x H] in the workspace (flux_moe_workspace_size
+ * FLUX_OP_MOE_AG counts it), each 256-row tile published by a ready count
+ * that its GEMM tiles wait for; opts->moe_pull_gather selects the gather in
+ * the GEMM's producer warps instead (no copy).
  * Requires T and F divisible by R, H % 8 == 0, (F/R) % 8 == 0, 1 <= E <= FLUX_MAX_EXPERTS. */
 flux_status_t flux_moe_ag_grouped_gemm(int R, int T, int H, int F, int E, int topk,
                                        flux_dtype_t dtype, const void* const* x_shards,

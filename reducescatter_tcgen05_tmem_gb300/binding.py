@@ -50,14 +50,15 @@ FLUX_MAX_EXPERTS = 1024
 FLUX_NOALLOC_SCRATCH_BYTES = 16 * 1024 * 1024
 
 WAIT_SITES = {1: "ready flag", 2: "smem slot free", 3: "smem slot full",
-              4: "accumulator free", 5: "accumulator full", 6: "drain"}
+              4: "accumulator free", 5: "accumulator full", 6: "drain",
+              7: "deterministic turn", 8: "staged rows"}
 
 
 class flux_opts_t(ctypes.Structure):
     _fields_ = [("epoch", ctypes.c_uint32), ("reserved0", ctypes.c_uint32),
                 ("timeout_ns", ctypes.c_uint64), ("num_ctas", ctypes.c_int32),
                 ("group_n", ctypes.c_int32), ("tiles_per_group", ctypes.c_int32),
-                ("deterministic_rs", ctypes.c_int32)]
+                ("deterministic_rs", ctypes.c_int32), ("moe_pull_gather", ctypes.c_int32)]
 
 
 class flux_device_report_t(ctypes.Structure):

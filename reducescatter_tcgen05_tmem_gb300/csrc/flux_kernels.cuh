@@ -17,6 +17,9 @@
 //                       MOE_GATHER   STORE with A rows gathered by expert (MoE layer0)
 //                       MOE_SCATTER  gate-weighted fp32 add into the owning token row;
 //                                    the last of R*topk contributions converts (MoE layer1)
+//                       MOE_STAGED   STORE for MoE layer0 whose A rows were first
+//                                    gathered into a grouped staging buffer by every
+//                                    CTA of the same launch (per-tile ready counters)
 //
 // PAIR = 1: one CTA computes a 128 x 256 tile with tcgen05.mma.cta_group::1
 //           (4-stage ring of 48 KB: A 128x64 + B 64x256); two 256-column
@@ -42,8 +45,13 @@
 //           read it: each "empty" barrier counts one commit per pair.
 //
 // MoE layer1, CL = 2: a CTA pair computes a 256 x 256 tile inside one expert.
-// MoE layer0 gathers its A rows with cp.async, whose completion can only be
-// signalled in the issuing CTA, so it runs on single CTAs.
+// MoE layer0, two forms:
+//   MOE_GATHER, CL = 1: the producer gathers the A rows with cp.async, whose
+//     completion can only be signalled in the issuing CTA, so single CTAs.
+//   MOE_STAGED, CL = 2: every CTA first copies a share of the grouped A rows
+//     into a staging buffer and counts each finished 32-row block on its
+//     m-unit's ready counter; then CTA pairs compute 256 x 256 tiles whose
+//     producers wait for their unit's count and load A by TMA.
 //
 // The template parameter CL is the number of CTAs of a cluster (1, 2 or 4);
 // PAIR = min(CL, 2) is the tcgen05 CTA group and MC = CL / PAIR the pairs that
@@ -126,11 +134,31 @@ __device__ __forceinline__ uint32_t b_box_mask(int N, int n0, int cta) {
   return m;
 }
 
-enum Mode { MODE_STORE = 0, MODE_REDUCE = 1, MODE_MOE_GATHER = 2, MODE_MOE_SCATTER = 3 };
+enum Mode {
+  MODE_STORE = 0,
+  MODE_REDUCE = 1,
+  MODE_MOE_GATHER = 2,
+  MODE_MOE_SCATTER = 3,
+  MODE_MOE_STAGED = 4
+};
+__host__ __device__ constexpr bool is_moe(int mode) {
+  return mode == MODE_MOE_GATHER || mode == MODE_MOE_SCATTER || mode == MODE_MOE_STAGED;
+}
+constexpr int STAGE_BLK = 32;     // MOE_STAGED: rows per staging block (one ready count)
+constexpr int STAGE_UNROLL = 16;  // MOE_STAGED: 16-byte loads in flight per lane
 
 // device status header at the start of every workspace (256 bytes)
 enum HdrField { H_STATUS = 0, H_WHERE = 1, H_ARG0 = 2, H_ARG1 = 3, H_ABORT = 4 };
-enum WaitSite { W_FLAG = 1, W_EMPTY = 2, W_FULL = 3, W_TEMPTY = 4, W_TFULL = 5, W_DRAIN = 6, W_TURN = 7 };
+enum WaitSite {
+  W_FLAG = 1,
+  W_EMPTY = 2,
+  W_FULL = 3,
+  W_TEMPTY = 4,
+  W_TFULL = 5,
+  W_DRAIN = 6,
+  W_TURN = 7,
+  W_STAGE = 8
+};
 constexpr uint32_t ST_TIMEOUT = 5;
 constexpr uint32_t ST_INVALID = 1;
 
@@ -166,6 +194,8 @@ struct KParams {
   const int32_t* row_to_slot;  // [T*topk]
   const int32_t* tile_off;     // [E+1] first m-tile of each expert
   const float* topk_w;         // [T*topk]
+  void* stage;                 // MOE_STAGED: grouped A rows [T*topk x H], 16-bit
+  uint32_t* unit_cnt;          // MOE_STAGED: finished staging blocks per m-unit (zeroed by routing)
   int E, topk, T, H;
   int moe_tp;  // MoE: ranks per expert group (R: tensor parallel, 1: expert parallel)
   int moe_el;  // MoE: experts per group; rank g moe_tp + t holds block t of group g's experts
@@ -283,9 +313,10 @@ static __device__ __noinline__ bool wait_flag(const uint32_t* flags, int s, uint
 }
 
 // Bounded wait until *cnt >= target (acquire at gpu scope): the deterministic
-// GEMM-RS turn of one rank on one 32-row quarter.  True when it is this
-// rank's turn.
-static __device__ __noinline__ bool wait_turn(const uint32_t* cnt, uint32_t target, const Ctl& c) {
+// GEMM-RS turn of one rank on one 32-row quarter (W_TURN), or the staged rows
+// of one MoE m-unit (W_STAGE).  True when reached.
+static __device__ __noinline__ bool wait_count(const uint32_t* cnt, uint32_t target, const Ctl& c,
+                                               uint32_t where) {
   uint32_t v = ld_acquire_u32(cnt);
   if (v >= target) return true;
   const uint64_t t0 = globaltimer();
@@ -296,7 +327,7 @@ static __device__ __noinline__ bool wait_turn(const uint32_t* cnt, uint32_t targ
     if ((it & 7u) == 0u) {
       if (aborted(c)) return false;
       if (globaltimer() - t0 > c.pipe_timeout || it > (1u << 28)) {
-        raise_error(c, ST_TIMEOUT, W_TURN, target, v);
+        raise_error(c, ST_TIMEOUT, where, target, v);
         return false;
       }
     }
@@ -328,6 +359,7 @@ struct Work {
 //   dense modes, CL 2 / 4: CTA pairs with 256 x 512 tiles (MC pairs share B)
 //   MOE_SCATTER, CL 2: one CTA pair, 256 x 256 tiles
 //   MOE_GATHER: single CTAs only (cp.async row gather)
+//   MOE_STAGED, CL 2: one CTA pair, 256 x 256 tiles
 template <int MODE, int CL>
 struct Unit {
   static constexpr bool DENSE = MODE == MODE_STORE || MODE == MODE_REDUCE;
@@ -337,7 +369,8 @@ struct Unit {
   static constexpr int ROWS = BM * CL;
   using G = Geo<PAIR, NM>;
   static_assert(DENSE || MC == 1, "MoE tiles: no B sharing between pairs");
-  static_assert(MODE != MODE_MOE_GATHER || CL == 1, "MoE layer0: single CTAs");
+  static_assert(MODE != MODE_MOE_GATHER || CL == 1, "MoE layer0 gather: single CTAs");
+  static_assert(MODE != MODE_MOE_STAGED || CL == 2, "MoE layer0 staged: CTA pairs");
 };
 
 // AllGather / plain GEMM: unit -> (rank, m-tile, n-tile).  Ranks are the
@@ -445,7 +478,7 @@ struct ItemIter {
   int u, stride, cta;
 
   __device__ ItemIter(const KParams& p_, int total_mt_, int cta_) : p(p_), total_mt(total_mt_), cta(cta_) {
-    if (MODE == MODE_MOE_GATHER || MODE == MODE_MOE_SCATTER) {
+    if (is_moe(MODE)) {
       num_units = total_mt * p.Nt * p.moe_tp;
     } else {
       num_units = p.num_units;
@@ -522,9 +555,19 @@ __device__ void producer_tma(const KParams& p, const Smem& s, const Ctl& c, int 
   uint32_t stage = 0, phase = 0;
   uint32_t issued = 0;
   uint32_t ready = (p.flags == nullptr) ? 0xFFFFFFFFu : 0u;
+  int staged_mt = -1;  // MOE_STAGED: the last m-unit whose rows were seen staged
   bool ok = true;
   while (ok && iter.next(w)) {
     int nbox_a = w.m0 < w.row_end ? 1 : 0;  // a CTA part wholly past the last row loads no A
+    if (MODE == MODE_MOE_STAGED && nbox_a && w.mt != staged_mt) {
+      // every 32-row block of the unit must be staged (acquire), then be
+      // visible to the TMA reads of this thread
+      const int rows_u = min(BM * CL, w.row_end - (w.m0 - cta * BM));
+      const uint32_t target = static_cast<uint32_t>((rows_u + STAGE_BLK - 1) / STAGE_BLK);
+      if (!wait_count(p.unit_cnt + w.mt, target, c, W_STAGE)) break;
+      fence_proxy_async_global();
+      staged_mt = w.mt;
+    }
     if (MODE == MODE_STORE) {
       // shards covering the valid rows of this CTA's part must be published first
       nbox_a = 0;
@@ -583,7 +626,7 @@ __device__ void producer_tma(const KParams& p, const Smem& s, const Ctl& c, int 
         if (MC == 2 && (j >> 1) != half) continue;  // the partner multicasts this box
         const int n = b_box_col<PAIR>(n0, cta, j);
         const uint32_t dst = sb + j * B_BOX_N * BK * 2;
-        if (MODE == MODE_MOE_SCATTER) {
+        if (MODE == MODE_MOE_SCATTER || MODE == MODE_MOE_STAGED) {
           if (PAIR == 2) tma_load_3d_pair(dst, &p.tmB[w.r], fbc, n, kc, w.e);
           else tma_load_3d(dst, &p.tmB[w.r], fb, n, kc, w.e);
         } else if (PAIR == 2) {
@@ -908,7 +951,7 @@ __device__ void epilogue(const KParams& p, const Smem& s, const Ctl& c, uint32_t
       tok = slot / p.topk;
       gate = __ldg(p.topk_w + slot);
     }
-    if (MODE == MODE_STORE || MODE == MODE_MOE_GATHER) {
+    if (MODE == MODE_STORE || MODE == MODE_MOE_GATHER || MODE == MODE_MOE_STAGED) {
       // 64 columns at a time: two TMEM loads, one row-contiguous store pass
       for (int ch = 0; ch < G::TILE_N / 64; ++ch) {
         if (ch * 64 >= ncols) break;  // warp-uniform
@@ -927,8 +970,9 @@ __device__ void epilogue(const KParams& p, const Smem& s, const Ctl& c, uint32_t
         // of this quarter are in (its adds were fenced before it counted them)
         int ok_turn = 1;
         if (lane == 0)
-          ok_turn = wait_turn(p.counters + (static_cast<size_t>(w.tile) * 4 + q),
-                              static_cast<uint32_t>(w.r) * static_cast<uint32_t>(p.KT), c) ? 1 : 0;
+          ok_turn = wait_count(p.counters + (static_cast<size_t>(w.tile) * 4 + q),
+                               static_cast<uint32_t>(w.r) * static_cast<uint32_t>(p.KT), c,
+                               W_TURN) ? 1 : 0;
         ok_turn = __shfl_sync(0xFFFFFFFFu, ok_turn, 0);
         __syncwarp();  // the lanes' adds are ordered after lane 0's acquire
         if (!ok_turn) break;  // TMEM stays held: the MMA side times out too
@@ -1010,6 +1054,72 @@ __device__ void epilogue(const KParams& p, const Smem& s, const Ctl& c, uint32_t
   }
 }
 
+// MoE layer0, staged: every thread of every CTA takes part.  Blocks of 32
+// grouped rows, in ascending m-unit order, are dealt to the CTAs in turn; a
+// warp copies one row at a time (the token row of the shard that owns it,
+// after that shard's ready flag) into the staging buffer, 16 loads of 16
+// bytes in flight per lane.  When the whole CTA is done with a block, its
+// count goes to the unit's ready counter (release), which the GEMM producers
+// wait for.
+template <int CL>
+__device__ void stage_rows(const KParams& p, const Ctl& c, int total_mt) {
+  constexpr int UROWS = BM * CL;
+  constexpr int BLKS = UROWS / STAGE_BLK;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int nwarps = static_cast<int>(blockDim.x >> 5);
+  const int chunks = p.H / 8;  // 16-byte chunks per row
+  uint32_t ready = (p.flags == nullptr) ? 0xFFFFFFFFu : 0u;
+  const int items = total_mt * BLKS;
+  for (int i = blockIdx.x; i < items; i += gridDim.x) {
+    const int gmt = i / BLKS, b = i - (i / BLKS) * BLKS;
+    int lo = 0, hi = p.E;  // the unit's expert: largest e with tile_off[e] <= gmt
+    while (hi - lo > 1) {
+      const int mid = (lo + hi) >> 1;
+      if (__ldg(p.tile_off + mid) <= gmt) lo = mid; else hi = mid;
+    }
+    const int row_end = __ldg(p.offsets + lo + 1);
+    const int row0 = __ldg(p.offsets + lo) + (gmt - __ldg(p.tile_off + lo)) * UROWS + b * STAGE_BLK;
+    if (row0 >= row_end) continue;  // the same decision in every thread
+    const int nrows = min(STAGE_BLK, row_end - row0);
+    int ok = 1;
+    for (int rr = warp; rr < nrows && ok; rr += nwarps) {
+      const int row = row0 + rr;
+      const int tok = __ldg(p.row_to_slot + row) / p.topk;
+      const int sh = tok / p.rows_per_rank;
+      if (!((ready >> sh) & 1u)) {
+        if (lane == 0) ok = wait_flag(p.flags, sh, p.epoch, c) ? 1 : 0;
+        ok = __shfl_sync(0xFFFFFFFFu, ok, 0);
+        if (!ok) break;
+        ready |= 1u << sh;
+      }
+      const uint4* src = reinterpret_cast<const uint4*>(
+          static_cast<const char*>(p.xsrc[sh]) +
+          static_cast<size_t>(tok - sh * p.rows_per_rank) * p.H * 2);
+      uint4* dst = reinterpret_cast<uint4*>(static_cast<char*>(p.stage) +
+                                            static_cast<size_t>(row) * p.H * 2);
+      for (int c0 = 0; c0 < chunks; c0 += 32 * STAGE_UNROLL) {
+        uint4 v[STAGE_UNROLL];
+#pragma unroll
+        for (int j = 0; j < STAGE_UNROLL; ++j) {
+          const int ch = c0 + j * 32 + lane;
+          if (ch < chunks) v[j] = __ldg(src + ch);
+        }
+#pragma unroll
+        for (int j = 0; j < STAGE_UNROLL; ++j) {
+          const int ch = c0 + j * 32 + lane;
+          if (ch < chunks) dst[ch] = v[j];
+        }
+      }
+    }
+    // the block's rows, written by every thread, become visible (also to the
+    // readers' TMA) before its count
+    __threadfence();
+    fence_proxy_async_global();
+    if (!__syncthreads_and(ok)) return;  // a shard flag timed out (recorded)
+    if (threadIdx.x == 0) atomicAdd(p.unit_cnt + gmt, 1u);
+  }
+}
+
 // ---------------------------------------------------------------- kernel
 template <int MODE, int DT, int CL>
 struct KernelShape {
@@ -1083,7 +1193,8 @@ fused_gemm_kernel(const __grid_constant__ KParams p) {
   const uint32_t tmem_base = *s.tmem_slot;
 
   int total_mt = 0;
-  if (MODE == MODE_MOE_GATHER || MODE == MODE_MOE_SCATTER) total_mt = __ldg(p.tile_off + p.E);
+  if (is_moe(MODE)) total_mt = __ldg(p.tile_off + p.E);
+  if constexpr (MODE == MODE_MOE_STAGED) stage_rows<CL>(p, c, total_mt);
 
   const int lane = threadIdx.x & 31;
   if (warp == 0 && lane < p.R) {

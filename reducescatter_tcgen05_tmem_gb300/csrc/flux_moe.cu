@@ -22,7 +22,11 @@ constexpr int ROUTE_THREADS = 1024;
 //     pairs gathering rows with TMA tile::gather4 (2.7x slower: 32 gather
 //     operations per stage cost the TMA unit far more than one 128-row box).
 //   layer1: CTA pairs with 256 x 256 tiles (half the B bytes per SM).
+//   layer0 staged (the default): every CTA first copies a share of the
+//     grouped rows into the workspace, then CTA pairs with 256 x 256 tiles
+//     load them by TMA (see MODE_MOE_STAGED).
 constexpr int MOE0_CL = 1;
+constexpr int MOE0S_CL = 2;
 constexpr int MOE1_CL = 2;
 constexpr int ROUTE_CHUNK = 4096;  // expert ids staged in shared memory per pass
 constexpr int ROUTE_WARPS = ROUTE_THREADS / 32;
@@ -58,12 +62,14 @@ __device__ int block_exclusive_scan(int v, int* warp_sums, int* total) {
 // One CTA: counts[e], offsets[e] (exclusive prefix sum), the stable
 // permutation slot_to_row / row_to_slot (rows grouped by expert, ascending slot
 // order inside an expert) and, if tile_off != nullptr, the first unit of
-// `unit_rows` rows of each expert in the grouped GEMM.  Ids outside [0, E) are not routed; their
-// slot_to_row entry is -1 and FLUX_ERR_INVALID_ARG is recorded in hdr.
+// `unit_rows` rows of each expert in the grouped GEMM; with unit_cnt !=
+// nullptr the ready counters of those units are zeroed for the staged layer0.
+// Ids outside [0, E) are not routed; their slot_to_row entry is -1 and
+// FLUX_ERR_INVALID_ARG is recorded in hdr.
 __global__ void __launch_bounds__(ROUTE_THREADS, 1)
 moe_route_kernel(const int32_t* __restrict__ ids, int n, int E, int32_t* counts,
                  int32_t* offsets, int32_t* slot_to_row, int32_t* row_to_slot, int32_t* tile_off,
-                 int unit_rows, uint32_t* hdr) {
+                 int unit_rows, uint32_t* unit_cnt, uint32_t* hdr) {
   __shared__ int hist[FLUX_MAX_EXPERTS];
   __shared__ int base[FLUX_MAX_EXPERTS];
   __shared__ int warp_sums[32];
@@ -95,6 +101,8 @@ moe_route_kernel(const int32_t* __restrict__ ids, int n, int E, int32_t* counts,
     offsets[E] = totals[0];
     if (tile_off) tile_off[E] = totals[1];
   }
+  if (unit_cnt)
+    for (int i = tid; i < totals[1]; i += ROUTE_THREADS) unit_cnt[i] = 0u;
   __syncthreads();
   // stable permutation: row(slot) = offsets[e] + number of earlier slots of
   // expert e.  Slots are taken 32 at a time; __match_any_sync ranks the lanes
@@ -291,9 +299,12 @@ bool moe_shape_ok(int R, int T, int H, int F, int E, int topk) {
 
 size_t a256(size_t v) { return round_up(v, WS_ALIGN); }
 
-// workspace layout (offsets from the start)
+// workspace layout (offsets from the start): header, tile table, then the
+// layer1 part (MOE_RS, MOE_LAYERS), then the layer0 part (MOE_AG,
+// MOE_LAYERS), so that the one-call layer finds each part where the single
+// calls put it
 struct MoeWs {
-  size_t tile_off, counts, offsets, s2r, r2s, counters, acc, total;
+  size_t tile_off, counts, offsets, s2r, r2s, counters, acc, unit_cnt, stage, total;
 };
 
 MoeWs moe_layout(flux_op_t op, int R, int T, int H, int F, int E, int topk) {
@@ -304,7 +315,7 @@ MoeWs moe_layout(flux_op_t op, int R, int T, int H, int F, int E, int topk) {
   size_t o = WS_HEADER;
   w.tile_off = o;
   o += a256((E + 1) * sizeof(int32_t));
-  if (op == FLUX_OP_MOE_RS) {
+  if (op == FLUX_OP_MOE_RS || op == FLUX_OP_MOE_LAYERS) {
     // routing recomputed here when the caller passes none
     w.counts = o;
     o += a256(E * sizeof(int32_t));
@@ -320,15 +331,24 @@ MoeWs moe_layout(flux_op_t op, int R, int T, int H, int F, int E, int topk) {
     w.acc = o;
     o += a256(static_cast<size_t>(T) * H * sizeof(float));
   }
+  if (op == FLUX_OP_MOE_AG || op == FLUX_OP_MOE_LAYERS) {
+    // staged layer0: one ready counter per m-unit of BM * MOE0S_CL rows, and
+    // the grouped A rows [T*topk x H] (16-bit)
+    const size_t units = (n + BM * MOE0S_CL - 1) / (BM * MOE0S_CL) + static_cast<size_t>(E);
+    w.unit_cnt = o;
+    o += a256(units * sizeof(uint32_t));
+    w.stage = o;
+    o += a256(n * static_cast<size_t>(H) * 2);
+  }
   w.total = o;
   return w;
 }
 
 flux_status_t launch_route(const int32_t* ids, int n, int E, int32_t* counts, int32_t* offsets,
                            int32_t* s2r, int32_t* r2s, int32_t* tile_off, int unit_rows,
-                           uint32_t* hdr, cudaStream_t s) {
+                           uint32_t* unit_cnt, uint32_t* hdr, cudaStream_t s) {
   moe_route_kernel<<<1, ROUTE_THREADS, 0, s>>>(ids, n, E, counts, offsets, s2r, r2s, tile_off,
-                                               unit_rows, hdr);
+                                               unit_rows, unit_cnt, hdr);
   cudaError_t e = cudaGetLastError();
   return e == cudaSuccess ? FLUX_OK : cuda_fail(e);
 }
@@ -348,9 +368,7 @@ extern "C" size_t flux_moe_workspace_size(flux_op_t op, int R, int T, int H, int
   }
   if (!moe_shape_ok(R, T, H, F, E, topk)) return 0;
   if (op != FLUX_OP_MOE_AG && op != FLUX_OP_MOE_RS && op != FLUX_OP_MOE_LAYERS) return 0;
-  // the one-call layer runs layer0 inside layer1's workspace, whose routing
-  // slots receive layer0's routing
-  return moe_layout(op == FLUX_OP_MOE_LAYERS ? FLUX_OP_MOE_RS : op, R, T, H, F, E, topk).total;
+  return moe_layout(op, R, T, H, F, E, topk).total;
 }
 
 extern "C" flux_status_t flux_moe_topk_gate(int T, int E, int topk, const float* logits,
@@ -394,6 +412,7 @@ extern "C" flux_status_t flux_moe_route(int T, int E, int topk, const int32_t* t
   flux_status_t st = current_device(&dev);
   if (st != FLUX_OK) return st;
   return launch_route(topk_ids, n, E, counts, offsets, slot_to_row, row_to_slot, nullptr, BM,
+                      nullptr,
                       static_cast<uint32_t*>(workspace), static_cast<cudaStream_t>(stream));
 }
 
@@ -404,9 +423,10 @@ namespace {
 // parallel).  Rank r = g tp + t: w1_shards[r] [E/EP x H x F/tp] holds column
 // block t of the experts of group g, and h_out[r] [T*topk x F/tp] receives the
 // rows of those experts (the other rows are left as they were, so ranks of
-// different groups may share one buffer).
+// different groups may share one buffer).  `ws_op` names the layout of the
+// workspace (MOE_AG, or MOE_LAYERS inside the one-call layer).
 flux_status_t moe_layer0_impl(
-    int tp, int R, int T, int H, int F, int E, int topk, flux_dtype_t dtype,
+    flux_op_t ws_op, int tp, int R, int T, int H, int F, int E, int topk, flux_dtype_t dtype,
     const void* const* x_shards, const void* const* w1_shards, const int32_t* topk_ids,
     void* const* h_out, int32_t* counts, int32_t* offsets, int32_t* slot_to_row,
     int32_t* row_to_slot, const uint32_t* ready_flags, void* workspace, size_t workspace_bytes,
@@ -417,9 +437,11 @@ flux_status_t moe_layer0_impl(
       offsets == nullptr || slot_to_row == nullptr || row_to_slot == nullptr ||
       (T > 0 && topk_ids == nullptr))
     return FLUX_ERR_INVALID_ARG;
-  const MoeWs L = moe_layout(FLUX_OP_MOE_AG, R, T, H, F, E, topk);
+  const MoeWs L = moe_layout(ws_op, R, T, H, F, E, topk);
   flux_status_t st = check_workspace(workspace, workspace_bytes, L.total);
   if (st != FLUX_OK) return st;
+  const bool pull = opts != nullptr && opts->moe_pull_gather != 0;
+  const int cl = pull ? MOE0_CL : MOE0S_CL;
   // output columns per rank and experts per rank's weight block
   const int Fr = F / tp, EB = E / (R / tp), rows = T / R, n = T * topk;
   for (int r = 0; r < R; ++r) {
@@ -434,8 +456,9 @@ flux_status_t moe_layer0_impl(
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   uint8_t* ws = static_cast<uint8_t*>(workspace);
   int32_t* tile_off = reinterpret_cast<int32_t*>(ws + L.tile_off);
+  uint32_t* unit_cnt = pull ? nullptr : reinterpret_cast<uint32_t*>(ws + L.unit_cnt);
   if ((st = launch_route(topk_ids, n, E, counts, offsets, slot_to_row, row_to_slot, tile_off,
-                         BM * MOE0_CL, static_cast<uint32_t*>(workspace), s)) != FLUX_OK)
+                         BM * cl, unit_cnt, static_cast<uint32_t*>(workspace), s)) != FLUX_OK)
     return st;
   if (n == 0 || Fr == 0) return FLUX_OK;
   if (H == 0) {
@@ -446,11 +469,19 @@ flux_status_t moe_layer0_impl(
     return FLUX_OK;
   }
   KParams p{};
+  void* stage = ws + L.stage;
+  CUtensorMap tm_stage;
+  if (!pull &&
+      (st = encode_2d(&tm_stage, dtype, stage, H, n, static_cast<uint64_t>(H) * 2, BK, BM)) != FLUX_OK)
+    return st;
   for (int r = 0; r < R; ++r) {
     if ((st = encode_3d(&p.tmB[r], dtype, w1_shards[r], Fr, H, EB, B_BOX_N, BK)) != FLUX_OK) return st;
+    if (!pull) p.tmA[r] = tm_stage;  // every rank reads the one staged copy of the rows
     p.out[r] = h_out[r];
     p.xsrc[r] = x_shards[r];
   }
+  p.stage = stage;
+  p.unit_cnt = unit_cnt;
   p.moe_tp = tp;
   p.moe_el = EB;
   p.R = R;
@@ -475,11 +506,16 @@ flux_status_t moe_layer0_impl(
   p.seq = next_seq();
   p.hdr = static_cast<uint32_t*>(workspace);
   const long long max_units =
-      (static_cast<long long>((n + BM * MOE0_CL - 1) / (BM * MOE0_CL)) + E) * p.Nt *
+      (static_cast<long long>((n + BM * cl - 1) / (BM * cl)) + E) * p.Nt *
       static_cast<long long>(tp);
-  const int grid = grid_dt<MODE_MOE_GATHER, MOE0_CL>(dtype, dev, opts, max_units);
+  if (pull) {
+    const int grid = grid_dt<MODE_MOE_GATHER, MOE0_CL>(dtype, dev, opts, max_units);
+    if (grid == 0) return FLUX_ERR_CUDA;
+    return launch_dt<MODE_MOE_GATHER, MOE0_CL>(dtype, p, grid, s);
+  }
+  const int grid = grid_dt<MODE_MOE_STAGED, MOE0S_CL>(dtype, dev, opts, max_units);
   if (grid == 0) return FLUX_ERR_CUDA;
-  return launch_dt<MODE_MOE_GATHER, MOE0_CL>(dtype, p, grid, s);
+  return launch_dt<MODE_MOE_STAGED, MOE0S_CL>(dtype, p, grid, s);
 }
 
 // Layer1 for an EP x TP split.  Rank r = g tp + t: h_shards[r] [T*topk x F/tp]
@@ -530,7 +566,7 @@ flux_status_t moe_layer1_impl(
     row_to_slot = reinterpret_cast<int32_t*>(ws + L.r2s);
     if ((st = launch_route(topk_ids, n, E, reinterpret_cast<int32_t*>(ws + L.counts),
                            const_cast<int32_t*>(offsets), reinterpret_cast<int32_t*>(ws + L.s2r),
-                           const_cast<int32_t*>(row_to_slot), tile_off, BM * MOE1_CL,
+                           const_cast<int32_t*>(row_to_slot), tile_off, BM * MOE1_CL, nullptr,
                            static_cast<uint32_t*>(workspace), s)) != FLUX_OK)
       return st;
   } else {
@@ -587,7 +623,8 @@ extern "C" flux_status_t flux_moe_ag_grouped_gemm(
     const void* const* w1_shards, const int32_t* topk_ids, void* const* h_out, int32_t* counts,
     int32_t* offsets, int32_t* slot_to_row, int32_t* row_to_slot, const uint32_t* ready_flags,
     void* workspace, size_t workspace_bytes, const flux_opts_t* opts, void* stream) {
-  return moe_layer0_impl(R, R, T, H, F, E, topk, dtype, x_shards, w1_shards, topk_ids, h_out,
+  return moe_layer0_impl(FLUX_OP_MOE_AG, R, R, T, H, F, E, topk, dtype, x_shards, w1_shards,
+                         topk_ids, h_out,
                          counts, offsets, slot_to_row, row_to_slot, ready_flags, workspace,
                          workspace_bytes, opts, stream);
 }
@@ -609,7 +646,8 @@ extern "C" flux_status_t flux_moe_ep_dispatch_gemm(
     void* const* h_out, int32_t* counts, int32_t* offsets, int32_t* slot_to_row,
     int32_t* row_to_slot, const uint32_t* ready_flags, void* workspace, size_t workspace_bytes,
     const flux_opts_t* opts, void* stream) {
-  return moe_layer0_impl(tp, R, T, H, F, E, topk, dtype, x_shards, w1_shards, topk_ids, h_out,
+  return moe_layer0_impl(FLUX_OP_MOE_AG, tp, R, T, H, F, E, topk, dtype, x_shards, w1_shards,
+                         topk_ids, h_out,
                          counts, offsets, slot_to_row, row_to_slot, ready_flags, workspace,
                          workspace_bytes, opts, stream);
 }
@@ -634,7 +672,7 @@ extern "C" flux_status_t flux_moe_layers(int R, int T, int H, int F, int E, int 
                                          void* workspace, size_t workspace_bytes,
                                          const flux_opts_t* opts, void* stream) {
   if (!moe_shape_ok(R, T, H, F, E, topk) || h == nullptr) return FLUX_ERR_INVALID_ARG;
-  const MoeWs L = moe_layout(FLUX_OP_MOE_RS, R, T, H, F, E, topk);
+  const MoeWs L = moe_layout(FLUX_OP_MOE_LAYERS, R, T, H, F, E, topk);
   flux_status_t st = check_workspace(workspace, workspace_bytes, L.total);
   if (st != FLUX_OK) return st;
   uint8_t* ws = static_cast<uint8_t*>(workspace);
@@ -642,10 +680,10 @@ extern "C" flux_status_t flux_moe_layers(int R, int T, int H, int F, int E, int 
   int32_t* offsets = reinterpret_cast<int32_t*>(ws + L.offsets);
   int32_t* s2r = reinterpret_cast<int32_t*>(ws + L.s2r);
   int32_t* r2s = reinterpret_cast<int32_t*>(ws + L.r2s);
-  // layer0 uses the head of the same workspace (status header + its tile table)
-  if ((st = flux_moe_ag_grouped_gemm(R, T, H, F, E, topk, dtype, x_shards, w1_shards, topk_ids, h,
-                                     counts, offsets, s2r, r2s, ready_flags, workspace,
-                                     workspace_bytes, opts, stream)) != FLUX_OK)
+  // layer0 writes its routing into layer1's part of the workspace
+  if ((st = moe_layer0_impl(FLUX_OP_MOE_LAYERS, R, R, T, H, F, E, topk, dtype, x_shards,
+                            w1_shards, topk_ids, h, counts, offsets, s2r, r2s, ready_flags,
+                            workspace, workspace_bytes, opts, stream)) != FLUX_OK)
     return st;
   return flux_moe_grouped_gemm_rs(R, T, H, F, E, topk, dtype, reinterpret_cast<const void* const*>(h),
                                   w2_shards, topk_ids, topk_weights, offsets, s2r, r2s, out,

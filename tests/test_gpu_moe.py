@@ -136,21 +136,50 @@ def _layer0(c, d=None, flags=None, opts=None):
     return d, H, routing
 
 
+@pytest.mark.parametrize("pull", [False, True], ids=["staged", "pull"])
 @pytest.mark.parametrize("R,T,H,F,E,topk,dtype,empty", [
     (2, 256, 256, 640, 4, 2, "bf16", ()),      # F/R = 320: ragged n tail
     (4, 512, 192, 1024, 8, 2, "f16", (5,)),    # H = 192: ragged k tail; an empty expert
     (8, 1024, 512, 2048, 8, 2, "bf16", ()),    # the MoE workload's structure, reduced
     (1, 64, 64, 256, 3, 1, "f16", ()),
+    (2, 200, 136, 256, 5, 3, "bf16", ()),      # H = 136: a 16-byte row tail in the staging copy
 ])
-def test_layer0_matches_oracle(R, T, H, F, E, topk, dtype, empty):
+def test_layer0_matches_oracle(R, T, H, F, E, topk, dtype, empty, pull):
+    # staged: every CTA first copies a share of the grouped rows, then CTA pairs
+    # compute; pull: the GEMM producer gathers the rows of each tile itself
     c = configs.small(configs.CONFIGS["moe"], R=R, T=T, H=H, F=F, E=E, topk=topk, dtype=dtype,
                       seed=60 + R, force_empty=empty)
-    d, Hd, routing = _layer0(c)
+    d, Hd, routing = _layer0(c, opts={"moe_pull_gather": 1} if pull else None)
     ref, want_routing = oracle.moe_layer0(d["x_shards"], d["w1_shards"], d["topk_ids"], E, dtype)
     for g, w in zip(routing, want_routing):
         assert np.array_equal(g.cpu().numpy(), w)
     for r in range(R):
         check_close(oracle.widen(from_device(Hd[r]), dtype), ref[r], f"layer0 rank {r}")
+
+
+def test_layer0_staged_withheld_flag_times_out_and_gpu_stays_usable():
+    # token shard 1 never publishes: the staging copy of its rows gives up after
+    # the timeout, the GEMM tiles waiting for those rows leave too
+    c = configs.small(configs.CONFIGS["moe"], R=4, T=512, H=256, F=1024, E=8, topk=2, seed=66)
+    flags = torch.tensor([1, 0, 1, 1], dtype=torch.int32, device="cuda")
+    d = configs.moe_inputs(c)
+    n = c.T * c.topk
+    X = [to_device(x, c.dtype) for x in d["x_shards"]]
+    W1 = [to_device(w, c.dtype) for w in d["w1_shards"]]
+    ids = torch.from_numpy(d["topk_ids"]).cuda()
+    H = [torch.empty(n, c.F // c.R, dtype=torch_dtype(c.dtype), device="cuda") for _ in range(c.R)]
+    counts, offsets, s2r, r2s = _i32(c.E), _i32(c.E + 1), _i32(n), _i32(n)
+    ws = _ws(fx.flux_moe_workspace_size(fx.FLUX_OP_MOE_AG, c.R, c.T, c.H, c.F, c.E, c.topk))
+    fx.flux_moe_ag_grouped_gemm(c.R, c.T, c.H, c.F, c.E, c.topk, DT[c.dtype], X, W1, ids, H, counts,
+                                offsets, s2r, r2s, flags, ws, opts={"timeout_ns": 20_000_000})
+    st, rep = fx.flux_get_status(ws)
+    assert st == fx.FLUX_ERR_TIMEOUT
+    assert rep["where"] in ("ready flag", "staged rows"), rep
+    # the same workspace (reset by flux_get_status) and GPU work normally afterwards
+    flags.fill_(1)
+    d2, Hd, _ = _layer0(c, d=d, flags=flags)
+    ref, _ = oracle.moe_layer0(d["x_shards"], d["w1_shards"], d["topk_ids"], c.E, c.dtype)
+    check_close(oracle.widen(from_device(Hd[1]), c.dtype), ref[1], "after timeout")
 
 
 # ---------------------------------------------------------------- layer1
