@@ -58,7 +58,8 @@ class flux_opts_t(ctypes.Structure):
     _fields_ = [("epoch", ctypes.c_uint32), ("reserved0", ctypes.c_uint32),
                 ("timeout_ns", ctypes.c_uint64), ("num_ctas", ctypes.c_int32),
                 ("group_n", ctypes.c_int32), ("tiles_per_group", ctypes.c_int32),
-                ("deterministic_rs", ctypes.c_int32), ("moe_pull_gather", ctypes.c_int32)]
+                ("deterministic_rs", ctypes.c_int32), ("moe_pull_gather", ctypes.c_int32),
+                ("moe_stage_ctas", ctypes.c_int32)]
 
 
 class flux_device_report_t(ctypes.Structure):

@@ -196,9 +196,11 @@ struct KParams {
   const float* topk_w;         // [T*topk]
   void* stage;                 // MOE_STAGED: grouped A rows [T*topk x H], 16-bit
   uint32_t* unit_cnt;          // MOE_STAGED: finished staging blocks per m-unit (zeroed by routing)
+  int stage_ctas;              // MOE_STAGED: CTAs that copy rows before computing (0 = all)
   int E, topk, T, H;
   int moe_tp;  // MoE: ranks per expert group (R: tensor parallel, 1: expert parallel)
   int moe_el;  // MoE: experts per group; rank g moe_tp + t holds block t of group g's experts
+  int moe_order;  // MoE: unit order (see decode_moe)
 };
 
 struct Ctl {
@@ -438,13 +440,38 @@ __device__ __forceinline__ Work decode_reduce(const KParams& p, int u, int cta) 
 // An m-unit of expert e runs on the moe_tp ranks of e's group g = e / moe_el
 // (ranks g moe_tp + [0, moe_tp)), each with its block of the expert's weight
 // (local expert e % moe_el).  Tensor parallel: one group of R ranks; expert
-// parallel: R groups of one rank.
+// parallel: R groups of one rank.  Unit order (moe_order):
+//   0  rank outermost, then bands of group_n n-tiles with the m-tile fastest
+//   1  rank innermost: the ranks' tiles of one (m, n) are consecutive units
+//   2  band outermost, then rank, then the m-tile fastest inside the band
 template <int CL>
 __device__ __forceinline__ Work decode_moe(const KParams& p, int u, int total_mt, int cta) {
   Work w;
   const int per_rank = total_mt * p.Nt;
-  const int tr = u / per_rank;  // rank inside the expert's group
-  int t = u - tr * per_rank;
+  int tr, t;  // rank inside the expert's group; the unit's index among that rank's
+  if (p.moe_order == 1) {
+    tr = u % p.moe_tp;
+    t = u / p.moe_tp;
+  } else if (p.moe_order == 2) {
+    const int gn = p.group_n;
+    const int full = p.Nt / gn;              // full bands
+    const int band = total_mt * gn;          // one rank's units in a full band
+    const int done = full * band * p.moe_tp;
+    if (u < done) {
+      const int g = u / (band * p.moe_tp);
+      const int rem = u - g * band * p.moe_tp;
+      tr = rem / band;
+      t = g * band + (rem - tr * band);
+    } else {
+      const int tail = total_mt * (p.Nt - full * gn);
+      const int rem = u - done;
+      tr = rem / tail;
+      t = full * band + (rem - tr * tail);
+    }
+  } else {
+    tr = u / per_rank;
+    t = u - tr * per_rank;
+  }
   int gmt, nt;
   // m-tile fastest inside bands of group_n n-tiles
   raster(t, total_mt, p.Nt, p.group_n, gmt, nt);
@@ -1054,8 +1081,9 @@ __device__ void epilogue(const KParams& p, const Smem& s, const Ctl& c, uint32_t
   }
 }
 
-// MoE layer0, staged: every thread of every CTA takes part.  Blocks of 32
-// grouped rows, in ascending m-unit order, are dealt to the CTAs in turn; a
+// MoE layer0, staged: every thread of the first stage_ctas CTAs (all CTAs
+// by default) takes part.  Blocks of 32 grouped rows, in ascending m-unit
+// order, are dealt to those CTAs in turn; a
 // warp copies one row at a time (the token row of the shard that owns it,
 // after that shard's ready flag) into the staging buffer, 16 loads of 16
 // bytes in flight per lane.  When the whole CTA is done with a block, its
@@ -1070,7 +1098,10 @@ __device__ void stage_rows(const KParams& p, const Ctl& c, int total_mt) {
   const int chunks = p.H / 8;  // 16-byte chunks per row
   uint32_t ready = (p.flags == nullptr) ? 0xFFFFFFFFu : 0u;
   const int items = total_mt * BLKS;
-  for (int i = blockIdx.x; i < items; i += gridDim.x) {
+  const int copiers = p.stage_ctas > 0 ? min(p.stage_ctas, static_cast<int>(gridDim.x))
+                                       : static_cast<int>(gridDim.x);
+  if (static_cast<int>(blockIdx.x) >= copiers) return;
+  for (int i = blockIdx.x; i < items; i += copiers) {
     const int gmt = i / BLKS, b = i - (i / BLKS) * BLKS;
     int lo = 0, hi = p.E;  // the unit's expert: largest e with tile_off[e] <= gmt
     while (hi - lo > 1) {

@@ -482,8 +482,10 @@ flux_status_t moe_layer0_impl(
   }
   p.stage = stage;
   p.unit_cnt = unit_cnt;
+  p.stage_ctas = (opts && opts->moe_stage_ctas > 0) ? opts->moe_stage_ctas : 0;
   p.moe_tp = tp;
   p.moe_el = EB;
+  p.moe_order = 1;  // rank innermost: the ranks of one m-tile reuse its A rows in L2
   p.R = R;
   p.M = n;
   p.N = Fr;
@@ -584,6 +586,7 @@ flux_status_t moe_layer1_impl(
   }
   p.moe_tp = tp;
   p.moe_el = EB;
+  p.moe_order = 0;  // rank outermost: concurrent tiles add into different token rows
   p.R = R;
   p.M = n;
   p.N = H;

@@ -157,6 +157,16 @@ def test_layer0_matches_oracle(R, T, H, F, E, topk, dtype, empty, pull):
         check_close(oracle.widen(from_device(Hd[r]), dtype), ref[r], f"layer0 rank {r}")
 
 
+@pytest.mark.parametrize("stage_ctas", [1, 3, 1000])
+def test_layer0_staging_split_matches_oracle(stage_ctas):
+    # only the first stage_ctas CTAs copy rows; the others compute from the start
+    c = configs.small(configs.CONFIGS["moe"], R=4, T=512, H=320, F=1024, E=8, topk=2, seed=67)
+    d, Hd, _ = _layer0(c, opts={"moe_stage_ctas": stage_ctas})
+    ref, _ = oracle.moe_layer0(d["x_shards"], d["w1_shards"], d["topk_ids"], c.E, c.dtype)
+    for r in range(c.R):
+        check_close(oracle.widen(from_device(Hd[r]), c.dtype), ref[r], f"layer0 rank {r}")
+
+
 def test_layer0_staged_withheld_flag_times_out_and_gpu_stays_usable():
     # token shard 1 never publishes: the staging copy of its rows gives up after
     # the timeout, the GEMM tiles waiting for those rows leave too
