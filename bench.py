@@ -41,12 +41,17 @@ WORKLOAD = ("hot-path step, R=8 virtual ranks: dense TP-MLP AG-GEMM 4096x12288x4
             "MoE layer T=4096 H=4096 F=14336 E=8: top-2 gate on router scores + routing + "
             "layer0 + layer1 (bf16)")
 DTYPE = "f16/bf16 operands, fp32 accumulate"
-KERNEL_SOURCES = ["flux_kernels.cuh", "flux_ptx.cuh", "flux_dense.cu", "flux_moe.cu"]
+# the sources that decide what each op's kernel does (device code + the host
+# code that fills its parameters); a traffic figure is valid for one hash
+KERNEL_SOURCES = {
+    "dense": ["flux_kernels.cuh", "flux_ptx.cuh", "flux_dense.cu"],
+    "moe": ["flux_kernels.cuh", "flux_ptx.cuh", "flux_moe.cu"],
+}
 
 
-def kernel_hash() -> str:
+def kernel_hash(op: str = "gemm_rs") -> str:
     h = hashlib.sha256()
-    for f in KERNEL_SOURCES:
+    for f in KERNEL_SOURCES["moe" if op.startswith("moe") else "dense"]:
         with open(os.path.join(ROOT, "reducescatter_tcgen05_tmem_gb300", "csrc", f), "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()[:16]
@@ -421,7 +426,7 @@ def load_traffic(kernel):
     except Exception:
         return None
     ent = d.get(kernel)
-    if not ent or ent.get("kernel_hash") != kernel_hash():
+    if not ent or ent.get("kernel_hash") != kernel_hash(kernel):
         return None
     return ent.get("dram_bytes_per_launch")
 

@@ -124,13 +124,19 @@ __device__ __forceinline__ int b_box_col(int n0, int cta, int j) {
 
 // Boxes (bit j) that start inside the N columns; the others are not loaded
 // (their shared-memory slots keep stale data that only feeds columns >= N,
-// which are never stored).
+// which are never stored).  In a CTA pair a CTA with no column of the tile
+// still loads box 0 (from the tile's first column; the results are never
+// stored): the pair's MMAs wait only for the bytes its "full" barrier
+// expects, so a CTA that loaded nothing into a stage (no rows of the unit
+// either) could be lapped by two rounds of that stage and then wait for a
+// phase of its "empty" barrier that parity cannot tell apart.
 template <int PAIR, int NBOX>
 __device__ __forceinline__ uint32_t b_box_mask(int N, int n0, int cta) {
   uint32_t m = 0;
 #pragma unroll
   for (int j = 0; j < NBOX; ++j)
     if (b_box_col<PAIR>(n0, cta, j) < N) m |= 1u << j;
+  if (PAIR == 2 && m == 0) m = 1u;
   return m;
 }
 
@@ -651,7 +657,8 @@ __device__ void producer_tma(const KParams& p, const Smem& s, const Ctl& c, int 
       for (int j = 0; j < G::B_BOXES; ++j) {
         if (!((bmask >> j) & 1u)) continue;
         if (MC == 2 && (j >> 1) != half) continue;  // the partner multicasts this box
-        const int n = b_box_col<PAIR>(n0, cta, j);
+        const int nc = b_box_col<PAIR>(n0, cta, j);
+        const int n = nc < p.N ? nc : n0;  // the padding box of a CTA without columns
         const uint32_t dst = sb + j * B_BOX_N * BK * 2;
         if (MODE == MODE_MOE_SCATTER || MODE == MODE_MOE_STAGED) {
           if (PAIR == 2) tma_load_3d_pair(dst, &p.tmB[w.r], fbc, n, kc, w.e);

@@ -157,6 +157,26 @@ def test_layer0_matches_oracle(R, T, H, F, E, topk, dtype, empty, pull):
         check_close(oracle.widen(from_device(Hd[r]), dtype), ref[r], f"layer0 rank {r}")
 
 
+@pytest.mark.parametrize("layer", [0, 1])
+def test_pairs_with_an_idle_cta_match_oracle(layer):
+    # units whose odd CTA holds no rows, in a last n-tile of 128 columns (none
+    # for the odd CTA): that CTA loads nothing of its own into those stages
+    if layer == 0:
+        c = configs.small(configs.CONFIGS["moe"], R=8, T=2048, H=512, F=8 * 896, E=8, topk=2, seed=68)
+        d, Hd, _ = _layer0(c)
+        ref, _ = oracle.moe_layer0(d["x_shards"], d["w1_shards"], d["topk_ids"], c.E, c.dtype)
+        for r in range(c.R):
+            check_close(oracle.widen(from_device(Hd[r]), c.dtype), ref[r], f"layer0 rank {r}")
+    else:
+        c = configs.small(configs.CONFIGS["moe"], R=8, T=2048, H=384, F=8 * 512, E=8, topk=2, seed=69)
+        d = configs.moe_inputs(c)
+        out, _ = _layer1(c, d)
+        ref = oracle.moe_layer1(d["h_shards"], d["w2_shards"], d["topk_ids"], d["topk_weights"], c.E,
+                                c.dtype)
+        for o in range(c.R):
+            check_close(oracle.widen(from_device(out[o]), c.dtype), ref[o], f"layer1 owner {o}")
+
+
 @pytest.mark.parametrize("stage_ctas", [1, 3, 1000])
 def test_layer0_staging_split_matches_oracle(stage_ctas):
     # only the first stage_ctas CTAs copy rows; the others compute from the start
