@@ -107,7 +107,7 @@ typedef struct {
                                A tile's token rows themselves (single CTAs, 128 x 256
                                tiles); 0 (default) = every CTA first stages a share of
                                the grouped rows in the workspace and CTA pairs compute
-                               256 x 256 tiles once their rows' ready counts are in */
+                               256 x 512 tiles once their rows' ready counts are in */
   int32_t moe_stage_ctas;   /* MoE layer0 staged: how many CTAs copy rows before they
                                compute (0 = all; fewer = a communication / computation
                                split of the grid, the others compute from the start) */

@@ -50,7 +50,7 @@
 //     completion can only be signalled in the issuing CTA, so single CTAs.
 //   MOE_STAGED, CL = 2: every CTA first copies a share of the grouped A rows
 //     into a staging buffer and counts each finished 32-row block on its
-//     m-unit's ready counter; then CTA pairs compute 256 x 256 tiles whose
+//     m-unit's ready counter; then CTA pairs compute 256 x 512 tiles whose
 //     producers wait for their unit's count and load A by TMA.
 //
 // The template parameter CL is the number of CTAs of a cluster (1, 2 or 4);
@@ -367,12 +367,12 @@ struct Work {
 //   dense modes, CL 2 / 4: CTA pairs with 256 x 512 tiles (MC pairs share B)
 //   MOE_SCATTER, CL 2: one CTA pair, 256 x 256 tiles
 //   MOE_GATHER: single CTAs only (cp.async row gather)
-//   MOE_STAGED, CL 2: one CTA pair, 256 x 256 tiles
+//   MOE_STAGED, CL 2: one CTA pair, 256 x 512 tiles
 template <int MODE, int CL>
 struct Unit {
   static constexpr bool DENSE = MODE == MODE_STORE || MODE == MODE_REDUCE;
   static constexpr int PAIR = CL >= 2 ? 2 : 1;
-  static constexpr int NM = (DENSE && PAIR == 2) ? 2 : 1;
+  static constexpr int NM = ((DENSE || MODE == MODE_MOE_STAGED) && PAIR == 2) ? 2 : 1;
   static constexpr int MC = CL / PAIR;
   static constexpr int ROWS = BM * CL;
   using G = Geo<PAIR, NM>;
@@ -811,6 +811,9 @@ __device__ void mma_issuer(const KParams& p, const Smem& s, const Ctl& c, uint32
       break;
     tc_fence_after();
     const uint32_t d = tmem_base + b * G::ACC_COLS;
+    // 256-column halves of the tile that start below N (a half wholly past N
+    // has nothing to compute; its accumulator columns are never stored)
+    const int n_live = (G::N_MMA > 1 && w.nt * G::TILE_N + BN >= p.N) ? 1 : G::N_MMA;
     for (int k = w.k0; k < w.k1; ++k) {
       if (wait_bar(smem_u32(&s.full[stage]), phase, c, W_FULL, stage) != 0) { ok = false; break; }
       tc_fence_after();
@@ -823,6 +826,7 @@ __device__ void mma_issuer(const KParams& p, const Smem& s, const Ctl& c, uint32
         const uint32_t acc = (k > w.k0 || kk > 0) ? 1u : 0u;
 #pragma unroll
         for (int h = 0; h < G::N_MMA; ++h) {
+          if (h >= n_live) break;
           // B: N-major; 64-column (128 B) panels BK*128 B apart, 8-k-row groups
           // 1024 B apart; a 16-deep k step is 16 rows = +2048 B.  MMA h of a
           // pair reads panels 2h, 2h+1 and writes TMEM columns 256h ..
