@@ -253,6 +253,31 @@ class Step:
                                         fx.FLUX_BF16, self.eH, self.eW2, self.ids, self.gw,
                                         self.offsets, self.s2r, self.r2s, self.mY, self.ws_e1)
 
+    def tune(self):
+        """Record per-problem launch options for this step's ops (flux_tune_*);
+        the step's calls pass no options, so they use the recorded ones."""
+        fx, ag, rs, dec, moe = self.fx, self.ag, self.rs, self.dec, self.moe
+        keep = lambda o: {k: v for k, v in o.items() if v}  # noqa: E731
+        chosen = {}
+        if "ag_gemm" in self.ops:
+            chosen["ag_gemm"] = keep(fx.flux_tune_ag_gemm(ag.R, ag.M, ag.N, ag.K, fx.FLUX_F16, self.X,
+                                                          self.W1, self.out1, self.flags, self.ws_ag))
+        if "gemm_rs" in self.ops:
+            chosen["gemm_rs"] = keep(fx.flux_tune_gemm_rs(rs.R, rs.M, rs.N, rs.K, fx.FLUX_F16, self.out1,
+                                                          self.W2, self.out2, self.ws_rs))
+        if "decode_rs" in self.ops:
+            chosen["decode_rs"] = keep(fx.flux_tune_gemm_rs(dec.R, dec.M, dec.N, dec.K, fx.FLUX_BF16,
+                                                            self.dA, self.dW, self.dout, self.ws_dec))
+        if "moe_layer0" in self.ops or "moe_layer1" in self.ops:
+            chosen["moe_layer0"] = keep(fx.flux_tune_moe_layer0(
+                moe.R, moe.R, moe.T, moe.H, moe.F, moe.E, moe.topk, fx.FLUX_BF16, self.mX, self.mW1,
+                self.ids, self.mH, self.counts, self.offsets, self.s2r, self.r2s, self.mflags, self.ws_m0))
+        if "moe_layer1" in self.ops:
+            chosen["moe_layer1"] = keep(fx.flux_tune_moe_layer1(
+                moe.R, moe.R, moe.T, moe.H, moe.F, moe.E, moe.topk, fx.FLUX_BF16, self.mH, self.mW2,
+                self.ids, self.gw, self.offsets, self.s2r, self.r2s, self.mY, self.ws_m1))
+        return chosen
+
     def step(self, events=None):
         for name in self.ops:
             if events is not None:
@@ -313,6 +338,7 @@ def run_ours(args):
     import reducescatter_tcgen05_tmem_gb300 as fx
 
     st = Step(torch, fx, dev, small=args.small, ops=args.ops.split(",") if args.ops else None)
+    tuned = st.tune() if args.tune else None
     for _ in range(args.warmup):
         st.step()
     torch.cuda.synchronize()
@@ -400,7 +426,10 @@ def run_ours(args):
         "config": {"workload": WORKLOAD + (" [reduced sizes]" if args.small else ""),
                    "parallelism": f"R=8 virtual TP ranks per GPU; replicas x{ws_}",
                    "l2": "inputs larger than L2 (weights 0.47-1.2 GB per op stream from HBM every step)",
-                   "step_tflop": round(flops / 1e12, 3)},
+                   "step_tflop": round(flops / 1e12, 3),
+                   "launch_options": ("tuned on this GPU before warm-up (flux_tune_*): "
+                                      + json.dumps(tuned, sort_keys=True)) if tuned is not None
+                   else "library defaults"},
         "roofline": roofline,
         "breakdown": breakdown,
         "overhead_vs_plain_gemm": overhead,
@@ -606,6 +635,8 @@ def main():
     ap.add_argument("--small", action="store_true", help="reduced sizes (profiling captures)")
     ap.add_argument("--ops", default="", help="comma list of ops to run (default: the whole step)")
     ap.add_argument("--no-overhead", action="store_true")
+    ap.add_argument("--tune", action="store_true",
+                    help="record per-problem launch options (flux_tune_*) before the warm-up")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-rows", type=int, default=512)
     ap.add_argument("--cpu-cols", type=int, default=8192)

@@ -380,6 +380,56 @@ flux_status_t flux_moe_ep_gemm_combine(int R, int tp, int T, int H, int F, int E
                                        void* const* out, void* workspace, size_t workspace_bytes,
                                        const flux_opts_t* opts, void* stream);
 
+/* ---------------------------------------------------------------- tuning
+ *
+ * Per-problem launch options chosen by measurement (FLUX paper review,
+ * "关键优化": the fused kernel's tile is searched per problem; COMET article,
+ * "动态负载平衡": precompiled variants picked at run time by token count and
+ * parallel layout).  Each flux_tune_* call runs its op on the given buffers
+ * with every candidate option set (one warm-up and five timed calls each, on
+ * `stream`, synchronising it), records the fastest for that problem -- this
+ * device, the op, the dtype and the sizes -- in a process-wide table, and
+ * copies it to *best (may be NULL).  Afterwards a call of the same op and
+ * problem with opts == NULL uses the recorded options; passing opts overrides
+ * the table.  The outputs hold the result of the last candidate run; a
+ * candidate that fails (argument, launch or device-side error) ends the call
+ * with that status and records nothing.  Arguments as in the op itself.
+ * Candidates:
+ *   AllGather + GEMM          group_n in {2, 4, 8, 16}
+ *   GEMM + ReduceScatter      group_n in {4, 8, 16} x tiles_per_group in {0, 2};
+ *                             the stream-K (decode) form: num_ctas in
+ *                             {0, SMs, 7/8 SMs, SMs / 2}
+ *   MoE layer0 (any tp)       staged with group_n 8 or 16, or moe_pull_gather
+ *   MoE layer1 (any tp)       group_n in {4, 8, 16}
+ * flux_moe_ag_grouped_gemm / flux_moe_grouped_gemm_rs are the tp = R
+ * problems of the two MoE tuners. */
+flux_status_t flux_tune_ag_gemm(int R, int M, int N, int K, flux_dtype_t dtype,
+                                const void* const* x_shards, const void* const* w_shards,
+                                void* const* out, const uint32_t* ready_flags, void* workspace,
+                                size_t workspace_bytes, void* stream, flux_opts_t* best);
+flux_status_t flux_tune_gemm_rs(int R, int M, int N, int K, flux_dtype_t dtype,
+                                const void* const* a_shards, const void* const* b_shards,
+                                void* const* out, void* workspace, size_t workspace_bytes,
+                                void* stream, flux_opts_t* best);
+flux_status_t flux_tune_moe_layer0(int R, int tp, int T, int H, int F, int E, int topk,
+                                   flux_dtype_t dtype, const void* const* x_shards,
+                                   const void* const* w1_shards, const int32_t* topk_ids,
+                                   void* const* h_out, int32_t* counts, int32_t* offsets,
+                                   int32_t* slot_to_row, int32_t* row_to_slot,
+                                   const uint32_t* ready_flags, void* workspace,
+                                   size_t workspace_bytes, void* stream, flux_opts_t* best);
+flux_status_t flux_tune_moe_layer1(int R, int tp, int T, int H, int F, int E, int topk,
+                                   flux_dtype_t dtype, const void* const* h_shards,
+                                   const void* const* w2_shards, const int32_t* topk_ids,
+                                   const float* topk_weights, const int32_t* offsets,
+                                   const int32_t* slot_to_row, const int32_t* row_to_slot,
+                                   void* const* out, void* workspace, size_t workspace_bytes,
+                                   void* stream, flux_opts_t* best);
+
+/* Forget every recorded problem / how many are recorded. */
+void flux_tune_clear(void);
+int flux_tune_count(void);
+
 #ifdef __cplusplus
 }
 #endif

@@ -104,6 +104,14 @@ _SIGS = {
     "flux_mlp_ag_rs": ([_i, _i, _i, _i, _i, _vpp, _vpp, _vpp, _vpp, _vpp, _vp, _vp, _sz, _opt, _vp], _i),
     "flux_moe_layers": ([_i, _i, _i, _i, _i, _i, _i, _vpp, _vpp, _vpp, _vp, _vp, _vpp, _vpp, _vp,
                          _vp, _sz, _opt, _vp], _i),
+    "flux_tune_ag_gemm": ([_i, _i, _i, _i, _i, _vpp, _vpp, _vpp, _vp, _vp, _sz, _vp, _opt], _i),
+    "flux_tune_gemm_rs": ([_i, _i, _i, _i, _i, _vpp, _vpp, _vpp, _vp, _sz, _vp, _opt], _i),
+    "flux_tune_moe_layer0": ([_i, _i, _i, _i, _i, _i, _i, _i, _vpp, _vpp, _vp, _vpp, _vp, _vp,
+                              _vp, _vp, _vp, _vp, _sz, _vp, _opt], _i),
+    "flux_tune_moe_layer1": ([_i, _i, _i, _i, _i, _i, _i, _i, _vpp, _vpp, _vp, _vp, _vp, _vp,
+                              _vp, _vpp, _vp, _sz, _vp, _opt], _i),
+    "flux_tune_clear": ([], None),
+    "flux_tune_count": ([], _i),
     "flux_moe_ep_dispatch_gemm": ([_i, _i, _i, _i, _i, _i, _i, _i, _vpp, _vpp, _vp, _vpp, _vp,
                                    _vp, _vp, _vp, _vp, _vp, _sz, _opt, _vp], _i),
     "flux_moe_ep_gemm_combine": ([_i, _i, _i, _i, _i, _i, _i, _i, _vpp, _vpp, _vp, _vp, _vp,
@@ -304,3 +312,59 @@ def flux_moe_ep_gemm_combine(R, tp, T, H, F, E, topk, dtype, h_shards, w2_shards
         _ptr(topk_weights), _ptr(offsets), _ptr(slot_to_row), _ptr(row_to_slot), _ptrs(out),
         _ptr(workspace), _nbytes(workspace), _opts(opts), _stream(stream)),
         "flux_moe_ep_gemm_combine")
+
+
+def _tuned(st, what, best):
+    _check(st, what)
+    return {f: getattr(best, f) for f, _ in flux_opts_t._fields_}
+
+
+def flux_tune_ag_gemm(R, M, N, K, dtype, x_shards, w_shards, out, ready_flags, workspace,
+                      stream=None) -> dict:
+    """Time the AllGather + GEMM candidates; record and return the fastest options."""
+    best = flux_opts_t()
+    return _tuned(_lib.flux_tune_ag_gemm(R, M, N, K, dtype, _ptrs(x_shards), _ptrs(w_shards),
+                                         _ptrs(out), _ptr(ready_flags), _ptr(workspace),
+                                         _nbytes(workspace), _stream(stream), ctypes.byref(best)),
+                  "flux_tune_ag_gemm", best)
+
+
+def flux_tune_gemm_rs(R, M, N, K, dtype, a_shards, b_shards, out, workspace, stream=None) -> dict:
+    """Time the GEMM + ReduceScatter candidates; record and return the fastest options."""
+    best = flux_opts_t()
+    return _tuned(_lib.flux_tune_gemm_rs(R, M, N, K, dtype, _ptrs(a_shards), _ptrs(b_shards),
+                                         _ptrs(out), _ptr(workspace), _nbytes(workspace),
+                                         _stream(stream), ctypes.byref(best)),
+                  "flux_tune_gemm_rs", best)
+
+
+def flux_tune_moe_layer0(R, tp, T, H, F, E, topk, dtype, x_shards, w1_shards, topk_ids, h_out,
+                         counts, offsets, slot_to_row, row_to_slot, ready_flags, workspace,
+                         stream=None) -> dict:
+    """Time the MoE layer0 candidates (staged / pull); record and return the fastest."""
+    best = flux_opts_t()
+    return _tuned(_lib.flux_tune_moe_layer0(
+        R, tp, T, H, F, E, topk, dtype, _ptrs(x_shards), _ptrs(w1_shards), _ptr(topk_ids),
+        _ptrs(h_out), _ptr(counts), _ptr(offsets), _ptr(slot_to_row), _ptr(row_to_slot),
+        _ptr(ready_flags), _ptr(workspace), _nbytes(workspace), _stream(stream),
+        ctypes.byref(best)), "flux_tune_moe_layer0", best)
+
+
+def flux_tune_moe_layer1(R, tp, T, H, F, E, topk, dtype, h_shards, w2_shards, topk_ids,
+                         topk_weights, offsets, slot_to_row, row_to_slot, out, workspace,
+                         stream=None) -> dict:
+    """Time the MoE layer1 candidates; record and return the fastest."""
+    best = flux_opts_t()
+    return _tuned(_lib.flux_tune_moe_layer1(
+        R, tp, T, H, F, E, topk, dtype, _ptrs(h_shards), _ptrs(w2_shards), _ptr(topk_ids),
+        _ptr(topk_weights), _ptr(offsets), _ptr(slot_to_row), _ptr(row_to_slot), _ptrs(out),
+        _ptr(workspace), _nbytes(workspace), _stream(stream), ctypes.byref(best)),
+        "flux_tune_moe_layer1", best)
+
+
+def flux_tune_clear() -> None:
+    _lib.flux_tune_clear()
+
+
+def flux_tune_count() -> int:
+    return _lib.flux_tune_count()

@@ -20,7 +20,7 @@ BUILD = os.path.join(HERE, "_build")
 LIB_NAME = "libflux_gb300.so"
 LIB_PATH = os.path.join(HERE, LIB_NAME)
 
-SOURCES = ["flux_core.cu", "flux_dense.cu", "flux_moe.cu", "flux_noalloc.cu"]
+SOURCES = ["flux_core.cu", "flux_dense.cu", "flux_moe.cu", "flux_noalloc.cu", "flux_tune.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 CFLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-Xcompiler", "-O2",
           "-diag-suppress", "550", "-Xptxas", "-v"]

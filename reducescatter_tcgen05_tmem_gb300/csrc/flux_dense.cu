@@ -68,6 +68,11 @@ extern "C" size_t flux_workspace_size(flux_op_t op, int R, int M, int N, int K) 
   }
 }
 
+bool flux::rs_uses_stream_k(int R, int M, int N, int sm, bool deterministic) {
+  const long long units128 = static_cast<long long>((M + BM - 1) / BM) * ((N + BN - 1) / BN) * R;
+  return units128 < 4LL * sm && !deterministic;
+}
+
 extern "C" flux_status_t flux_ag_gemm(int R, int M, int N, int K, flux_dtype_t dtype,
                                       const void* const* x_shards, const void* const* w_shards,
                                       void* const* out, const uint32_t* ready_flags,
@@ -79,6 +84,9 @@ extern "C" flux_status_t flux_ag_gemm(int R, int M, int N, int K, flux_dtype_t d
   if (x_shards == nullptr || w_shards == nullptr || out == nullptr) return FLUX_ERR_INVALID_ARG;
   flux_status_t st = check_workspace(workspace, workspace_bytes, WS_HEADER);
   if (st != FLUX_OK) return st;
+  flux_opts_t tuned;
+  if (opts == nullptr && tuned_opts(FLUX_OP_AG_GEMM, {R, M, N, K, 0, 0, 0, 0}, dtype, &tuned))
+    opts = &tuned;
   const int rows = M / R, Nr = N / R;
   if (M == 0 || Nr == 0) return FLUX_OK;
   for (int r = 0; r < R; ++r) {
@@ -150,6 +158,9 @@ extern "C" flux_status_t flux_gemm_rs(int R, int M, int N, int K, flux_dtype_t d
   const size_t need = flux_workspace_size(FLUX_OP_GEMM_RS, R, M, N, K);
   flux_status_t st = check_workspace(workspace, workspace_bytes, need);
   if (st != FLUX_OK) return st;
+  flux_opts_t tuned;
+  if (opts == nullptr && tuned_opts(FLUX_OP_GEMM_RS, {R, M, N, K, 0, 0, 0, 0}, dtype, &tuned))
+    opts = &tuned;
   if (M == 0 || N == 0) return FLUX_OK;
   const int Kr = K / R, rows = M / R;
   for (int r = 0; r < R; ++r) {
@@ -194,11 +205,10 @@ extern "C" flux_status_t flux_gemm_rs(int R, int M, int N, int K, flux_dtype_t d
   // fp32 owner tile).  Otherwise: whole 512 x 512 units on clusters of two CTA
   // pairs, strided over a persistent grid.
   const int sm = (opts && opts->num_ctas > 0) ? opts->num_ctas : dev.sm_count;
-  const long long units128 = static_cast<long long>((M + BM - 1) / BM) * ((N + BN - 1) / BN) * R;
   // deterministic_rs: whole tiles (no k split), each rank's partial of a tile
   // on consecutive units (tile-major), added in ascending rank order
   p.deterministic = (opts && opts->deterministic_rs) ? 1 : 0;
-  if (units128 < 4 * sm && !p.deterministic) {
+  if (rs_uses_stream_k(R, M, N, sm, p.deterministic != 0)) {
     p.Nt = (N + BN - 1) / BN;
     p.Mt = (M + BM - 1) / BM;
     p.num_units = p.Mt * p.Nt * R;

@@ -7,6 +7,8 @@
 #include <stddef.h>
 #include <stdint.h>
 
+#include <array>
+
 #include "../../include/flux_gb300.h"
 
 namespace flux {
@@ -52,5 +54,13 @@ flux_status_t check_workspace(const void* ws, size_t have, size_t need);
 
 // Default timeout when opts is NULL or timeout_ns == 0.
 constexpr uint64_t DEFAULT_TIMEOUT_NS = 2000000000ull;
+
+// Launch options recorded by flux_tune_* for one problem (this device, op,
+// dtype and up to eight sizes); false if that problem was never tuned.
+bool tuned_opts(flux_op_t op, const std::array<int, 8>& dims, flux_dtype_t dt, flux_opts_t* out);
+
+// Whether flux_gemm_rs takes its stream-K form (single CTAs, k-slices split
+// evenly over the grid) for this problem on a GPU with `sm` SMs.
+bool rs_uses_stream_k(int R, int M, int N, int sm, bool deterministic);
 
 }  // namespace flux

@@ -440,6 +440,9 @@ flux_status_t moe_layer0_impl(
   const MoeWs L = moe_layout(ws_op, R, T, H, F, E, topk);
   flux_status_t st = check_workspace(workspace, workspace_bytes, L.total);
   if (st != FLUX_OK) return st;
+  flux_opts_t tuned;
+  if (opts == nullptr && tuned_opts(FLUX_OP_MOE_AG, {R, tp, T, H, F, E, topk, 0}, dtype, &tuned))
+    opts = &tuned;
   const bool pull = opts != nullptr && opts->moe_pull_gather != 0;
   const int cl = pull ? MOE0_CL : MOE0S_CL;
   // output columns per rank and experts per rank's weight block
@@ -541,6 +544,9 @@ flux_status_t moe_layer1_impl(
   const MoeWs L = moe_layout(FLUX_OP_MOE_RS, R, T, H, F, E, topk);
   flux_status_t st = check_workspace(workspace, workspace_bytes, L.total);
   if (st != FLUX_OK) return st;
+  flux_opts_t tuned;
+  if (opts == nullptr && tuned_opts(FLUX_OP_MOE_RS, {R, tp, T, H, F, E, topk, 0}, dtype, &tuned))
+    opts = &tuned;
   // reduction length per rank and experts per rank's weight block
   const int Fr = F / tp, EB = E / (R / tp), rows = T / R, n = T * topk;
   for (int r = 0; r < R; ++r) {
