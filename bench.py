@@ -427,6 +427,7 @@ def run_ours(args):
                    "parallelism": f"R=8 virtual TP ranks per GPU; replicas x{ws_}",
                    "l2": "inputs larger than L2 (weights 0.47-1.2 GB per op stream from HBM every step)",
                    "step_tflop": round(flops / 1e12, 3),
+                   "dense_kernel_grid": fx.flux_launch_info(fx.FLUX_OP_AG_GEMM, fx.FLUX_F16),
                    "launch_options": ("tuned on this GPU before warm-up (flux_tune_*): "
                                       + json.dumps(tuned, sort_keys=True)) if tuned is not None
                    else "library defaults"},

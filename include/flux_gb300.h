@@ -142,6 +142,13 @@ int flux_last_cuda_error(void);
  * or invalid sizes. */
 size_t flux_workspace_size(flux_op_t op, int R, int M, int N, int K);
 
+/* Launch shape of a dense op's whole-tile kernel on the current device: CTAs
+ * per cluster and how many of its CTAs are resident at once (its persistent
+ * grid).  FLUX_OP_GEMM / AG_GEMM / GEMM_RS / MLP; other ops return
+ * FLUX_ERR_INVALID_ARG. */
+flux_status_t flux_launch_info(flux_op_t op, flux_dtype_t dtype, int* cluster_ctas,
+                               int* resident_ctas);
+
 /* Bytes of workspace a MoE op needs (FLUX_OP_MOE_AG / MOE_RS / MOE_LAYERS / MOE_EP_AG /
  * MOE_EP_RS); 0 for an unknown op or invalid sizes. */
 size_t flux_moe_workspace_size(flux_op_t op, int R, int T, int H, int F, int E, int topk);

@@ -110,6 +110,7 @@ _SIGS = {
                               _vp, _vp, _vp, _vp, _sz, _vp, _opt], _i),
     "flux_tune_moe_layer1": ([_i, _i, _i, _i, _i, _i, _i, _i, _vpp, _vpp, _vp, _vp, _vp, _vp,
                               _vp, _vpp, _vp, _sz, _vp, _opt], _i),
+    "flux_launch_info": ([_i, _i, ctypes.POINTER(ctypes.c_int), ctypes.POINTER(ctypes.c_int)], _i),
     "flux_tune_clear": ([], None),
     "flux_tune_count": ([], _i),
     "flux_moe_ep_dispatch_gemm": ([_i, _i, _i, _i, _i, _i, _i, _i, _vpp, _vpp, _vp, _vpp, _vp,
@@ -368,3 +369,10 @@ def flux_tune_clear() -> None:
 
 def flux_tune_count() -> int:
     return _lib.flux_tune_count()
+
+
+def flux_launch_info(op, dtype) -> dict:
+    """CTAs per cluster and resident CTAs of a dense op's kernel on this GPU."""
+    cl, res = ctypes.c_int(0), ctypes.c_int(0)
+    _check(_lib.flux_launch_info(op, dtype, ctypes.byref(cl), ctypes.byref(res)), "flux_launch_info")
+    return {"cluster_ctas": cl.value, "resident_ctas": res.value}

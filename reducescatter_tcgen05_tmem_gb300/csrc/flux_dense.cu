@@ -68,6 +68,34 @@ extern "C" size_t flux_workspace_size(flux_op_t op, int R, int M, int N, int K) 
   }
 }
 
+extern "C" flux_status_t flux_launch_info(flux_op_t op, flux_dtype_t dtype, int* cluster_ctas,
+                                          int* resident_ctas) {
+  if (!valid_dtype(dtype) || cluster_ctas == nullptr || resident_ctas == nullptr)
+    return FLUX_ERR_INVALID_ARG;
+  DeviceInfo dev;
+  flux_status_t st = current_device(&dev);
+  if (st != FLUX_OK) return st;
+  int cl = 0, cap = 0;
+  switch (op) {
+    case FLUX_OP_GEMM:
+    case FLUX_OP_AG_GEMM:
+      cl = DENSE_CL;
+      cap = grid_dt<MODE_STORE, DENSE_CL>(dtype, dev, nullptr, 1LL << 30);
+      break;
+    case FLUX_OP_GEMM_RS:
+    case FLUX_OP_MLP:
+      cl = DENSE_CL;
+      cap = grid_dt<MODE_REDUCE, DENSE_CL>(dtype, dev, nullptr, 1LL << 30);
+      break;
+    default:
+      return FLUX_ERR_INVALID_ARG;
+  }
+  if (cap == 0) return FLUX_ERR_CUDA;
+  *cluster_ctas = cl;
+  *resident_ctas = cap;
+  return FLUX_OK;
+}
+
 bool flux::rs_uses_stream_k(int R, int M, int N, int sm, bool deterministic) {
   const long long units128 = static_cast<long long>((M + BM - 1) / BM) * ((N + BN - 1) / BN) * R;
   return units128 < 4LL * sm && !deterministic;
