@@ -118,7 +118,9 @@ typedef struct {
   uint32_t status; /* flux_status_t of the first device-side error, 0 if none */
   uint32_t where;  /* which wait gave up: 1 ready flag, 2 smem slot free, 3 smem slot full,
                       4 accumulator free, 5 accumulator full, 6 drain,
-                      7 deterministic GEMM-RS turn, 8 staged MoE rows of an m-tile */
+                      7 deterministic GEMM-RS turn, 8 staged MoE rows of an m-tile,
+                      9 next unit of the dynamic schedule (dense ops), 10 a cluster
+                      of an unexpected shape under the dynamic schedule */
   uint32_t arg0;   /* flag wait: shard index; pipeline waits: CTA index */
   uint32_t arg1;   /* flag wait: last flag value seen; pipeline waits: stage / buffer */
 } flux_device_report_t;
@@ -135,16 +137,23 @@ const char* flux_status_string(flux_status_t s);
 int flux_last_cuda_error(void);
 
 /* Bytes of workspace a dense op needs (FLUX_OP_GEMM / AG_GEMM / GEMM_RS / MLP).
- * M, N, K as in the op's own signature (FLUX_OP_MLP: M, H, F).  GEMM and
- * AG-GEMM need only the 256-byte status header; GEMM-RS adds per-tile arrival
- * counters and the fp32 accumulation buffer of the owners' row chunks (M x N
- * floats); the MLP needs what its GEMM-RS needs.  Returns 0 for an unknown op
- * or invalid sizes. */
+ * M, N, K as in the op's own signature (FLUX_OP_MLP: M, H, F).  Every dense op
+ * needs the 256-byte status header; GEMM-RS adds per-tile arrival counters and
+ * the fp32 accumulation buffer of the owners' row chunks (M x N floats).  Each
+ * op then adds the mailboxes of its dynamic unit schedule: 4 x (2 U + 256)
+ * bytes rounded up to 256, U = R x ceil(M / 512) x ceil(N_r / 512) work units
+ * (N_r = the op's output columns per rank).  With that area the op runs on
+ * every SM (clusters of CTA pairs, 4 preferred, units claimed at run time);
+ * given only the header (GEMM, AG-GEMM) or only header + counters +
+ * accumulators (GEMM-RS), it runs its static schedule on 4-CTA clusters.  The
+ * MLP needs the larger of its two calls' workspaces.  Returns 0 for an unknown
+ * op or invalid sizes. */
 size_t flux_workspace_size(flux_op_t op, int R, int M, int N, int K);
 
 /* Launch shape of a dense op's whole-tile kernel on the current device: CTAs
- * per cluster and how many of its CTAs are resident at once (its persistent
- * grid).  FLUX_OP_GEMM / AG_GEMM / GEMM_RS / MLP; other ops return
+ * per (preferred) cluster and its persistent grid -- the dynamic schedule's
+ * grid when that launch form is available, else the CTAs of 4-CTA clusters
+ * resident at once.  FLUX_OP_GEMM / AG_GEMM / GEMM_RS / MLP; other ops return
  * FLUX_ERR_INVALID_ARG. */
 flux_status_t flux_launch_info(flux_op_t op, flux_dtype_t dtype, int* cluster_ctas,
                                int* resident_ctas);

@@ -20,6 +20,18 @@ int grid_dt(flux_dtype_t dt, const DeviceInfo& dev, const flux_opts_t* opts, lon
                          : grid_for<MODE, 0, CL>(dev, opts, units);
 }
 
+template <int MODE, int CL>
+int grid_dyn_dt(flux_dtype_t dt, const DeviceInfo& dev) {
+  return dt == FLUX_BF16 ? Launcher<MODE, 1, CL>::max_ctas_dyn(dev)
+                         : Launcher<MODE, 0, CL>::max_ctas_dyn(dev);
+}
+
+template <int MODE, int CL>
+flux_status_t launch_dyn_dt(flux_dtype_t dt, const KParams& p, int grid, cudaStream_t s) {
+  return dt == FLUX_BF16 ? Launcher<MODE, 1, CL>::launch_dyn(p, grid, s)
+                         : Launcher<MODE, 0, CL>::launch_dyn(p, grid, s);
+}
+
 // Dense whole-tile kernels run on clusters of two CTA pairs stacked along M
 // (512 x 512 per cluster, B multicast between the pairs).
 constexpr int DENSE_CL = 4;
@@ -49,6 +61,46 @@ size_t rs_counter_bytes(int M, int N) {
   return round_up(Mt * Nt * 4 * sizeof(uint32_t), WS_ALIGN);
 }
 
+// GEMM-RS workspace without the dynamic schedule's mailboxes: header, arrival
+// counters, fp32 owner rows (the least a call accepts; it then runs the static
+// schedule).
+size_t rs_min_bytes(int M, int N) {
+  return WS_HEADER + rs_counter_bytes(M, N) + static_cast<size_t>(M) * N * sizeof(float);
+}
+
+// Whole 512 x 512 units of a dense op over R ranks with `cols` output columns each.
+long long dense_units(int R, int M, int cols) {
+  return static_cast<long long>(R) * ((M + DenseUnit::ROWS - 1) / DenseUnit::ROWS) *
+         ((cols + DenseGeo::TILE_N - 1) / DenseGeo::TILE_N);
+}
+
+// Mailboxes of the dynamic schedule: with g <= MAX_REGIONS regions of
+// 2 ceil(U / g) + 2 entries each, at most 2 U + 4 MAX_REGIONS entries.
+size_t sched_bytes(long long units) {
+  return round_up(static_cast<size_t>(2 * units + 4 * MAX_REGIONS) * sizeof(uint32_t), WS_ALIGN);
+}
+
+// Set up the dynamic schedule of a dense CL = 4 launch if the workspace has
+// room for its mailboxes at `mbox` and the launch form is available; returns
+// its grid, or 0 (then the static schedule runs).
+template <int MODE>
+int setup_dyn(KParams& p, flux_dtype_t dt, const DeviceInfo& dev, const flux_opts_t* opts,
+              uint8_t* mbox, size_t room) {
+  if (room < sched_bytes(p.num_units)) return 0;
+  int grid = grid_dyn_dt<MODE, DENSE_CL>(dt, dev);
+  if (opts && opts->num_ctas > 0 && opts->num_ctas < grid) grid = opts->num_ctas - opts->num_ctas % DENSE_CL;
+  if (grid < DENSE_CL) return 0;
+  const long long regions = grid / DENSE_CL;
+  if (regions > p.num_units) {
+    grid = static_cast<int>(p.num_units) * DENSE_CL;
+  }
+  const long long g = grid / DENSE_CL;
+  p.dyn = 1;
+  p.mbox_cap = static_cast<int>(2 * ((p.num_units + g - 1) / g) + 2);
+  p.mbox = reinterpret_cast<uint32_t*>(mbox);
+  return grid;
+}
+
 }  // namespace
 }  // namespace flux
 
@@ -59,10 +111,14 @@ extern "C" size_t flux_workspace_size(flux_op_t op, int R, int M, int N, int K) 
   switch (op) {
     case FLUX_OP_GEMM:
     case FLUX_OP_AG_GEMM:
-      return WS_HEADER;
+      return WS_HEADER + sched_bytes(dense_units(R, M, N / R));
     case FLUX_OP_GEMM_RS:
-    case FLUX_OP_MLP:  // (R, M, H, F): what its GEMM-RS (R, M, N = H, K = F) needs
-      return WS_HEADER + rs_counter_bytes(M, N) + static_cast<size_t>(M) * N * sizeof(float);
+      return rs_min_bytes(M, N) + sched_bytes(dense_units(R, M, N));
+    case FLUX_OP_MLP: {  // (R, M, H, F): its AG-GEMM (R, M, F, H), then its GEMM-RS (R, M, H, F)
+      const size_t ag = flux_workspace_size(FLUX_OP_AG_GEMM, R, M, K, N);
+      const size_t rs = flux_workspace_size(FLUX_OP_GEMM_RS, R, M, N, K);
+      return ag > rs ? ag : rs;
+    }
     default:
       return 0;
   }
@@ -80,12 +136,14 @@ extern "C" flux_status_t flux_launch_info(flux_op_t op, flux_dtype_t dtype, int*
     case FLUX_OP_GEMM:
     case FLUX_OP_AG_GEMM:
       cl = DENSE_CL;
-      cap = grid_dt<MODE_STORE, DENSE_CL>(dtype, dev, nullptr, 1LL << 30);
+      cap = grid_dyn_dt<MODE_STORE, DENSE_CL>(dtype, dev);
+      if (cap == 0) cap = grid_dt<MODE_STORE, DENSE_CL>(dtype, dev, nullptr, 1LL << 30);
       break;
     case FLUX_OP_GEMM_RS:
     case FLUX_OP_MLP:
       cl = DENSE_CL;
-      cap = grid_dt<MODE_REDUCE, DENSE_CL>(dtype, dev, nullptr, 1LL << 30);
+      cap = grid_dyn_dt<MODE_REDUCE, DENSE_CL>(dtype, dev);
+      if (cap == 0) cap = grid_dt<MODE_REDUCE, DENSE_CL>(dtype, dev, nullptr, 1LL << 30);
       break;
     default:
       return FLUX_ERR_INVALID_ARG;
@@ -161,6 +219,16 @@ extern "C" flux_status_t flux_ag_gemm(int R, int M, int N, int K, flux_dtype_t d
   fill_common(p, opts, workspace);
   // bands of 4 n-tiles (2048 columns) measured best for the 512 x 512 units
   if (!(opts && opts->group_n > 0)) p.group_n = 4;
+  // dynamic schedule over every SM when the workspace holds its mailboxes
+  const int dgrid = setup_dyn<MODE_STORE>(p, dtype, dev, opts,
+                                          static_cast<uint8_t*>(workspace) + WS_HEADER,
+                                          workspace_bytes - WS_HEADER);
+  if (dgrid > 0) {
+    if (launch_dyn_dt<MODE_STORE, DENSE_CL>(dtype, p, dgrid, s) == FLUX_OK) return FLUX_OK;
+    p.dyn = 0;  // launch form refused: the static schedule below
+    p.mbox = nullptr;
+    p.mbox_cap = 0;
+  }
   const int grid = grid_dt<MODE_STORE, DENSE_CL>(dtype, dev, opts, p.num_units);
   if (grid == 0) return FLUX_ERR_CUDA;
   return launch_dt<MODE_STORE, DENSE_CL>(dtype, p, grid, s);
@@ -183,8 +251,7 @@ extern "C" flux_status_t flux_gemm_rs(int R, int M, int N, int K, flux_dtype_t d
     return FLUX_ERR_INVALID_ARG;
   if (M % R || K % R) return FLUX_ERR_INVALID_ARG;
   if (a_shards == nullptr || b_shards == nullptr || out == nullptr) return FLUX_ERR_INVALID_ARG;
-  const size_t need = flux_workspace_size(FLUX_OP_GEMM_RS, R, M, N, K);
-  flux_status_t st = check_workspace(workspace, workspace_bytes, need);
+  flux_status_t st = check_workspace(workspace, workspace_bytes, rs_min_bytes(M, N));
   if (st != FLUX_OK) return st;
   flux_opts_t tuned;
   if (opts == nullptr && tuned_opts(FLUX_OP_GEMM_RS, {R, M, N, K, 0, 0, 0, 0}, dtype, &tuned))
@@ -269,11 +336,29 @@ extern "C" flux_status_t flux_gemm_rs(int R, int M, int N, int K, flux_dtype_t d
   p.num_units = tiles * R;
   p.total_ksteps = static_cast<long long>(p.num_units) * p.KT;
   p.stream_k = 0;
+  auto tiles_per_group = [&](int grid) {
+    const int tg = p.deterministic ? 1
+                  : (opts && opts->tiles_per_group > 0) ? opts->tiles_per_group : grid / DENSE_CL;
+    return tg < tiles ? tg : tiles;
+  };
+  if (!p.deterministic) {
+    // dynamic schedule over every SM when the workspace holds its mailboxes
+    // (the deterministic order keeps the static schedule: its waits point at
+    // lower units, which must already sit on resident clusters)
+    const size_t off = rs_min_bytes(M, N);
+    const int dgrid = setup_dyn<MODE_REDUCE>(p, dtype, dev, opts, ws + off,
+                                             workspace_bytes > off ? workspace_bytes - off : 0);
+    if (dgrid > 0) {
+      p.tiles_per_group = tiles_per_group(dgrid);
+      if (launch_dyn_dt<MODE_REDUCE, DENSE_CL>(dtype, p, dgrid, s) == FLUX_OK) return FLUX_OK;
+      p.dyn = 0;  // launch form refused: the static schedule below
+      p.mbox = nullptr;
+      p.mbox_cap = 0;
+    }
+  }
   const int grid = grid_dt<MODE_REDUCE, DENSE_CL>(dtype, dev, opts, p.num_units);
   if (grid == 0) return FLUX_ERR_CUDA;
-  const int tg = p.deterministic ? 1
-                : (opts && opts->tiles_per_group > 0) ? opts->tiles_per_group : grid / DENSE_CL;
-  p.tiles_per_group = tg < tiles ? tg : tiles;
+  p.tiles_per_group = tiles_per_group(grid);
   return launch_dt<MODE_REDUCE, DENSE_CL>(dtype, p, grid, s);
 }
 
@@ -284,10 +369,12 @@ extern "C" flux_status_t flux_mlp_ag_rs(int R, int M, int H, int F, flux_dtype_t
                                         void* workspace, size_t workspace_bytes,
                                         const flux_opts_t* opts, void* stream) {
   if (h == nullptr) return FLUX_ERR_INVALID_ARG;
-  // validate both calls before launching either
-  const size_t need = flux_workspace_size(FLUX_OP_MLP, R, M, H, F);
-  if (need == 0 || M % R || F % R || !valid_dtype(dtype)) return FLUX_ERR_INVALID_ARG;
-  flux_status_t st = check_workspace(workspace, workspace_bytes, need);
+  // validate both calls before launching either (the least each accepts: the
+  // GEMM-RS part; the AG-GEMM needs only the header)
+  if (R < 1 || R > FLUX_MAX_RANKS || M < 0 || H < 0 || F < 0 || M % R || F % R ||
+      !valid_dtype(dtype))
+    return FLUX_ERR_INVALID_ARG;
+  flux_status_t st = check_workspace(workspace, workspace_bytes, rs_min_bytes(M, H));
   if (st != FLUX_OK) return st;
   if ((st = flux_ag_gemm(R, M, F, H, dtype, x_shards, w1_shards, h, ready_flags, workspace,
                          workspace_bytes, opts, stream)) != FLUX_OK)

@@ -15,6 +15,8 @@ namespace flux {
 
 constexpr size_t WS_HEADER = 256;  // status header at the start of every workspace
 constexpr size_t WS_ALIGN = 256;
+// Dynamic schedule of the dense kernels: at most this many regions of 4 CTAs.
+constexpr int MAX_REGIONS = 64;
 
 struct DeviceInfo {
   int device;

@@ -57,6 +57,17 @@
 // PAIR = min(CL, 2) is the tcgen05 CTA group and MC = CL / PAIR the pairs that
 // share B (dense modes only).
 //
+// Dynamic schedule (dense modes, CL = 4, KParams::dyn): clusters of 4 CTAs fit
+// on only part of the SMs (144 of 152 on GB300), so the kernel is launched with
+// CTA pairs as the cluster size and 4 as the preferred one.  Every aligned group
+// of 4 CTAs (a "region") is then either one 4-CTA cluster or two pair clusters.
+// The region computes one 512 x 512 unit at a time either way: pair clusters
+// load their own B instead of sharing it by multicast.  Regions claim units from
+// a counter in the workspace header, so that the slower pair regions take fewer
+// of them; the region's first CTA claims the next unit a few k-slices before
+// its current one ends and writes it into the region's mailbox in the
+// workspace, from which every role of the region's CTAs reads its units.
+//
 // Every wait is bounded: after timeout_ns (or an iteration cap) the thread
 // records FLUX_ERR_TIMEOUT in the workspace header, raises the per-call abort
 // word, and the CTA drains its in-flight copies and MMAs, frees TMEM and exits.
@@ -154,7 +165,9 @@ constexpr int STAGE_BLK = 32;     // MOE_STAGED: rows per staging block (one rea
 constexpr int STAGE_UNROLL = 16;  // MOE_STAGED: 16-byte loads in flight per lane
 
 // device status header at the start of every workspace (256 bytes)
-enum HdrField { H_STATUS = 0, H_WHERE = 1, H_ARG0 = 2, H_ARG1 = 3, H_ABORT = 4 };
+// H_CLAIM / H_EXIT: dynamic schedule's unit counter and count of finished
+// CTAs (the last CTA out zeroes both and the mailboxes).
+enum HdrField { H_STATUS = 0, H_WHERE = 1, H_ARG0 = 2, H_ARG1 = 3, H_ABORT = 4, H_CLAIM = 8, H_EXIT = 9 };
 enum WaitSite {
   W_FLAG = 1,
   W_EMPTY = 2,
@@ -163,7 +176,9 @@ enum WaitSite {
   W_TFULL = 5,
   W_DRAIN = 6,
   W_TURN = 7,
-  W_STAGE = 8
+  W_STAGE = 8,
+  W_SCHED = 9,  // dynamic schedule: the region's next unit
+  W_SHAPE = 10  // dynamic schedule: a cluster of an unexpected size or CTA order
 };
 constexpr uint32_t ST_TIMEOUT = 5;
 constexpr uint32_t ST_INVALID = 1;
@@ -207,7 +222,16 @@ struct KParams {
   int moe_tp;  // MoE: ranks per expert group (R: tensor parallel, 1: expert parallel)
   int moe_el;  // MoE: experts per group; rank g moe_tp + t holds block t of group g's experts
   int moe_order;  // MoE: unit order (see decode_moe)
+  // dense CL = 4 kernels: units claimed at run time (see the dynamic schedule above)
+  int dyn;
+  int mbox_cap;    // mailbox entries per region
+  uint32_t* mbox;  // [gridDim / 4 regions x mbox_cap] claimed unit + 1, or MBOX_DONE
 };
+
+constexpr uint32_t MBOX_DONE = 0xFFFFFFFFu;
+// k-slices before the end of its current unit at which a region claims the next
+// (the other CTAs of the region read it when they finish the current unit)
+constexpr int CLAIM_AHEAD = 8;
 
 struct Ctl {
   uint32_t* hdr;
@@ -501,16 +525,27 @@ __device__ __forceinline__ Work decode_moe(const KParams& p, int u, int total_mt
 }
 
 // Iterates the items of this CTA identically in every role.  All CTAs of a
-// cluster walk the same units (cluster index = blockIdx / CL).
+// cluster (of a region, under the dynamic schedule) walk the same units
+// (region index = blockIdx / CL).  `cta` is the CTA's part of the unit.
+// Static schedule: units u, u + stride, ... of the persistent grid.  Dynamic
+// schedule: the units the region's mailbox receives, in order; `warp_uniform`
+// (a whole warp calls next) makes lane 0 read the mailbox for the warp.
 template <int MODE, int CL>
 struct ItemIter {
+  static constexpr bool DYN_OK = Unit<MODE, CL>::DENSE && CL == 4;
   const KParams& p;
+  const Ctl* ctl;
   int total_mt;      // MoE: device-computed number of m-tiles
   int num_units;
   long long pos, end;  // stream-K k-step range
   int u, stride, cta;
+  bool dyn, warp_uniform;
+  uint32_t* box;     // dynamic: the region's mailbox
+  int taken;         // dynamic: mailbox entries read so far
 
-  __device__ ItemIter(const KParams& p_, int total_mt_, int cta_) : p(p_), total_mt(total_mt_), cta(cta_) {
+  __device__ ItemIter(const KParams& p_, int total_mt_, int cta_, const Ctl* ctl_ = nullptr,
+                      bool warp_uniform_ = false)
+      : p(p_), ctl(ctl_), total_mt(total_mt_), cta(cta_), warp_uniform(warp_uniform_) {
     if (is_moe(MODE)) {
       num_units = total_mt * p.Nt * p.moe_tp;
     } else {
@@ -518,6 +553,9 @@ struct ItemIter {
     }
     u = blockIdx.x / CL;
     stride = gridDim.x / CL;
+    dyn = DYN_OK && p.dyn != 0 && ctl != nullptr;
+    box = dyn ? p.mbox + static_cast<size_t>(u) * p.mbox_cap : nullptr;
+    taken = 0;
     if (MODE == MODE_REDUCE && p.stream_k) {
       const long long L = p.total_ksteps;
       pos = L * u / stride;
@@ -526,6 +564,20 @@ struct ItemIter {
   }
 
   __device__ bool next(Work& w) {
+    if (DYN_OK && dyn) {
+      uint32_t v = 0;
+      if (!warp_uniform || (threadIdx.x & 31) == 0) {
+        // bounded: a timeout is recorded, an abort ends the walk
+        if (wait_count(box + taken, 1u, *ctl, W_SCHED)) v = ld_acquire_u32(box + taken);
+      }
+      if (warp_uniform) v = __shfl_sync(0xFFFFFFFFu, v, 0);
+      ++taken;
+      if (v == 0u || v == MBOX_DONE) return false;
+      const int unit = static_cast<int>(v - 1u);
+      if (MODE == MODE_STORE) w = decode_store<CL>(p, unit, cta);
+      else w = decode_reduce<CL>(p, unit, cta);
+      return true;
+    }
     if (MODE == MODE_REDUCE && p.stream_k) {
       if (pos >= end) return false;
       const int unit = static_cast<int>(pos / p.KT);
@@ -547,6 +599,30 @@ struct ItemIter {
   }
 };
 
+// Dynamic schedule: the region's first CTA writes its next unit (+ 1) into
+// entry j of the region's mailbox, or MBOX_DONE once the counter has run out or
+// the mailbox is full (then the other regions take the remaining units: the
+// mailboxes together hold more entries than there are units).
+__device__ __forceinline__ void claim_unit(const KParams& p, uint32_t* box, int j) {
+  uint32_t v = MBOX_DONE;
+  if (j < p.mbox_cap - 1) {
+    const uint32_t u = atomicAdd(p.hdr + H_CLAIM, 1u);
+    if (u < static_cast<uint32_t>(p.num_units)) v = u + 1u;
+  }
+  st_release_u32(box + j, v);
+}
+
+// Where a CTA sits.  vrank: its 128-row part of the unit (0 .. CL-1); hw_rank,
+// hw_cl: its rank in, and the size of, the cluster it was launched in (under
+// the dynamic schedule a region may be two pair clusters); mc2: the unit's two
+// pairs share B by multicast (one cluster holds both).
+struct Pos {
+  int vrank;
+  int hw_rank;
+  int hw_cl;
+  bool mc2;
+};
+
 // ---------------------------------------------------------------- roles
 struct Smem {
   uint8_t* a;       // STAGES x A_STAGE
@@ -557,6 +633,7 @@ struct Smem {
   uint64_t* tempty; // [2]
   uint64_t* drain;  // [1]
   uint32_t* tmem_slot;
+  uint32_t* misc;   // [2] dynamic schedule: cluster-shape check, last CTA out
   uint8_t* stg;     // EPI_WARPS x STG_WARP epilogue staging (1024-byte aligned)
 };
 
@@ -573,17 +650,23 @@ __device__ __forceinline__ uint32_t pair_peer_bytes(const KParams& p, const Work
   return a + __popc(mask) * B_BOX_N * BK * 2;
 }
 
-// TMA producer (one thread).  `rank` is the CTA's rank in its cluster.
+// TMA producer (one thread).  Under the dynamic schedule the producer of a
+// region's first CTA also claims the region's units.
 template <int MODE, int CL>
-__device__ void producer_tma(const KParams& p, const Smem& s, const Ctl& c, int total_mt, int rank) {
+__device__ void producer_tma(const KParams& p, const Smem& s, const Ctl& c, int total_mt,
+                             const Pos& ps) {
   constexpr int PAIR = Unit<MODE, CL>::PAIR;
   constexpr int MC = Unit<MODE, CL>::MC;
   using G = typename Unit<MODE, CL>::G;
-  const int cta = rank & (PAIR - 1);  // position in the pair
-  const int half = rank / PAIR;       // MC = 2: the B half this CTA multicasts
-  // MC = 2: this CTA and the one holding the same B columns in the other tile
-  const uint16_t mc_mask = static_cast<uint16_t>((1u << rank) | (1u << (rank ^ PAIR)));
-  ItemIter<MODE, CL> iter(p, total_mt, rank);
+  const int cta = ps.vrank & (PAIR - 1);  // position in the pair
+  const bool mc2 = MC == 2 && ps.mc2;     // B shared with the other pair by multicast
+  const int half = ps.hw_rank / PAIR;     // mc2: the B half this CTA multicasts
+  // mc2: this CTA and the one holding the same B columns in the other tile
+  const uint16_t mc_mask = static_cast<uint16_t>((1u << ps.hw_rank) | (1u << (ps.hw_rank ^ PAIR)));
+  ItemIter<MODE, CL> iter(p, total_mt, ps.vrank, &c);
+  const bool leader = iter.dyn && ps.vrank == 0;
+  int claimed = 0;  // mailbox entries the leader has written
+  if (leader) claim_unit(p, iter.box, claimed++);
   Work w;
   uint32_t stage = 0, phase = 0;
   uint32_t issued = 0;
@@ -626,9 +709,15 @@ __device__ void producer_tma(const KParams& p, const Smem& s, const Ctl& c, int 
       // the even CTA's barrier also counts the odd CTA's bytes of the same stage
       bytes += pair_peer_bytes<MODE, G>(p, w);
     }
+    const int claim_k = max(w.k0, w.k1 - CLAIM_AHEAD);
+    bool to_claim = leader;
     for (int k = w.k0; k < w.k1; ++k) {
+      if (to_claim && k == claim_k) {
+        claim_unit(p, iter.box, claimed++);
+        to_claim = false;
+      }
       // the empty barrier is completed by a remote commit whenever another CTA's MMAs read the stage
-      if (((PAIR == 2 && cta != 0) || (MC == 2 && PAIR == 2)
+      if (((PAIR == 2 && cta != 0) || mc2
                ? wait_bar_remote(smem_u32(&s.empty[stage]), phase ^ 1u, c, W_EMPTY, stage)
                : wait_bar(smem_u32(&s.empty[stage]), phase ^ 1u, c, W_EMPTY, stage)) != 0) {
         ok = false;
@@ -637,7 +726,7 @@ __device__ void producer_tma(const KParams& p, const Smem& s, const Ctl& c, int 
       const uint32_t fb = smem_u32(&s.full[stage]);
       if (PAIR == 1 || cta == 0) mbar_arrive_expect_tx(fb, bytes);
       // barrier in the even CTA of this CTA's pair
-      const uint32_t fbc = PAIR == 2 ? mapa_shared(fb, static_cast<uint32_t>(rank & ~1)) : fb;
+      const uint32_t fbc = PAIR == 2 ? mapa_shared(fb, static_cast<uint32_t>(ps.hw_rank & ~1)) : fb;
       const uint32_t sa = smem_u32(s.a + stage * A_STAGE);
       const uint32_t sb = smem_u32(s.b + stage * G::B_STAGE);
       const int kc = k * BK;
@@ -656,7 +745,7 @@ __device__ void producer_tma(const KParams& p, const Smem& s, const Ctl& c, int 
       }
       for (int j = 0; j < G::B_BOXES; ++j) {
         if (!((bmask >> j) & 1u)) continue;
-        if (MC == 2 && (j >> 1) != half) continue;  // the partner multicasts this box
+        if (mc2 && (j >> 1) != half) continue;  // the partner multicasts this box
         const int nc = b_box_col<PAIR>(n0, cta, j);
         const int n = nc < p.N ? nc : n0;  // the padding box of a CTA without columns
         const uint32_t dst = sb + j * B_BOX_N * BK * 2;
@@ -664,7 +753,7 @@ __device__ void producer_tma(const KParams& p, const Smem& s, const Ctl& c, int 
           if (PAIR == 2) tma_load_3d_pair(dst, &p.tmB[w.r], fbc, n, kc, w.e);
           else tma_load_3d(dst, &p.tmB[w.r], fb, n, kc, w.e);
         } else if (PAIR == 2) {
-          if (MC == 2) tma_load_2d_pair_mc(dst, &p.tmB[w.r], fbc, n, kc, mc_mask);
+          if (mc2) tma_load_2d_pair_mc(dst, &p.tmB[w.r], fbc, n, kc, mc_mask);
           else tma_load_2d_pair(dst, &p.tmB[w.r], fbc, n, kc);
         } else {
           tma_load_2d(dst, &p.tmB[w.r], fb, n, kc);
@@ -673,6 +762,7 @@ __device__ void producer_tma(const KParams& p, const Smem& s, const Ctl& c, int 
       ++issued;
       if (++stage == G::STAGES) { stage = 0; phase ^= 1u; }
     }
+    if (to_claim && ok) claim_unit(p, iter.box, claimed++);  // a unit without k-slices
   }
   // drain: every issued copy must land before the CTA may exit.  The odd CTA of
   // a pair cannot see its copies complete (they count on the even CTA's
@@ -682,7 +772,7 @@ __device__ void producer_tma(const KParams& p, const Smem& s, const Ctl& c, int 
     const uint32_t fills = issued / G::STAGES + (st < issued % G::STAGES ? 1u : 0u);
     if (fills == 0) continue;
     if (PAIR == 2 && cta != 0) {
-      // (with MC = 2 the empty barrier also waits for the other pair, whose
+      // (with mc2 the empty barrier also waits for the other pair, whose
       // multicast copies land here too)
       wait_bar_remote_drain(smem_u32(&s.empty[st]), (fills - 1u) & 1u, c, W_DRAIN, st);
     } else {
@@ -788,16 +878,16 @@ __device__ void producer_gather(const KParams& p, const Smem& s, const Ctl& c, i
 // MMA issuer (one thread; with pairs only in the even CTA of each pair).
 template <int MODE, int DT, int CL>
 __device__ void mma_issuer(const KParams& p, const Smem& s, const Ctl& c, uint32_t tmem_base,
-                           int total_mt, int rank) {
+                           int total_mt, const Pos& ps) {
   constexpr int PAIR = Unit<MODE, CL>::PAIR;
-  constexpr int MC = Unit<MODE, CL>::MC;
   using G = typename Unit<MODE, CL>::G;
   constexpr uint32_t IDESC = idesc_f16(DT, BM * PAIR, BN, 0, 1);
-  // stage release reaches every CTA whose shared memory the stage's copies
-  // fill; the accumulator-full signal only this pair
-  constexpr uint16_t EMPTY_MASK = static_cast<uint16_t>((1u << CL) - 1u);
-  const uint16_t pair_mask = static_cast<uint16_t>(0x3u << (rank & ~1));
-  ItemIter<MODE, CL> iter(p, total_mt, rank);
+  // stage release reaches every CTA of the cluster (with a multicast B every
+  // CTA's shared memory is filled by both pairs); the accumulator-full signal
+  // only this pair
+  const uint16_t EMPTY_MASK = static_cast<uint16_t>((1u << ps.hw_cl) - 1u);
+  const uint16_t pair_mask = static_cast<uint16_t>(0x3u << (ps.hw_rank & ~1));
+  ItemIter<MODE, CL> iter(p, total_mt, ps.vrank, &c);
   Work w;
   uint32_t stage = 0, phase = 0;
   int it = 0;
@@ -949,17 +1039,17 @@ __device__ __forceinline__ void convert8(float* src, uint16_t* dst) {
 
 template <int MODE, int DT, int CL>
 __device__ void epilogue(const KParams& p, const Smem& s, const Ctl& c, uint32_t tmem_base,
-                         int total_mt, int warp, int rank) {
+                         int total_mt, int warp, const Pos& ps) {
   constexpr int PAIR = Unit<MODE, CL>::PAIR;
-  const int cta = rank & (PAIR - 1);
+  const int cta = ps.vrank & (PAIR - 1);
   const int lane = threadIdx.x & 31;
   const int q = warp & 3;  // TMEM lane quarter this warp may access
-  ItemIter<MODE, CL> iter(p, total_mt, rank);
+  ItemIter<MODE, CL> iter(p, total_mt, ps.vrank, &c, true);
   Work w;
   int it = 0;
   // the accumulator-empty barrier lives in the even CTA of a pair
   const uint32_t tempty0 = (PAIR == 2 && cta != 0)
-                               ? mapa_shared(smem_u32(&s.tempty[0]), static_cast<uint32_t>(rank & ~1))
+                               ? mapa_shared(smem_u32(&s.tempty[0]), static_cast<uint32_t>(ps.hw_rank & ~1))
                                : smem_u32(&s.tempty[0]);
   const uint32_t sstg = smem_u32(s.stg + q * STG_WARP);
   using G = typename Unit<MODE, CL>::G;
@@ -1197,10 +1287,18 @@ fused_gemm_kernel(const __grid_constant__ KParams p) {
   s.tempty = bars + 2 * G::STAGES + 2;
   s.drain = bars + 2 * G::STAGES + 4;
   s.tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * G::STAGES + 5);
+  s.misc = s.tmem_slot + 1;
 
   const int warp = threadIdx.x >> 5;
-  const int rank = CL > 1 ? static_cast<int>(cluster_ctarank()) : 0;
-  const int cta = rank & (PAIR - 1);
+  const bool dyn = ItemIter<MODE, CL>::DYN_OK && p.dyn != 0;
+  Pos ps;
+  ps.hw_rank = CL > 1 ? static_cast<int>(cluster_ctarank()) : 0;
+  ps.hw_cl = CL > 1 ? static_cast<int>(cluster_nctarank()) : 1;
+  // dynamic schedule: the CTA's part of the unit is its place in the region of
+  // CL CTAs, whichever cluster size the launch gave the region
+  ps.vrank = dyn ? static_cast<int>(blockIdx.x % CL) : ps.hw_rank;
+  ps.mc2 = ps.hw_cl == CL;
+  const int cta = ps.vrank & (PAIR - 1);
   Ctl c;
   c.hdr = p.hdr;
   c.seq = p.seq;
@@ -1208,9 +1306,15 @@ fused_gemm_kernel(const __grid_constant__ KParams p) {
   c.pipe_timeout = 2 * p.timeout_ns + 10000000ull;
 
   if (threadIdx.x == 0) {
+    // the dynamic schedule expects clusters of CL or PAIR CTAs made of
+    // consecutive, aligned CTA indices
+    s.misc[0] = (dyn && ((ps.hw_cl != CL && ps.hw_cl != PAIR) ||
+                         ps.hw_rank != static_cast<int>(blockIdx.x % ps.hw_cl))) ? 1u : 0u;
+    s.misc[1] = 0u;
     for (int i = 0; i < G::STAGES; ++i) {
       mbar_init(smem_u32(&s.full[i]), KS::FULL_COUNT);
-      mbar_init(smem_u32(&s.empty[i]), MC);  // one commit per pair that reads the stage
+      // one commit per pair that reads the stage
+      mbar_init(smem_u32(&s.empty[i]), (MC == 2 && ps.mc2) ? 2 : 1);
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(smem_u32(&s.tfull[i]), 1);
@@ -1233,6 +1337,15 @@ fused_gemm_kernel(const __grid_constant__ KParams p) {
   if (CL > 1) cluster_sync();  // peer barriers initialised and TMEM allocated in every CTA
   tc_fence_after();
   const uint32_t tmem_base = *s.tmem_slot;
+  bool run = true;
+  if (dyn) {
+    // one decision for the whole cluster: any CTA of an unexpected shape stops them all
+    for (int r = 0; r < ps.hw_cl; ++r)
+      if (ld_shared_cluster_u32(mapa_shared(smem_u32(s.misc), static_cast<uint32_t>(r))) != 0u)
+        run = false;
+    if (!run && threadIdx.x == 0 && ps.hw_rank == 0)
+      raise_error(c, ST_INVALID, W_SHAPE, blockIdx.x, static_cast<uint32_t>(ps.hw_cl));
+  }
 
   int total_mt = 0;
   if (is_moe(MODE)) total_mt = __ldg(p.tile_off + p.E);
@@ -1244,18 +1357,20 @@ fused_gemm_kernel(const __grid_constant__ KParams p) {
     tma_prefetch_desc(&p.tmB[lane]);
     if (!KS::CPASYNC_GATHER) tma_prefetch_desc(&p.tmA[lane]);
   }
-  if (warp < KS::PRODUCER_WARPS) {
+  if (!run) {
+    // (the cluster shape check failed: recorded above; no role runs)
+  } else if (warp < KS::PRODUCER_WARPS) {
     if constexpr (KS::CPASYNC_GATHER) {
       producer_gather<KS::PRODUCER_WARPS * 32>(p, s, c, total_mt);
     } else if (lane == 0) {
-      producer_tma<MODE, CL>(p, s, c, total_mt, rank);
+      producer_tma<MODE, CL>(p, s, c, total_mt, ps);
     }
   } else if (warp == KS::MMA_WARP) {
     // the even CTA of a pair issues the MMAs for both
-    if (lane == 0 && cta == 0) mma_issuer<MODE, DT, CL>(p, s, c, tmem_base, total_mt, rank);
+    if (lane == 0 && cta == 0) mma_issuer<MODE, DT, CL>(p, s, c, tmem_base, total_mt, ps);
     __syncwarp();
   } else {
-    epilogue<MODE, DT, CL>(p, s, c, tmem_base, total_mt, warp, rank);
+    epilogue<MODE, DT, CL>(p, s, c, tmem_base, total_mt, warp, ps);
   }
 
   tc_fence_before();
@@ -1265,6 +1380,25 @@ fused_gemm_kernel(const __grid_constant__ KParams p) {
     tc_fence_after();
     if (PAIR == 2) tmem_dealloc2(tmem_base, TMEM_COLS);
     else tmem_dealloc(tmem_base, TMEM_COLS);
+  }
+  if (dyn) {
+    // The last CTA to finish clears the schedule (counter, exit count and
+    // mailboxes) so that the workspace is zero again for the next call.  Every
+    // CTA's claims and mailbox reads come before its exit count.
+    if (threadIdx.x == 0) {
+      __threadfence();
+      s.misc[1] = (atomicAdd(p.hdr + H_EXIT, 1u) + 1u == gridDim.x) ? 1u : 0u;
+    }
+    __syncthreads();
+    if (s.misc[1] != 0u) {
+      __threadfence();
+      const int n = static_cast<int>(gridDim.x / CL) * p.mbox_cap;
+      for (int i = threadIdx.x; i < n; i += blockDim.x) p.mbox[i] = 0u;
+      if (threadIdx.x == 0) {
+        p.hdr[H_CLAIM] = 0u;
+        p.hdr[H_EXIT] = 0u;
+      }
+    }
   }
 }
 

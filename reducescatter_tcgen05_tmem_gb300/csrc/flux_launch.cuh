@@ -61,6 +61,69 @@ struct Launcher {
     return ctas;
   }
 
+  // Dynamic schedule (dense CL = 4 kernels): the grid when clusters are CTA
+  // pairs with CL as the preferred size, a multiple of CL of at most
+  // 4 * MAX_REGIONS CTAs; 0 if this launch form is not available.
+  static int max_ctas_dyn(const DeviceInfo& dev) {
+    static_assert(CL == 4, "regions of two CTA pairs");
+    if (max_ctas(dev) <= 0) return 0;  // sets the shared memory attribute
+    static std::once_flag once;
+    static int ctas = 0;
+    std::call_once(once, [&dev] {
+      cudaLaunchConfig_t cfg = {};
+      cfg.gridDim = dim3(2 * (dev.sm_count / 2), 1, 1);
+      cfg.blockDim = dim3(KernelShape<MODE, DT, CL>::THREADS, 1, 1);
+      cfg.dynamicSmemBytes = SMEM_BYTES;
+      cudaLaunchAttribute attr[1];
+      attr[0].id = cudaLaunchAttributeClusterDimension;
+      attr[0].val.clusterDim.x = 2;
+      attr[0].val.clusterDim.y = 1;
+      attr[0].val.clusterDim.z = 1;
+      cfg.attrs = attr;
+      cfg.numAttrs = 1;
+      int clusters = 0;
+      if (cudaOccupancyMaxActiveClusters(&clusters, fused_gemm_kernel<MODE, DT, CL>, &cfg) !=
+          cudaSuccess) {
+        (void)cudaGetLastError();
+        clusters = 0;
+      }
+      int g = clusters * 2;
+      g -= g % CL;
+      if (g > CL * MAX_REGIONS) g = CL * MAX_REGIONS;
+      ctas = g;
+      if (debug_enabled())
+        std::fprintf(stderr, "[flux] mode %d dtype %d: %d CTA pairs resident at once (dynamic grid %d)\n",
+                     MODE, DT, clusters, g);
+    });
+    return ctas;
+  }
+
+  static flux_status_t launch_dyn(const KParams& p, int grid, cudaStream_t stream) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid, 1, 1);
+    cfg.blockDim = dim3(KernelShape<MODE, DT, CL>::THREADS, 1, 1);
+    cfg.dynamicSmemBytes = SMEM_BYTES;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[2];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    attr[1].id = cudaLaunchAttributePreferredClusterDimension;
+    attr[1].val.preferredClusterDim.x = CL;
+    attr[1].val.preferredClusterDim.y = 1;
+    attr[1].val.preferredClusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 2;
+    if (debug_enabled())
+      std::fprintf(stderr,
+                   "[flux] mode %d dtype %d: dynamic schedule, grid %d (pairs, preferred %d), units %d, "
+                   "mailbox %d per region, tiles %d x %d, k-slices %d\n",
+                   MODE, DT, grid, CL, p.num_units, p.mbox_cap, p.Mt, p.Nt, p.KT);
+    cudaError_t e = cudaLaunchKernelEx(&cfg, fused_gemm_kernel<MODE, DT, CL>, p);
+    return e == cudaSuccess ? FLUX_OK : cuda_fail(e);
+  }
+
   static flux_status_t launch(const KParams& p, int grid, cudaStream_t stream) {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(grid, 1, 1);

@@ -44,12 +44,22 @@ def test_version_and_status_strings(fx):
     assert fx.flux_status_string(99) == "FLUX_ERR_UNKNOWN"
 
 
+def _sched(units):
+    # mailboxes of the dynamic unit schedule: (2 U + 4 x 64 regions) uint32, 256-byte rounded
+    return -(-(2 * units + 256) * 4 // 256) * 256
+
+
 def test_workspace_sizes(fx):
-    assert fx.flux_workspace_size(fx.FLUX_OP_GEMM, 1, 4096, 12288, 6144) == 256
-    assert fx.flux_workspace_size(fx.FLUX_OP_AG_GEMM, 8, 4096, 49152, 12288) == 256
+    # header + schedule of the 512 x 512 units (8 m-units x 24 n-units)
+    assert fx.flux_workspace_size(fx.FLUX_OP_GEMM, 1, 4096, 12288, 6144) == 256 + _sched(8 * 24)
+    # 8 ranks x 8 m-units x 12 n-units of 6144 columns
+    assert fx.flux_workspace_size(fx.FLUX_OP_AG_GEMM, 8, 4096, 49152, 12288) == 256 + _sched(768)
     # header + counters (32 x 48 tiles x 4 quarters x 4 B) + fp32 owner chunks (M x N)
-    assert fx.flux_workspace_size(fx.FLUX_OP_GEMM_RS, 8, 4096, 12288, 49152) == \
-        256 + 32 * 48 * 16 + 4096 * 12288 * 4
+    # + schedule (8 ranks x 8 x 24 units)
+    rs = 256 + 32 * 48 * 16 + 4096 * 12288 * 4 + _sched(8 * 8 * 24)
+    assert fx.flux_workspace_size(fx.FLUX_OP_GEMM_RS, 8, 4096, 12288, 49152) == rs
+    # the MLP's workspace serves both of its calls
+    assert fx.flux_workspace_size(fx.FLUX_OP_MLP, 8, 4096, 12288, 49152) == rs
     assert fx.flux_workspace_size(fx.FLUX_OP_GEMM_RS, 0, 1, 1, 1) == 0
     assert fx.flux_workspace_size(99, 1, 1, 1, 1) == 0
     s = fx.flux_moe_workspace_size(fx.FLUX_OP_MOE_RS, 8, 4096, 4096, 14336, 8, 2)
@@ -108,7 +118,9 @@ def test_host_validation_without_gpu(fx):
         fx.FLUX_ERR_WORKSPACE
     assert _err(fx, fx.flux_gemm, 64, 64, 64, fx.FLUX_F16, FAKE, FAKE, FAKE, WS(256, FAKE + 16),
                 stream=S) == fx.FLUX_ERR_WORKSPACE
-    need = fx.flux_workspace_size(fx.FLUX_OP_GEMM_RS, 2, 64, 64, 64)
+    # the least GEMM-RS accepts: header + counters + fp32 rows (no schedule mailboxes)
+    need = 256 + 256 + 64 * 64 * 4
+    assert need < fx.flux_workspace_size(fx.FLUX_OP_GEMM_RS, 2, 64, 64, 64)
     assert _err(fx, fx.flux_gemm_rs, 2, 64, 64, 64, fx.FLUX_F16, p, p, p, WS(need - 1), stream=S) == \
         fx.FLUX_ERR_WORKSPACE
     assert _err(fx, fx.flux_gemm_rs, 2, 63, 64, 64, fx.FLUX_F16, p, p, p, WS(need), stream=S) == \

@@ -243,3 +243,59 @@ def test_argument_errors_launch_nothing():
         fx.flux_gemm_rs(2, 64, 64, 64, fx.FLUX_F16, [a] * 2, [a] * 2, [a] * 2, ws)
     with pytest.raises(fx.FluxError, match="UNSUPPORTED"):
         fx.flux_gemm(64, 64, 64, fx.FLUX_F16, a.data_ptr() + 2, a, a, ws)
+
+
+# ---------------------------------------------------------------- unit schedules
+def _static_ws_bytes(op, R, M, N, K):
+    """Workspace without the dynamic schedule's mailboxes (the static schedule runs)."""
+    if op == fx.FLUX_OP_AG_GEMM:
+        return 256
+    # header + arrival counters (4 per 128 x 256 tile) + fp32 owner rows
+    return 256 + -(-((-(-M // 128)) * (-(-N // 256)) * 16) // 256) * 256 + M * N * 4
+
+
+@pytest.mark.parametrize("num_ctas", [0, 8])
+def test_ag_gemm_dynamic_schedule_matches_static_bit_for_bit(num_ctas):
+    # 8 ranks x 4 m-units x 4 n-units = 128 units: several per region, so the
+    # regions claim repeatedly (num_ctas 8: two regions, 64+ units each)
+    c = configs.small(configs.CONFIGS["ag_mlp0"], R=8, M=2048, N=16384, K=256, dtype="bf16", seed=71)
+    xs, w_s = configs.ag_inputs(c)
+    X = [to_device(x, c.dtype) for x in xs]
+    W = [to_device(w, c.dtype) for w in w_s]
+    opts = {"num_ctas": num_ctas} if num_ctas else None
+    outs = {}
+    for name, nbytes in (("static", _static_ws_bytes(fx.FLUX_OP_AG_GEMM, c.R, c.M, c.N, c.K)),
+                         ("dynamic", fx.flux_workspace_size(fx.FLUX_OP_AG_GEMM, c.R, c.M, c.N, c.K))):
+        ws = _ws(nbytes)
+        out = [_out(c.M, c.N // c.R, c.dtype) for _ in range(c.R)]
+        for _ in range(2):  # the second call runs on the schedule the first left zeroed
+            fx.flux_ag_gemm(c.R, c.M, c.N, c.K, DT[c.dtype], X, W, out, None, ws, opts=opts)
+        _ok(ws)
+        assert torch.count_nonzero(ws).item() == 0, name
+        outs[name] = out
+    for r in range(c.R):
+        assert torch.equal(outs["static"][r].view(torch.int16), outs["dynamic"][r].view(torch.int16))
+    ref = oracle.ag_gemm(xs, w_s, c.dtype)
+    for r in (0, 5):
+        check_close(oracle.widen(from_device(outs["dynamic"][r]), c.dtype), ref[r], f"ag dyn rank {r}")
+
+
+@pytest.mark.parametrize("num_ctas", [0, 12])
+def test_gemm_rs_dynamic_schedule_integer_inputs_bit_exact(num_ctas):
+    # integer inputs: every fp32 partial and sum is exact, whatever the order of the adds
+    c = configs.small(configs.CONFIGS["rs_mlp1"], R=8, M=1024, N=4096, K=512, dist="int", seed=72)
+    As, Bs = configs.rs_inputs(c)
+    A = [to_device(a, c.dtype) for a in As]
+    B = [to_device(b, c.dtype) for b in Bs]
+    ref = oracle.gemm_rs(As, Bs, c.dtype)
+    opts = {"num_ctas": num_ctas} if num_ctas else None
+    for name, nbytes in (("static", _static_ws_bytes(fx.FLUX_OP_GEMM_RS, c.R, c.M, c.N, c.K)),
+                         ("dynamic", fx.flux_workspace_size(fx.FLUX_OP_GEMM_RS, c.R, c.M, c.N, c.K))):
+        ws = _ws(nbytes)
+        out = [_out(c.M // c.R, c.N, c.dtype) for _ in range(c.R)]
+        for _ in range(2):
+            fx.flux_gemm_rs(c.R, c.M, c.N, c.K, DT[c.dtype], A, B, out, ws, opts=opts)
+        _ok(ws)
+        for o in range(c.R):
+            assert np.array_equal(oracle.widen(from_device(out[o]), c.dtype), ref[o]), (name, o)
+        assert torch.count_nonzero(ws).item() == 0, name
