@@ -303,7 +303,9 @@ def time_plain(torch, fx, dev, M, N, K, dtype, iters=5):
     A = torch.randn(M, K, device=dev, dtype=td)
     B = torch.randn(K, N, device=dev, dtype=td) * 0.02
     C = torch.empty(M, N, device=dev, dtype=td)
-    ws = torch.zeros(64, dtype=torch.int32, device=dev)
+    # the full workspace: the own GEMM runs the dynamic unit schedule, like the fused ops
+    ws = torch.zeros(fx.flux_workspace_size(fx.FLUX_OP_GEMM, 1, M, N, K) // 4, dtype=torch.int32,
+                     device=dev)
     code = fx.FLUX_F16 if dtype == "f16" else fx.FLUX_BF16
     res = {}
     for name, fn in (("cublas", lambda: torch.matmul(A, B, out=C)),
