@@ -89,7 +89,10 @@ def dist_env():
 
 # ---------------------------------------------------------------- clocks
 class ClockSampler:
-    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+    """nvidia-smi samples (every 20 ms, timestamped) from before the warm-up to
+    after the timed region; stop() keeps the samples taken inside the timed
+    region's host wall-clock window."""
+    FIELDS = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
@@ -104,11 +107,13 @@ class ClockSampler:
             self.fh = open(self.path, "w")
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(self.idx), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
-                 "-lms", "100"], stdout=self.fh, stderr=subprocess.DEVNULL)
+                 "-lms", "20"], stdout=self.fh, stderr=subprocess.DEVNULL)
         except Exception:
             self.proc = None
 
-    def stop(self):
+    def stop(self, t0: float, t1: float):
+        """Summary of the samples taken between host wall-clock times t0 and t1."""
+        import datetime
         if self.proc is None:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
         self.proc.terminate()
@@ -117,24 +122,37 @@ class ClockSampler:
         except Exception:
             self.proc.kill()
         self.fh.close()
-        sm, smax, reasons = [], None, set()
+        sm, pw, smax, reasons, seen = [], [], None, set(), 0
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
         with open(self.path) as f:
             for line in f:
                 parts = [p.strip() for p in line.split(",")]
-                if len(parts) < 9:
+                if len(parts) < 10:
                     continue
                 try:
-                    sm.append(float(parts[1]))
-                    smax = float(parts[2])
+                    ts = datetime.datetime.strptime(parts[0], "%Y/%m/%d %H:%M:%S.%f").timestamp()
+                    mhz, mx = float(parts[2]), float(parts[3])
                 except ValueError:
                     continue
-                for n, v in zip(names, parts[5:9]):
+                seen += 1
+                if not t0 <= ts <= t1:
+                    continue
+                sm.append(mhz)
+                smax = mx
+                try:
+                    pw.append(float(parts[4]))
+                except ValueError:
+                    pass
+                for n, v in zip(names, parts[6:10]):
                     if v.lower() == "active":
                         reasons.add(n)
-        under = [s for s in sm if smax and s > 0.5 * smax] or sm
-        return {"sm_mhz": statistics.median(under) if under else None, "sm_max_mhz": smax,
-                "reasons": sorted(reasons), "samples": len(sm)}
+        out = {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": smax,
+               "reasons": sorted(reasons), "samples": len(sm),
+               "power_w_median": statistics.median(pw) if pw else None,
+               "window_s": round(t1 - t0, 3)}
+        if not sm:
+            out["note"] = f"no sample inside the timed region ({seen} in the whole run)"
+        return out
 
 
 # ---------------------------------------------------------------- our arm
@@ -297,8 +315,10 @@ class Step:
         return sum(self.flops[o] for o in self.ops)
 
 
-def time_plain(torch, fx, dev, M, N, K, dtype, iters=5):
-    """min(cuBLAS, own tcgen05 plain GEMM) time in ms for C[M x N] = A[M x K] B[K x N]."""
+def time_plain(torch, fx, dev, M, N, K, dtype, seconds=0.6):
+    """min(cuBLAS, own tcgen05 plain GEMM) time in ms for C[M x N] = A[M x K] B[K x N],
+    each measured like the fused ops inside the step: back to back for about
+    `seconds` (clocks settle under the power cap), median of the second half."""
     td = torch.float16 if dtype == "f16" else torch.bfloat16
     A = torch.randn(M, K, device=dev, dtype=td)
     B = torch.randn(K, N, device=dev, dtype=td) * 0.02
@@ -313,15 +333,21 @@ def time_plain(torch, fx, dev, M, N, K, dtype, iters=5):
         for _ in range(2):
             fn()
         torch.cuda.synchronize()
-        ts = []
-        for _ in range(iters):
-            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            e0.record()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        fn()
+        e1.record()
+        torch.cuda.synchronize()
+        n = max(6, min(400, int(seconds * 1e3 / max(e0.elapsed_time(e1), 1e-3))))
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in range(n)]
+        for a, b in evs:
+            a.record()
             fn()
-            e1.record()
-            torch.cuda.synchronize()
-            ts.append(e0.elapsed_time(e1))
-        res[name] = min(ts)
+            b.record()
+        torch.cuda.synchronize()
+        ts = sorted(a.elapsed_time(b) for a, b in evs[n // 2:])
+        res[name] = ts[len(ts) // 2]
     del A, B, C
     torch.cuda.empty_cache()
     return res
@@ -341,6 +367,8 @@ def run_ours(args):
 
     st = Step(torch, fx, dev, small=args.small, ops=args.ops.split(",") if args.ops else None)
     tuned = st.tune() if args.tune else None
+    clocks = ClockSampler(local)
+    clocks.start()
     for _ in range(args.warmup):
         st.step()
     torch.cuda.synchronize()
@@ -350,14 +378,12 @@ def run_ours(args):
     events = {o: (torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
               for o in st.ops}
     per_op = {o: 0.0 for o in st.ops}
-    clocks = ClockSampler(local)
-    clocks.start()
-    time.sleep(0.3)
     if ws_ > 1:
         torch.distributed.barrier()
     torch.cuda.synchronize()
     t_start = torch.cuda.Event(enable_timing=True)
     t_end = torch.cuda.Event(enable_timing=True)
+    wall0 = time.time()
     t_start.record()
     per_step_events = []
     for _ in range(args.steps):
@@ -367,9 +393,11 @@ def run_ours(args):
         per_step_events.append(ev)
     t_end.record()
     torch.cuda.synchronize()
+    wall1 = time.time()
     if ws_ > 1:
         torch.distributed.barrier()
-    clk = clocks.stop()
+    time.sleep(0.1)  # the sampler's last lines cover the end of the window
+    clk = clocks.stop(wall0, wall1)
     ms_total = t_start.elapsed_time(t_end)
     for ev in per_step_events:
         for o in st.ops:
@@ -632,8 +660,9 @@ def run_reference(args):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
-    ap.add_argument("--warmup", type=int, default=5)
+    # defaults: a timed region of about one second (sustained clocks and power)
+    ap.add_argument("--steps", type=int, default=120)
+    ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--small", action="store_true", help="reduced sizes (profiling captures)")
     ap.add_argument("--ops", default="", help="comma list of ops to run (default: the whole step)")
