@@ -120,7 +120,8 @@ typedef struct {
                       4 accumulator free, 5 accumulator full, 6 drain,
                       7 deterministic GEMM-RS turn, 8 staged MoE rows of an m-tile,
                       9 next unit of the dynamic schedule (dense ops), 10 a cluster
-                      of an unexpected shape under the dynamic schedule */
+                      of an unexpected shape under the dynamic schedule, 11 MoE
+                      layer1's grid barrier before the token rows are converted */
   uint32_t arg0;   /* flag wait: shard index; pipeline waits: CTA index */
   uint32_t arg1;   /* flag wait: last flag value seen; pipeline waits: stage / buffer */
 } flux_device_report_t;
@@ -318,8 +319,12 @@ flux_status_t flux_moe_ag_grouped_gemm(int R, int T, int H, int F, int E, int to
  *                 (from flux_moe_route or layer0), or all three NULL to have
  *                 this call recompute them in its workspace
  *   out[o]        device, [T/R x H]
- * Contributions are accumulated in fp32 in the workspace; the last of the
- * R*topk contributions to a token row converts it to 16 bits.
+ * Contributions are accumulated in fp32 in the workspace (gate-weighted adds
+ * in each tile's epilogue); when every tile is done, the CTAs of the launch
+ * meet at a grid-wide barrier (the launch is sized so that all of them are
+ * resident at once; a kernel of another stream that holds SMs the whole time
+ * can delay it until timeout_ns, FLUX_ERR_TIMEOUT at wait site 11) and each
+ * converts a share of the token rows to 16 bits.
  * Requires T and F divisible by R, (F/R) % 8 == 0, H % 8 == 0. */
 flux_status_t flux_moe_grouped_gemm_rs(int R, int T, int H, int F, int E, int topk,
                                        flux_dtype_t dtype, const void* const* h_shards,

@@ -16,7 +16,8 @@
 //                                    (GEMM + ReduceScatter)
 //                       MOE_GATHER   STORE with A rows gathered by expert (MoE layer0)
 //                       MOE_SCATTER  gate-weighted fp32 add into the owning token row;
-//                                    the last of R*topk contributions converts (MoE layer1)
+//                                    after a grid-wide barrier every CTA converts a
+//                                    share of the token rows (MoE layer1)
 //                       MOE_STAGED   STORE for MoE layer0 whose A rows were first
 //                                    gathered into a grouped staging buffer by every
 //                                    CTA of the same launch (per-tile ready counters)
@@ -166,8 +167,13 @@ constexpr int STAGE_UNROLL = 16;  // MOE_STAGED: 16-byte loads in flight per lan
 
 // device status header at the start of every workspace (256 bytes)
 // H_CLAIM / H_EXIT: dynamic schedule's unit counter and count of finished
-// CTAs (the last CTA out zeroes both and the mailboxes).
-enum HdrField { H_STATUS = 0, H_WHERE = 1, H_ARG0 = 2, H_ARG1 = 3, H_ABORT = 4, H_CLAIM = 8, H_EXIT = 9 };
+// CTAs (the last CTA out zeroes both and the mailboxes).  H_GRID /
+// H_GRID_EXIT: MoE layer1's grid barrier before the row conversion and its
+// exit count (the last CTA out zeroes both).
+enum HdrField {
+  H_STATUS = 0, H_WHERE = 1, H_ARG0 = 2, H_ARG1 = 3, H_ABORT = 4,
+  H_CLAIM = 8, H_EXIT = 9, H_GRID = 10, H_GRID_EXIT = 11
+};
 enum WaitSite {
   W_FLAG = 1,
   W_EMPTY = 2,
@@ -178,7 +184,8 @@ enum WaitSite {
   W_TURN = 7,
   W_STAGE = 8,
   W_SCHED = 9,  // dynamic schedule: the region's next unit
-  W_SHAPE = 10  // dynamic schedule: a cluster of an unexpected size or CTA order
+  W_SHAPE = 10, // dynamic schedule: a cluster of an unexpected size or CTA order
+  W_GRID = 11   // MoE layer1: every CTA's adds in before the rows are converted
 };
 constexpr uint32_t ST_TIMEOUT = 5;
 constexpr uint32_t ST_INVALID = 1;
@@ -208,7 +215,7 @@ struct KParams {
   uint32_t seq;            // per-call id, written to the abort word on error
   uint64_t timeout_ns;
   uint32_t* hdr;           // workspace header
-  uint32_t* counters;      // REDUCE / MOE_SCATTER arrival counters
+  uint32_t* counters;      // REDUCE arrival counters
   float* acc;              // REDUCE / MOE_SCATTER fp32 accumulation rows
   // MoE routing (device arrays)
   const int32_t* offsets;      // [E+1]
@@ -1152,32 +1159,75 @@ __device__ void epilogue(const KParams& p, const Smem& s, const Ctl& c, uint32_t
         }
         if (lane == 0) atomicExch(cnt, 0u);
       }
-    } else if (MODE == MODE_MOE_SCATTER) {
-      // a row's adds were issued by eight lanes of the warp: every lane fences
-      // its own, and the warp barrier orders them all before the row's count
-      __threadfence();
-      __syncwarp();
-      uint32_t* cnt = p.counters + (static_cast<size_t>(tok) * p.Nt + w.nt);
-      bool last = false;
-      if (row_ok) {
-        const uint32_t old = atomicAdd(cnt, 1u);
-        // every (token, k) adds once per rank of its expert's group
-        last = (old + 1u == static_cast<uint32_t>(p.moe_tp * p.topk));
+    }
+  }
+}
+
+// MoE layer1, after every role of this CTA is done: the CTAs of the launch
+// meet at a grid-wide barrier (the launch is sized so that all of them are
+// resident at once; the wait is bounded), which makes every gate-weighted add
+// of the call visible; then each CTA converts a share of the fp32 token rows
+// to 16 bits into the owner ranks' outputs and zeroes them for the next call.
+// The last CTA out resets the barrier's counters.  `flag` is a shared word.
+template <int DT>
+__device__ void finish_token_rows(const KParams& p, const Ctl& c, uint32_t* flag) {
+  __threadfence();  // this thread's adds, before the CTA's arrival
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    __threadfence();
+    atomicAdd(p.hdr + H_GRID, 1u);
+    *flag = wait_count(p.hdr + H_GRID, gridDim.x, c, W_GRID) ? 1u : 0u;
+  }
+  __syncthreads();
+  if (*flag != 0u) {
+    // 8 columns per chunk; a thread takes FIN_BATCH chunks a grid-stride
+    // apart per round and issues all their loads before any store
+    constexpr int FIN_BATCH = 4;
+    const int chunks = p.H / 8;
+    const long long total = static_cast<long long>(p.T) * chunks;
+    const long long step = static_cast<long long>(gridDim.x) * blockDim.x;
+    const float4 zero = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (long long i0 = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; i0 < total;
+         i0 += step * FIN_BATCH) {
+      float4 a[FIN_BATCH], b[FIN_BATCH];
+#pragma unroll
+      for (int j = 0; j < FIN_BATCH; ++j) {
+        const long long i = i0 + j * step;
+        if (i < total) {
+          const int t = static_cast<int>(i / chunks);
+          const float* src = p.acc + static_cast<long long>(t) * p.N + (i - static_cast<long long>(t) * chunks) * 8;
+          a[j] = ld_cg_f4(src);
+          b[j] = ld_cg_f4(src + 4);
+        }
       }
-      uint32_t lmask = __ballot_sync(0xFFFFFFFFu, last);
-      if (lmask) __threadfence();
-      while (lmask) {
-        const int src = __ffs(lmask) - 1;
-        lmask &= lmask - 1;
-        const int t = __shfl_sync(0xFFFFFFFFu, tok, src);
-        const int o = t / p.rows_per_rank;
-        const int lt = t - o * p.rows_per_rank;
-        const int col = n0 + lane * 8;
-        if (col < p.N)
-          convert8<DT>(p.acc + static_cast<long long>(t) * p.N + col,
-                       static_cast<uint16_t*>(p.out[o]) + static_cast<long long>(lt) * p.ldo + col);
-        if (lane == src) atomicExch(p.counters + (static_cast<size_t>(t) * p.Nt + w.nt), 0u);
+#pragma unroll
+      for (int j = 0; j < FIN_BATCH; ++j) {
+        const long long i = i0 + j * step;
+        if (i < total) {
+          const int t = static_cast<int>(i / chunks);
+          const int col = static_cast<int>(i - static_cast<long long>(t) * chunks) * 8;
+          const int o = t / p.rows_per_rank;
+          const int lt = t - o * p.rows_per_rank;
+          uint4 q;
+          q.x = pack2<DT>(a[j].x, a[j].y);
+          q.y = pack2<DT>(a[j].z, a[j].w);
+          q.z = pack2<DT>(b[j].x, b[j].y);
+          q.w = pack2<DT>(b[j].z, b[j].w);
+          *reinterpret_cast<uint4*>(static_cast<uint16_t*>(p.out[o]) + static_cast<long long>(lt) * p.ldo + col) = q;
+          float* src = p.acc + static_cast<long long>(t) * p.N + col;
+          st_cg_f4(src, zero);
+          st_cg_f4(src + 4, zero);
+        }
       }
+    }
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    __threadfence();
+    if (atomicAdd(p.hdr + H_GRID_EXIT, 1u) + 1u == gridDim.x) {
+      // every CTA has passed the barrier and converted its rows
+      p.hdr[H_GRID] = 0u;
+      p.hdr[H_GRID_EXIT] = 0u;
     }
   }
 }
@@ -1381,6 +1431,7 @@ fused_gemm_kernel(const __grid_constant__ KParams p) {
     if (PAIR == 2) tmem_dealloc2(tmem_base, TMEM_COLS);
     else tmem_dealloc(tmem_base, TMEM_COLS);
   }
+  if constexpr (MODE == MODE_MOE_SCATTER) finish_token_rows<DT>(p, c, s.misc + 1);
   if (dyn) {
     // The last CTA to finish clears the schedule (counter, exit count and
     // mailboxes) so that the workspace is zero again for the next call.  Every

@@ -304,7 +304,7 @@ size_t a256(size_t v) { return round_up(v, WS_ALIGN); }
 // MOE_LAYERS), so that the one-call layer finds each part where the single
 // calls put it
 struct MoeWs {
-  size_t tile_off, counts, offsets, s2r, r2s, counters, acc, unit_cnt, stage, total;
+  size_t tile_off, counts, offsets, s2r, r2s, acc, unit_cnt, stage, total;
 };
 
 MoeWs moe_layout(flux_op_t op, int R, int T, int H, int F, int E, int topk) {
@@ -325,9 +325,6 @@ MoeWs moe_layout(flux_op_t op, int R, int T, int H, int F, int E, int topk) {
     o += a256(n * sizeof(int32_t));
     w.r2s = o;
     o += a256(n * sizeof(int32_t));
-    const size_t Nt = (static_cast<size_t>(H) + BN - 1) / BN;
-    w.counters = o;
-    o += a256(static_cast<size_t>(T) * Nt * sizeof(uint32_t));
     w.acc = o;
     o += a256(static_cast<size_t>(T) * H * sizeof(float));
   }
@@ -609,7 +606,6 @@ flux_status_t moe_layer1_impl(
   p.topk = topk;
   p.T = T;
   p.H = H;
-  p.counters = reinterpret_cast<uint32_t*>(ws + L.counters);
   p.acc = reinterpret_cast<float*>(ws + L.acc);
   p.timeout_ns = (opts && opts->timeout_ns) ? opts->timeout_ns : DEFAULT_TIMEOUT_NS;
   p.epoch = (opts && opts->epoch) ? opts->epoch : 1u;

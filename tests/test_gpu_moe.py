@@ -251,10 +251,11 @@ def test_layer1_matches_oracle(R, T, H, F, E, topk, dtype, given):
     ref = oracle.moe_layer1(d["h_shards"], d["w2_shards"], d["topk_ids"], d["topk_weights"], E, dtype)
     for o in range(R):
         check_close(oracle.widen(from_device(out[o]), dtype), ref[o], f"layer1 owner {o}")
-    # the arrival counters and fp32 accumulators (the tail of the workspace) are left at zero
-    nt = (H + 255) // 256
-    tail = (-(-T * nt * 4 // 256) * 256 + -(-T * H * 4 // 256) * 256) // 4
+    # the fp32 token rows (the tail of the workspace) and the header, which holds the
+    # grid barrier's counters, are left at zero
+    tail = -(-T * H * 4 // 256) * 256 // 4
     assert torch.count_nonzero(ws[-tail:]).item() == 0
+    assert torch.count_nonzero(ws[:64]).item() == 0
 
 
 def test_layer0_then_layer1_chained():
