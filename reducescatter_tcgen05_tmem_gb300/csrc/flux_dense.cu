@@ -35,6 +35,9 @@ flux_status_t launch_dyn_dt(flux_dtype_t dt, const KParams& p, int grid, cudaStr
 // Dense whole-tile kernels run on clusters of two CTA pairs stacked along M
 // (512 x 512 per cluster, B multicast between the pairs).
 constexpr int DENSE_CL = 4;
+// GEMM-RS of few rows: clusters of 4 CTAs reduce the R partials of a tile
+// through distributed shared memory (each CTA computes R / 4 partials)
+constexpr int RS_CLUSTER_CL = 4;
 using DenseUnit = Unit<MODE_STORE, DENSE_CL>;
 using DenseGeo = DenseUnit::G;
 
@@ -303,6 +306,21 @@ extern "C" flux_status_t flux_gemm_rs(int R, int M, int N, int K, flux_dtype_t d
   // deterministic_rs: whole tiles (no k split), each rank's partial of a tile
   // on consecutive units (tile-major), added in ascending rank order
   p.deterministic = (opts && opts->deterministic_rs) ? 1 : 0;
+  // At most 128 rows and 4 or 8 ranks, every 256-column tile on a resident
+  // cluster of 4 CTAs (no grid given): the cluster computes the tile's R
+  // partials and reduces them through distributed shared memory into the
+  // owners' rows -- no fp32 workspace traffic, no atomics.
+  if (!p.deterministic && !(opts && opts->num_ctas > 0) && M <= BM && (R == 4 || R == 8)) {
+    const int nt = (N + BN - 1) / BN;
+    const int cap = grid_dt<MODE_RS_CLUSTER, RS_CLUSTER_CL>(dtype, dev, nullptr, 1LL << 30);
+    if (cap > 0 && nt * RS_CLUSTER_CL <= cap) {
+      p.Mt = 1;
+      p.Nt = nt;
+      p.num_units = nt;
+      p.stream_k = 0;
+      return launch_dt<MODE_RS_CLUSTER, RS_CLUSTER_CL>(dtype, p, nt * RS_CLUSTER_CL, s);
+    }
+  }
   if (rs_uses_stream_k(R, M, N, sm, p.deterministic != 0)) {
     p.Nt = (N + BN - 1) / BN;
     p.Mt = (M + BM - 1) / BM;

@@ -21,6 +21,12 @@
 //                       MOE_STAGED   STORE for MoE layer0 whose A rows were first
 //                                    gathered into a grouped staging buffer by every
 //                                    CTA of the same launch (per-tile ready counters)
+//                       RS_CLUSTER   GEMM + ReduceScatter of few rows (M <= 128, the
+//                                    decode shapes): a cluster of 4 CTAs computes all
+//                                    R partials of one 128 x 256 tile (R / 4 each, in
+//                                    separate accumulators), then reduces them through
+//                                    distributed shared memory, each CTA into the rows
+//                                    of the owner ranks it serves (no fp32 workspace)
 //
 // PAIR = 1: one CTA computes a 128 x 256 tile with tcgen05.mma.cta_group::1
 //           (4-stage ring of 48 KB: A 128x64 + B 64x256); two 256-column
@@ -157,7 +163,8 @@ enum Mode {
   MODE_REDUCE = 1,
   MODE_MOE_GATHER = 2,
   MODE_MOE_SCATTER = 3,
-  MODE_MOE_STAGED = 4
+  MODE_MOE_STAGED = 4,
+  MODE_RS_CLUSTER = 5
 };
 __host__ __device__ constexpr bool is_moe(int mode) {
   return mode == MODE_MOE_GATHER || mode == MODE_MOE_SCATTER || mode == MODE_MOE_STAGED;
@@ -185,7 +192,8 @@ enum WaitSite {
   W_STAGE = 8,
   W_SCHED = 9,  // dynamic schedule: the region's next unit
   W_SHAPE = 10, // dynamic schedule: a cluster of an unexpected size or CTA order
-  W_GRID = 11   // MoE layer1: every CTA's adds in before the rows are converted
+  W_GRID = 11,  // MoE layer1: every CTA's adds in before the rows are converted
+  W_XCHG = 12   // cluster ReduceScatter: peers' rings free / partial rows received
 };
 constexpr uint32_t ST_TIMEOUT = 5;
 constexpr uint32_t ST_INVALID = 1;
@@ -402,9 +410,10 @@ struct Work {
 template <int MODE, int CL>
 struct Unit {
   static constexpr bool DENSE = MODE == MODE_STORE || MODE == MODE_REDUCE;
-  static constexpr int PAIR = CL >= 2 ? 2 : 1;
+  // RS_CLUSTER: every CTA of the cluster runs its own 128 x 256 tiles
+  static constexpr int PAIR = (CL >= 2 && MODE != MODE_RS_CLUSTER) ? 2 : 1;
   static constexpr int NM = ((DENSE || MODE == MODE_MOE_STAGED) && PAIR == 2) ? 2 : 1;
-  static constexpr int MC = CL / PAIR;
+  static constexpr int MC = MODE == MODE_RS_CLUSTER ? 1 : CL / PAIR;
   static constexpr int ROWS = BM * CL;
   using G = Geo<PAIR, NM>;
   static_assert(DENSE || MC == 1, "MoE tiles: no B sharing between pairs");
@@ -571,6 +580,22 @@ struct ItemIter {
   }
 
   __device__ bool next(Work& w) {
+    if (MODE == MODE_RS_CLUSTER) {
+      // the cluster's n-tile u; this CTA's ranks cta, cta + CL, ...
+      const int r = cta + taken * CL;
+      if (u >= p.Nt || r >= p.R) return false;
+      ++taken;
+      w.r = r;
+      w.mt = 0;
+      w.nt = u;
+      w.m0 = 0;
+      w.row_end = p.M;
+      w.e = 0;
+      w.k0 = 0;
+      w.k1 = p.KT;
+      w.tile = 0;
+      return true;
+    }
     if (DYN_OK && dyn) {
       uint32_t v = 0;
       if (!warp_uniform || (threadIdx.x & 31) == 0) {
@@ -641,6 +666,7 @@ struct Smem {
   uint64_t* drain;  // [1]
   uint32_t* tmem_slot;
   uint32_t* misc;   // [2] dynamic schedule: cluster-shape check, last CTA out
+  uint64_t* xbar;   // [2] RS_CLUSTER: peers' rings free, partial rows received
   uint8_t* stg;     // EPI_WARPS x STG_WARP epilogue staging (1024-byte aligned)
 };
 
@@ -1163,6 +1189,115 @@ __device__ void epilogue(const KParams& p, const Smem& s, const Ctl& c, uint32_t
   }
 }
 
+// RS_CLUSTER epilogue (the EPI_WARPS epilogue warps of every CTA).  The tile's
+// rows are the M <= 128 activation rows; owner rank o holds rows
+// [o M/R, (o+1) M/R), and CTA d of the cluster reduces the owners d, d + CL,
+// ... (M / CL rows).  Each CTA holds one fp32 accumulator per rank it
+// computed (ranks cta, cta + CL, ...).
+//   1. once its accumulators are complete, its MMAs are done and its operand
+//      ring is free: it tells every CTA of the cluster (xbar[0], CL arrivals);
+//   2. when every ring is free, each thread (one row) adds its row of the
+//      accumulators and writes it into slot `cta` of the ring of the CTA that
+//      reduces the row's owner (st.shared::cluster), then arrives there
+//      (xbar[1], M arrivals per CTA, release at cluster scope);
+//   3. when its M rows are in, the CTA adds the CL slots in slot order,
+//      converts to 16 bits and stores its owners' rows.
+// Exchange layout in each ring: slot c (0 .. CL-1) of M / CL rows x 256 fp32.
+template <int DT, int CL>
+__device__ void epilogue_rs_cluster(const KParams& p, const Smem& s, const Ctl& c, uint32_t tmem_base,
+                                    int warp, const Pos& ps) {
+  using G = typename Unit<MODE_RS_CLUSTER, CL>::G;
+  constexpr int ROWB = BN * 4;  // bytes of one fp32 row of the tile
+  const int lane = threadIdx.x & 31;
+  const int q = warp & 3;  // TMEM lane quarter: rows 32q .. 32q + 31
+  const int cta = ps.vrank;
+  const int nacc = (p.R - cta + CL - 1) / CL;  // accumulators of this CTA
+  const int rows_o = p.M / p.R;                // rows per owner rank
+  const int rows_d = p.M / CL;                 // rows each CTA reduces
+  const uint32_t ring = smem_u32(s.a);
+  const uint32_t xfree = smem_u32(&s.xbar[0]), xrows = smem_u32(&s.xbar[1]);
+  const int n0 = static_cast<int>(blockIdx.x / CL) * BN;
+
+  // 1. this CTA's partials are complete (each accumulator is used once)
+  int ok = 1;
+  if (lane == 0) {
+    for (int b = 0; b < nacc && ok; ++b)
+      if (wait_bar(smem_u32(&s.tfull[b]), 0u, c, W_TFULL, static_cast<uint32_t>(b)) != 0) ok = 0;
+  }
+  ok = __shfl_sync(0xFFFFFFFFu, ok, 0);
+  if (!ok) return;  // recorded; the peers' bounded waits see the abort
+  tc_fence_after();
+  if (q == 0 && lane == 0)
+    for (int d = 0; d < CL; ++d) mbar_arrive_remote(mapa_shared(xfree, static_cast<uint32_t>(d)));
+
+  // 2. every ring of the cluster is free: send each row to its reducer
+  if (lane == 0) ok = wait_bar_remote(xfree, 0u, c, W_XCHG, 0u) == 0 ? 1 : 0;
+  ok = __shfl_sync(0xFFFFFFFFu, ok, 0);
+  if (!ok) return;
+  const int row = q * 32 + lane;
+  const bool valid = row < p.M;
+  uint32_t dst = 0;
+  int dcta = 0;
+  if (valid) {
+    const int o = row / rows_o;
+    dcta = o % CL;
+    const int lr = (o / CL) * rows_o + (row - o * rows_o);
+    dst = mapa_shared(ring + static_cast<uint32_t>((cta * rows_d + lr) * ROWB), static_cast<uint32_t>(dcta));
+  }
+  const uint32_t taddr = tmem_base + (static_cast<uint32_t>(q * 32) << 16);
+  for (int ch = 0; ch < BN / 32; ++ch) {
+    uint32_t v[32];
+    tmem_ld_32x32b_x32(taddr + ch * 32, v);  // warp-collective: every lane, valid row or not
+    if (nacc > 1) {
+      uint32_t u[32];
+      tmem_ld_32x32b_x32(taddr + G::ACC_COLS + ch * 32, u);
+#pragma unroll
+      for (int i = 0; i < 32; ++i) v[i] = __float_as_uint(__uint_as_float(v[i]) + __uint_as_float(u[i]));
+    }
+    if (valid) {
+#pragma unroll
+      for (int g = 0; g < 8; ++g)
+        st_shared_cluster_f4(dst + ch * 128 + g * 16, __uint_as_float(v[4 * g]), __uint_as_float(v[4 * g + 1]),
+                             __uint_as_float(v[4 * g + 2]), __uint_as_float(v[4 * g + 3]));
+    }
+  }
+  if (valid) mbar_arrive_remote(mapa_shared(xrows, static_cast<uint32_t>(dcta)));
+
+  // 3. this CTA's rows from every CTA of the cluster: add, convert, store
+  if (lane == 0) ok = wait_bar_remote(xrows, 0u, c, W_XCHG, 1u) == 0 ? 1 : 0;
+  ok = __shfl_sync(0xFFFFFFFFu, ok, 0);
+  if (!ok) return;
+  fence_acq_rel_cluster();
+  const int tid = q * 32 + lane;  // 0 .. 127
+  // items: (row lr, 8-column group g); a warp covers one row's 32 groups
+  for (int item = tid; item < rows_d * (BN / 8); item += EPI_WARPS * 32) {
+    const int lr = item / (BN / 8), g = item % (BN / 8);
+    const int col = n0 + g * 8;
+    float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+    for (int sc = 0; sc < CL; ++sc) {
+      const uint32_t a = ring + static_cast<uint32_t>((sc * rows_d + lr) * ROWB + g * 32);
+      float x[8];
+      asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];"
+                   : "=f"(x[0]), "=f"(x[1]), "=f"(x[2]), "=f"(x[3]) : "r"(a) : "memory");
+      asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];"
+                   : "=f"(x[4]), "=f"(x[5]), "=f"(x[6]), "=f"(x[7]) : "r"(a + 16) : "memory");
+#pragma unroll
+      for (int i = 0; i < 8; ++i) acc[i] += x[i];
+    }
+    if (col < p.N) {
+      const int o = cta + (lr / rows_o) * CL;
+      const int orow = lr - (lr / rows_o) * rows_o;
+      uint4 qv;
+      qv.x = pack2<DT>(acc[0], acc[1]);
+      qv.y = pack2<DT>(acc[2], acc[3]);
+      qv.z = pack2<DT>(acc[4], acc[5]);
+      qv.w = pack2<DT>(acc[6], acc[7]);
+      *reinterpret_cast<uint4*>(static_cast<uint16_t*>(p.out[o]) + static_cast<long long>(orow) * p.ldo + col) = qv;
+    }
+  }
+}
+
 // MoE layer1, after every role of this CTA is done: the CTAs of the launch
 // meet at a grid-wide barrier (the launch is sized so that all of them are
 // resident at once; the wait is bounded), which makes every gate-weighted add
@@ -1338,6 +1473,7 @@ fused_gemm_kernel(const __grid_constant__ KParams p) {
   s.drain = bars + 2 * G::STAGES + 4;
   s.tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * G::STAGES + 5);
   s.misc = s.tmem_slot + 1;
+  s.xbar = bars + 2 * G::STAGES + 7;
 
   const int warp = threadIdx.x >> 5;
   const bool dyn = ItemIter<MODE, CL>::DYN_OK && p.dyn != 0;
@@ -1371,6 +1507,10 @@ fused_gemm_kernel(const __grid_constant__ KParams p) {
       mbar_init(smem_u32(&s.tempty[i]), EPI_WARPS * PAIR);
     }
     mbar_init(smem_u32(s.drain), 1);
+    if (MODE == MODE_RS_CLUSTER) {
+      mbar_init(smem_u32(&s.xbar[0]), CL);                          // rings free
+      mbar_init(smem_u32(&s.xbar[1]), static_cast<uint32_t>(p.M));  // rows received
+    }
     fence_mbar_init();
   }
   if (warp == KS::MMA_WARP) {
@@ -1419,6 +1559,8 @@ fused_gemm_kernel(const __grid_constant__ KParams p) {
     // the even CTA of a pair issues the MMAs for both
     if (lane == 0 && cta == 0) mma_issuer<MODE, DT, CL>(p, s, c, tmem_base, total_mt, ps);
     __syncwarp();
+  } else if constexpr (MODE == MODE_RS_CLUSTER) {
+    epilogue_rs_cluster<DT, CL>(p, s, c, tmem_base, warp, ps);
   } else {
     epilogue<MODE, DT, CL>(p, s, c, tmem_base, total_mt, warp, ps);
   }

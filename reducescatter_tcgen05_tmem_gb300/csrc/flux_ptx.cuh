@@ -72,6 +72,18 @@ __device__ __forceinline__ uint32_t ld_shared_cluster_u32(uint32_t cluster_addr)
   asm volatile("ld.shared::cluster.u32 %0, [%1];" : "=r"(v) : "r"(cluster_addr) : "memory");
   return v;
 }
+// 16-byte store into the shared memory of a CTA of the cluster (address from mapa)
+__device__ __forceinline__ void st_shared_cluster_f4(uint32_t cluster_addr, float a, float b, float c,
+                                                     float d) {
+  asm volatile("st.shared::cluster.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(cluster_addr), "f"(a),
+               "f"(b), "f"(c), "f"(d)
+               : "memory");
+}
+// acquire at cluster scope: shared-memory writes of other CTAs of the cluster
+// that were released before a barrier phase this thread observed are visible
+__device__ __forceinline__ void fence_acq_rel_cluster() {
+  asm volatile("fence.acq_rel.cluster;" ::: "memory");
+}
 // shared::cluster address of the variable at shared::cta address `a` in CTA `rank`
 __device__ __forceinline__ uint32_t mapa_shared(uint32_t a, uint32_t rank) {
   uint32_t r;

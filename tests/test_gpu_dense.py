@@ -299,3 +299,40 @@ def test_gemm_rs_dynamic_schedule_integer_inputs_bit_exact(num_ctas):
         for o in range(c.R):
             assert np.array_equal(oracle.widen(from_device(out[o]), c.dtype), ref[o]), (name, o)
         assert torch.count_nonzero(ws).item() == 0, name
+
+
+# ---------------------------------------------------------------- cluster ReduceScatter (few rows)
+@pytest.mark.parametrize("R,M,N,K,dtype", [
+    (8, 128, 2048, 4096, "bf16"),   # decode-like: 8 n-tiles on 8 clusters, 2 partials per CTA
+    (4, 128, 1000, 2048, "f16"),    # ragged last n-tile (1000 = 3 x 256 + 232)
+    (8, 40, 264, 576, "f16"),       # 5 rows per owner, ragged k tail (72 per rank)
+    (4, 64, 4096, 1024, "bf16"),    # 16 clusters, rows 64..127 of each tile empty
+    (8, 16, 512, 256, "bf16"),      # 2 rows per owner, one k-slice per rank
+])
+def test_gemm_rs_cluster_form_matches_oracle(R, M, N, K, dtype):
+    c = configs.small(configs.CONFIGS["rs_decode"], R=R, M=M, N=N, K=K, dtype=dtype, seed=90 + R)
+    As, Bs, out, ws = _rs_case(c)
+    _ok(ws)
+    ref = oracle.gemm_rs(As, Bs, dtype)
+    for o in range(R):
+        check_close(oracle.widen(from_device(out[o]), dtype), ref[o], f"cluster rs owner {o}")
+
+
+@pytest.mark.parametrize("R", [4, 8])
+def test_gemm_rs_cluster_form_integer_inputs_bit_exact_and_repeatable(R):
+    # exact fp32 partials and sums; the slot order is fixed, so repeat calls give the same bits
+    # |entries| <= 2, 64 products per rank: every sum is an integer below 2049, exact in f16
+    c = configs.small(configs.CONFIGS["rs_decode"], R=R, M=128, N=1536, K=R * 64, dist="int",
+                      dtype="f16", seed=95 + R)
+    As, Bs, out, ws = _rs_case(c, calls=2)
+    _ok(ws)
+    ref = oracle.gemm_rs(As, Bs, c.dtype)
+    for o in range(R):
+        assert np.array_equal(oracle.widen(from_device(out[o]), c.dtype), ref[o]), o
+    first = [o.clone() for o in out]
+    fx.flux_gemm_rs(c.R, c.M, c.N, c.K, DT[c.dtype], [to_device(a, c.dtype) for a in As],
+                    [to_device(b, c.dtype) for b in Bs], out, ws)
+    _ok(ws)
+    for o in range(R):
+        assert torch.equal(first[o].view(torch.int16), out[o].view(torch.int16))
+    assert torch.count_nonzero(ws).item() == 0
