@@ -121,7 +121,9 @@ typedef struct {
                       7 deterministic GEMM-RS turn, 8 staged MoE rows of an m-tile,
                       9 next unit of the dynamic schedule (dense ops), 10 a cluster
                       of an unexpected shape under the dynamic schedule, 11 MoE
-                      layer1's grid barrier before the token rows are converted */
+                      layer1's grid barrier before the token rows are converted,
+                      12 the exchange of a cluster ReduceScatter (GEMM-RS of few
+                      rows) */
   uint32_t arg0;   /* flag wait: shard index; pipeline waits: CTA index */
   uint32_t arg1;   /* flag wait: last flag value seen; pipeline waits: stage / buffer */
 } flux_device_report_t;
@@ -208,8 +210,12 @@ flux_status_t flux_ag_gemm(int R, int M, int N, int K, flux_dtype_t dtype,
  *   out[o]       device, [M/R x N]: owner rank o's row chunk of the reduced product
  * Every rank's partial tile is accumulated in fp32 into the owner's chunk of
  * the workspace; the last partial to arrive converts the tile to 16 bits and
- * stores it in out[owner].  Requires M and K divisible by R, (K/R) % 8 == 0,
- * N % 8 == 0. */
+ * stores it in out[owner].  Few rows (M <= 128, R = 4 or 8, no num_ctas or
+ * deterministic_rs option, every 256-column tile on a resident 4-CTA
+ * cluster): a cluster of 4 CTAs computes the R partials of a tile and reduces
+ * them through distributed shared memory instead, summing in a fixed order
+ * (repeat calls give the same bits) without touching the workspace's
+ * accumulators.  Requires M and K divisible by R, (K/R) % 8 == 0, N % 8 == 0. */
 flux_status_t flux_gemm_rs(int R, int M, int N, int K, flux_dtype_t dtype,
                            const void* const* a_shards, const void* const* b_shards,
                            void* const* out, void* workspace, size_t workspace_bytes,

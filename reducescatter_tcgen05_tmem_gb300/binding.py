@@ -52,7 +52,7 @@ FLUX_NOALLOC_SCRATCH_BYTES = 16 * 1024 * 1024
 WAIT_SITES = {1: "ready flag", 2: "smem slot free", 3: "smem slot full",
               4: "accumulator free", 5: "accumulator full", 6: "drain",
               7: "deterministic turn", 8: "staged rows", 9: "unit schedule",
-              10: "cluster shape", 11: "grid barrier"}
+              10: "cluster shape", 11: "grid barrier", 12: "cluster exchange"}
 
 
 class flux_opts_t(ctypes.Structure):
