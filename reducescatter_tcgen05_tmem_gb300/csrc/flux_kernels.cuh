@@ -683,6 +683,65 @@ __device__ __forceinline__ uint32_t pair_peer_bytes(const KParams& p, const Work
   return a + __popc(mask) * B_BOX_N * BK * 2;
 }
 
+// The k-slices [kb, ke) of work item `w` (TMA producer thread).  MC2: the
+// pairs of a 4-CTA cluster share B by multicast (compile-time, so that the
+// per-slice loop carries no branch on it).  False when a wait gave up.
+template <int MODE, int CL, bool MC2>
+__device__ __forceinline__ bool produce_ksteps(const KParams& p, const Smem& s, const Ctl& c,
+                                               const Work& w, int kb, int ke, int nbox_a,
+                                               uint32_t bmask, uint32_t bytes, int n0, int cta,
+                                               int half, uint16_t mc_mask, int hw_rank,
+                                               uint32_t& stage, uint32_t& phase, uint32_t& issued) {
+  constexpr int PAIR = Unit<MODE, CL>::PAIR;
+  using G = typename Unit<MODE, CL>::G;
+  for (int k = kb; k < ke; ++k) {
+    // the empty barrier is completed by a remote commit whenever another CTA's MMAs read the stage
+    if (((PAIR == 2 && cta != 0) || MC2
+             ? wait_bar_remote(smem_u32(&s.empty[stage]), phase ^ 1u, c, W_EMPTY, stage)
+             : wait_bar(smem_u32(&s.empty[stage]), phase ^ 1u, c, W_EMPTY, stage)) != 0)
+      return false;
+    const uint32_t fb = smem_u32(&s.full[stage]);
+    if (PAIR == 1 || cta == 0) mbar_arrive_expect_tx(fb, bytes);
+    // barrier in the even CTA of this CTA's pair
+    const uint32_t fbc = PAIR == 2 ? mapa_shared(fb, static_cast<uint32_t>(hw_rank & ~1)) : fb;
+    const uint32_t sa = smem_u32(s.a + stage * A_STAGE);
+    const uint32_t sb = smem_u32(s.b + stage * G::B_STAGE);
+    const int kc = k * BK;
+    if (MODE == MODE_STORE) {
+      for (int bx = 0; bx < nbox_a; ++bx) {
+        const int row = w.m0 + bx * p.a_box_m;
+        const int sh = row / p.rows_per_rank;
+        if (PAIR == 2)
+          tma_load_2d_pair(sa + bx * p.a_box_m * BK * 2, &p.tmA[sh], fbc, kc, row - sh * p.rows_per_rank);
+        else
+          tma_load_2d(sa + bx * p.a_box_m * BK * 2, &p.tmA[sh], fb, kc, row - sh * p.rows_per_rank);
+      }
+    } else if (nbox_a) {
+      if (PAIR == 2) tma_load_2d_pair(sa, &p.tmA[w.r], fbc, kc, w.m0);
+      else tma_load_2d(sa, &p.tmA[w.r], fb, kc, w.m0);
+    }
+    for (int j = 0; j < G::B_BOXES; ++j) {
+      if (!((bmask >> j) & 1u)) continue;
+      if (MC2 && (j >> 1) != half) continue;  // the partner multicasts this box
+      const int nc = b_box_col<PAIR>(n0, cta, j);
+      const int n = nc < p.N ? nc : n0;  // the padding box of a CTA without columns
+      const uint32_t dst = sb + j * B_BOX_N * BK * 2;
+      if (MODE == MODE_MOE_SCATTER || MODE == MODE_MOE_STAGED) {
+        if (PAIR == 2) tma_load_3d_pair(dst, &p.tmB[w.r], fbc, n, kc, w.e);
+        else tma_load_3d(dst, &p.tmB[w.r], fb, n, kc, w.e);
+      } else if (PAIR == 2) {
+        if (MC2) tma_load_2d_pair_mc(dst, &p.tmB[w.r], fbc, n, kc, mc_mask);
+        else tma_load_2d_pair(dst, &p.tmB[w.r], fbc, n, kc);
+      } else {
+        tma_load_2d(dst, &p.tmB[w.r], fb, n, kc);
+      }
+    }
+    ++issued;
+    if (++stage == G::STAGES) { stage = 0; phase ^= 1u; }
+  }
+  return true;
+}
+
 // TMA producer (one thread).  Under the dynamic schedule the producer of a
 // region's first CTA also claims the region's units.
 template <int MODE, int CL>
@@ -742,60 +801,23 @@ __device__ void producer_tma(const KParams& p, const Smem& s, const Ctl& c, int 
       // the even CTA's barrier also counts the odd CTA's bytes of the same stage
       bytes += pair_peer_bytes<MODE, G>(p, w);
     }
-    const int claim_k = max(w.k0, w.k1 - CLAIM_AHEAD);
-    bool to_claim = leader;
-    for (int k = w.k0; k < w.k1; ++k) {
-      if (to_claim && k == claim_k) {
-        claim_unit(p, iter.box, claimed++);
-        to_claim = false;
+    // k-slices up to the claim point, the leader's claim of the region's
+    // next unit, then the rest (no per-slice branch on either)
+    const int claim_k = leader ? max(w.k0, w.k1 - CLAIM_AHEAD) : w.k1;
+    for (int seg = 0; seg < 2 && ok; ++seg) {
+      const int kb = seg == 0 ? w.k0 : claim_k, ke = seg == 0 ? claim_k : w.k1;
+      if (seg == 1 && leader) claim_unit(p, iter.box, claimed++);
+      if (kb >= ke) continue;
+      if constexpr (MC == 2) {
+        ok = mc2 ? produce_ksteps<MODE, CL, true>(p, s, c, w, kb, ke, nbox_a, bmask, bytes, n0, cta, half,
+                                                  mc_mask, ps.hw_rank, stage, phase, issued)
+                 : produce_ksteps<MODE, CL, false>(p, s, c, w, kb, ke, nbox_a, bmask, bytes, n0, cta,
+                                                   half, mc_mask, ps.hw_rank, stage, phase, issued);
+      } else {
+        ok = produce_ksteps<MODE, CL, false>(p, s, c, w, kb, ke, nbox_a, bmask, bytes, n0, cta, half,
+                                             mc_mask, ps.hw_rank, stage, phase, issued);
       }
-      // the empty barrier is completed by a remote commit whenever another CTA's MMAs read the stage
-      if (((PAIR == 2 && cta != 0) || mc2
-               ? wait_bar_remote(smem_u32(&s.empty[stage]), phase ^ 1u, c, W_EMPTY, stage)
-               : wait_bar(smem_u32(&s.empty[stage]), phase ^ 1u, c, W_EMPTY, stage)) != 0) {
-        ok = false;
-        break;
-      }
-      const uint32_t fb = smem_u32(&s.full[stage]);
-      if (PAIR == 1 || cta == 0) mbar_arrive_expect_tx(fb, bytes);
-      // barrier in the even CTA of this CTA's pair
-      const uint32_t fbc = PAIR == 2 ? mapa_shared(fb, static_cast<uint32_t>(ps.hw_rank & ~1)) : fb;
-      const uint32_t sa = smem_u32(s.a + stage * A_STAGE);
-      const uint32_t sb = smem_u32(s.b + stage * G::B_STAGE);
-      const int kc = k * BK;
-      if (MODE == MODE_STORE) {
-        for (int bx = 0; bx < nbox_a; ++bx) {
-          const int row = w.m0 + bx * p.a_box_m;
-          const int sh = row / p.rows_per_rank;
-          if (PAIR == 2)
-            tma_load_2d_pair(sa + bx * p.a_box_m * BK * 2, &p.tmA[sh], fbc, kc, row - sh * p.rows_per_rank);
-          else
-            tma_load_2d(sa + bx * p.a_box_m * BK * 2, &p.tmA[sh], fb, kc, row - sh * p.rows_per_rank);
-        }
-      } else if (nbox_a) {
-        if (PAIR == 2) tma_load_2d_pair(sa, &p.tmA[w.r], fbc, kc, w.m0);
-        else tma_load_2d(sa, &p.tmA[w.r], fb, kc, w.m0);
-      }
-      for (int j = 0; j < G::B_BOXES; ++j) {
-        if (!((bmask >> j) & 1u)) continue;
-        if (mc2 && (j >> 1) != half) continue;  // the partner multicasts this box
-        const int nc = b_box_col<PAIR>(n0, cta, j);
-        const int n = nc < p.N ? nc : n0;  // the padding box of a CTA without columns
-        const uint32_t dst = sb + j * B_BOX_N * BK * 2;
-        if (MODE == MODE_MOE_SCATTER || MODE == MODE_MOE_STAGED) {
-          if (PAIR == 2) tma_load_3d_pair(dst, &p.tmB[w.r], fbc, n, kc, w.e);
-          else tma_load_3d(dst, &p.tmB[w.r], fb, n, kc, w.e);
-        } else if (PAIR == 2) {
-          if (mc2) tma_load_2d_pair_mc(dst, &p.tmB[w.r], fbc, n, kc, mc_mask);
-          else tma_load_2d_pair(dst, &p.tmB[w.r], fbc, n, kc);
-        } else {
-          tma_load_2d(dst, &p.tmB[w.r], fb, n, kc);
-        }
-      }
-      ++issued;
-      if (++stage == G::STAGES) { stage = 0; phase ^= 1u; }
     }
-    if (to_claim && ok) claim_unit(p, iter.box, claimed++);  // a unit without k-slices
   }
   // drain: every issued copy must land before the CTA may exit.  The odd CTA of
   // a pair cannot see its copies complete (they count on the even CTA's
