@@ -143,7 +143,7 @@ int flux_last_cuda_error(void);
  * M, N, K as in the op's own signature (FLUX_OP_MLP: M, H, F).  Every dense op
  * needs the 256-byte status header; GEMM-RS adds per-tile arrival counters and
  * the fp32 accumulation buffer of the owners' row chunks (M x N floats).  Each
- * op then adds the mailboxes of its dynamic unit schedule: 4 x (2 U + 256)
+ * op then adds the mailboxes of its dynamic unit schedule: 4 x (2 U + 384)
  * bytes rounded up to 256, U = R x ceil(M / 512) x ceil(N_r / 512) work units
  * (N_r = the op's output columns per rank).  With that area the op runs on
  * every SM (clusters of CTA pairs, 4 preferred, units claimed at run time);

@@ -77,10 +77,12 @@ long long dense_units(int R, int M, int cols) {
          ((cols + DenseGeo::TILE_N - 1) / DenseGeo::TILE_N);
 }
 
-// Mailboxes of the dynamic schedule: with g <= MAX_REGIONS regions of
-// 2 ceil(U / g) + 2 entries each, at most 2 U + 4 MAX_REGIONS entries.
+// Mailboxes of the dynamic schedule: C <= U + MAX_REGIONS claims (the last
+// units of a store-mode op are claimed as two halves, at most one per region)
+// over g <= MAX_REGIONS regions of 2 ceil(C / g) + 2 entries each: at most
+// 2 U + 6 MAX_REGIONS entries.
 size_t sched_bytes(long long units) {
-  return round_up(static_cast<size_t>(2 * units + 4 * MAX_REGIONS) * sizeof(uint32_t), WS_ALIGN);
+  return round_up(static_cast<size_t>(2 * units + 6 * MAX_REGIONS) * sizeof(uint32_t), WS_ALIGN);
 }
 
 // Set up the dynamic schedule of a dense CL = 4 launch if the workspace has
@@ -98,8 +100,13 @@ int setup_dyn(KParams& p, flux_dtype_t dt, const DeviceInfo& dev, const flux_opt
     grid = static_cast<int>(p.num_units) * DENSE_CL;
   }
   const long long g = grid / DENSE_CL;
+  // store mode: the last g units are claimed as two 256-column halves, so
+  // that the last wave of units ends more evenly over the regions
+  p.split_from = p.num_units;
+  if (MODE == MODE_STORE) p.split_from = static_cast<int>(p.num_units > g ? p.num_units - g : 0);
+  p.num_claims = p.num_units + (p.num_units - p.split_from);
   p.dyn = 1;
-  p.mbox_cap = static_cast<int>(2 * ((p.num_units + g - 1) / g) + 2);
+  p.mbox_cap = static_cast<int>(2 * ((p.num_claims + g - 1) / g) + 2);
   p.mbox = reinterpret_cast<uint32_t*>(mbox);
   return grid;
 }

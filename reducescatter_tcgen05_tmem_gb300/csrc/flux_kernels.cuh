@@ -217,6 +217,9 @@ struct KParams {
   int stream_k;            // REDUCE: 1 = contiguous k-step ranges per CTA
   int deterministic;       // REDUCE: ranks add their partials in ascending order
   int num_units;           // dense modes: number of work units
+  int num_claims;          // dynamic schedule: claim ids (units, the last ones as two halves)
+  int split_from;          // dynamic schedule, store mode: units from here on are claimed as
+                           // two 256-column halves (num_units: none)
   long long total_ksteps;  // REDUCE stream-K: num_units * KT
   const uint32_t* flags;   // AG ready flags (nullptr = all ready)
   uint32_t epoch;
@@ -395,6 +398,7 @@ __device__ __forceinline__ void raster(int t, int Mt, int Nt, int group_n, int& 
 struct Work {
   int r;       // rank whose operands feed the tile
   int mt, nt;  // scheduled tile coordinates (mt counts TILE_M-row tiles)
+  int n0, n_end;  // the item's output columns [n0, n_end) (a tile, or half of one)
   int m0;      // first A row of THIS CTA's part of the tile
   int row_end; // rows >= row_end are not part of the tile's problem
   int e;       // expert (MoE)
@@ -438,6 +442,8 @@ __device__ __forceinline__ Work decode_store(const KParams& p, int u, int cta) {
   if (mt_per_shard > 0 && p.rows_per_rank % TM == 0) mt = (mt + w.r * mt_per_shard) % p.Mt;
   w.mt = mt;
   w.nt = nt;
+  w.n0 = nt * Unit<MODE_STORE, CL>::G::TILE_N;
+  w.n_end = min(p.N, w.n0 + Unit<MODE_STORE, CL>::G::TILE_N);
   w.m0 = mt * TM + cta * BM;
   w.row_end = p.M;
   w.e = 0;
@@ -471,6 +477,8 @@ __device__ __forceinline__ Work decode_reduce(const KParams& p, int u, int cta) 
     t = full_groups * TG + (rem - w.r * tl);
   }
   raster(t, p.Mt, p.Nt, p.group_n, w.mt, w.nt);
+  w.n0 = w.nt * Unit<MODE_REDUCE, CL>::G::TILE_N;
+  w.n_end = min(p.N, w.n0 + Unit<MODE_REDUCE, CL>::G::TILE_N);
   w.tile = (w.mt * CL + cta) * p.Nt + w.nt;
   w.m0 = w.mt * TM + cta * BM;
   w.row_end = p.M;
@@ -491,7 +499,7 @@ __device__ __forceinline__ Work decode_reduce(const KParams& p, int u, int cta) 
 //   1  rank innermost: the ranks' tiles of one (m, n) are consecutive units
 //   2  band outermost, then rank, then the m-tile fastest inside the band
 template <int CL>
-__device__ __forceinline__ Work decode_moe(const KParams& p, int u, int total_mt, int cta) {
+__device__ __forceinline__ Work decode_moe(const KParams& p, int u, int total_mt, int cta, int tile_n) {
   Work w;
   const int per_rank = total_mt * p.Nt;
   int tr, t;  // rank inside the expert's group; the unit's index among that rank's
@@ -534,6 +542,8 @@ __device__ __forceinline__ Work decode_moe(const KParams& p, int u, int total_mt
   w.row_end = __ldg(p.offsets + lo + 1);
   w.mt = gmt;
   w.nt = nt;
+  w.n0 = nt * tile_n;
+  w.n_end = min(p.N, w.n0 + tile_n);
   w.k0 = 0;
   w.k1 = p.KT;
   w.tile = 0;
@@ -588,6 +598,8 @@ struct ItemIter {
       w.r = r;
       w.mt = 0;
       w.nt = u;
+      w.n0 = u * BN;
+      w.n_end = min(p.N, w.n0 + BN);
       w.m0 = 0;
       w.row_end = p.M;
       w.e = 0;
@@ -605,9 +617,20 @@ struct ItemIter {
       if (warp_uniform) v = __shfl_sync(0xFFFFFFFFu, v, 0);
       ++taken;
       if (v == 0u || v == MBOX_DONE) return false;
-      const int unit = static_cast<int>(v - 1u);
-      if (MODE == MODE_STORE) w = decode_store<CL>(p, unit, cta);
-      else w = decode_reduce<CL>(p, unit, cta);
+      const int id = static_cast<int>(v - 1u);
+      if (MODE == MODE_STORE) {
+        if (id < p.split_from) {
+          w = decode_store<CL>(p, id, cta);
+        } else {
+          // the last units are claimed as two 256-column halves
+          const int half = (id - p.split_from) & 1;
+          w = decode_store<CL>(p, p.split_from + ((id - p.split_from) >> 1), cta);
+          w.n0 += half * BN;
+          w.n_end = min(w.n_end, w.n0 + BN);
+        }
+      } else {
+        w = decode_reduce<CL>(p, id, cta);
+      }
       return true;
     }
     if (MODE == MODE_REDUCE && p.stream_k) {
@@ -625,21 +648,33 @@ struct ItemIter {
     if (u >= num_units) return false;
     if (MODE == MODE_STORE) w = decode_store<CL>(p, u, cta);
     else if (MODE == MODE_REDUCE) w = decode_reduce<CL>(p, u, cta);
-    else w = decode_moe<CL>(p, u, total_mt, cta);
+    else w = decode_moe<CL>(p, u, total_mt, cta, Unit<MODE, CL>::G::TILE_N);
     u += stride;
     return true;
   }
 };
 
-// Dynamic schedule: the region's first CTA writes its next unit (+ 1) into
-// entry j of the region's mailbox, or MBOX_DONE once the counter has run out or
-// the mailbox is full (then the other regions take the remaining units: the
-// mailboxes together hold more entries than there are units).
+// Dynamic schedule: the region's first CTA writes its next claim id (+ 1)
+// into entry j of the region's mailbox, or MBOX_DONE once the counter has run
+// out or the mailbox is full (then the other regions take the remaining
+// claims: the mailboxes together hold more entries than there are claims).
+// Store mode: ids from split_from on are the two 256-column halves of the
+// last units; a half without columns is skipped here.
+template <int MODE, int CL>
 __device__ __forceinline__ void claim_unit(const KParams& p, uint32_t* box, int j) {
   uint32_t v = MBOX_DONE;
   if (j < p.mbox_cap - 1) {
-    const uint32_t u = atomicAdd(p.hdr + H_CLAIM, 1u);
-    if (u < static_cast<uint32_t>(p.num_units)) v = u + 1u;
+    for (;;) {
+      const uint32_t u = atomicAdd(p.hdr + H_CLAIM, 1u);
+      if (u >= static_cast<uint32_t>(p.num_claims)) break;
+      const int id = static_cast<int>(u);
+      // the second half of a last unit narrower than 257 columns has no columns
+      if (MODE == MODE_STORE && id >= p.split_from && ((id - p.split_from) & 1) &&
+          decode_store<CL>(p, p.split_from + ((id - p.split_from) >> 1), 0).n0 + BN >= p.N)
+        continue;
+      v = u + 1u;
+      break;
+    }
   }
   st_release_u32(box + j, v);
 }
@@ -679,7 +714,7 @@ __device__ __forceinline__ uint32_t pair_peer_bytes(const KParams& p, const Work
   uint32_t a = nbox_a * A_STAGE;
   if (MODE == MODE_STORE && nbox_a)
     a = ((min(m0 + BM, w.row_end) - m0 + p.a_box_m - 1) / p.a_box_m) * p.a_box_m * BK * 2;
-  const uint32_t mask = b_box_mask<2, G::B_BOXES>(p.N, w.nt * G::TILE_N, 1);
+  const uint32_t mask = b_box_mask<2, G::B_BOXES>(w.n_end, w.n0, 1);
   return a + __popc(mask) * B_BOX_N * BK * 2;
 }
 
@@ -724,7 +759,7 @@ __device__ __forceinline__ bool produce_ksteps(const KParams& p, const Smem& s, 
       if (!((bmask >> j) & 1u)) continue;
       if (MC2 && (j >> 1) != half) continue;  // the partner multicasts this box
       const int nc = b_box_col<PAIR>(n0, cta, j);
-      const int n = nc < p.N ? nc : n0;  // the padding box of a CTA without columns
+      const int n = nc < w.n_end ? nc : n0;  // the padding box of a CTA without columns
       const uint32_t dst = sb + j * B_BOX_N * BK * 2;
       if (MODE == MODE_MOE_SCATTER || MODE == MODE_MOE_STAGED) {
         if (PAIR == 2) tma_load_3d_pair(dst, &p.tmB[w.r], fbc, n, kc, w.e);
@@ -758,7 +793,7 @@ __device__ void producer_tma(const KParams& p, const Smem& s, const Ctl& c, int 
   ItemIter<MODE, CL> iter(p, total_mt, ps.vrank, &c);
   const bool leader = iter.dyn && ps.vrank == 0;
   int claimed = 0;  // mailbox entries the leader has written
-  if (leader) claim_unit(p, iter.box, claimed++);
+  if (leader) claim_unit<MODE, CL>(p, iter.box, claimed++);
   Work w;
   uint32_t stage = 0, phase = 0;
   uint32_t issued = 0;
@@ -793,8 +828,8 @@ __device__ void producer_tma(const KParams& p, const Smem& s, const Ctl& c, int 
         nbox_a = (min(w.m0 + BM, w.row_end) - w.m0 + p.a_box_m - 1) / p.a_box_m;
       }
     }
-    const int n0 = w.nt * G::TILE_N;
-    const uint32_t bmask = b_box_mask<PAIR, G::B_BOXES>(p.N, n0, cta);
+    const int n0 = w.n0;
+    const uint32_t bmask = b_box_mask<PAIR, G::B_BOXES>(w.n_end, n0, cta);
     uint32_t bytes = ((MODE == MODE_STORE) ? nbox_a * p.a_box_m * BK * 2 : nbox_a * A_STAGE) +
                      __popc(bmask) * B_BOX_N * BK * 2;
     if (PAIR == 2 && cta == 0) {
@@ -806,7 +841,7 @@ __device__ void producer_tma(const KParams& p, const Smem& s, const Ctl& c, int 
     const int claim_k = leader ? max(w.k0, w.k1 - CLAIM_AHEAD) : w.k1;
     for (int seg = 0; seg < 2 && ok; ++seg) {
       const int kb = seg == 0 ? w.k0 : claim_k, ke = seg == 0 ? claim_k : w.k1;
-      if (seg == 1 && leader) claim_unit(p, iter.box, claimed++);
+      if (seg == 1 && leader) claim_unit<MODE, CL>(p, iter.box, claimed++);
       if (kb >= ke) continue;
       if constexpr (MC == 2) {
         ok = mc2 ? produce_ksteps<MODE, CL, true>(p, s, c, w, kb, ke, nbox_a, bmask, bytes, n0, cta, half,
@@ -958,7 +993,7 @@ __device__ void mma_issuer(const KParams& p, const Smem& s, const Ctl& c, uint32
     const uint32_t d = tmem_base + b * G::ACC_COLS;
     // 256-column halves of the tile that start below N (a half wholly past N
     // has nothing to compute; its accumulator columns are never stored)
-    const int n_live = (G::N_MMA > 1 && w.nt * G::TILE_N + BN >= p.N) ? 1 : G::N_MMA;
+    const int n_live = (G::N_MMA > 1 && w.n0 + BN >= w.n_end) ? 1 : G::N_MMA;
     for (int k = w.k0; k < w.k1; ++k) {
       if (wait_bar(smem_u32(&s.full[stage]), phase, c, W_FULL, stage) != 0) { ok = false; break; }
       tc_fence_after();
@@ -1124,8 +1159,8 @@ __device__ void epilogue(const KParams& p, const Smem& s, const Ctl& c, uint32_t
     const int row = row0 + lane;           // row of the A row space held by this thread
     const bool row_ok = row < w.row_end;
     const uint32_t taddr = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + b * G::ACC_COLS;
-    const int n0 = w.nt * G::TILE_N;
-    const int ncols = min(G::TILE_N, p.N - n0);
+    const int n0 = w.n0;
+    const int ncols = w.n_end - n0;
     // per-row routing data
     float gate = 1.0f;
     int tok = 0;

@@ -45,8 +45,8 @@ def test_version_and_status_strings(fx):
 
 
 def _sched(units):
-    # mailboxes of the dynamic unit schedule: (2 U + 4 x 64 regions) uint32, 256-byte rounded
-    return -(-(2 * units + 256) * 4 // 256) * 256
+    # mailboxes of the dynamic unit schedule: (2 U + 6 x 64 regions) uint32, 256-byte rounded
+    return -(-(2 * units + 384) * 4 // 256) * 256
 
 
 def test_workspace_sizes(fx):

@@ -254,11 +254,16 @@ def _static_ws_bytes(op, R, M, N, K):
     return 256 + -(-((-(-M // 128)) * (-(-N // 256)) * 16) // 256) * 256 + M * N * 4
 
 
-@pytest.mark.parametrize("num_ctas", [0, 8])
-def test_ag_gemm_dynamic_schedule_matches_static_bit_for_bit(num_ctas):
-    # 8 ranks x 4 m-units x 4 n-units = 128 units: several per region, so the
-    # regions claim repeatedly (num_ctas 8: two regions, 64+ units each)
-    c = configs.small(configs.CONFIGS["ag_mlp0"], R=8, M=2048, N=16384, K=256, dtype="bf16", seed=71)
+@pytest.mark.parametrize("num_ctas,N", [
+    (0, 16384),   # 8 ranks x 4 m-units x 4 n-units = 128 units, the last 38 claimed as halves
+    (8, 16384),   # two regions, 64+ units each; the last 2 units as halves
+    (0, 6144),    # N/R = 768: every rank's last n-unit is 256 wide (its second half is empty)
+    (0, 5120),    # N/R = 640: last n-units 128 wide
+])
+def test_ag_gemm_dynamic_schedule_matches_static_bit_for_bit(num_ctas, N):
+    # the regions claim repeatedly; the last units of the schedule are split
+    # into 256-column halves, halves past N are skipped
+    c = configs.small(configs.CONFIGS["ag_mlp0"], R=8, M=2048, N=N, K=256, dtype="bf16", seed=71)
     xs, w_s = configs.ag_inputs(c)
     X = [to_device(x, c.dtype) for x in xs]
     W = [to_device(w, c.dtype) for w in w_s]
