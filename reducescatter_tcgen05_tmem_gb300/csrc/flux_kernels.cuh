@@ -60,9 +60,13 @@
 //     m-unit's ready counter; then CTA pairs compute 256 x 512 tiles whose
 //     producers wait for their unit's count and load A by TMA.
 //
+// RS_CLUSTER, CL = 4: four independent single-CTA (PAIR = 1) 128 x 256
+// tiles per cluster, one n-tile per cluster; the cluster only serves the
+// distributed-shared-memory reduction of the partials.
+//
 // The template parameter CL is the number of CTAs of a cluster (1, 2 or 4);
-// PAIR = min(CL, 2) is the tcgen05 CTA group and MC = CL / PAIR the pairs that
-// share B (dense modes only).
+// PAIR = min(CL, 2) is the tcgen05 CTA group (1 for RS_CLUSTER) and
+// MC = CL / PAIR the pairs that share B (dense modes only).
 //
 // Dynamic schedule (dense modes, CL = 4, KParams::dyn): clusters of 4 CTAs fit
 // on only part of the SMs (144 of 152 on GB300), so the kernel is launched with
@@ -73,7 +77,8 @@
 // a counter in the workspace header, so that the slower pair regions take fewer
 // of them; the region's first CTA claims the next unit a few k-slices before
 // its current one ends and writes it into the region's mailbox in the
-// workspace, from which every role of the region's CTAs reads its units.
+// workspace, from which every role of the region's CTAs reads its units.  In
+// store mode the last units are claimed as two 256-column halves each.
 //
 // Every wait is bounded: after timeout_ns (or an iteration cap) the thread
 // records FLUX_ERR_TIMEOUT in the workspace header, raises the per-call abort
