@@ -32,9 +32,13 @@ flux_status_t launch_dyn_dt(flux_dtype_t dt, const KParams& p, int grid, cudaStr
                          : Launcher<MODE, 0, CL>::launch_dyn(p, grid, s);
 }
 
-// Dense whole-tile kernels run on clusters of two CTA pairs stacked along M
-// (512 x 512 per cluster, B multicast between the pairs).
+// Dense whole-tile kernels: on the static schedule, clusters of two CTA pairs
+// stacked along M (512 x 512 per cluster, B multicast between the pairs); on
+// the dynamic schedule, store mode runs regions of four pairs (512 x 1024: A
+// multicast between the pairs side by side along N as well) where 8-CTA
+// clusters fit and pairs elsewhere; reduce mode regions of two pairs.
 constexpr int DENSE_CL = 4;
+constexpr int DENSE_CL8 = 8;
 // GEMM-RS of few rows: clusters of 4 CTAs reduce the R partials of a tile
 // through distributed shared memory (each CTA computes R / 4 partials)
 constexpr int RS_CLUSTER_CL = 4;
@@ -88,22 +92,23 @@ size_t sched_bytes(long long units) {
 // Set up the dynamic schedule of a dense CL = 4 launch if the workspace has
 // room for its mailboxes at `mbox` and the launch form is available; returns
 // its grid, or 0 (then the static schedule runs).
-template <int MODE>
+template <int MODE, int CL>
 int setup_dyn(KParams& p, flux_dtype_t dt, const DeviceInfo& dev, const flux_opts_t* opts,
               uint8_t* mbox, size_t room) {
   if (room < sched_bytes(p.num_units)) return 0;
-  int grid = grid_dyn_dt<MODE, DENSE_CL>(dt, dev);
-  if (opts && opts->num_ctas > 0 && opts->num_ctas < grid) grid = opts->num_ctas - opts->num_ctas % DENSE_CL;
-  if (grid < DENSE_CL) return 0;
-  const long long regions = grid / DENSE_CL;
+  int grid = grid_dyn_dt<MODE, CL>(dt, dev);
+  if (opts && opts->num_ctas > 0 && opts->num_ctas < grid) grid = opts->num_ctas - opts->num_ctas % CL;
+  if (grid < CL) return 0;
+  const long long regions = grid / CL;
   if (regions > p.num_units) {
-    grid = static_cast<int>(p.num_units) * DENSE_CL;
+    grid = static_cast<int>(p.num_units) * CL;
   }
-  const long long g = grid / DENSE_CL;
-  // store mode: the last g units are claimed as two 256-column halves, so
-  // that the last wave of units ends more evenly over the regions
+  const long long g = grid / CL;
+  // store mode, regions of 4: the last g units are claimed as two 256-column
+  // halves, so that the last wave of units ends more evenly over the regions
   p.split_from = p.num_units;
-  if (MODE == MODE_STORE) p.split_from = static_cast<int>(p.num_units > g ? p.num_units - g : 0);
+  if (MODE == MODE_STORE && CL == 4)
+    p.split_from = static_cast<int>(p.num_units > g ? p.num_units - g : 0);
   p.num_claims = p.num_units + (p.num_units - p.split_from);
   p.dyn = 1;
   p.mbox_cap = static_cast<int>(2 * ((p.num_claims + g - 1) / g) + 2);
@@ -145,9 +150,12 @@ extern "C" flux_status_t flux_launch_info(flux_op_t op, flux_dtype_t dtype, int*
   switch (op) {
     case FLUX_OP_GEMM:
     case FLUX_OP_AG_GEMM:
-      cl = DENSE_CL;
-      cap = grid_dyn_dt<MODE_STORE, DENSE_CL>(dtype, dev);
-      if (cap == 0) cap = grid_dt<MODE_STORE, DENSE_CL>(dtype, dev, nullptr, 1LL << 30);
+      cl = DENSE_CL8;
+      cap = grid_dyn_dt<MODE_STORE, DENSE_CL8>(dtype, dev);
+      if (cap == 0) {
+        cl = DENSE_CL;
+        cap = grid_dt<MODE_STORE, DENSE_CL>(dtype, dev, nullptr, 1LL << 30);
+      }
       break;
     case FLUX_OP_GEMM_RS:
     case FLUX_OP_MLP:
@@ -229,8 +237,26 @@ extern "C" flux_status_t flux_ag_gemm(int R, int M, int N, int K, flux_dtype_t d
   fill_common(p, opts, workspace);
   // bands of 4 n-tiles (2048 columns) measured best for the 512 x 512 units
   if (!(opts && opts->group_n > 0)) p.group_n = 4;
-  // dynamic schedule over every SM when the workspace holds its mailboxes
-  const int dgrid = setup_dyn<MODE_STORE>(p, dtype, dev, opts,
+  // dynamic schedule over every SM when the workspace holds its mailboxes:
+  // regions of 8 CTAs (512 x 1024 units, 64-row A boxes that must not
+  // straddle two shards), else regions of 4
+  if (R == 1 || rows % 64 == 0) {
+    KParams q = p;
+    for (int r = 0; r < R; ++r)
+      if ((st = encode_2d(&q.tmA[r], dtype, x_shards[r], K, rows, static_cast<uint64_t>(K) * 2, BK,
+                          64)) != FLUX_OK)
+        return st;
+    q.a_box_m = 64;
+    q.Nt = (Nr + Unit<MODE_STORE, DENSE_CL8>::UNIT_N - 1) / Unit<MODE_STORE, DENSE_CL8>::UNIT_N;
+    q.num_units = R * q.Mt * q.Nt;
+    // bands of 2 n-units (2048 columns), as 4 for the 512-column units
+    if (!(opts && opts->group_n > 0)) q.group_n = 2;
+    const int g8 = setup_dyn<MODE_STORE, DENSE_CL8>(q, dtype, dev, opts,
+                                                    static_cast<uint8_t*>(workspace) + WS_HEADER,
+                                                    workspace_bytes - WS_HEADER);
+    if (g8 > 0 && launch_dyn_dt<MODE_STORE, DENSE_CL8>(dtype, q, g8, s) == FLUX_OK) return FLUX_OK;
+  }
+  const int dgrid = setup_dyn<MODE_STORE, DENSE_CL>(p, dtype, dev, opts,
                                           static_cast<uint8_t*>(workspace) + WS_HEADER,
                                           workspace_bytes - WS_HEADER);
   if (dgrid > 0) {
@@ -352,29 +378,33 @@ extern "C" flux_status_t flux_gemm_rs(int R, int M, int N, int K, flux_dtype_t d
       }
     }
     p.tiles_per_group = p.Mt * p.Nt;
+    p.Nt_tile = p.Nt;
     return launch_dt<MODE_REDUCE, 1>(dtype, p, grid, s);
   }
   using RsUnit = Unit<MODE_REDUCE, DENSE_CL>;
   p.Nt = (N + RsUnit::G::TILE_N - 1) / RsUnit::G::TILE_N;
+  p.Nt_tile = p.Nt;
   p.Mt = (M + RsUnit::ROWS - 1) / RsUnit::ROWS;
   const int tiles = p.Mt * p.Nt;
   p.num_units = tiles * R;
   p.total_ksteps = static_cast<long long>(p.num_units) * p.KT;
   p.stream_k = 0;
-  auto tiles_per_group = [&](int grid) {
+  auto tiles_per_group = [&](int grid, int cl, int ntiles) {
     const int tg = p.deterministic ? 1
-                  : (opts && opts->tiles_per_group > 0) ? opts->tiles_per_group : grid / DENSE_CL;
-    return tg < tiles ? tg : tiles;
+                  : (opts && opts->tiles_per_group > 0) ? opts->tiles_per_group : grid / cl;
+    return tg < ntiles ? tg : ntiles;
   };
   if (!p.deterministic) {
     // dynamic schedule over every SM when the workspace holds its mailboxes
     // (the deterministic order keeps the static schedule: its waits point at
-    // lower units, which must already sit on resident clusters)
+    // lower units, which must already sit on resident clusters).  Regions of
+    // 4 CTAs: regions of 8 (A shared as well) measured no faster here -- four
+    // pairs in lockstep stall together on their fp32 drains.
     const size_t off = rs_min_bytes(M, N);
-    const int dgrid = setup_dyn<MODE_REDUCE>(p, dtype, dev, opts, ws + off,
-                                             workspace_bytes > off ? workspace_bytes - off : 0);
+    const size_t room = workspace_bytes > off ? workspace_bytes - off : 0;
+    const int dgrid = setup_dyn<MODE_REDUCE, DENSE_CL>(p, dtype, dev, opts, ws + off, room);
     if (dgrid > 0) {
-      p.tiles_per_group = tiles_per_group(dgrid);
+      p.tiles_per_group = tiles_per_group(dgrid, DENSE_CL, tiles);
       if (launch_dyn_dt<MODE_REDUCE, DENSE_CL>(dtype, p, dgrid, s) == FLUX_OK) return FLUX_OK;
       p.dyn = 0;  // launch form refused: the static schedule below
       p.mbox = nullptr;
@@ -383,7 +413,7 @@ extern "C" flux_status_t flux_gemm_rs(int R, int M, int N, int K, flux_dtype_t d
   }
   const int grid = grid_dt<MODE_REDUCE, DENSE_CL>(dtype, dev, opts, p.num_units);
   if (grid == 0) return FLUX_ERR_CUDA;
-  p.tiles_per_group = tiles_per_group(grid);
+  p.tiles_per_group = tiles_per_group(grid, DENSE_CL, tiles);
   return launch_dt<MODE_REDUCE, DENSE_CL>(dtype, p, grid, s);
 }
 

@@ -222,6 +222,7 @@ struct KParams {
   int stream_k;            // REDUCE: 1 = contiguous k-step ranges per CTA
   int deterministic;       // REDUCE: ranks add their partials in ascending order
   int num_units;           // dense modes: number of work units
+  int Nt_tile;             // REDUCE: output tiles (TILE_N columns) per row block, for the counters
   int num_claims;          // dynamic schedule: claim ids (units, the last ones as two halves)
   int split_from;          // dynamic schedule, store mode: units from here on are claimed as
                            // two 256-column halves (num_units: none)
@@ -422,9 +423,14 @@ struct Unit {
   // RS_CLUSTER: every CTA of the cluster runs its own 128 x 256 tiles
   static constexpr int PAIR = (CL >= 2 && MODE != MODE_RS_CLUSTER) ? 2 : 1;
   static constexpr int NM = ((DENSE || MODE == MODE_MOE_STAGED) && PAIR == 2) ? 2 : 1;
-  static constexpr int MC = MODE == MODE_RS_CLUSTER ? 1 : CL / PAIR;
-  static constexpr int ROWS = BM * CL;
+  // pairs side by side along N (share A by multicast) and stacked along M
+  // (share B by multicast)
+  static constexpr int PN = (DENSE && CL == 8) ? 2 : 1;
+  static constexpr int PM = MODE == MODE_RS_CLUSTER ? 1 : CL / PAIR / PN;
+  static constexpr int MC = PM;
+  static constexpr int ROWS = BM * PAIR * PM;
   using G = Geo<PAIR, NM>;
+  static constexpr int UNIT_N = G::TILE_N * PN;
   static_assert(DENSE || MC == 1, "MoE tiles: no B sharing between pairs");
   static_assert(MODE != MODE_MOE_GATHER || CL == 1, "MoE layer0 gather: single CTAs");
   static_assert(MODE != MODE_MOE_STAGED || CL == 2, "MoE layer0 staged: CTA pairs");
@@ -445,11 +451,13 @@ __device__ __forceinline__ Work decode_store(const KParams& p, int u, int cta) {
   raster(u - w.r * per_rank, p.Mt, p.Nt, p.group_n, mt, nt);
   const int mt_per_shard = p.rows_per_rank / TM;
   if (mt_per_shard > 0 && p.rows_per_rank % TM == 0) mt = (mt + w.r * mt_per_shard) % p.Mt;
+  using U = Unit<MODE_STORE, CL>;
+  const int pr = cta / U::PAIR;  // pair of the region
   w.mt = mt;
   w.nt = nt;
-  w.n0 = nt * Unit<MODE_STORE, CL>::G::TILE_N;
-  w.n_end = min(p.N, w.n0 + Unit<MODE_STORE, CL>::G::TILE_N);
-  w.m0 = mt * TM + cta * BM;
+  w.n0 = nt * U::UNIT_N + (pr / U::PM) * U::G::TILE_N;
+  w.n_end = min(p.N, w.n0 + U::G::TILE_N);
+  w.m0 = mt * TM + (pr % U::PM) * (BM * U::PAIR) + (cta % U::PAIR) * BM;
   w.row_end = p.M;
   w.e = 0;
   w.k0 = 0;
@@ -482,10 +490,13 @@ __device__ __forceinline__ Work decode_reduce(const KParams& p, int u, int cta) 
     t = full_groups * TG + (rem - w.r * tl);
   }
   raster(t, p.Mt, p.Nt, p.group_n, w.mt, w.nt);
-  w.n0 = w.nt * Unit<MODE_REDUCE, CL>::G::TILE_N;
-  w.n_end = min(p.N, w.n0 + Unit<MODE_REDUCE, CL>::G::TILE_N);
-  w.tile = (w.mt * CL + cta) * p.Nt + w.nt;
-  w.m0 = w.mt * TM + cta * BM;
+  using U = Unit<MODE_REDUCE, CL>;
+  const int pr = cta / U::PAIR;  // pair of the region
+  w.n0 = w.nt * U::UNIT_N + (pr / U::PM) * U::G::TILE_N;
+  w.n_end = min(p.N, w.n0 + U::G::TILE_N);
+  w.m0 = w.mt * TM + (pr % U::PM) * (BM * U::PAIR) + (cta % U::PAIR) * BM;
+  // counters: 128-row block x output tile (TILE_N columns) of this CTA's part
+  w.tile = (w.m0 / BM) * p.Nt_tile + w.n0 / U::G::TILE_N;
   w.row_end = p.M;
   w.e = 0;
   w.k0 = 0;
@@ -563,7 +574,7 @@ __device__ __forceinline__ Work decode_moe(const KParams& p, int u, int total_mt
 // (a whole warp calls next) makes lane 0 read the mailbox for the warp.
 template <int MODE, int CL>
 struct ItemIter {
-  static constexpr bool DYN_OK = Unit<MODE, CL>::DENSE && CL == 4;
+  static constexpr bool DYN_OK = Unit<MODE, CL>::DENSE && (CL == 4 || CL == 8);
   const KParams& p;
   const Ctl* ctl;
   int total_mt;      // MoE: device-computed number of m-tiles
@@ -624,7 +635,7 @@ struct ItemIter {
       if (v == 0u || v == MBOX_DONE) return false;
       const int id = static_cast<int>(v - 1u);
       if (MODE == MODE_STORE) {
-        if (id < p.split_from) {
+        if (CL != 4 || id < p.split_from) {
           w = decode_store<CL>(p, id, cta);
         } else {
           // the last units are claimed as two 256-column halves
@@ -674,7 +685,7 @@ __device__ __forceinline__ void claim_unit(const KParams& p, uint32_t* box, int 
       if (u >= static_cast<uint32_t>(p.num_claims)) break;
       const int id = static_cast<int>(u);
       // the second half of a last unit narrower than 257 columns has no columns
-      if (MODE == MODE_STORE && id >= p.split_from && ((id - p.split_from) & 1) &&
+      if (MODE == MODE_STORE && CL == 4 && id >= p.split_from && ((id - p.split_from) & 1) &&
           decode_store<CL>(p, p.split_from + ((id - p.split_from) >> 1), 0).n0 + BN >= p.N)
         continue;
       v = u + 1u;
@@ -732,6 +743,11 @@ __device__ __forceinline__ bool produce_ksteps(const KParams& p, const Smem& s, 
                                                uint32_t bmask, uint32_t bytes, int n0, int cta,
                                                int half, uint16_t mc_mask, int hw_rank,
                                                uint32_t& stage, uint32_t& phase, uint32_t& issued) {
+  // PN = 2: this CTA and its N neighbour (hw_rank ^ 4) hold the same A rows;
+  // each issues one of the two 64-row A boxes as a multicast to both
+  constexpr bool MCA = Unit<MODE, CL>::PN == 2;
+  const uint16_t mask_a = static_cast<uint16_t>((1u << hw_rank) | (1u << (hw_rank ^ 4)));
+  const int a_half = (hw_rank >> 2) & 1;
   constexpr int PAIR = Unit<MODE, CL>::PAIR;
   using G = typename Unit<MODE, CL>::G;
   for (int k = kb; k < ke; ++k) {
@@ -749,16 +765,33 @@ __device__ __forceinline__ bool produce_ksteps(const KParams& p, const Smem& s, 
     const int kc = k * BK;
     if (MODE == MODE_STORE) {
       for (int bx = 0; bx < nbox_a; ++bx) {
+        if (MCA && MC2 && bx != a_half) continue;  // the N neighbour multicasts this box
         const int row = w.m0 + bx * p.a_box_m;
         const int sh = row / p.rows_per_rank;
-        if (PAIR == 2)
+        if (MCA && MC2)
+          tma_load_2d_pair_mc(sa + bx * p.a_box_m * BK * 2, &p.tmA[sh], fbc, kc, row - sh * p.rows_per_rank,
+                              mask_a);
+        else if (PAIR == 2)
           tma_load_2d_pair(sa + bx * p.a_box_m * BK * 2, &p.tmA[sh], fbc, kc, row - sh * p.rows_per_rank);
         else
           tma_load_2d(sa + bx * p.a_box_m * BK * 2, &p.tmA[sh], fb, kc, row - sh * p.rows_per_rank);
       }
     } else if (nbox_a) {
-      if (PAIR == 2) tma_load_2d_pair(sa, &p.tmA[w.r], fbc, kc, w.m0);
-      else tma_load_2d(sa, &p.tmA[w.r], fb, kc, w.m0);
+      if (MCA) {
+        // two 64-row boxes (the map's box is 64 rows); with a 8-CTA cluster
+        // each of the two N neighbours issues one of them to both
+        for (int bx = 0; bx < 2; ++bx) {
+          if (MC2 && bx != a_half) continue;
+          if (MC2)
+            tma_load_2d_pair_mc(sa + bx * 64 * BK * 2, &p.tmA[w.r], fbc, kc, w.m0 + bx * 64, mask_a);
+          else
+            tma_load_2d_pair(sa + bx * 64 * BK * 2, &p.tmA[w.r], fbc, kc, w.m0 + bx * 64);
+        }
+      } else if (PAIR == 2) {
+        tma_load_2d_pair(sa, &p.tmA[w.r], fbc, kc, w.m0);
+      } else {
+        tma_load_2d(sa, &p.tmA[w.r], fb, kc, w.m0);
+      }
     }
     for (int j = 0; j < G::B_BOXES; ++j) {
       if (!((bmask >> j) & 1u)) continue;
@@ -792,7 +825,7 @@ __device__ void producer_tma(const KParams& p, const Smem& s, const Ctl& c, int 
   using G = typename Unit<MODE, CL>::G;
   const int cta = ps.vrank & (PAIR - 1);  // position in the pair
   const bool mc2 = MC == 2 && ps.mc2;     // B shared with the other pair by multicast
-  const int half = ps.hw_rank / PAIR;     // mc2: the B half this CTA multicasts
+  const int half = (ps.hw_rank / PAIR) % 2;  // mc2: the B half this CTA multicasts
   // mc2: this CTA and the one holding the same B columns in the other tile
   const uint16_t mc_mask = static_cast<uint16_t>((1u << ps.hw_rank) | (1u << (ps.hw_rank ^ PAIR)));
   ItemIter<MODE, CL> iter(p, total_mt, ps.vrank, &c);
@@ -1218,8 +1251,9 @@ __device__ void epilogue(const KParams& p, const Smem& s, const Ctl& c, uint32_t
 
     if (MODE == MODE_REDUCE) {
       // arrival counter of this tile's 32-row quarter counts k-slices; quarters
-      // wholly past the last row have nothing to count
-      if (row0 >= w.row_end) continue;
+      // wholly past the last row, and the parts of a region past the last
+      // column (no tile of their own), have nothing to count
+      if (row0 >= w.row_end || ncols <= 0) continue;
       // the rows' adds were issued by eight lanes each: every lane fences its
       // own, and the warp barrier orders them all before the count
       __threadfence();
@@ -1518,7 +1552,7 @@ fused_gemm_kernel(const __grid_constant__ KParams p) {
   constexpr int PAIR = Unit<MODE, CL>::PAIR;
   constexpr int MC = Unit<MODE, CL>::MC;
   using G = typename Unit<MODE, CL>::G;
-  static_assert(CL == 1 || CL == 2 || CL == 4, "cluster of 1, 2 or 4 CTAs");
+  static_assert(CL == 1 || CL == 2 || CL == 4 || CL == 8, "cluster of 1, 2, 4 or 8 CTAs");
   static_assert(MC <= 2, "at most two tiles share a B box");
   extern __shared__ uint8_t smem_raw[];
   uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -1562,7 +1596,7 @@ fused_gemm_kernel(const __grid_constant__ KParams p) {
     for (int i = 0; i < G::STAGES; ++i) {
       mbar_init(smem_u32(&s.full[i]), KS::FULL_COUNT);
       // one commit per pair that reads the stage
-      mbar_init(smem_u32(&s.empty[i]), (MC == 2 && ps.mc2) ? 2 : 1);
+      mbar_init(smem_u32(&s.empty[i]), (MC == 2 && ps.mc2) ? ps.hw_cl / PAIR : 1);
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(smem_u32(&s.tfull[i]), 1);

@@ -65,7 +65,7 @@ struct Launcher {
   // pairs with CL as the preferred size, a multiple of CL of at most
   // 4 * MAX_REGIONS CTAs; 0 if this launch form is not available.
   static int max_ctas_dyn(const DeviceInfo& dev) {
-    static_assert(CL == 4, "regions of two CTA pairs");
+    static_assert(CL == 4 || CL == 8, "regions of two or four CTA pairs");
     if (max_ctas(dev) <= 0) return 0;  // sets the shared memory attribute
     static std::once_flag once;
     static int ctas = 0;
