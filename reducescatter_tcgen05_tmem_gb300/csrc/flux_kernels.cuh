@@ -79,6 +79,11 @@
 // its current one ends and writes it into the region's mailbox in the
 // workspace, from which every role of the region's CTAs reads its units.  In
 // store mode the last units are claimed as two 256-column halves each.
+// CL = 8 (store mode, dynamic schedule only): regions of four pairs, two
+// stacked along M and two side by side along N (512 x 1024 units); in an
+// 8-CTA cluster CTA r shares B with r ^ 2 and A with r ^ 4, each issuing half
+// of the shared boxes as multicasts (A in two 64-row boxes); where an 8-CTA
+// cluster does not fit the region runs as four pair clusters.
 //
 // Every wait is bounded: after timeout_ns (or an iteration cap) the thread
 // records FLUX_ERR_TIMEOUT in the workspace header, raises the per-call abort
