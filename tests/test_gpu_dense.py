@@ -341,3 +341,14 @@ def test_gemm_rs_cluster_form_integer_inputs_bit_exact_and_repeatable(R):
     for o in range(R):
         assert torch.equal(first[o].view(torch.int16), out[o].view(torch.int16))
     assert torch.count_nonzero(ws).item() == 0
+
+
+def test_launch_info_reports_the_dense_launch_shapes():
+    # store mode: regions of 8 CTAs (8-CTA clusters preferred); reduce mode: regions of 4
+    for op, cl in ((fx.FLUX_OP_AG_GEMM, 8), (fx.FLUX_OP_GEMM, 8), (fx.FLUX_OP_GEMM_RS, 4)):
+        info = fx.flux_launch_info(op, fx.FLUX_F16)
+        assert info["cluster_ctas"] == cl, (op, info)
+        sms = torch.cuda.get_device_properties(0).multi_processor_count
+        assert cl <= info["resident_ctas"] <= sms and info["resident_ctas"] % cl == 0, (op, info)
+    with pytest.raises(fx.FluxError):
+        fx.flux_launch_info(fx.FLUX_OP_MOE_AG, fx.FLUX_F16)
