@@ -96,10 +96,11 @@ class ClockSampler:
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
-    def __init__(self, gpu_index: int):
+    def __init__(self, gpu_index: int, out_dir: str = ""):
+        import tempfile
         self.idx = gpu_index
         self.proc = None
-        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_rank{gpu_index}.csv")
+        self.path = os.path.join(out_dir or tempfile.gettempdir(), f"flux_clocks_rank{gpu_index}.csv")
 
     def start(self):
         try:
@@ -367,7 +368,7 @@ def run_ours(args):
 
     st = Step(torch, fx, dev, small=args.small, ops=args.ops.split(",") if args.ops else None)
     tuned = st.tune() if args.tune else None
-    clocks = ClockSampler(local)
+    clocks = ClockSampler(local, args.clocks_dir)
     clocks.start()
     for _ in range(args.warmup):
         st.step()
@@ -670,6 +671,8 @@ def main():
     ap.add_argument("--tune", action="store_true",
                     help="record per-problem launch options (flux_tune_*) before the warm-up")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--clocks-dir", default="",
+                    help="where the raw nvidia-smi samples are written (default: the temp dir)")
     ap.add_argument("--cpu-rows", type=int, default=512)
     ap.add_argument("--cpu-cols", type=int, default=8192)
     ap.add_argument("--cpu-tokens", type=int, default=2048)
