@@ -17,7 +17,8 @@
 //                       MOE_GATHER   STORE with A rows gathered by expert (MoE layer0)
 //                       MOE_SCATTER  gate-weighted fp32 add into the owning token row;
 //                                    after a grid-wide barrier every CTA converts a
-//                                    share of the token rows (MoE layer1)
+//                                    share of the token rows (MoE layer1); the
+//                                    _WIDE form runs 256 x 512 tiles (long K)
 //                       MOE_STAGED   STORE for MoE layer0 whose A rows were first
 //                                    gathered into a grouped staging buffer by every
 //                                    CTA of the same launch (per-tile ready counters)
@@ -174,10 +175,18 @@ enum Mode {
   MODE_MOE_GATHER = 2,
   MODE_MOE_SCATTER = 3,
   MODE_MOE_STAGED = 4,
-  MODE_RS_CLUSTER = 5
+  MODE_RS_CLUSTER = 5,
+  // MOE_SCATTER on 256 x 512 pair tiles with one accumulator: for long
+  // reductions, where the accumulator's fp32 drain is short against the
+  // tile's main loop and the wider tile receives fewer bytes per MMA
+  MODE_MOE_SCATTER_WIDE = 6
 };
+// MoE layer1 (gate-weighted adds into the token rows), either tile width
+__host__ __device__ constexpr bool is_scatter(int mode) {
+  return mode == MODE_MOE_SCATTER || mode == MODE_MOE_SCATTER_WIDE;
+}
 __host__ __device__ constexpr bool is_moe(int mode) {
-  return mode == MODE_MOE_GATHER || mode == MODE_MOE_SCATTER || mode == MODE_MOE_STAGED;
+  return mode == MODE_MOE_GATHER || is_scatter(mode) || mode == MODE_MOE_STAGED;
 }
 constexpr int STAGE_BLK = 32;     // MOE_STAGED: rows per staging block (one ready count)
 constexpr int STAGE_UNROLL = 16;  // MOE_STAGED: 16-byte loads in flight per lane
@@ -419,7 +428,7 @@ struct Work {
 
 // Shape of the work of one cluster of CL CTAs (128 rows of A per CTA).
 //   dense modes, CL 2 / 4: CTA pairs with 256 x 512 tiles (MC pairs share B)
-//   MOE_SCATTER, CL 2: one CTA pair, 256 x 256 tiles
+//   MOE_SCATTER, CL 2: one CTA pair, 256 x 256 tiles (_WIDE: 256 x 512)
 //   MOE_GATHER: single CTAs only (cp.async row gather)
 //   MOE_STAGED, CL 2: one CTA pair, 256 x 512 tiles
 template <int MODE, int CL>
@@ -427,7 +436,8 @@ struct Unit {
   static constexpr bool DENSE = MODE == MODE_STORE || MODE == MODE_REDUCE;
   // RS_CLUSTER: every CTA of the cluster runs its own 128 x 256 tiles
   static constexpr int PAIR = (CL >= 2 && MODE != MODE_RS_CLUSTER) ? 2 : 1;
-  static constexpr int NM = ((DENSE || MODE == MODE_MOE_STAGED) && PAIR == 2) ? 2 : 1;
+  static constexpr int NM =
+      ((DENSE || MODE == MODE_MOE_STAGED || MODE == MODE_MOE_SCATTER_WIDE) && PAIR == 2) ? 2 : 1;
   // pairs side by side along N (share A by multicast) and stacked along M
   // (share B by multicast)
   static constexpr int PN = (DENSE && CL == 8) ? 2 : 1;
@@ -804,7 +814,7 @@ __device__ __forceinline__ bool produce_ksteps(const KParams& p, const Smem& s, 
       const int nc = b_box_col<PAIR>(n0, cta, j);
       const int n = nc < w.n_end ? nc : n0;  // the padding box of a CTA without columns
       const uint32_t dst = sb + j * B_BOX_N * BK * 2;
-      if (MODE == MODE_MOE_SCATTER || MODE == MODE_MOE_STAGED) {
+      if (is_scatter(MODE) || MODE == MODE_MOE_STAGED) {
         if (PAIR == 2) tma_load_3d_pair(dst, &p.tmB[w.r], fbc, n, kc, w.e);
         else tma_load_3d(dst, &p.tmB[w.r], fb, n, kc, w.e);
       } else if (PAIR == 2) {
@@ -1207,7 +1217,7 @@ __device__ void epilogue(const KParams& p, const Smem& s, const Ctl& c, uint32_t
     // per-row routing data
     float gate = 1.0f;
     int tok = 0;
-    if (MODE == MODE_MOE_SCATTER && row_ok) {
+    if (is_scatter(MODE) && row_ok) {
       const int slot = __ldg(p.row_to_slot + row);
       tok = slot / p.topk;
       gate = __ldg(p.topk_w + slot);
@@ -1674,7 +1684,7 @@ fused_gemm_kernel(const __grid_constant__ KParams p) {
     if (PAIR == 2) tmem_dealloc2(tmem_base, TMEM_COLS);
     else tmem_dealloc(tmem_base, TMEM_COLS);
   }
-  if constexpr (MODE == MODE_MOE_SCATTER) finish_token_rows<DT>(p, c, s.misc + 1);
+  if constexpr (is_scatter(MODE)) finish_token_rows<DT>(p, c, s.misc + 1);
   if (dyn) {
     // The last CTA to finish clears the schedule (counter, exit count and
     // mailboxes) so that the workspace is zero again for the next call.  Every

@@ -238,6 +238,10 @@ def _layer1(c, d, h_dev=None, routing=None):
     (4, 512, 256, 768, 8, 2, "f16", True),     # F/R = 192: ragged k tail
     (8, 1024, 512, 2048, 8, 2, "bf16", True),
     (1, 96, 256, 128, 2, 2, "f16", False),
+    # from 48 k-slices on: 256 x 512 tiles (H = 640: the last tile's second half
+    # is past N; F/R = 3104: a 32-deep last k-slice)
+    (2, 256, 640, 6208, 4, 2, "bf16", False),
+    (4, 192, 1024, 12800, 8, 2, "f16", True),
 ])
 def test_layer1_matches_oracle(R, T, H, F, E, topk, dtype, given):
     c = configs.small(configs.CONFIGS["moe"], R=R, T=T, H=H, F=F, E=E, topk=topk, dtype=dtype,

@@ -125,6 +125,9 @@ def _layer1(c, tp, d, h_shards, given_routing):
     (4, 2, 256, 320, 640, 4, 2, "f16", False),
     (2, 2, 256, 512, 512, 4, 2, "bf16", True),
     (8, 1, 96, 136, 256, 8, 3, "f16", False),    # ragged rows and n-tiles
+    # from 48 k-slices per rank on: 256 x 512 tiles
+    (4, 1, 256, 384, 3072, 8, 2, "bf16", True),
+    (8, 2, 128, 520, 6400, 8, 2, "f16", False),  # 8 columns in the last tile
 ])
 def test_ep_layer1_matches_oracle(R, tp, T, H, F, E, topk, dtype, given):
     c = configs.small(configs.CONFIGS["moe"], R=R, T=T, H=H, F=F, E=E, topk=topk, dtype=dtype,
