@@ -330,7 +330,10 @@ flux_status_t flux_moe_ag_grouped_gemm(int R, int T, int H, int F, int E, int to
  * meet at a grid-wide barrier (the launch is sized so that all of them are
  * resident at once; a kernel of another stream that holds SMs the whole time
  * can delay it until timeout_ns, FLUX_ERR_TIMEOUT at wait site 11) and each
- * converts a share of the token rows to 16 bits.
+ * converts a share of the token rows to 16 bits.  Tiles are 256 x 256 on CTA
+ * pairs with two accumulators (each tile's adds overlap the next tile), or,
+ * for reductions of 48 or more 64-deep k-slices (F/R > 3008, also the
+ * per-rank length of flux_moe_ep_gemm_combine), 256 x 512 with one.
  * Requires T and F divisible by R, (F/R) % 8 == 0, H % 8 == 0. */
 flux_status_t flux_moe_grouped_gemm_rs(int R, int T, int H, int F, int E, int topk,
                                        flux_dtype_t dtype, const void* const* h_shards,
