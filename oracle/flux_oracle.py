@@ -43,7 +43,7 @@ import numpy as np
 __all__ = [
     "widen", "round_to", "gemm", "ag_gemm", "gemm_rs", "moe_route",
     "moe_layer0", "moe_layer1", "ag_gemm_at", "gemm_rs_at", "moe_layer0_rows",
-    "moe_layer1_rows", "moe_ep_layer0", "moe_ep_layer1", "moe_topk_gate",
+    "moe_layer1_rows", "moe_ep_layer0", "moe_ep_layer1", "moe_ep_layer1_rows", "moe_topk_gate",
 ]
 
 
@@ -430,5 +430,35 @@ def moe_layer1_rows(h_shards, w2_shards, topk_ids, topk_weights, E: int, dtype: 
                 hrow = widen(np.asarray(h_shards[r])[slot_to_row[t * topk + k]], dtype)
                 v = g[t, k] * (hrow @ widen(np.asarray(w2_shards[r])[e], dtype))
                 acc = v if acc is None else acc + v
+        out.append(acc)
+    return np.asarray(out)
+
+
+def moe_ep_layer1_rows(h, w2_ep, topk_ids, topk_weights, E: int, dtype: str, R: int, o: int, rows,
+                       h_dtype: str | None = None, tp: int = 1):
+    """Owner o's rows ``rows`` (full H width) of :func:`moe_ep_layer1`, token by
+    token (float64): for each slot k of the token, the tp partials of its
+    expert's group (t ascending), weighted by g[t,k] and added k ascending.
+    ``h`` is the full grouped [T*topk x F] matrix, as there."""
+    ids = np.asarray(topk_ids)
+    g = np.asarray(topk_weights, dtype=np.float32).astype(np.float64)
+    T, topk = ids.shape
+    el = E // (R // tp)
+    _, _, slot_to_row, _ = moe_route(ids, E)
+    hd = dtype if h_dtype is None else h_dtype
+    fb = np.asarray(w2_ep[0]).shape[1]
+    out = []
+    for lr in np.asarray(rows, dtype=np.int64):
+        tok = o * (T // R) + int(lr)
+        acc = None
+        for k in range(topk):
+            e = int(ids[tok, k])
+            grp = e // el
+            hrow = widen(np.asarray(h)[slot_to_row[tok * topk + k]], hd)
+            part = None
+            for t in range(tp):
+                v = hrow[t * fb:(t + 1) * fb] @ widen(np.asarray(w2_ep[grp * tp + t])[e % el], dtype)
+                part = v if part is None else part + v
+            acc = g[tok, k] * part if acc is None else acc + g[tok, k] * part
         out.append(acc)
     return np.asarray(out)

@@ -6,7 +6,7 @@ import pytest
 
 import oracle
 from tests.parity import check_close
-from workloads import configs
+from workloads import configs, gen
 from workloads.torch_io import from_device, to_device, torch_dtype
 
 pytestmark = pytest.mark.gpu
@@ -140,3 +140,30 @@ def test_moe_full_size_routing_exact_and_layers_sampled():
         ref = oracle.moe_layer1_rows(d["h_shards"], d["w2_shards"], d["topk_ids"], d["topk_weights"],
                                      c.E, c.dtype, o, lr)
         check_close(got, ref, f"moe layer1 owner {o}")
+
+
+def test_moe_ep_combine_full_size_sampled():
+    # expert parallel, one expert per rank (tp = 1): each rank reduces over the
+    # whole F = 14336 (224 k-slices, the 256 x 512 tile form); every rank reads
+    # the same grouped H [T*topk x F]
+    c = configs.CONFIGS["moe"]
+    d = configs.moe_ep_inputs(c, 1, with_h=False)
+    del d["w1_shards"]
+    n = c.T * c.topk
+    h = gen.normal16((c.seed, 23), (n, c.F), 1.0, c.dtype)
+    Hd = to_device(h, c.dtype)
+    W2 = [to_device(w, c.dtype) for w in d["w2_shards"]]
+    ids = torch.from_numpy(d["topk_ids"]).cuda()
+    gw = torch.from_numpy(d["topk_weights"]).cuda()
+    Y = [torch.full((c.T // c.R, c.H), float("nan"), dtype=torch_dtype(c.dtype), device="cuda")
+         for _ in range(c.R)]
+    ws = _ws(fx.flux_moe_workspace_size(fx.FLUX_OP_MOE_EP_RS, c.R, c.T, c.H, c.F, c.E, c.topk))
+    fx.flux_moe_ep_gemm_combine(c.R, 1, c.T, c.H, c.F, c.E, c.topk, DT[c.dtype], [Hd] * c.R, W2,
+                                ids, gw, None, None, None, Y, ws)
+    _ok(ws)
+    for o in (0, c.R - 1):
+        lr = np.array([0, c.T // c.R - 1, 301])
+        got = oracle.widen(from_device(Y[o])[lr], c.dtype)
+        ref = oracle.moe_ep_layer1_rows(h, d["w2_shards"], d["topk_ids"], d["topk_weights"], c.E,
+                                        c.dtype, c.R, o, lr)
+        check_close(got, ref, f"moe ep combine owner {o}")

@@ -441,6 +441,20 @@ def test_moe_ep_layer1_equals_tp_with_row_blocks():
         assert np.allclose(y_ep[o], y_tp[o], rtol=1e-12, atol=1e-12)
 
 
+@pytest.mark.parametrize("tp", [1, 2])
+def test_moe_ep_layer1_rows_match_full(tp):
+    c, d = _moe_small(R=2, T=8, H=6, F=8, E=4, topk=2)
+    W1, W2, _, _, _, _ = _ep_weights(c)
+    _, w2 = _eptp_shards(W1, W2, c.R, tp)
+    h = gen.normal16((22, tp), (c.T * c.topk, c.F), 1.0, "f16")
+    y = oracle.moe_ep_layer1(h, w2, d["topk_ids"], d["topk_weights"], c.E, "f16", c.R, tp=tp)
+    lr = np.array([0, 3, 2])
+    for o in range(c.R):
+        got = oracle.moe_ep_layer1_rows(h, w2, d["topk_ids"], d["topk_weights"], c.E, "f16", c.R,
+                                        o, lr, tp=tp)
+        assert np.allclose(got, y[o][lr], rtol=1e-13, atol=1e-14)
+
+
 def test_moe_ep_chain_brute_force_integers():
     # per token, per slot, in exact rationals: y_t = sum_k g (x_t W1_e) W2_e
     c, d = _moe_small(R=2, T=4, H=3, F=4, E=2, topk=2, dist="int")
