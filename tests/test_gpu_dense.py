@@ -90,6 +90,7 @@ def _ag_case(c, ready=None, opts=None):
     (4, 512, 1024, 320, "bf16"),
     (8, 320, 576, 200, "f16"),     # 40 rows per shard (8-row boxes), ragged N and K tails
     (8, 1024, 2048, 128, "bf16"),  # shard = 128 rows: rank-rotated m order
+    (16, 512, 2048, 256, "f16"),   # the most ranks a call takes: 32-row shards, 128 columns each
 ])
 def test_ag_gemm_matches_oracle(R, M, N, K, dtype):
     c = configs.small(configs.CONFIGS["ag_mlp0"], R=R, M=M, N=N, K=K, dtype=dtype, seed=20 + R)
@@ -156,6 +157,8 @@ def test_rs_config_r2_small_matches_oracle():
     (8, 128, 2048, 4096, "bf16", 0),    # decode-like: split along K over the grid
     (8, 128, 2048, 4096, "bf16", 5),    # odd grid: k ranges straddle tiles
     (1, 300, 136, 200, "f16", 0),
+    (16, 256, 512, 2048, "bf16", 0),    # the most ranks a call takes: 16-row owner chunks
+    (16, 128, 1024, 8192, "bf16", 0),   # decode-like at 16 ranks: 8-row owner chunks, stream-K
 ])
 def test_gemm_rs_matches_oracle(R, M, N, K, dtype, num_ctas):
     c = configs.small(configs.CONFIGS["rs_mlp1"], R=R, M=M, N=N, K=K, dtype=dtype, seed=40 + R)

@@ -143,6 +143,7 @@ def _layer0(c, d=None, flags=None, opts=None):
     (8, 1024, 512, 2048, 8, 2, "bf16", ()),    # the MoE workload's structure, reduced
     (1, 64, 64, 256, 3, 1, "f16", ()),
     (2, 200, 136, 256, 5, 3, "bf16", ()),      # H = 136: a 16-byte row tail in the staging copy
+    (16, 1024, 256, 4096, 8, 2, "bf16", ()),   # the most ranks a call takes: 64 tokens per shard
 ])
 def test_layer0_matches_oracle(R, T, H, F, E, topk, dtype, empty, pull):
     # staged: every CTA first copies a share of the grouped rows, then CTA pairs
@@ -242,6 +243,7 @@ def _layer1(c, d, h_dev=None, routing=None):
     # is past N; F/R = 3104: a 32-deep last k-slice)
     (2, 256, 640, 6208, 4, 2, "bf16", False),
     (4, 192, 1024, 12800, 8, 2, "f16", True),
+    (16, 512, 256, 4096, 8, 2, "f16", True),   # the most ranks a call takes: 32 tokens per owner
 ])
 def test_layer1_matches_oracle(R, T, H, F, E, topk, dtype, given):
     c = configs.small(configs.CONFIGS["moe"], R=R, T=T, H=H, F=F, E=E, topk=topk, dtype=dtype,
