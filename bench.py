@@ -516,7 +516,9 @@ def e2e_measure(torch, st, args, dev):
     host_out = [torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in dev_out(0)]
     h2d = sum(t.numel() * t.element_size() for t in host_in)
     d2h = sum(t.numel() * t.element_size() for t in host_out)
-    n = max(3, args.steps // 2)
+    # as many steps as the device-timed region, so that both run equally long
+    # under the power limit
+    n = max(3, args.steps)
     comp = torch.cuda.current_stream()
     cp = torch.cuda.Stream()
     ev = lambda: torch.cuda.Event()  # noqa: E731
