@@ -80,6 +80,21 @@ def max_over_ranks(value: float) -> float:
     return float(t.item())
 
 
+def pg_timeout_s() -> float:
+    """How long a rank waits in a host collective for the others.  A replica
+    that died or never arrives ends the other ranks' next collective with an
+    error after this time instead of holding their GPUs indefinitely."""
+    return float(os.environ.get("FLUX_BENCH_PG_TIMEOUT_S", "600"))
+
+
+def dist_init():
+    """Host process group of the replicas (gloo: the timing max is the only
+    cross-rank step; no tensor of the path crosses ranks)."""
+    import datetime
+    import torch.distributed as td
+    td.init_process_group("gloo", timeout=datetime.timedelta(seconds=pg_timeout_s()))
+
+
 def dist_env():
     ws = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -358,8 +373,7 @@ def run_ours(args):
     import torch
     ws_, rank, local = dist_env()
     if ws_ > 1:
-        import torch.distributed as td
-        td.init_process_group("gloo")
+        dist_init()
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
     import __graft_entry__

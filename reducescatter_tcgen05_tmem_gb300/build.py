@@ -8,6 +8,7 @@ Usage:  python -m reducescatter_tcgen05_tmem_gb300.build  [--verbose]
 """
 from __future__ import annotations
 
+import fcntl
 import os
 import shutil
 import subprocess
@@ -52,17 +53,32 @@ def _run(cmd, verbose):
     return r.stdout + r.stderr
 
 
-def build(verbose: bool = False, force: bool = False) -> str:
-    """Compile and link; returns the path of the shared library."""
-    nvcc = _nvcc()
-    os.makedirs(BUILD, exist_ok=True)
+def _up_to_date() -> bool:
     deps = [os.path.join(CSRC, f) for f in os.listdir(CSRC)]
     deps.append(os.path.join(os.path.dirname(HERE), "include", "flux_gb300.h"))
-    newest = max(os.path.getmtime(d) for d in deps)
-    if (not force and os.path.exists(LIB_PATH) and os.path.getmtime(LIB_PATH) >= newest
-            and os.path.getmtime(LIB_PATH) >= os.path.getmtime(__file__)):
-        return LIB_PATH
+    deps.append(__file__)
+    return os.path.exists(LIB_PATH) and os.path.getmtime(LIB_PATH) >= max(
+        os.path.getmtime(d) for d in deps)
 
+
+def build(verbose: bool = False, force: bool = False) -> str:
+    """Compile and link; returns the path of the shared library.
+
+    Several processes may call this at once (one per rank of a multi-GPU
+    launch): they take turns on a lock file, and whoever comes after a
+    finished build finds the library up to date and returns."""
+    nvcc = _nvcc()
+    os.makedirs(BUILD, exist_ok=True)
+    if not force and _up_to_date():
+        return LIB_PATH
+    with open(os.path.join(BUILD, ".lock"), "w") as lock:
+        fcntl.flock(lock, fcntl.LOCK_EX)
+        if not force and _up_to_date():
+            return LIB_PATH
+        return _build_locked(nvcc, verbose)
+
+
+def _build_locked(nvcc: str, verbose: bool) -> str:
     def compile_one(src):
         obj = os.path.join(BUILD, src.replace(".cu", ".o"))
         _run([nvcc, *ARCH, *CFLAGS, "-c", os.path.join(CSRC, src), "-o", obj], verbose)
@@ -71,7 +87,7 @@ def build(verbose: bool = False, force: bool = False) -> str:
     with ThreadPoolExecutor(len(SOURCES)) as ex:
         objs = list(ex.map(compile_one, SOURCES))
     libdir = _cuda_lib_dir(nvcc)
-    tmp = LIB_PATH + ".tmp"
+    tmp = f"{LIB_PATH}.tmp{os.getpid()}"
     _run([nvcc, *ARCH, "-shared", "-cudart", "shared", "-o", tmp, *objs,
           f"-L{libdir}", "-Xlinker", f"-rpath={libdir}"], verbose)
     os.replace(tmp, LIB_PATH)
