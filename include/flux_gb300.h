@@ -251,8 +251,10 @@ flux_status_t flux_mlp_ag_rs(int R, int M, int H, int F, flux_dtype_t dtype,
  *   - The first call on a device looks up the array's device address (with
  *     that device current); make it before any stream capture begins.
  *   - All calls on a device share the array and it keeps the last call's
- *     contents; each call zeroes the part it uses on `stream` first.  Calls
- *     that overlap on the GPU race on it: order them (one stream or events).
+ *     contents; each call checks its arguments first (a refused call leaves
+ *     the stream and the array alone), then zeroes the part it uses on
+ *     `stream`.  Calls that overlap on the GPU race on it: order them (one
+ *     stream or events).
  *   - Device-side status (flux_get_status) is not available for these calls. */
 #define FLUX_NOALLOC_SCRATCH_BYTES (16u * 1024u * 1024u)
 flux_status_t flux_gemm_rs_noalloc(int R, int M, int N, int K, flux_dtype_t dtype,

@@ -133,34 +133,42 @@ def gemm_rs(a_shards, b_shards, dtype: str):
 
 
 def ag_gemm_at(x_shards, w_shards, dtype: str, r: int, rows, cols) -> np.ndarray:
-    """Output1_r[rows[i], cols[i]] for sampled index pairs (float64)."""
+    """Output1_r[rows[i], cols[i]] for sampled index pairs (float64): the dot
+    product of gathered row rows[i] of X with column cols[i] of W1_r (only the
+    sampled columns of W1_r are widened)."""
     rows = np.asarray(rows, dtype=np.int64)
     cols = np.asarray(cols, dtype=np.int64)
     m_local = np.asarray(x_shards[0]).shape[0]
     out = np.empty(rows.shape[0], dtype=np.float64)
-    w = widen(w_shards[r], dtype)
-    for i, (row, col) in enumerate(zip(rows, cols)):
-        s, lr = divmod(int(row), m_local)
-        xrow = widen(np.asarray(x_shards[s])[lr], dtype)
-        out[i] = float(np.dot(xrow, w[:, col]))
+    ucols, cidx = np.unique(cols, return_inverse=True)
+    w = widen(np.asarray(w_shards[r])[:, ucols], dtype)  # [K x sampled columns]
+    xrows = {}
+    for i, (row, ci) in enumerate(zip(rows, cidx)):
+        if int(row) not in xrows:
+            s, lr = divmod(int(row), m_local)
+            xrows[int(row)] = widen(np.asarray(x_shards[s])[lr], dtype)
+        out[i] = float(np.dot(xrows[int(row)], w[:, ci]))
     return out
 
 
 def gemm_rs_at(a_shards, b_shards, dtype: str, o: int, rows, cols) -> np.ndarray:
-    """Output2_o[rows[i], cols[i]] (rows local to owner o) for sampled pairs."""
+    """Output2_o[rows[i], cols[i]] (rows local to owner o) for sampled pairs:
+    sum over ranks r ascending of the dot product of row o M/R + rows[i] of A_r
+    with column cols[i] of B_r (only the sampled rows and columns are widened)."""
     R = len(a_shards)
     M = np.asarray(a_shards[0]).shape[0]
     h = M // R
     rows = np.asarray(rows, dtype=np.int64)
     cols = np.asarray(cols, dtype=np.int64)
+    urows, ridx = np.unique(rows, return_inverse=True)
+    ucols, cidx = np.unique(cols, return_inverse=True)
+    a = [widen(np.asarray(a_shards[r])[o * h + urows], dtype) for r in range(R)]
+    b = [widen(np.asarray(b_shards[r])[:, ucols], dtype) for r in range(R)]
     out = np.zeros(rows.shape[0], dtype=np.float64)
-    for i, (row, col) in enumerate(zip(rows, cols)):
-        g = o * h + int(row)
+    for i, (ri, ci) in enumerate(zip(ridx, cidx)):
         acc = 0.0
         for r in range(R):
-            a = widen(np.asarray(a_shards[r])[g], dtype)
-            b = widen(np.asarray(b_shards[r])[:, col], dtype)
-            acc = acc + float(np.dot(a, b))
+            acc = acc + float(np.dot(a[r][ri], b[r][:, ci]))
         out[i] = acc
     return out
 
@@ -413,25 +421,32 @@ def moe_layer0_rows(x_shards, w1_shards, topk_ids, E: int, dtype: str, r: int, r
 
 def moe_layer1_rows(h_shards, w2_shards, topk_ids, topk_weights, E: int, dtype: str,
                     o: int, rows):
-    """Output_o[rows] (full H width) for sampled owner-local token rows (float64)."""
+    """Output_o[rows] (full H width) for sampled owner-local token rows (float64):
+    for each token t, the sum over ranks r ascending and then slots k ascending
+    of g[t,k] (H_r[row(t,k)] . W2_r[id[t,k]]).  Each rank's weights are widened
+    once, and the products of one (r, k, expert) are taken for all sampled
+    tokens at a time."""
     ids = np.asarray(topk_ids)
     g = np.asarray(topk_weights, dtype=np.float32).astype(np.float64)
     T, topk = ids.shape
     R = len(h_shards)
     _, _, slot_to_row, _ = moe_route(ids, E)
     h = T // R
-    out = []
-    for lr in np.asarray(rows, dtype=np.int64):
-        t = o * h + int(lr)
-        acc = None
-        for r in range(R):
-            for k in range(topk):
-                e = int(ids[t, k])
-                hrow = widen(np.asarray(h_shards[r])[slot_to_row[t * topk + k]], dtype)
-                v = g[t, k] * (hrow @ widen(np.asarray(w2_shards[r])[e], dtype))
-                acc = v if acc is None else acc + v
-        out.append(acc)
-    return np.asarray(out)
+    toks = o * h + np.asarray(rows, dtype=np.int64)
+    acc = None
+    for r in range(R):
+        w = widen(np.asarray(w2_shards[r]), dtype)  # [E, F/R, H]
+        hs = np.asarray(h_shards[r])
+        for k in range(topk):
+            part = np.zeros((toks.shape[0], w.shape[2]), dtype=np.float64)
+            ek = ids[toks, k]
+            for e in np.unique(ek):
+                sel = np.nonzero(ek == e)[0]
+                hrows = widen(hs[slot_to_row[toks[sel] * topk + k]], dtype)
+                part[sel] = hrows @ w[int(e)]
+            v = g[toks, k][:, None] * part
+            acc = v if acc is None else acc + v
+    return acc
 
 
 def moe_ep_layer1_rows(h, w2_ep, topk_ids, topk_weights, E: int, dtype: str, R: int, o: int, rows,

@@ -73,13 +73,30 @@ extern "C" flux_status_t flux_gemm_rs_noalloc(int R, int M, int N, int K, flux_d
   if (M % R || K % R || a_shards == nullptr || b_shards == nullptr || out == nullptr ||
       (dtype != FLUX_F16 && dtype != FLUX_BF16))
     return FLUX_ERR_INVALID_ARG;
+  // Every check flux_gemm_rs makes on the arguments comes first, so that a
+  // call that is going to be refused leaves the stream and the shared array
+  // alone.
+  const int Kr = K / R;
+  if (M > 0 && N > 0) {
+    for (int r = 0; r < R; ++r) {
+      if (a_shards[r] == nullptr || b_shards[r] == nullptr || out[r] == nullptr)
+        return FLUX_ERR_INVALID_ARG;
+      if (!aligned16(a_shards[r]) || !aligned16(b_shards[r]) || !aligned16(out[r]))
+        return FLUX_ERR_UNSUPPORTED;
+    }
+    if (Kr % 8 || N % 8) return FLUX_ERR_UNSUPPORTED;
+  }
   DeviceInfo dev;
   flux_status_t st = current_device(&dev);
   if (st != FLUX_OK) return st;
   void* scratch = nullptr;
   if ((st = scratch_address(&scratch)) != FLUX_OK) return st;
-  // the header, arrival counters and fp32 accumulators must start at zero
-  cudaError_t e = cudaMemsetAsync(scratch, 0, need, static_cast<cudaStream_t>(stream));
-  if (e != cudaSuccess) return cuda_fail(e);
+  // Nothing to reduce (empty output, or a zero-length K that only zero-fills
+  // the outputs): the scratch is not used, so it is not cleared either.
+  if (M > 0 && N > 0 && Kr > 0) {
+    // the header, arrival counters and fp32 accumulators must start at zero
+    cudaError_t e = cudaMemsetAsync(scratch, 0, need, static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e);
+  }
   return flux_gemm_rs(R, M, N, K, dtype, a_shards, b_shards, out, scratch, need, opts, stream);
 }

@@ -141,7 +141,8 @@ def test_ag_gemm_at_matches_full():
     xs = [gen.normal16((8, r), (4, 16), 1.0, "bf16") for r in range(R)]
     ws = [gen.normal16((9, r), (16, 6), 0.02, "bf16") for r in range(R)]
     full = oracle.ag_gemm(xs, ws, "bf16")
-    rows, cols = np.array([0, 7, 3]), np.array([5, 0, 2])
+    # repeated rows and columns included (the helper widens each one once)
+    rows, cols = np.array([0, 7, 3, 7, 0]), np.array([5, 0, 2, 2, 5])
     assert np.allclose(oracle.ag_gemm_at(xs, ws, "bf16", 1, rows, cols),
                        full[1][rows, cols], rtol=1e-14, atol=1e-15)
 
@@ -203,7 +204,7 @@ def test_gemm_rs_at_matches_full():
     As = [gen.normal16((51, r), (6, 8), 1.0, "f16") for r in range(R)]
     Bs = [gen.normal16((52, r), (8, 5), 0.02, "f16") for r in range(R)]
     full = oracle.gemm_rs(As, Bs, "f16")
-    rows, cols = np.array([0, 2, 1]), np.array([4, 0, 3])
+    rows, cols = np.array([0, 2, 1, 2, 0]), np.array([4, 0, 3, 3, 4])  # with repeats
     assert np.allclose(oracle.gemm_rs_at(As, Bs, "f16", 1, rows, cols),
                        full[1][rows, cols], rtol=1e-14, atol=1e-15)
 
@@ -350,7 +351,7 @@ def test_moe_rows_helpers_match_full():
     assert np.allclose(oracle.moe_layer0_rows(d["x_shards"], d["w1_shards"], d["topk_ids"], c.E,
                                               "f16", 1, rows), h[1][rows], rtol=1e-14, atol=1e-15)
     y = oracle.moe_layer1(d["h_shards"], d["w2_shards"], d["topk_ids"], d["topk_weights"], c.E, "f16")
-    lr = np.array([0, 3])
+    lr = np.array([0, 3, 1, 2, 3])  # every owner row, one twice
     assert np.allclose(oracle.moe_layer1_rows(d["h_shards"], d["w2_shards"], d["topk_ids"],
                                               d["topk_weights"], c.E, "f16", 1, lr),
                        y[1][lr], rtol=1e-13, atol=1e-14)
