@@ -365,6 +365,40 @@ class Step:
             if st != self.fx.FLUX_OK:
                 raise RuntimeError(f"device status {st}: {rep}")
 
+    def io_buffers(self):
+        """(inputs, outputs) of the selected ops as attribute names: the
+        activations that enter the chain from the host every step (weights
+        stay resident) and the results that leave it."""
+        o = set(self.ops)
+        ins, outs = [], []
+        if "ag_gemm" in o:
+            ins.append("X")
+        elif "gemm_rs" in o:
+            ins.append("out1")
+        if "gemm_rs" in o:
+            outs.append("out2")
+        elif "ag_gemm" in o:
+            outs.append("out1")
+        if "decode_rs" in o:
+            ins.append("dA")
+            outs.append("dout")
+        if "moe_gate" in o:
+            ins.append("logits")
+        if o & {"moe_layer0", "moe_ep_layer0"}:
+            ins.append("mX")
+        if "moe_layer1" in o:
+            outs.append("mY")
+            if "moe_layer0" not in o:
+                ins.append("mH")
+        elif "moe_layer0" in o:
+            outs.append("mH")
+        if "moe_ep_layer1" in o:
+            if "mY" not in outs:
+                outs.append("mY")
+        elif "moe_ep_layer0" in o:
+            outs.append("eH")
+        return ins, outs
+
     def total_flops(self):
         return sum(self.flops[o] for o in self.ops)
 
@@ -562,17 +596,30 @@ def e2e_measure(torch, st, args, dev):
     step computes: step i+1's inputs go in and step i-1's results come out
     during step i (the order a serving loop would use); the timed region
     spans the first copy in to the last copy out."""
-    in_lists, out_lists = ("X", "dA", "mX"), ("out2", "dout", "mY")
-    sets = [{a: getattr(st, a) for a in in_lists + out_lists + ("logits",)}, {}]
+    in_lists, out_lists = st.io_buffers()
+    sets = [{a: getattr(st, a) for a in in_lists + out_lists}, {}]
     for a in in_lists + out_lists:
-        sets[1][a] = [torch.empty_like(t) for t in sets[0][a]]
-    sets[1]["logits"] = torch.empty_like(sets[0]["logits"])
+        v = sets[0][a]
+        if isinstance(v, list):
+            twin = {}
+            sets[1][a] = [twin.setdefault(t.data_ptr(), torch.empty_like(t)) for t in v]
+        else:
+            sets[1][a] = torch.empty_like(v)
+
+    def _flat(v):
+        v = v if isinstance(v, list) else [v]
+        seen, out = set(), []
+        for t in v:  # a buffer shared by several ranks crosses the link once
+            if t.data_ptr() not in seen:
+                seen.add(t.data_ptr())
+                out.append(t)
+        return out
 
     def dev_in(k):
-        return sum((sets[k][a] for a in in_lists), []) + [sets[k]["logits"]]
+        return sum((_flat(sets[k][a]) for a in in_lists), [])
 
     def dev_out(k):
-        return sum((sets[k][a] for a in out_lists), [])
+        return sum((_flat(sets[k][a]) for a in out_lists), [])
 
     host_in = [torch.empty(t.shape, dtype=t.dtype, pin_memory=True).copy_(t) for t in dev_in(0)]
     host_out = [torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in dev_out(0)]

@@ -111,6 +111,37 @@ typedef struct {
   int32_t moe_stage_ctas;   /* MoE layer0 staged: how many CTAs copy rows before they
                                compute (0 = all; fewer = a communication / computation
                                split of the grid, the others compute from the start) */
+  int32_t rs_tile;          /* GEMM-RS on whole units (dynamic schedule): 0 = the
+                               library's choice; 1 = regions of 4 CTAs, 256 x 512
+                               CTA-pair tiles with one 512-column accumulator, B shared
+                               by multicast between the two pairs; 2 = regions of 8
+                               CTAs, 256 x 256 pair tiles with two accumulators (the
+                               fp32 adds of one tile overlap the next tile's MMAs), A
+                               and B shared by multicast between the four pairs */
+  int32_t moe_l1_ranks;     /* MoE layer1 with tp > 1 ranks per expert group (fewer than
+                               48 k-slices per rank): how many ranks' partials of one
+                               256 x 256 tile a CTA pair computes back to back and sums
+                               in fp32 on chip before its gate-weighted adds into the
+                               token rows (a divisor of tp; tp = all ranks of the
+                               group, one add per slot).  0 or 1 = none: every rank's
+                               partial is added into the token rows on its own (the
+                               default, faster at the measured sizes) */
+  void* trace;              /* optional per-unit trace (device memory, NULL = off): every
+                               CTA of the fused kernel records, per work item, eight
+                               64-bit words -- a tag (unit id + 1 in bits 0..31, rank
+                               in 32..39, first k-slice in 40..63) and %globaltimer
+                               stamps (ns): producer start / last issue, MMA
+                               accumulator free / first operands in / last commit,
+                               epilogue accumulator full / done.  Words 0 and 1
+                               hold the grid size and the records per CTA,
+                               (trace_words - 8) / (8 * grid); CTA b's records
+                               start at word 8 + 8 * b * (records per CTA); later
+                               items of a CTA are dropped; the caller zeroes the
+                               buffer.  Dense ops and MoE layers (not the
+                               cluster ReduceScatter of few rows, not the pull
+                               gather of MoE layer0).  Compiled out when the
+                               library is built with -DFLUX_TRACE=0. */
+  uint64_t trace_words;     /* size of `trace` in 64-bit words */
 } flux_opts_t;
 
 /* What flux_get_status found in a workspace header. */

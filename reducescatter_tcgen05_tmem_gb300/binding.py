@@ -60,7 +60,9 @@ class flux_opts_t(ctypes.Structure):
                 ("timeout_ns", ctypes.c_uint64), ("num_ctas", ctypes.c_int32),
                 ("group_n", ctypes.c_int32), ("tiles_per_group", ctypes.c_int32),
                 ("deterministic_rs", ctypes.c_int32), ("moe_pull_gather", ctypes.c_int32),
-                ("moe_stage_ctas", ctypes.c_int32)]
+                ("moe_stage_ctas", ctypes.c_int32), ("rs_tile", ctypes.c_int32),
+                ("moe_l1_ranks", ctypes.c_int32), ("trace", ctypes.c_void_p),
+                ("trace_words", ctypes.c_uint64)]
 
 
 class flux_device_report_t(ctypes.Structure):
@@ -162,6 +164,11 @@ def _opts(opts):
     if isinstance(opts, dict):
         o = flux_opts_t()
         for k, v in opts.items():
+            if k == "trace" and v is not None and not isinstance(v, int):
+                # a tensor: its address, and its size unless given
+                if "trace_words" not in opts:
+                    o.trace_words = _nbytes(v) // 8
+                v = v.data_ptr()
             setattr(o, k, v)
         opts = o
     return ctypes.byref(opts)

@@ -136,7 +136,7 @@ flux_status_t check_workspace(const void* ws, size_t have, size_t need) {
 
 using namespace flux;
 
-extern "C" int flux_version(void) { return 100; }
+extern "C" int flux_version(void) { return 200; }
 
 extern "C" const char* flux_status_string(flux_status_t s) {
   switch (s) {

@@ -39,6 +39,9 @@ flux_status_t launch_dyn_dt(flux_dtype_t dt, const KParams& p, int grid, cudaStr
 // clusters fit and pairs elsewhere; reduce mode regions of two pairs.
 constexpr int DENSE_CL = 4;
 constexpr int DENSE_CL8 = 8;
+// GEMM-RS form of the whole-unit dynamic schedule when opts->rs_tile is 0
+// (1: regions of 4, 256 x 512 pair tiles; 2: regions of 8, 256 x 256 pair tiles)
+constexpr int DEFAULT_RS_TILE = 1;
 // GEMM-RS of few rows: clusters of 4 CTAs reduce the R partials of a tile
 // through distributed shared memory (each CTA computes R / 4 partials)
 constexpr int RS_CLUSTER_CL = 4;
@@ -53,6 +56,8 @@ void fill_common(KParams& p, const flux_opts_t* opts, void* ws) {
   p.group_n = (opts && opts->group_n > 0) ? opts->group_n : 8;
   p.seq = next_seq();
   p.hdr = static_cast<uint32_t*>(ws);
+  p.trace = opts ? static_cast<unsigned long long*>(opts->trace) : nullptr;
+  p.trace_words = (opts && opts->trace) ? static_cast<long long>(opts->trace_words) : 0;
 }
 
 flux_status_t zero_outputs(void* const* out, int n, size_t bytes, cudaStream_t s) {
@@ -111,6 +116,12 @@ int setup_dyn(KParams& p, flux_dtype_t dt, const DeviceInfo& dev, const flux_opt
     p.split_from = static_cast<int>(p.num_units > g ? p.num_units - g : 0);
   p.num_claims = p.num_units + (p.num_units - p.split_from);
   p.dyn = 1;
+  // regions of pair clusters leave the last claims to the full-cluster ones
+  {
+    const int full = (dt == FLUX_BF16 ? Launcher<MODE, 1, CL>::max_ctas(dev)
+                                      : Launcher<MODE, 0, CL>::max_ctas(dev)) / CL;
+    p.claim_reserve = (opts && opts->num_ctas > 0) ? 0 : full;
+  }
   p.mbox_cap = static_cast<int>(2 * ((p.num_claims + g - 1) / g) + 2);
   p.mbox = reinterpret_cast<uint32_t*>(mbox);
   return grid;
@@ -221,6 +232,8 @@ extern "C" flux_status_t flux_ag_gemm(int R, int M, int N, int K, flux_dtype_t d
                         BK)) != FLUX_OK)
       return st;
     p.out[r] = out[r];
+    if ((st = encode_2d(&p.tmOut[r], dtype, out[r], Nr, M, static_cast<uint64_t>(Nr) * 2, 64, 32)) != FLUX_OK)
+      return st;
   }
   p.R = R;
   p.M = M;
@@ -397,11 +410,36 @@ extern "C" flux_status_t flux_gemm_rs(int R, int M, int N, int K, flux_dtype_t d
   if (!p.deterministic) {
     // dynamic schedule over every SM when the workspace holds its mailboxes
     // (the deterministic order keeps the static schedule: its waits point at
-    // lower units, which must already sit on resident clusters).  Regions of
-    // 4 CTAs: regions of 8 (A shared as well) measured no faster here -- four
-    // pairs in lockstep stall together on their fp32 drains.
+    // lower units, which must already sit on resident clusters).
     const size_t off = rs_min_bytes(M, N);
     const size_t room = workspace_bytes > off ? workspace_bytes - off : 0;
+    const int form = (opts && opts->rs_tile > 0) ? opts->rs_tile : DEFAULT_RS_TILE;
+    if (form == 2) {
+      // regions of 8 CTAs: four pairs of 256 x 256 tiles (two accumulators
+      // each) on the same 512 x 512 units, A shared by multicast between the
+      // pairs side by side along N (two 64-row boxes), B between the pairs
+      // stacked along M
+      using U8 = Unit<MODE_REDUCE, DENSE_CL8>;
+      KParams q = p;
+      for (int r = 0; r < R; ++r)
+        if ((st = encode_2d(&q.tmA[r], dtype, a_shards[r], Kr, M, static_cast<uint64_t>(Kr) * 2, BK,
+                            64)) != FLUX_OK)
+          return st;
+      q.Nt = (N + U8::UNIT_N - 1) / U8::UNIT_N;
+      q.Nt_tile = (N + U8::G::TILE_N - 1) / U8::G::TILE_N;
+      q.Mt = (M + U8::ROWS - 1) / U8::ROWS;
+      const int tiles8 = q.Mt * q.Nt;
+      q.num_units = tiles8 * R;
+      q.total_ksteps = static_cast<long long>(q.num_units) * q.KT;
+      q.stream_k = 0;
+      const int g8 = setup_dyn<MODE_REDUCE, DENSE_CL8>(q, dtype, dev, opts, ws + off, room);
+      if (g8 > 0) {
+        q.tiles_per_group = tiles_per_group(g8, DENSE_CL8, tiles8);
+        if (launch_dyn_dt<MODE_REDUCE, DENSE_CL8>(dtype, q, g8, s) == FLUX_OK) return FLUX_OK;
+      }
+    }
+    // regions of 4 CTAs: two pairs of 256 x 512 tiles stacked along M, B
+    // shared by multicast
     const int dgrid = setup_dyn<MODE_REDUCE, DENSE_CL>(p, dtype, dev, opts, ws + off, room);
     if (dgrid > 0) {
       p.tiles_per_group = tiles_per_group(dgrid, DENSE_CL, tiles);

@@ -93,6 +93,13 @@
 
 #include "flux_ptx.cuh"
 
+// Per-unit tracing: every work item of a CTA can record %globaltimer stamps of
+// its roles into a caller buffer (KParams::trace).  Built in by default; build
+// with -DFLUX_TRACE=0 to compile it out.
+#ifndef FLUX_TRACE
+#define FLUX_TRACE 1
+#endif
+
 namespace flux {
 
 constexpr int BM = 128;  // rows of A per CTA (TMEM lanes)
@@ -124,22 +131,26 @@ static_assert(32 * STG_PITCH <= STG_WARP, "row staging fits");
 //   <1,1> 128 x 256, B 256 columns per CTA, 4 stages of 48 KB, 2 accumulators
 //   <2,1> 256 x 256, B 128 columns per CTA, 6 stages of 32 KB, 2 accumulators
 //   <2,2> 256 x 512, B 256 columns per CTA, 4 stages of 48 KB, 1 accumulator
-template <int PAIR, int NM>
+//   <2,1,8> 256 x 256 with eight epilogue warps (MoE layer1 reducing the rank
+//           partials in registers): 5 stages of 32 KB
+template <int PAIR, int NM, int EW = EPI_WARPS>
 struct Geo {
   static constexpr int TILE_M = BM * PAIR;             // rows of one tile
   static constexpr int TILE_N = BN * NM;               // columns of one tile
   static constexpr int N_MMA = NM;                     // N = 256 MMAs per 16-deep k step
   static constexpr int B_BOXES = TILE_N / PAIR / B_BOX_N;  // 64-column B boxes per CTA and stage
   static constexpr int B_STAGE = B_BOXES * B_BOX_N * BK * 2;
-  static constexpr int STAGES = (192 * 1024) / (A_STAGE + B_STAGE);
+  // the ring gives up the room the epilogue warps beyond four stage in
+  static constexpr int STAGES = (192 * 1024 - (EW - EPI_WARPS) * STG_WARP) / (A_STAGE + B_STAGE);
   static constexpr int ACC_BUFS = 2 / NM;              // accumulators in the 512 TMEM columns
   static constexpr int ACC_COLS = TILE_N;              // TMEM columns of one accumulator
-  static constexpr int SMEM = STAGES * (A_STAGE + B_STAGE) + EPI_WARPS * STG_WARP + 1024 /*align*/ +
+  static constexpr int SMEM = STAGES * (A_STAGE + B_STAGE) + EW * STG_WARP + 1024 /*align*/ +
                               512 /*barriers*/;
   static_assert(ACC_BUFS * ACC_COLS == TMEM_COLS, "TMEM budget");
 };
 constexpr int cmax(int a, int b) { return a > b ? a : b; }
-constexpr int SMEM_BYTES = cmax(Geo<1, 1>::SMEM, cmax(Geo<2, 1>::SMEM, Geo<2, 2>::SMEM));
+constexpr int SMEM_BYTES = cmax(cmax(Geo<1, 1>::SMEM, Geo<2, 1, 8>::SMEM),
+                                cmax(Geo<2, 1>::SMEM, Geo<2, 2>::SMEM));
 
 // First output column of B box j (0..3) of CTA `cta` in a tile starting at
 // column n0.  A single CTA holds columns n0 .. n0+255 in order; a pair splits
@@ -179,11 +190,21 @@ enum Mode {
   // MOE_SCATTER on 256 x 512 pair tiles with one accumulator: for long
   // reductions, where the accumulator's fp32 drain is short against the
   // tile's main loop and the wider tile receives fewer bytes per MMA
-  MODE_MOE_SCATTER_WIDE = 6
+  MODE_MOE_SCATTER_WIDE = 6,
+  // MOE_SCATTER whose CTA pair computes the partials of several ranks for one
+  // 256 x 256 tile back to back (alternating accumulators) and reduces them in
+  // the epilogue warps' registers, so that each token row receives one
+  // gate-weighted add per (slot, rank group) instead of one per rank
+  MODE_MOE_SCATTER_RED = 7
 };
-// MoE layer1 (gate-weighted adds into the token rows), either tile width
+// MoE layer1 (gate-weighted adds into the token rows), any tile form
 __host__ __device__ constexpr bool is_scatter(int mode) {
-  return mode == MODE_MOE_SCATTER || mode == MODE_MOE_SCATTER_WIDE;
+  return mode == MODE_MOE_SCATTER || mode == MODE_MOE_SCATTER_WIDE || mode == MODE_MOE_SCATTER_RED;
+}
+// epilogue warps of a mode: eight where a tile's rank partials are summed in
+// registers (a thread holds 128 fp32 columns of its row), else four
+__host__ __device__ constexpr int epi_warps(int mode) {
+  return mode == MODE_MOE_SCATTER_RED ? 8 : EPI_WARPS;
 }
 __host__ __device__ constexpr bool is_moe(int mode) {
   return mode == MODE_MOE_GATHER || is_scatter(mode) || mode == MODE_MOE_STAGED;
@@ -198,7 +219,8 @@ constexpr int STAGE_UNROLL = 16;  // MOE_STAGED: 16-byte loads in flight per lan
 // exit count (the last CTA out zeroes both).
 enum HdrField {
   H_STATUS = 0, H_WHERE = 1, H_ARG0 = 2, H_ARG1 = 3, H_ABORT = 4,
-  H_CLAIM = 8, H_EXIT = 9, H_GRID = 10, H_GRID_EXIT = 11
+  H_CLAIM = 8, H_EXIT = 9, H_GRID = 10, H_GRID_EXIT = 11,
+  H_FAST = 12  // dynamic schedule: regions that run as one full cluster (registered at start)
 };
 enum WaitSite {
   W_FLAG = 1,
@@ -221,6 +243,7 @@ struct KParams {
   CUtensorMap tmA[MAXR];   // per-rank A operand maps (K-major, 128B swizzle)
   CUtensorMap tmB[MAXR];   // per-rank B operand maps (N-major, 128B swizzle)
   CUtensorMap tmAcc;       // REDUCE: fp32 accumulation rows [M x N], 32 x 32 boxes
+  CUtensorMap tmOut[MAXR]; // store modes: per-rank 16-bit outputs, 64-column x 32-row boxes
   void* out[MAXR];         // per-rank outputs
   const void* xsrc[MAXR];  // MOE_GATHER: per-shard token rows
   int R;
@@ -260,10 +283,18 @@ struct KParams {
   int moe_tp;  // MoE: ranks per expert group (R: tensor parallel, 1: expert parallel)
   int moe_el;  // MoE: experts per group; rank g moe_tp + t holds block t of group g's experts
   int moe_order;  // MoE: unit order (see decode_moe)
+  int moe_rgroup; // MOE_SCATTER_RED: ranks of a group whose partials of one tile are reduced on chip
+  // per-unit trace (nullptr = off): trace_words 64-bit words, TR_FIELDS per record
+  unsigned long long* trace;
+  long long trace_words;
   // dense CL = 4 kernels: units claimed at run time (see the dynamic schedule above)
   int dyn;
   int mbox_cap;    // mailbox entries per region
   uint32_t* mbox;  // [gridDim / 4 regions x mbox_cap] claimed unit + 1, or MBOX_DONE
+  // regions made of pair clusters (slower: no multicast) stop claiming once at
+  // most this many claims are left, and at most as many full-cluster regions
+  // have registered, so that the faster regions take the last units (0 = off)
+  int claim_reserve;
 };
 
 constexpr uint32_t MBOX_DONE = 0xFFFFFFFFu;
@@ -424,7 +455,52 @@ struct Work {
   int e;       // expert (MoE)
   int k0, k1;  // k-slice range of this item
   int tile;    // linear 128-row output-tile id of this CTA's part (REDUCE counters)
+  int rsub;    // MOE_SCATTER_RED: place of this rank's partial in the tile's rank group
+  int rcnt;    // MOE_SCATTER_RED: partials of the tile reduced on chip (the group's size)
+  int uid;     // the unit (or claim) id the item came from (traces)
 };
+
+// Trace record of one work item of one CTA: eight 64-bit words.
+//   0  tag: unit id + 1 (bits 0..31), rank (32..39), k-slice range start (40..63)
+//   1  producer: the item's first k-slice may be issued (flags and claims done)
+//   2  producer: its last k-slice issued
+//   3  MMA (even CTA of a pair): the accumulator is free
+//   4  MMA: the first k-slice's operands have landed
+//   5  MMA: the last k-slice's MMAs issued and committed
+//   6  epilogue (first epilogue warp): the accumulator is full
+//   7  epilogue: the item's stores or adds are issued (for GEMM-RS, its
+//      arrival counted and, if last, its rows converted)
+// The first eight words are a header (word 0: gridDim.x, word 1: records per
+// CTA); the records of CTA b start at trace + 8 + b * items * 8, items =
+// (trace_words - 8) / (8 * gridDim.x); items beyond that are not recorded.
+enum TraceField {
+  TR_TAG = 0, TR_PROD_START = 1, TR_PROD_END = 2, TR_MMA_ACC = 3, TR_MMA_FIRST = 4,
+  TR_MMA_END = 5, TR_EPI_FULL = 6, TR_EPI_END = 7, TR_FIELDS = 8
+};
+
+// Record field `f` of this CTA's item `item` (no-op without a trace buffer).
+__device__ __forceinline__ void trace_put(const KParams& p, int item, int f, unsigned long long v) {
+#if FLUX_TRACE
+  if (p.trace == nullptr) return;
+  const long long per_cta = (p.trace_words - TR_FIELDS) / (TR_FIELDS * static_cast<long long>(gridDim.x));
+  if (item >= per_cta) return;
+  p.trace[TR_FIELDS + (static_cast<long long>(blockIdx.x) * per_cta + item) * TR_FIELDS + f] = v;
+#endif
+}
+__device__ __forceinline__ void trace_now(const KParams& p, int item, int f) {
+#if FLUX_TRACE
+  if (p.trace != nullptr) trace_put(p, item, f, globaltimer());
+#endif
+}
+__device__ __forceinline__ void trace_tag(const KParams& p, int item, const Work& w) {
+#if FLUX_TRACE
+  if (p.trace != nullptr)
+    trace_put(p, item, TR_TAG,
+              (static_cast<unsigned long long>(static_cast<uint32_t>(w.uid + 1))) |
+                  (static_cast<unsigned long long>(w.r & 0xFF) << 32) |
+                  (static_cast<unsigned long long>(w.k0 & 0xFFFFFF) << 40));
+#endif
+}
 
 // Shape of the work of one cluster of CL CTAs (128 rows of A per CTA).
 //   dense modes, CL 2 / 4: CTA pairs with 256 x 512 tiles (MC pairs share B)
@@ -436,19 +512,37 @@ struct Unit {
   static constexpr bool DENSE = MODE == MODE_STORE || MODE == MODE_REDUCE;
   // RS_CLUSTER: every CTA of the cluster runs its own 128 x 256 tiles
   static constexpr int PAIR = (CL >= 2 && MODE != MODE_RS_CLUSTER) ? 2 : 1;
+  // GEMM-RS in regions of 8: 256 x 256 pair tiles (two accumulators, so the
+  // fp32 adds of one tile overlap the next tile's MMAs); the other dense and
+  // wide forms: 256 x 512 pair tiles
   static constexpr int NM =
-      ((DENSE || MODE == MODE_MOE_STAGED || MODE == MODE_MOE_SCATTER_WIDE) && PAIR == 2) ? 2 : 1;
+      (MODE == MODE_REDUCE && CL == 8) ? 1
+      : ((DENSE || MODE == MODE_MOE_STAGED || MODE == MODE_MOE_SCATTER_WIDE) && PAIR == 2) ? 2 : 1;
+  static constexpr int EW = epi_warps(MODE);
   // pairs side by side along N (share A by multicast) and stacked along M
   // (share B by multicast)
   static constexpr int PN = (DENSE && CL == 8) ? 2 : 1;
   static constexpr int PM = MODE == MODE_RS_CLUSTER ? 1 : CL / PAIR / PN;
   static constexpr int MC = PM;
   static constexpr int ROWS = BM * PAIR * PM;
-  using G = Geo<PAIR, NM>;
+  using G = Geo<PAIR, NM, EW>;
   static constexpr int UNIT_N = G::TILE_N * PN;
   static_assert(DENSE || MC == 1, "MoE tiles: no B sharing between pairs");
   static_assert(MODE != MODE_MOE_GATHER || CL == 1, "MoE layer0 gather: single CTAs");
   static_assert(MODE != MODE_MOE_STAGED || CL == 2, "MoE layer0 staged: CTA pairs");
+  static_assert(MODE != MODE_MOE_SCATTER_RED || CL == 2, "MoE layer1 rank reduction: CTA pairs");
+};
+
+template <int MODE, int DT, int CL>
+struct KernelShape {
+  // the cp.async row gather (single-CTA MoE layer0) takes four producer warps
+  static constexpr bool CPASYNC_GATHER = MODE == MODE_MOE_GATHER && CL == 1;
+  static constexpr int PRODUCER_WARPS = CPASYNC_GATHER ? 4 : 1;
+  static constexpr int MMA_WARP = PRODUCER_WARPS;
+  static constexpr int EPI_WARP0 = PRODUCER_WARPS + 1;
+  static constexpr int EPI = epi_warps(MODE);
+  static constexpr int THREADS = 32 * (PRODUCER_WARPS + 1 + EPI);
+  static constexpr int FULL_COUNT = CPASYNC_GATHER ? (BM + 1) : 1;
 };
 
 // AllGather / plain GEMM: unit -> (rank, m-tile, n-tile).  Ranks are the
@@ -578,6 +672,8 @@ __device__ __forceinline__ Work decode_moe(const KParams& p, int u, int total_mt
   w.k0 = 0;
   w.k1 = p.KT;
   w.tile = 0;
+  w.rsub = 0;
+  w.rcnt = 1;
   return w;
 }
 
@@ -599,15 +695,20 @@ struct ItemIter {
   bool dyn, warp_uniform;
   uint32_t* box;     // dynamic: the region's mailbox
   int taken;         // dynamic: mailbox entries read so far
+  int sub;           // MOE_SCATTER_RED: next rank of the current tile's group
 
   __device__ ItemIter(const KParams& p_, int total_mt_, int cta_, const Ctl* ctl_ = nullptr,
                       bool warp_uniform_ = false)
       : p(p_), ctl(ctl_), total_mt(total_mt_), cta(cta_), warp_uniform(warp_uniform_) {
-    if (is_moe(MODE)) {
+    if (MODE == MODE_MOE_SCATTER_RED) {
+      // a unit is one tile of one rank group: moe_rgroup consecutive items
+      num_units = total_mt * p.Nt * (p.moe_tp / p.moe_rgroup);
+    } else if (is_moe(MODE)) {
       num_units = total_mt * p.Nt * p.moe_tp;
     } else {
       num_units = p.num_units;
     }
+    sub = 0;
     u = blockIdx.x / CL;
     stride = gridDim.x / CL;
     dyn = DYN_OK && p.dyn != 0 && ctl != nullptr;
@@ -637,6 +738,7 @@ struct ItemIter {
       w.k0 = 0;
       w.k1 = p.KT;
       w.tile = 0;
+      w.uid = u * MAXR + r;
       return true;
     }
     if (DYN_OK && dyn) {
@@ -662,6 +764,7 @@ struct ItemIter {
       } else {
         w = decode_reduce<CL>(p, id, cta);
       }
+      w.uid = id;
       return true;
     }
     if (MODE == MODE_REDUCE && p.stream_k) {
@@ -673,13 +776,30 @@ struct ItemIter {
       w = decode_reduce<CL>(p, unit, cta);
       w.k0 = k0;
       w.k1 = static_cast<int>(k1);
+      w.uid = unit;
       pos += k1 - k0;
+      return true;
+    }
+    if (MODE == MODE_MOE_SCATTER_RED) {
+      // the group's ranks of one tile back to back on this CTA pair (rank
+      // innermost order: item u * g + sub is rank (u * g + sub) % moe_tp)
+      if (u >= num_units) return false;
+      const int g = p.moe_rgroup;
+      w = decode_moe<CL>(p, u * g + sub, total_mt, cta, Unit<MODE, CL>::G::TILE_N);
+      w.rsub = sub;
+      w.rcnt = g;
+      w.uid = u * g + sub;
+      if (++sub == g) {
+        sub = 0;
+        u += stride;
+      }
       return true;
     }
     if (u >= num_units) return false;
     if (MODE == MODE_STORE) w = decode_store<CL>(p, u, cta);
     else if (MODE == MODE_REDUCE) w = decode_reduce<CL>(p, u, cta);
     else w = decode_moe<CL>(p, u, total_mt, cta, Unit<MODE, CL>::G::TILE_N);
+    w.uid = u;
     u += stride;
     return true;
   }
@@ -692,9 +812,18 @@ struct ItemIter {
 // Store mode: ids from split_from on are the two 256-column halves of the
 // last units; a half without columns is skipped here.
 template <int MODE, int CL>
-__device__ __forceinline__ void claim_unit(const KParams& p, uint32_t* box, int j) {
+__device__ __forceinline__ void claim_unit(const KParams& p, uint32_t* box, int j, bool slow) {
   uint32_t v = MBOX_DONE;
-  if (j < p.mbox_cap - 1) {
+  bool stop = false;
+  if (slow && p.claim_reserve > 0) {
+    // leave the last claims to the full-cluster regions (one each at most);
+    // they registered before their first claim and claim until the counter
+    // runs out, so no unit is left behind
+    const uint32_t fast = min(ld_volatile_u32(p.hdr + H_FAST), static_cast<uint32_t>(p.claim_reserve));
+    const uint32_t seen = ld_volatile_u32(p.hdr + H_CLAIM);
+    stop = fast > 0 && seen + fast >= static_cast<uint32_t>(p.num_claims);
+  }
+  if (j < p.mbox_cap - 1 && !stop) {
     for (;;) {
       const uint32_t u = atomicAdd(p.hdr + H_CLAIM, 1u);
       if (u >= static_cast<uint32_t>(p.num_claims)) break;
@@ -810,7 +939,8 @@ __device__ __forceinline__ bool produce_ksteps(const KParams& p, const Smem& s, 
     }
     for (int j = 0; j < G::B_BOXES; ++j) {
       if (!((bmask >> j) & 1u)) continue;
-      if (MC2 && (j >> 1) != half) continue;  // the partner multicasts this box
+      // the pair stacked with this one multicasts the other half of the boxes
+      if (MC2 && (j * 2) / G::B_BOXES != half) continue;
       const int nc = b_box_col<PAIR>(n0, cta, j);
       const int n = nc < w.n_end ? nc : n0;  // the padding box of a CTA without columns
       const uint32_t dst = sb + j * B_BOX_N * BK * 2;
@@ -845,14 +975,19 @@ __device__ void producer_tma(const KParams& p, const Smem& s, const Ctl& c, int 
   const uint16_t mc_mask = static_cast<uint16_t>((1u << ps.hw_rank) | (1u << (ps.hw_rank ^ PAIR)));
   ItemIter<MODE, CL> iter(p, total_mt, ps.vrank, &c);
   const bool leader = iter.dyn && ps.vrank == 0;
+  const bool slow_region = !ps.mc2;  // a region of pair clusters (no multicast)
   int claimed = 0;  // mailbox entries the leader has written
-  if (leader) claim_unit<MODE, CL>(p, iter.box, claimed++);
+  if (leader) {
+    if (!slow_region) atomicAdd(p.hdr + H_FAST, 1u);  // before its first claim
+    claim_unit<MODE, CL>(p, iter.box, claimed++, slow_region);
+  }
   Work w;
   uint32_t stage = 0, phase = 0;
   uint32_t issued = 0;
   uint32_t ready = (p.flags == nullptr) ? 0xFFFFFFFFu : 0u;
   int staged_mt = -1;  // MOE_STAGED: the last m-unit whose rows were seen staged
   bool ok = true;
+  int item = 0;  // trace record index
   while (ok && iter.next(w)) {
     int nbox_a = w.m0 < w.row_end ? 1 : 0;  // a CTA part wholly past the last row loads no A
     if (MODE == MODE_MOE_STAGED && nbox_a && w.mt != staged_mt) {
@@ -889,12 +1024,14 @@ __device__ void producer_tma(const KParams& p, const Smem& s, const Ctl& c, int 
       // the even CTA's barrier also counts the odd CTA's bytes of the same stage
       bytes += pair_peer_bytes<MODE, G>(p, w);
     }
+    trace_tag(p, item, w);
+    trace_now(p, item, TR_PROD_START);
     // k-slices up to the claim point, the leader's claim of the region's
     // next unit, then the rest (no per-slice branch on either)
     const int claim_k = leader ? max(w.k0, w.k1 - CLAIM_AHEAD) : w.k1;
     for (int seg = 0; seg < 2 && ok; ++seg) {
       const int kb = seg == 0 ? w.k0 : claim_k, ke = seg == 0 ? claim_k : w.k1;
-      if (seg == 1 && leader) claim_unit<MODE, CL>(p, iter.box, claimed++);
+      if (seg == 1 && leader) claim_unit<MODE, CL>(p, iter.box, claimed++, slow_region);
       if (kb >= ke) continue;
       if constexpr (MC == 2) {
         ok = mc2 ? produce_ksteps<MODE, CL, true>(p, s, c, w, kb, ke, nbox_a, bmask, bytes, n0, cta, half,
@@ -906,6 +1043,8 @@ __device__ void producer_tma(const KParams& p, const Smem& s, const Ctl& c, int 
                                              mc_mask, ps.hw_rank, stage, phase, issued);
       }
     }
+    trace_now(p, item, TR_PROD_END);
+    ++item;
   }
   // drain: every issued copy must land before the CTA may exit.  The odd CTA of
   // a pair cannot see its copies complete (they count on the even CTA's
@@ -1042,6 +1181,7 @@ __device__ void mma_issuer(const KParams& p, const Smem& s, const Ctl& c, uint32
     if ((PAIR == 2 ? wait_bar_remote(smem_u32(&s.tempty[b]), (use & 1u) ^ 1u, c, W_TEMPTY, b)
                    : wait_bar(smem_u32(&s.tempty[b]), (use & 1u) ^ 1u, c, W_TEMPTY, b)) != 0)
       break;
+    trace_now(p, it, TR_MMA_ACC);
     tc_fence_after();
     const uint32_t d = tmem_base + b * G::ACC_COLS;
     // 256-column halves of the tile that start below N (a half wholly past N
@@ -1049,6 +1189,7 @@ __device__ void mma_issuer(const KParams& p, const Smem& s, const Ctl& c, uint32
     const int n_live = (G::N_MMA > 1 && w.n0 + BN >= w.n_end) ? 1 : G::N_MMA;
     for (int k = w.k0; k < w.k1; ++k) {
       if (wait_bar(smem_u32(&s.full[stage]), phase, c, W_FULL, stage) != 0) { ok = false; break; }
+      if (k == w.k0) trace_now(p, it, TR_MMA_FIRST);
       tc_fence_after();
       const uint32_t sa = smem_u32(s.a + stage * A_STAGE);
       const uint32_t sb = smem_u32(s.b + stage * G::B_STAGE);
@@ -1077,6 +1218,7 @@ __device__ void mma_issuer(const KParams& p, const Smem& s, const Ctl& c, uint32
     if (!ok) break;
     if (PAIR == 2) umma2_commit_mc(smem_u32(&s.tfull[b]), pair_mask);
     else umma_commit(smem_u32(&s.tfull[b]));
+    trace_now(p, it, TR_MMA_END);
     ++it;
   }
   if (any) {
@@ -1132,15 +1274,19 @@ __device__ __forceinline__ void store_rows_chunk64(void* out, int ldo, long long
 // warp instruction adds four whole rows into their tokens' fp32 rows with
 // red.global.add.v4.f32 (the load/store path, clear of the TMA queue that
 // feeds the main loop).  Rows with row_ok == false add nothing.
+__device__ __forceinline__ float as_f32(uint32_t x) { return __uint_as_float(x); }
+__device__ __forceinline__ float as_f32(float x) { return x; }
+
+template <class T>
 __device__ __forceinline__ void scatter_add_chunk(float* acc, int ld_acc, int col0, int ncols_valid,
                                                   uint32_t sstg, int lane, int tok, bool row_ok,
-                                                  float gate, const uint32_t (&v)[32]) {
+                                                  float gate, const T (&v)[32]) {
   const uint32_t srow = sstg + lane * STG_PITCH;
   __syncwarp();  // the previous chunk's read-back is done
 #pragma unroll
   for (int g = 0; g < 8; ++g) {
-    const float a = __uint_as_float(v[g * 4 + 0]) * gate, b = __uint_as_float(v[g * 4 + 1]) * gate;
-    const float c = __uint_as_float(v[g * 4 + 2]) * gate, d = __uint_as_float(v[g * 4 + 3]) * gate;
+    const float a = as_f32(v[g * 4 + 0]) * gate, b = as_f32(v[g * 4 + 1]) * gate;
+    const float c = as_f32(v[g * 4 + 2]) * gate, d = as_f32(v[g * 4 + 3]) * gate;
     asm volatile("st.shared.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(srow + g * 16), "f"(a), "f"(b),
                  "f"(c), "f"(d) : "memory");
   }
@@ -1196,6 +1342,9 @@ __device__ void epilogue(const KParams& p, const Smem& s, const Ctl& c, uint32_t
                                : smem_u32(&s.tempty[0]);
   const uint32_t sstg = smem_u32(s.stg + q * STG_WARP);
   using G = typename Unit<MODE, CL>::G;
+  // the first epilogue warp records the trace stamps
+  const bool tracer = warp == KernelShape<MODE, DT, CL>::EPI_WARP0 && lane == 0;
+  int nst = 0;  // tensor bulk stores this warp has committed
   while (iter.next(w)) {
     const uint32_t b = it % G::ACC_BUFS;
     const uint32_t use = static_cast<uint32_t>(it / G::ACC_BUFS);
@@ -1207,6 +1356,7 @@ __device__ void epilogue(const KParams& p, const Smem& s, const Ctl& c, uint32_t
                                    : wait_bar(smem_u32(&s.tfull[b]), use & 1u, c, W_TFULL, b);
     wr = __shfl_sync(0xFFFFFFFFu, wr, 0);
     if (wr != 0) break;
+    if (tracer) trace_now(p, it, TR_EPI_FULL);
     tc_fence_after();
     const int row0 = w.m0 + q * 32;       // first of this warp's 32 rows
     const int row = row0 + lane;           // row of the A row space held by this thread
@@ -1229,8 +1379,45 @@ __device__ void epilogue(const KParams& p, const Smem& s, const Ctl& c, uint32_t
         uint32_t v[32], u[32];
         tmem_ld_32x32b_x32(taddr + ch * 64, v);
         tmem_ld_32x32b_x32(taddr + ch * 64 + 32, u);
-        store_rows_chunk64<DT>(p.out[w.r], p.ldo, row0, w.row_end - row0, n0 + ch * 64,
-                               ncols - ch * 64, sstg, lane, v, u);
+        if (row0 + 32 <= w.row_end || w.row_end == p.M) {
+          // the warp's 32 x 64 box, staged in the 128-byte swizzled layout of
+          // the output map, goes out as one tensor bulk store (rows past the
+          // tensor are clipped); two staging boxes per warp alternate
+          const uint32_t buf = sstg + (nst & 1) * STG_BOX;
+          if (nst >= 2) {
+            if (lane == 0) bulk_wait_read<1>();
+            __syncwarp();
+          }
+#pragma unroll
+          for (int g = 0; g < 8; ++g) {
+            const uint32_t(&x)[32] = g < 4 ? v : u;
+            const int b = (g & 3) * 8;
+            asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};"
+                         ::"r"(buf + lane * 128 + ((g ^ (lane & 7)) << 4)),
+                           "r"(pack2<DT>(__uint_as_float(x[b + 0]), __uint_as_float(x[b + 1]))),
+                           "r"(pack2<DT>(__uint_as_float(x[b + 2]), __uint_as_float(x[b + 3]))),
+                           "r"(pack2<DT>(__uint_as_float(x[b + 4]), __uint_as_float(x[b + 5]))),
+                           "r"(pack2<DT>(__uint_as_float(x[b + 6]), __uint_as_float(x[b + 7])))
+                         : "memory");
+          }
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) {
+            tma_store_2d(&p.tmOut[w.r], buf, n0 + ch * 64, row0);
+            bulk_commit();
+          }
+          ++nst;
+        } else {
+          // the warp's rows run past this tile's last row into rows of another
+          // tile (MoE: the next expert's): plain row stores up to the last row,
+          // through the staging rows once no bulk store still reads them
+          if (nst > 0) {
+            if (lane == 0) bulk_wait_read_all();
+            __syncwarp();
+          }
+          store_rows_chunk64<DT>(p.out[w.r], p.ldo, row0, w.row_end - row0, n0 + ch * 64,
+                                 ncols - ch * 64, sstg, lane, v, u);
+        }
       }
     } else {
       // fp32 adds: into this tile's own rows (REDUCE) or the rows' tokens,
@@ -1248,11 +1435,40 @@ __device__ void epilogue(const KParams& p, const Smem& s, const Ctl& c, uint32_t
         __syncwarp();  // the lanes' adds are ordered after lane 0's acquire
         if (!ok_turn) break;  // TMEM stays held: the MMA side times out too
       }
-      for (int ch = 0; ch < G::TILE_N / 32; ++ch) {
-        if (ch * 32 >= ncols) break;  // warp-uniform
-        uint32_t v[32];
-        tmem_ld_32x32b_x32(taddr + ch * 32, v);
-        scatter_add_chunk(p.acc, p.N, n0 + ch * 32, ncols - ch * 32, sstg, lane, key, row_ok, gate, v);
+      if constexpr (MODE == MODE_REDUCE) {
+        // each 32 x 32 fp32 box of the warp goes out as one tensor bulk
+        // reduce-add (the TMA engine reads the staged box and adds it in L2);
+        // two staging boxes per warp alternate
+        if (row0 < w.row_end) {
+          for (int ch = 0; ch < G::TILE_N / 32; ++ch) {
+            if (ch * 32 >= ncols) break;  // warp-uniform
+            uint32_t v[32];
+            tmem_ld_32x32b_x32(taddr + ch * 32, v);
+            const uint32_t buf = sstg + (ch & 1) * STG_BOX;
+            if (ch >= 2) {
+              if (lane == 0) bulk_wait_read<1>();
+              __syncwarp();
+            }
+#pragma unroll
+            for (int g = 0; g < 8; ++g)
+              asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};"
+                           ::"r"(buf + lane * 128 + ((g ^ (lane & 7)) << 4)), "r"(v[g * 4 + 0]),
+                             "r"(v[g * 4 + 1]), "r"(v[g * 4 + 2]), "r"(v[g * 4 + 3]) : "memory");
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) {
+              tma_reduce_add_2d(&p.tmAcc, buf, n0 + ch * 32, row0);
+              bulk_commit();
+            }
+          }
+        }
+      } else {
+        for (int ch = 0; ch < G::TILE_N / 32; ++ch) {
+          if (ch * 32 >= ncols) break;  // warp-uniform
+          uint32_t v[32];
+          tmem_ld_32x32b_x32(taddr + ch * 32, v);
+          scatter_add_chunk(p.acc, p.N, n0 + ch * 32, ncols - ch * 32, sstg, lane, key, row_ok, gate, v);
+        }
       }
     }
     // hand the accumulator back to the MMA warp
@@ -1263,14 +1479,19 @@ __device__ void epilogue(const KParams& p, const Smem& s, const Ctl& c, uint32_t
       else mbar_arrive(smem_u32(&s.tempty[b]));
     }
     ++it;
+    if (tracer && MODE != MODE_REDUCE) trace_now(p, it - 1, TR_EPI_END);
 
     if (MODE == MODE_REDUCE) {
       // arrival counter of this tile's 32-row quarter counts k-slices; quarters
       // wholly past the last row, and the parts of a region past the last
       // column (no tile of their own), have nothing to count
-      if (row0 >= w.row_end || ncols <= 0) continue;
-      // the rows' adds were issued by eight lanes each: every lane fences its
-      // own, and the warp barrier orders them all before the count
+      if (row0 >= w.row_end || ncols <= 0) {
+        if (tracer) trace_now(p, it - 1, TR_EPI_END);
+        continue;
+      }
+      // the box reduces of this quarter have completed
+      if (lane == 0) bulk_wait_all();
+      __syncwarp();
       __threadfence();
       __syncwarp();
       const uint32_t nk = static_cast<uint32_t>(w.k1 - w.k0);
@@ -1296,7 +1517,104 @@ __device__ void epilogue(const KParams& p, const Smem& s, const Ctl& c, uint32_t
         }
         if (lane == 0) atomicExch(cnt, 0u);
       }
+      if (tracer) trace_now(p, it - 1, TR_EPI_END);
     }
+  }
+  if (nst > 0) {
+    if (lane == 0) bulk_wait_all();
+    __syncwarp();
+  }
+}
+
+// MoE layer1 with the rank partials of each tile reduced on chip
+// (MOE_SCATTER_RED, CTA pairs, eight epilogue warps).  The pair computes the
+// partials of a rank group's ranks for one 256 x 256 tile back to back, in
+// alternating accumulators.  Epilogue warp ew (0..7) reads TMEM lane quarter
+// ew % 4 and the 128-column half ew / 4 of each accumulator; every thread keeps
+// its row's 128 columns in registers, taking the group's first partial and
+// adding the others in fp32 in rank order.  An accumulator goes back to the
+// MMA warp as soon as it is read, so the next partial's MMAs do not wait for
+// any global traffic.  After the group's last partial each row, times its
+// slot's gate, is added into its token's fp32 row (row-contiguous
+// red.global.add.v4.f32 through the warp's staging rows): one add per slot
+// and rank group instead of one per rank.
+template <int CL>
+__device__ void epilogue_scatter_red(const KParams& p, const Smem& s, const Ctl& c, uint32_t tmem_base,
+                                     int total_mt, int warp, int ew, const Pos& ps) {
+  using U = Unit<MODE_MOE_SCATTER_RED, CL>;
+  using G = typename U::G;
+  constexpr int PAIR = U::PAIR;
+  constexpr int HALF = G::TILE_N / 2;  // columns per thread
+  constexpr int CH = HALF / 32;        // 32-column TMEM loads per accumulator
+  const int cta = ps.vrank & (PAIR - 1);
+  const int lane = threadIdx.x & 31;
+  const int q = warp & 3;  // TMEM lane quarter this warp may access
+  const int hh = ew >> 2;  // column half of the tile
+  ItemIter<MODE_MOE_SCATTER_RED, CL> iter(p, total_mt, ps.vrank, &c, true);
+  const uint32_t tempty0 = (PAIR == 2 && cta != 0)
+                               ? mapa_shared(smem_u32(&s.tempty[0]), static_cast<uint32_t>(ps.hw_rank & ~1))
+                               : smem_u32(&s.tempty[0]);
+  const uint32_t sstg = smem_u32(s.stg + ew * STG_WARP);
+  float acc[CH][32];
+  Work w;
+  int it = 0;
+  while (iter.next(w)) {
+    const uint32_t b = it % G::ACC_BUFS;
+    const uint32_t use = static_cast<uint32_t>(it / G::ACC_BUFS);
+    int wr = 0;
+    if (lane == 0) {
+      // a few blocking probes first: the bounded slow wait is a call, which
+      // would have to save the 128 running sums around it
+      const uint32_t bar = smem_u32(&s.tfull[b]);
+      bool done = false;
+      for (int k = 0; k < 64 && !done; ++k) done = mbar_try_wait(bar, use & 1u);
+      if (!done)
+        wr = (PAIR == 2 && cta != 0) ? wait_bar_remote(bar, use & 1u, c, W_TFULL, b)
+                                     : wait_bar(bar, use & 1u, c, W_TFULL, b);
+    }
+    wr = __shfl_sync(0xFFFFFFFFu, wr, 0);
+    if (wr != 0) break;
+    if (ew == 0 && lane == 0) trace_now(p, it, TR_EPI_FULL);
+    tc_fence_after();
+    const uint32_t taddr =
+        tmem_base + (static_cast<uint32_t>(q * 32) << 16) + b * G::ACC_COLS + hh * HALF;
+    const bool first = w.rsub == 0;
+#pragma unroll
+    for (int ch = 0; ch < CH; ++ch) {
+      uint32_t v[32];
+      tmem_ld_32x32b_x32(taddr + ch * 32, v);
+#pragma unroll
+      for (int i = 0; i < 32; ++i) acc[ch][i] = first ? __uint_as_float(v[i]) : acc[ch][i] + __uint_as_float(v[i]);
+    }
+    // hand the accumulator back to the MMA warp
+    tc_fence_before();
+    __syncwarp();
+    if (lane == 0) {
+      if (PAIR == 2 && cta != 0) mbar_arrive_remote(tempty0 + b * 8);
+      else mbar_arrive(smem_u32(&s.tempty[b]));
+    }
+    ++it;
+    if (w.rsub + 1 < w.rcnt) {
+      if (ew == 0 && lane == 0) trace_now(p, it - 1, TR_EPI_END);
+      continue;
+    }
+    // the group's sum of this row: gate-weighted add into the token's row
+    const int row = w.m0 + q * 32 + lane;
+    const bool row_ok = row < w.row_end;
+    float gate = 0.0f;
+    int tok = 0;
+    if (row_ok) {
+      const int slot = __ldg(p.row_to_slot + row);
+      tok = slot / p.topk;
+      gate = __ldg(p.topk_w + slot);
+    }
+    const int c0 = w.n0 + hh * HALF;
+    const int ncols = w.n_end - c0;
+#pragma unroll
+    for (int ch = 0; ch < CH; ++ch)
+      if (ch * 32 < ncols)  // warp-uniform
+        scatter_add_chunk(p.acc, p.N, c0 + ch * 32, ncols - ch * 32, sstg, lane, tok, row_ok, gate, acc[ch]);
+    if (ew == 0 && lane == 0) trace_now(p, it - 1, TR_EPI_END);
   }
 }
 
@@ -1549,16 +1867,6 @@ __device__ void stage_rows(const KParams& p, const Ctl& c, int total_mt) {
 }
 
 // ---------------------------------------------------------------- kernel
-template <int MODE, int DT, int CL>
-struct KernelShape {
-  // the cp.async row gather (single-CTA MoE layer0) takes four producer warps
-  static constexpr bool CPASYNC_GATHER = MODE == MODE_MOE_GATHER && CL == 1;
-  static constexpr int PRODUCER_WARPS = CPASYNC_GATHER ? 4 : 1;
-  static constexpr int MMA_WARP = PRODUCER_WARPS;
-  static constexpr int EPI_WARP0 = PRODUCER_WARPS + 1;
-  static constexpr int THREADS = 32 * (PRODUCER_WARPS + 1 + EPI_WARPS);
-  static constexpr int FULL_COUNT = CPASYNC_GATHER ? (BM + 1) : 1;
-};
 
 template <int MODE, int DT, int CL>
 __global__ void __launch_bounds__(KernelShape<MODE, DT, CL>::THREADS, 1)
@@ -1576,7 +1884,7 @@ fused_gemm_kernel(const __grid_constant__ KParams p) {
   s.a = base;
   s.b = base + G::STAGES * A_STAGE;
   s.stg = base + G::STAGES * (A_STAGE + G::B_STAGE);
-  uint64_t* bars = reinterpret_cast<uint64_t*>(s.stg + EPI_WARPS * STG_WARP);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(s.stg + KS::EPI * STG_WARP);
   s.full = bars;
   s.empty = bars + G::STAGES;
   s.tfull = bars + 2 * G::STAGES;
@@ -1615,7 +1923,7 @@ fused_gemm_kernel(const __grid_constant__ KParams p) {
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(smem_u32(&s.tfull[i]), 1);
-      mbar_init(smem_u32(&s.tempty[i]), EPI_WARPS * PAIR);
+      mbar_init(smem_u32(&s.tempty[i]), KS::EPI * PAIR);
     }
     mbar_init(smem_u32(s.drain), 1);
     if (MODE == MODE_RS_CLUSTER) {
@@ -1648,6 +1956,12 @@ fused_gemm_kernel(const __grid_constant__ KParams p) {
       raise_error(c, ST_INVALID, W_SHAPE, blockIdx.x, static_cast<uint32_t>(ps.hw_cl));
   }
 
+#if FLUX_TRACE
+  if (p.trace != nullptr && blockIdx.x == 0 && threadIdx.x == 0 && p.trace_words >= TR_FIELDS) {
+    p.trace[0] = gridDim.x;
+    p.trace[1] = (p.trace_words - TR_FIELDS) / (TR_FIELDS * static_cast<long long>(gridDim.x));
+  }
+#endif
   int total_mt = 0;
   if (is_moe(MODE)) total_mt = __ldg(p.tile_off + p.E);
   if constexpr (MODE == MODE_MOE_STAGED) stage_rows<CL>(p, c, total_mt);
@@ -1672,6 +1986,8 @@ fused_gemm_kernel(const __grid_constant__ KParams p) {
     __syncwarp();
   } else if constexpr (MODE == MODE_RS_CLUSTER) {
     epilogue_rs_cluster<DT, CL>(p, s, c, tmem_base, warp, ps);
+  } else if constexpr (MODE == MODE_MOE_SCATTER_RED) {
+    epilogue_scatter_red<CL>(p, s, c, tmem_base, total_mt, warp, warp - KS::EPI_WARP0, ps);
   } else {
     epilogue<MODE, DT, CL>(p, s, c, tmem_base, total_mt, warp, ps);
   }
@@ -1701,6 +2017,7 @@ fused_gemm_kernel(const __grid_constant__ KParams p) {
       if (threadIdx.x == 0) {
         p.hdr[H_CLAIM] = 0u;
         p.hdr[H_EXIT] = 0u;
+        p.hdr[H_FAST] = 0u;
       }
     }
   }

@@ -172,15 +172,18 @@ extern "C" flux_status_t flux_tune_gemm_rs(int R, int M, int N, int K, flux_dtyp
       cands.push_back(o);
     }
   } else {
-    for (int g : {4, 8, 16})
-      for (int tg : {0, 2}) {
-        flux_opts_t o = base_opts();
-        o.group_n = g;
-        // 0: one rank group per wave; 2: pairs of tiles (the R partials of a
-        // tile in consecutive units)
-        o.tiles_per_group = tg;
-        cands.push_back(o);
-      }
+    for (int form : {1, 2})
+      for (int g : {4, 8, 16})
+        for (int tg : {0, 2}) {
+          flux_opts_t o = base_opts();
+          // regions of 4 with 256 x 512 pair tiles, or of 8 with 256 x 256
+          o.rs_tile = form;
+          o.group_n = g;
+          // 0: one rank group per wave; 2: pairs of tiles (the R partials of a
+          // tile in consecutive units)
+          o.tiles_per_group = tg;
+          cands.push_back(o);
+        }
   }
   return pick(FLUX_OP_GEMM_RS, {R, M, N, K, 0, 0, 0, 0}, dtype, cands,
               [&](const flux_opts_t* o) {
@@ -224,11 +227,18 @@ extern "C" flux_status_t flux_tune_moe_layer1(
     const int32_t* row_to_slot, void* const* out, void* workspace, size_t workspace_bytes,
     void* stream, flux_opts_t* best) {
   std::vector<flux_opts_t> cands;
-  for (int g : {4, 8, 16}) {
-    flux_opts_t o = base_opts();
-    o.group_n = g;
-    cands.push_back(o);
-  }
+  // partials of how many ranks a CTA pair sums on chip (1: none, tp: the
+  // whole group, tp / 2: half groups, twice the units for the same adds x 2)
+  std::vector<int> groups = {1};
+  if (tp > 1) groups.push_back(tp);
+  if (tp % 2 == 0 && tp / 2 > 1) groups.push_back(tp / 2);
+  for (int rg : groups)
+    for (int g : {4, 8, 16}) {
+      flux_opts_t o = base_opts();
+      o.group_n = g;
+      o.moe_l1_ranks = rg;
+      cands.push_back(o);
+    }
   return pick(FLUX_OP_MOE_RS, {R, tp, T, H, F, E, topk, 0}, dtype, cands,
               [&](const flux_opts_t* o) {
                 return flux_moe_ep_gemm_combine(R, tp, T, H, F, E, topk, dtype, h_shards,

@@ -100,18 +100,20 @@ def test_ag_gemm_writes_stay_inside(R, M, N, K, dtype):
         check_close(oracle.widen(from_device(g.outs[r]), dtype), ref[r], f"ag rank {r}")
 
 
-@pytest.mark.parametrize("R,M,N,K,dtype", [
-    (4, 96, 264, 512, "f16"),       # at most 128 rows, 4 ranks: 4-CTA cluster reduction, 24-row owners
-    (2, 64, 1000, 4096, "bf16"),    # few tiles: stream-K, 32-row owners, ragged last n-tile
-    (8, 1088, 2056, 256, "f16"),    # 648 rank tiles: whole units on the dynamic schedule, 136-row owners
+@pytest.mark.parametrize("R,M,N,K,dtype,rs_tile", [
+    (4, 96, 264, 512, "f16", 0),     # at most 128 rows, 4 ranks: 4-CTA cluster reduction, 24-row owners
+    (2, 64, 1000, 4096, "bf16", 0),  # few tiles: stream-K, 32-row owners, ragged last n-tile
+    (8, 1088, 2056, 256, "f16", 1),  # 648 rank tiles: whole units, regions of 4, 136-row owners
+    (8, 1088, 2056, 256, "f16", 2),  # the same on regions of 8 (256 x 256 pair tiles)
 ])
-def test_gemm_rs_writes_stay_inside(R, M, N, K, dtype):
+def test_gemm_rs_writes_stay_inside(R, M, N, K, dtype, rs_tile):
     c = configs.small(configs.CONFIGS["rs_mlp1"], R=R, M=M, N=N, K=K, dtype=dtype, seed=303)
     As, Bs = configs.rs_inputs(c)
     g = Guarded([(M // R, N)] * R, dtype)
     ws = _ws(fx.flux_workspace_size(fx.FLUX_OP_GEMM_RS, R, M, N, K))
     fx.flux_gemm_rs(R, M, N, K, DT[dtype], [to_device(a, dtype) for a in As],
-                    [to_device(b, dtype) for b in Bs], g.outs, ws)
+                    [to_device(b, dtype) for b in Bs], g.outs, ws,
+                    opts={"rs_tile": rs_tile} if rs_tile else None)
     _ok(ws)
     g.check_guards("gemm_rs")
     ref = oracle.gemm_rs(As, Bs, dtype)

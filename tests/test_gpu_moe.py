@@ -214,7 +214,7 @@ def test_layer0_staged_withheld_flag_times_out_and_gpu_stays_usable():
 
 
 # ---------------------------------------------------------------- layer1
-def _layer1(c, d, h_dev=None, routing=None):
+def _layer1(c, d, h_dev=None, routing=None, opts=None):
     dt = c.dtype
     n = c.T * c.topk
     Hs = h_dev if h_dev is not None else [to_device(h, dt) for h in d["h_shards"]]
@@ -228,7 +228,7 @@ def _layer1(c, d, h_dev=None, routing=None):
     if routing is not None:
         _, off, s2r, r2s = routing
     fx.flux_moe_grouped_gemm_rs(c.R, c.T, c.H, c.F, c.E, c.topk, DT[dt], Hs, W2, ids, gw, off, s2r,
-                                r2s, out, ws)
+                                r2s, out, ws, opts=opts)
     st, rep = fx.flux_get_status(ws)
     assert st == fx.FLUX_OK, rep
     return out, ws
@@ -245,7 +245,14 @@ def _layer1(c, d, h_dev=None, routing=None):
     (4, 192, 1024, 12800, 8, 2, "f16", True),
     (16, 512, 256, 4096, 8, 2, "f16", True),   # the most ranks a call takes: 32 tokens per owner
 ])
-def test_layer1_matches_oracle(R, T, H, F, E, topk, dtype, given):
+@pytest.mark.parametrize("l1_ranks", [0, -1, 2], ids=["per-rank-adds", "all-ranks-on-chip", "pairs-on-chip"])
+def test_layer1_matches_oracle(R, T, H, F, E, topk, dtype, given, l1_ranks):
+    # l1_ranks: partials of how many ranks a CTA pair sums on chip before its
+    # adds into the token rows (0: the default, none; -1: all R ranks)
+    if l1_ranks == -1:
+        l1_ranks = R
+    if l1_ranks > 1 and R % l1_ranks:
+        pytest.skip("group size must divide the ranks")
     c = configs.small(configs.CONFIGS["moe"], R=R, T=T, H=H, F=F, E=E, topk=topk, dtype=dtype,
                       seed=80 + R)
     d = configs.moe_inputs(c)
@@ -253,7 +260,7 @@ def test_layer1_matches_oracle(R, T, H, F, E, topk, dtype, given):
     if given:
         ids = d["topk_ids"]
         routing = tuple(torch.from_numpy(a).cuda() for a in oracle.moe_route(ids, E))
-    out, ws = _layer1(c, d, routing=routing)
+    out, ws = _layer1(c, d, routing=routing, opts={"moe_l1_ranks": l1_ranks} if l1_ranks else None)
     ref = oracle.moe_layer1(d["h_shards"], d["w2_shards"], d["topk_ids"], d["topk_weights"], E, dtype)
     for o in range(R):
         check_close(oracle.widen(from_device(out[o]), dtype), ref[o], f"layer1 owner {o}")
@@ -262,6 +269,29 @@ def test_layer1_matches_oracle(R, T, H, F, E, topk, dtype, given):
     tail = -(-T * H * 4 // 256) * 256 // 4
     assert torch.count_nonzero(ws[-tail:]).item() == 0
     assert torch.count_nonzero(ws[:64]).item() == 0
+
+
+@pytest.mark.parametrize("l1_ranks", [0, 4])
+def test_layer1_integer_inputs_bit_exact(l1_ranks):
+    # integer H and W2 in [-2, 2], gates 1/2: every fp32 partial, the on-chip
+    # sum over ranks and the gate-weighted adds are exact, and |2 Y| <= 4 F <=
+    # 1024 keeps every output exact in fp16
+    c = configs.small(configs.CONFIGS["moe"], R=4, T=256, H=256, F=256, E=4, topk=2, dtype="f16",
+                      dist="int", seed=93)
+    d = configs.moe_inputs(c)
+    d["topk_weights"] = np.full_like(d["topk_weights"], 0.5)
+    out, _ = _layer1(c, d, opts={"moe_l1_ranks": l1_ranks} if l1_ranks else None)
+    ref = oracle.moe_layer1(d["h_shards"], d["w2_shards"], d["topk_ids"], d["topk_weights"], c.E,
+                            c.dtype)
+    for o in range(c.R):
+        assert np.array_equal(oracle.widen(from_device(out[o]), c.dtype), ref[o]), o
+
+
+def test_layer1_rank_group_must_divide_the_ranks():
+    c = configs.small(configs.CONFIGS["moe"], R=4, T=256, H=256, F=1024, E=4, topk=2, seed=94)
+    d = configs.moe_inputs(c)
+    with pytest.raises(fx.FluxError, match="INVALID_ARG"):
+        _layer1(c, d, opts={"moe_l1_ranks": 3})
 
 
 def test_layer0_then_layer1_chained():
