@@ -210,7 +210,13 @@ flux_status_t flux_get_status(void* workspace, size_t bytes, void* stream,
 
 /* Plain non-split GEMM: C[M x N] = A[M x K] . B[K x N].
  * The GEMM_non-split baseline of ECT (paper review, section 三, "核心公式").
- * A, B, C device; K = 0 writes zeros. */
+ * A, B, C device; K = 0 writes zeros.  At most 128 rows (M divisible by 4 or
+ * 8, K / S a multiple of 8 and at least 256 for S = 8 or 4 K slices), given
+ * the workspace flux_workspace_size(FLUX_OP_GEMM, 1, M, N, K) asks for then:
+ * K is split into S slices whose fp32 partials are summed on chip (the
+ * few-row GEMM + ReduceScatter form of flux_gemm_rs, the slices in place of
+ * ranks); with less workspace, or opts->num_ctas set, the whole-tile form
+ * runs. */
 flux_status_t flux_gemm(int M, int N, int K, flux_dtype_t dtype, const void* A, const void* B,
                         void* C, void* workspace, size_t workspace_bytes, const flux_opts_t* opts,
                         void* stream);

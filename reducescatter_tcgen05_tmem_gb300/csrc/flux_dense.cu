@@ -80,6 +80,20 @@ size_t rs_min_bytes(int M, int N) {
   return WS_HEADER + rs_counter_bytes(M, N) + static_cast<size_t>(M) * N * sizeof(float);
 }
 
+flux_status_t gemm_rs_impl(int R, int M, int N, int K, flux_dtype_t dtype,
+                           const void* const* a_shards, long long lda, const void* const* b_shards,
+                           void* const* out, void* workspace, size_t workspace_bytes,
+                           const flux_opts_t* opts, void* stream);
+
+// K slices of the few-row plain GEMM (0 = not split): at most 128 rows, each
+// slice at least 256 deep and a multiple of 8, the rows dividing into S chunks.
+int gemm_k_split(int M, int N, int K) {
+  if (M < 1 || M > BM || N < 1 || N % 8) return 0;
+  for (int S : {8, 4})
+    if (M % S == 0 && K % (8 * S) == 0 && K / S >= 256) return S;
+  return 0;
+}
+
 // Whole 512 x 512 units of a dense op over R ranks with `cols` output columns each.
 long long dense_units(int R, int M, int cols) {
   return static_cast<long long>(R) * ((M + DenseUnit::ROWS - 1) / DenseUnit::ROWS) *
@@ -110,7 +124,10 @@ int setup_dyn(KParams& p, flux_dtype_t dt, const DeviceInfo& dev, const flux_opt
   }
   const long long g = grid / CL;
   // store mode, regions of 4: the last g units are claimed as two 256-column
-  // halves, so that the last wave of units ends more evenly over the regions
+  // halves, so that the last wave of units ends more evenly over the regions.
+  // (Regions of 8 take no halves: there a half unit, every pair computing a
+  // 256-column half of its tile, still takes 90 % of a whole unit's time --
+  // the k-slices of the ring are latency-bound below that much work.)
   p.split_from = p.num_units;
   if (MODE == MODE_STORE && CL == 4)
     p.split_from = static_cast<int>(p.num_units > g ? p.num_units - g : 0);
@@ -135,7 +152,14 @@ using namespace flux;
 extern "C" size_t flux_workspace_size(flux_op_t op, int R, int M, int N, int K) {
   if (R < 1 || R > FLUX_MAX_RANKS || M < 0 || N < 0 || K < 0) return 0;
   switch (op) {
-    case FLUX_OP_GEMM:
+    case FLUX_OP_GEMM: {
+      const size_t plain = WS_HEADER + sched_bytes(dense_units(R, M, N / R));
+      // few rows: the split-K form needs the GEMM + ReduceScatter workspace
+      const int S = R == 1 ? gemm_k_split(M, N, K) : 0;
+      if (S == 0) return plain;
+      const size_t split = rs_min_bytes(M, N) + sched_bytes(dense_units(S, M, N));
+      return split > plain ? split : plain;
+    }
     case FLUX_OP_AG_GEMM:
       return WS_HEADER + sched_bytes(dense_units(R, M, N / R));
     case FLUX_OP_GEMM_RS:
@@ -286,16 +310,43 @@ extern "C" flux_status_t flux_ag_gemm(int R, int M, int N, int K, flux_dtype_t d
 extern "C" flux_status_t flux_gemm(int M, int N, int K, flux_dtype_t dtype, const void* A,
                                    const void* B, void* C, void* workspace,
                                    size_t workspace_bytes, const flux_opts_t* opts, void* stream) {
+  // Few rows: one 128-row tile leaves most SMs idle, so K is split into S
+  // slices that play the ranks of a GEMM + ReduceScatter (slice s: columns
+  // [s K/S, (s+1) K/S) of A, the same rows of B), whose partials are summed in
+  // fp32 -- inside 4-CTA clusters through distributed shared memory where the
+  // n-tiles fit, else by k-slice ranges over the grid -- and "owner" o writes
+  // rows [o M/S, (o+1) M/S) of C.
+  const int S = gemm_k_split(M, N, K);
+  if (S > 1 && valid_dtype(dtype) && !(opts && opts->num_ctas > 0) && workspace != nullptr &&
+      workspace_bytes >= rs_min_bytes(M, N) && A != nullptr && B != nullptr && C != nullptr &&
+      aligned16(A) && aligned16(B) && aligned16(C)) {
+    const int Ks = K / S;
+    const void* a[FLUX_MAX_RANKS];
+    const void* b[FLUX_MAX_RANKS];
+    void* c[FLUX_MAX_RANKS];
+    for (int s = 0; s < S; ++s) {
+      a[s] = static_cast<const uint16_t*>(A) + static_cast<size_t>(s) * Ks;
+      b[s] = static_cast<const uint16_t*>(B) + static_cast<size_t>(s) * Ks * N;
+      c[s] = static_cast<uint16_t*>(C) + static_cast<size_t>(s) * (M / S) * N;
+    }
+    return gemm_rs_impl(S, M, N, K, dtype, a, K, b, c, workspace, workspace_bytes, opts, stream);
+  }
   const void* a[1] = {A};
   const void* b[1] = {B};
   void* c[1] = {C};
   return flux_ag_gemm(1, M, N, K, dtype, a, b, c, nullptr, workspace, workspace_bytes, opts, stream);
 }
 
-extern "C" flux_status_t flux_gemm_rs(int R, int M, int N, int K, flux_dtype_t dtype,
-                                      const void* const* a_shards, const void* const* b_shards,
-                                      void* const* out, void* workspace, size_t workspace_bytes,
-                                      const flux_opts_t* opts, void* stream) {
+namespace flux {
+namespace {
+
+// GEMM + ReduceScatter; `lda` is the row pitch of every A shard in elements
+// (K / R for separate shard buffers; the full K when the shards are column
+// slices of one matrix, as in the split-K plain GEMM).
+flux_status_t gemm_rs_impl(int R, int M, int N, int K, flux_dtype_t dtype,
+                           const void* const* a_shards, long long lda, const void* const* b_shards,
+                           void* const* out, void* workspace, size_t workspace_bytes,
+                           const flux_opts_t* opts, void* stream) {
   if (R < 1 || R > FLUX_MAX_RANKS || M < 0 || N < 0 || K < 0 || !valid_dtype(dtype))
     return FLUX_ERR_INVALID_ARG;
   if (M % R || K % R) return FLUX_ERR_INVALID_ARG;
@@ -321,7 +372,7 @@ extern "C" flux_status_t flux_gemm_rs(int R, int M, int N, int K, flux_dtype_t d
 
   KParams p{};
   for (int r = 0; r < R; ++r) {
-    if ((st = encode_2d(&p.tmA[r], dtype, a_shards[r], Kr, M, static_cast<uint64_t>(Kr) * 2, BK,
+    if ((st = encode_2d(&p.tmA[r], dtype, a_shards[r], Kr, M, static_cast<uint64_t>(lda) * 2, BK,
                         BM)) != FLUX_OK)
       return st;
     if ((st = encode_2d(&p.tmB[r], dtype, b_shards[r], N, Kr, static_cast<uint64_t>(N) * 2, B_BOX_N,
@@ -422,7 +473,7 @@ extern "C" flux_status_t flux_gemm_rs(int R, int M, int N, int K, flux_dtype_t d
       using U8 = Unit<MODE_REDUCE, DENSE_CL8>;
       KParams q = p;
       for (int r = 0; r < R; ++r)
-        if ((st = encode_2d(&q.tmA[r], dtype, a_shards[r], Kr, M, static_cast<uint64_t>(Kr) * 2, BK,
+        if ((st = encode_2d(&q.tmA[r], dtype, a_shards[r], Kr, M, static_cast<uint64_t>(lda) * 2, BK,
                             64)) != FLUX_OK)
           return st;
       q.Nt = (N + U8::UNIT_N - 1) / U8::UNIT_N;
@@ -453,6 +504,17 @@ extern "C" flux_status_t flux_gemm_rs(int R, int M, int N, int K, flux_dtype_t d
   if (grid == 0) return FLUX_ERR_CUDA;
   p.tiles_per_group = tiles_per_group(grid, DENSE_CL, tiles);
   return launch_dt<MODE_REDUCE, DENSE_CL>(dtype, p, grid, s);
+}
+
+}  // namespace
+}  // namespace flux
+
+extern "C" flux_status_t flux_gemm_rs(int R, int M, int N, int K, flux_dtype_t dtype,
+                                      const void* const* a_shards, const void* const* b_shards,
+                                      void* const* out, void* workspace, size_t workspace_bytes,
+                                      const flux_opts_t* opts, void* stream) {
+  return gemm_rs_impl(R, M, N, K, dtype, a_shards, R >= 1 ? K / R : 0, b_shards, out, workspace,
+                      workspace_bytes, opts, stream);
 }
 
 extern "C" flux_status_t flux_mlp_ag_rs(int R, int M, int H, int F, flux_dtype_t dtype,

@@ -64,6 +64,43 @@ def test_gemm_integer_inputs_are_bit_exact(dtype):
     assert np.array_equal(oracle.widen(from_device(C), dtype), ref)
 
 
+@pytest.mark.parametrize("M,N,K,dtype", [
+    (128, 8192, 8192, "bf16"),   # 8 K slices, 32 n-tiles on 4-CTA clusters
+    (64, 2048, 4096, "f16"),     # 8 slices, 8-row chunks
+    (100, 1000, 2048, "f16"),    # 4 slices (100 rows), ragged last n-tile
+    (128, 12288, 4096, "bf16"),  # more n-tiles than clusters fit: slices reduced by fp32 adds
+])
+def test_gemm_few_rows_split_k_matches_oracle(M, N, K, dtype):
+    # at most 128 rows: K split into slices whose partials are summed on chip
+    A = gen.normal16((9, 1), (M, K), 1.0, dtype)
+    B = gen.normal16((9, 2), (K, N), 0.02, dtype)
+    C = _out(M, N, dtype)
+    nbytes = fx.flux_workspace_size(fx.FLUX_OP_GEMM, 1, M, N, K)
+    assert nbytes >= M * N * 4  # the split form's fp32 rows
+    ws = _ws(nbytes)
+    for _ in range(2):
+        fx.flux_gemm(M, N, K, DT[dtype], to_device(A, dtype), to_device(B, dtype), C, ws)
+    _ok(ws)
+    ref = oracle.gemm(oracle.widen(A, dtype), oracle.widen(B, dtype))
+    check_close(oracle.widen(from_device(C), dtype), ref, f"few-row gemm {M}x{N}x{K} {dtype}")
+    assert torch.count_nonzero(ws).item() == 0
+
+
+def test_gemm_few_rows_split_k_integer_inputs_bit_exact():
+    # |entries| <= 2, K = 1024: every partial and sum is an integer below 4097, exact in fp32
+    # and (below 2048 in magnitude with high probability; checked) in fp16
+    M, N, K = 128, 2048, 1024
+    A = gen.integers16((10, 1), (M, K), -1, 1, "f16")
+    B = gen.integers16((10, 2), (K, N), -1, 1, "f16")
+    ref = oracle.gemm(oracle.widen(A, "f16"), oracle.widen(B, "f16"))
+    assert np.abs(ref).max() <= 2048
+    C = _out(M, N, "f16")
+    ws = _ws(fx.flux_workspace_size(fx.FLUX_OP_GEMM, 1, M, N, K))
+    fx.flux_gemm(M, N, K, fx.FLUX_F16, to_device(A, "f16"), to_device(B, "f16"), C, ws)
+    _ok(ws)
+    assert np.array_equal(oracle.widen(from_device(C), "f16"), ref)
+
+
 def test_gemm_k_zero_writes_zeros():
     C = _out(64, 64, "f16")
     a = torch.zeros(64, 8, dtype=torch.float16, device="cuda")

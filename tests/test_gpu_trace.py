@@ -27,7 +27,7 @@ def _ws(nbytes):
 
 
 def _check_records(t, units, per_unit):
-    """Every unit id in [0, units) recorded by exactly `per_unit` CTAs; the
+    """Every unit (claim) id in [0, units) recorded by exactly `per_unit` CTAs; the
     stamps of every record in pipeline order, and per CTA in item order."""
     tag_ok = t["unit"] >= 0
     ids, counts = np.unique(t["unit"][tag_ok], return_counts=True)
