@@ -170,9 +170,12 @@ class Step:
     LAUNCHES = {"ag_gemm": 1, "gemm_rs": 1, "decode_rs": 1, "moe_layer0": 2, "moe_layer1": 2,
                 "moe_gate": 1, "moe_ep_layer0": 2, "moe_ep_layer1": 2}
 
-    def __init__(self, torch, fx, dev, small=False, ops=None):
+    def __init__(self, torch, fx, dev, small=False, ops=None, op_opts=None):
         from workloads.torch_io import to_device
         self.torch, self.fx, self.dev = torch, fx, dev
+        # launch options per op (flux_opts_t fields); ops without any use the
+        # library's defaults (or what flux_tune_* recorded)
+        self.op_opts = dict(op_opts or {})
         self.ops = list(ops) if ops else list(self.STEP_OPS)
         unknown = [o for o in self.ops if o not in self.STEP_OPS + self.EXTRA_OPS]
         if unknown:
@@ -200,7 +203,9 @@ class Step:
             self.W1 = [T(w, "f16") for w in w1]
             del xs, w1
             self.flags = torch.ones(ag.R, dtype=torch.int32, device=dev)
-            self.ws_ag = ws(fx.flux_workspace_size(fx.FLUX_OP_AG_GEMM, ag.R, ag.M, ag.N, ag.K))
+            ag_op = fx.FLUX_OP_AG_GEMM_PUSH if self.op_opts.get("ag_gemm", {}).get("ag_push") \
+                else fx.FLUX_OP_AG_GEMM
+            self.ws_ag = ws(fx.flux_workspace_size(ag_op, ag.R, ag.M, ag.N, ag.K))
             self.workspaces.append(self.ws_ag)
         if "ag_gemm" in want or "gemm_rs" in want:
             # Output1: written by the AG-GEMM in the chained step, else the
@@ -297,34 +302,62 @@ class Step:
                 self.run_op("moe_ep_layer0")
         self.launches_per_step = sum(self.LAUNCHES[o] for o in self.ops)
 
-    def run_op(self, name):
+    def run_op(self, name, extra=None):
         fx, ag, rs, dec, moe = self.fx, self.ag, self.rs, self.dec, self.moe
+        o = dict(self.op_opts.get(name, {}))
+        o.update(extra or {})
+        o = o or None
         if name == "ag_gemm":
             fx.flux_ag_gemm(ag.R, ag.M, ag.N, ag.K, fx.FLUX_F16, self.X, self.W1, self.out1, self.flags,
-                            self.ws_ag)
+                            self.ws_ag, opts=o)
         elif name == "gemm_rs":
-            fx.flux_gemm_rs(rs.R, rs.M, rs.N, rs.K, fx.FLUX_F16, self.out1, self.W2, self.out2, self.ws_rs)
+            fx.flux_gemm_rs(rs.R, rs.M, rs.N, rs.K, fx.FLUX_F16, self.out1, self.W2, self.out2, self.ws_rs,
+                            opts=o)
         elif name == "decode_rs":
-            fx.flux_gemm_rs(dec.R, dec.M, dec.N, dec.K, fx.FLUX_BF16, self.dA, self.dW, self.dout, self.ws_dec)
+            fx.flux_gemm_rs(dec.R, dec.M, dec.N, dec.K, fx.FLUX_BF16, self.dA, self.dW, self.dout, self.ws_dec,
+                            opts=o)
         elif name == "moe_layer0":
             fx.flux_moe_ag_grouped_gemm(moe.R, moe.T, moe.H, moe.F, moe.E, moe.topk, fx.FLUX_BF16, self.mX,
                                         self.mW1, self.ids, self.mH, self.counts, self.offsets, self.s2r,
-                                        self.r2s, self.mflags, self.ws_m0)
+                                        self.r2s, self.mflags, self.ws_m0, opts=o)
         elif name == "moe_layer1":
             fx.flux_moe_grouped_gemm_rs(moe.R, moe.T, moe.H, moe.F, moe.E, moe.topk, fx.FLUX_BF16, self.mH,
                                         self.mW2, self.ids, self.gw, self.offsets, self.s2r, self.r2s,
-                                        self.mY, self.ws_m1)
+                                        self.mY, self.ws_m1, opts=o)
         elif name == "moe_gate":
             fx.flux_moe_topk_gate(moe.T, moe.E, moe.topk, self.logits, self.ids, self.gw)
         elif name == "moe_ep_layer0":
             fx.flux_moe_ep_dispatch_gemm(moe.R, self.tp, moe.T, moe.H, moe.F, moe.E, moe.topk,
                                          fx.FLUX_BF16, self.mX, self.eW1, self.ids, self.eH,
                                          self.counts, self.offsets, self.s2r, self.r2s, self.mflags,
-                                         self.ws_e0)
+                                         self.ws_e0, opts=o)
         elif name == "moe_ep_layer1":
             fx.flux_moe_ep_gemm_combine(moe.R, self.tp, moe.T, moe.H, moe.F, moe.E, moe.topk,
                                         fx.FLUX_BF16, self.eH, self.eW2, self.ids, self.gw,
-                                        self.offsets, self.s2r, self.r2s, self.mY, self.ws_e1)
+                                        self.offsets, self.s2r, self.r2s, self.mY, self.ws_e1, opts=o)
+
+    def trace(self, out_dir):
+        """One traced call of every fused op of the step (flux_opts_t.trace):
+        the records go to out_dir/trace_<op>.npy and the summary of each to
+        out_dir/trace_summary.json, which is also returned."""
+        from reducescatter_tcgen05_tmem_gb300 import trace as ftrace
+        torch = self.torch
+        os.makedirs(out_dir, exist_ok=True)
+        buf = torch.zeros(8 + 8 * 152 * 256, dtype=torch.int64, device=self.dev)
+        out = {}
+        for name in self.ops:
+            if name == "moe_gate":
+                continue
+            buf.zero_()
+            self.run_op(name, {"trace": buf})
+            torch.cuda.synchronize()
+            self.check_status()
+            arr = buf.cpu().numpy()
+            np.save(os.path.join(out_dir, f"trace_{name}.npy"), arr)
+            out[name] = ftrace.summary(ftrace.records(arr))
+        with open(os.path.join(out_dir, "trace_summary.json"), "w") as f:
+            json.dump(out, f, indent=1)
+        return out
 
     def tune(self):
         """Record per-problem launch options for this step's ops (flux_tune_*);
@@ -468,7 +501,8 @@ def run_ours(args):
     __graft_entry__.build()
     import reducescatter_tcgen05_tmem_gb300 as fx
 
-    st = Step(torch, fx, dev, small=args.small, ops=args.ops.split(",") if args.ops else None)
+    st = Step(torch, fx, dev, small=args.small, ops=args.ops.split(",") if args.ops else None,
+              op_opts=json.loads(args.op_opts) if args.op_opts else None)
     tuned = st.tune() if args.tune else None
     clocks = ClockSampler(0, args.clocks_dir)
     clocks.start()
@@ -506,6 +540,9 @@ def run_ours(args):
 
     # ------------------------------------------------------------ end to end through the public API
     e2e = e2e_measure(torch, st, args, dev)
+
+    # ------------------------------------------------------------ per-unit traces (on request)
+    traces = st.trace(args.trace_dir) if args.trace_dir else None
 
     # ------------------------------------------------------------ overhead vs plain unsplit GEMMs
     overhead = {}
@@ -560,12 +597,14 @@ def run_ours(args):
                    "dense_kernel_grid": fx.flux_launch_info(fx.FLUX_OP_AG_GEMM, fx.FLUX_F16),
                    "launch_options": ("tuned on this GPU before warm-up (flux_tune_*): "
                                       + json.dumps(tuned, sort_keys=True)) if tuned is not None
+                   else ("per op: " + json.dumps(st.op_opts, sort_keys=True)) if st.op_opts
                    else "library defaults"},
         "roofline": roofline,
         "breakdown": breakdown,
         "overhead_vs_plain_gemm": overhead,
         "e2e": e2e,
         "gpu_launches": st.launches_per_step * args.steps,
+        **({"trace": traces} if traces is not None else {}),
         "clocks": clk,
     }
     if not args.no_cpu_baseline:
@@ -782,6 +821,10 @@ def main():
     ap.add_argument("--tune", action="store_true",
                     help="record per-problem launch options (flux_tune_*) before the warm-up")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--op-opts", default="",
+                    help='launch options per op as JSON, e.g. \'{"gemm_rs": {"rs_tile": 2}}\'')
+    ap.add_argument("--trace-dir", default="",
+                    help="after the timed region, trace one call of each fused op into this directory")
     ap.add_argument("--clocks-dir", default="",
                     help="where the raw nvidia-smi samples are written (default: the temp dir)")
     ap.add_argument("--cpu-rows", type=int, default=512)

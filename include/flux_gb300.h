@@ -89,7 +89,8 @@ typedef enum {
   FLUX_OP_MLP = 5,        /* flux_mlp_ag_rs */
   FLUX_OP_MOE_LAYERS = 6, /* flux_moe_layers */
   FLUX_OP_MOE_EP_AG = 7,  /* flux_moe_ep_dispatch_gemm */
-  FLUX_OP_MOE_EP_RS = 8   /* flux_moe_ep_gemm_combine */
+  FLUX_OP_MOE_EP_RS = 8,  /* flux_moe_ep_gemm_combine */
+  FLUX_OP_AG_GEMM_PUSH = 9 /* flux_ag_gemm with opts->ag_push (the push form) */
 } flux_op_t;
 
 /* Optional per-call settings; pass NULL for the defaults. */
@@ -108,9 +109,10 @@ typedef struct {
                                tiles); 0 (default) = every CTA first stages a share of
                                the grouped rows in the workspace and CTA pairs compute
                                256 x 512 tiles once their rows' ready counts are in */
-  int32_t moe_stage_ctas;   /* MoE layer0 staged: how many CTAs copy rows before they
-                               compute (0 = all; fewer = a communication / computation
-                               split of the grid, the others compute from the start) */
+  int32_t moe_stage_ctas;   /* MoE layer0 staged, and the push form of AllGather + GEMM:
+                               how many CTAs copy rows before they compute (0 = all;
+                               fewer = a communication / computation split of the grid,
+                               the others compute from the start) */
   int32_t rs_tile;          /* GEMM-RS on whole units (dynamic schedule): 0 = the
                                library's choice; 1 = regions of 4 CTAs, 256 x 512
                                CTA-pair tiles with one 512-column accumulator, B shared
@@ -142,6 +144,15 @@ typedef struct {
                                gather of MoE layer0).  Compiled out when the
                                library is built with -DFLUX_TRACE=0. */
   uint64_t trace_words;     /* size of `trace` in 64-bit words */
+  int32_t ag_push;          /* AllGather + GEMM: nonzero = the push form.  Copy CTAs first
+                               push every shard's rows (after its ready flag) into one
+                               gathered copy of X in the workspace and count each 128-row
+                               block; the GEMM tiles wait for their block's count and load A
+                               from the copy.  0 (default) = the pull form: each tile loads
+                               its A rows from the owning shard after the shard's flag.
+                               Needs flux_workspace_size(FLUX_OP_AG_GEMM_PUSH, ...) and the
+                               dynamic schedule; moe_stage_ctas sets the copy CTAs. */
+  int32_t reserved1;
 } flux_opts_t;
 
 /* What flux_get_status found in a workspace header. */

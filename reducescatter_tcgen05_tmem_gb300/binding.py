@@ -44,6 +44,7 @@ FLUX_OP_MLP = 5
 FLUX_OP_MOE_LAYERS = 6
 FLUX_OP_MOE_EP_AG = 7
 FLUX_OP_MOE_EP_RS = 8
+FLUX_OP_AG_GEMM_PUSH = 9
 
 FLUX_MAX_RANKS = 16
 FLUX_MAX_EXPERTS = 1024
@@ -62,7 +63,8 @@ class flux_opts_t(ctypes.Structure):
                 ("deterministic_rs", ctypes.c_int32), ("moe_pull_gather", ctypes.c_int32),
                 ("moe_stage_ctas", ctypes.c_int32), ("rs_tile", ctypes.c_int32),
                 ("moe_l1_ranks", ctypes.c_int32), ("trace", ctypes.c_void_p),
-                ("trace_words", ctypes.c_uint64)]
+                ("trace_words", ctypes.c_uint64), ("ag_push", ctypes.c_int32),
+                ("reserved1", ctypes.c_int32)]
 
 
 class flux_device_report_t(ctypes.Structure):

@@ -144,6 +144,10 @@ int setup_dyn(KParams& p, flux_dtype_t dt, const DeviceInfo& dev, const flux_opt
   return grid;
 }
 
+// Push form of AllGather + GEMM: per 128-row block a ready count, then the
+// gathered copy of X [M x K] (16-bit), after the header and the mailboxes.
+size_t push_counter_bytes(int M) { return round_up(static_cast<size_t>((M + BM - 1) / BM) * 4, WS_ALIGN); }
+
 }  // namespace
 }  // namespace flux
 
@@ -152,6 +156,9 @@ using namespace flux;
 extern "C" size_t flux_workspace_size(flux_op_t op, int R, int M, int N, int K) {
   if (R < 1 || R > FLUX_MAX_RANKS || M < 0 || N < 0 || K < 0) return 0;
   switch (op) {
+    case FLUX_OP_AG_GEMM_PUSH:
+      return WS_HEADER + sched_bytes(dense_units(R, M, N / R)) + push_counter_bytes(M) +
+             round_up(static_cast<size_t>(M) * K * 2, WS_ALIGN);
     case FLUX_OP_GEMM: {
       const size_t plain = WS_HEADER + sched_bytes(dense_units(R, M, N / R));
       // few rows: the split-K form needs the GEMM + ReduceScatter workspace
@@ -274,6 +281,38 @@ extern "C" flux_status_t flux_ag_gemm(int R, int M, int N, int K, flux_dtype_t d
   fill_common(p, opts, workspace);
   // bands of 4 n-tiles (2048 columns) measured best for the 512 x 512 units
   if (!(opts && opts->group_n > 0)) p.group_n = 4;
+  if (opts && opts->ag_push) {
+    // Push form: copy CTAs push every shard's rows into one gathered copy of X
+    // in the workspace (a ready count per 128-row block); the tiles load A
+    // from that copy, so the producers see a single shard of M rows.
+    const size_t sched = sched_bytes(dense_units(R, M, Nr));
+    const size_t need = flux_workspace_size(FLUX_OP_AG_GEMM_PUSH, R, M, N, K);
+    if (workspace_bytes < need) return FLUX_ERR_WORKSPACE;
+    uint8_t* ws = static_cast<uint8_t*>(workspace);
+    p.unit_cnt = reinterpret_cast<uint32_t*>(ws + WS_HEADER + sched);
+    p.stage = ws + WS_HEADER + sched + push_counter_bytes(M);
+    p.push = 1;
+    p.push_rows_total = M;
+    p.push_shard_rows = rows;
+    p.stage_ctas = opts->moe_stage_ctas > 0 ? opts->moe_stage_ctas : 0;
+    p.rows_per_rank = M;
+    for (int r = 0; r < R; ++r) p.xsrc[r] = x_shards[r];
+    KParams q = p;
+    if ((st = encode_2d(&q.tmA[0], dtype, p.stage, K, M, static_cast<uint64_t>(K) * 2, BK, 64)) != FLUX_OK)
+      return st;
+    q.a_box_m = 64;
+    q.Nt = (Nr + Unit<MODE_STORE, DENSE_CL8>::UNIT_N - 1) / Unit<MODE_STORE, DENSE_CL8>::UNIT_N;
+    q.num_units = R * q.Mt * q.Nt;
+    if (!(opts && opts->group_n > 0)) q.group_n = 2;
+    const int g8 = setup_dyn<MODE_STORE, DENSE_CL8>(q, dtype, dev, opts, ws + WS_HEADER, sched);
+    if (g8 > 0 && launch_dyn_dt<MODE_STORE, DENSE_CL8>(dtype, q, g8, s) == FLUX_OK) return FLUX_OK;
+    if ((st = encode_2d(&p.tmA[0], dtype, p.stage, K, M, static_cast<uint64_t>(K) * 2, BK, BM)) != FLUX_OK)
+      return st;
+    p.a_box_m = BM;
+    const int dgrid = setup_dyn<MODE_STORE, DENSE_CL>(p, dtype, dev, opts, ws + WS_HEADER, sched);
+    if (dgrid > 0 && launch_dyn_dt<MODE_STORE, DENSE_CL>(dtype, p, dgrid, s) == FLUX_OK) return FLUX_OK;
+    return FLUX_ERR_UNSUPPORTED;  // the push form runs on the dynamic schedule only
+  }
   // dynamic schedule over every SM when the workspace holds its mailboxes:
   // regions of 8 CTAs (512 x 1024 units, 64-row A boxes that must not
   // straddle two shards), else regions of 4

@@ -276,9 +276,14 @@ struct KParams {
   const int32_t* row_to_slot;  // [T*topk]
   const int32_t* tile_off;     // [E+1] first m-tile of each expert
   const float* topk_w;         // [T*topk]
-  void* stage;                 // MOE_STAGED: grouped A rows [T*topk x H], 16-bit
-  uint32_t* unit_cnt;          // MOE_STAGED: finished staging blocks per m-unit (zeroed by routing)
-  int stage_ctas;              // MOE_STAGED: CTAs that copy rows before computing (0 = all)
+  void* stage;                 // MOE_STAGED: grouped A rows [T*topk x H], 16-bit;
+                               // push AG-GEMM: the gathered X [M x K], 16-bit
+  uint32_t* unit_cnt;          // MOE_STAGED: finished staging blocks per m-unit (zeroed by routing);
+                               // push AG-GEMM: copied 128-row blocks (one count each)
+  int stage_ctas;              // MOE_STAGED / push: CTAs that copy rows before computing (0 = all)
+  int push;                    // STORE: the push form of AllGather + GEMM (see push_rows)
+  int push_rows_total;         // push: rows of X (the shards' rows back to back)
+  int push_shard_rows;         // push: rows per X shard (the producers see one gathered shard)
   int E, topk, T, H;
   int moe_tp;  // MoE: ranks per expert group (R: tensor parallel, 1: expert parallel)
   int moe_el;  // MoE: experts per group; rank g moe_tp + t holds block t of group g's experts
@@ -1000,19 +1005,26 @@ __device__ void producer_tma(const KParams& p, const Smem& s, const Ctl& c, int 
       staged_mt = w.mt;
     }
     if (MODE == MODE_STORE) {
-      // shards covering the valid rows of this CTA's part must be published first
       nbox_a = 0;
       if (w.m0 < w.row_end) {
-        const int last_row = min(w.m0 + BM, w.row_end) - 1;
-        const int s0 = w.m0 / p.rows_per_rank, s1 = last_row / p.rows_per_rank;
-        for (int sh = s0; sh <= s1 && ok; ++sh) {
-          if (!((ready >> sh) & 1u)) {
-            if (!wait_flag(p.flags, sh, p.epoch, c)) ok = false;
-            else ready |= 1u << sh;
+        if (p.push) {
+          // push form: this part's 128-row block of the gathered copy must be
+          // complete (acquire), then visible to this thread's TMA reads
+          if (!wait_count(p.unit_cnt + w.m0 / BM, 1u, c, W_STAGE)) break;
+          fence_proxy_async_global();
+        } else {
+          // shards covering the valid rows of this CTA's part must be published first
+          const int last_row = min(w.m0 + BM, w.row_end) - 1;
+          const int s0 = w.m0 / p.rows_per_rank, s1 = last_row / p.rows_per_rank;
+          for (int sh = s0; sh <= s1 && ok; ++sh) {
+            if (!((ready >> sh) & 1u)) {
+              if (!wait_flag(p.flags, sh, p.epoch, c)) ok = false;
+              else ready |= 1u << sh;
+            }
           }
+          if (!ok) break;
+          if (p.flags != nullptr) fence_proxy_async_global();
         }
-        if (!ok) break;
-        if (p.flags != nullptr) fence_proxy_async_global();
         nbox_a = (min(w.m0 + BM, w.row_end) - w.m0 + p.a_box_m - 1) / p.a_box_m;
       }
     }
@@ -1796,6 +1808,62 @@ __device__ void finish_token_rows(const KParams& p, const Ctl& c, uint32_t* flag
   }
 }
 
+// AllGather + GEMM, push form: the first stage_ctas CTAs (all by default)
+// push the rows of every shard into the gathered copy of X, one 128-row block
+// at a time (blocks dealt to those CTAs in turn, ascending, so that the
+// first units' rows come first); a warp copies a row with 16-byte loads, 16
+// in flight per lane, after the ready flag of the shard that owns it.  When
+// the whole CTA is done with a block it counts the block (release); the GEMM
+// producers of the same launch wait for that count.  Block b of the copy
+// holds rows [128 b, 128 b + 128) of the concatenated shards.
+static __device__ void push_rows(const KParams& p, const Ctl& c) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int nwarps = static_cast<int>(blockDim.x >> 5);
+  const int chunks = p.K / 8;  // 16-byte chunks per row
+  uint32_t ready = (p.flags == nullptr) ? 0xFFFFFFFFu : 0u;
+  const int nblk = (p.push_rows_total + BM - 1) / BM;
+  const int copiers = p.stage_ctas > 0 ? min(p.stage_ctas, static_cast<int>(gridDim.x))
+                                       : static_cast<int>(gridDim.x);
+  if (static_cast<int>(blockIdx.x) >= copiers) return;
+  for (int blk = blockIdx.x; blk < nblk; blk += copiers) {
+    const int row0 = blk * BM;
+    const int nrows = min(BM, p.push_rows_total - row0);
+    int ok = 1;
+    for (int rr = warp; rr < nrows && ok; rr += nwarps) {
+      const int row = row0 + rr;
+      const int sh = row / p.push_shard_rows;
+      if (!((ready >> sh) & 1u)) {
+        if (lane == 0) ok = wait_flag(p.flags, sh, p.epoch, c) ? 1 : 0;
+        ok = __shfl_sync(0xFFFFFFFFu, ok, 0);
+        if (!ok) break;
+        ready |= 1u << sh;
+      }
+      const uint4* src = reinterpret_cast<const uint4*>(
+          static_cast<const char*>(p.xsrc[sh]) + static_cast<size_t>(row - sh * p.push_shard_rows) * p.K * 2);
+      uint4* dst = reinterpret_cast<uint4*>(static_cast<char*>(p.stage) + static_cast<size_t>(row) * p.K * 2);
+      for (int c0 = 0; c0 < chunks; c0 += 32 * STAGE_UNROLL) {
+        uint4 v[STAGE_UNROLL];
+#pragma unroll
+        for (int j = 0; j < STAGE_UNROLL; ++j) {
+          const int ch = c0 + j * 32 + lane;
+          if (ch < chunks) v[j] = __ldg(src + ch);
+        }
+#pragma unroll
+        for (int j = 0; j < STAGE_UNROLL; ++j) {
+          const int ch = c0 + j * 32 + lane;
+          if (ch < chunks) dst[ch] = v[j];
+        }
+      }
+    }
+    // the block's rows, written by every thread, become visible (also to the
+    // readers' TMA) before its count
+    __threadfence();
+    fence_proxy_async_global();
+    if (!__syncthreads_and(ok)) return;  // a shard flag timed out (recorded)
+    if (threadIdx.x == 0) atomicAdd(p.unit_cnt + blk, 1u);
+  }
+}
+
 // MoE layer0, staged: every thread of the first stage_ctas CTAs (all CTAs
 // by default) takes part.  Blocks of 32 grouped rows, in ascending m-unit
 // order, are dealt to those CTAs in turn; a
@@ -1965,6 +2033,9 @@ fused_gemm_kernel(const __grid_constant__ KParams p) {
   int total_mt = 0;
   if (is_moe(MODE)) total_mt = __ldg(p.tile_off + p.E);
   if constexpr (MODE == MODE_MOE_STAGED) stage_rows<CL>(p, c, total_mt);
+  if constexpr (MODE == MODE_STORE) {
+    if (p.push && run) push_rows(p, c);
+  }
 
   const int lane = threadIdx.x & 31;
   if (warp == 0 && lane < p.R) {
@@ -2014,6 +2085,8 @@ fused_gemm_kernel(const __grid_constant__ KParams p) {
       __threadfence();
       const int n = static_cast<int>(gridDim.x / CL) * p.mbox_cap;
       for (int i = threadIdx.x; i < n; i += blockDim.x) p.mbox[i] = 0u;
+      if (MODE == MODE_STORE && p.push)
+        for (int i = threadIdx.x; i < (p.push_rows_total + BM - 1) / BM; i += blockDim.x) p.unit_cnt[i] = 0u;
       if (threadIdx.x == 0) {
         p.hdr[H_CLAIM] = 0u;
         p.hdr[H_EXIT] = 0u;

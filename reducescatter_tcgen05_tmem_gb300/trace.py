@@ -29,3 +29,36 @@ def records(buf) -> dict:
     out["k0"] = (tag >> 40).astype(np.int64)
     out["grid"], out["per_cta"] = grid, per
     return out
+
+
+def summary(rec: dict) -> dict | None:
+    """Where one traced call spent its time, from the records of the CTAs that
+    issue their pair's MMAs (medians over those CTAs; shares of the call's
+    span from the first producer start to the last epilogue end):
+    k-loop (first operands in .. last commit of each unit), waits for the
+    accumulator (last commit of the previous unit .. accumulator free) and for
+    the first operands (accumulator free .. first operands in), and the idle
+    time after the CTA's last unit.  None if nothing was recorded."""
+    ok = rec["unit"] >= 0
+    mma = np.any(rec["mma_end"] > 0, axis=1) & np.any(ok, axis=1)
+    if not np.any(mma):
+        return None
+    t0 = rec["prod_start"][ok].min()
+    t1 = rec["epi_end"][ok].max()
+    span = float(t1 - t0)
+    kl, wacc, wop, idle, items, it_k, it_e = [], [], [], [], [], [], []
+    for b in np.nonzero(mma)[0]:
+        it = np.nonzero(ok[b])[0]
+        ma, mf, me = rec["mma_acc"][b, it], rec["mma_first"][b, it], rec["mma_end"][b, it]
+        kl.append(np.sum(me - mf))
+        wacc.append(np.sum(ma - np.concatenate([[t0], me[:-1]])))
+        wop.append(np.sum(mf - ma))
+        idle.append(t1 - me[-1])
+        items.append(len(it))
+        it_k.extend((me - mf).tolist())
+        it_e.extend((rec["epi_end"][b, it] - rec["epi_full"][b, it]).tolist())
+    med = lambda x: float(np.median(np.asarray(x, dtype=np.float64)))  # noqa: E731
+    return {"span_us": round(span / 1e3, 1), "mma_ctas": int(np.sum(mma)), "units_per_cta": med(items),
+            "kloop_share": round(med(kl) / span, 4), "acc_wait_share": round(med(wacc) / span, 4),
+            "operand_wait_share": round(med(wop) / span, 4), "idle_after_last_share": round(med(idle) / span, 4),
+            "unit_kloop_us": round(med(it_k) / 1e3, 2), "unit_epilogue_us": round(med(it_e) / 1e3, 2)}

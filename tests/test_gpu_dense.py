@@ -164,6 +164,70 @@ def test_ag_gemm_withheld_flag_times_out_and_gpu_stays_usable():
     check_close(oracle.widen(from_device(out[2]), c.dtype), ref[2], "after timeout")
 
 
+# ---------------------------------------------------------------- AllGather + GEMM, push form
+@pytest.mark.parametrize("R,M,N,K,dtype,copiers", [
+    (8, 320, 576, 200, "f16", 0),     # 40-row shards: blocks of 128 rows straddle shards
+    (4, 512, 1024, 320, "bf16", 0),
+    (8, 1024, 2048, 128, "bf16", 8),  # 8 copy CTAs, the others compute from the start
+    (2, 256, 1024, 512, "f16", 1),    # one copy CTA
+    (16, 512, 2048, 256, "f16", 0),   # the most ranks a call takes
+])
+def test_ag_gemm_push_form_matches_pull_and_oracle(R, M, N, K, dtype, copiers):
+    # the push form: copy CTAs push every shard into one gathered copy (ready
+    # count per 128-row block), tiles load A from it; same bits as the pull form
+    c = configs.small(configs.CONFIGS["ag_mlp0"], R=R, M=M, N=N, K=K, dtype=dtype, seed=120 + R)
+    xs, w_s = configs.ag_inputs(c)
+    X = [to_device(x, dtype) for x in xs]
+    W = [to_device(w, dtype) for w in w_s]
+    outs = {}
+    for form in ("pull", "push"):
+        out = [_out(M, N // R, dtype) for _ in range(R)]
+        op = fx.FLUX_OP_AG_GEMM_PUSH if form == "push" else fx.FLUX_OP_AG_GEMM
+        ws = _ws(fx.flux_workspace_size(op, R, M, N, K))
+        opts = {"ag_push": 1, "moe_stage_ctas": copiers} if form == "push" else None
+        flags = torch.ones(R, dtype=torch.int32, device="cuda")
+        for _ in range(2):  # the second call finds the counters the first left at zero
+            fx.flux_ag_gemm(R, M, N, K, DT[dtype], X, W, out, flags, ws, opts=opts)
+        _ok(ws)
+        outs[form] = out
+    ref = oracle.ag_gemm(xs, w_s, dtype)
+    for r in range(R):
+        assert torch.equal(outs["pull"][r].view(torch.int16), outs["push"][r].view(torch.int16)), r
+        check_close(oracle.widen(from_device(outs["push"][r]), dtype), ref[r], f"push ag rank {r}")
+
+
+def test_ag_gemm_push_form_needs_its_workspace():
+    c = configs.small(configs.CONFIGS["ag_mlp0"], R=2, M=256, N=512, K=256, seed=126)
+    xs, w_s = configs.ag_inputs(c)
+    out = [_out(c.M, c.N // c.R, c.dtype) for _ in range(c.R)]
+    ws = _ws(fx.flux_workspace_size(fx.FLUX_OP_AG_GEMM, c.R, c.M, c.N, c.K))
+    with pytest.raises(fx.FluxError, match="WORKSPACE"):
+        fx.flux_ag_gemm(c.R, c.M, c.N, c.K, DT[c.dtype], [to_device(x, c.dtype) for x in xs],
+                        [to_device(w, c.dtype) for w in w_s], out, None, ws, opts={"ag_push": 1})
+
+
+def test_ag_gemm_push_withheld_flag_times_out_and_gpu_stays_usable():
+    # shard 1 never publishes: the push copy of its rows gives up after the
+    # timeout, and so do the tiles waiting for those rows' blocks
+    c = configs.small(configs.CONFIGS["ag_mlp0"], R=4, M=512, N=512, K=128, seed=127)
+    xs, w_s = configs.ag_inputs(c)
+    X = [to_device(x, c.dtype) for x in xs]
+    W = [to_device(w, c.dtype) for w in w_s]
+    out = [_out(c.M, c.N // c.R, c.dtype) for _ in range(c.R)]
+    ws = _ws(fx.flux_workspace_size(fx.FLUX_OP_AG_GEMM_PUSH, c.R, c.M, c.N, c.K))
+    flags = torch.tensor([1, 0, 1, 1], dtype=torch.int32, device="cuda")
+    fx.flux_ag_gemm(c.R, c.M, c.N, c.K, DT[c.dtype], X, W, out, flags, ws,
+                    opts={"ag_push": 1, "timeout_ns": 20_000_000})
+    st, rep = fx.flux_get_status(ws)
+    assert st == fx.FLUX_ERR_TIMEOUT
+    flags.fill_(1)
+    fx.flux_ag_gemm(c.R, c.M, c.N, c.K, DT[c.dtype], X, W, out, flags, ws, opts={"ag_push": 1})
+    _ok(ws)
+    ref = oracle.ag_gemm(xs, w_s, c.dtype)
+    for r in range(c.R):
+        check_close(oracle.widen(from_device(out[r]), c.dtype), ref[r], f"push after timeout rank {r}")
+
+
 # ---------------------------------------------------------------- GEMM + ReduceScatter
 def _rs_case(c, opts=None, ws=None, calls=1):
     As, Bs = configs.rs_inputs(c)
