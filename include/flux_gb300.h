@@ -119,7 +119,10 @@ typedef struct {
                                by multicast between the two pairs; 2 = regions of 8
                                CTAs, 256 x 256 pair tiles with two accumulators (the
                                fp32 adds of one tile overlap the next tile's MMAs), A
-                               and B shared by multicast between the four pairs */
+                               and B shared by multicast between the four pairs; 3 = as
+                               1, but a region claims one output tile and computes all
+                               R ranks' partials of it back to back (the tile's fp32
+                               rows stay in L2 between the partials) */
   int32_t moe_l1_ranks;     /* MoE layer1 with tp > 1 ranks per expert group (fewer than
                                48 k-slices per rank): how many ranks' partials of one
                                256 x 256 tile a CTA pair computes back to back and sums

@@ -531,6 +531,17 @@ flux_status_t gemm_rs_impl(int R, int M, int N, int K, flux_dtype_t dtype,
     // regions of 4 CTAs: two pairs of 256 x 512 tiles stacked along M, B
     // shared by multicast
     const int dgrid = setup_dyn<MODE_REDUCE, DENSE_CL>(p, dtype, dev, opts, ws + off, room);
+    if (dgrid > 0 && form == 3) {
+      // tile-major: one claim per output tile, whose R partials the region
+      // computes back to back (units u = tile * R + rank)
+      p.rs_tile_major = 1;
+      p.tiles_per_group = 1;
+      p.num_claims = tiles;
+      const int g = dgrid / DENSE_CL;
+      p.mbox_cap = 2 * ((tiles + g - 1) / g) + 2;
+      if (launch_dyn_dt<MODE_REDUCE, DENSE_CL>(dtype, p, dgrid, s) == FLUX_OK) return FLUX_OK;
+      p.rs_tile_major = 0;
+    }
     if (dgrid > 0) {
       p.tiles_per_group = tiles_per_group(dgrid, DENSE_CL, tiles);
       if (launch_dyn_dt<MODE_REDUCE, DENSE_CL>(dtype, p, dgrid, s) == FLUX_OK) return FLUX_OK;

@@ -300,6 +300,9 @@ struct KParams {
   // most this many claims are left, and at most as many full-cluster regions
   // have registered, so that the faster regions take the last units (0 = off)
   int claim_reserve;
+  // GEMM-RS, dynamic schedule: a claim is one output tile, and the region runs
+  // the R ranks' partials of it back to back (R items per claim)
+  int rs_tile_major;
 };
 
 constexpr uint32_t MBOX_DONE = 0xFFFFFFFFu;
@@ -577,6 +580,9 @@ __device__ __forceinline__ Work decode_store(const KParams& p, int u, int cta) {
   w.k0 = 0;
   w.k1 = p.KT;
   w.tile = 0;
+  w.rsub = 0;
+  w.rcnt = 1;
+  w.uid = u;
   return w;
 }
 
@@ -615,6 +621,9 @@ __device__ __forceinline__ Work decode_reduce(const KParams& p, int u, int cta) 
   w.e = 0;
   w.k0 = 0;
   w.k1 = p.KT;
+  w.rsub = 0;
+  w.rcnt = 1;
+  w.uid = u;
   return w;
 }
 
@@ -700,7 +709,8 @@ struct ItemIter {
   bool dyn, warp_uniform;
   uint32_t* box;     // dynamic: the region's mailbox
   int taken;         // dynamic: mailbox entries read so far
-  int sub;           // MOE_SCATTER_RED: next rank of the current tile's group
+  int sub;           // MOE_SCATTER_RED / tile-major GEMM-RS: next rank of the current tile
+  int cur_claim;     // tile-major GEMM-RS: the tile this region claimed last
 
   __device__ ItemIter(const KParams& p_, int total_mt_, int cta_, const Ctl* ctl_ = nullptr,
                       bool warp_uniform_ = false)
@@ -714,6 +724,7 @@ struct ItemIter {
       num_units = p.num_units;
     }
     sub = 0;
+    cur_claim = 0;
     u = blockIdx.x / CL;
     stride = gridDim.x / CL;
     dyn = DYN_OK && p.dyn != 0 && ctl != nullptr;
@@ -743,10 +754,21 @@ struct ItemIter {
       w.k0 = 0;
       w.k1 = p.KT;
       w.tile = 0;
+      w.rsub = 0;
+      w.rcnt = 1;
       w.uid = u * MAXR + r;
       return true;
     }
     if (DYN_OK && dyn) {
+      if (MODE == MODE_REDUCE && p.rs_tile_major && sub > 0) {
+        // the next rank of the tile this region claimed
+        w = decode_reduce<CL>(p, cur_claim * p.R + sub, cta);
+        w.rsub = sub;
+        w.rcnt = p.R;
+        w.uid = cur_claim;
+        if (++sub == p.R) sub = 0;
+        return true;
+      }
       uint32_t v = 0;
       if (!warp_uniform || (threadIdx.x & 31) == 0) {
         // bounded: a timeout is recorded, an abort ends the walk
@@ -766,6 +788,13 @@ struct ItemIter {
           w.n0 += half * BN;
           w.n_end = min(w.n_end, w.n0 + BN);
         }
+      } else if (p.rs_tile_major) {
+        // claim id = output tile; its rank 0 now, the other ranks next
+        cur_claim = id;
+        w = decode_reduce<CL>(p, id * p.R, cta);
+        w.rsub = 0;
+        w.rcnt = p.R;
+        sub = p.R > 1 ? 1 : 0;
       } else {
         w = decode_reduce<CL>(p, id, cta);
       }
@@ -818,6 +847,7 @@ struct ItemIter {
 // last units; a half without columns is skipped here.
 template <int MODE, int CL>
 __device__ __forceinline__ void claim_unit(const KParams& p, uint32_t* box, int j, bool slow) {
+  if (j >= p.mbox_cap) return;  // past the region's DONE entry: never read, never written
   uint32_t v = MBOX_DONE;
   bool stop = false;
   if (slow && p.claim_reserve > 0) {
@@ -1040,10 +1070,13 @@ __device__ void producer_tma(const KParams& p, const Smem& s, const Ctl& c, int 
     trace_now(p, item, TR_PROD_START);
     // k-slices up to the claim point, the leader's claim of the region's
     // next unit, then the rest (no per-slice branch on either)
-    const int claim_k = leader ? max(w.k0, w.k1 - CLAIM_AHEAD) : w.k1;
+    // (one claim per item the mailbox hands out: under the tile-major GEMM-RS
+    // schedule the next tile is claimed during the last rank's item)
+    const bool claims_here = leader && w.rsub + 1 >= w.rcnt;
+    const int claim_k = claims_here ? max(w.k0, w.k1 - CLAIM_AHEAD) : w.k1;
     for (int seg = 0; seg < 2 && ok; ++seg) {
       const int kb = seg == 0 ? w.k0 : claim_k, ke = seg == 0 ? claim_k : w.k1;
-      if (seg == 1 && leader) claim_unit<MODE, CL>(p, iter.box, claimed++, slow_region);
+      if (seg == 1 && claims_here) claim_unit<MODE, CL>(p, iter.box, claimed++, slow_region);
       if (kb >= ke) continue;
       if constexpr (MC == 2) {
         ok = mc2 ? produce_ksteps<MODE, CL, true>(p, s, c, w, kb, ke, nbox_a, bmask, bytes, n0, cta, half,

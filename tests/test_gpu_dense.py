@@ -389,11 +389,12 @@ def test_ag_gemm_dynamic_schedule_matches_static_bit_for_bit(num_ctas, N):
         check_close(oracle.widen(from_device(outs["dynamic"][r]), c.dtype), ref[r], f"ag dyn rank {r}")
 
 
-@pytest.mark.parametrize("rs_tile", [1, 2])
+@pytest.mark.parametrize("rs_tile", [1, 2, 3])
 @pytest.mark.parametrize("num_ctas", [0, 12])
 def test_gemm_rs_dynamic_schedule_integer_inputs_bit_exact(num_ctas, rs_tile):
     # integer inputs: every fp32 partial and sum is exact, whatever the order of the adds
-    # (rs_tile 1: regions of 4 with 256 x 512 pair tiles; 2: regions of 8, 256 x 256)
+    # (rs_tile 1: regions of 4 with 256 x 512 pair tiles; 2: regions of 8, 256 x 256;
+    # 3: regions of 4, each claiming a tile and computing all its ranks' partials)
     c = configs.small(configs.CONFIGS["rs_mlp1"], R=8, M=1024, N=4096, K=512, dist="int", seed=72)
     As, Bs = configs.rs_inputs(c)
     A = [to_device(a, c.dtype) for a in As]
@@ -413,19 +414,21 @@ def test_gemm_rs_dynamic_schedule_integer_inputs_bit_exact(num_ctas, rs_tile):
 
 
 @pytest.mark.parametrize("R,M,N,K,dtype,num_ctas", [
-    (8, 1000, 2056, 1024, "f16", 16),   # ragged M and N tails, 125-row owner chunks, two regions
+    (8, 1000, 2056, 1024, "f16", 16),   # ragged M and N tails, 125-row owner chunks
     (4, 512, 1032, 2048, "bf16", 16),   # ragged last n-unit (8 columns past 1024)
     (8, 2048, 4096, 4096, "bf16", 0),   # every SM: 8-CTA clusters where they fit, pairs elsewhere
     (16, 1024, 2048, 2048, "f16", 0),   # the most ranks a call takes
 ])
-def test_gemm_rs_regions_of_8_match_oracle(R, M, N, K, dtype, num_ctas):
+@pytest.mark.parametrize("rs_tile", [2, 3])
+def test_gemm_rs_alternative_forms_match_oracle(R, M, N, K, dtype, num_ctas, rs_tile):
+    # rs_tile 2: regions of 8 with 256 x 256 tiles; 3: tile-major regions of 4
     c = configs.small(configs.CONFIGS["rs_mlp1"], R=R, M=M, N=N, K=K, dtype=dtype, seed=80 + R)
-    opts = {"rs_tile": 2, "num_ctas": num_ctas}
+    opts = {"rs_tile": rs_tile, "num_ctas": num_ctas}
     As, Bs, out, ws = _rs_case(c, opts=opts, calls=2)
     _ok(ws)
     ref = oracle.gemm_rs(As, Bs, dtype)
     for o in range(R):
-        check_close(oracle.widen(from_device(out[o]), dtype), ref[o], f"rs regions of 8, owner {o}")
+        check_close(oracle.widen(from_device(out[o]), dtype), ref[o], f"rs form {rs_tile}, owner {o}")
     assert torch.count_nonzero(ws).item() == 0
 
 

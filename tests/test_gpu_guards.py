@@ -105,6 +105,7 @@ def test_ag_gemm_writes_stay_inside(R, M, N, K, dtype):
     (2, 64, 1000, 4096, "bf16", 0),  # few tiles: stream-K, 32-row owners, ragged last n-tile
     (8, 1088, 2056, 256, "f16", 1),  # 648 rank tiles: whole units, regions of 4, 136-row owners
     (8, 1088, 2056, 256, "f16", 2),  # the same on regions of 8 (256 x 256 pair tiles)
+    (8, 1088, 2056, 256, "f16", 3),  # regions of 4, tile-major (a tile's ranks back to back)
 ])
 def test_gemm_rs_writes_stay_inside(R, M, N, K, dtype, rs_tile):
     c = configs.small(configs.CONFIGS["rs_mlp1"], R=R, M=M, N=N, K=K, dtype=dtype, seed=303)
