@@ -155,7 +155,11 @@ typedef struct {
                                its A rows from the owning shard after the shard's flag.
                                Needs flux_workspace_size(FLUX_OP_AG_GEMM_PUSH, ...) and the
                                dynamic schedule; moe_stage_ctas sets the copy CTAs. */
-  int32_t reserved1;
+  int32_t debug_probe;      /* checked build only (libflux_gb300_checked.so, see
+                               flux_checks_enabled): nonzero makes the kernel fail one
+                               check on purpose (report: FLUX_ERR_INVALID_ARG, wait site
+                               13, arg0 = 15, arg1 = this value), to show that checks
+                               report; ignored by the regular build */
 } flux_opts_t;
 
 /* What flux_get_status found in a workspace header. */
@@ -168,7 +172,7 @@ typedef struct {
                       of an unexpected shape under the dynamic schedule, 11 MoE
                       layer1's grid barrier before the token rows are converted,
                       12 the exchange of a cluster ReduceScatter (GEMM-RS of few
-                      rows) */
+                      rows), 13 a failed check of the checked build */
   uint32_t arg0;   /* flag wait: shard index; pipeline waits: CTA index */
   uint32_t arg1;   /* flag wait: last flag value seen; pipeline waits: stage / buffer */
 } flux_device_report_t;
@@ -177,6 +181,17 @@ typedef struct {
 
 /* Version of this ABI (major * 10000 + minor * 100 + patch). */
 int flux_version(void);
+
+/* 1 in the checked build of the library (libflux_gb300_checked.so, compiled
+ * with -DFLUX_CHECKS=1), 0 in the regular one.  In the checked build every
+ * TMA coordinate and every global store or add of the kernels is checked
+ * against the tensor it addresses; a failed check ends the call with
+ * FLUX_ERR_INVALID_ARG (reported by flux_get_status: wait site 13, arg0 the
+ * check -- 1 A row, 2 A k, 3 B column, 4 B k, 5 output row, 6 output
+ * column, 7 fp32 row or token, 8 fp32 column, 9 owner rank, 15 the
+ * requested probe -- and arg1 the offending value) and the access is
+ * skipped, or, for a load, moved to the tensor's origin.  No check traps. */
+int flux_checks_enabled(void);
 
 /* Human-readable name of a status code (static string, never NULL). */
 const char* flux_status_string(flux_status_t s);

@@ -14,7 +14,10 @@ import ctypes
 import os
 
 HERE = os.path.dirname(os.path.abspath(__file__))
-LIB_PATH = os.path.join(HERE, "libflux_gb300.so")
+# FLUX_CHECKED=1 in the environment loads the checked build (bounds checks in
+# every kernel, see flux_checks_enabled in the header) instead of the regular one
+CHECKED = os.environ.get("FLUX_CHECKED", "") not in ("", "0")
+LIB_PATH = os.path.join(HERE, "libflux_gb300_checked.so" if CHECKED else "libflux_gb300.so")
 
 if not os.path.exists(LIB_PATH):
     raise ImportError(
@@ -53,7 +56,7 @@ FLUX_NOALLOC_SCRATCH_BYTES = 16 * 1024 * 1024
 WAIT_SITES = {1: "ready flag", 2: "smem slot free", 3: "smem slot full",
               4: "accumulator free", 5: "accumulator full", 6: "drain",
               7: "deterministic turn", 8: "staged rows", 9: "unit schedule",
-              10: "cluster shape", 11: "grid barrier", 12: "cluster exchange"}
+              10: "cluster shape", 11: "grid barrier", 12: "cluster exchange", 13: "check"}
 
 
 class flux_opts_t(ctypes.Structure):
@@ -64,7 +67,7 @@ class flux_opts_t(ctypes.Structure):
                 ("moe_stage_ctas", ctypes.c_int32), ("rs_tile", ctypes.c_int32),
                 ("moe_l1_ranks", ctypes.c_int32), ("trace", ctypes.c_void_p),
                 ("trace_words", ctypes.c_uint64), ("ag_push", ctypes.c_int32),
-                ("reserved1", ctypes.c_int32)]
+                ("debug_probe", ctypes.c_int32)]
 
 
 class flux_device_report_t(ctypes.Structure):
@@ -90,6 +93,7 @@ _opt = ctypes.POINTER(flux_opts_t)
 
 _SIGS = {
     "flux_version": ([], ctypes.c_int),
+    "flux_checks_enabled": ([], ctypes.c_int),
     "flux_status_string": ([_i], ctypes.c_char_p),
     "flux_last_cuda_error": ([], ctypes.c_int),
     "flux_workspace_size": ([_i, _i, _i, _i, _i], _sz),
@@ -195,6 +199,10 @@ def dtype_code(t) -> int:
 # ---------------------------------------------------------------- API (same names as the C ABI)
 def flux_version() -> int:
     return _lib.flux_version()
+
+
+def flux_checks_enabled() -> bool:
+    return bool(_lib.flux_checks_enabled())
 
 
 def flux_status_string(status: int) -> str:

@@ -20,6 +20,9 @@ CSRC = os.path.join(HERE, "csrc")
 BUILD = os.path.join(HERE, "_build")
 LIB_NAME = "libflux_gb300.so"
 LIB_PATH = os.path.join(HERE, LIB_NAME)
+# the checked build: the same sources with every kernel access checked
+# (-DFLUX_CHECKS=1; loaded by the binding when FLUX_CHECKED=1)
+CHECKED_LIB_PATH = os.path.join(HERE, "libflux_gb300_checked.so")
 
 SOURCES = ["flux_core.cu", "flux_dense.cu", "flux_moe.cu", "flux_noalloc.cu", "flux_tune.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
@@ -57,8 +60,9 @@ def _up_to_date() -> bool:
     deps = [os.path.join(CSRC, f) for f in os.listdir(CSRC)]
     deps.append(os.path.join(os.path.dirname(HERE), "include", "flux_gb300.h"))
     deps.append(__file__)
-    return os.path.exists(LIB_PATH) and os.path.getmtime(LIB_PATH) >= max(
-        os.path.getmtime(d) for d in deps)
+    newest = max(os.path.getmtime(d) for d in deps)
+    return all(os.path.exists(lib) and os.path.getmtime(lib) >= newest
+               for lib in (LIB_PATH, CHECKED_LIB_PATH))
 
 
 def build(verbose: bool = False, force: bool = False) -> str:
@@ -79,18 +83,28 @@ def build(verbose: bool = False, force: bool = False) -> str:
 
 
 def _build_locked(nvcc: str, verbose: bool) -> str:
-    def compile_one(src):
-        obj = os.path.join(BUILD, src.replace(".cu", ".o"))
-        _run([nvcc, *ARCH, *CFLAGS, "-c", os.path.join(CSRC, src), "-o", obj], verbose)
+    # both libraries' translation units compile in parallel
+    variants = ((LIB_PATH, BUILD, []), (CHECKED_LIB_PATH, os.path.join(BUILD, "checked"), ["-DFLUX_CHECKS=1"]))
+    jobs = []
+    for lib, bdir, defs in variants:
+        os.makedirs(bdir, exist_ok=True)
+        for src in SOURCES:
+            jobs.append((src, os.path.join(bdir, src.replace(".cu", ".o")), defs))
+
+    def compile_one(job):
+        src, obj, defs = job
+        _run([nvcc, *ARCH, *CFLAGS, *defs, "-c", os.path.join(CSRC, src), "-o", obj], verbose)
         return obj
 
-    with ThreadPoolExecutor(len(SOURCES)) as ex:
-        objs = list(ex.map(compile_one, SOURCES))
+    with ThreadPoolExecutor(len(jobs)) as ex:
+        objs = list(ex.map(compile_one, jobs))
     libdir = _cuda_lib_dir(nvcc)
-    tmp = f"{LIB_PATH}.tmp{os.getpid()}"
-    _run([nvcc, *ARCH, "-shared", "-cudart", "shared", "-o", tmp, *objs,
-          f"-L{libdir}", "-Xlinker", f"-rpath={libdir}"], verbose)
-    os.replace(tmp, LIB_PATH)
+    for i, (lib, _, _) in enumerate(variants):
+        tmp = f"{lib}.tmp{os.getpid()}"
+        _run([nvcc, *ARCH, "-shared", "-cudart", "shared", "-o", tmp,
+              *objs[i * len(SOURCES):(i + 1) * len(SOURCES)],
+              f"-L{libdir}", "-Xlinker", f"-rpath={libdir}"], verbose)
+        os.replace(tmp, lib)
     return LIB_PATH
 
 

@@ -6,6 +6,10 @@
 
 #include "flux_host.h"
 
+#ifndef FLUX_CHECKS
+#define FLUX_CHECKS 0
+#endif
+
 namespace flux {
 
 namespace {
@@ -137,6 +141,8 @@ flux_status_t check_workspace(const void* ws, size_t have, size_t need) {
 using namespace flux;
 
 extern "C" int flux_version(void) { return 200; }
+
+extern "C" int flux_checks_enabled(void) { return FLUX_CHECKS ? 1 : 0; }
 
 extern "C" const char* flux_status_string(flux_status_t s) {
   switch (s) {

@@ -99,6 +99,15 @@
 #ifndef FLUX_TRACE
 #define FLUX_TRACE 1
 #endif
+// Checked build (-DFLUX_CHECKS=1, libflux_gb300_checked.so): every TMA
+// coordinate and every global store or add of the kernels is checked against
+// the tensor it addresses; a failed check records FLUX_ERR_INVALID_ARG with
+// the check's code and the offending value (wait site W_CHECK) and the access
+// is skipped (stores, adds) or moved to a safe coordinate (loads, whose bytes
+// the stage barrier expects).  The regular build compiles the checks out.
+#ifndef FLUX_CHECKS
+#define FLUX_CHECKS 0
+#endif
 
 namespace flux {
 
@@ -234,7 +243,21 @@ enum WaitSite {
   W_SCHED = 9,  // dynamic schedule: the region's next unit
   W_SHAPE = 10, // dynamic schedule: a cluster of an unexpected size or CTA order
   W_GRID = 11,  // MoE layer1: every CTA's adds in before the rows are converted
-  W_XCHG = 12   // cluster ReduceScatter: peers' rings free / partial rows received
+  W_XCHG = 12,  // cluster ReduceScatter: peers' rings free / partial rows received
+  W_CHECK = 13  // checked build: a coordinate or address check failed (arg0 = CheckCode)
+};
+// What a failed check of the checked build was about (report arg0).
+enum CheckCode {
+  CK_A_ROW = 1,     // A box start row outside its tensor (or the shard index outside [0, R))
+  CK_A_K = 2,       // A box k coordinate outside [0, K) or not 16-byte aligned
+  CK_B_COL = 3,     // B box column outside [0, N) or not 16-byte aligned
+  CK_B_K = 4,       // B box k coordinate outside [0, K)
+  CK_OUT_ROW = 5,   // output row outside its buffer
+  CK_OUT_COL = 6,   // output column outside its row (or not 16-byte aligned)
+  CK_ACC_ROW = 7,   // fp32 accumulation row outside [0, M) (GEMM-RS) or token outside [0, T)
+  CK_ACC_COL = 8,   // fp32 accumulation column outside [0, N)
+  CK_OWNER = 9,     // owner rank outside [0, R)
+  CK_PROBE = 15     // the deliberate failure requested by flux_opts_t.debug_probe
 };
 constexpr uint32_t ST_TIMEOUT = 5;
 constexpr uint32_t ST_INVALID = 1;
@@ -303,6 +326,7 @@ struct KParams {
   // GEMM-RS, dynamic schedule: a claim is one output tile, and the region runs
   // the R ranks' partials of it back to back (R items per claim)
   int rs_tile_major;
+  int debug_probe;  // checked build: nonzero makes CTA 0 fail one check (CK_PROBE) on purpose
 };
 
 constexpr uint32_t MBOX_DONE = 0xFFFFFFFFu;
@@ -330,6 +354,19 @@ static __device__ __noinline__ void raise_error(const Ctl& c, uint32_t code, uin
   }
   __threadfence();
   atomicExch(c.hdr + H_ABORT, c.seq);
+}
+
+// Checked build: true when `cond` holds; otherwise records the failure (first
+// error wins, the call is aborted so that the other roles leave) and returns
+// false.  Always true in the regular build.
+__device__ __forceinline__ bool check_ok(const Ctl& c, bool cond, uint32_t code, uint32_t value) {
+#if FLUX_CHECKS
+  if (!cond) raise_error(c, ST_INVALID, W_CHECK, code, value);
+  return cond;
+#else
+  (void)c; (void)code; (void)value;
+  return true;
+#endif
 }
 
 // Waits that have not finished within this many SM cycles start the (slow)
@@ -946,30 +983,38 @@ __device__ __forceinline__ bool produce_ksteps(const KParams& p, const Smem& s, 
       for (int bx = 0; bx < nbox_a; ++bx) {
         if (MCA && MC2 && bx != a_half) continue;  // the N neighbour multicasts this box
         const int row = w.m0 + bx * p.a_box_m;
-        const int sh = row / p.rows_per_rank;
+        int sh = row / p.rows_per_rank;
+        int lrow = row - sh * p.rows_per_rank;
+        int kx = kc;
+        if (!check_ok(c, row >= 0 && sh < p.R, CK_A_ROW, static_cast<uint32_t>(row))) sh = lrow = 0;
+        if (!check_ok(c, kc >= 0 && kc < p.K && (kc & 7) == 0, CK_A_K, static_cast<uint32_t>(kc))) kx = 0;
         if (MCA && MC2)
-          tma_load_2d_pair_mc(sa + bx * p.a_box_m * BK * 2, &p.tmA[sh], fbc, kc, row - sh * p.rows_per_rank,
-                              mask_a);
+          tma_load_2d_pair_mc(sa + bx * p.a_box_m * BK * 2, &p.tmA[sh], fbc, kx, lrow, mask_a);
         else if (PAIR == 2)
-          tma_load_2d_pair(sa + bx * p.a_box_m * BK * 2, &p.tmA[sh], fbc, kc, row - sh * p.rows_per_rank);
+          tma_load_2d_pair(sa + bx * p.a_box_m * BK * 2, &p.tmA[sh], fbc, kx, lrow);
         else
-          tma_load_2d(sa + bx * p.a_box_m * BK * 2, &p.tmA[sh], fb, kc, row - sh * p.rows_per_rank);
+          tma_load_2d(sa + bx * p.a_box_m * BK * 2, &p.tmA[sh], fb, kx, lrow);
       }
     } else if (nbox_a) {
+      // (checked build: a box outside the tensor is recorded and moved to its origin)
+      int ar = w.r, am0 = w.m0, ak = kc;
+      if (!check_ok(c, ar >= 0 && ar < p.R && am0 >= 0 && am0 < p.M, CK_A_ROW, static_cast<uint32_t>(am0)))
+        ar = am0 = 0;
+      if (!check_ok(c, ak >= 0 && ak < p.K && (ak & 7) == 0, CK_A_K, static_cast<uint32_t>(ak))) ak = 0;
       if (MCA) {
         // two 64-row boxes (the map's box is 64 rows); with a 8-CTA cluster
         // each of the two N neighbours issues one of them to both
         for (int bx = 0; bx < 2; ++bx) {
           if (MC2 && bx != a_half) continue;
           if (MC2)
-            tma_load_2d_pair_mc(sa + bx * 64 * BK * 2, &p.tmA[w.r], fbc, kc, w.m0 + bx * 64, mask_a);
+            tma_load_2d_pair_mc(sa + bx * 64 * BK * 2, &p.tmA[ar], fbc, ak, am0 + bx * 64, mask_a);
           else
-            tma_load_2d_pair(sa + bx * 64 * BK * 2, &p.tmA[w.r], fbc, kc, w.m0 + bx * 64);
+            tma_load_2d_pair(sa + bx * 64 * BK * 2, &p.tmA[ar], fbc, ak, am0 + bx * 64);
         }
       } else if (PAIR == 2) {
-        tma_load_2d_pair(sa, &p.tmA[w.r], fbc, kc, w.m0);
+        tma_load_2d_pair(sa, &p.tmA[ar], fbc, ak, am0);
       } else {
-        tma_load_2d(sa, &p.tmA[w.r], fb, kc, w.m0);
+        tma_load_2d(sa, &p.tmA[ar], fb, ak, am0);
       }
     }
     for (int j = 0; j < G::B_BOXES; ++j) {
@@ -977,7 +1022,12 @@ __device__ __forceinline__ bool produce_ksteps(const KParams& p, const Smem& s, 
       // the pair stacked with this one multicasts the other half of the boxes
       if (MC2 && (j * 2) / G::B_BOXES != half) continue;
       const int nc = b_box_col<PAIR>(n0, cta, j);
-      const int n = nc < w.n_end ? nc : n0;  // the padding box of a CTA without columns
+      int n = nc < w.n_end ? nc : n0;  // the padding box of a CTA without columns
+      // (a padding box may start up to a tile past N: the load reads fill values)
+      if (!check_ok(c, n >= 0 && n < p.N + Unit<MODE, CL>::G::TILE_N && (n & 7) == 0 && w.r >= 0 && w.r < p.R,
+                    CK_B_COL, static_cast<uint32_t>(n)))
+        n = 0;
+      check_ok(c, kc >= 0 && kc < p.K, CK_B_K, static_cast<uint32_t>(kc));
       const uint32_t dst = sb + j * B_BOX_N * BK * 2;
       if (is_scatter(MODE) || MODE == MODE_MOE_STAGED) {
         if (PAIR == 2) tma_load_3d_pair(dst, &p.tmB[w.r], fbc, n, kc, w.e);
@@ -1424,6 +1474,12 @@ __device__ void epilogue(const KParams& p, const Smem& s, const Ctl& c, uint32_t
         uint32_t v[32], u[32];
         tmem_ld_32x32b_x32(taddr + ch * 64, v);
         tmem_ld_32x32b_x32(taddr + ch * 64 + 32, u);
+        // (checked build: a box outside the rank's output is recorded and not written)
+        if (!check_ok(c, w.r >= 0 && w.r < p.R && row0 >= 0 && row0 < p.M, CK_OUT_ROW,
+                      static_cast<uint32_t>(row0)) ||
+            !check_ok(c, n0 + ch * 64 >= 0 && n0 + ch * 64 < p.ldo && ((n0 + ch * 64) & 7) == 0, CK_OUT_COL,
+                      static_cast<uint32_t>(n0 + ch * 64)))
+          continue;
         if (row0 + 32 <= w.row_end || w.row_end == p.M) {
           // the warp's 32 x 64 box, staged in the 128-byte swizzled layout of
           // the output map, goes out as one tensor bulk store (rows past the
@@ -1489,6 +1545,11 @@ __device__ void epilogue(const KParams& p, const Smem& s, const Ctl& c, uint32_t
             if (ch * 32 >= ncols) break;  // warp-uniform
             uint32_t v[32];
             tmem_ld_32x32b_x32(taddr + ch * 32, v);
+            // (checked build: a box outside the fp32 rows is recorded and not added)
+            if (!check_ok(c, row0 >= 0 && row0 < p.M, CK_ACC_ROW, static_cast<uint32_t>(row0)) ||
+                !check_ok(c, n0 + ch * 32 >= 0 && n0 + ch * 32 < p.N && ((n0 + ch * 32) & 3) == 0, CK_ACC_COL,
+                          static_cast<uint32_t>(n0 + ch * 32)))
+              continue;
             const uint32_t buf = sstg + (ch & 1) * STG_BOX;
             if (ch >= 2) {
               if (lane == 0) bulk_wait_read<1>();
@@ -1508,11 +1569,15 @@ __device__ void epilogue(const KParams& p, const Smem& s, const Ctl& c, uint32_t
           }
         }
       } else {
+        // (checked build: a token outside [0, T) or a tile outside the row is
+        // recorded and not added)
+        const bool tok_ok = check_ok(c, !row_ok || (key >= 0 && key < p.T), CK_ACC_ROW, static_cast<uint32_t>(key));
+        const bool col_ok = check_ok(c, n0 >= 0 && n0 < p.N, CK_ACC_COL, static_cast<uint32_t>(n0));
         for (int ch = 0; ch < G::TILE_N / 32; ++ch) {
-          if (ch * 32 >= ncols) break;  // warp-uniform
+          if (ch * 32 >= ncols || !col_ok) break;  // warp-uniform
           uint32_t v[32];
           tmem_ld_32x32b_x32(taddr + ch * 32, v);
-          scatter_add_chunk(p.acc, p.N, n0 + ch * 32, ncols - ch * 32, sstg, lane, key, row_ok, gate, v);
+          scatter_add_chunk(p.acc, p.N, n0 + ch * 32, ncols - ch * 32, sstg, lane, key, row_ok && tok_ok, gate, v);
         }
       }
     }
@@ -1552,10 +1617,11 @@ __device__ void epilogue(const KParams& p, const Smem& s, const Ctl& c, uint32_t
           if (grow >= w.row_end) break;
           const int o = grow / p.rows_per_rank;
           const int lr = grow - o * p.rows_per_rank;
+          if (!check_ok(c, o >= 0 && o < p.R, CK_OWNER, static_cast<uint32_t>(o))) break;
 #pragma unroll
           for (int c0 = 0; c0 < G::TILE_N; c0 += 256) {
             const int col = n0 + c0 + lane * 8;
-            if (col < p.N)
+            if (col < p.N && check_ok(c, col >= 0 && (col & 7) == 0, CK_OUT_COL, static_cast<uint32_t>(col)))
               convert8<DT>(p.acc + static_cast<long long>(grow) * p.N + col,
                            static_cast<uint16_t*>(p.out[o]) + static_cast<long long>(lr) * p.ldo + col);
           }
@@ -1653,12 +1719,14 @@ __device__ void epilogue_scatter_red(const KParams& p, const Smem& s, const Ctl&
       tok = slot / p.topk;
       gate = __ldg(p.topk_w + slot);
     }
+    const bool tok_ok = check_ok(c, !row_ok || (tok >= 0 && tok < p.T), CK_ACC_ROW, static_cast<uint32_t>(tok));
     const int c0 = w.n0 + hh * HALF;
     const int ncols = w.n_end - c0;
 #pragma unroll
     for (int ch = 0; ch < CH; ++ch)
       if (ch * 32 < ncols)  // warp-uniform
-        scatter_add_chunk(p.acc, p.N, c0 + ch * 32, ncols - ch * 32, sstg, lane, tok, row_ok, gate, acc[ch]);
+        scatter_add_chunk(p.acc, p.N, c0 + ch * 32, ncols - ch * 32, sstg, lane, tok, row_ok && tok_ok, gate,
+                          acc[ch]);
     if (ew == 0 && lane == 0) trace_now(p, it - 1, TR_EPI_END);
   }
 }
@@ -1759,9 +1827,9 @@ __device__ void epilogue_rs_cluster(const KParams& p, const Smem& s, const Ctl& 
 #pragma unroll
       for (int i = 0; i < 8; ++i) acc[i] += x[i];
     }
-    if (col < p.N) {
-      const int o = cta + (lr / rows_o) * CL;
-      const int orow = lr - (lr / rows_o) * rows_o;
+    const int o = cta + (lr / rows_o) * CL;
+    const int orow = lr - (lr / rows_o) * rows_o;
+    if (col < p.N && check_ok(c, o >= 0 && o < p.R && orow < rows_o, CK_OWNER, static_cast<uint32_t>(o))) {
       uint4 qv;
       qv.x = pack2<DT>(acc[0], acc[1]);
       qv.y = pack2<DT>(acc[2], acc[3]);
@@ -1817,6 +1885,7 @@ __device__ void finish_token_rows(const KParams& p, const Ctl& c, uint32_t* flag
           const int col = static_cast<int>(i - static_cast<long long>(t) * chunks) * 8;
           const int o = t / p.rows_per_rank;
           const int lt = t - o * p.rows_per_rank;
+          if (!check_ok(c, o >= 0 && o < p.R, CK_OWNER, static_cast<uint32_t>(o))) continue;
           uint4 q;
           q.x = pack2<DT>(a[j].x, a[j].y);
           q.y = pack2<DT>(a[j].z, a[j].w);
@@ -2057,6 +2126,8 @@ fused_gemm_kernel(const __grid_constant__ KParams p) {
       raise_error(c, ST_INVALID, W_SHAPE, blockIdx.x, static_cast<uint32_t>(ps.hw_cl));
   }
 
+  if (p.debug_probe != 0 && blockIdx.x == 0 && threadIdx.x == 0)
+    check_ok(c, false, CK_PROBE, static_cast<uint32_t>(p.debug_probe));  // checked build only
 #if FLUX_TRACE
   if (p.trace != nullptr && blockIdx.x == 0 && threadIdx.x == 0 && p.trace_words >= TR_FIELDS) {
     p.trace[0] = gridDim.x;

@@ -167,3 +167,17 @@ def _ws256():
         def element_size(self):
             return 1
     return W()
+
+
+def test_checked_build_exports_the_same_symbols_and_says_so(fx):
+    # the checked build (-DFLUX_CHECKS=1) is a drop-in copy of the library
+    path = os.path.join(os.path.dirname(fx.LIB_PATH), "libflux_gb300_checked.so")
+    assert os.path.exists(path), "build() makes the checked library too"
+    lib = ctypes.CDLL(path)
+    for name in declared_functions():
+        assert hasattr(lib, name), f"{name} missing from the checked build"
+    lib.flux_checks_enabled.restype = ctypes.c_int
+    assert lib.flux_checks_enabled() == 1
+    regular = ctypes.CDLL(os.path.join(os.path.dirname(fx.LIB_PATH), "libflux_gb300.so"))
+    regular.flux_checks_enabled.restype = ctypes.c_int
+    assert regular.flux_checks_enabled() == 0
