@@ -1474,6 +1474,7 @@ __device__ void epilogue(const KParams& p, const Smem& s, const Ctl& c, uint32_t
         uint32_t v[32], u[32];
         tmem_ld_32x32b_x32(taddr + ch * 64, v);
         tmem_ld_32x32b_x32(taddr + ch * 64 + 32, u);
+        if (row0 >= w.row_end) continue;  // none of this warp's rows is in the tile
         // (checked build: a box outside the rank's output is recorded and not written)
         if (!check_ok(c, w.r >= 0 && w.r < p.R && row0 >= 0 && row0 < p.M, CK_OUT_ROW,
                       static_cast<uint32_t>(row0)) ||

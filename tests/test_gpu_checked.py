@@ -140,7 +140,7 @@ def test_checked_build_runs_every_op_clean_and_reports_the_probe():
     assert r.returncode == 0, r.stdout[-3000:] + r.stderr[-3000:]
     line = [ln for ln in r.stdout.splitlines() if ln.startswith("RESULT ")][-1]
     res = json.loads(line[len("RESULT "):])
-    assert len(res["done"]) == 13, res["done"]
+    assert len(res["done"]) == 14, res["done"]  # 2 AG, 6 GEMM-RS, 1 plain GEMM, 4 MoE, 1 after the probe
     assert res["probe"]["status"] == fx.FLUX_ERR_INVALID_ARG
     rep = res["probe"]["report"]
     assert rep["where"] == "check" and rep["arg0"] == 15 and rep["arg1"] == 1234, rep
