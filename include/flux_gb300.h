@@ -160,6 +160,13 @@ typedef struct {
                                check on purpose (report: FLUX_ERR_INVALID_ARG, wait site
                                13, arg0 = 15, arg1 = this value), to show that checks
                                report; ignored by the regular build */
+  int32_t moe_static_schedule; /* MoE layer0 (staged form): nonzero = the static unit
+                               schedule (CTA pair i takes units i, i + pairs, ...);
+                               0 (default) = the dynamic one: each pair claims its next
+                               unit from a counter in the workspace while it computes
+                               the current one, so pairs that drew cheaper units (the
+                               half-wide last column tile, an expert's partial last
+                               rows) take more of them */
 } flux_opts_t;
 
 /* What flux_get_status found in a workspace header. */
@@ -168,7 +175,7 @@ typedef struct {
   uint32_t where;  /* which wait gave up: 1 ready flag, 2 smem slot free, 3 smem slot full,
                       4 accumulator free, 5 accumulator full, 6 drain,
                       7 deterministic GEMM-RS turn, 8 staged MoE rows of an m-tile,
-                      9 next unit of the dynamic schedule (dense ops), 10 a cluster
+                      9 next unit of the dynamic schedule (dense ops, MoE layer0), 10 a cluster
                       of an unexpected shape under the dynamic schedule, 11 MoE
                       layer1's grid barrier before the token rows are converted,
                       12 the exchange of a cluster ReduceScatter (GEMM-RS of few

@@ -736,7 +736,10 @@ __device__ __forceinline__ Work decode_moe(const KParams& p, int u, int total_mt
 // (a whole warp calls next) makes lane 0 read the mailbox for the warp.
 template <int MODE, int CL>
 struct ItemIter {
-  static constexpr bool DYN_OK = Unit<MODE, CL>::DENSE && (CL == 4 || CL == 8);
+  // dense tiles in regions of two or four pairs; the staged MoE layer0 in
+  // regions of one pair (its unit count comes from the device tile table)
+  static constexpr bool DYN_OK =
+      (Unit<MODE, CL>::DENSE && (CL == 4 || CL == 8)) || (MODE == MODE_MOE_STAGED && CL == 2);
   const KParams& p;
   const Ctl* ctl;
   int total_mt;      // MoE: device-computed number of m-tiles
@@ -773,6 +776,9 @@ struct ItemIter {
       end = L * (u + 1) / stride;
     }
   }
+
+  // dynamic schedule: how many claim ids the counter hands out
+  __device__ int claims() const { return is_moe(MODE) ? num_units : p.num_claims; }
 
   __device__ bool next(Work& w) {
     if (MODE == MODE_RS_CLUSTER) {
@@ -825,6 +831,8 @@ struct ItemIter {
           w.n0 += half * BN;
           w.n_end = min(w.n_end, w.n0 + BN);
         }
+      } else if (is_moe(MODE)) {
+        w = decode_moe<CL>(p, id, total_mt, cta, Unit<MODE, CL>::G::TILE_N);
       } else if (p.rs_tile_major) {
         // claim id = output tile; its rank 0 now, the other ranks next
         cur_claim = id;
@@ -880,10 +888,13 @@ struct ItemIter {
 // into entry j of the region's mailbox, or MBOX_DONE once the counter has run
 // out or the mailbox is full (then the other regions take the remaining
 // claims: the mailboxes together hold more entries than there are claims).
-// Store mode: ids from split_from on are the two 256-column halves of the
-// last units; a half without columns is skipped here.
+// The counter hands out ids below num_claims: the host's count for the dense
+// ops, the device-computed unit count for MoE layer0.  Store mode: ids from
+// split_from on are the two 256-column halves of the last units; a half
+// without columns is skipped here.
 template <int MODE, int CL>
-__device__ __forceinline__ void claim_unit(const KParams& p, uint32_t* box, int j, bool slow) {
+__device__ __forceinline__ void claim_unit(const KParams& p, uint32_t* box, int j, bool slow,
+                                           int num_claims) {
   if (j >= p.mbox_cap) return;  // past the region's DONE entry: never read, never written
   uint32_t v = MBOX_DONE;
   bool stop = false;
@@ -893,12 +904,12 @@ __device__ __forceinline__ void claim_unit(const KParams& p, uint32_t* box, int 
     // runs out, so no unit is left behind
     const uint32_t fast = min(ld_volatile_u32(p.hdr + H_FAST), static_cast<uint32_t>(p.claim_reserve));
     const uint32_t seen = ld_volatile_u32(p.hdr + H_CLAIM);
-    stop = fast > 0 && seen + fast >= static_cast<uint32_t>(p.num_claims);
+    stop = fast > 0 && seen + fast >= static_cast<uint32_t>(num_claims);
   }
   if (j < p.mbox_cap - 1 && !stop) {
     for (;;) {
       const uint32_t u = atomicAdd(p.hdr + H_CLAIM, 1u);
-      if (u >= static_cast<uint32_t>(p.num_claims)) break;
+      if (u >= static_cast<uint32_t>(num_claims)) break;
       const int id = static_cast<int>(u);
       // the second half of a last unit narrower than 257 columns has no columns
       if (MODE == MODE_STORE && CL == 4 && id >= p.split_from && ((id - p.split_from) & 1) &&
@@ -1064,7 +1075,7 @@ __device__ void producer_tma(const KParams& p, const Smem& s, const Ctl& c, int 
   int claimed = 0;  // mailbox entries the leader has written
   if (leader) {
     if (!slow_region) atomicAdd(p.hdr + H_FAST, 1u);  // before its first claim
-    claim_unit<MODE, CL>(p, iter.box, claimed++, slow_region);
+    claim_unit<MODE, CL>(p, iter.box, claimed++, slow_region, iter.claims());
   }
   Work w;
   uint32_t stage = 0, phase = 0;
@@ -1126,7 +1137,7 @@ __device__ void producer_tma(const KParams& p, const Smem& s, const Ctl& c, int 
     const int claim_k = claims_here ? max(w.k0, w.k1 - CLAIM_AHEAD) : w.k1;
     for (int seg = 0; seg < 2 && ok; ++seg) {
       const int kb = seg == 0 ? w.k0 : claim_k, ke = seg == 0 ? claim_k : w.k1;
-      if (seg == 1 && claims_here) claim_unit<MODE, CL>(p, iter.box, claimed++, slow_region);
+      if (seg == 1 && claims_here) claim_unit<MODE, CL>(p, iter.box, claimed++, slow_region, iter.claims());
       if (kb >= ke) continue;
       if constexpr (MC == 2) {
         ok = mc2 ? produce_ksteps<MODE, CL, true>(p, s, c, w, kb, ke, nbox_a, bmask, bytes, n0, cta, half,

@@ -311,12 +311,22 @@ size_t a256(size_t v) { return round_up(v, WS_ALIGN); }
 // MOE_LAYERS), so that the one-call layer finds each part where the single
 // calls put it
 struct MoeWs {
-  size_t tile_off, counts, offsets, s2r, r2s, acc, unit_cnt, stage, total;
+  size_t tile_off, counts, offsets, s2r, r2s, acc, unit_cnt, stage, mbox, mbox_bytes, total;
 };
 
+// Dynamic schedule of the staged layer0: at most this many regions (CTA pairs).
+constexpr int MOE0_MAX_REGIONS = 256;
+
+// Bound on the staged layer0's units for any EP x TP split of these sizes:
+// m-units of BM * MOE0S_CL rows (one partial m-unit per expert at most) times
+// ceil(F / tp / 512) * tp <= ceil(F / 512) + R column tiles over the ranks.
+long long moe0_unit_bound(int R, int T, int F, int E, int topk) {
+  const long long n = static_cast<long long>(T) * topk;
+  const long long mts = (n + BM * MOE0S_CL - 1) / (BM * MOE0S_CL) + E;
+  return mts * ((F + 2 * BN - 1) / (2 * BN) + R);
+}
+
 MoeWs moe_layout(flux_op_t op, int R, int T, int H, int F, int E, int topk) {
-  (void)R;
-  (void)F;
   MoeWs w{};
   const size_t n = static_cast<size_t>(T) * topk;
   size_t o = WS_HEADER;
@@ -343,6 +353,12 @@ MoeWs moe_layout(flux_op_t op, int R, int T, int H, int F, int E, int topk) {
     o += a256(units * sizeof(uint32_t));
     w.stage = o;
     o += a256(n * static_cast<size_t>(H) * 2);
+    // mailboxes of the dynamic unit schedule: g regions of 2 ceil(U / g) + 2
+    // entries, at most 2 U + 4 MOE0_MAX_REGIONS
+    w.mbox = o;
+    w.mbox_bytes = a256(static_cast<size_t>(2 * moe0_unit_bound(R, T, F, E, topk) + 4 * MOE0_MAX_REGIONS) *
+                        sizeof(uint32_t));
+    o += w.mbox_bytes;
   }
   w.total = o;
   return w;
@@ -529,6 +545,18 @@ flux_status_t moe_layer0_impl(
   }
   const int grid = grid_dt<MODE_MOE_STAGED, MOE0S_CL>(dtype, dev, opts, max_units);
   if (grid == 0) return FLUX_ERR_CUDA;
+  const long long g = grid / MOE0S_CL;
+  const long long cap = 2 * ((max_units + g - 1) / g) + 2;
+  if (!(opts && opts->moe_static_schedule) && g <= MOE0_MAX_REGIONS &&
+      static_cast<size_t>(g * cap) * sizeof(uint32_t) <= L.mbox_bytes) {
+    // dynamic: each pair's producer claims the pair's next unit from the
+    // counter (units differ in cost: a half-wide last column tile, the
+    // experts' partial last m-units), so the last wave ends evenly
+    p.dyn = 1;
+    p.mbox = reinterpret_cast<uint32_t*>(ws + L.mbox);
+    p.mbox_cap = static_cast<int>(cap);
+    p.claim_reserve = 0;
+  }
   return launch_dt<MODE_MOE_STAGED, MOE0S_CL>(dtype, p, grid, s);
 }
 

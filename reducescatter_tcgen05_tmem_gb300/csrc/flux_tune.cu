@@ -203,7 +203,12 @@ extern "C" flux_status_t flux_tune_moe_layer0(
   for (int g : {8, 16}) {
     flux_opts_t o = base_opts();
     o.group_n = g;
-    cands.push_back(o);  // staged copy, CTA pairs
+    cands.push_back(o);  // staged copy, CTA pairs, dynamic unit schedule
+  }
+  {
+    flux_opts_t o = base_opts();
+    o.moe_static_schedule = 1;  // staged copy, CTA pairs, static unit schedule
+    cands.push_back(o);
   }
   {
     flux_opts_t o = base_opts();

@@ -188,6 +188,37 @@ def test_layer0_staging_split_matches_oracle(stage_ctas):
         check_close(oracle.widen(from_device(Hd[r]), c.dtype), ref[r], f"layer0 rank {r}")
 
 
+@pytest.mark.parametrize("num_ctas", [0, 2, 6])
+def test_layer0_dynamic_schedule_matches_static_bit_for_bit(num_ctas):
+    # the staged layer0 claims its units from a counter (default) or takes them
+    # round-robin (moe_static_schedule): a unit's arithmetic does not depend on
+    # which pair runs it.  One pair (2 CTAs) and three pairs fill their
+    # mailboxes with many claims each; three calls on one workspace show the
+    # schedule leaves it clean for the next call
+    c = configs.small(configs.CONFIGS["moe"], R=8, T=1024, H=512, F=8 * 640, E=8, topk=2, seed=65,
+                      force_empty=(2,))
+    d = configs.moe_inputs(c)
+    base = {"num_ctas": num_ctas} if num_ctas else {}
+    _, Hs, _ = _layer0(c, d=d, opts=dict(base, moe_static_schedule=1))
+    ref, _ = oracle.moe_layer0(d["x_shards"], d["w1_shards"], d["topk_ids"], c.E, c.dtype)
+    for r in range(c.R):
+        check_close(oracle.widen(from_device(Hs[r]), c.dtype), ref[r], f"static layer0 rank {r}")
+    n, Fr = c.T * c.topk, c.F // c.R
+    X = [to_device(x, c.dtype) for x in d["x_shards"]]
+    W1 = [to_device(w, c.dtype) for w in d["w1_shards"]]
+    ids = torch.from_numpy(d["topk_ids"]).cuda()
+    counts, offsets, s2r, r2s = _i32(c.E), _i32(c.E + 1), _i32(n), _i32(n)
+    ws = _ws(fx.flux_moe_workspace_size(fx.FLUX_OP_MOE_AG, c.R, c.T, c.H, c.F, c.E, c.topk))
+    for call in range(3):
+        Hd = [torch.full((n, Fr), float("nan"), dtype=torch_dtype(c.dtype), device="cuda") for _ in range(c.R)]
+        fx.flux_moe_ag_grouped_gemm(c.R, c.T, c.H, c.F, c.E, c.topk, DT[c.dtype], X, W1, ids, Hd, counts,
+                                    offsets, s2r, r2s, None, ws, opts=base or None)
+        st, rep = fx.flux_get_status(ws)
+        assert st == fx.FLUX_OK, rep
+        for r in range(c.R):
+            assert torch.equal(Hd[r], Hs[r]), f"call {call} rank {r}: dynamic differs from static"
+
+
 def test_layer0_staged_withheld_flag_times_out_and_gpu_stays_usable():
     # token shard 1 never publishes: the staging copy of its rows gives up after
     # the timeout, the GEMM tiles waiting for those rows leave too

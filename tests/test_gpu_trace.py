@@ -93,6 +93,32 @@ def test_gemm_rs_trace_covers_every_unit_in_order():
     assert set(np.unique(t["rank"][t["unit"] >= 0])) == set(range(c.R))
 
 
+def test_moe_layer0_dynamic_trace_covers_every_unit_once():
+    # the staged layer0's dynamic schedule: every unit of the device tile table
+    # claimed once and run by both CTAs of one pair
+    c = configs.small(configs.CONFIGS["moe"], R=8, T=2048, H=512, F=8 * 896, E=8, topk=2, seed=504)
+    d = configs.moe_inputs(c)
+    n, Fr = c.T * c.topk, c.F // c.R
+    H = [torch.full((n, Fr), float("nan"), dtype=torch.bfloat16, device="cuda") for _ in range(c.R)]
+    i32 = lambda k: torch.empty(k, dtype=torch.int32, device="cuda")  # noqa: E731
+    counts, off, s2r, r2s = i32(c.E), i32(c.E + 1), i32(n), i32(n)
+    ws = _ws(fx.flux_moe_workspace_size(fx.FLUX_OP_MOE_AG, c.R, c.T, c.H, c.F, c.E, c.topk))
+    tr = torch.zeros(8 + 152 * 64 * 8, dtype=torch.int64, device="cuda")
+    fx.flux_moe_ag_grouped_gemm(c.R, c.T, c.H, c.F, c.E, c.topk, fx.FLUX_BF16,
+                                [to_device(x, "bf16") for x in d["x_shards"]],
+                                [to_device(w, "bf16") for w in d["w1_shards"]],
+                                torch.from_numpy(d["topk_ids"]).cuda(), H, counts, off, s2r, r2s, None, ws,
+                                opts={"trace": tr})
+    st, rep = fx.flux_get_status(ws)
+    assert st == fx.FLUX_OK, rep
+    ref, (want_counts, _, _, _) = oracle.moe_layer0(d["x_shards"], d["w1_shards"], d["topk_ids"], c.E, "bf16")
+    for r in (0, c.R - 1):
+        check_close(oracle.widen(from_device(H[r]), "bf16"), ref[r], f"traced layer0 rank {r}")
+    m_units = int(sum((int(k) + 255) // 256 for k in want_counts))
+    t = ftrace.records(tr)
+    _check_records(t, units=m_units * ((Fr + 511) // 512) * c.R, per_unit=2)
+
+
 def test_trace_off_leaves_the_buffer_alone():
     c = configs.small(configs.CONFIGS["ag_mlp0"], R=2, M=256, N=1024, K=256, dtype="f16", seed=503)
     xs, w_s = configs.ag_inputs(c)
