@@ -167,6 +167,12 @@ typedef struct {
                                the current one, so pairs that drew cheaper units (the
                                half-wide last column tile, an expert's partial last
                                rows) take more of them */
+  int32_t acc_whole;        /* tiles with one 512-column accumulator (256 x 512 pair tiles):
+                               nonzero = the next tile's MMAs wait until the epilogue has
+                               read the whole accumulator; 0 (default) = the epilogue hands
+                               back its first 256 columns early and the next tile's first
+                               k-slices (as many as the operand ring holds) run their
+                               MMAs into those columns meanwhile.  Same results. */
 } flux_opts_t;
 
 /* What flux_get_status found in a workspace header. */

@@ -59,6 +59,7 @@ void fill_common(KParams& p, const flux_opts_t* opts, void* ws) {
   p.trace = opts ? static_cast<unsigned long long*>(opts->trace) : nullptr;
   p.trace_words = (opts && opts->trace) ? static_cast<long long>(opts->trace_words) : 0;
   p.debug_probe = opts ? opts->debug_probe : 0;
+  p.acc_halves = (opts && opts->acc_whole) ? 0 : 1;
 }
 
 flux_status_t zero_outputs(void* const* out, int n, size_t bytes, cudaStream_t s) {

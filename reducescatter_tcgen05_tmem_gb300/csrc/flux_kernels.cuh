@@ -327,6 +327,7 @@ struct KParams {
   // the R ranks' partials of it back to back (R items per claim)
   int rs_tile_major;
   int debug_probe;  // checked build: nonzero makes CTA 0 fail one check (CK_PROBE) on purpose
+  int acc_halves;   // one 512-column accumulator: handed back in two 256-column halves
 };
 
 constexpr uint32_t MBOX_DONE = 0xFFFFFFFFu;
@@ -941,6 +942,7 @@ struct Smem {
   uint64_t* empty;  // [STAGES] the MMAs reading the stage completed
   uint64_t* tfull;  // [2]
   uint64_t* tempty; // [2]
+  uint64_t* thalf;  // [2] the accumulator's first 256 columns read (acc_halves)
   uint64_t* drain;  // [1]
   uint32_t* tmem_slot;
   uint32_t* misc;   // [2] dynamic schedule: cluster-shape check, last CTA out
@@ -1275,6 +1277,12 @@ __device__ void mma_issuer(const KParams& p, const Smem& s, const Ctl& c, uint32
   // only this pair
   const uint16_t EMPTY_MASK = static_cast<uint16_t>((1u << ps.hw_cl) - 1u);
   const uint16_t pair_mask = static_cast<uint16_t>(0x3u << (ps.hw_rank & ~1));
+  // One 512-column accumulator (acc_halves): the epilogue hands back its first
+  // 256 columns before the rest, and the next tile's first k-slices (as many
+  // as the ring holds) issue their half-0 MMAs before the whole accumulator is
+  // free; their half-1 MMAs follow once it is.  Each half still accumulates
+  // its k-slices in order, so the results are those of the plain order.
+  constexpr bool SPLIT = G::ACC_BUFS == 1 && G::N_MMA == 2;
   ItemIter<MODE, CL> iter(p, total_mt, ps.vrank, &c);
   Work w;
   uint32_t stage = 0, phase = 0;
@@ -1284,19 +1292,49 @@ __device__ void mma_issuer(const KParams& p, const Smem& s, const Ctl& c, uint32
   while (ok && iter.next(w)) {
     const uint32_t b = it % G::ACC_BUFS;
     const uint32_t use = static_cast<uint32_t>(it / G::ACC_BUFS);
-    if ((PAIR == 2 ? wait_bar_remote(smem_u32(&s.tempty[b]), (use & 1u) ^ 1u, c, W_TEMPTY, b)
-                   : wait_bar(smem_u32(&s.tempty[b]), (use & 1u) ^ 1u, c, W_TEMPTY, b)) != 0)
-      break;
-    trace_now(p, it, TR_MMA_ACC);
-    tc_fence_after();
     const uint32_t d = tmem_base + b * G::ACC_COLS;
     // 256-column halves of the tile that start below N (a half wholly past N
     // has nothing to compute; its accumulator columns are never stored)
     const int n_live = (G::N_MMA > 1 && w.n0 + BN >= w.n_end) ? 1 : G::N_MMA;
-    for (int k = w.k0; k < w.k1; ++k) {
-      if (wait_bar(smem_u32(&s.full[stage]), phase, c, W_FULL, stage) != 0) { ok = false; break; }
-      if (k == w.k0) trace_now(p, it, TR_MMA_FIRST);
+    int pre = 0;  // leading k-slices whose half-0 MMAs were issued early
+    if (SPLIT && p.acc_halves && use > 0 && n_live == 2) {
+      if ((PAIR == 2 ? wait_bar_remote(smem_u32(&s.thalf[b]), (use & 1u) ^ 1u, c, W_TEMPTY, b + 2)
+                     : wait_bar(smem_u32(&s.thalf[b]), (use & 1u) ^ 1u, c, W_TEMPTY, b + 2)) != 0)
+        break;
+      trace_now(p, it, TR_MMA_ACC);
       tc_fence_after();
+      pre = min(G::STAGES, w.k1 - w.k0);
+      uint32_t st = stage, ph = phase;
+      for (int j = 0; j < pre; ++j) {
+        if (wait_bar(smem_u32(&s.full[st]), ph, c, W_FULL, st) != 0) { ok = false; break; }
+        if (j == 0) trace_now(p, it, TR_MMA_FIRST);
+        tc_fence_after();
+        const uint32_t sa = smem_u32(s.a + st * A_STAGE);
+        const uint32_t sb = smem_u32(s.b + st * G::B_STAGE);
+#pragma unroll
+        for (int kk = 0; kk < BK / UK; ++kk) {
+          const uint64_t ad = sdesc_sw128(sa + kk * UK * 2, 16, 1024);
+          const uint64_t bd = sdesc_sw128(sb + kk * UK * 128, BK * 128, 1024);
+          const uint32_t acc = (j > 0 || kk > 0) ? 1u : 0u;
+          if (PAIR == 2) umma2_f16(d, ad, bd, IDESC, acc);
+          else umma_f16(d, ad, bd, IDESC, acc);
+        }
+        if (++st == G::STAGES) { st = 0; ph ^= 1u; }
+      }
+      if (!ok) break;
+    }
+    if ((PAIR == 2 ? wait_bar_remote(smem_u32(&s.tempty[b]), (use & 1u) ^ 1u, c, W_TEMPTY, b)
+                   : wait_bar(smem_u32(&s.tempty[b]), (use & 1u) ^ 1u, c, W_TEMPTY, b)) != 0)
+      break;
+    if (pre == 0) trace_now(p, it, TR_MMA_ACC);
+    tc_fence_after();
+    for (int k = w.k0; k < w.k1; ++k) {
+      const bool early = k - w.k0 < pre;  // its stage is known full, its half 0 issued
+      if (!early) {
+        if (wait_bar(smem_u32(&s.full[stage]), phase, c, W_FULL, stage) != 0) { ok = false; break; }
+        if (k == w.k0) trace_now(p, it, TR_MMA_FIRST);
+        tc_fence_after();
+      }
       const uint32_t sa = smem_u32(s.a + stage * A_STAGE);
       const uint32_t sb = smem_u32(s.b + stage * G::B_STAGE);
 #pragma unroll
@@ -1307,6 +1345,7 @@ __device__ void mma_issuer(const KParams& p, const Smem& s, const Ctl& c, uint32
 #pragma unroll
         for (int h = 0; h < G::N_MMA; ++h) {
           if (h >= n_live) break;
+          if (SPLIT && h == 0 && early) continue;
           // B: N-major; 64-column (128 B) panels BK*128 B apart, 8-k-row groups
           // 1024 B apart; a 16-deep k step is 16 rows = +2048 B.  MMA h of a
           // pair reads panels 2h, 2h+1 and writes TMEM columns 256h ..
@@ -1448,12 +1487,30 @@ __device__ void epilogue(const KParams& p, const Smem& s, const Ctl& c, uint32_t
                                : smem_u32(&s.tempty[0]);
   const uint32_t sstg = smem_u32(s.stg + q * STG_WARP);
   using G = typename Unit<MODE, CL>::G;
+  constexpr bool SPLIT = G::ACC_BUFS == 1 && G::N_MMA == 2;
+  const uint32_t thalf0 = (PAIR == 2 && cta != 0)
+                              ? mapa_shared(smem_u32(&s.thalf[0]), static_cast<uint32_t>(ps.hw_rank & ~1))
+                              : smem_u32(&s.thalf[0]);
   // the first epilogue warp records the trace stamps
   const bool tracer = warp == KernelShape<MODE, DT, CL>::EPI_WARP0 && lane == 0;
   int nst = 0;  // tensor bulk stores this warp has committed
   while (iter.next(w)) {
     const uint32_t b = it % G::ACC_BUFS;
     const uint32_t use = static_cast<uint32_t>(it / G::ACC_BUFS);
+    // one 512-column accumulator: once this warp's loads of its first 256
+    // columns have completed, say so (every item, whether or not the MMA
+    // side uses it, so that the barrier's phases follow the items)
+    bool half_out = !SPLIT;
+    auto free_half = [&]() {
+      if (half_out) return;
+      half_out = true;
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) {
+        if (PAIR == 2 && cta != 0) mbar_arrive_remote(thalf0 + b * 8);
+        else mbar_arrive(smem_u32(&s.thalf[b]));
+      }
+    };
     // one lane waits so that the whole warp takes the same exit decision
     // before the warp-collective tcgen05.ld below
     int wr = 0;
@@ -1481,6 +1538,7 @@ __device__ void epilogue(const KParams& p, const Smem& s, const Ctl& c, uint32_t
     if (MODE == MODE_STORE || MODE == MODE_MOE_GATHER || MODE == MODE_MOE_STAGED) {
       // 64 columns at a time: two TMEM loads, one row-contiguous store pass
       for (int ch = 0; ch < G::TILE_N / 64; ++ch) {
+        if (ch * 64 == BN) free_half();
         if (ch * 64 >= ncols) break;  // warp-uniform
         uint32_t v[32], u[32];
         tmem_ld_32x32b_x32(taddr + ch * 64, v);
@@ -1554,6 +1612,7 @@ __device__ void epilogue(const KParams& p, const Smem& s, const Ctl& c, uint32_t
         // two staging boxes per warp alternate
         if (row0 < w.row_end) {
           for (int ch = 0; ch < G::TILE_N / 32; ++ch) {
+            if (ch * 32 == BN) free_half();
             if (ch * 32 >= ncols) break;  // warp-uniform
             uint32_t v[32];
             tmem_ld_32x32b_x32(taddr + ch * 32, v);
@@ -1586,6 +1645,7 @@ __device__ void epilogue(const KParams& p, const Smem& s, const Ctl& c, uint32_t
         const bool tok_ok = check_ok(c, !row_ok || (key >= 0 && key < p.T), CK_ACC_ROW, static_cast<uint32_t>(key));
         const bool col_ok = check_ok(c, n0 >= 0 && n0 < p.N, CK_ACC_COL, static_cast<uint32_t>(n0));
         for (int ch = 0; ch < G::TILE_N / 32; ++ch) {
+          if (ch * 32 == BN) free_half();
           if (ch * 32 >= ncols || !col_ok) break;  // warp-uniform
           uint32_t v[32];
           tmem_ld_32x32b_x32(taddr + ch * 32, v);
@@ -1594,6 +1654,7 @@ __device__ void epilogue(const KParams& p, const Smem& s, const Ctl& c, uint32_t
       }
     }
     // hand the accumulator back to the MMA warp
+    free_half();
     tc_fence_before();
     __syncwarp();
     if (lane == 0) {
@@ -2075,6 +2136,7 @@ fused_gemm_kernel(const __grid_constant__ KParams p) {
   s.tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * G::STAGES + 5);
   s.misc = s.tmem_slot + 1;
   s.xbar = bars + 2 * G::STAGES + 7;
+  s.thalf = bars + 2 * G::STAGES + 9;
 
   const int warp = threadIdx.x >> 5;
   const bool dyn = ItemIter<MODE, CL>::DYN_OK && p.dyn != 0;
@@ -2106,6 +2168,7 @@ fused_gemm_kernel(const __grid_constant__ KParams p) {
     for (int i = 0; i < 2; ++i) {
       mbar_init(smem_u32(&s.tfull[i]), 1);
       mbar_init(smem_u32(&s.tempty[i]), KS::EPI * PAIR);
+      mbar_init(smem_u32(&s.thalf[i]), KS::EPI * PAIR);
     }
     mbar_init(smem_u32(s.drain), 1);
     if (MODE == MODE_RS_CLUSTER) {

@@ -535,6 +535,7 @@ flux_status_t moe_layer0_impl(
   p.trace = opts ? static_cast<unsigned long long*>(opts->trace) : nullptr;
   p.trace_words = (opts && opts->trace) ? static_cast<long long>(opts->trace_words) : 0;
   p.debug_probe = opts ? opts->debug_probe : 0;
+  p.acc_halves = (opts && opts->acc_whole) ? 0 : 1;
   const long long max_units =
       (static_cast<long long>((n + BM * cl - 1) / (BM * cl)) + E) * p.Nt *
       static_cast<long long>(tp);
@@ -666,6 +667,7 @@ flux_status_t moe_layer1_impl(
   p.trace = opts ? static_cast<unsigned long long*>(opts->trace) : nullptr;
   p.trace_words = (opts && opts->trace) ? static_cast<long long>(opts->trace_words) : 0;
   p.debug_probe = opts ? opts->debug_probe : 0;
+  p.acc_halves = (opts && opts->acc_whole) ? 0 : 1;
   const long long max_units =
       (static_cast<long long>((n + BM * MOE1_CL - 1) / (BM * MOE1_CL)) + E) * p.Nt *
       static_cast<long long>(tp);

@@ -413,6 +413,58 @@ def test_gemm_rs_dynamic_schedule_integer_inputs_bit_exact(num_ctas, rs_tile):
         assert torch.count_nonzero(ws).item() == 0, name
 
 
+@pytest.mark.parametrize("K", [128, 1024])
+@pytest.mark.parametrize("form", ["dynamic", "static"])
+def test_ag_gemm_accumulator_halves_match_whole_bit_for_bit(form, K):
+    # 256 x 512 pair tiles hand their accumulator back in two halves (default)
+    # or whole (acc_whole): the next tile's first k-slices (2 of them at
+    # K = 128, the ring's 4 at K = 1024) run their first-half MMAs early; each
+    # half still accumulates in k order, so the bits are those of the whole
+    # hand-over.  N/R = 768: every rank's last tile is 256 wide (no early MMAs)
+    c = configs.small(configs.CONFIGS["ag_mlp0"], R=8, M=1024, N=6144, K=K, dtype="f16", seed=73)
+    xs, w_s = configs.ag_inputs(c)
+    X = [to_device(x, c.dtype) for x in xs]
+    W = [to_device(w, c.dtype) for w in w_s]
+    nbytes = (_static_ws_bytes(fx.FLUX_OP_AG_GEMM, c.R, c.M, c.N, c.K) if form == "static"
+              else fx.flux_workspace_size(fx.FLUX_OP_AG_GEMM, c.R, c.M, c.N, c.K))
+    outs = []
+    for whole in (0, 1):
+        ws = _ws(nbytes)
+        out = [_out(c.M, c.N // c.R, c.dtype) for _ in range(c.R)]
+        fx.flux_ag_gemm(c.R, c.M, c.N, c.K, DT[c.dtype], X, W, out, None, ws, opts={"acc_whole": whole})
+        _ok(ws)
+        outs.append(out)
+    for r in range(c.R):
+        assert torch.equal(outs[0][r].view(torch.int16), outs[1][r].view(torch.int16)), f"rank {r}"
+    ref = oracle.ag_gemm(xs, w_s, c.dtype)
+    for r in (0, 7):
+        check_close(oracle.widen(from_device(outs[0][r]), c.dtype), ref[r], f"ag halves rank {r}")
+
+
+@pytest.mark.parametrize("N", [1288, 1280])
+@pytest.mark.parametrize("rs_tile", [1, 3])
+def test_gemm_rs_accumulator_halves_integer_inputs_bit_exact(rs_tile, N):
+    # GEMM-RS's 256 x 512 pair tiles with the two-half hand-over (default) and
+    # the whole one; integer inputs make every fp32 sum exact in any order.
+    # N = 1288: the last tile's second half holds 8 columns; N = 1280: the
+    # last tile is 256 wide.  K / R = 512: 8 k-slices per rank, twice the ring
+    c = configs.small(configs.CONFIGS["rs_mlp1"], R=8, M=1024, N=N, K=4096, dist="int", seed=74)
+    As, Bs = configs.rs_inputs(c)
+    A = [to_device(a, c.dtype) for a in As]
+    B = [to_device(b, c.dtype) for b in Bs]
+    ref = oracle.gemm_rs(As, Bs, c.dtype)
+    for whole in (0, 1):
+        ws = _ws(fx.flux_workspace_size(fx.FLUX_OP_GEMM_RS, c.R, c.M, c.N, c.K))
+        out = [_out(c.M // c.R, c.N, c.dtype) for _ in range(c.R)]
+        for _ in range(2):
+            fx.flux_gemm_rs(c.R, c.M, c.N, c.K, DT[c.dtype], A, B, out, ws,
+                            opts={"rs_tile": rs_tile, "acc_whole": whole})
+        _ok(ws)
+        for o in range(c.R):
+            assert np.array_equal(oracle.widen(from_device(out[o]), c.dtype), ref[o]), (whole, o)
+        assert torch.count_nonzero(ws).item() == 0
+
+
 @pytest.mark.parametrize("R,M,N,K,dtype,num_ctas", [
     (8, 1000, 2056, 1024, "f16", 16),   # ragged M and N tails, 125-row owner chunks
     (4, 512, 1032, 2048, "bf16", 16),   # ragged last n-unit (8 columns past 1024)

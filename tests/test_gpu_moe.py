@@ -219,6 +219,20 @@ def test_layer0_dynamic_schedule_matches_static_bit_for_bit(num_ctas):
             assert torch.equal(Hd[r], Hs[r]), f"call {call} rank {r}: dynamic differs from static"
 
 
+def test_layer0_accumulator_halves_match_whole_bit_for_bit():
+    # the staged layer0's 256 x 512 tiles with the two-half accumulator
+    # hand-over (default) and the whole one (acc_whole): same bits.  F/R = 768:
+    # each rank's last column tile is 256 wide; H = 192: 3 k-slices per tile
+    c = configs.small(configs.CONFIGS["moe"], R=4, T=1024, H=192, F=4 * 768, E=8, topk=2, seed=75)
+    d = configs.moe_inputs(c)
+    _, Ha, _ = _layer0(c, d=d)
+    _, Hb, _ = _layer0(c, d=d, opts={"acc_whole": 1})
+    for r in range(c.R):
+        assert torch.equal(Ha[r], Hb[r]), f"rank {r}"
+    ref, _ = oracle.moe_layer0(d["x_shards"], d["w1_shards"], d["topk_ids"], c.E, c.dtype)
+    check_close(oracle.widen(from_device(Ha[0]), c.dtype), ref[0], "layer0 halves rank 0")
+
+
 def test_layer0_staged_withheld_flag_times_out_and_gpu_stays_usable():
     # token shard 1 never publishes: the staging copy of its rows gives up after
     # the timeout, the GEMM tiles waiting for those rows leave too
