@@ -106,13 +106,15 @@ typedef struct {
                                are serialised over the ranks) */
   int32_t moe_pull_gather;  /* MoE layer0: nonzero = the GEMM's producer warps gather each
                                A tile's token rows themselves (single CTAs, 128 x 256
-                               tiles); 0 (default) = every CTA first stages a share of
-                               the grouped rows in the workspace and CTA pairs compute
-                               256 x 512 tiles once their rows' ready counts are in */
-  int32_t moe_stage_ctas;   /* MoE layer0 staged, and the push form of AllGather + GEMM:
-                               how many CTAs copy rows before they compute (0 = all;
-                               fewer = a communication / computation split of the grid,
-                               the others compute from the start) */
+                               tiles); 0 (default) = the epilogue warps of every CTA
+                               copy a share of the grouped rows into the workspace
+                               while CTA pairs compute 256 x 512 tiles, each once its
+                               rows' ready counts are in */
+  int32_t moe_stage_ctas;   /* MoE layer0 staged: how many CTAs' epilogue warps copy rows
+                               (0 = all); the push form of AllGather + GEMM: how many
+                               CTAs copy rows before they compute (0 = all; fewer = a
+                               communication / computation split of the grid, the
+                               others compute from the start) */
   int32_t rs_tile;          /* GEMM-RS on whole units (dynamic schedule): 0 = the
                                library's choice; 1 = regions of 4 CTAs, 256 x 512
                                CTA-pair tiles with one 512-column accumulator, B shared

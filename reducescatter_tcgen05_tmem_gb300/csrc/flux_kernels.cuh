@@ -218,7 +218,10 @@ __host__ __device__ constexpr int epi_warps(int mode) {
 __host__ __device__ constexpr bool is_moe(int mode) {
   return mode == MODE_MOE_GATHER || is_scatter(mode) || mode == MODE_MOE_STAGED;
 }
-constexpr int STAGE_BLK = 32;     // MOE_STAGED: rows per staging block (one ready count)
+// MOE_STAGED: rows per staging block (one ready count).  Small, so that the
+// rows of the first units are spread over every copying CTA and ready early
+// (8 rows: 10 us less per call than 32 at the MoE workload's sizes)
+constexpr int STAGE_BLK = 8;
 constexpr int STAGE_UNROLL = 16;  // MOE_STAGED: 16-byte loads in flight per lane
 
 // device status header at the start of every workspace (256 bytes)
@@ -2039,26 +2042,36 @@ static __device__ void push_rows(const KParams& p, const Ctl& c) {
   }
 }
 
-// MoE layer0, staged: every thread of the first stage_ctas CTAs (all CTAs
-// by default) takes part.  Blocks of 32 grouped rows, in ascending m-unit
-// order, are dealt to those CTAs in turn; a
-// warp copies one row at a time (the token row of the shard that owns it,
-// after that shard's ready flag) into the staging buffer, 16 loads of 16
-// bytes in flight per lane.  When the whole CTA is done with a block, its
-// count goes to the unit's ready counter (release), which the GEMM producers
-// wait for.
+// MoE layer0, staged: the epilogue warps of the first stage_ctas CTAs (all
+// CTAs by default) copy the grouped rows while the producer and MMA warps
+// start on the units whose rows are in (the epilogue warps have nothing else
+// to do until the CTA's first accumulator is full).  Blocks of STAGE_BLK
+// grouped rows, in ascending m-unit order, are dealt to those CTAs in turn
+// (so the first units' rows are spread over all of them); a warp
+// copies one row at a time (the token row of the shard that owns it, after
+// that shard's ready flag) into the staging buffer, 16 loads of 16 bytes in
+// flight per lane.  When the group's warps are done with a block (named
+// barrier 1), its count goes to the unit's ready counter (release), which the
+// GEMM producers wait for.  False when a shard's flag timed out (recorded).
+__device__ __forceinline__ bool group_all(int v, int nthreads) {
+  int r;
+  asm volatile("{\n\t.reg .pred a, b;\n\tsetp.ne.s32 a, %1, 0;\n\t"
+               "bar.red.and.pred b, 1, %2, a;\n\tselp.s32 %0, 1, 0, b;\n\t}"
+               : "=r"(r) : "r"(v), "r"(nthreads) : "memory");
+  return r != 0;
+}
+
 template <int CL>
-__device__ void stage_rows(const KParams& p, const Ctl& c, int total_mt) {
+__device__ bool stage_rows(const KParams& p, const Ctl& c, int total_mt, int warp, int nwarps) {
   constexpr int UROWS = BM * CL;
   constexpr int BLKS = UROWS / STAGE_BLK;
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int nwarps = static_cast<int>(blockDim.x >> 5);
+  const int lane = threadIdx.x & 31;
   const int chunks = p.H / 8;  // 16-byte chunks per row
   uint32_t ready = (p.flags == nullptr) ? 0xFFFFFFFFu : 0u;
   const int items = total_mt * BLKS;
   const int copiers = p.stage_ctas > 0 ? min(p.stage_ctas, static_cast<int>(gridDim.x))
                                        : static_cast<int>(gridDim.x);
-  if (static_cast<int>(blockIdx.x) >= copiers) return;
+  if (static_cast<int>(blockIdx.x) >= copiers) return true;
   for (int i = blockIdx.x; i < items; i += copiers) {
     const int gmt = i / BLKS, b = i - (i / BLKS) * BLKS;
     int lo = 0, hi = p.E;  // the unit's expert: largest e with tile_off[e] <= gmt
@@ -2104,9 +2117,10 @@ __device__ void stage_rows(const KParams& p, const Ctl& c, int total_mt) {
     // readers' TMA) before its count
     __threadfence();
     fence_proxy_async_global();
-    if (!__syncthreads_and(ok)) return;  // a shard flag timed out (recorded)
-    if (threadIdx.x == 0) atomicAdd(p.unit_cnt + gmt, 1u);
+    if (!group_all(ok, nwarps * 32)) return false;
+    if (warp == 0 && lane == 0) atomicAdd(p.unit_cnt + gmt, 1u);
   }
+  return true;
 }
 
 // ---------------------------------------------------------------- kernel
@@ -2211,7 +2225,6 @@ fused_gemm_kernel(const __grid_constant__ KParams p) {
 #endif
   int total_mt = 0;
   if (is_moe(MODE)) total_mt = __ldg(p.tile_off + p.E);
-  if constexpr (MODE == MODE_MOE_STAGED) stage_rows<CL>(p, c, total_mt);
   if constexpr (MODE == MODE_STORE) {
     if (p.push && run) push_rows(p, c);
   }
@@ -2239,6 +2252,10 @@ fused_gemm_kernel(const __grid_constant__ KParams p) {
   } else if constexpr (MODE == MODE_MOE_SCATTER_RED) {
     epilogue_scatter_red<CL>(p, s, c, tmem_base, total_mt, warp, warp - KS::EPI_WARP0, ps);
   } else {
+    // (staged MoE layer0: the copy first; after a shard flag timed out the
+    // epilogue still runs, its waits give up as the producer's do)
+    if constexpr (MODE == MODE_MOE_STAGED)
+      stage_rows<CL>(p, c, total_mt, warp - KS::EPI_WARP0, KS::EPI);
     epilogue<MODE, DT, CL>(p, s, c, tmem_base, total_mt, warp, ps);
   }
 
