@@ -678,41 +678,59 @@ __device__ __forceinline__ Work decode_reduce(const KParams& p, int u, int cta) 
 //   0  rank outermost, then bands of group_n n-tiles with the m-tile fastest
 //   1  rank innermost: the ranks' tiles of one (m, n) are consecutive units
 //   2  band outermost, then rank, then the m-tile fastest inside the band
+//   3  expert outermost, then n-tile, then the expert's m-units, rank fastest:
+//      the weight blocks of one expert column tile and the expert's rows are
+//      in use together, and each is read while the other stays in L2
 template <int CL>
 __device__ __forceinline__ Work decode_moe(const KParams& p, int u, int total_mt, int cta, int tile_n) {
   Work w;
   const int per_rank = total_mt * p.Nt;
   int tr, t;  // rank inside the expert's group; the unit's index among that rank's
-  if (p.moe_order == 1) {
-    tr = u % p.moe_tp;
-    t = u / p.moe_tp;
-  } else if (p.moe_order == 2) {
-    const int gn = p.group_n;
-    const int full = p.Nt / gn;              // full bands
-    const int band = total_mt * gn;          // one rank's units in a full band
-    const int done = full * band * p.moe_tp;
-    if (u < done) {
-      const int g = u / (band * p.moe_tp);
-      const int rem = u - g * band * p.moe_tp;
-      tr = rem / band;
-      t = g * band + (rem - tr * band);
-    } else {
-      const int tail = total_mt * (p.Nt - full * gn);
-      const int rem = u - done;
-      tr = rem / tail;
-      t = full * band + (rem - tr * tail);
-    }
-  } else {
-    tr = u / per_rank;
-    t = u - tr * per_rank;
-  }
   int gmt, nt;
-  // m-tile fastest inside bands of group_n n-tiles
-  raster(t, total_mt, p.Nt, p.group_n, gmt, nt);
-  int lo = 0, hi = p.E;  // largest e with tile_off[e] <= gmt
-  while (hi - lo > 1) {
-    const int mid = (lo + hi) >> 1;
-    if (__ldg(p.tile_off + mid) <= gmt) lo = mid; else hi = mid;
+  int lo = 0, hi = p.E;  // the m-unit's expert: largest e with tile_off[e] <= gmt
+  if (p.moe_order == 3) {
+    const int per_mt = p.Nt * p.moe_tp;  // units per m-unit
+    while (hi - lo > 1) {
+      const int mid = (lo + hi) >> 1;
+      if (__ldg(p.tile_off + mid) * per_mt <= u) lo = mid; else hi = mid;
+    }
+    const int t0 = __ldg(p.tile_off + lo);
+    const int ke = __ldg(p.tile_off + lo + 1) - t0;  // >= 1: u lies in this expert's units
+    const int local = u - t0 * per_mt;
+    nt = local / (ke * p.moe_tp);
+    const int rem = local - nt * ke * p.moe_tp;
+    gmt = t0 + rem / p.moe_tp;
+    tr = rem - (rem / p.moe_tp) * p.moe_tp;
+  } else {
+    if (p.moe_order == 1) {
+      tr = u % p.moe_tp;
+      t = u / p.moe_tp;
+    } else if (p.moe_order == 2) {
+      const int gn = p.group_n;
+      const int full = p.Nt / gn;              // full bands
+      const int band = total_mt * gn;          // one rank's units in a full band
+      const int done = full * band * p.moe_tp;
+      if (u < done) {
+        const int g = u / (band * p.moe_tp);
+        const int rem = u - g * band * p.moe_tp;
+        tr = rem / band;
+        t = g * band + (rem - tr * band);
+      } else {
+        const int tail = total_mt * (p.Nt - full * gn);
+        const int rem = u - done;
+        tr = rem / tail;
+        t = full * band + (rem - tr * tail);
+      }
+    } else {
+      tr = u / per_rank;
+      t = u - tr * per_rank;
+    }
+    // m-tile fastest inside bands of group_n n-tiles
+    raster(t, total_mt, p.Nt, p.group_n, gmt, nt);
+    while (hi - lo > 1) {
+      const int mid = (lo + hi) >> 1;
+      if (__ldg(p.tile_off + mid) <= gmt) lo = mid; else hi = mid;
+    }
   }
   const int grp = lo / p.moe_el;
   w.r = grp * p.moe_tp + tr;
