@@ -571,7 +571,8 @@ def run_ours(args):
     dom = max(st.ops, key=lambda o: per_op[o])
     dom_ms = per_op[dom] / args.steps
     dom_tf = st.flops[dom] / (dom_ms * 1e-3) / 1e12
-    traffic = load_traffic(dom)
+    # (the committed DRAM bytes are for the full-size launch: none at reduced sizes)
+    traffic = None if args.small else load_traffic(dom)
     # the peak that matches the timed window: the burst figure (a matmul timed
     # alone) for a region under a second, the sustained one (seconds back to
     # back under the power limit) for longer regions
