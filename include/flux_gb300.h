@@ -208,6 +208,10 @@ int flux_version(void);
  * skipped, or, for a load, moved to the tensor's origin.  No check traps. */
 int flux_checks_enabled(void);
 
+/* sizeof(flux_opts_t) as this library was compiled: a binding checks its own
+ * copy of the struct against it before passing options. */
+size_t flux_opts_size(void);
+
 /* Human-readable name of a status code (static string, never NULL). */
 const char* flux_status_string(flux_status_t s);
 

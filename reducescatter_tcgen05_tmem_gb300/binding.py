@@ -95,6 +95,7 @@ _opt = ctypes.POINTER(flux_opts_t)
 _SIGS = {
     "flux_version": ([], ctypes.c_int),
     "flux_checks_enabled": ([], ctypes.c_int),
+    "flux_opts_size": ([], _sz),
     "flux_status_string": ([_i], ctypes.c_char_p),
     "flux_last_cuda_error": ([], ctypes.c_int),
     "flux_workspace_size": ([_i, _i, _i, _i, _i], _sz),
@@ -134,6 +135,10 @@ for _name, (_args, _res) in _SIGS.items():
     _fn.restype = _res
 
 EXPORTED = tuple(_SIGS)
+if _lib.flux_opts_size() != ctypes.sizeof(flux_opts_t):
+    raise ImportError(f"flux_opts_t: the binding's copy ({ctypes.sizeof(flux_opts_t)} bytes) does not match "
+                      f"{LIB_PATH} ({_lib.flux_opts_size()} bytes); rebuild the library")
+_OPT_FIELDS = frozenset(name for name, _ in flux_opts_t._fields_)
 
 
 # ---------------------------------------------------------------- marshalling
@@ -171,6 +176,8 @@ def _opts(opts):
     if isinstance(opts, dict):
         o = flux_opts_t()
         for k, v in opts.items():
+            if k not in _OPT_FIELDS:
+                raise KeyError(f"flux_opts_t has no field {k!r}")
             if k == "trace" and v is not None and not isinstance(v, int):
                 # a tensor: its address, and its size unless given
                 if "trace_words" not in opts:
@@ -204,6 +211,10 @@ def flux_version() -> int:
 
 def flux_checks_enabled() -> bool:
     return bool(_lib.flux_checks_enabled())
+
+
+def flux_opts_size() -> int:
+    return int(_lib.flux_opts_size())
 
 
 def flux_status_string(status: int) -> str:

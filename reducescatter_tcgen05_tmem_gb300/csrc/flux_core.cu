@@ -144,6 +144,8 @@ extern "C" int flux_version(void) { return 200; }
 
 extern "C" int flux_checks_enabled(void) { return FLUX_CHECKS ? 1 : 0; }
 
+extern "C" size_t flux_opts_size(void) { return sizeof(flux_opts_t); }
+
 extern "C" const char* flux_status_string(flux_status_t s) {
   switch (s) {
     case FLUX_OK: return "FLUX_OK";

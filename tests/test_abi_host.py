@@ -38,6 +38,41 @@ def test_library_exports_every_declared_symbol(fx):
         assert name in fx.EXPORTED, f"{name} has no Python binding"
 
 
+def _opts_fields_in_header():
+    text = open(HEADER).read()
+    body = re.search(r"typedef struct \{(.*?)\} flux_opts_t;", text, flags=re.S).group(1)
+    body = re.sub(r"/\*.*?\*/", "", body, flags=re.S)
+    return re.findall(r"^\s*[a-z0-9_]+\*?\s+\*?([a-z0-9_]+);", body, flags=re.M)
+
+
+def test_opts_struct_matches_the_header(fx):
+    # the binding's copy of flux_opts_t has the header's fields in the header's
+    # order and the size the library was compiled with
+    names = [n for n, _ in fx.binding.flux_opts_t._fields_]
+    assert names == _opts_fields_in_header()
+    assert fx.flux_opts_size() == ctypes.sizeof(fx.binding.flux_opts_t)
+
+
+class _WS:  # stand-in workspace: only its address and size are looked at
+    def __init__(self, n, addr=1 << 20):
+        self.n, self.addr = n, addr
+
+    def data_ptr(self):
+        return self.addr
+
+    def numel(self):
+        return self.n
+
+    def element_size(self):
+        return 1
+
+
+def test_unknown_option_is_refused_before_the_call(fx):
+    # a misspelt option name is an error, not a silently ignored attribute
+    with pytest.raises(KeyError, match="acc_whol"):
+        fx.flux_gemm(64, 64, 64, fx.FLUX_F16, FAKE, FAKE, FAKE, _WS(256), opts={"acc_whol": 1}, stream=0)
+
+
 def test_version_and_status_strings(fx):
     assert fx.flux_version() >= 100
     assert fx.flux_status_string(fx.FLUX_ERR_TIMEOUT) == "FLUX_ERR_TIMEOUT"
@@ -65,7 +100,12 @@ def test_workspace_sizes(fx):
     s = fx.flux_moe_workspace_size(fx.FLUX_OP_MOE_RS, 8, 4096, 4096, 14336, 8, 2)
     # header + tile table + routing + fp32 token rows (T x H)
     assert s >= 256 + 4096 * 4096 * 4
-    assert fx.flux_moe_workspace_size(fx.FLUX_OP_MOE_AG, 8, 4096, 4096, 14336, 8, 2) > 256
+    # layer0: header, tile table, a ready count per 256-row unit, the staged rows
+    # [T*topk x H] and the mailboxes of its unit schedule, 2 U + 1024 entries for
+    # U = (ceil(T*topk / 256) + E)(ceil(F / 512) + R)
+    u = (8192 // 256 + 8) * (-(-14336 // 512) + 8)
+    m0 = fx.flux_moe_workspace_size(fx.FLUX_OP_MOE_AG, 8, 4096, 4096, 14336, 8, 2)
+    assert m0 == 256 + 256 + 256 + 8192 * 4096 * 2 + -(-(2 * u + 1024) * 4 // 256) * 256
     assert fx.flux_moe_workspace_size(fx.FLUX_OP_MOE_AG, 3, 4096, 4096, 14336, 8, 2) == 0
     # the EP x TP split does not change the workspace, and F need not divide by R
     assert fx.flux_moe_workspace_size(fx.FLUX_OP_MOE_EP_RS, 8, 4096, 4096, 14336, 8, 2) == s
