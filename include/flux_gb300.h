@@ -169,6 +169,14 @@ typedef struct {
                                the current one, so pairs that drew cheaper units (the
                                half-wide last column tile, an expert's partial last
                                rows) take more of them */
+  int32_t rs_group;         /* GEMM-RS on regions of 4 CTAs (rs_tile 1): how many ranks'
+                               partials of one output tile a region computes back to
+                               back into one TMEM accumulator before it adds the sum
+                               into the owner's fp32 rows (a divisor of R; 0 = the
+                               library's choice, 1 = every rank's partial added on its
+                               own).  Fewer adds and accumulator hand-overs, longer
+                               work units; the summation order of the ranks changes
+                               (results within the fp32 rounding of the adds) */
   int32_t acc_whole;        /* tiles with one 512-column accumulator (256 x 512 pair tiles):
                                nonzero = the next tile's MMAs wait until the epilogue has
                                read the whole accumulator; 0 (default) = the epilogue hands

@@ -68,7 +68,8 @@ class flux_opts_t(ctypes.Structure):
                 ("moe_l1_ranks", ctypes.c_int32), ("trace", ctypes.c_void_p),
                 ("trace_words", ctypes.c_uint64), ("ag_push", ctypes.c_int32),
                 ("debug_probe", ctypes.c_int32),
-                ("moe_static_schedule", ctypes.c_int32), ("acc_whole", ctypes.c_int32)]
+                ("moe_static_schedule", ctypes.c_int32), ("rs_group", ctypes.c_int32),
+                ("acc_whole", ctypes.c_int32)]
 
 
 class flux_device_report_t(ctypes.Structure):

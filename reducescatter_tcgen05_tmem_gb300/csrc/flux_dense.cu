@@ -42,6 +42,12 @@ constexpr int DENSE_CL8 = 8;
 // GEMM-RS form of the whole-unit dynamic schedule when opts->rs_tile is 0
 // (1: regions of 4, 256 x 512 pair tiles; 2: regions of 8, 256 x 256 pair tiles)
 constexpr int DEFAULT_RS_TILE = 1;
+// GEMM-RS on regions of 4: ranks whose partials of one tile are summed in TMEM
+// before the fp32 adds (see rs_group in the kernel parameters).  At 4096 x
+// 49152 x 12288 over 8 ranks, against each rank's partial added on its own:
+// 1, 2, 4, 8 ranks 3255-3263, 3056-3107, 3045-3062, 2971-3023 us alone; the
+// whole step (power-limited) best with 4
+constexpr int DEFAULT_RS_GROUP = 4;
 // GEMM-RS of few rows: clusters of 4 CTAs reduce the R partials of a tile
 // through distributed shared memory (each CTA computes R / 4 partials)
 constexpr int RS_CLUSTER_CL = 4;
@@ -546,7 +552,22 @@ flux_status_t gemm_rs_impl(int R, int M, int N, int K, flux_dtype_t dtype,
     }
     if (dgrid > 0) {
       p.tiles_per_group = tiles_per_group(dgrid, DENSE_CL, tiles);
+      // rank groups: a region sums the partials of G ranks of one tile in
+      // TMEM and drains the sum once (one fp32 add per G partials)
+      const int G = (opts && opts->rs_group > 0) ? opts->rs_group : DEFAULT_RS_GROUP;
+      if (G > 1 && R % G == 0) {
+        // the last g group claims go out rank by rank: G times as many claims,
+        // each a single rank's unit
+        const int g = dgrid / DENSE_CL;
+        const int groups = p.num_units / G;
+        p.rs_group = G;
+        p.split_from = groups > g ? groups - g : 0;
+        p.num_claims = p.split_from + (groups - p.split_from) * G;
+        p.mbox_cap = 2 * ((p.num_claims + g - 1) / g) + 2;
+      }
       if (launch_dyn_dt<MODE_REDUCE, DENSE_CL>(dtype, p, dgrid, s) == FLUX_OK) return FLUX_OK;
+      p.rs_group = 1;
+      p.split_from = p.num_units;
       p.dyn = 0;  // launch form refused: the static schedule below
       p.mbox = nullptr;
       p.mbox_cap = 0;

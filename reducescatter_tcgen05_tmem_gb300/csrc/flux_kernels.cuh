@@ -288,7 +288,8 @@ struct KParams {
   int Nt_tile;             // REDUCE: output tiles (TILE_N columns) per row block, for the counters
   int num_claims;          // dynamic schedule: claim ids (units, the last ones as two halves)
   int split_from;          // dynamic schedule, store mode: units from here on are claimed as
-                           // two 256-column halves (num_units: none)
+                           // two 256-column halves (num_units: none); reduce mode with
+                           // rank groups: group claims from here on are claimed rank by rank
   long long total_ksteps;  // REDUCE stream-K: num_units * KT
   const uint32_t* flags;   // AG ready flags (nullptr = all ready)
   uint32_t epoch;
@@ -329,6 +330,8 @@ struct KParams {
   // GEMM-RS, dynamic schedule: a claim is one output tile, and the region runs
   // the R ranks' partials of it back to back (R items per claim)
   int rs_tile_major;
+  int rs_group;      // REDUCE, dynamic: ranks whose partials of one tile a region sums in
+                     // TMEM before one drain (1 = each rank's partial drained on its own)
   int debug_probe;  // checked build: nonzero makes CTA 0 fail one check (CK_PROBE) on purpose
   int acc_halves;   // one 512-column accumulator: handed back in two 256-column halves
 };
@@ -504,8 +507,10 @@ struct Work {
   int e;       // expert (MoE)
   int k0, k1;  // k-slice range of this item
   int tile;    // linear 128-row output-tile id of this CTA's part (REDUCE counters)
-  int rsub;    // MOE_SCATTER_RED: place of this rank's partial in the tile's rank group
-  int rcnt;    // MOE_SCATTER_RED: partials of the tile reduced on chip (the group's size)
+  int rsub;    // MOE_SCATTER_RED, grouped REDUCE: place of this rank's partial in the
+               // tile's rank group
+  int rcnt;    // MOE_SCATTER_RED, grouped REDUCE: partials of the tile reduced on chip
+               // (the group's size)
   int uid;     // the unit (or claim) id the item came from (traces)
 };
 
@@ -750,6 +755,32 @@ __device__ __forceinline__ Work decode_moe(const KParams& p, int u, int total_mt
   return w;
 }
 
+// GEMM-RS with rank groups (rs_group = G > 1): claim c stands for the G units
+// of one output tile whose ranks form group rg; the claims follow the unit
+// order of decode_reduce with the ranks taken G at a time (rank group rg of
+// tile group g: units g TG R + (rg G + j) TG + t, j < G).  Returns the unit
+// of the claim's j-th rank.
+__device__ __forceinline__ int rs_group_unit(const KParams& p, int c, int j) {
+  const int G = p.rs_group, RG = p.R / G;
+  const int tiles = p.Mt * p.Nt;
+  const int TG = p.tiles_per_group;
+  const int full_groups = tiles / TG;
+  const int full_claims = full_groups * TG * RG;
+  int base, tgg, rem;
+  if (c < full_claims) {
+    const int g = c / (TG * RG);
+    rem = c - g * TG * RG;
+    base = g * TG * p.R;
+    tgg = TG;
+  } else {
+    rem = c - full_claims;
+    base = full_groups * TG * p.R;
+    tgg = tiles - full_groups * TG;
+  }
+  const int rg = rem / tgg, t = rem - rg * tgg;
+  return base + (rg * G + j) * tgg + t;
+}
+
 // Iterates the items of this CTA identically in every role.  All CTAs of a
 // cluster (of a region, under the dynamic schedule) walk the same units
 // (region index = blockIdx / CL).  `cta` is the CTA's part of the unit.
@@ -825,13 +856,16 @@ struct ItemIter {
       return true;
     }
     if (DYN_OK && dyn) {
-      if (MODE == MODE_REDUCE && p.rs_tile_major && sub > 0) {
-        // the next rank of the tile this region claimed
-        w = decode_reduce<CL>(p, cur_claim * p.R + sub, cta);
+      if (MODE == MODE_REDUCE && sub > 0) {
+        // the next rank of the tile this region claimed (tile-major: all R
+        // ranks; rank groups: the group's G)
+        const int cnt = p.rs_tile_major ? p.R : p.rs_group;
+        w = decode_reduce<CL>(p, p.rs_tile_major ? cur_claim * p.R + sub : rs_group_unit(p, cur_claim, sub),
+                              cta);
         w.rsub = sub;
-        w.rcnt = p.R;
+        w.rcnt = cnt;
         w.uid = cur_claim;
-        if (++sub == p.R) sub = 0;
+        if (++sub == cnt) sub = 0;
         return true;
       }
       uint32_t v = 0;
@@ -862,6 +896,18 @@ struct ItemIter {
         w.rsub = 0;
         w.rcnt = p.R;
         sub = p.R > 1 ? 1 : 0;
+      } else if (MODE == MODE_REDUCE && p.rs_group > 1 && id >= p.split_from) {
+        // the last rank groups are claimed rank by rank (their partials added
+        // one by one), so that the regions run out of work at about the same time
+        const int j = id - p.split_from;
+        w = decode_reduce<CL>(p, rs_group_unit(p, p.split_from + j / p.rs_group, j % p.rs_group), cta);
+      } else if (MODE == MODE_REDUCE && p.rs_group > 1) {
+        // claim id = one tile's rank group; its first rank now, the others next
+        cur_claim = id;
+        w = decode_reduce<CL>(p, rs_group_unit(p, id, 0), cta);
+        w.rsub = 0;
+        w.rcnt = p.rs_group;
+        sub = 1;
       } else {
         w = decode_reduce<CL>(p, id, cta);
       }
@@ -1305,31 +1351,37 @@ __device__ void mma_issuer(const KParams& p, const Smem& s, const Ctl& c, uint32
   // free; their half-1 MMAs follow once it is.  Each half still accumulates
   // its k-slices in order, so the results are those of the plain order.
   constexpr bool SPLIT = G::ACC_BUFS == 1 && G::N_MMA == 2;
+  // GEMM-RS with rank groups (rs_group > 1): the group's ranks accumulate into
+  // one accumulator back to back; only the last one hands it to the epilogue
+  const bool grouped = MODE == MODE_REDUCE && p.rs_group > 1;
   ItemIter<MODE, CL> iter(p, total_mt, ps.vrank, &c);
   Work w;
   uint32_t stage = 0, phase = 0;
-  int it = 0;
+  int it = 0;    // accumulator hand-overs so far
+  int item = 0;  // trace record index
   bool any = false;
   bool ok = true;
   while (ok && iter.next(w)) {
     const uint32_t b = it % G::ACC_BUFS;
     const uint32_t use = static_cast<uint32_t>(it / G::ACC_BUFS);
     const uint32_t d = tmem_base + b * G::ACC_COLS;
+    const bool cont = grouped && w.rsub > 0;               // adds onto the group's sum
+    const bool last = !grouped || w.rsub + 1 >= w.rcnt;   // hands the sum over
     // 256-column halves of the tile that start below N (a half wholly past N
     // has nothing to compute; its accumulator columns are never stored)
     const int n_live = (G::N_MMA > 1 && w.n0 + BN >= w.n_end) ? 1 : G::N_MMA;
     int pre = 0;  // leading k-slices whose half-0 MMAs were issued early
-    if (SPLIT && p.acc_halves && use > 0 && n_live == 2) {
+    if (SPLIT && !cont && p.acc_halves && use > 0 && n_live == 2) {
       if ((PAIR == 2 ? wait_bar_remote(smem_u32(&s.thalf[b]), (use & 1u) ^ 1u, c, W_TEMPTY, b + 2)
                      : wait_bar(smem_u32(&s.thalf[b]), (use & 1u) ^ 1u, c, W_TEMPTY, b + 2)) != 0)
         break;
-      trace_now(p, it, TR_MMA_ACC);
+      trace_now(p, item, TR_MMA_ACC);
       tc_fence_after();
       pre = min(G::STAGES, w.k1 - w.k0);
       uint32_t st = stage, ph = phase;
       for (int j = 0; j < pre; ++j) {
         if (wait_bar(smem_u32(&s.full[st]), ph, c, W_FULL, st) != 0) { ok = false; break; }
-        if (j == 0) trace_now(p, it, TR_MMA_FIRST);
+        if (j == 0) trace_now(p, item, TR_MMA_FIRST);
         tc_fence_after();
         const uint32_t sa = smem_u32(s.a + st * A_STAGE);
         const uint32_t sb = smem_u32(s.b + st * G::B_STAGE);
@@ -1345,16 +1397,16 @@ __device__ void mma_issuer(const KParams& p, const Smem& s, const Ctl& c, uint32
       }
       if (!ok) break;
     }
-    if ((PAIR == 2 ? wait_bar_remote(smem_u32(&s.tempty[b]), (use & 1u) ^ 1u, c, W_TEMPTY, b)
-                   : wait_bar(smem_u32(&s.tempty[b]), (use & 1u) ^ 1u, c, W_TEMPTY, b)) != 0)
+    if (!cont && (PAIR == 2 ? wait_bar_remote(smem_u32(&s.tempty[b]), (use & 1u) ^ 1u, c, W_TEMPTY, b)
+                            : wait_bar(smem_u32(&s.tempty[b]), (use & 1u) ^ 1u, c, W_TEMPTY, b)) != 0)
       break;
-    if (pre == 0) trace_now(p, it, TR_MMA_ACC);
+    if (pre == 0) trace_now(p, item, TR_MMA_ACC);
     tc_fence_after();
     for (int k = w.k0; k < w.k1; ++k) {
       const bool early = k - w.k0 < pre;  // its stage is known full, its half 0 issued
       if (!early) {
         if (wait_bar(smem_u32(&s.full[stage]), phase, c, W_FULL, stage) != 0) { ok = false; break; }
-        if (k == w.k0) trace_now(p, it, TR_MMA_FIRST);
+        if (k == w.k0) trace_now(p, item, TR_MMA_FIRST);
         tc_fence_after();
       }
       const uint32_t sa = smem_u32(s.a + stage * A_STAGE);
@@ -1363,7 +1415,7 @@ __device__ void mma_issuer(const KParams& p, const Smem& s, const Ctl& c, uint32
       for (int kk = 0; kk < BK / UK; ++kk) {
         // A: K-major rows of 128 B, 8-row groups 1024 B apart; a 16-wide k step is +32 B.
         const uint64_t ad = sdesc_sw128(sa + kk * UK * 2, 16, 1024);
-        const uint32_t acc = (k > w.k0 || kk > 0) ? 1u : 0u;
+        const uint32_t acc = (cont || k > w.k0 || kk > 0) ? 1u : 0u;
 #pragma unroll
         for (int h = 0; h < G::N_MMA; ++h) {
           if (h >= n_live) break;
@@ -1383,9 +1435,11 @@ __device__ void mma_issuer(const KParams& p, const Smem& s, const Ctl& c, uint32
       if (++stage == G::STAGES) { stage = 0; phase ^= 1u; }
     }
     if (!ok) break;
+    trace_now(p, item, TR_MMA_END);
+    ++item;
+    if (!last) continue;
     if (PAIR == 2) umma2_commit_mc(smem_u32(&s.tfull[b]), pair_mask);
     else umma_commit(smem_u32(&s.tfull[b]));
-    trace_now(p, it, TR_MMA_END);
     ++it;
   }
   if (any) {
@@ -1516,7 +1570,13 @@ __device__ void epilogue(const KParams& p, const Smem& s, const Ctl& c, uint32_t
   // the first epilogue warp records the trace stamps
   const bool tracer = warp == KernelShape<MODE, DT, CL>::EPI_WARP0 && lane == 0;
   int nst = 0;  // tensor bulk stores this warp has committed
+  // GEMM-RS with rank groups: only a group's last item hands over the
+  // accumulator, holding the sum of the group's partials
+  const bool grouped = MODE == MODE_REDUCE && p.rs_group > 1;
+  int item = -1;  // trace record index
   while (iter.next(w)) {
+    ++item;
+    if (grouped && w.rsub + 1 < w.rcnt) continue;
     const uint32_t b = it % G::ACC_BUFS;
     const uint32_t use = static_cast<uint32_t>(it / G::ACC_BUFS);
     // one 512-column accumulator: once this warp's loads of its first 256
@@ -1541,7 +1601,7 @@ __device__ void epilogue(const KParams& p, const Smem& s, const Ctl& c, uint32_t
                                    : wait_bar(smem_u32(&s.tfull[b]), use & 1u, c, W_TFULL, b);
     wr = __shfl_sync(0xFFFFFFFFu, wr, 0);
     if (wr != 0) break;
-    if (tracer) trace_now(p, it, TR_EPI_FULL);
+    if (tracer) trace_now(p, item, TR_EPI_FULL);
     tc_fence_after();
     const int row0 = w.m0 + q * 32;       // first of this warp's 32 rows
     const int row = row0 + lane;           // row of the A row space held by this thread
@@ -1684,14 +1744,14 @@ __device__ void epilogue(const KParams& p, const Smem& s, const Ctl& c, uint32_t
       else mbar_arrive(smem_u32(&s.tempty[b]));
     }
     ++it;
-    if (tracer && MODE != MODE_REDUCE) trace_now(p, it - 1, TR_EPI_END);
+    if (tracer && MODE != MODE_REDUCE) trace_now(p, item, TR_EPI_END);
 
     if (MODE == MODE_REDUCE) {
       // arrival counter of this tile's 32-row quarter counts k-slices; quarters
       // wholly past the last row, and the parts of a region past the last
       // column (no tile of their own), have nothing to count
       if (row0 >= w.row_end || ncols <= 0) {
-        if (tracer) trace_now(p, it - 1, TR_EPI_END);
+        if (tracer) trace_now(p, item, TR_EPI_END);
         continue;
       }
       // the box reduces of this quarter have completed
@@ -1699,7 +1759,8 @@ __device__ void epilogue(const KParams& p, const Smem& s, const Ctl& c, uint32_t
       __syncwarp();
       __threadfence();
       __syncwarp();
-      const uint32_t nk = static_cast<uint32_t>(w.k1 - w.k0);
+      // (a rank group's sum counts the k-slices of all its ranks)
+      const uint32_t nk = static_cast<uint32_t>(w.k1 - w.k0) * static_cast<uint32_t>(grouped ? w.rcnt : 1);
       const uint32_t target = static_cast<uint32_t>(p.R) * static_cast<uint32_t>(p.KT);
       uint32_t* cnt = p.counters + (static_cast<size_t>(w.tile) * 4 + q);
       uint32_t old = 0;
@@ -1723,7 +1784,7 @@ __device__ void epilogue(const KParams& p, const Smem& s, const Ctl& c, uint32_t
         }
         if (lane == 0) atomicExch(cnt, 0u);
       }
-      if (tracer) trace_now(p, it - 1, TR_EPI_END);
+      if (tracer) trace_now(p, item, TR_EPI_END);
     }
   }
   if (nst > 0) {

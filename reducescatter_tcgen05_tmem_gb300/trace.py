@@ -56,7 +56,10 @@ def summary(rec: dict) -> dict | None:
         idle.append(t1 - me[-1])
         items.append(len(it))
         it_k.extend((me - mf).tolist())
-        it_e.extend((rec["epi_end"][b, it] - rec["epi_full"][b, it]).tolist())
+        # (items whose partial stays in TMEM for the next rank of its group
+        # have no epilogue of their own)
+        ef, ee = rec["epi_full"][b, it], rec["epi_end"][b, it]
+        it_e.extend((ee - ef)[ef > 0].tolist())
     med = lambda x: float(np.median(np.asarray(x, dtype=np.float64)))  # noqa: E731
     return {"span_us": round(span / 1e3, 1), "mma_ctas": int(np.sum(mma)), "units_per_cta": med(items),
             "kloop_share": round(med(kl) / span, 4), "acc_wait_share": round(med(wacc) / span, 4),

@@ -465,6 +465,42 @@ def test_gemm_rs_accumulator_halves_integer_inputs_bit_exact(rs_tile, N):
         assert torch.count_nonzero(ws).item() == 0
 
 
+@pytest.mark.parametrize("rs_group", [1, 2, 4, 8])
+@pytest.mark.parametrize("num_ctas", [0, 12])
+def test_gemm_rs_rank_groups_integer_inputs_bit_exact(rs_group, num_ctas):
+    # a region sums the partials of rs_group ranks of one tile in TMEM and adds
+    # the sum once; integer inputs make every sum exact in any order.  Two
+    # calls on one workspace: the schedule and the counters are left clean
+    c = configs.small(configs.CONFIGS["rs_mlp1"], R=8, M=1000, N=2056, K=8 * 1024, dist="int", seed=77)
+    As, Bs = configs.rs_inputs(c)
+    ref = oracle.gemm_rs(As, Bs, c.dtype)
+    opts = {"rs_group": rs_group}
+    if num_ctas:
+        opts["num_ctas"] = num_ctas
+    _, _, out, ws = _rs_case(c, opts=opts, calls=2)
+    _ok(ws)
+    for o in range(c.R):
+        assert np.array_equal(oracle.widen(from_device(out[o]), c.dtype), ref[o]), o
+    assert torch.count_nonzero(ws).item() == 0
+
+
+@pytest.mark.parametrize("R,M,N,K,dtype,rs_group", [
+    (8, 1024, 2048, 8192, "bf16", 2),
+    (4, 512, 1032, 4096, "f16", 4),    # ragged last n-unit (8 columns past 1024)
+    (16, 1024, 2048, 4096, "f16", 2),  # the most ranks a call takes
+    (6, 768, 1024, 3072, "bf16", 3),   # a group of 3 (6 ranks)
+    (6, 768, 1024, 3072, "bf16", 4),   # 4 does not divide 6: each rank added on its own
+])
+def test_gemm_rs_rank_groups_match_oracle(R, M, N, K, dtype, rs_group):
+    c = configs.small(configs.CONFIGS["rs_mlp1"], R=R, M=M, N=N, K=K, dtype=dtype, seed=90 + R)
+    As, Bs, out, ws = _rs_case(c, opts={"rs_group": rs_group})
+    _ok(ws)
+    ref = oracle.gemm_rs(As, Bs, dtype)
+    for o in range(R):
+        check_close(oracle.widen(from_device(out[o]), dtype), ref[o], f"rs group {rs_group} owner {o}")
+    assert torch.count_nonzero(ws).item() == 0
+
+
 @pytest.mark.parametrize("R,M,N,K,dtype,num_ctas", [
     (8, 1000, 2056, 1024, "f16", 16),   # ragged M and N tails, 125-row owner chunks
     (4, 512, 1032, 2048, "bf16", 16),   # ragged last n-unit (8 columns past 1024)

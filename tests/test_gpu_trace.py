@@ -26,13 +26,16 @@ def _ws(nbytes):
     return torch.zeros(max(nbytes, 256) // 4, dtype=torch.int32, device="cuda")
 
 
-def _check_records(t, units, per_unit):
-    """Every unit (claim) id in [0, units) recorded by exactly `per_unit` CTAs; the
-    stamps of every record in pipeline order, and per CTA in item order."""
+def _check_records(t, units, per_unit, drains=None):
+    """Every unit (claim) id in [0, units) recorded `per_unit` times (CTAs x the
+    claim's items; an array: per id); the stamps of every record in pipeline
+    order, and per CTA in item order.  `drains`: how many of all records hand
+    an accumulator to the epilogue (default: every one)."""
     tag_ok = t["unit"] >= 0
     ids, counts = np.unique(t["unit"][tag_ok], return_counts=True)
     assert np.array_equal(ids, np.arange(units)), "units missing from the trace"
     assert np.all(counts == per_unit), np.unique(counts)
+    n_drained = 0
     for b in range(t["grid"]):
         items = np.nonzero(tag_ok[b])[0]
         if items.size == 0:
@@ -42,12 +45,18 @@ def _check_records(t, units, per_unit):
         assert np.all(ps > 0) and np.all(pe >= ps), f"CTA {b}: producer stamps"
         assert np.all(np.diff(ps) >= 0), f"CTA {b}: items out of order"
         ef, ee = t["epi_full"][b, items], t["epi_end"][b, items]
-        assert np.all(ef > 0) and np.all(ee >= ef), f"CTA {b}: epilogue stamps"
-        assert np.all(ef >= ps), f"CTA {b}: accumulator full before its loads began"
+        d = ef > 0  # the items that handed their accumulator to the epilogue
+        n_drained += int(np.sum(d))
+        if drains is None:
+            assert np.all(d), f"CTA {b}: epilogue records"
+        assert np.all(ee[d] >= ef[d]), f"CTA {b}: epilogue stamps"
+        assert np.all(ef[d] >= ps[d]), f"CTA {b}: accumulator full before its loads began"
         ma, mf, me = t["mma_acc"][b, items], t["mma_first"][b, items], t["mma_end"][b, items]
         if np.any(me):  # the CTA that issues its pair's MMAs
             assert np.all(mf >= ma) and np.all(me >= mf), f"CTA {b}: MMA stamps"
-            assert np.all(ef >= me - 2000), f"CTA {b}: accumulator read before its commit"
+            assert np.all(ef[d] >= me[d] - 2000), f"CTA {b}: accumulator read before its commit"
+    if drains is not None:
+        assert n_drained == drains, (n_drained, drains)
 
 
 def test_ag_gemm_trace_covers_every_unit_in_order():
@@ -81,7 +90,8 @@ def test_gemm_rs_trace_covers_every_unit_in_order():
            for _ in range(c.R)]
     ws = _ws(fx.flux_workspace_size(fx.FLUX_OP_GEMM_RS, c.R, c.M, c.N, c.K))
     tr = torch.zeros(8 + 152 * 64 * 8, dtype=torch.int64, device="cuda")
-    fx.flux_gemm_rs(c.R, c.M, c.N, c.K, DT[c.dtype], A, B, out, ws, opts={"trace": tr, "rs_tile": 1})
+    fx.flux_gemm_rs(c.R, c.M, c.N, c.K, DT[c.dtype], A, B, out, ws,
+                    opts={"trace": tr, "rs_tile": 1, "rs_group": 1})
     st, rep = fx.flux_get_status(ws)
     assert st == fx.FLUX_OK, rep
     ref = oracle.gemm_rs(As, Bs, c.dtype)
@@ -117,6 +127,34 @@ def test_moe_layer0_dynamic_trace_covers_every_unit_once():
     m_units = int(sum((int(k) + 255) // 256 for k in want_counts))
     t = ftrace.records(tr)
     _check_records(t, units=m_units * ((Fr + 511) // 512) * c.R, per_unit=2)
+
+
+def test_gemm_rs_rank_group_trace_covers_every_claim():
+    # rank groups of 2: every claim (a tile's pair of ranks) is recorded by the
+    # 4 CTAs of its region, once per rank; the last claims (one per region)
+    # go out rank by rank, one record per CTA
+    c = configs.small(configs.CONFIGS["rs_mlp1"], R=8, M=1024, N=4096, K=2048, dtype="f16", seed=505)
+    As, Bs = configs.rs_inputs(c)
+    out = [torch.full((c.M // c.R, c.N), float("nan"), dtype=torch.float16, device="cuda")
+           for _ in range(c.R)]
+    ws = _ws(fx.flux_workspace_size(fx.FLUX_OP_GEMM_RS, c.R, c.M, c.N, c.K))
+    tr = torch.zeros(8 + 152 * 64 * 8, dtype=torch.int64, device="cuda")
+    fx.flux_gemm_rs(c.R, c.M, c.N, c.K, DT[c.dtype], [to_device(a, c.dtype) for a in As],
+                    [to_device(b, c.dtype) for b in Bs], out, ws,
+                    opts={"trace": tr, "rs_tile": 1, "rs_group": 2})
+    st, rep = fx.flux_get_status(ws)
+    assert st == fx.FLUX_OK, rep
+    ref = oracle.gemm_rs(As, Bs, c.dtype)
+    for o in (0, c.R - 1):
+        check_close(oracle.widen(from_device(out[o]), c.dtype), ref[o], f"traced grouped rs owner {o}")
+    t = ftrace.records(tr)
+    groups = c.R * (c.M // 512) * (c.N // 512) // 2
+    regions = t["grid"] // 4
+    split = max(groups - regions, 0)
+    claims = split + (groups - split) * 2
+    per = np.array([8] * split + [4] * (claims - split))
+    # drains: one per claim (a group's sum, or a single rank's partial) in each of the 4 CTAs
+    _check_records(t, units=claims, per_unit=per, drains=4 * claims)
 
 
 def test_trace_off_leaves_the_buffer_alone():
