@@ -184,6 +184,14 @@ extern "C" flux_status_t flux_tune_gemm_rs(int R, int M, int N, int K, flux_dtyp
           o.tiles_per_group = tg;
           cands.push_back(o);
         }
+    // regions of 4: how many ranks' partials of a tile are summed in TMEM
+    for (int rg : {1, 2, 8}) {
+      if (R % rg) continue;
+      flux_opts_t o = base_opts();
+      o.rs_tile = 1;
+      o.rs_group = rg;
+      cands.push_back(o);
+    }
   }
   return pick(FLUX_OP_GEMM_RS, {R, M, N, K, 0, 0, 0, 0}, dtype, cands,
               [&](const flux_opts_t* o) {
