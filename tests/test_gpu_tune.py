@@ -69,6 +69,9 @@ def test_tune_gemm_rs(R, M, N, K, dtype):
     assert fx.flux_tune_count() == 1
     if M == 128:
         assert best["num_ctas"] >= 0 and best["group_n"] == 0
+    elif best["rs_group"]:
+        # a rank-group candidate: regions of 4, the library's raster
+        assert best["rs_tile"] == 1 and best["rs_group"] in (1, 2, 8) and best["group_n"] == 0
     else:
         assert best["group_n"] in (4, 8, 16) and best["tiles_per_group"] in (0, 2)
     fx.flux_gemm_rs(R, M, N, K, DT[dtype], A, B, out, ws)
