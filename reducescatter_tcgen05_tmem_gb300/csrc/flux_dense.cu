@@ -564,9 +564,19 @@ flux_status_t gemm_rs_impl(int R, int M, int N, int K, flux_dtype_t dtype,
         p.split_from = groups > g ? groups - g : 0;
         p.num_claims = p.split_from + (groups - p.split_from) * G;
         p.mbox_cap = 2 * ((p.num_claims + g - 1) / g) + 2;
+        // a group of all R ranks sums the whole tile: stored straight into the
+        // owner's 16-bit rows when every 128-row CTA part lies in one owner
+        if (G == R && rows % BM == 0) {
+          bool ok = true;
+          for (int o = 0; o < R && ok; ++o)
+            ok = encode_2d(&p.tmOut[o], dtype, out[o], N, rows, static_cast<uint64_t>(N) * 2, 64, 32) ==
+                 FLUX_OK;
+          p.rs_direct = ok ? 1 : 0;
+        }
       }
       if (launch_dyn_dt<MODE_REDUCE, DENSE_CL>(dtype, p, dgrid, s) == FLUX_OK) return FLUX_OK;
       p.rs_group = 1;
+      p.rs_direct = 0;
       p.split_from = p.num_units;
       p.dyn = 0;  // launch form refused: the static schedule below
       p.mbox = nullptr;

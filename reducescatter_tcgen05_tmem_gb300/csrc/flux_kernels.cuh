@@ -332,6 +332,8 @@ struct KParams {
   int rs_tile_major;
   int rs_group;      // REDUCE, dynamic: ranks whose partials of one tile a region sums in
                      // TMEM before one drain (1 = each rank's partial drained on its own)
+  int rs_direct;     // REDUCE, rs_group == R: a group's sum is the tile's result and is
+                     // stored in the owner's 16-bit rows (tmOut[owner]) without fp32 rows
   int debug_probe;  // checked build: nonzero makes CTA 0 fail one check (CK_PROBE) on purpose
   int acc_halves;   // one 512-column accumulator: handed back in two 256-column halves
 };
@@ -1617,7 +1619,13 @@ __device__ void epilogue(const KParams& p, const Smem& s, const Ctl& c, uint32_t
       tok = slot / p.topk;
       gate = __ldg(p.topk_w + slot);
     }
-    if (MODE == MODE_STORE || MODE == MODE_MOE_GATHER || MODE == MODE_MOE_STAGED) {
+    // GEMM-RS whose group holds all R ranks: the sum is the tile's result and
+    // goes to the owner's 16-bit rows like an AllGather tile (no fp32 rows,
+    // no arrival count); the owner's rows hold whole 128-row CTA parts
+    const bool direct = MODE == MODE_REDUCE && p.rs_direct && grouped && w.rcnt == p.R;
+    const int orank = MODE == MODE_REDUCE ? w.m0 / max(p.rows_per_rank, 1) : w.r;  // output tensor
+    const int orow0 = MODE == MODE_REDUCE ? row0 - orank * p.rows_per_rank : row0;  // its row
+    if (MODE == MODE_STORE || MODE == MODE_MOE_GATHER || MODE == MODE_MOE_STAGED || direct) {
       // 64 columns at a time: two TMEM loads, one row-contiguous store pass
       for (int ch = 0; ch < G::TILE_N / 64; ++ch) {
         if (ch * 64 == BN) free_half();
@@ -1627,7 +1635,7 @@ __device__ void epilogue(const KParams& p, const Smem& s, const Ctl& c, uint32_t
         tmem_ld_32x32b_x32(taddr + ch * 64 + 32, u);
         if (row0 >= w.row_end) continue;  // none of this warp's rows is in the tile
         // (checked build: a box outside the rank's output is recorded and not written)
-        if (!check_ok(c, w.r >= 0 && w.r < p.R && row0 >= 0 && row0 < p.M, CK_OUT_ROW,
+        if (!check_ok(c, orank >= 0 && orank < p.R && row0 >= 0 && row0 < p.M, CK_OUT_ROW,
                       static_cast<uint32_t>(row0)) ||
             !check_ok(c, n0 + ch * 64 >= 0 && n0 + ch * 64 < p.ldo && ((n0 + ch * 64) & 7) == 0, CK_OUT_COL,
                       static_cast<uint32_t>(n0 + ch * 64)))
@@ -1656,7 +1664,7 @@ __device__ void epilogue(const KParams& p, const Smem& s, const Ctl& c, uint32_t
           fence_proxy_async_smem();
           __syncwarp();
           if (lane == 0) {
-            tma_store_2d(&p.tmOut[w.r], buf, n0 + ch * 64, row0);
+            tma_store_2d(&p.tmOut[orank], buf, n0 + ch * 64, orow0);
             bulk_commit();
           }
           ++nst;
@@ -1668,9 +1676,16 @@ __device__ void epilogue(const KParams& p, const Smem& s, const Ctl& c, uint32_t
             if (lane == 0) bulk_wait_read_all();
             __syncwarp();
           }
-          store_rows_chunk64<DT>(p.out[w.r], p.ldo, row0, w.row_end - row0, n0 + ch * 64,
+          store_rows_chunk64<DT>(p.out[orank], p.ldo, orow0, w.row_end - row0, n0 + ch * 64,
                                  ncols - ch * 64, sstg, lane, v, u);
         }
+      }
+      if (direct && nst > 0) {
+        // the fp32 path of the next item stages from its first box on: this
+        // item's stores must have read their staging boxes (their writes
+        // complete before the warp leaves, below)
+        if (lane == 0) bulk_wait_read_all();
+        __syncwarp();
       }
     } else {
       // fp32 adds: into this tile's own rows (REDUCE) or the rows' tokens,
@@ -1744,9 +1759,9 @@ __device__ void epilogue(const KParams& p, const Smem& s, const Ctl& c, uint32_t
       else mbar_arrive(smem_u32(&s.tempty[b]));
     }
     ++it;
-    if (tracer && MODE != MODE_REDUCE) trace_now(p, item, TR_EPI_END);
+    if (tracer && (MODE != MODE_REDUCE || direct)) trace_now(p, item, TR_EPI_END);
 
-    if (MODE == MODE_REDUCE) {
+    if (MODE == MODE_REDUCE && !direct) {
       // arrival counter of this tile's 32-row quarter counts k-slices; quarters
       // wholly past the last row, and the parts of a region past the last
       // column (no tile of their own), have nothing to count

@@ -465,13 +465,17 @@ def test_gemm_rs_accumulator_halves_integer_inputs_bit_exact(rs_tile, N):
         assert torch.count_nonzero(ws).item() == 0
 
 
+@pytest.mark.parametrize("M", [1000, 1024])
 @pytest.mark.parametrize("rs_group", [1, 2, 4, 8])
 @pytest.mark.parametrize("num_ctas", [0, 12])
-def test_gemm_rs_rank_groups_integer_inputs_bit_exact(rs_group, num_ctas):
+def test_gemm_rs_rank_groups_integer_inputs_bit_exact(rs_group, num_ctas, M):
     # a region sums the partials of rs_group ranks of one tile in TMEM and adds
-    # the sum once; integer inputs make every sum exact in any order.  Two
-    # calls on one workspace: the schedule and the counters are left clean
-    c = configs.small(configs.CONFIGS["rs_mlp1"], R=8, M=1000, N=2056, K=8 * 1024, dist="int", seed=77)
+    # the sum once; integer inputs make every sum exact in any order.  Groups
+    # of all 8 ranks with 128-row owner chunks (M = 1024) store their sums
+    # straight into the owners' 16-bit rows; the last groups, claimed rank by
+    # rank, still go through the fp32 rows.  Two calls on one workspace: the
+    # schedule and the counters are left clean
+    c = configs.small(configs.CONFIGS["rs_mlp1"], R=8, M=M, N=2056, K=8 * 1024, dist="int", seed=77)
     As, Bs = configs.rs_inputs(c)
     ref = oracle.gemm_rs(As, Bs, c.dtype)
     opts = {"rs_group": rs_group}
@@ -490,6 +494,8 @@ def test_gemm_rs_rank_groups_integer_inputs_bit_exact(rs_group, num_ctas):
     (16, 1024, 2048, 4096, "f16", 2),  # the most ranks a call takes
     (6, 768, 1024, 3072, "bf16", 3),   # a group of 3 (6 ranks)
     (6, 768, 1024, 3072, "bf16", 4),   # 4 does not divide 6: each rank added on its own
+    (8, 2048, 2056, 8192, "bf16", 8),  # all ranks in a group: sums stored as 16-bit, ragged N
+    (16, 2048, 1024, 4096, "f16", 16), # all 16 ranks, 128-row owner chunks
 ])
 def test_gemm_rs_rank_groups_match_oracle(R, M, N, K, dtype, rs_group):
     c = configs.small(configs.CONFIGS["rs_mlp1"], R=R, M=M, N=N, K=K, dtype=dtype, seed=90 + R)
