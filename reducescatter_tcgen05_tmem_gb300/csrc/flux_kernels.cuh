@@ -286,7 +286,7 @@ struct KParams {
   int deterministic;       // REDUCE: ranks add their partials in ascending order
   int num_units;           // dense modes: number of work units
   int Nt_tile;             // REDUCE: output tiles (TILE_N columns) per row block, for the counters
-  int num_claims;          // dynamic schedule: claim ids (units, the last ones as two halves)
+  int num_claims;          // dynamic schedule: claim ids (units; see split_from, rs_group)
   int split_from;          // dynamic schedule, store mode: units from here on are claimed as
                            // two 256-column halves (num_units: none); reduce mode with
                            // rank groups: group claims from here on are claimed rank by rank
