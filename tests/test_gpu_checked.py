@@ -56,10 +56,12 @@ for push in (0, 1):
     for r in range(c.R):
         check_close(oracle.widen(from_device(out[r]), "f16"), ref[r], f"checked ag rank {r}")
 
-# GEMM + ReduceScatter: whole units (three forms), stream-K, cluster form; plain GEMM split-K
+# GEMM + ReduceScatter: whole units (three forms; rank groups summed in TMEM, and groups of
+# all ranks stored as 16-bit), stream-K, cluster form; plain GEMM split-K
 for (R, M, N, K, dt, o) in [(8, 1088, 2056, 256, "f16", {}), (8, 1088, 2056, 256, "f16", {"rs_tile": 2}),
                             (8, 1088, 2056, 256, "f16", {"rs_tile": 3}), (2, 64, 1000, 4096, "bf16", {}),
-                            (8, 128, 2048, 4096, "bf16", {}), (4, 256, 512, 1024, "f16", {"deterministic_rs": 1})]:
+                            (8, 128, 2048, 4096, "bf16", {}), (4, 256, 512, 1024, "f16", {"deterministic_rs": 1}),
+                            (8, 1024, 2056, 4096, "bf16", {"rs_group": 8})]:
     c = configs.small(configs.CONFIGS["rs_mlp1"], R=R, M=M, N=N, K=K, dtype=dt, seed=702)
     As, Bs = configs.rs_inputs(c)
     out = [torch.full((M // R, N), float("nan"), dtype=torch_dtype(dt), device="cuda") for _ in range(R)]
@@ -140,7 +142,7 @@ def test_checked_build_runs_every_op_clean_and_reports_the_probe():
     assert r.returncode == 0, r.stdout[-3000:] + r.stderr[-3000:]
     line = [ln for ln in r.stdout.splitlines() if ln.startswith("RESULT ")][-1]
     res = json.loads(line[len("RESULT "):])
-    assert len(res["done"]) == 14, res["done"]  # 2 AG, 6 GEMM-RS, 1 plain GEMM, 4 MoE, 1 after the probe
+    assert len(res["done"]) == 15, res["done"]  # 2 AG, 7 GEMM-RS, 1 plain GEMM, 4 MoE, 1 after the probe
     assert res["probe"]["status"] == fx.FLUX_ERR_INVALID_ARG
     rep = res["probe"]["report"]
     assert rep["where"] == "check" and rep["arg0"] == 15 and rep["arg1"] == 1234, rep
