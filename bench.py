@@ -436,14 +436,48 @@ class Step:
         return sum(self.flops[o] for o in self.ops)
 
 
+def per_expert_gemms(torch, st, op):
+    """The MoE layer's GEMMs as plain per-expert cuBLAS calls (no gather, no
+    combine, no ReduceScatter): for every rank r and expert e with n_e rows
+    routed to it, [n_e x K] . W_r[e] into a slice of a grouped output -- R x E
+    matmuls, the unfused baseline of a grouped GEMM.  The routing counts are
+    the step's own.  None for other ops."""
+    if op not in ("moe_layer0", "moe_layer1"):
+        return None
+    moe = st.moe
+    counts = st.counts[:moe.E].cpu().tolist()
+    n = moe.T * moe.topk
+    if op == "moe_layer0":
+        A = torch.randn(n, moe.H, device=st.dev, dtype=torch.bfloat16)
+        Ws = st.mW1  # R x [E x H x F/R]
+        outs = [torch.empty(n, moe.F // moe.R, device=st.dev, dtype=torch.bfloat16) for _ in range(moe.R)]
+        As = [A] * moe.R
+    else:
+        As = st.mH   # R x [n x F/R] grouped rows
+        Ws = st.mW2  # R x [E x F/R x H]
+        outs = [torch.empty(n, moe.H, device=st.dev, dtype=torch.bfloat16) for _ in range(moe.R)]
+    offs = [0]
+    for c in counts:
+        offs.append(offs[-1] + int(c))
+
+    def run():
+        for r in range(moe.R):
+            for e in range(moe.E):
+                lo, hi = offs[e], offs[e + 1]
+                if hi > lo:
+                    torch.matmul(As[r][lo:hi], Ws[r][e], out=outs[r][lo:hi])
+    return run
+
+
 def compare_plain(torch, fx, st, op, M, N, K, dtype, iters, clocks):
     """The fused op against a plain unsplit GEMM of the same shape, C[M x N] =
-    A[M x K] B[K x N] by cuBLAS and by this library's own tcgen05 GEMM,
-    measured in the same conditions: one region of `iters` rounds, each round
-    launching the fused op, then cuBLAS, then the own GEMM back to back, so
-    that all three see the same clocks and power limit.  Returns the median
-    CUDA-event time of each (after the first round), the region's median SM
-    clock, and time x clock (cycles) for each."""
+    A[M x K] B[K x N] by cuBLAS and by this library's own tcgen05 GEMM (and,
+    for the MoE layers, against their per-expert cuBLAS GEMMs), measured in
+    the same conditions: one region of `iters` rounds, each round launching
+    the fused op, then the plain GEMMs back to back, so that all see the same
+    clocks and power limit.  Returns the median CUDA-event time of each
+    (after the first round), the region's median SM clock, and time x clock
+    (cycles) for each."""
     dev = st.dev
     td = torch.float16 if dtype == "f16" else torch.bfloat16
     A = torch.randn(M, K, device=dev, dtype=td)
@@ -453,9 +487,12 @@ def compare_plain(torch, fx, st, op, M, N, K, dtype, iters, clocks):
     ws = torch.zeros(fx.flux_workspace_size(fx.FLUX_OP_GEMM, 1, M, N, K) // 4, dtype=torch.int32,
                      device=dev)
     code = fx.FLUX_F16 if dtype == "f16" else fx.FLUX_BF16
-    fns = (("fused", lambda: st.run_op(op)),
+    fns = [("fused", lambda: st.run_op(op)),
            ("cublas", lambda: torch.matmul(A, B, out=C)),
-           ("own", lambda: fx.flux_gemm(M, N, K, code, A, B, C, ws)))
+           ("own", lambda: fx.flux_gemm(M, N, K, code, A, B, C, ws))]
+    pe = per_expert_gemms(torch, st, op)
+    if pe is not None:
+        fns.append(("per_expert", pe))
     for _ in range(2):
         for _, fn in fns:
             fn()
@@ -477,7 +514,7 @@ def compare_plain(torch, fx, st, op, M, N, K, dtype, iters, clocks):
     if st_ws[0] != fx.FLUX_OK:
         raise RuntimeError(f"plain GEMM device status {st_ws}")
     med = {k: statistics.median(a.elapsed_time(b) for a, b in evs[k][1:]) for k, _ in fns}
-    del A, B, C, ws
+    del A, B, C, ws, fns, pe
     torch.cuda.empty_cache()
     clk = clocks.summary(w0, w1)
     mhz = clk.get("sm_mhz")
@@ -488,6 +525,9 @@ def compare_plain(torch, fx, st, op, M, N, K, dtype, iters, clocks):
            "overhead_frac": round(med["fused"] / best - 1.0, 4),
            "plain_shape": f"{M}x{N}x{K} {dtype}", "rounds": n,
            "region_s": round(w1 - w0, 3), "sm_mhz": mhz, "reasons": clk.get("reasons")}
+    if "per_expert" in med:
+        out["plain_per_expert_us"] = round(med["per_expert"] * 1e3, 1)
+        out["vs_per_expert_frac"] = round(med["fused"] / med["per_expert"] - 1.0, 4)
     if mhz:
         out["mcycles"] = {k: round(med[k] * 1e-3 * mhz, 3) for k in med}  # ms x MHz = 1e3 x Mcycles / 1e3
     return out
