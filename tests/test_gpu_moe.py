@@ -144,6 +144,7 @@ def _layer0(c, d=None, flags=None, opts=None):
     (1, 64, 64, 256, 3, 1, "f16", ()),
     (2, 200, 136, 256, 5, 3, "bf16", ()),      # H = 136: a 16-byte row tail in the staging copy
     (16, 1024, 256, 4096, 8, 2, "bf16", ()),   # the most ranks a call takes: 64 tokens per shard
+    (4, 1000, 256, 2048, 64, 2, "f16", (3, 9, 40)),  # 64 experts, most with a partial last unit
 ])
 def test_layer0_matches_oracle(R, T, H, F, E, topk, dtype, empty, pull):
     # staged: every CTA first copies a share of the grouped rows, then CTA pairs
@@ -284,6 +285,7 @@ def _layer1(c, d, h_dev=None, routing=None, opts=None):
     (4, 512, 256, 768, 8, 2, "f16", True),     # F/R = 192: ragged k tail
     (8, 1024, 512, 2048, 8, 2, "bf16", True),
     (1, 96, 256, 128, 2, 2, "f16", False),
+    (4, 1000, 256, 2048, 64, 2, "f16", False),  # 64 experts, most with a partial last tile
     # from 48 k-slices on: 256 x 512 tiles (H = 640: the last tile's second half
     # is past N; F/R = 3104: a 32-deep last k-slice)
     (2, 256, 640, 6208, 4, 2, "bf16", False),
