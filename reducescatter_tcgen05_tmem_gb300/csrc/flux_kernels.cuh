@@ -794,7 +794,11 @@ struct ItemIter {
   // dense tiles in regions of two or four pairs; the staged MoE layer0 in
   // regions of one pair (its unit count comes from the device tile table)
   static constexpr bool DYN_OK =
-      (Unit<MODE, CL>::DENSE && (CL == 4 || CL == 8)) || (MODE == MODE_MOE_STAGED && CL == 2);
+      (Unit<MODE, CL>::DENSE && (CL == 4 || CL == 8)) ||
+      ((MODE == MODE_MOE_STAGED || MODE == MODE_MOE_SCATTER_WIDE) && CL == 2);
+  // rank groups summed in TMEM (rs_group > 1): GEMM-RS, and MoE layer1 on
+  // 256 x 512 tiles with the ranks innermost in the unit order (moe_order 1)
+  static constexpr bool GROUPS = MODE == MODE_REDUCE || MODE == MODE_MOE_SCATTER_WIDE;
   const KParams& p;
   const Ctl* ctl;
   int total_mt;      // MoE: device-computed number of m-tiles
@@ -804,8 +808,9 @@ struct ItemIter {
   bool dyn, warp_uniform;
   uint32_t* box;     // dynamic: the region's mailbox
   int taken;         // dynamic: mailbox entries read so far
-  int sub;           // MOE_SCATTER_RED / tile-major GEMM-RS: next rank of the current tile
-  int cur_claim;     // tile-major GEMM-RS: the tile this region claimed last
+  int sub;           // MOE_SCATTER_RED / tile-major GEMM-RS / rank groups: next rank of the tile
+  int cur_claim;     // tile-major GEMM-RS / rank groups: the claim this region took last
+  int msplit;        // MoE layer1 rank groups: group claims from here on go out rank by rank
 
   __device__ ItemIter(const KParams& p_, int total_mt_, int cta_, const Ctl* ctl_ = nullptr,
                       bool warp_uniform_ = false)
@@ -822,6 +827,12 @@ struct ItemIter {
     cur_claim = 0;
     u = blockIdx.x / CL;
     stride = gridDim.x / CL;
+    msplit = 0;
+    if (MODE == MODE_MOE_SCATTER_WIDE && p.rs_group > 1) {
+      // the last split_from group claims (a count, 0 = none) go out rank by rank
+      const int groups = num_units / p.rs_group;
+      msplit = groups > p.split_from ? groups - p.split_from : 0;
+    }
     dyn = DYN_OK && p.dyn != 0 && ctl != nullptr;
     box = dyn ? p.mbox + static_cast<size_t>(u) * p.mbox_cap : nullptr;
     taken = 0;
@@ -833,7 +844,11 @@ struct ItemIter {
   }
 
   // dynamic schedule: how many claim ids the counter hands out
-  __device__ int claims() const { return is_moe(MODE) ? num_units : p.num_claims; }
+  __device__ int claims() const {
+    if (MODE == MODE_MOE_SCATTER_WIDE && p.rs_group > 1)
+      return msplit + (num_units / p.rs_group - msplit) * p.rs_group;
+    return is_moe(MODE) ? num_units : p.num_claims;
+  }
 
   __device__ bool next(Work& w) {
     if (MODE == MODE_RS_CLUSTER) {
@@ -858,12 +873,15 @@ struct ItemIter {
       return true;
     }
     if (DYN_OK && dyn) {
-      if (MODE == MODE_REDUCE && sub > 0) {
+      if (GROUPS && sub > 0) {
         // the next rank of the tile this region claimed (tile-major: all R
         // ranks; rank groups: the group's G)
         const int cnt = p.rs_tile_major ? p.R : p.rs_group;
-        w = decode_reduce<CL>(p, p.rs_tile_major ? cur_claim * p.R + sub : rs_group_unit(p, cur_claim, sub),
-                              cta);
+        if (MODE == MODE_REDUCE)
+          w = decode_reduce<CL>(p, p.rs_tile_major ? cur_claim * p.R + sub : rs_group_unit(p, cur_claim, sub),
+                                cta);
+        else
+          w = decode_moe<CL>(p, cur_claim * cnt + sub, total_mt, cta, Unit<MODE, CL>::G::TILE_N);
         w.rsub = sub;
         w.rcnt = cnt;
         w.uid = cur_claim;
@@ -888,6 +906,19 @@ struct ItemIter {
           w = decode_store<CL>(p, p.split_from + ((id - p.split_from) >> 1), cta);
           w.n0 += half * BN;
           w.n_end = min(w.n_end, w.n0 + BN);
+        }
+      } else if (MODE == MODE_MOE_SCATTER_WIDE && p.rs_group > 1) {
+        // rank innermost: the group of claim c is units c G .. c G + G - 1
+        const int G = p.rs_group;
+        if (id >= msplit) {
+          const int j = id - msplit;
+          w = decode_moe<CL>(p, (msplit + j / G) * G + j % G, total_mt, cta, Unit<MODE, CL>::G::TILE_N);
+        } else {
+          cur_claim = id;
+          w = decode_moe<CL>(p, id * G, total_mt, cta, Unit<MODE, CL>::G::TILE_N);
+          w.rsub = 0;
+          w.rcnt = G;
+          sub = 1;
         }
       } else if (is_moe(MODE)) {
         w = decode_moe<CL>(p, id, total_mt, cta, Unit<MODE, CL>::G::TILE_N);
@@ -1355,7 +1386,7 @@ __device__ void mma_issuer(const KParams& p, const Smem& s, const Ctl& c, uint32
   constexpr bool SPLIT = G::ACC_BUFS == 1 && G::N_MMA == 2;
   // GEMM-RS with rank groups (rs_group > 1): the group's ranks accumulate into
   // one accumulator back to back; only the last one hands it to the epilogue
-  const bool grouped = MODE == MODE_REDUCE && p.rs_group > 1;
+  const bool grouped = ItemIter<MODE, CL>::GROUPS && p.rs_group > 1;
   ItemIter<MODE, CL> iter(p, total_mt, ps.vrank, &c);
   Work w;
   uint32_t stage = 0, phase = 0;
@@ -1574,7 +1605,7 @@ __device__ void epilogue(const KParams& p, const Smem& s, const Ctl& c, uint32_t
   int nst = 0;  // tensor bulk stores this warp has committed
   // GEMM-RS with rank groups: only a group's last item hands over the
   // accumulator, holding the sum of the group's partials
-  const bool grouped = MODE == MODE_REDUCE && p.rs_group > 1;
+  const bool grouped = ItemIter<MODE, CL>::GROUPS && p.rs_group > 1;
   int item = -1;  // trace record index
   while (iter.next(w)) {
     ++item;

@@ -31,6 +31,7 @@ constexpr int ROUTE_THREADS = 1024;
 //   layer0 staged (the default): every CTA first copies a share of the
 //     grouped rows into the workspace, then CTA pairs with 256 x 512 tiles
 //     load them by TMA (see MODE_MOE_STAGED; 256 x 256 measured 11 % slower).
+constexpr int MOE1_SPLIT_TAIL = 0;  // layer1 rank groups: split the last groups rank by rank
 constexpr int MOE0_CL = 1;
 constexpr int MOE0S_CL = 2;
 constexpr int MOE1_CL = 2;
@@ -311,7 +312,8 @@ size_t a256(size_t v) { return round_up(v, WS_ALIGN); }
 // MOE_LAYERS), so that the one-call layer finds each part where the single
 // calls put it
 struct MoeWs {
-  size_t tile_off, counts, offsets, s2r, r2s, acc, unit_cnt, stage, mbox, mbox_bytes, total;
+  size_t tile_off, counts, offsets, s2r, r2s, acc, unit_cnt, stage, mbox, mbox_bytes, mbox1, mbox1_bytes,
+      total;
 };
 
 // Dynamic schedule of the staged layer0: at most this many regions (CTA pairs).
@@ -344,6 +346,15 @@ MoeWs moe_layout(flux_op_t op, int R, int T, int H, int F, int E, int topk) {
     o += a256(n * sizeof(int32_t));
     w.acc = o;
     o += a256(static_cast<size_t>(T) * H * sizeof(float));
+    // mailboxes of layer1's dynamic schedule (rank groups on 256 x 512 tiles):
+    // at most 2 U + 4 MOE0_MAX_REGIONS entries for U = (ceil(T*topk / 256) + E)
+    // ceil(H / 512) R units (every rank of an expert's group computes all H
+    // columns of its partial) over any EP x TP split
+    const long long u1 = (static_cast<long long>((n + BM * MOE0S_CL - 1) / (BM * MOE0S_CL)) + E) *
+                         ((H + 2 * BN - 1) / (2 * BN)) * R;
+    w.mbox1 = o;
+    w.mbox1_bytes = a256(static_cast<size_t>(2 * u1 + 4 * MOE0_MAX_REGIONS) * sizeof(uint32_t));
+    o += w.mbox1_bytes;
   }
   if (op == FLUX_OP_MOE_AG || op == FLUX_OP_MOE_LAYERS) {
     // staged layer0: one ready counter per m-unit of BM * MOE0S_CL rows, and
@@ -648,10 +659,18 @@ flux_status_t moe_layer1_impl(
   // experts, top-2, R 8 the rank-innermost unit order re-reads each m-tile's H
   // rows from DRAM once per wave (3.0 GB against 1.9 GB per launch) and the
   // layer runs 0.76-0.81 ms against 0.73-0.75 ms with one add per rank.
-  const int rg = (opts && opts->moe_l1_ranks > 0) ? opts->moe_l1_ranks : 1;
-  const bool red = !wide && tp > 1 && rg > 1 && tp % rg == 0;
+  // rank groups (moe_l1_ranks; default all tp ranks of the expert group): a
+  // CTA pair computes the partials of rg ranks of one 256 x 512 tile back to
+  // back into one TMEM accumulator (rank-innermost claims on the dynamic
+  // schedule) and makes one gate-weighted add per slot for the group.  At
+  // T 4096, H 4096, F 14336, 8 experts, top-2, 8 ranks: 654 against 697 us
+  // with one 256 x 256 tile and one add per rank (groups of 4: 716 us, the
+  // last wave of 4-rank claims idles 13 % of the call)
+  const int rg = (opts && opts->moe_l1_ranks > 0) ? opts->moe_l1_ranks : tp;
   if (opts && opts->moe_l1_ranks > 0 && tp % opts->moe_l1_ranks) return FLUX_ERR_INVALID_ARG;
-  const int tile_n = wide ? 2 * BN : BN;
+  const bool grouped = tp > 1 && rg > 1;
+  const bool red = false;
+  const int tile_n = (wide || grouped) ? 2 * BN : BN;
   p.Nt = (H + tile_n - 1) / tile_n;
   p.ldo = H;
   p.rows_per_rank = rows;
@@ -676,6 +695,23 @@ flux_status_t moe_layer1_impl(
   const long long max_units =
       (static_cast<long long>((n + BM * MOE1_CL - 1) / (BM * MOE1_CL)) + E) * p.Nt *
       static_cast<long long>(tp);
+  if (grouped) {
+    const int grid = grid_dt<MODE_MOE_SCATTER_WIDE, MOE1_CL>(dtype, dev, opts, max_units);
+    if (grid == 0) return FLUX_ERR_CUDA;
+    const long long g = grid / MOE1_CL;
+    const long long cap = 2 * ((max_units + g - 1) / g) + 2;
+    // (the area holds 2 U + 4 MOE0_MAX_REGIONS entries, U >= max_units)
+    if (g > MOE0_MAX_REGIONS || static_cast<size_t>(g * cap) * sizeof(uint32_t) > L.mbox1_bytes)
+      return FLUX_ERR_WORKSPACE;
+    p.moe_order = 1;
+    p.rs_group = rg;
+    p.split_from = MOE1_SPLIT_TAIL ? static_cast<int>(g) : 0;  // group claims split rank by rank
+    p.dyn = 1;
+    p.mbox = reinterpret_cast<uint32_t*>(ws + L.mbox1);
+    p.mbox_cap = static_cast<int>(cap);
+    p.claim_reserve = 0;
+    return launch_dt<MODE_MOE_SCATTER_WIDE, MOE1_CL>(dtype, p, grid, s);
+  }
   if (wide) {
     const int grid = grid_dt<MODE_MOE_SCATTER_WIDE, MOE1_CL>(dtype, dev, opts, max_units);
     if (grid == 0) return FLUX_ERR_CUDA;
