@@ -125,14 +125,15 @@ typedef struct {
                                1, but a region claims one output tile and computes all
                                R ranks' partials of it back to back (the tile's fp32
                                rows stay in L2 between the partials) */
-  int32_t moe_l1_ranks;     /* MoE layer1 with tp > 1 ranks per expert group (fewer than
-                               48 k-slices per rank): how many ranks' partials of one
-                               256 x 256 tile a CTA pair computes back to back and sums
-                               in fp32 on chip before its gate-weighted adds into the
-                               token rows (a divisor of tp; tp = all ranks of the
-                               group, one add per slot).  0 or 1 = none: every rank's
-                               partial is added into the token rows on its own (the
-                               default, faster at the measured sizes) */
+  int32_t moe_l1_ranks;     /* MoE layer1 with tp > 1 ranks per expert group: how many
+                               ranks' partials of one 256 x 512 tile a CTA pair computes
+                               back to back into one TMEM accumulator before its
+                               gate-weighted adds into the token rows (a divisor of tp;
+                               the units are claimed at run time from a counter in the
+                               workspace).  0 = tp (all ranks of the group: one add per
+                               slot; the default); 1 = none: every rank's partial is
+                               added on its own, from 256 x 256 tiles with two
+                               accumulators (256 x 512 from 48 k-slices per rank on) */
   void* trace;              /* optional per-unit trace (device memory, NULL = off): every
                                CTA of the fused kernel records, per work item, eight
                                64-bit words -- a tag (unit id + 1 in bits 0..31, rank

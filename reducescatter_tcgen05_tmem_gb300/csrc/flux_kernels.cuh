@@ -140,8 +140,6 @@ static_assert(32 * STG_PITCH <= STG_WARP, "row staging fits");
 //   <1,1> 128 x 256, B 256 columns per CTA, 4 stages of 48 KB, 2 accumulators
 //   <2,1> 256 x 256, B 128 columns per CTA, 6 stages of 32 KB, 2 accumulators
 //   <2,2> 256 x 512, B 256 columns per CTA, 4 stages of 48 KB, 1 accumulator
-//   <2,1,8> 256 x 256 with eight epilogue warps (MoE layer1 reducing the rank
-//           partials in registers): 5 stages of 32 KB
 template <int PAIR, int NM, int EW = EPI_WARPS>
 struct Geo {
   static constexpr int TILE_M = BM * PAIR;             // rows of one tile
@@ -158,8 +156,7 @@ struct Geo {
   static_assert(ACC_BUFS * ACC_COLS == TMEM_COLS, "TMEM budget");
 };
 constexpr int cmax(int a, int b) { return a > b ? a : b; }
-constexpr int SMEM_BYTES = cmax(cmax(Geo<1, 1>::SMEM, Geo<2, 1, 8>::SMEM),
-                                cmax(Geo<2, 1>::SMEM, Geo<2, 2>::SMEM));
+constexpr int SMEM_BYTES = cmax(Geo<1, 1>::SMEM, cmax(Geo<2, 1>::SMEM, Geo<2, 2>::SMEM));
 
 // First output column of B box j (0..3) of CTA `cta` in a tile starting at
 // column n0.  A single CTA holds columns n0 .. n0+255 in order; a pair splits
@@ -197,23 +194,14 @@ enum Mode {
   MODE_MOE_STAGED = 4,
   MODE_RS_CLUSTER = 5,
   // MOE_SCATTER on 256 x 512 pair tiles with one accumulator: for long
-  // reductions, where the accumulator's fp32 drain is short against the
-  // tile's main loop and the wider tile receives fewer bytes per MMA
-  MODE_MOE_SCATTER_WIDE = 6,
-  // MOE_SCATTER whose CTA pair computes the partials of several ranks for one
-  // 256 x 256 tile back to back (alternating accumulators) and reduces them in
-  // the epilogue warps' registers, so that each token row receives one
-  // gate-weighted add per (slot, rank group) instead of one per rank
-  MODE_MOE_SCATTER_RED = 7
+  // reductions (the accumulator's fp32 drain is short against the tile's main
+  // loop and the wider tile receives fewer bytes per MMA), and for rank
+  // groups whose partials are summed in TMEM before the adds (rs_group)
+  MODE_MOE_SCATTER_WIDE = 6
 };
 // MoE layer1 (gate-weighted adds into the token rows), any tile form
 __host__ __device__ constexpr bool is_scatter(int mode) {
-  return mode == MODE_MOE_SCATTER || mode == MODE_MOE_SCATTER_WIDE || mode == MODE_MOE_SCATTER_RED;
-}
-// epilogue warps of a mode: eight where a tile's rank partials are summed in
-// registers (a thread holds 128 fp32 columns of its row), else four
-__host__ __device__ constexpr int epi_warps(int mode) {
-  return mode == MODE_MOE_SCATTER_RED ? 8 : EPI_WARPS;
+  return mode == MODE_MOE_SCATTER || mode == MODE_MOE_SCATTER_WIDE;
 }
 __host__ __device__ constexpr bool is_moe(int mode) {
   return mode == MODE_MOE_GATHER || is_scatter(mode) || mode == MODE_MOE_STAGED;
@@ -315,7 +303,6 @@ struct KParams {
   int moe_tp;  // MoE: ranks per expert group (R: tensor parallel, 1: expert parallel)
   int moe_el;  // MoE: experts per group; rank g moe_tp + t holds block t of group g's experts
   int moe_order;  // MoE: unit order (see decode_moe)
-  int moe_rgroup; // MOE_SCATTER_RED: ranks of a group whose partials of one tile are reduced on chip
   // per-unit trace (nullptr = off): trace_words 64-bit words, TR_FIELDS per record
   unsigned long long* trace;
   long long trace_words;
@@ -509,10 +496,9 @@ struct Work {
   int e;       // expert (MoE)
   int k0, k1;  // k-slice range of this item
   int tile;    // linear 128-row output-tile id of this CTA's part (REDUCE counters)
-  int rsub;    // MOE_SCATTER_RED, grouped REDUCE: place of this rank's partial in the
+  int rsub;    // rank groups / tile-major GEMM-RS: place of this rank's partial in the
                // tile's rank group
-  int rcnt;    // MOE_SCATTER_RED, grouped REDUCE: partials of the tile reduced on chip
-               // (the group's size)
+  int rcnt;    // rank groups / tile-major GEMM-RS: the group's size
   int uid;     // the unit (or claim) id the item came from (traces)
 };
 
@@ -574,7 +560,7 @@ struct Unit {
   static constexpr int NM =
       (MODE == MODE_REDUCE && CL == 8) ? 1
       : ((DENSE || MODE == MODE_MOE_STAGED || MODE == MODE_MOE_SCATTER_WIDE) && PAIR == 2) ? 2 : 1;
-  static constexpr int EW = epi_warps(MODE);
+  static constexpr int EW = EPI_WARPS;
   // pairs side by side along N (share A by multicast) and stacked along M
   // (share B by multicast)
   static constexpr int PN = (DENSE && CL == 8) ? 2 : 1;
@@ -586,7 +572,6 @@ struct Unit {
   static_assert(DENSE || MC == 1, "MoE tiles: no B sharing between pairs");
   static_assert(MODE != MODE_MOE_GATHER || CL == 1, "MoE layer0 gather: single CTAs");
   static_assert(MODE != MODE_MOE_STAGED || CL == 2, "MoE layer0 staged: CTA pairs");
-  static_assert(MODE != MODE_MOE_SCATTER_RED || CL == 2, "MoE layer1 rank reduction: CTA pairs");
 };
 
 template <int MODE, int DT, int CL>
@@ -596,7 +581,7 @@ struct KernelShape {
   static constexpr int PRODUCER_WARPS = CPASYNC_GATHER ? 4 : 1;
   static constexpr int MMA_WARP = PRODUCER_WARPS;
   static constexpr int EPI_WARP0 = PRODUCER_WARPS + 1;
-  static constexpr int EPI = epi_warps(MODE);
+  static constexpr int EPI = EPI_WARPS;
   static constexpr int THREADS = 32 * (PRODUCER_WARPS + 1 + EPI);
   static constexpr int FULL_COUNT = CPASYNC_GATHER ? (BM + 1) : 1;
 };
@@ -808,17 +793,14 @@ struct ItemIter {
   bool dyn, warp_uniform;
   uint32_t* box;     // dynamic: the region's mailbox
   int taken;         // dynamic: mailbox entries read so far
-  int sub;           // MOE_SCATTER_RED / tile-major GEMM-RS / rank groups: next rank of the tile
+  int sub;           // tile-major GEMM-RS / rank groups: next rank of the tile
   int cur_claim;     // tile-major GEMM-RS / rank groups: the claim this region took last
   int msplit;        // MoE layer1 rank groups: group claims from here on go out rank by rank
 
   __device__ ItemIter(const KParams& p_, int total_mt_, int cta_, const Ctl* ctl_ = nullptr,
                       bool warp_uniform_ = false)
       : p(p_), ctl(ctl_), total_mt(total_mt_), cta(cta_), warp_uniform(warp_uniform_) {
-    if (MODE == MODE_MOE_SCATTER_RED) {
-      // a unit is one tile of one rank group: moe_rgroup consecutive items
-      num_units = total_mt * p.Nt * (p.moe_tp / p.moe_rgroup);
-    } else if (is_moe(MODE)) {
+    if (is_moe(MODE)) {
       num_units = total_mt * p.Nt * p.moe_tp;
     } else {
       num_units = p.num_units;
@@ -958,21 +940,6 @@ struct ItemIter {
       w.k1 = static_cast<int>(k1);
       w.uid = unit;
       pos += k1 - k0;
-      return true;
-    }
-    if (MODE == MODE_MOE_SCATTER_RED) {
-      // the group's ranks of one tile back to back on this CTA pair (rank
-      // innermost order: item u * g + sub is rank (u * g + sub) % moe_tp)
-      if (u >= num_units) return false;
-      const int g = p.moe_rgroup;
-      w = decode_moe<CL>(p, u * g + sub, total_mt, cta, Unit<MODE, CL>::G::TILE_N);
-      w.rsub = sub;
-      w.rcnt = g;
-      w.uid = u * g + sub;
-      if (++sub == g) {
-        sub = 0;
-        u += stride;
-      }
       return true;
     }
     if (u >= num_units) return false;
@@ -1839,100 +1806,6 @@ __device__ void epilogue(const KParams& p, const Smem& s, const Ctl& c, uint32_t
   }
 }
 
-// MoE layer1 with the rank partials of each tile reduced on chip
-// (MOE_SCATTER_RED, CTA pairs, eight epilogue warps).  The pair computes the
-// partials of a rank group's ranks for one 256 x 256 tile back to back, in
-// alternating accumulators.  Epilogue warp ew (0..7) reads TMEM lane quarter
-// ew % 4 and the 128-column half ew / 4 of each accumulator; every thread keeps
-// its row's 128 columns in registers, taking the group's first partial and
-// adding the others in fp32 in rank order.  An accumulator goes back to the
-// MMA warp as soon as it is read, so the next partial's MMAs do not wait for
-// any global traffic.  After the group's last partial each row, times its
-// slot's gate, is added into its token's fp32 row (row-contiguous
-// red.global.add.v4.f32 through the warp's staging rows): one add per slot
-// and rank group instead of one per rank.
-template <int CL>
-__device__ void epilogue_scatter_red(const KParams& p, const Smem& s, const Ctl& c, uint32_t tmem_base,
-                                     int total_mt, int warp, int ew, const Pos& ps) {
-  using U = Unit<MODE_MOE_SCATTER_RED, CL>;
-  using G = typename U::G;
-  constexpr int PAIR = U::PAIR;
-  constexpr int HALF = G::TILE_N / 2;  // columns per thread
-  constexpr int CH = HALF / 32;        // 32-column TMEM loads per accumulator
-  const int cta = ps.vrank & (PAIR - 1);
-  const int lane = threadIdx.x & 31;
-  const int q = warp & 3;  // TMEM lane quarter this warp may access
-  const int hh = ew >> 2;  // column half of the tile
-  ItemIter<MODE_MOE_SCATTER_RED, CL> iter(p, total_mt, ps.vrank, &c, true);
-  const uint32_t tempty0 = (PAIR == 2 && cta != 0)
-                               ? mapa_shared(smem_u32(&s.tempty[0]), static_cast<uint32_t>(ps.hw_rank & ~1))
-                               : smem_u32(&s.tempty[0]);
-  const uint32_t sstg = smem_u32(s.stg + ew * STG_WARP);
-  float acc[CH][32];
-  Work w;
-  int it = 0;
-  while (iter.next(w)) {
-    const uint32_t b = it % G::ACC_BUFS;
-    const uint32_t use = static_cast<uint32_t>(it / G::ACC_BUFS);
-    int wr = 0;
-    if (lane == 0) {
-      // a few blocking probes first: the bounded slow wait is a call, which
-      // would have to save the 128 running sums around it
-      const uint32_t bar = smem_u32(&s.tfull[b]);
-      bool done = false;
-      for (int k = 0; k < 64 && !done; ++k) done = mbar_try_wait(bar, use & 1u);
-      if (!done)
-        wr = (PAIR == 2 && cta != 0) ? wait_bar_remote(bar, use & 1u, c, W_TFULL, b)
-                                     : wait_bar(bar, use & 1u, c, W_TFULL, b);
-    }
-    wr = __shfl_sync(0xFFFFFFFFu, wr, 0);
-    if (wr != 0) break;
-    if (ew == 0 && lane == 0) trace_now(p, it, TR_EPI_FULL);
-    tc_fence_after();
-    const uint32_t taddr =
-        tmem_base + (static_cast<uint32_t>(q * 32) << 16) + b * G::ACC_COLS + hh * HALF;
-    const bool first = w.rsub == 0;
-#pragma unroll
-    for (int ch = 0; ch < CH; ++ch) {
-      uint32_t v[32];
-      tmem_ld_32x32b_x32(taddr + ch * 32, v);
-#pragma unroll
-      for (int i = 0; i < 32; ++i) acc[ch][i] = first ? __uint_as_float(v[i]) : acc[ch][i] + __uint_as_float(v[i]);
-    }
-    // hand the accumulator back to the MMA warp
-    tc_fence_before();
-    __syncwarp();
-    if (lane == 0) {
-      if (PAIR == 2 && cta != 0) mbar_arrive_remote(tempty0 + b * 8);
-      else mbar_arrive(smem_u32(&s.tempty[b]));
-    }
-    ++it;
-    if (w.rsub + 1 < w.rcnt) {
-      if (ew == 0 && lane == 0) trace_now(p, it - 1, TR_EPI_END);
-      continue;
-    }
-    // the group's sum of this row: gate-weighted add into the token's row
-    const int row = w.m0 + q * 32 + lane;
-    const bool row_ok = row < w.row_end;
-    float gate = 0.0f;
-    int tok = 0;
-    if (row_ok) {
-      const int slot = __ldg(p.row_to_slot + row);
-      tok = slot / p.topk;
-      gate = __ldg(p.topk_w + slot);
-    }
-    const bool tok_ok = check_ok(c, !row_ok || (tok >= 0 && tok < p.T), CK_ACC_ROW, static_cast<uint32_t>(tok));
-    const int c0 = w.n0 + hh * HALF;
-    const int ncols = w.n_end - c0;
-#pragma unroll
-    for (int ch = 0; ch < CH; ++ch)
-      if (ch * 32 < ncols)  // warp-uniform
-        scatter_add_chunk(p.acc, p.N, c0 + ch * 32, ncols - ch * 32, sstg, lane, tok, row_ok && tok_ok, gate,
-                          acc[ch]);
-    if (ew == 0 && lane == 0) trace_now(p, it - 1, TR_EPI_END);
-  }
-}
-
 // RS_CLUSTER epilogue (the EPI_WARPS epilogue warps of every CTA).  The tile's
 // rows are the M <= 128 activation rows; owner rank o holds rows
 // [o M/R, (o+1) M/R), and CTA d of the cluster reduces the owners d, d + CL,
@@ -2375,8 +2248,6 @@ fused_gemm_kernel(const __grid_constant__ KParams p) {
     __syncwarp();
   } else if constexpr (MODE == MODE_RS_CLUSTER) {
     epilogue_rs_cluster<DT, CL>(p, s, c, tmem_base, warp, ps);
-  } else if constexpr (MODE == MODE_MOE_SCATTER_RED) {
-    epilogue_scatter_red<CL>(p, s, c, tmem_base, total_mt, warp, warp - KS::EPI_WARP0, ps);
   } else {
     // (staged MoE layer0: the copy first; after a shard flag timed out the
     // epilogue still runs, its waits give up as the producer's do)

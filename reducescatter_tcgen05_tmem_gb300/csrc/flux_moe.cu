@@ -21,17 +21,25 @@ constexpr int ROUTE_THREADS = 1024;
 //     (slower; multicast does not lower the bytes an SM receives) and CTA
 //     pairs gathering rows with TMA tile::gather4 (2.7x slower: 32 gather
 //     operations per stage cost the TMA unit far more than one 128-row box).
-//   layer1: CTA pairs with 256 x 256 tiles and two accumulators, so that the
-//     fp32 adds of one tile overlap the main loop of the next; from
-//     MOE1_WIDE_KT k-slices on, 256 x 512 tiles with one accumulator
-//     (MODE_MOE_SCATTER_WIDE).  Measured at T 4096, H 4096, F 14336, 8 experts,
-//     top-2: with 28 k-slices per tile (tensor parallel over 8 ranks) the wide
-//     tile is 13 % slower (0.76 -> 0.87 ms: the MMAs wait for each drain), with
-//     224 (expert parallel, one rank per expert) 14 % faster (0.78 -> 0.67 ms).
-//   layer0 staged (the default): every CTA first copies a share of the
-//     grouped rows into the workspace, then CTA pairs with 256 x 512 tiles
-//     load them by TMA (see MODE_MOE_STAGED; 256 x 256 measured 11 % slower).
-constexpr int MOE1_SPLIT_TAIL = 0;  // layer1 rank groups: split the last groups rank by rank
+//   layer1: CTA pairs.  With several ranks per expert group (tensor
+//     parallel), 256 x 512 tiles whose ranks' partials are summed in TMEM
+//     before one add (MODE_MOE_SCATTER_WIDE with rank groups, the default);
+//     with one rank per group (or on request, moe_l1_ranks 1): 256 x 256
+//     tiles with two accumulators, so that the fp32 adds of one tile overlap
+//     the main loop of the next, and from MOE1_WIDE_KT k-slices on 256 x 512
+//     tiles with one accumulator.  Measured at T 4096, H 4096, F 14336, 8
+//     experts, top-2: with 28 k-slices per tile and per rank the wide tile
+//     alone is 13 % slower (0.76 -> 0.87 ms: the MMAs wait for each drain),
+//     with 224 (expert parallel, one rank per expert) 14 % faster (0.78 ->
+//     0.67 ms); the 8-rank groups make the tensor-parallel layer 224 k-slices
+//     per drain too.
+//   layer0 staged (the default): the epilogue warps copy the grouped rows
+//     into the workspace while CTA pairs with 256 x 512 tiles load them by
+//     TMA (see MODE_MOE_STAGED; 256 x 256 measured slower).
+// layer1 rank groups: claim the last groups rank by rank (measured slower with
+// 8-rank groups, 713-718 against 654 us: a quarter of the work then drains
+// rank by rank)
+constexpr int MOE1_SPLIT_TAIL = 0;
 constexpr int MOE0_CL = 1;
 constexpr int MOE0S_CL = 2;
 constexpr int MOE1_CL = 2;
@@ -653,12 +661,6 @@ flux_status_t moe_layer1_impl(
   p.K = Fr;
   p.KT = (Fr + BK - 1) / BK;
   const bool wide = p.KT >= MOE1_WIDE_KT;
-  // short reductions over several ranks per expert group, on request: a CTA
-  // pair computes the partials of `rg` ranks for one tile back to back and
-  // sums them on chip.  Not the default: at T 4096, H 4096, F 14336, 8
-  // experts, top-2, R 8 the rank-innermost unit order re-reads each m-tile's H
-  // rows from DRAM once per wave (3.0 GB against 1.9 GB per launch) and the
-  // layer runs 0.76-0.81 ms against 0.73-0.75 ms with one add per rank.
   // rank groups (moe_l1_ranks; default all tp ranks of the expert group): a
   // CTA pair computes the partials of rg ranks of one 256 x 512 tile back to
   // back into one TMEM accumulator (rank-innermost claims on the dynamic
@@ -669,7 +671,6 @@ flux_status_t moe_layer1_impl(
   const int rg = (opts && opts->moe_l1_ranks > 0) ? opts->moe_l1_ranks : tp;
   if (opts && opts->moe_l1_ranks > 0 && tp % opts->moe_l1_ranks) return FLUX_ERR_INVALID_ARG;
   const bool grouped = tp > 1 && rg > 1;
-  const bool red = false;
   const int tile_n = (wide || grouped) ? 2 * BN : BN;
   p.Nt = (H + tile_n - 1) / tile_n;
   p.ldo = H;
@@ -716,14 +717,6 @@ flux_status_t moe_layer1_impl(
     const int grid = grid_dt<MODE_MOE_SCATTER_WIDE, MOE1_CL>(dtype, dev, opts, max_units);
     if (grid == 0) return FLUX_ERR_CUDA;
     return launch_dt<MODE_MOE_SCATTER_WIDE, MOE1_CL>(dtype, p, grid, s);
-  }
-  if (red) {
-    // rank innermost: item u * rg + j is rank (u * rg + j) % tp of tile (u * rg + j) / tp
-    p.moe_order = 1;
-    p.moe_rgroup = rg;
-    const int grid = grid_dt<MODE_MOE_SCATTER_RED, MOE1_CL>(dtype, dev, opts, max_units / rg);
-    if (grid == 0) return FLUX_ERR_CUDA;
-    return launch_dt<MODE_MOE_SCATTER_RED, MOE1_CL>(dtype, p, grid, s);
   }
   const int grid = grid_dt<MODE_MOE_SCATTER, MOE1_CL>(dtype, dev, opts, max_units);
   if (grid == 0) return FLUX_ERR_CUDA;

@@ -292,12 +292,11 @@ def _layer1(c, d, h_dev=None, routing=None, opts=None):
     (4, 192, 1024, 12800, 8, 2, "f16", True),
     (16, 512, 256, 4096, 8, 2, "f16", True),   # the most ranks a call takes: 32 tokens per owner
 ])
-@pytest.mark.parametrize("l1_ranks", [0, -1, 2], ids=["per-rank-adds", "all-ranks-on-chip", "pairs-on-chip"])
+@pytest.mark.parametrize("l1_ranks", [0, 1, 2], ids=["all-ranks-in-tmem", "per-rank-adds", "pairs-in-tmem"])
 def test_layer1_matches_oracle(R, T, H, F, E, topk, dtype, given, l1_ranks):
-    # l1_ranks: partials of how many ranks a CTA pair sums on chip before its
-    # adds into the token rows (0: the default, none; -1: all R ranks)
-    if l1_ranks == -1:
-        l1_ranks = R
+    # l1_ranks: partials of how many ranks a CTA pair sums in TMEM before its
+    # adds into the token rows (0: the default, all ranks of the expert group;
+    # 1: one add per rank on 256 x 256 tiles)
     if l1_ranks > 1 and R % l1_ranks:
         pytest.skip("group size must divide the ranks")
     c = configs.small(configs.CONFIGS["moe"], R=R, T=T, H=H, F=F, E=E, topk=topk, dtype=dtype,
@@ -318,7 +317,7 @@ def test_layer1_matches_oracle(R, T, H, F, E, topk, dtype, given, l1_ranks):
     assert torch.count_nonzero(ws[:64]).item() == 0
 
 
-@pytest.mark.parametrize("l1_ranks", [0, 4])
+@pytest.mark.parametrize("l1_ranks", [0, 1, 2])
 def test_layer1_integer_inputs_bit_exact(l1_ranks):
     # integer H and W2 in [-2, 2], gates 1/2: every fp32 partial, the on-chip
     # sum over ranks and the gate-weighted adds are exact, and |2 Y| <= 4 F <=
