@@ -673,6 +673,8 @@ __device__ __forceinline__ Work decode_reduce(const KParams& p, int u, int cta) 
 //   3  expert outermost, then n-tile, then the expert's m-units, rank fastest:
 //      the weight blocks of one expert column tile and the expert's rows are
 //      in use together, and each is read while the other stays in L2
+//   5  rank innermost, then the n-tiles of one m-unit, then the m-units: the
+//      rows of an m-unit serve all its column tiles while they are in L2
 template <int CL>
 __device__ __forceinline__ Work decode_moe(const KParams& p, int u, int total_mt, int cta, int tile_n) {
   Work w;
@@ -694,7 +696,7 @@ __device__ __forceinline__ Work decode_moe(const KParams& p, int u, int total_mt
     gmt = t0 + rem / p.moe_tp;
     tr = rem - (rem / p.moe_tp) * p.moe_tp;
   } else {
-    if (p.moe_order == 1) {
+    if (p.moe_order == 1 || p.moe_order == 5) {
       tr = u % p.moe_tp;
       t = u / p.moe_tp;
     } else if (p.moe_order == 2) {
@@ -717,8 +719,13 @@ __device__ __forceinline__ Work decode_moe(const KParams& p, int u, int total_mt
       tr = u / per_rank;
       t = u - tr * per_rank;
     }
-    // m-tile fastest inside bands of group_n n-tiles
-    raster(t, total_mt, p.Nt, p.group_n, gmt, nt);
+    if (p.moe_order == 5) {
+      gmt = t / p.Nt;
+      nt = t - gmt * p.Nt;
+    } else {
+      // m-tile fastest inside bands of group_n n-tiles
+      raster(t, total_mt, p.Nt, p.group_n, gmt, nt);
+    }
     while (hi - lo > 1) {
       const int mid = (lo + hi) >> 1;
       if (__ldg(p.tile_off + mid) <= gmt) lo = mid; else hi = mid;

@@ -704,7 +704,9 @@ flux_status_t moe_layer1_impl(
     // (the area holds 2 U + 4 MOE0_MAX_REGIONS entries, U >= max_units)
     if (g > MOE0_MAX_REGIONS || static_cast<size_t>(g * cap) * sizeof(uint32_t) > L.mbox1_bytes)
       return FLUX_ERR_WORKSPACE;
-    p.moe_order = 1;
+    // rank innermost (a group's ranks are consecutive units), then the column
+    // tiles of one m-unit (650 against 664 us with the m-units fastest)
+    p.moe_order = 5;
     p.rs_group = rg;
     p.split_from = MOE1_SPLIT_TAIL ? static_cast<int>(g) : 0;  // group claims split rank by rank
     p.dyn = 1;
