@@ -210,6 +210,8 @@ __host__ __device__ constexpr bool is_moe(int mode) {
 // rows of the first units are spread over every copying CTA and ready early
 // (8 rows: 10 us less per call than 32 at the MoE workload's sizes)
 constexpr int STAGE_BLK = 8;
+// MOE_STAGED with xcols: column tiles per group in the unit order (see decode_moe)
+constexpr int XCOL_GROUP = 8;
 constexpr int STAGE_UNROLL = 16;  // MOE_STAGED: 16-byte loads in flight per lane
 
 // device status header at the start of every workspace (256 bytes)
@@ -323,6 +325,11 @@ struct KParams {
                      // stored in the owner's 16-bit rows (tmOut[owner]) without fp32 rows
   int debug_probe;  // checked build: nonzero makes CTA 0 fail one check (CK_PROBE) on purpose
   int acc_halves;   // one 512-column accumulator: handed back in two 256-column halves
+  // MOE_STAGED: the output columns of an expert group's ranks side by side
+  // (N = moe_tp x xcols), xcols columns per rank, a multiple of 64: a column
+  // tile may span two ranks (each 64-column B box and output box lies in
+  // one); units carry no rank.  0: tiles within one rank's columns
+  int xcols;
 };
 
 constexpr uint32_t MBOX_DONE = 0xFFFFFFFFu;
@@ -672,7 +679,12 @@ __device__ __forceinline__ Work decode_reduce(const KParams& p, int u, int cta) 
 //   2  band outermost, then rank, then the m-tile fastest inside the band
 //   3  expert outermost, then n-tile, then the expert's m-units, rank fastest:
 //      the weight blocks of one expert column tile and the expert's rows are
-//      in use together, and each is read while the other stays in L2
+//      in use together, and each is read while the other stays in L2.  With
+//      xcols (no rank index) the column tiles take the ranks' place in groups
+//      of XCOL_GROUP: expert, group, m-unit, tile of the group fastest, so
+//      that consecutive units share the rows (in L2) and not a weight tile
+//      (streamed from DRAM: units that start together on one weight tile all
+//      wait on the same misses)
 //   5  rank innermost, then the n-tiles of one m-unit, then the m-units: the
 //      rows of an m-unit serve all its column tiles while they are in L2
 template <int CL>
@@ -682,7 +694,30 @@ __device__ __forceinline__ Work decode_moe(const KParams& p, int u, int total_mt
   int tr, t;  // rank inside the expert's group; the unit's index among that rank's
   int gmt, nt;
   int lo = 0, hi = p.E;  // the m-unit's expert: largest e with tile_off[e] <= gmt
-  if (p.moe_order == 3) {
+  if (p.moe_order == 3 && p.xcols > 0) {
+    while (hi - lo > 1) {
+      const int mid = (lo + hi) >> 1;
+      if (__ldg(p.tile_off + mid) * p.Nt <= u) lo = mid; else hi = mid;
+    }
+    const int t0 = __ldg(p.tile_off + lo);
+    const int ke = __ldg(p.tile_off + lo + 1) - t0;  // >= 1: u lies in this expert's units
+    const int local = u - t0 * p.Nt;
+    const int full = p.Nt / XCOL_GROUP;  // whole groups of column tiles
+    int g0, gs, rem;                     // the group's first tile and size; the unit inside it
+    if (local < full * XCOL_GROUP * ke) {
+      const int g = local / (XCOL_GROUP * ke);
+      g0 = g * XCOL_GROUP;
+      gs = XCOL_GROUP;
+      rem = local - g * XCOL_GROUP * ke;
+    } else {
+      g0 = full * XCOL_GROUP;
+      gs = p.Nt - g0;
+      rem = local - full * XCOL_GROUP * ke;
+    }
+    gmt = t0 + rem / gs;
+    nt = g0 + (rem - (rem / gs) * gs);
+    tr = 0;
+  } else if (p.moe_order == 3) {
     const int per_mt = p.Nt * p.moe_tp;  // units per m-unit
     while (hi - lo > 1) {
       const int mid = (lo + hi) >> 1;
@@ -808,7 +843,7 @@ struct ItemIter {
                       bool warp_uniform_ = false)
       : p(p_), ctl(ctl_), total_mt(total_mt_), cta(cta_), warp_uniform(warp_uniform_) {
     if (is_moe(MODE)) {
-      num_units = total_mt * p.Nt * p.moe_tp;
+      num_units = total_mt * p.Nt * (p.xcols > 0 ? 1 : p.moe_tp);
     } else {
       num_units = p.num_units;
     }
@@ -1053,6 +1088,36 @@ __device__ __forceinline__ bool produce_ksteps(const KParams& p, const Smem& s, 
   const int a_half = (hw_rank >> 2) & 1;
   constexpr int PAIR = Unit<MODE, CL>::PAIR;
   using G = typename Unit<MODE, CL>::G;
+  // the item's B boxes: tensor map and column (only the k coordinate moves
+  // in the loop; the single issuing thread's per-slice work stays short)
+  const CUtensorMap* bmap[G::B_BOXES];
+  int bcol[G::B_BOXES];
+#pragma unroll
+  for (int j = 0; j < G::B_BOXES; ++j) {
+    const int nc = b_box_col<PAIR>(n0, cta, j);
+    int n = nc < w.n_end ? nc : n0;  // the padding box of a CTA without columns
+    // (a padding box may start up to a tile past N: the load reads fill values)
+    if (!check_ok(c, n >= 0 && n < p.N + Unit<MODE, CL>::G::TILE_N && (n & 7) == 0 && w.r >= 0 && w.r < p.R,
+                  CK_B_COL, static_cast<uint32_t>(n)))
+      n = 0;
+    int br = w.r;
+    if (MODE == MODE_MOE_STAGED && p.xcols > 0) {
+      // the box's rank in the expert group, and its column in that rank's block
+      const int t = n / p.xcols;
+      br += t;
+      n -= t * p.xcols;
+      if (!check_ok(c, br < p.R, CK_B_COL, static_cast<uint32_t>(br))) br = w.r;
+    }
+    bmap[j] = &p.tmB[br];
+    bcol[j] = n;
+  }
+  // store mode: shard and shard row of the item's first A box (the next boxes
+  // step from there; a box never spans two shards)
+  int a_sh0 = 0, a_lrow0 = 0;
+  if (MODE == MODE_STORE) {
+    a_sh0 = w.m0 / p.rows_per_rank;
+    a_lrow0 = w.m0 - a_sh0 * p.rows_per_rank;
+  }
   for (int k = kb; k < ke; ++k) {
     // The empty barrier is completed by a remote commit whenever another CTA's
     // MMAs read the stage; the producer still waits in try_wait rather than
@@ -1068,13 +1133,22 @@ __device__ __forceinline__ bool produce_ksteps(const KParams& p, const Smem& s, 
     const uint32_t sb = smem_u32(s.b + stage * G::B_STAGE);
     const int kc = k * BK;
     if (MODE == MODE_STORE) {
+      int bsh = a_sh0, blrow = a_lrow0;
       for (int bx = 0; bx < nbox_a; ++bx) {
+        if (bx > 0) {
+          blrow += p.a_box_m;
+          if (blrow >= p.rows_per_rank) {
+            blrow -= p.rows_per_rank;
+            ++bsh;
+          }
+        }
         if (MCA && MC2 && bx != a_half) continue;  // the N neighbour multicasts this box
         const int row = w.m0 + bx * p.a_box_m;
-        int sh = row / p.rows_per_rank;
-        int lrow = row - sh * p.rows_per_rank;
+        int sh = bsh, lrow = blrow;
         int kx = kc;
-        if (!check_ok(c, row >= 0 && sh < p.R, CK_A_ROW, static_cast<uint32_t>(row))) sh = lrow = 0;
+        if (!check_ok(c, row >= 0 && sh < p.R && sh * p.rows_per_rank + lrow == row, CK_A_ROW,
+                      static_cast<uint32_t>(row)))
+          sh = lrow = 0;
         if (!check_ok(c, kc >= 0 && kc < p.K && (kc & 7) == 0, CK_A_K, static_cast<uint32_t>(kc))) kx = 0;
         if (MCA && MC2)
           tma_load_2d_pair_mc(sa + bx * p.a_box_m * BK * 2, &p.tmA[sh], fbc, kx, lrow, mask_a);
@@ -1105,26 +1179,21 @@ __device__ __forceinline__ bool produce_ksteps(const KParams& p, const Smem& s, 
         tma_load_2d(sa, &p.tmA[ar], fb, ak, am0);
       }
     }
+#pragma unroll
     for (int j = 0; j < G::B_BOXES; ++j) {
       if (!((bmask >> j) & 1u)) continue;
       // the pair stacked with this one multicasts the other half of the boxes
       if (MC2 && (j * 2) / G::B_BOXES != half) continue;
-      const int nc = b_box_col<PAIR>(n0, cta, j);
-      int n = nc < w.n_end ? nc : n0;  // the padding box of a CTA without columns
-      // (a padding box may start up to a tile past N: the load reads fill values)
-      if (!check_ok(c, n >= 0 && n < p.N + Unit<MODE, CL>::G::TILE_N && (n & 7) == 0 && w.r >= 0 && w.r < p.R,
-                    CK_B_COL, static_cast<uint32_t>(n)))
-        n = 0;
       check_ok(c, kc >= 0 && kc < p.K, CK_B_K, static_cast<uint32_t>(kc));
       const uint32_t dst = sb + j * B_BOX_N * BK * 2;
       if (is_scatter(MODE) || MODE == MODE_MOE_STAGED) {
-        if (PAIR == 2) tma_load_3d_pair(dst, &p.tmB[w.r], fbc, n, kc, w.e);
-        else tma_load_3d(dst, &p.tmB[w.r], fb, n, kc, w.e);
+        if (PAIR == 2) tma_load_3d_pair(dst, bmap[j], fbc, bcol[j], kc, w.e);
+        else tma_load_3d(dst, bmap[j], fb, bcol[j], kc, w.e);
       } else if (PAIR == 2) {
-        if (MC2) tma_load_2d_pair_mc(dst, &p.tmB[w.r], fbc, n, kc, mc_mask);
-        else tma_load_2d_pair(dst, &p.tmB[w.r], fbc, n, kc);
+        if (MC2) tma_load_2d_pair_mc(dst, bmap[j], fbc, bcol[j], kc, mc_mask);
+        else tma_load_2d_pair(dst, bmap[j], fbc, bcol[j], kc);
       } else {
-        tma_load_2d(dst, &p.tmB[w.r], fb, n, kc);
+        tma_load_2d(dst, bmap[j], fb, bcol[j], kc);
       }
     }
     ++issued;
@@ -1639,11 +1708,17 @@ __device__ void epilogue(const KParams& p, const Smem& s, const Ctl& c, uint32_t
         tmem_ld_32x32b_x32(taddr + ch * 64, v);
         tmem_ld_32x32b_x32(taddr + ch * 64 + 32, u);
         if (row0 >= w.row_end) continue;  // none of this warp's rows is in the tile
+        // the box's output tensor and column (xcols: the rank whose block holds it)
+        int crank = orank, ccol = n0 + ch * 64;
+        if (MODE == MODE_MOE_STAGED && p.xcols > 0) {
+          const int t = ccol / p.xcols;
+          crank += t;
+          ccol -= t * p.xcols;
+        }
         // (checked build: a box outside the rank's output is recorded and not written)
-        if (!check_ok(c, orank >= 0 && orank < p.R && row0 >= 0 && row0 < p.M, CK_OUT_ROW,
+        if (!check_ok(c, crank >= 0 && crank < p.R && row0 >= 0 && row0 < p.M, CK_OUT_ROW,
                       static_cast<uint32_t>(row0)) ||
-            !check_ok(c, n0 + ch * 64 >= 0 && n0 + ch * 64 < p.ldo && ((n0 + ch * 64) & 7) == 0, CK_OUT_COL,
-                      static_cast<uint32_t>(n0 + ch * 64)))
+            !check_ok(c, ccol >= 0 && ccol < p.ldo && (ccol & 7) == 0, CK_OUT_COL, static_cast<uint32_t>(ccol)))
           continue;
         if (row0 + 32 <= w.row_end || w.row_end == p.M) {
           // the warp's 32 x 64 box, staged in the 128-byte swizzled layout of
@@ -1669,7 +1744,7 @@ __device__ void epilogue(const KParams& p, const Smem& s, const Ctl& c, uint32_t
           fence_proxy_async_smem();
           __syncwarp();
           if (lane == 0) {
-            tma_store_2d(&p.tmOut[orank], buf, n0 + ch * 64, orow0);
+            tma_store_2d(&p.tmOut[crank], buf, ccol, orow0);
             bulk_commit();
           }
           ++nst;
@@ -1681,8 +1756,8 @@ __device__ void epilogue(const KParams& p, const Smem& s, const Ctl& c, uint32_t
             if (lane == 0) bulk_wait_read_all();
             __syncwarp();
           }
-          store_rows_chunk64<DT>(p.out[orank], p.ldo, orow0, w.row_end - row0, n0 + ch * 64,
-                                 ncols - ch * 64, sstg, lane, v, u);
+          store_rows_chunk64<DT>(p.out[crank], p.ldo, orow0, w.row_end - row0, ccol, ncols - ch * 64, sstg,
+                                 lane, v, u);
         }
       }
       if (direct && nst > 0) {

@@ -329,7 +329,8 @@ constexpr int MOE0_MAX_REGIONS = 256;
 
 // Bound on the staged layer0's units for any EP x TP split of these sizes:
 // m-units of BM * MOE0S_CL rows (one partial m-unit per expert at most) times
-// ceil(F / tp / 512) * tp <= ceil(F / 512) + R column tiles over the ranks.
+// ceil(F / tp / 512) * tp <= ceil(F / 512) + R column tiles over the ranks
+// (ceil(F / 512) with the ranks' columns side by side).
 long long moe0_unit_bound(int R, int T, int F, int E, int topk) {
   const long long n = static_cast<long long>(T) * topk;
   const long long mts = (n + BM * MOE0S_CL - 1) / (BM * MOE0S_CL) + E;
@@ -535,11 +536,17 @@ flux_status_t moe_layer0_impl(
   // sizes 1.42 GB, 1.5 % faster than the m-fastest order over all experts:
   // 1.52 GB)
   p.moe_order = 3;
+  // staged: the 512-column tiles run over the group's ranks' columns side by
+  // side where every 64-column box lies in one rank (F/tp a multiple of 64),
+  // so a rank block of 3.5 tiles leaves no half-wide tile (at the MoE
+  // workload's sizes a half tile's k-loop took 89 % of a whole one's time)
+  const bool xcols = !pull && Fr % B_BOX_N == 0;
+  p.xcols = xcols ? Fr : 0;
   p.R = R;
   p.M = n;
-  p.N = Fr;
+  p.N = xcols ? tp * Fr : Fr;
   p.K = H;
-  p.Nt = pull ? (Fr + BN - 1) / BN : (Fr + 2 * BN - 1) / (2 * BN);  // 256- / 512-column tiles
+  p.Nt = pull ? (Fr + BN - 1) / BN : (p.N + 2 * BN - 1) / (2 * BN);  // 256- / 512-column tiles
   p.KT = (H + BK - 1) / BK;
   p.ldo = Fr;
   p.rows_per_rank = rows;
@@ -562,7 +569,7 @@ flux_status_t moe_layer0_impl(
   p.acc_halves = (opts && opts->acc_whole) ? 0 : 1;
   const long long max_units =
       (static_cast<long long>((n + BM * cl - 1) / (BM * cl)) + E) * p.Nt *
-      static_cast<long long>(tp);
+      static_cast<long long>(xcols ? 1 : tp);
   if (pull) {
     const int grid = grid_dt<MODE_MOE_GATHER, MOE0_CL>(dtype, dev, opts, max_units);
     if (grid == 0) return FLUX_ERR_CUDA;

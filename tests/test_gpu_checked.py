@@ -81,9 +81,10 @@ ok(ws, "plain gemm split-K")
 check_close(oracle.widen(from_device(C), "bf16"), oracle.gemm(oracle.widen(A, "bf16"), oracle.widen(B, "bf16")),
             "checked plain gemm")
 
-# MoE layers (staged and pull layer0; layer1 per rank and with ranks summed on chip), empty expert
-for pull, l1 in ((0, 0), (1, 4)):
-    c = configs.small(configs.CONFIGS["moe"], R=4, T=512, H=320, F=4 * 448, E=8, topk=2, seed=704,
+# MoE layers (staged layer0 with column tiles over the ranks' blocks side by side and within
+# each rank's block, pull layer0; layer1 per rank and with ranks summed on chip), empty expert
+for pull, l1, Fr in ((0, 0, 448), (1, 4, 448), (0, 1, 440)):
+    c = configs.small(configs.CONFIGS["moe"], R=4, T=512, H=320, F=4 * Fr, E=8, topk=2, seed=704,
                       force_empty=(5,))
     d = configs.moe_inputs(c)
     n, Fr = c.T * c.topk, c.F // c.R
@@ -142,7 +143,7 @@ def test_checked_build_runs_every_op_clean_and_reports_the_probe():
     assert r.returncode == 0, r.stdout[-3000:] + r.stderr[-3000:]
     line = [ln for ln in r.stdout.splitlines() if ln.startswith("RESULT ")][-1]
     res = json.loads(line[len("RESULT "):])
-    assert len(res["done"]) == 15, res["done"]  # 2 AG, 7 GEMM-RS, 1 plain GEMM, 4 MoE, 1 after the probe
+    assert len(res["done"]) == 17, res["done"]  # 2 AG, 7 GEMM-RS, 1 plain GEMM, 6 MoE, 1 after the probe
     assert res["probe"]["status"] == fx.FLUX_ERR_INVALID_ARG
     rep = res["probe"]["report"]
     assert rep["where"] == "check" and rep["arg0"] == 15 and rep["arg1"] == 1234, rep

@@ -145,6 +145,7 @@ def _layer0(c, d=None, flags=None, opts=None):
     (2, 200, 136, 256, 5, 3, "bf16", ()),      # H = 136: a 16-byte row tail in the staging copy
     (16, 1024, 256, 4096, 8, 2, "bf16", ()),   # the most ranks a call takes: 64 tokens per shard
     (4, 1000, 256, 2048, 64, 2, "f16", (3, 9, 40)),  # 64 experts, most with a partial last unit
+    (4, 512, 256, 800, 8, 2, "bf16", ()),      # F/R = 200, not a multiple of 64: tiles within each rank
 ])
 def test_layer0_matches_oracle(R, T, H, F, E, topk, dtype, empty, pull):
     # staged: every CTA first copies a share of the grouped rows, then CTA pairs
@@ -159,12 +160,16 @@ def test_layer0_matches_oracle(R, T, H, F, E, topk, dtype, empty, pull):
         check_close(oracle.widen(from_device(Hd[r]), dtype), ref[r], f"layer0 rank {r}")
 
 
-@pytest.mark.parametrize("layer", [0, 1])
-def test_pairs_with_an_idle_cta_match_oracle(layer):
-    # units whose odd CTA holds no rows, in a last n-tile of 128 columns (none
-    # for the odd CTA): that CTA loads nothing of its own into those stages
-    if layer == 0:
-        c = configs.small(configs.CONFIGS["moe"], R=8, T=2048, H=512, F=8 * 896, E=8, topk=2, seed=68)
+@pytest.mark.parametrize("case", ["layer0_ranks_side_by_side", "layer0_per_rank", "layer1"])
+def test_pairs_with_an_idle_cta_match_oracle(case):
+    # units whose odd CTA holds no rows, in a last n-tile of at most 128 columns
+    # (none for the odd CTA): that CTA loads nothing of its own into those
+    # stages.  Layer0 with F/R a multiple of 64 runs its column tiles over the
+    # ranks' blocks side by side (2 x 448 = 512 + 384 columns); otherwise
+    # within each rank's block (888 = 512 + 376 columns)
+    if case.startswith("layer0"):
+        R, Fr = (2, 448) if case == "layer0_ranks_side_by_side" else (8, 888)
+        c = configs.small(configs.CONFIGS["moe"], R=R, T=2048, H=512, F=R * Fr, E=8, topk=2, seed=68)
         d, Hd, _ = _layer0(c)
         ref, _ = oracle.moe_layer0(d["x_shards"], d["w1_shards"], d["topk_ids"], c.E, c.dtype)
         for r in range(c.R):

@@ -126,7 +126,9 @@ def test_moe_layer0_dynamic_trace_covers_every_unit_once():
         check_close(oracle.widen(from_device(H[r]), "bf16"), ref[r], f"traced layer0 rank {r}")
     m_units = int(sum((int(k) + 255) // 256 for k in want_counts))
     t = ftrace.records(tr)
-    _check_records(t, units=m_units * ((Fr + 511) // 512) * c.R, per_unit=2)
+    # (F/R = 896 is a multiple of 64: the 512-column tiles run over the ranks'
+    # column blocks side by side, 14 per m-unit instead of 2 x 8 with 8 half-wide)
+    _check_records(t, units=m_units * ((c.R * Fr + 511) // 512), per_unit=2)
 
 
 def test_gemm_rs_rank_group_trace_covers_every_claim():
