@@ -127,8 +127,35 @@ def test_moe_layer0_dynamic_trace_covers_every_unit_once():
     m_units = int(sum((int(k) + 255) // 256 for k in want_counts))
     t = ftrace.records(tr)
     # (F/R = 896 is a multiple of 64: the 512-column tiles run over the ranks'
-    # column blocks side by side, 14 per m-unit instead of 2 x 8 with 8 half-wide)
+    # column blocks side by side, 14 per m-unit instead of 2 x 8 with 8
+    # half-wide)
     _check_records(t, units=m_units * ((c.R * Fr + 511) // 512), per_unit=2)
+
+
+def test_moe_layer1_rank_group_trace_covers_every_claim():
+    # layer1 with the ranks of a tile summed in TMEM: a claim is one 256 x 512
+    # tile for all R ranks, recorded by both CTAs of its pair once per rank;
+    # each CTA drains once per claim
+    c = configs.small(configs.CONFIGS["moe"], R=4, T=1024, H=1536, F=4 * 256, E=8, topk=2, seed=506)
+    d = configs.moe_inputs(c)
+    n = c.T * c.topk
+    Y = [torch.full((c.T // c.R, c.H), float("nan"), dtype=torch.bfloat16, device="cuda") for _ in range(c.R)]
+    ws = _ws(fx.flux_moe_workspace_size(fx.FLUX_OP_MOE_RS, c.R, c.T, c.H, c.F, c.E, c.topk))
+    tr = torch.zeros(8 + 152 * 64 * 8, dtype=torch.int64, device="cuda")
+    fx.flux_moe_grouped_gemm_rs(c.R, c.T, c.H, c.F, c.E, c.topk, fx.FLUX_BF16,
+                                [to_device(h, "bf16") for h in d["h_shards"]],
+                                [to_device(w, "bf16") for w in d["w2_shards"]],
+                                torch.from_numpy(d["topk_ids"]).cuda(), torch.from_numpy(d["topk_weights"]).cuda(),
+                                None, None, None, Y, ws, opts={"trace": tr})
+    st, rep = fx.flux_get_status(ws)
+    assert st == fx.FLUX_OK, rep
+    ref = oracle.moe_layer1(d["h_shards"], d["w2_shards"], d["topk_ids"], d["topk_weights"], c.E, "bf16")
+    for o in (0, c.R - 1):
+        check_close(oracle.widen(from_device(Y[o]), "bf16"), ref[o], f"traced layer1 owner {o}")
+    counts = np.bincount(d["topk_ids"].ravel(), minlength=c.E)
+    m_units = int(sum((int(k) + 255) // 256 for k in counts))
+    claims = m_units * ((c.H + 511) // 512)
+    _check_records(ftrace.records(tr), units=claims, per_unit=2 * c.R, drains=2 * claims)
 
 
 def test_gemm_rs_rank_group_trace_covers_every_claim():
