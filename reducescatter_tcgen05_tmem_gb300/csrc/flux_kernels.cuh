@@ -210,8 +210,11 @@ __host__ __device__ constexpr bool is_moe(int mode) {
 // rows of the first units are spread over every copying CTA and ready early
 // (8 rows: 10 us less per call than 32 at the MoE workload's sizes)
 constexpr int STAGE_BLK = 8;
-// MOE_STAGED with xcols: column tiles per group in the unit order (see decode_moe)
-constexpr int XCOL_GROUP = 8;
+// MOE_STAGED with xcols: column tiles per group in the unit order (see
+// decode_moe).  At the MoE workload's sizes (28 tiles per expert) groups of
+// 4 / 8 / 16 / 28 gave 605 / 612 / 621 / 639 us: the fewer weight tiles in
+// use at once, the better
+constexpr int XCOL_GROUP = 4;
 constexpr int STAGE_UNROLL = 16;  // MOE_STAGED: 16-byte loads in flight per lane
 
 // device status header at the start of every workspace (256 bytes)
