@@ -328,6 +328,13 @@ struct KParams {
                      // stored in the owner's 16-bit rows (tmOut[owner]) without fp32 rows
   int debug_probe;  // checked build: nonzero makes CTA 0 fail one check (CK_PROBE) on purpose
   int acc_halves;   // one 512-column accumulator: handed back in two 256-column halves
+  // MOE_SCATTER_WIDE with rank groups: arrivals per (token, 512-column tile)
+  // [T x row_tiles] (nullptr: the end-of-call pass converts every token
+  // row).  The add that brings a tile of a token to row_arrivals (topk x
+  // the group count per slot) converts it and zeroes it and its count.
+  uint32_t* row_cnt;
+  int row_tiles;
+  int row_arrivals;
   // MOE_STAGED: the output columns of an expert group's ranks side by side
   // (N = moe_tp x xcols), xcols columns per rank, a multiple of 64: a column
   // tile may span two ranks (each 64-column B box and output box lies in
@@ -1626,6 +1633,58 @@ __device__ __forceinline__ void convert8(float* src, uint16_t* dst) {
   st_cg_f4(src + 4, z);
 }
 
+// MoE layer1 with rank groups: convert the token tiles of the warp's slots in
+// `todo` (bit i: slot of lane i, token tok of that lane) whose last add has
+// landed: the fp32 row's columns [n0, n0 + ncols) of the tile go to the
+// owner's 16-bit output row and are zeroed.  Two tiles at a time, 16 lanes
+// each, 32 columns per lane (four 8-column chunks).
+template <int DT>
+__device__ __forceinline__ void convert_token_tiles(const KParams& p, const Ctl& c, uint32_t todo, int tok,
+                                                    int n0, int ncols, int lane) {
+  const int half = lane >> 4, hl = lane & 15;
+  const float4 zero = make_float4(0.f, 0.f, 0.f, 0.f);
+  while (todo != 0u) {
+    const int r0 = __ffs(todo) - 1;
+    todo &= todo - 1u;
+    int r1 = -1;
+    if (todo != 0u) {
+      r1 = __ffs(todo) - 1;
+      todo &= todo - 1u;
+    }
+    const int mine = half == 0 ? r0 : r1;
+    const int t = __shfl_sync(0xFFFFFFFFu, tok, mine < 0 ? 0 : mine);
+    if (mine < 0) continue;  // (the second half of the warp has no tile this round)
+    const int o = t / p.rows_per_rank;
+    const int lt = t - o * p.rows_per_rank;
+    if (!check_ok(c, o >= 0 && o < p.R, CK_OWNER, static_cast<uint32_t>(o))) continue;
+    float* src = p.acc + static_cast<long long>(t) * p.N + n0;
+    uint16_t* dst = static_cast<uint16_t*>(p.out[o]) + static_cast<long long>(lt) * p.ldo + n0;
+    float4 a[4], b[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const int col = (j * 16 + hl) * 8;  // 8-column chunk of this lane
+      if (col < ncols) {
+        a[j] = ld_cg_f4(src + col);
+        b[j] = ld_cg_f4(src + col + 4);
+      }
+    }
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const int col = (j * 16 + hl) * 8;
+      if (col < ncols) {
+        uint4 q;
+        q.x = pack2<DT>(a[j].x, a[j].y);
+        q.y = pack2<DT>(a[j].z, a[j].w);
+        q.z = pack2<DT>(b[j].x, b[j].y);
+        q.w = pack2<DT>(b[j].z, b[j].w);
+        *reinterpret_cast<uint4*>(dst + col) = q;
+        st_cg_f4(src + col, zero);
+        st_cg_f4(src + col + 4, zero);
+      }
+    }
+  }
+}
+
 template <int MODE, int DT, int CL>
 __device__ void epilogue(const KParams& p, const Smem& s, const Ctl& c, uint32_t tmem_base,
                          int total_mt, int warp, const Pos& ps) {
@@ -1652,6 +1711,10 @@ __device__ void epilogue(const KParams& p, const Smem& s, const Ctl& c, uint32_t
   // GEMM-RS with rank groups: only a group's last item hands over the
   // accumulator, holding the sum of the group's partials
   const bool grouped = ItemIter<MODE, CL>::GROUPS && p.rs_group > 1;
+  // every slot routed (the routing's last offset is T*topk): the token tiles
+  // are converted as their last add lands, else by the end-of-call pass
+  const bool count_rows = MODE == MODE_MOE_SCATTER_WIDE && p.row_cnt != nullptr &&
+                          __ldg(p.offsets + p.E) == p.T * p.topk;
   int item = -1;  // trace record index
   while (iter.next(w)) {
     ++item;
@@ -1843,6 +1906,28 @@ __device__ void epilogue(const KParams& p, const Smem& s, const Ctl& c, uint32_t
     }
     ++it;
     if (tracer && (MODE != MODE_REDUCE || direct)) trace_now(p, item, TR_EPI_END);
+
+    if (MODE == MODE_MOE_SCATTER_WIDE && grouped && count_rows && ncols > 0) {
+      // this tile's adds of the warp's 32 slots are issued: make them visible,
+      // then count each slot's token tile; the add that completes a token
+      // tile converts it (after the accumulator went back, so the next
+      // tile's MMAs do not wait for it)
+      __syncwarp();
+      __threadfence();
+      __syncwarp();
+      const int tile = n0 / G::TILE_N;
+      bool done = false;
+      if (row_ok && tok >= 0 && tok < p.T) {
+        uint32_t* cnt = p.row_cnt + static_cast<size_t>(tok) * p.row_tiles + tile;
+        done = atomicAdd(cnt, 1u) + 1u == static_cast<uint32_t>(p.row_arrivals);
+        if (done) *cnt = 0u;  // no other add of this call reaches the tile
+      }
+      const uint32_t todo = __ballot_sync(0xFFFFFFFFu, done);
+      if (todo != 0u) {
+        __threadfence();  // the other adds to those tiles, before this warp reads them
+        convert_token_tiles<DT>(p, c, todo, tok, n0, ncols, lane);
+      }
+    }
 
     if (MODE == MODE_REDUCE && !direct) {
       // arrival counter of this tile's 32-row quarter counts k-slices; quarters
@@ -2349,7 +2434,12 @@ fused_gemm_kernel(const __grid_constant__ KParams p) {
     if (PAIR == 2) tmem_dealloc2(tmem_base, TMEM_COLS);
     else tmem_dealloc(tmem_base, TMEM_COLS);
   }
-  if constexpr (is_scatter(MODE)) finish_token_rows<DT>(p, c, s.misc + 1);
+  if constexpr (is_scatter(MODE)) {
+    // (with rank groups and every slot routed the epilogues converted the rows)
+    const bool counted = MODE == MODE_MOE_SCATTER_WIDE && p.rs_group > 1 && p.row_cnt != nullptr &&
+                         __ldg(p.offsets + p.E) == p.T * p.topk;
+    if (!counted) finish_token_rows<DT>(p, c, s.misc + 1);
+  }
   if (dyn) {
     // The last CTA to finish clears the schedule (counter, exit count and
     // mailboxes) so that the workspace is zero again for the next call.  Every

@@ -320,7 +320,7 @@ size_t a256(size_t v) { return round_up(v, WS_ALIGN); }
 // MOE_LAYERS), so that the one-call layer finds each part where the single
 // calls put it
 struct MoeWs {
-  size_t tile_off, counts, offsets, s2r, r2s, acc, unit_cnt, stage, mbox, mbox_bytes, mbox1, mbox1_bytes,
+  size_t tile_off, counts, offsets, s2r, r2s, acc, row_cnt, unit_cnt, stage, mbox, mbox_bytes, mbox1, mbox1_bytes,
       total;
 };
 
@@ -355,6 +355,9 @@ MoeWs moe_layout(flux_op_t op, int R, int T, int H, int F, int E, int topk) {
     o += a256(n * sizeof(int32_t));
     w.acc = o;
     o += a256(static_cast<size_t>(T) * H * sizeof(float));
+    // rank groups: adds per (token, 512-column tile) of the fp32 rows
+    w.row_cnt = o;
+    o += a256(static_cast<size_t>(T) * ((H + 2 * BN - 1) / (2 * BN)) * sizeof(uint32_t));
     // mailboxes of layer1's dynamic schedule (rank groups on 256 x 512 tiles):
     // at most 2 U + 4 MOE0_MAX_REGIONS entries for U = (ceil(T*topk / 256) + E)
     // ceil(H / 512) R units (every rank of an expert's group computes all H
@@ -715,6 +718,12 @@ flux_status_t moe_layer1_impl(
     // tiles of one m-unit (650 against 664 us with the m-units fastest)
     p.moe_order = 5;
     p.rs_group = rg;
+    // each (token, column tile) receives topk x tp / rg adds; the last one
+    // converts it and no end-of-call pass runs (634-635 against 654-655 us
+    // with the pass at the MoE workload's sizes)
+    p.row_cnt = reinterpret_cast<uint32_t*>(ws + L.row_cnt);
+    p.row_tiles = (H + 2 * BN - 1) / (2 * BN);
+    p.row_arrivals = topk * (tp / rg);
     p.split_from = MOE1_SPLIT_TAIL ? static_cast<int>(g) : 0;  // group claims split rank by rank
     p.dyn = 1;
     p.mbox = reinterpret_cast<uint32_t*>(ws + L.mbox1);

@@ -265,7 +265,7 @@ def test_layer0_staged_withheld_flag_times_out_and_gpu_stays_usable():
 
 
 # ---------------------------------------------------------------- layer1
-def _layer1(c, d, h_dev=None, routing=None, opts=None):
+def _layer1(c, d, h_dev=None, routing=None, opts=None, ws=None):
     dt = c.dtype
     n = c.T * c.topk
     Hs = h_dev if h_dev is not None else [to_device(h, dt) for h in d["h_shards"]]
@@ -274,7 +274,8 @@ def _layer1(c, d, h_dev=None, routing=None, opts=None):
     gw = torch.from_numpy(d["topk_weights"]).cuda()
     out = [torch.full((c.T // c.R, c.H), float("nan"), dtype=torch_dtype(dt), device="cuda")
            for _ in range(c.R)]
-    ws = _ws(fx.flux_moe_workspace_size(fx.FLUX_OP_MOE_RS, c.R, c.T, c.H, c.F, c.E, c.topk))
+    if ws is None:
+        ws = _ws(fx.flux_moe_workspace_size(fx.FLUX_OP_MOE_RS, c.R, c.T, c.H, c.F, c.E, c.topk))
     off = s2r = r2s = None
     if routing is not None:
         _, off, s2r, r2s = routing
@@ -315,11 +316,55 @@ def test_layer1_matches_oracle(R, T, H, F, E, topk, dtype, given, l1_ranks):
     ref = oracle.moe_layer1(d["h_shards"], d["w2_shards"], d["topk_ids"], d["topk_weights"], E, dtype)
     for o in range(R):
         check_close(oracle.widen(from_device(out[o]), dtype), ref[o], f"layer1 owner {o}")
-    # the fp32 token rows (the tail of the workspace) and the header, which holds the
-    # grid barrier's counters, are left at zero
-    tail = -(-T * H * 4 // 256) * 256 // 4
-    assert torch.count_nonzero(ws[-tail:]).item() == 0
+    # the fp32 token rows, the per-tile add counts and the mailboxes (everything
+    # after the routing tables) and the header, which holds the grid barrier's
+    # counters, are left at zero
+    a256 = lambda b: -(-b // 256) * 256  # noqa: E731
+    acc_off = 256 + a256((E + 1) * 4) + a256(E * 4) + a256((E + 1) * 4) + 2 * a256(T * topk * 4)
+    assert torch.count_nonzero(ws[acc_off // 4:]).item() == 0
     assert torch.count_nonzero(ws[:64]).item() == 0
+
+
+def test_layer1_with_an_unrouted_slot_converts_in_the_end_pass():
+    # a slot whose expert id is out of range is routed nowhere (offsets[E] <
+    # T*topk), so its token's tiles never see all their adds: the layer then
+    # converts the token rows in the end-of-call pass instead of at each tile's
+    # last add.  The result is the layer without that slot (the oracle with
+    # its gate weight 0), and the workspace is clean for the next call
+    R, T, H, F, E, topk = 4, 256, 256, 1024, 4, 2
+    c = configs.small(configs.CONFIGS["moe"], R=R, T=T, H=H, F=F, E=E, topk=topk, seed=95)
+    d = configs.moe_inputs(c)
+    n = T * topk
+    ids = d["topk_ids"].copy()
+    ids[5, 1] = E
+    counts, off, s2r, r2s = _i32(E), _i32(E + 1), _i32(n), _i32(n)
+    ws_r = _ws(256)
+    fx.flux_moe_route(T, E, topk, torch.from_numpy(ids).cuda(), counts, off, s2r, r2s, ws_r)
+    assert fx.flux_get_status(ws_r)[0] == fx.FLUX_ERR_INVALID_ARG
+    rows = int(off[E].item())
+    assert rows == n - 1
+    # d["h_shards"][r][s]: rank r's layer0 row of slot s, placed in each routing's row order
+    r2s_gpu = r2s[:rows].cpu().numpy()
+    h_gpu = []
+    for h in d["h_shards"]:
+        g = np.zeros_like(h)
+        g[:rows] = h[r2s_gpu]
+        h_gpu.append(g)
+    ids_ref = ids.copy()
+    ids_ref[5, 1] = 0
+    w_ref = d["topk_weights"].copy()
+    w_ref[5, 1] = 0.0
+    r2s_ref = oracle.moe_route(ids_ref, E)[3]
+    ref = oracle.moe_layer1([h[r2s_ref] for h in d["h_shards"]], d["w2_shards"], ids_ref, w_ref, E, c.dtype)
+    out, ws = _layer1(c, dict(d, topk_ids=ids), h_dev=[to_device(h, c.dtype) for h in h_gpu],
+                      routing=(counts, off, s2r, r2s))
+    for o in range(R):
+        check_close(oracle.widen(from_device(out[o]), c.dtype), ref[o], f"unrouted slot, owner {o}")
+    # the same workspace, every slot routed: the tiles are converted at their last add
+    out2, _ = _layer1(c, d, ws=ws)
+    ref2 = oracle.moe_layer1(d["h_shards"], d["w2_shards"], d["topk_ids"], d["topk_weights"], E, c.dtype)
+    for o in range(R):
+        check_close(oracle.widen(from_device(out2[o]), c.dtype), ref2[o], f"next call, owner {o}")
 
 
 @pytest.mark.parametrize("l1_ranks", [0, 1, 2])
