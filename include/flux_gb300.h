@@ -422,11 +422,15 @@ flux_status_t flux_moe_ag_grouped_gemm(int R, int T, int H, int F, int E, int to
  *                 this call recompute them in its workspace
  *   out[o]        device, [T/R x H]
  * Contributions are accumulated in fp32 in the workspace (gate-weighted adds
- * in each tile's epilogue); when every tile is done, the CTAs of the launch
- * meet at a grid-wide barrier (the launch is sized so that all of them are
- * resident at once; a kernel of another stream that holds SMs the whole time
- * can delay it until timeout_ns, FLUX_ERR_TIMEOUT at wait site 11) and each
- * converts a share of the token rows to 16 bits.  Tiles are 256 x 256 on CTA
+ * in each tile's epilogue).  With rank groups (the default when an expert
+ * group has several ranks) every (token, 512-column tile) receives a known
+ * number of adds, and the add that completes it converts it to 16 bits and
+ * zeroes it.  Otherwise (one add per rank, or a slot whose expert id is out
+ * of range, routed nowhere) the CTAs of the launch meet at a grid-wide
+ * barrier when every tile is done (the launch is sized so that all of them
+ * are resident at once; a kernel of another stream that holds SMs the whole
+ * time can delay it until timeout_ns, FLUX_ERR_TIMEOUT at wait site 11) and
+ * each converts a share of the token rows.  Tiles are 256 x 256 on CTA
  * pairs with two accumulators (each tile's adds overlap the next tile), or,
  * for reductions of 48 or more 64-deep k-slices (F/R > 3008, also the
  * per-rank length of flux_moe_ep_gemm_combine), 256 x 512 with one.
