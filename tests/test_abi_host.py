@@ -98,8 +98,14 @@ def test_workspace_sizes(fx):
     assert fx.flux_workspace_size(fx.FLUX_OP_GEMM_RS, 0, 1, 1, 1) == 0
     assert fx.flux_workspace_size(99, 1, 1, 1, 1) == 0
     s = fx.flux_moe_workspace_size(fx.FLUX_OP_MOE_RS, 8, 4096, 4096, 14336, 8, 2)
-    # header + tile table + routing + fp32 token rows (T x H)
-    assert s >= 256 + 4096 * 4096 * 4
+    # layer1: header, tile table, routing (counts, offsets, both permutations),
+    # fp32 token rows [T x H], one add count per (token, 512-column tile), and
+    # the mailboxes of its rank-group claims, 2 U + 1024 entries for
+    # U = (ceil(T*topk / 256) + E) ceil(H / 512) R
+    a256 = lambda b: -(-b // 256) * 256  # noqa: E731
+    u1 = (8192 // 256 + 8) * (4096 // 512) * 8
+    assert s == (256 + a256(9 * 4) + a256(8 * 4) + a256(9 * 4) + 2 * a256(8192 * 4) + 4096 * 4096 * 4
+                 + a256(4096 * 8 * 4) + a256((2 * u1 + 1024) * 4))
     # layer0: header, tile table, a ready count per 256-row unit, the staged rows
     # [T*topk x H] and the mailboxes of its unit schedule, 2 U + 1024 entries for
     # U = (ceil(T*topk / 256) + E)(ceil(F / 512) + R)
