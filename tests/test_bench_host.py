@@ -1,5 +1,5 @@
-"""Host-side logic of bench.py (no GPU): the multi-GPU refusal and the clock
-summary of a window."""
+"""Host-side logic of bench.py (no GPU): the multi-GPU refusal, the clock
+summary of a window, and the DRAM traffic record keyed to the kernel sources."""
 import json
 import os
 import subprocess
@@ -60,3 +60,28 @@ def test_clock_summary_keeps_only_the_window(tmp_path):
     assert s["sm_mhz"] == 1600
     assert s["sm_max_mhz"] == 2070
     assert s["reasons"] == ["sw_power_cap"]
+
+
+def test_traffic_is_reported_only_for_the_sources_it_was_captured_on(tmp_path, monkeypatch):
+    sys.path.insert(0, ROOT)
+    import bench
+    (tmp_path / "profiles").mkdir()
+    with open(tmp_path / "profiles" / "ncu_traffic.json", "w") as f:
+        json.dump({"gemm_rs": {"kernel_hash": "aaaa", "dram_bytes_per_launch": 123},
+                   "ag_gemm": {"kernel_hash": "bbbb", "dram_bytes_per_launch": 456}}, f)
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    monkeypatch.setattr(bench, "kernel_hash", lambda op="gemm_rs": "aaaa")
+    assert bench.load_traffic("gemm_rs") == 123
+    assert bench.load_traffic("ag_gemm") is None  # captured on other sources
+    assert bench.load_traffic("moe_layer0") is None  # never captured
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path / "missing"))
+    assert bench.load_traffic("gemm_rs") is None
+
+
+def test_committed_traffic_record_names_every_fused_op():
+    with open(os.path.join(ROOT, "profiles", "ncu_traffic.json")) as f:
+        d = json.load(f)
+    for op in ("ag_gemm", "gemm_rs", "moe_layer0", "moe_layer1"):
+        e = d[op]
+        assert e["dram_bytes_per_launch"] == e["dram_bytes_read"] + e["dram_bytes_write"]
+        assert len(e["kernel_hash"]) == 16 and e["duration_us"] > 0
